@@ -1,0 +1,323 @@
+"""fp64 oracle of the routed Mixture-of-Experts FFN step (test infrastructure).
+
+Every function states the passage of the pages it follows. The pages are:
+  * "Inferno" README (GLM-5.2 Q2 on Apple Silicon) -- sections "Current
+    Scope", "Model", "Memory Strategy";
+  * GeekNews article on TurboFieldfare (Gemma 4 26B-A4B) -- sections
+    "execution architecture" (weight format) and "token generation" (router,
+    LFU cache, shared expert, combine, prefill chunk);
+  * "Colibri" analysis report -- section 2 "Exact Architecture and Data-Flow
+    Reconstruction" (Route / Union / Place / Overlap) and section 3 (exact
+    routing);
+  * Colibri README -- "What's implemented" (batch-union MoE, dequant-on-use).
+
+What the pages leave open is filled with the plainest reading, recorded where
+it is used (nibble order, softmax renormalised over the selected experts,
+ties to the lower index, LFU details).
+
+Everything here is computed in float64 with numpy; no blocking, fusion or
+reordering beyond the definitions. Parity status: every function below is
+pinned by tests in ``tests/test_oracle_pins.py`` (hand-computed values,
+closed forms, brute force and an independent pure-Python restatement).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64 (exact)."""
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns -> float64 (exact): the upper half of a binary32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def dequant_q4g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """Affine group-64 4-bit dequantisation, W[n][k] = code(n,k) * s[n][k//64] + b[n][k//64].
+
+    Follows TurboFieldfare "execution architecture" (MLX affine 4-bit, group
+    64; the shared and routed experts are 4-bit) and Colibri README
+    "dequant-on-use". Storage reading (the pages are silent): codes are
+    row-major [N][K/2] bytes, element k in byte k//2, low nibble for even k;
+    scale and bias are binary16 [N][K/64]. The fp64 result is exact.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, half_k = codes.shape
+    K = 2 * half_k
+    q = np.empty((N, K), dtype=np.float64)
+    q[:, 0::2] = codes & 0x0F
+    q[:, 1::2] = codes >> 4
+    s = np.repeat(f16_bits_to_f64(scale).reshape(N, K // 64), 64, axis=1)
+    b = np.repeat(f16_bits_to_f64(bias).reshape(N, K // 64), 64, axis=1)
+    return q * s + b
+
+
+def dequant_q8g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """Affine group-64 8-bit dequantisation, W[n][k] = code(n,k) * s[n][k//64] + b[n][k//64].
+
+    TurboFieldfare "execution architecture": the router is stored at 8 bits in
+    the same affine group-64 scheme. codes are row-major [N][K] bytes.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, K = codes.shape
+    s = np.repeat(f16_bits_to_f64(scale).reshape(N, K // 64), 64, axis=1)
+    b = np.repeat(f16_bits_to_f64(bias).reshape(N, K // 64), 64, axis=1)
+    return codes.astype(np.float64) * s + b
+
+
+def router_weights_f64(router) -> np.ndarray:
+    """Router matrix [E][H] in float64: fp32 values, or the dequantised 8-bit codes."""
+    if router.fmt == "f32":
+        return np.asarray(router.w, dtype=np.float32).astype(np.float64)
+    q = router.q
+    return dequant_q8g64(q.codes, q.scale, q.bias)
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+
+def router_logits(Wr: np.ndarray, x: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
+    """l_e = sum_k Wr[e][k] x[k] (+ bias_e).
+
+    TurboFieldfare "token generation": the router runs on the GPU with weights
+    that always stay in memory; Colibri report section 2 "Route": the resident
+    routing matrix scores the token's hidden state. The optional per-expert
+    bias (skewed popularity workload) is added to the logits before selection
+    and before the softmax.
+    """
+    l = Wr @ np.asarray(x, dtype=np.float64)
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float32).astype(np.float64)
+    return l
+
+
+@dataclass
+class RouteInfo:
+    ids: np.ndarray        # int64 [k], selection order
+    weights: np.ndarray    # float64 [k]
+    gap: float             # l_(k) - l_(k+1) (inf when k == E)
+    scale: float           # sum_i |Wr[e][i] x[i]| max over e (fp32 rounding scale)
+
+
+def select_topk(l: np.ndarray, k: int) -> tuple[np.ndarray, float]:
+    """Exact top-k: the first k of the experts stably sorted by (-l_e, e).
+
+    Inferno "Current Scope" and Colibri report section 3: exact top-8 routing,
+    no approximation. Ties go to the lower expert index (stable sort on the
+    negated logits). Also returns the gap between the k-th and (k+1)-th
+    largest logits.
+    """
+    order = np.argsort(-np.asarray(l, dtype=np.float64), kind="stable")
+    ids = order[:k]
+    gap = float(l[order[k - 1]] - l[order[k]]) if k < len(l) else float("inf")
+    return ids.astype(np.int64), gap
+
+
+def routing_weights(l_sel: np.ndarray) -> np.ndarray:
+    """Softmax over the selected logits: w_j = exp(l_j - max) / sum_j' exp(l_j' - max).
+
+    A full softmax over all experts renormalised over the selected ones is the
+    same quantity; the pages name softmax top-8 with renormalised weights only
+    through the benchmark spec, so this is the plainest reading.
+    """
+    l_sel = np.asarray(l_sel, dtype=np.float64)
+    e = np.exp(l_sel - l_sel.max())
+    return e / e.sum()
+
+
+# ---------------------------------------------------------------------------
+# expert FFN and the layer
+# ---------------------------------------------------------------------------
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z / (1 + exp(-z)), written to avoid overflow for very negative z."""
+    z = np.asarray(z, dtype=np.float64)
+    out = np.empty_like(z)
+    pos = z >= 0
+    out[pos] = z[pos] / (1.0 + np.exp(-z[pos]))
+    ez = np.exp(z[~pos])
+    out[~pos] = z[~pos] * ez / (1.0 + ez)
+    return out
+
+
+def _deq(m) -> np.ndarray:
+    return dequant_q4g64(m.codes, m.scale, m.bias)
+
+
+def expert_ffn(expert, x: np.ndarray) -> np.ndarray:
+    """f(x) = W_down (silu(W_gate x) * (W_up x)), each matrix dequantised on use.
+
+    Inferno "Model": each routed expert is a gate, an up and a down matrix;
+    the gated (SwiGLU) form is the plainest reading of gate/up/down.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    g = _deq(expert.gate) @ x
+    u = _deq(expert.up) @ x
+    h = silu(g) * u
+    return _deq(expert.down) @ h
+
+
+def _x_f64(layer, x) -> np.ndarray:
+    if layer.spec.act == "bf16":
+        return bf16_bits_to_f64(x)
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def route_token(layer, x64: np.ndarray, Wr: np.ndarray | None = None) -> RouteInfo:
+    if Wr is None:
+        Wr = router_weights_f64(layer.router)
+    l = router_logits(Wr, x64, layer.router_bias)
+    ids, gap = select_topk(l, layer.spec.top_k)
+    w = routing_weights(l[ids])
+    scale = float(np.max(np.abs(Wr * x64[None, :]).sum(axis=1)))
+    return RouteInfo(ids, w, gap, scale)
+
+
+def moe_token(layer, x, ids: np.ndarray | None = None, Wr: np.ndarray | None = None):
+    """One decode token: y = f_shared(x) + sum_j w_j f_{S_j}(x).
+
+    TurboFieldfare "token generation": the router picks the top-8 experts; the
+    always-resident shared expert runs on every token; after the routed
+    experts run, the shared and routed outputs are combined. Colibri report
+    section 2: Route, then the experts. The shared expert is unweighted.
+
+    ``ids`` overrides the selection (used when the GPU's fp32 logits resolve a
+    near-tie the other way; the weights are then the softmax over those ids).
+    Returns (y float64 [H], RouteInfo).
+    """
+    x64 = _x_f64(layer, x)
+    if Wr is None:
+        Wr = router_weights_f64(layer.router)
+    info = route_token(layer, x64, Wr)
+    if ids is not None:
+        l = router_logits(Wr, x64, layer.router_bias)
+        ids = np.asarray(ids, dtype=np.int64)
+        info = RouteInfo(ids, routing_weights(l[ids]), info.gap, info.scale)
+    y = np.zeros(layer.spec.hidden, dtype=np.float64)
+    if layer.shared is not None:
+        y += expert_ffn(layer.shared, x64)
+    for j, e in enumerate(info.ids):
+        y += info.weights[j] * expert_ffn(layer.experts[int(e)], x64)
+    return y, info
+
+
+def moe_tokens(layer, X, ids: np.ndarray | None = None):
+    """A chunk of tokens (prefill): row t is exactly the decode of token t.
+
+    TurboFieldfare "token generation" (prefill in chunks of up to 128 tokens
+    so a fetched expert serves several rows) and Colibri "Union" / batch-union
+    MoE (each distinct expert of the batch read once, applied to every row
+    routed to it): both are execution strategies; the rows are independent.
+    """
+    Wr = router_weights_f64(layer.router)
+    ys, infos = [], []
+    for t in range(len(X)):
+        y, info = moe_token(layer, X[t], None if ids is None else ids[t], Wr)
+        ys.append(y)
+        infos.append(info)
+    return np.stack(ys), infos
+
+
+def layer_dense_f64(layer, x) -> np.ndarray:
+    """Brute force: evaluate every expert densely, then mask to the selected set.
+
+    Used only to pin ``moe_token``: the same output obtained without the
+    sparse dispatch, weights taken from the full softmax renormalised over S.
+    """
+    x64 = _x_f64(layer, x)
+    Wr = router_weights_f64(layer.router)
+    l = router_logits(Wr, x64, layer.router_bias)
+    E, k = layer.spec.n_experts, layer.spec.top_k
+    p = np.exp(l - l.max())
+    p /= p.sum()
+    S = set(int(i) for i in np.argsort(-l, kind="stable")[:k])
+    mask = np.array([1.0 if e in S else 0.0 for e in range(E)])
+    pm = p * mask
+    pm /= pm.sum()
+    outs = np.stack([expert_ffn(layer.experts[e], x64) for e in range(E)])
+    y = pm @ outs
+    if layer.shared is not None:
+        y = y + expert_ffn(layer.shared, x64)
+    return y
+
+
+# ---------------------------------------------------------------------------
+# per-layer LFU expert cache (residency trace)
+# ---------------------------------------------------------------------------
+
+class LFUCache:
+    """Per-layer expert cache with a fixed number of slots, least-frequently-used eviction.
+
+    TurboFieldfare "token generation": the CPU matches the router's 8 expert
+    IDs against a 16-slot LFU cache per layer and fills the misses. Readings
+    (the pages are silent on the details):
+      * an expert's count starts at 1 when it is admitted and grows by 1 on
+        every use while it stays resident; the count is dropped on eviction;
+      * the victim is the resident expert with the smallest count that the
+        current token does not need; ties go to the least recently used, then
+        to the lower expert index;
+      * the IDs of one token are processed in selection order; hits are
+        counted before any miss of the same token is admitted.
+    """
+
+    def __init__(self, slots: int):
+        self.slots = slots
+        self.count: dict[int, int] = {}
+        self.last: dict[int, int] = {}
+        self.slot_of: dict[int, int] = {}
+        self.clock = 0
+
+    def access(self, ids) -> tuple[list[int], list[tuple[int, int, int]]]:
+        """Process one token's expert IDs.
+
+        Returns (hits, fills) where fills lists (expert, slot, evicted expert
+        or -1) in the order the misses are admitted.
+        """
+        ids = [int(e) for e in ids]
+        assert len(set(ids)) == len(ids) <= self.slots
+        self.clock += 1
+        need = set(ids)
+        hits, fills = [], []
+        for e in ids:
+            if e in self.count:
+                hits.append(e)
+                self.count[e] += 1
+                self.last[e] = self.clock
+        for e in ids:
+            if e in self.count:
+                continue
+            if len(self.count) < self.slots:
+                used = set(self.slot_of.values())
+                slot = min(s for s in range(self.slots) if s not in used)
+                victim = -1
+            else:
+                cands = [r for r in self.count if r not in need]
+                victim = min(cands, key=lambda r: (self.count[r], self.last[r], r))
+                slot = self.slot_of.pop(victim)
+                del self.count[victim]
+                del self.last[victim]
+            self.count[e] = 1
+            self.last[e] = self.clock
+            self.slot_of[e] = slot
+            fills.append((e, slot, victim))
+        return hits, fills
+
+
+def lfu_trace(id_rows, slots: int):
+    """Hit/miss trace of a sequence of tokens through one LFU cache."""
+    c = LFUCache(slots)
+    out = []
+    for ids in id_rows:
+        out.append(c.access(ids))
+    return out

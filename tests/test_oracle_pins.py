@@ -1,0 +1,136 @@
+"""The fp64 oracle against facts fixed outside itself (CPU only).
+
+Every pin runs on the oracle as it stands; then a list of plausible mistakes
+is planted in the oracle (monkeypatched, on the CPU) and each must make at
+least one pin fail.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.moe as om
+import _pins
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+@pytest.mark.parametrize("pin", _pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+# --- planted mistakes --------------------------------------------------------
+
+_real = {name: getattr(om, name) for name in
+         ("dequant_q4g64", "dequant_q8g64", "routing_weights", "select_topk",
+          "silu", "expert_ffn", "router_logits", "moe_token")}
+
+
+def _deq_swapped_nibbles(codes, scale, bias):
+    codes = np.asarray(codes, np.uint8)
+    swapped = ((codes & 0x0F) << 4) | (codes >> 4)
+    return _real["dequant_q4g64"](swapped.astype(np.uint8), scale, bias)
+
+
+def _deq_bias_sign(codes, scale, bias):
+    return _real["dequant_q4g64"](codes, scale, np.asarray(bias, np.uint16) ^ np.uint16(0x8000))
+
+
+def _deq_group_32(codes, scale, bias):
+    codes = np.asarray(codes, np.uint8)
+    N, hk = codes.shape
+    K = 2 * hk
+    q = np.empty((N, K))
+    q[:, 0::2] = codes & 15
+    q[:, 1::2] = codes >> 4
+    s = om.f16_bits_to_f64(scale).reshape(N, -1)
+    b = om.f16_bits_to_f64(bias).reshape(N, -1)
+    idx = np.minimum(np.arange(K) // 32, s.shape[1] - 1)
+    return q * s[:, idx] + b[:, idx]
+
+
+def _q8_no_bias(codes, scale, bias):
+    return _real["dequant_q8g64"](codes, scale, np.zeros_like(np.asarray(bias)))
+
+
+def _weights_unnormalised(l_sel):
+    l_sel = np.asarray(l_sel, np.float64)
+    return np.exp(l_sel - l_sel.max())
+
+
+def _topk_ties_high(l, k):
+    l = np.asarray(l, np.float64)
+    order = np.lexsort((-np.arange(len(l)), -l))
+    gap = float(l[order[k - 1]] - l[order[k]]) if k < len(l) else float("inf")
+    return order[:k].astype(np.int64), gap
+
+
+def _silu_is_sigmoid(z):
+    z = np.asarray(z, np.float64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def _ffn_gate_up_swapped(expert, x):
+    x = np.asarray(x, np.float64)
+    g = om._deq(expert.gate) @ x
+    u = om._deq(expert.up) @ x
+    return om._deq(expert.down) @ (om.silu(u) * g)
+
+
+def _ffn_no_down(expert, x):
+    x = np.asarray(x, np.float64)
+    g = om._deq(expert.gate) @ x
+    u = om._deq(expert.up) @ x
+    h = om.silu(g) * u
+    H = expert.down.N
+    return np.resize(h, H)
+
+
+def _logits_no_bias(Wr, x, bias=None):
+    return _real["router_logits"](Wr, x, None)
+
+
+def _token_weighted_shared(layer, x, ids=None, Wr=None):
+    y, info = _real["moe_token"](layer, x, ids, Wr)
+    if layer.shared is not None:
+        x64 = om._x_f64(layer, x)
+        y = y + (info.weights[0] - 1.0) * om.expert_ffn(layer.shared, x64)
+    return y, info
+
+
+def _token_no_shared(layer, x, ids=None, Wr=None):
+    y, info = _real["moe_token"](layer, x, ids, Wr)
+    if layer.shared is not None:
+        y = y - om.expert_ffn(layer.shared, om._x_f64(layer, x))
+    return y, info
+
+
+MISTAKES = {
+    "nibble order swapped": ("dequant_q4g64", _deq_swapped_nibbles),
+    "bias sign flipped": ("dequant_q4g64", _deq_bias_sign),
+    "group size 32": ("dequant_q4g64", _deq_group_32),
+    "8-bit bias dropped": ("dequant_q8g64", _q8_no_bias),
+    "weights not renormalised": ("routing_weights", _weights_unnormalised),
+    "ties to the higher index": ("select_topk", _topk_ties_high),
+    "silu replaced by sigmoid": ("silu", _silu_is_sigmoid),
+    "gate and up swapped": ("expert_ffn", _ffn_gate_up_swapped),
+    "down projection dropped": ("expert_ffn", _ffn_no_down),
+    "router bias dropped": ("router_logits", _logits_no_bias),
+    "shared expert weighted": ("moe_token", _token_weighted_shared),
+    "shared expert dropped": ("moe_token", _token_no_shared),
+}
+
+
+@pytest.mark.parametrize("name", list(MISTAKES))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fake = MISTAKES[name]
+    monkeypatch.setattr(om, attr, fake)
+    if hasattr(oracle, attr):
+        monkeypatch.setattr(oracle, attr, fake)
+    failed = []
+    for pin in _pins.ALL_PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake: {name}"
