@@ -1,0 +1,324 @@
+"""Benchmark of the routed-MoE layer decode step on GB300.
+
+Default workload: the GLM-scale layer (hidden 6144, expert intermediate 2048,
+256 routed experts, top-8, one shared expert, affine group-64 4-bit experts,
+fp32 router, bf16 activations). One step = 1000 seeded tokens decoded one
+after another, each a separate moe_decode call. Weights are synthetic
+(seeded), inputs are seeded N(0,1) rounded to bf16.
+
+L2 is defeated by rotating 4 device replicas of the layer (token t uses
+replica t mod 4): between two uses of the same bytes ~600 MB of other weights
+stream through the 129 MB L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. Under torchrun with N > 1 every rank runs its own
+replica of the workload on its own GPU (the decode path has no exchange
+step); rank 0 prints tokens/s summed over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the CPU baseline is the oracle on one core: keep BLAS single-threaded
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s vs 8 TB/s roofline"
+UNIT = "tokens/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(spec: si.LayerSpec):
+    """Bytes one decode token must read: router + (top_k + n_shared) experts (canonical format)."""
+    router = spec.n_experts * spec.hidden * 4 if spec.router_fmt == "f32" else \
+        spec.n_experts * spec.hidden + spec.n_experts * spec.hidden // 64 * 4
+    ns = spec.top_k + spec.n_shared
+    gu = ns * 2 * spec.inter * (spec.hidden // 2 + spec.hidden // 16)
+    down = ns * spec.hidden * (spec.inter // 2 + spec.inter // 16)
+    return router + gu + down, gu, down, router
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_sample(layer, X, n_tokens):
+    """Time the fp64 oracle on n_tokens tokens; returns tokens/s."""
+    import oracle
+    Wr = oracle.router_weights_f64(layer.router)
+    t0 = time.perf_counter()
+    for t in range(n_tokens):
+        oracle.moe_token(layer, X[t], Wr=Wr)
+    return n_tokens / (time.perf_counter() - t0)
+
+
+def run_reference(args, spec, workload):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    layer = si.gen_layer(0, 0, spec)
+    X = si.gen_tokens(0, 0, 4, spec)
+    per_step = 2
+    for _ in range(args.warmup):
+        oracle_sample(layer, X, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(layer, X, per_step)
+    dt = time.perf_counter() - t0
+    v = args.steps * per_step / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "tokens_per_step": per_step},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} tokens per step of the same layer, fp64 numpy, 1 BLAS thread"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="glm_decode", choices=["glm_decode", "gemma_decode", "tiny"])
+    ap.add_argument("--tokens", type=int, default=1000)
+    ap.add_argument("--replicas", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    spec = si.CONFIGS[args.workload]
+    desc = {"glm_decode": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q4g64 experts, fp32 router",
+            "gemma_decode": "Gemma-style decode: H2816 I704 E128 top-8 + 1 shared, q4g64 experts, q8g64 router",
+            "tiny": "tiny layer: H512 I256 E32 top-8 + 1 shared, fp32 I/O"}[args.workload]
+    workload = f"{desc}; {args.tokens} sequential single-token decodes per step"
+    if args.impl == "reference":
+        run_reference(args, spec, workload)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import quantized_routed_expert_moe_gb300 as moe
+    from quantized_routed_expert_moe_gb300 import build as _b
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        _b.build()
+    if ws > 1:
+        dist.barrier()
+
+    R = args.replicas or {"glm_decode": 4, "gemma_decode": 16, "tiny": 64}[args.workload]
+    layer = si.gen_layer(0, 0, spec)
+    reps = [moe.MoELayer(layer, device=local) for _ in range(R)]
+    T = args.tokens
+    X = si.gen_tokens(1000 * rank, 0, T, spec)   # distinct tokens per rank
+    xdt = torch.bfloat16 if spec.act == "bf16" else torch.float32
+    x_np_view = X.view(np.int16) if spec.act == "bf16" else X
+    x_host = torch.from_numpy(np.ascontiguousarray(x_np_view)).view(xdt).pin_memory()
+    x_dev = x_host.to("cuda", non_blocking=False)
+    y_dev = torch.empty((T, spec.hidden), dtype=xdt, device="cuda")
+    y_host = torch.empty((T, spec.hidden), dtype=xdt).pin_memory()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    handles = [r.handle for r in reps]
+    dec = moe.lib().moe_decode
+    row = spec.hidden * x_dev.element_size()
+    xb, yb = x_dev.data_ptr(), y_dev.data_ptr()
+
+    def step():
+        for t in range(T):
+            st = dec(handles[t % R], xb + t * row, yb + t * row, None, sp)
+            if st:
+                raise moe.MoEError(st, "moe_decode", moe.moe_last_error())
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-kernel events recorded by the library on the same stream
+    for h in handles:
+        moe.moe_profile_start(h, (3 * T // R + 16) * args.steps)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    prof = {}
+    for h in handles:
+        for name, (n, t) in moe.moe_profile_stop(h).items():
+            a, b = prof.get(name, (0, 0.0))
+            prof[name] = (a + n, b + t)
+
+    # end to end: pinned host inputs -> device, decode, device -> pinned host outputs
+    for _ in range(args.warmup):
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y_dev, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+
+    mx = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    ms, e2e_s = float(mx[0]), float(mx[1])
+    total_tokens = T * args.steps * ws
+    value = total_tokens / (ms / 1e3)
+    e2e = total_tokens / e2e_s
+
+    hbm, _, peak_kind = peaks()
+    tot_b, gu_b, down_b, router_b = algorithmic_bytes(spec)
+    n_gu, t_gu = prof.get("gateup_decode", (0, 0.0))
+    gu_avg_ms = t_gu / max(n_gu, 1)
+    gu_gbs = gu_b / (gu_avg_ms / 1e3) / 1e9 if n_gu else None
+    launches = sum(n for n, _ in prof.values())
+    kernels = {k: {"launches": n, "avg_us": t / max(n, 1) * 1e3, "share": t / max(sum(v[1] for v in prof.values()), 1e-9)}
+               for k, (n, t) in prof.items()}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        n_cpu = {"glm_decode": 6, "gemma_decode": 60, "tiny": 400}[args.workload]
+        v = oracle_sample(layer, X, n_cpu)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_cpu} tokens of the same layer through the fp64 numpy oracle, 1 BLAS thread"}
+
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", f"{args.workload}_gateup_traffic.json")
+    if os.path.exists(tf):
+        traffic = json.load(open(tf)).get("bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload, "tokens_per_step": T, "layer_replicas": R,
+                   "l2": f"inputs larger than L2: {R} rotating layer replicas "
+                         f"({R * (len(layer.experts) + 1) * spec.expert_bytes() / 1e9:.1f} GB of weights)",
+                   "weights": "affine group-64 4-bit experts, dequantised on the fly; fp32 accumulate",
+                   "parallelism": f"replicas x{ws}"},
+        "effective_hbm_gbs": tot_b * value / ws / 1e9,
+        "hbm_roofline_frac_nominal_8tbs": tot_b * value / ws / 8e12,
+        "roofline": {"bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": (gu_gbs / hbm) if gu_gbs else None, "traffic": traffic,
+                     "kernel": "gateup_decode", "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "algorithmic_bytes_per_launch": gu_b},
+        "kernels": kernels,
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    for r in reps:
+        r.close()
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

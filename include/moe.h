@@ -1,0 +1,243 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed Mixture-of-Experts FFN step.
+ *
+ * One layer object holds a routed-MoE FFN: a router, n_experts routed experts
+ * and an optional always-resident shared expert, every expert a gated (SwiGLU)
+ * FFN over affine group-64 4-bit weights. The calls below compute, per token x:
+ *
+ *   l      = W_r x (+ bias)                      router logits
+ *   S      = first top_k experts by (-l_e, e)     exact top-k, ties to lower index
+ *   w_j    = softmax over the selected logits     renormalised routing weights
+ *   f_e(x) = W_down,e (silu(W_gate,e x) * W_up,e x)
+ *   y      = f_shared(x) + sum_j w_j f_{S_j}(x)
+ *
+ * Passages that define these operations:
+ *   - router, LFU cache, shared expert and combine: TurboFieldfare article
+ *     (GeekNews), section "token generation";
+ *   - weight format (affine 4-bit group 64; 8-bit router): same article,
+ *     section "execution architecture";
+ *   - exact top-8: Inferno README, "Current Scope"; Colibri report, section 3;
+ *   - gate/up/down experts stored side by side: Inferno README, "Model";
+ *   - prefill chunk (up to 128 tokens) and batch-union MoE: TurboFieldfare
+ *     "token generation"; Colibri report, section 2 ("Union"); Colibri README,
+ *     "What's implemented".
+ *
+ * Conventions for every call:
+ *   - Every call returns a moe_status and never aborts or exits. On failure
+ *     moe_last_error() returns a thread-local detail string.
+ *   - "device" pointers are CUDA global-memory pointers on the layer's device;
+ *     "host" pointers are ordinary (pageable or pinned) host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Work is enqueued on it; calls return without waiting unless
+ *     stated otherwise.
+ *   - A layer serves one call at a time; calls on one layer must not overlap
+ *     from several host threads, and work enqueued on different streams for
+ *     the same layer must not overlap on the GPU (they share scratch).
+ *   - Nothing falls back to the CPU: without a usable CUDA device every
+ *     compute call fails with MOE_E_CUDA.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1u
+#define MOE_MAX_TOP_K 8
+#define MOE_MAX_CHUNK 128
+#define MOE_GROUP 64
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_E_INVALID = 1,     /* bad argument or descriptor */
+    MOE_E_UNSUPPORTED = 2, /* valid but not built (format, shape) */
+    MOE_E_NOMEM = 3,       /* device or pinned host memory exhausted (checked up front) */
+    MOE_E_CUDA = 4,        /* a CUDA runtime error; detail in moe_last_error() */
+    MOE_E_TIMEOUT = 5,     /* a host wait passed its deadline */
+    MOE_E_STATE = 6,       /* layer state forbids the call (e.g. an expert slot is not valid) */
+    MOE_E_SOURCE = 7       /* the expert source callback failed or returned a short read */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum { MOE_W_F32 = 0, MOE_W_Q8G64 = 1, MOE_W_Q4G64 = 2 } moe_wfmt;
+
+/* Affine group-64 matrix [N][K] in canonical storage (host memory):
+ *   codes: 4-bit: uint8 [N][K/2], element k in byte k/2, low nibble for even k;
+ *          8-bit: uint8 [N][K];
+ *   scale, bias: IEEE binary16 bit patterns [N][K/64];
+ *   element (n, k) = code(n, k) * scale[n][k/64] + bias[n][k/64]. */
+typedef struct {
+    const uint8_t* codes;
+    const uint16_t* scale;
+    const uint16_t* bias;
+} moe_qmat;
+
+/* One expert: gate [I][H], up [I][H], down [H][I], all 4-bit group-64. */
+typedef struct {
+    moe_qmat gate, up, down;
+} moe_expert;
+
+/* Router weights [E][H]: `w` (fp32, row-major) when router_fmt == MOE_W_F32,
+ * `q` (8-bit group-64) when router_fmt == MOE_W_Q8G64. */
+typedef struct {
+    const float* w;
+    moe_qmat q;
+} moe_router;
+
+typedef struct {
+    uint32_t abi_version;  /* MOE_ABI_VERSION */
+    int32_t hidden;        /* H, multiple of 64 */
+    int32_t inter;         /* I, multiple of 64 */
+    int32_t n_experts;     /* E, top_k <= E <= 1024 */
+    int32_t top_k;         /* 1..MOE_MAX_TOP_K */
+    int32_t n_shared;      /* 0 or 1 */
+    int32_t router_fmt;    /* MOE_W_F32 or MOE_W_Q8G64 */
+    int32_t expert_fmt;    /* MOE_W_Q4G64 */
+    int32_t group;         /* 64 */
+    int32_t act_dtype;     /* MOE_F32 or MOE_BF16: dtype of x and y */
+    int32_t max_tokens;    /* largest T for moe_route / moe_prefill_chunk, 1..MOE_MAX_CHUNK */
+    int32_t cache_slots;   /* 0: all experts device-resident; > 0: streamed, that many slots (>= top_k) */
+} moe_layer_desc;
+
+typedef struct moe_layer moe_layer;
+
+/* Expert source for streamed layers: copy expert `expert`'s packed record
+ * (moe_expert_record_bytes bytes) into `dst`, host memory owned by the layer.
+ * Return 0 on success and nonzero on failure (short read, I/O error). */
+typedef int (*moe_expert_source)(void* user, int32_t expert, void* dst, size_t bytes);
+
+typedef struct {
+    uint64_t tokens;       /* tokens staged */
+    uint64_t hits;         /* expert lookups served from a resident slot */
+    uint64_t misses;       /* expert lookups that needed a host-to-device fill */
+    uint64_t bytes_h2d;    /* bytes copied host -> device for fills */
+    uint64_t stage_ns;     /* host time spent in moe_cache_stage */
+} moe_cache_stats_t;
+
+/* ---- layer lifetime ------------------------------------------------------ */
+
+/* Create a layer on CUDA device `device`.
+ *   router:       host, required. Copied and repacked; the caller may free it after.
+ *   router_bias:  host fp32 [E] or NULL. Added to the logits before selection
+ *                 and before the softmax.
+ *   shared:       host, required iff n_shared == 1.
+ *   experts:      host array of E experts, required when cache_slots == 0
+ *                 (copied, repacked into the kernel layout in device memory).
+ *                 Ignored when cache_slots > 0.
+ *   records:      streamed mode only (cache_slots > 0): host array of E
+ *                 pointers to packed expert records (moe_pack_expert_record),
+ *                 borrowed -- they must stay valid until the layer is
+ *                 destroyed; page-locked memory gives the fastest fills. May be
+ *                 NULL when `source` is given.
+ *   source/user:  streamed mode only: fills a layer-owned pinned staging
+ *                 buffer on demand when `records` is NULL.
+ * Capacity is checked against free device memory before anything is
+ * allocated (MOE_E_NOMEM). An invalid device fails with MOE_E_CUDA. */
+moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router,
+                            const float* router_bias, const moe_expert* shared,
+                            const moe_expert* experts, const void* const* records,
+                            moe_expert_source source, void* source_user,
+                            int32_t device, moe_layer** out);
+
+/* Release every device and host resource of the layer (NULL is ignored).
+ * Synchronises with the layer's own streams first. */
+void moe_layer_destroy(moe_layer* layer);
+
+/* Bytes of one packed expert record for this descriptor (0 if invalid). */
+size_t moe_expert_record_bytes(const moe_layer_desc* desc);
+
+/* Pack one expert from canonical storage into the library's record layout
+ * (host to host). `dst` must hold moe_expert_record_bytes(desc) bytes. */
+moe_status moe_pack_expert_record(const moe_layer_desc* desc, const moe_expert* expert, void* dst);
+
+/* Device bytes the layer holds (weights + slots + scratch). */
+size_t moe_layer_device_bytes(const moe_layer* layer);
+
+/* ---- compute --------------------------------------------------------------- */
+
+/* Router only, for T tokens (1 <= T <= max_tokens).
+ *   x:   device [T][H] of act_dtype.
+ *   ids: device int32 [T][top_k], selection order (descending logit, ties to lower index).
+ *   w:   device fp32 [T][top_k], softmax over the selected logits.
+ * Router GEMV/GEMM with fp32 accumulation; top-k and softmax in fp32. */
+moe_status moe_route(moe_layer* layer, const void* x, int32_t T, int32_t* ids, float* w, void* stream);
+
+/* One decode token.
+ *   x:     device [H] of act_dtype.
+ *   y:     device [H] of act_dtype (bf16 rounded to nearest even), may be NULL;
+ *   y_f32: device fp32 [H] or NULL (at least one of y, y_f32 non-NULL).
+ * Resident layers: no host synchronisation. Streamed layers: the host waits
+ * (with a deadline) for the router's expert IDs, stages the misses on the
+ * layer's copy stream while the shared expert runs, then runs the routed
+ * experts (MOE_E_TIMEOUT / MOE_E_SOURCE / MOE_E_STATE on failure). */
+moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, void* stream);
+
+/* A prefill chunk of T tokens (1 <= T <= max_tokens), resident layers.
+ *   x: device [T][H]; y: device [T][H] or NULL; y_f32: device fp32 [T][H] or NULL.
+ * Row t equals moe_decode of token t up to rounding: the tokens are grouped by
+ * expert (each distinct expert's weights read once per chunk), run through a
+ * grouped GEMM with the dequantised weights as bf16 tensor-core operands and
+ * fp32 accumulation, and combined per token in a fixed order. */
+moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y, float* y_f32,
+                             void* stream);
+
+/* T decode tokens from HOST buffers, one after another through moe_decode.
+ *   x_host: [T][H] act_dtype; y_host: [T][H] act_dtype.
+ * Copies the inputs to the device, runs the T decode steps and copies the
+ * outputs back, all on `stream`, then waits for the stream. */
+moe_status moe_decode_tokens_host(moe_layer* layer, const void* x_host, int32_t T, void* y_host,
+                                  void* stream);
+
+/* ---- streamed expert cache ------------------------------------------------- */
+
+/* Make the given experts resident (streamed layers). ids: host int32 [n]
+ * (n <= cache_slots, no repeats). Hits refresh the LFU counts; misses evict
+ * the least-frequently-used resident not in `ids` and are copied host ->
+ * device on the layer's copy stream; `stream` waits for those copies.
+ * n_hits / n_misses may be NULL. */
+moe_status moe_cache_stage(moe_layer* layer, const int32_t* ids, int32_t n, void* stream,
+                           int32_t* n_hits, int32_t* n_misses);
+
+/* Counters since creation. */
+moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out);
+
+/* Slot residency (streamed layers): slot_expert host int32 [cache_slots],
+ * -1 for an empty slot. */
+moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert);
+
+/* ---- per-kernel timing ---------------------------------------------------------- */
+
+/* Device time of one kernel kind, accumulated between moe_profile_start and
+ * moe_profile_stop. `name` points to a static string of the library. */
+typedef struct {
+    const char* name;
+    uint64_t launches;
+    double total_ms;
+} moe_kernel_time;
+
+/* Start recording a CUDA event pair around every kernel the layer launches
+ * (on the stream the kernel runs on), for at most `max_launches` launches;
+ * later launches are not recorded. Costs one event record per kernel edge. */
+moe_status moe_profile_start(moe_layer* layer, int32_t max_launches);
+
+/* Stop recording, wait for the recorded events, and return per-kernel-kind
+ * totals in `out` (host array of `cap` entries); *n_kinds receives the number
+ * of kinds with at least one launch. */
+moe_status moe_profile_stop(moe_layer* layer, moe_kernel_time* out, int32_t cap, int32_t* n_kinds);
+
+/* ---- errors ----------------------------------------------------------------- */
+
+const char* moe_status_str(moe_status s);
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,446 @@
+// C ABI entry points: layer lifetime, argument checks, scratch, dispatch.
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+moe_status fail(moe_status s, const std::string& msg) {
+    g_last_error = msg;
+    return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+    g_last_error = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return MOE_E_CUDA;
+}
+
+// Switches to the layer's device for the duration of a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err != cudaSuccess) return;
+        if (prev != dev) err = cudaSetDevice(dev);
+        ok = (err == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        if (ok && prev >= 0) {
+            int cur = -1;
+            if (cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+        }
+    }
+};
+
+static moe_status check_desc(const moe_layer_desc* d) {
+    if (!d) return fail(MOE_E_INVALID, "desc is NULL");
+    if (d->abi_version != MOE_ABI_VERSION) return fail(MOE_E_INVALID, "abi_version mismatch");
+    if (d->hidden <= 0 || d->hidden % 64) return fail(MOE_E_INVALID, "hidden must be a positive multiple of 64");
+    if (d->inter <= 0 || d->inter % 64) return fail(MOE_E_INVALID, "inter must be a positive multiple of 64");
+    if (d->hidden > 16384 || d->inter > 16384)
+        return fail(MOE_E_UNSUPPORTED, "hidden and inter are limited to 16384");
+    if (d->top_k < 1 || d->top_k > MOE_MAX_TOP_K) return fail(MOE_E_INVALID, "top_k must be in 1..8");
+    if (d->n_experts < d->top_k || d->n_experts > 1024)
+        return fail(MOE_E_INVALID, "n_experts must be in top_k..1024");
+    if (d->n_shared != 0 && d->n_shared != 1) return fail(MOE_E_INVALID, "n_shared must be 0 or 1");
+    if (d->router_fmt != MOE_W_F32 && d->router_fmt != MOE_W_Q8G64)
+        return fail(MOE_E_UNSUPPORTED, "router_fmt must be MOE_W_F32 or MOE_W_Q8G64");
+    if (d->expert_fmt != MOE_W_Q4G64) return fail(MOE_E_UNSUPPORTED, "expert_fmt must be MOE_W_Q4G64");
+    if (d->group != MOE_GROUP) return fail(MOE_E_UNSUPPORTED, "group must be 64");
+    if (d->act_dtype != MOE_F32 && d->act_dtype != MOE_BF16) return fail(MOE_E_INVALID, "act_dtype");
+    if (d->max_tokens < 1 || d->max_tokens > MOE_MAX_CHUNK)
+        return fail(MOE_E_INVALID, "max_tokens must be in 1..128");
+    if (d->cache_slots < 0) return fail(MOE_E_INVALID, "cache_slots must be >= 0");
+    if (d->cache_slots > 0 && d->cache_slots < d->top_k)
+        return fail(MOE_E_INVALID, "cache_slots must be >= top_k");
+    if (d->cache_slots > d->n_experts) return fail(MOE_E_INVALID, "cache_slots must be <= n_experts");
+    return MOE_OK;
+}
+
+static size_t act_size(const moe_layer_desc& d) { return d.act_dtype == MOE_BF16 ? 2 : 4; }
+
+static size_t router_bytes(const moe_layer_desc& d) {
+    const size_t E = d.n_experts, H = d.hidden;
+    if (d.router_fmt == MOE_W_F32) return E * H * 4;
+    return E * H + E * (H / 64) * 4;
+}
+
+static int pick_router_splits(int H) {
+    for (int s : {8, 4, 2})
+        if ((H / 64) % s == 0) return s;
+    return 1;
+}
+
+struct Alloc {
+    size_t total = 0;
+    size_t add(size_t b) {
+        size_t off = total;
+        total += (b + 255) / 256 * 256;
+        return off;
+    }
+};
+
+static void free_layer(Layer& L) {
+    if (L.cache) cache_destroy(L);
+    prof_destroy(L);
+    auto f = [](void* p) { if (p) cudaFree(p); };
+    f(L.router);
+    f(L.router_bias);
+    f(L.experts);
+    f(L.rec_table);
+    f(L.logits_part);  // scratch block base (see create)
+    f(L.io_x);
+    f(L.io_y);
+    f(L.pf.xp);        // prefill block base
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_E_INVALID: return "MOE_E_INVALID";
+        case MOE_E_UNSUPPORTED: return "MOE_E_UNSUPPORTED";
+        case MOE_E_NOMEM: return "MOE_E_NOMEM";
+        case MOE_E_CUDA: return "MOE_E_CUDA";
+        case MOE_E_TIMEOUT: return "MOE_E_TIMEOUT";
+        case MOE_E_STATE: return "MOE_E_STATE";
+        case MOE_E_SOURCE: return "MOE_E_SOURCE";
+    }
+    return "MOE_E_?";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+size_t moe_expert_record_bytes(const moe_layer_desc* desc) {
+    if (check_desc(desc) != MOE_OK) return 0;
+    return record_bytes(desc->hidden, desc->inter);
+}
+
+moe_status moe_pack_expert_record(const moe_layer_desc* desc, const moe_expert* expert, void* dst) {
+    moe_status st = check_desc(desc);
+    if (st != MOE_OK) return st;
+    if (!expert || !dst) return fail(MOE_E_INVALID, "expert and dst must be non-NULL");
+    const moe_qmat* m[3] = {&expert->gate, &expert->up, &expert->down};
+    for (auto q : m)
+        if (!q->codes || !q->scale || !q->bias) return fail(MOE_E_INVALID, "expert matrix pointer is NULL");
+    pack_expert(desc->hidden, desc->inter, *expert, static_cast<uint8_t*>(dst));
+    return MOE_OK;
+}
+
+size_t moe_layer_device_bytes(const moe_layer* layer) { return layer ? layer->L.device_bytes : 0; }
+
+moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router,
+                            const float* router_bias, const moe_expert* shared,
+                            const moe_expert* experts, const void* const* records,
+                            moe_expert_source source, void* source_user, int32_t device,
+                            moe_layer** out) {
+    if (!out) return fail(MOE_E_INVALID, "out is NULL");
+    *out = nullptr;
+    moe_status st = check_desc(desc);
+    if (st != MOE_OK) return st;
+    const moe_layer_desc& d = *desc;
+    if (!router) return fail(MOE_E_INVALID, "router is NULL");
+    if (d.router_fmt == MOE_W_F32 && !router->w) return fail(MOE_E_INVALID, "router->w is NULL");
+    if (d.router_fmt == MOE_W_Q8G64 && (!router->q.codes || !router->q.scale || !router->q.bias))
+        return fail(MOE_E_INVALID, "router->q has a NULL pointer");
+    if (d.n_shared && !shared) return fail(MOE_E_INVALID, "shared expert is NULL but n_shared == 1");
+    if (d.cache_slots == 0 && !experts) return fail(MOE_E_INVALID, "experts is NULL in resident mode");
+    if (d.cache_slots > 0 && !records && !source)
+        return fail(MOE_E_INVALID, "streamed mode needs records or a source");
+
+    int ndev = 0;
+    cudaError_t ce = cudaGetDeviceCount(&ndev);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaGetDeviceCount");
+    if (device < 0 || device >= ndev) return fail(MOE_E_CUDA, "invalid CUDA device index");
+    DeviceGuard g(device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+
+    moe_layer* layer = new (std::nothrow) moe_layer();
+    if (!layer) return fail(MOE_E_NOMEM, "host allocation failed");
+    Layer& L = layer->L;
+    L.d = d;
+    L.device = device;
+    L.rec_bytes = record_bytes(d.hidden, d.inter);
+    L.router_splits = pick_router_splits(d.hidden);
+    cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, device);
+
+    const int E = d.n_experts, H = d.hidden, I = d.inter, k = d.top_k, T = d.max_tokens;
+    const size_t n_rec = (d.cache_slots == 0) ? (size_t)E + d.n_shared : (size_t)d.n_shared;
+
+    // scratch block layout
+    Alloc sc;
+    size_t o_part = sc.add((size_t)L.router_splits * E * 4 * std::max(1, T));
+    size_t o_logits = sc.add((size_t)T * E * 4);
+    size_t o_ids = sc.add((size_t)T * k * 4);
+    size_t o_w = sc.add((size_t)T * k * 4);
+    size_t o_h = sc.add((size_t)(k + 1) * I * 4);
+    size_t o_cnt = sc.add(64 * 4);
+    // prefill block layout
+    const int rows = T * k + T * d.n_shared;
+    Alloc pf;
+    size_t o_xp = pf.add((size_t)rows * H * 2);
+    size_t o_hp = pf.add((size_t)rows * I * 2);
+    size_t o_yp = pf.add((size_t)rows * H * 4);
+    size_t o_counts = pf.add((size_t)(E + 2) * 4);
+    size_t o_offs = pf.add((size_t)(E + 3) * 4);
+    size_t o_ptok = pf.add((size_t)rows * 4);
+    size_t o_pos = pf.add((size_t)T * (k + 1) * 4);
+    const int max_tiles = rows / 16 + E + 2;
+    size_t o_te = pf.add((size_t)max_tiles * 4);
+    size_t o_tr = pf.add((size_t)max_tiles * 4);
+    size_t o_nt = pf.add(16);
+
+    size_t need = router_bytes(d) + (size_t)E * 4 + n_rec * L.rec_bytes + (size_t)(E + 1) * 8 +
+                  sc.total + (T > 1 ? pf.total : 0);
+    size_t free_b = 0, total_b = 0;
+    ce = cudaMemGetInfo(&free_b, &total_b);
+    if (ce != cudaSuccess) { delete layer; return cuda_fail(ce, "cudaMemGetInfo"); }
+    const size_t headroom = (size_t)256 << 20;
+    if (need + headroom > free_b) {
+        delete layer;
+        char buf[160];
+        std::snprintf(buf, sizeof buf, "layer needs %zu bytes of device memory, %zu free", need, free_b);
+        return fail(MOE_E_NOMEM, buf);
+    }
+
+#define TRY_ALLOC(ptr, bytes)                                             \
+    do {                                                                  \
+        cudaError_t _e = cudaMalloc((void**)&(ptr), (bytes));             \
+        if (_e != cudaSuccess) {                                          \
+            free_layer(L); delete layer;                                  \
+            return _e == cudaErrorMemoryAllocation ? fail(MOE_E_NOMEM, "cudaMalloc failed") \
+                                                   : cuda_fail(_e, "cudaMalloc"); \
+        }                                                                 \
+    } while (0)
+#define TRY_CUDA(expr)                                                    \
+    do {                                                                  \
+        cudaError_t _e = (expr);                                          \
+        if (_e != cudaSuccess) { free_layer(L); delete layer; return cuda_fail(_e, #expr); } \
+    } while (0)
+
+    // router
+    TRY_ALLOC(L.router, router_bytes(d));
+    if (d.router_fmt == MOE_W_F32) {
+        TRY_CUDA(cudaMemcpy(L.router, router->w, (size_t)E * H * 4, cudaMemcpyHostToDevice));
+    } else {
+        std::vector<uint8_t> tmp(router_bytes(d));
+        std::memcpy(tmp.data(), router->q.codes, (size_t)E * H);
+        uint8_t* meta = tmp.data() + (size_t)E * H;
+        const size_t G = (size_t)E * (H / 64);
+        for (size_t gi = 0; gi < G; ++gi) {
+            std::memcpy(meta + 4 * gi, router->q.scale + gi, 2);
+            std::memcpy(meta + 4 * gi + 2, router->q.bias + gi, 2);
+        }
+        TRY_CUDA(cudaMemcpy(L.router, tmp.data(), tmp.size(), cudaMemcpyHostToDevice));
+    }
+    if (router_bias) {
+        TRY_ALLOC(L.router_bias, (size_t)E * 4);
+        TRY_CUDA(cudaMemcpy(L.router_bias, router_bias, (size_t)E * 4, cudaMemcpyHostToDevice));
+    }
+
+    // experts: pack on the host into pinned staging, copy in chunks
+    TRY_ALLOC(L.experts, n_rec * L.rec_bytes);
+    {
+        const size_t rb = L.rec_bytes;
+        uint8_t* stage[2] = {nullptr, nullptr};
+        cudaEvent_t ev[2] = {nullptr, nullptr};
+        cudaStream_t cs = nullptr;
+        cudaError_t e2 = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+        for (int b = 0; b < 2 && e2 == cudaSuccess; ++b) {
+            e2 = cudaMallocHost((void**)&stage[b], rb);
+            if (e2 == cudaSuccess) e2 = cudaEventCreateWithFlags(&ev[b], cudaEventDisableTiming);
+        }
+        for (size_t r = 0; r < n_rec && e2 == cudaSuccess; ++r) {
+            const int b = (int)(r & 1);
+            if (r >= 2) e2 = cudaEventSynchronize(ev[b]);
+            if (e2 != cudaSuccess) break;
+            const moe_expert* src = (d.cache_slots == 0 && r < (size_t)E) ? &experts[r] : shared;
+            pack_expert(H, I, *src, stage[b]);
+            e2 = cudaMemcpyAsync(L.experts + r * rb, stage[b], rb, cudaMemcpyHostToDevice, cs);
+            if (e2 == cudaSuccess) e2 = cudaEventRecord(ev[b], cs);
+        }
+        if (cs) {
+            cudaError_t e3 = cudaStreamSynchronize(cs);
+            if (e2 == cudaSuccess) e2 = e3;
+            cudaStreamDestroy(cs);
+        }
+        for (int b = 0; b < 2; ++b) {
+            if (stage[b]) cudaFreeHost(stage[b]);
+            if (ev[b]) cudaEventDestroy(ev[b]);
+        }
+        if (e2 != cudaSuccess) { free_layer(L); delete layer; return cuda_fail(e2, "expert upload"); }
+    }
+
+    // record table: routed experts then the shared expert at index E
+    TRY_ALLOC(L.rec_table, (size_t)(E + 1) * sizeof(void*));
+    {
+        std::vector<const uint8_t*> tab(E + 1, nullptr);
+        if (d.cache_slots == 0)
+            for (int e = 0; e < E; ++e) tab[e] = L.experts + (size_t)e * L.rec_bytes;
+        if (d.n_shared) tab[E] = L.experts + (n_rec - 1) * L.rec_bytes;
+        TRY_CUDA(cudaMemcpy(L.rec_table, tab.data(), tab.size() * sizeof(void*), cudaMemcpyHostToDevice));
+    }
+
+    // scratch
+    {
+        uint8_t* base = nullptr;
+        TRY_ALLOC(base, sc.total);
+        TRY_CUDA(cudaMemset(base, 0, sc.total));
+        L.logits_part = reinterpret_cast<float*>(base + o_part);
+        L.logits = reinterpret_cast<float*>(base + o_logits);
+        L.ids = reinterpret_cast<int32_t*>(base + o_ids);
+        L.wts = reinterpret_cast<float*>(base + o_w);
+        L.h = reinterpret_cast<float*>(base + o_h);
+        L.counters = reinterpret_cast<unsigned*>(base + o_cnt);
+    }
+    if (T > 1) {
+        uint8_t* base = nullptr;
+        TRY_ALLOC(base, pf.total);
+        TRY_CUDA(cudaMemset(base, 0, pf.total));
+        L.pf.xp = base + o_xp;
+        L.pf.hp = base + o_hp;
+        L.pf.yp = reinterpret_cast<float*>(base + o_yp);
+        L.pf.counts = reinterpret_cast<int32_t*>(base + o_counts);
+        L.pf.offsets = reinterpret_cast<int32_t*>(base + o_offs);
+        L.pf.perm_token = reinterpret_cast<int32_t*>(base + o_ptok);
+        L.pf.pos = reinterpret_cast<int32_t*>(base + o_pos);
+        L.pf.tile_expert = reinterpret_cast<int32_t*>(base + o_te);
+        L.pf.tile_row0 = reinterpret_cast<int32_t*>(base + o_tr);
+        L.pf.n_tiles = reinterpret_cast<int32_t*>(base + o_nt);
+        L.pf.max_rows = rows;
+    }
+    L.device_bytes = need;
+
+    TRY_CUDA(decode_kernel_setup(L));
+    if (T > 1) TRY_CUDA(prefill_kernel_setup(L));
+
+    if (d.cache_slots > 0) {
+        st = cache_create(L, records, source, source_user);
+        if (st != MOE_OK) { std::string m = g_last_error; free_layer(L); delete layer; return fail(st, m); }
+    }
+#undef TRY_ALLOC
+#undef TRY_CUDA
+    *out = layer;
+    return MOE_OK;
+}
+
+void moe_layer_destroy(moe_layer* layer) {
+    if (!layer) return;
+    DeviceGuard g(layer->L.device);
+    cudaDeviceSynchronize();
+    free_layer(layer->L);
+    delete layer;
+}
+
+moe_status moe_route(moe_layer* layer, const void* x, int32_t T, int32_t* ids, float* w, void* stream) {
+    if (!layer || !x || !ids || !w) return fail(MOE_E_INVALID, "NULL argument");
+    Layer& L = layer->L;
+    if (T < 1 || T > L.d.max_tokens) return fail(MOE_E_INVALID, "T out of range 1..max_tokens");
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = (T == 1) ? launch_route_decode(L, x, s) : launch_route_tokens(L, x, T, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    const size_t nb = (size_t)T * L.d.top_k * 4;
+    MOE_CUDA_TRY(cudaMemcpyAsync(ids, L.ids, nb, cudaMemcpyDeviceToDevice, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(w, L.wts, nb, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, void* stream) {
+    if (!layer || !x) return fail(MOE_E_INVALID, "NULL argument");
+    if (!y && !y_f32) return fail(MOE_E_INVALID, "y and y_f32 are both NULL");
+    Layer& L = layer->L;
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (L.d.cache_slots > 0) return cache_decode(L, x, y, y_f32, s);
+    cudaError_t e = launch_route_decode(L, x, s);
+    if (e != cudaSuccess) return cuda_fail(e, "router launch");
+    e = launch_experts_decode(L, x, y, y_f32, RUN_ALL, s);
+    if (e != cudaSuccess) return cuda_fail(e, "expert launch");
+    return MOE_OK;
+}
+
+moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y, float* y_f32,
+                             void* stream) {
+    if (!layer || !x) return fail(MOE_E_INVALID, "NULL argument");
+    if (!y && !y_f32) return fail(MOE_E_INVALID, "y and y_f32 are both NULL");
+    Layer& L = layer->L;
+    if (T < 1 || T > L.d.max_tokens) return fail(MOE_E_INVALID, "T out of range 1..max_tokens");
+    if (L.d.cache_slots > 0)
+        return fail(MOE_E_UNSUPPORTED, "prefill on a streamed layer: stage experts and decode per token");
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 1) return moe_decode(layer, x, y, y_f32, stream);
+    cudaError_t e = launch_route_tokens(L, x, T, s);
+    if (e != cudaSuccess) return cuda_fail(e, "router launch");
+    e = launch_prefill(L, x, T, y, y_f32, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return MOE_OK;
+}
+
+moe_status moe_decode_tokens_host(moe_layer* layer, const void* x_host, int32_t T, void* y_host,
+                                  void* stream) {
+    if (!layer || !x_host || !y_host) return fail(MOE_E_INVALID, "NULL argument");
+    if (T < 1) return fail(MOE_E_INVALID, "T must be >= 1");
+    Layer& L = layer->L;
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t row = (size_t)L.d.hidden * act_size(L.d);
+    if (T > L.io_cap) {
+        MOE_CUDA_TRY(cudaStreamSynchronize(s));
+        if (L.io_x) cudaFree(L.io_x);
+        if (L.io_y) cudaFree(L.io_y);
+        L.io_x = L.io_y = nullptr;
+        L.io_cap = 0;
+        MOE_CUDA_TRY(cudaMalloc(&L.io_x, row * T));
+        MOE_CUDA_TRY(cudaMalloc(&L.io_y, row * T));
+        L.io_cap = T;
+    }
+    MOE_CUDA_TRY(cudaMemcpyAsync(L.io_x, x_host, row * T, cudaMemcpyHostToDevice, s));
+    for (int t = 0; t < T; ++t) {
+        const uint8_t* xt = static_cast<const uint8_t*>(L.io_x) + row * t;
+        uint8_t* yt = static_cast<uint8_t*>(L.io_y) + row * t;
+        moe_status st = moe_decode(layer, xt, yt, nullptr, stream);
+        if (st != MOE_OK) return st;
+    }
+    MOE_CUDA_TRY(cudaMemcpyAsync(y_host, L.io_y, row * T, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+moe_status moe_cache_stage(moe_layer* layer, const int32_t* ids, int32_t n, void* stream,
+                           int32_t* n_hits, int32_t* n_misses) {
+    if (!layer || !ids) return fail(MOE_E_INVALID, "NULL argument");
+    Layer& L = layer->L;
+    if (L.d.cache_slots == 0) return fail(MOE_E_STATE, "layer is not streamed (cache_slots == 0)");
+    if (n < 0 || n > L.d.cache_slots) return fail(MOE_E_INVALID, "n out of range 0..cache_slots");
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    int h = 0, m = 0;
+    moe_status st = cache_stage(L, ids, n, static_cast<cudaStream_t>(stream), &h, &m);
+    if (n_hits) *n_hits = h;
+    if (n_misses) *n_misses = m;
+    return st;
+}
+
+}  // extern "C"

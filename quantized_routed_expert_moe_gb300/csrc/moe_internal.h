@@ -1,0 +1,150 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- errors -----------------------------------------------------------------
+
+void set_error(const std::string& msg);
+moe_status fail(moe_status s, const std::string& msg);
+moe_status cuda_fail(cudaError_t e, const char* what);
+
+#define MOE_CUDA_TRY(expr)                                            \
+    do {                                                              \
+        cudaError_t _e = (expr);                                      \
+        if (_e != cudaSuccess) return ::moe::cuda_fail(_e, #expr);    \
+    } while (0)
+
+// ---- kernel layout of the weights ---------------------------------------------
+//
+// A quantised row of K inputs is stored as one "row record":
+//   [ codes: K/2 bytes, canonical nibble order (element k in byte k/2, low
+//     nibble for even k) ]
+//   [ meta: K/64 pairs (scale, bias) as two binary16 values, scale first;
+//     zero-padded to a multiple of 16 bytes ]
+// so one row is a single contiguous, 16-byte aligned run of bytes.
+//
+// An expert record is
+//   GU block: for i in 0..I-1: gate row i, then up row i   (2*I rows of K = H)
+//   D block:  for n in 0..H-1: down row n                  (H rows of K = I)
+//
+// The 8-bit router is stored as codes [E][H] followed by meta [E][H/64]
+// (scale, bias) binary16 pairs.
+
+inline size_t row_meta_bytes(int K) { return ((size_t)(K / 64) * 4 + 15) / 16 * 16; }
+inline size_t row_bytes(int K) { return (size_t)K / 2 + row_meta_bytes(K); }
+inline size_t gu_block_bytes(int H, int I) { return 2 * (size_t)I * row_bytes(H); }
+inline size_t record_bytes(int H, int I) { return gu_block_bytes(H, I) + (size_t)H * row_bytes(I); }
+
+void pack_expert(int H, int I, const moe_expert& e, uint8_t* dst);
+
+// ---- layer ------------------------------------------------------------------
+
+struct PrefillScratch {
+    // permutation of the (token, slot) pairs by expert
+    int32_t* counts = nullptr;      // [E + 1]
+    int32_t* offsets = nullptr;     // [E + 2] exclusive scan (+ shared group)
+    int32_t* perm_token = nullptr;  // [T*k + T] token of each permuted row
+    int32_t* pos = nullptr;         // [T][k] permuted row of (t, j)
+    int32_t* tile_expert = nullptr; // work list: expert of each (group, m-tile)
+    int32_t* tile_row0 = nullptr;   // first permuted row of each tile
+    int32_t* n_tiles = nullptr;     // [1]
+    void* xp = nullptr;             // [rows][H] bf16 gathered activations
+    void* hp = nullptr;             // [rows][I] bf16 SwiGLU outputs
+    float* yp = nullptr;            // [rows][H] fp32 expert outputs (unweighted)
+    int max_rows = 0;
+};
+
+struct CacheState;  // streamed mode (cache.cu)
+struct Profiler;    // per-kernel event timing (profile.cu)
+
+// Kernel kinds for per-kernel timing.
+enum KernelKind {
+    K_ROUTER_DECODE = 0,
+    K_ROUTER_TOKENS,
+    K_TOPK_TOKENS,
+    K_GATEUP_DECODE,
+    K_DOWN_DECODE,
+    K_PF_PERMUTE,
+    K_PF_GATHER,
+    K_PF_GEMM_GU,
+    K_PF_GEMM_DOWN,
+    K_PF_COMBINE,
+    K_CACHE_FILL,
+    K_NUM_KINDS
+};
+
+struct Layer {
+    moe_layer_desc d{};
+    int device = 0;
+    size_t rec_bytes = 0;
+
+    // router
+    void* router = nullptr;         // fp32 [E][H], or 8-bit codes + meta
+    float* router_bias = nullptr;   // fp32 [E] or null
+
+    // experts (resident mode): (E + n_shared) records; the shared expert is index E
+    uint8_t* experts = nullptr;
+    const uint8_t** rec_table = nullptr;  // device [E + 1] record pointer per expert
+
+    // decode scratch
+    float* logits_part = nullptr;   // [router_splits][E]
+    float* logits = nullptr;        // [max_tokens][E]
+    int32_t* ids = nullptr;         // [max_tokens][k]
+    float* wts = nullptr;           // [max_tokens][k]
+    float* h = nullptr;             // [k + 1][I]
+    unsigned* counters = nullptr;   // [8] last-block counters, kept at zero between launches
+    int router_splits = 1;
+
+    PrefillScratch pf;
+    CacheState* cache = nullptr;
+    Profiler* prof = nullptr;
+
+    // host I/O staging for moe_decode_tokens_host
+    void* io_x = nullptr;
+    void* io_y = nullptr;
+    int io_cap = 0;
+
+    size_t device_bytes = 0;
+    int num_sms = 0;
+    int occ_gu = 0, occ_down = 0;  // resident CTAs per SM of the decode expert kernels
+};
+
+// ---- launchers (decode.cu / prefill.cu) -----------------------------------------
+
+cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s);
+cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
+cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which,
+                                  cudaStream_t s);
+cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s);
+cudaError_t decode_kernel_setup(Layer& L);
+cudaError_t prefill_kernel_setup(Layer& L);
+
+// Event marks around a launch; no-ops unless profiling was started.
+void prof_begin(Layer& L, int kind, cudaStream_t s);
+void prof_end(Layer& L, cudaStream_t s);
+void prof_destroy(Layer& L);
+
+// which-mask for launch_experts_decode
+enum { RUN_SHARED_GU = 1, RUN_ROUTED_GU = 2, RUN_DOWN = 4, RUN_ALL = 7 };
+
+// ---- streamed cache (cache.cu) ---------------------------------------------------
+
+moe_status cache_create(Layer& L, const void* const* records, moe_expert_source src, void* user);
+void cache_destroy(Layer& L);
+moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int* hits, int* misses);
+moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s);
+
+}  // namespace moe
+
+struct moe_layer {
+    moe::Layer L;
+};

@@ -1,0 +1,72 @@
+"""Parity helpers: compare the CUDA library's outputs with the fp64 oracle.
+
+Tolerances:
+  * expert IDs are compared exactly, except where the oracle's fp64 logits put
+    the k-th and (k+1)-th experts (or two selected experts) within TAU * sigma
+    of each other, sigma = max_e sum_i |W_r[e][i] x_i| + |bias_e|; there the fp32
+    router may resolve the tie either way, so the GPU's selection is checked
+    for validity and the output is compared with the oracle run on the GPU's
+    selection. TAU = 2^-16 bounds the fp32 summation error of the router
+    (< 200 sequential fp32 additions per partial sum, each within 2^-24).
+  * routing weights: absolute 1e-5 (fp32 softmax of fp32 logits).
+  * layer output: max_i |y_i - yhat_i| / max_i |yhat_i| <= 2e-3 per token on
+    the fp32 output, and the bf16 output equals the fp32 output rounded to
+    nearest even.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+TAU = 2.0 ** -16
+REL_TOL = 2e-3
+W_TOL = 1e-5
+
+
+def f32_to_bf16_rne(a: np.ndarray) -> np.ndarray:
+    u = np.asarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
+
+
+def check_selection(layer, x, ids_gpu, Wr=None):
+    """Returns (ids_to_use, flagged). Raises AssertionError if the GPU selection is invalid."""
+    if Wr is None:
+        Wr = oracle.router_weights_f64(layer.router)
+    x64 = oracle.moe._x_f64(layer, x)
+    l = oracle.router_logits(Wr, x64, layer.router_bias)
+    k = layer.spec.top_k
+    ids_o, _ = oracle.select_topk(l, k)
+    sigma = float(np.max(np.abs(Wr * x64[None, :]).sum(axis=1)))
+    if layer.router_bias is not None:
+        sigma += float(np.max(np.abs(layer.router_bias)))
+    tau = TAU * sigma
+    ids_g = [int(v) for v in ids_gpu]
+    if ids_g == [int(v) for v in ids_o]:
+        return ids_o, False
+    # validity: distinct, in range, and every unselected expert's logit is not
+    # above any selected one by more than tau; the order within the selection
+    # descends up to tau
+    E = len(l)
+    assert len(set(ids_g)) == k and all(0 <= e < E for e in ids_g), ids_g
+    sel = set(ids_g)
+    lmin_sel = min(l[e] for e in ids_g)
+    lmax_unsel = max((l[e] for e in range(E) if e not in sel), default=-np.inf)
+    assert lmax_unsel <= lmin_sel + tau, (ids_g, list(ids_o), lmax_unsel - lmin_sel, tau)
+    for a, b in zip(ids_g, ids_g[1:]):
+        assert l[a] >= l[b] - tau, (ids_g, l[a] - l[b])
+    return np.array(ids_g, np.int64), True
+
+
+def compare_token(layer, x, y32, ids_gpu, w_gpu, y_out=None, Wr=None, y_bf16=None):
+    """Check one token; returns (normwise error, flagged)."""
+    ids_use, flagged = check_selection(layer, x, ids_gpu, Wr)
+    y_ref, info = oracle.moe_token(layer, x, ids=ids_use if flagged else None, Wr=Wr)
+    assert np.allclose(np.asarray(w_gpu, np.float64), info.weights, rtol=0, atol=W_TOL), (w_gpu, info.weights)
+    y32 = np.asarray(y32, np.float64)
+    err = float(np.max(np.abs(y32 - y_ref)) / max(np.max(np.abs(y_ref)), 1e-30))
+    assert err <= REL_TOL, err
+    if y_bf16 is not None:
+        assert np.array_equal(np.asarray(y_bf16, np.uint16), f32_to_bf16_rne(np.asarray(y32, np.float32)))
+    return err, flagged
