@@ -118,6 +118,16 @@ def dist_info():
     return ws, rank, local
 
 
+def kernel_source_sha() -> str:
+    """Hash of the CUDA sources: a stored ncu traffic figure is only used while it matches."""
+    import hashlib
+    d = os.path.join(ROOT, "quantized_routed_expert_moe_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def oracle_sample(layer, X, n_tokens):
     """Time the fp64 oracle on n_tokens tokens; returns tokens/s."""
     import oracle
@@ -162,6 +172,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=1000)
     ap.add_argument("--replicas", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "split", "fused"],
+                    help="decode implementation (auto: fused single kernel where supported)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -192,6 +204,9 @@ def main():
     R = args.replicas or {"glm_decode": 4, "gemma_decode": 16, "tiny": 64}[args.workload]
     layer = si.gen_layer(0, 0, spec)
     reps = [moe.MoELayer(layer, device=local) for _ in range(R)]
+    path = {"auto": moe.MOE_PATH_AUTO, "split": moe.MOE_PATH_SPLIT, "fused": moe.MOE_PATH_FUSED}[args.path]
+    for r in reps:
+        r.set_option(moe.MOE_OPT_DECODE_PATH, path)
     T = args.tokens
     X = si.gen_tokens(1000 * rank, 0, T, spec)   # distinct tokens per rank
     xdt = torch.bfloat16 if spec.act == "bf16" else torch.float32
@@ -217,9 +232,7 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # timed region: K steps, per-kernel events recorded by the library on the same stream
-    for h in handles:
-        moe.moe_profile_start(h, (3 * T // R + 16) * args.steps)
+    # timed region: K steps, CUDA events on the launching stream, clocks sampled alongside
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -235,6 +248,15 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
+
+    # the same K steps again with a CUDA event pair around every kernel the
+    # library launches (recorded by the library on the launch stream)
+    for h in handles:
+        moe.moe_profile_start(h, (3 * T // R + 16) * args.steps)
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
     prof = {}
     for h in handles:
         for name, (n, t) in moe.moe_profile_stop(h).items():
@@ -267,10 +289,14 @@ def main():
 
     hbm, _, peak_kind = peaks()
     tot_b, gu_b, down_b, router_b = algorithmic_bytes(spec)
-    n_gu, t_gu = prof.get("gateup_decode", (0, 0.0))
-    gu_avg_ms = t_gu / max(n_gu, 1)
-    gu_gbs = gu_b / (gu_avg_ms / 1e3) / 1e9 if n_gu else None
-    launches = sum(n for n, _ in prof.values())
+    if "decode_fused" in prof:
+        dom, dom_bytes = "decode_fused", tot_b       # one kernel does the whole token
+    else:
+        dom, dom_bytes = "gateup_decode", gu_b
+    n_dom, t_dom = prof.get(dom, (0, 0.0))
+    dom_avg_ms = t_dom / max(n_dom, 1)
+    dom_gbs = dom_bytes / (dom_avg_ms / 1e3) / 1e9 if n_dom else None
+    launches = sum(n for n, _ in prof.values()) // 1
     kernels = {k: {"launches": n, "avg_us": t / max(n, 1) * 1e3, "share": t / max(sum(v[1] for v in prof.values()), 1e-9)}
                for k, (n, t) in prof.items()}
 
@@ -287,9 +313,11 @@ def main():
                "sample": f"{n_cpu} tokens of the same layer through the fp64 numpy oracle, 1 BLAS thread"}
 
     traffic = None
-    tf = os.path.join(ROOT, "profiles", f"{args.workload}_gateup_traffic.json")
+    tf = os.path.join(ROOT, "profiles", f"{dom}_{args.workload}_traffic.json")
     if os.path.exists(tf):
-        traffic = json.load(open(tf)).get("bytes_per_launch")
+        tj = json.load(open(tf))
+        if tj.get("kernel_source_sha") == kernel_source_sha():
+            traffic = tj.get("bytes_per_launch")
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -302,10 +330,11 @@ def main():
                    "parallelism": f"replicas x{ws}"},
         "effective_hbm_gbs": tot_b * value / ws / 1e9,
         "hbm_roofline_frac_nominal_8tbs": tot_b * value / ws / 8e12,
-        "roofline": {"bound": "hbm", "achieved": gu_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": (gu_gbs / hbm) if gu_gbs else None, "traffic": traffic,
-                     "kernel": "gateup_decode", "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                     "algorithmic_bytes_per_launch": gu_b},
+        "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": (dom_gbs / hbm) if dom_gbs else None, "traffic": traffic,
+                     "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy), burst",
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "avg_launch_us": dom_avg_ms * 1e3},
         "kernels": kernels,
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},

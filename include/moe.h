@@ -210,6 +210,48 @@ moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out);
  * -1 for an empty slot. */
 moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert);
 
+/* ---- options and health ----------------------------------------------------------- */
+
+/* Decode implementations (MOE_OPT_DECODE_PATH):
+ *   MOE_PATH_AUTO   the fused single-kernel decode when the shape fits it, else
+ *                   the three-kernel decode;
+ *   MOE_PATH_SPLIT  three kernels: router + top-k, gate/up + SwiGLU, down + combine;
+ *   MOE_PATH_FUSED  one persistent cooperative kernel per token (setting it on
+ *                   a shape it does not support returns MOE_E_UNSUPPORTED). */
+enum { MOE_PATH_AUTO = 0, MOE_PATH_SPLIT = 1, MOE_PATH_FUSED = 2 };
+
+enum {
+    MOE_OPT_DECODE_PATH = 1,
+    /* Test hook for failure detection: while nonzero, the fused decode never
+     * publishes the expert IDs, so every device-side wait on them runs out
+     * (about half a second), records MOE_E_TIMEOUT for moe_layer_check and
+     * drains out cleanly. */
+    MOE_OPT_TEST_STALL_ROUTING = 2,
+    /* Phase tracing of the fused decode: while nonzero, every CTA records the
+     * GPU global timer (ns) at MOE_TRACE_POINTS phase boundaries of the last
+     * launch; read them with moe_trace_read. Costs a few stores per CTA. */
+    MOE_OPT_TRACE = 3
+};
+
+/* Trace points recorded per CTA (in this order): kernel start, activations
+ * staged, router chunks done, IDs published (only the CTA that selected, else
+ * 0), IDs seen by the producer, gate/up rows done, all SwiGLU outputs visible,
+ * SwiGLU outputs staged, down rows and combine done, exit. */
+#define MOE_TRACE_POINTS 10
+
+/* Copy the trace of the last fused decode (after it completed): out receives
+ * n_ctas * MOE_TRACE_POINTS uint64 timestamps (ns), CTA-major; *n_ctas receives
+ * the grid size. Waits for the device. */
+moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t* n_ctas);
+
+moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value);
+
+/* Wait for the layer's device work, then report device-side failures since
+ * the last check: MOE_E_TIMEOUT if a bounded wait inside a kernel gave up
+ * (bits, if non-NULL, receives the raw error bits), MOE_OK otherwise. The
+ * error state is cleared. */
+moe_status moe_layer_check(moe_layer* layer, uint32_t* bits);
+
 /* ---- per-kernel timing ---------------------------------------------------------- */
 
 /* Device time of one kernel kind, accumulated between moe_profile_start and

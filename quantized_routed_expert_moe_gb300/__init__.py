@@ -28,7 +28,14 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_route", "moe_decode", "moe_prefill_chunk",
            "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency",
-           "moe_profile_start", "moe_profile_stop", "moe_status_str", "moe_last_error")
+           "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read",
+           "moe_status_str", "moe_last_error")
+
+MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
+MOE_OPT_DECODE_PATH, MOE_OPT_TEST_STALL_ROUTING, MOE_OPT_TRACE = 1, 2, 3
+MOE_TRACE_POINTS = 10
+TRACE_NAMES = ("start", "x_staged", "router_done", "ids_published", "ids_seen", "gateup_done",
+               "h_visible", "h_staged", "down_done", "exit")
 
 
 class MoEError(RuntimeError):
@@ -113,6 +120,12 @@ def lib() -> ctypes.CDLL:
             L.moe_profile_start.argtypes = [vp, i32]
             L.moe_profile_stop.restype = st
             L.moe_profile_stop.argtypes = [vp, ctypes.POINTER(moe_kernel_time), i32, ctypes.POINTER(i32)]
+            L.moe_layer_set_option.restype = st
+            L.moe_layer_set_option.argtypes = [vp, i32, ctypes.c_int64]
+            L.moe_layer_check.restype = st
+            L.moe_layer_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+            L.moe_trace_read.restype = st
+            L.moe_trace_read.argtypes = [vp, vp, i32, ctypes.POINTER(i32)]
             L.moe_status_str.restype = ctypes.c_char_p
             L.moe_status_str.argtypes = [st]
             L.moe_last_error.restype = ctypes.c_char_p
@@ -274,6 +287,27 @@ def moe_profile_stop(handle) -> dict:
     return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(min(n.value, cap))}
 
 
+def moe_layer_set_option(handle, option: int, value: int) -> None:
+    _check(lib().moe_layer_set_option(handle, option, value), "moe_layer_set_option")
+
+
+def moe_layer_check(handle) -> tuple[int, int]:
+    """(status, error bits) of device-side bounded waits since the last check."""
+    bits = ctypes.c_uint32()
+    st = lib().moe_layer_check(handle, ctypes.byref(bits))
+    return st, bits.value
+
+
+def moe_trace_read(handle, max_ctas: int = 1024):
+    """Per-CTA phase timestamps (ns) of the last fused decode: list of lists."""
+    import array
+    cap = max_ctas * MOE_TRACE_POINTS
+    buf = (ctypes.c_uint64 * cap)()
+    n = ctypes.c_int32()
+    _check(lib().moe_trace_read(handle, ctypes.cast(buf, ctypes.c_void_p), cap, ctypes.byref(n)), "moe_trace_read")
+    return [list(buf[c * MOE_TRACE_POINTS:(c + 1) * MOE_TRACE_POINTS]) for c in range(n.value)]
+
+
 class MoELayer:
     """Owns one layer handle; ``layer`` is any object with ``spec``, ``router``,
     ``router_bias``, ``shared`` and ``experts`` attributes in canonical form."""
@@ -322,6 +356,12 @@ class MoELayer:
 
     def cache_stats(self):
         return moe_cache_stats(self.handle)
+
+    def set_option(self, option, value):
+        moe_layer_set_option(self.handle, option, value)
+
+    def check(self):
+        return moe_layer_check(self.handle)
 
     @property
     def device_bytes(self):

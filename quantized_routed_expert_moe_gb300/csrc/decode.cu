@@ -254,11 +254,35 @@ __device__ __forceinline__ void stage_vector_t(float4* dst, float* sums, int K, 
                                                const void* xsrc, int x_bf16) {
     // dst: nvec blocks of [8][K/32] float4; sums: nvec x [K/32]
     const int KG = K / 32;
-    for (int idx = threadIdx.x; idx < nvec * K; idx += blockDim.x) {
-        const int v = idx / K, i = idx - v * K;
-        const float val = src ? src[v][i] : load_act(xsrc, x_bf16, i);
-        const int hg = i >> 5, c = (i & 31) >> 2, comp = i & 3;
-        reinterpret_cast<float*>(dst + (size_t)v * 8 * KG + c * KG + hg)[comp] = val;
+    // 4 consecutive values per item, 4 items per thread in flight
+    const int nq = K / 4, nitems = nvec * nq;
+    for (int base = threadIdx.x; base < nitems; base += 4 * blockDim.x) {
+        float4 val[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            if (idx < nitems) {
+                const int v = idx / nq, i4 = idx - v * nq;
+                if (src) {
+                    val[u] = __ldcg(reinterpret_cast<const float4*>(src[v]) + i4);
+                } else if (x_bf16) {
+                    const uint2 w = __ldg(reinterpret_cast<const uint2*>(xsrc) + i4);
+                    val[u] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                                         __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+                } else {
+                    val[u] = __ldg(reinterpret_cast<const float4*>(xsrc) + i4);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * blockDim.x;
+            if (idx < nitems) {
+                const int v = idx / nq, i4 = idx - v * nq;
+                const int i = 4 * i4, hg = i >> 5, c = (i & 31) >> 2;
+                dst[(size_t)v * 8 * KG + c * KG + hg] = val[u];
+            }
+        }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < nvec * KG; idx += blockDim.x) {

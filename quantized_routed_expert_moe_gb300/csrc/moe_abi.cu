@@ -103,6 +103,7 @@ static void free_layer(Layer& L) {
     f(L.io_x);
     f(L.io_y);
     f(L.pf.xp);        // prefill block base
+    f(L.trace);
 }
 
 }  // namespace moe
@@ -329,6 +330,8 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
 
     TRY_CUDA(decode_kernel_setup(L));
     if (T > 1) TRY_CUDA(prefill_kernel_setup(L));
+    L.fused_ok = fused_setup(L);
+    cudaGetLastError();  // a rejected fused configuration leaves no sticky error
 
     if (d.cache_slots > 0) {
         st = cache_create(L, records, source, source_user);
@@ -371,6 +374,11 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (L.d.cache_slots > 0) return cache_decode(L, x, y, y_f32, s);
+    if (L.fused_ok && L.decode_path != MOE_PATH_SPLIT) {
+        cudaError_t ef = launch_decode_fused(L, x, y, y_f32, s);
+        if (ef != cudaSuccess) return cuda_fail(ef, "fused decode launch");
+        return MOE_OK;
+    }
     cudaError_t e = launch_route_decode(L, x, s);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     e = launch_experts_decode(L, x, y, y_f32, RUN_ALL, s);
@@ -425,6 +433,64 @@ moe_status moe_decode_tokens_host(moe_layer* layer, const void* x_host, int32_t 
     }
     MOE_CUDA_TRY(cudaMemcpyAsync(y_host, L.io_y, row * T, cudaMemcpyDeviceToHost, s));
     MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value) {
+    if (!layer) return fail(MOE_E_INVALID, "NULL layer");
+    Layer& L = layer->L;
+    switch (option) {
+        case MOE_OPT_DECODE_PATH:
+            if (value != MOE_PATH_AUTO && value != MOE_PATH_SPLIT && value != MOE_PATH_FUSED)
+                return fail(MOE_E_INVALID, "unknown decode path");
+            if (value == MOE_PATH_FUSED && !L.fused_ok)
+                return fail(MOE_E_UNSUPPORTED, "the fused decode does not support this layer's shape or mode");
+            L.decode_path = (int)value;
+            return MOE_OK;
+        case MOE_OPT_TEST_STALL_ROUTING:
+            L.test_no_publish = value ? 1 : 0;
+            return MOE_OK;
+        case MOE_OPT_TRACE:
+            if (value && !L.trace) {
+                DeviceGuard g(L.device);
+                const size_t nb = (size_t)L.num_sms * MOE_TRACE_POINTS * 8;
+                MOE_CUDA_TRY(cudaMalloc(&L.trace, nb));
+                MOE_CUDA_TRY(cudaMemset(L.trace, 0, nb));
+            }
+            L.trace_on = value != 0;
+            return MOE_OK;
+    }
+    return fail(MOE_E_INVALID, "unknown option");
+}
+
+moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t* n_ctas) {
+    if (!layer || !out) return fail(MOE_E_INVALID, "NULL argument");
+    Layer& L = layer->L;
+    if (!L.trace) return fail(MOE_E_STATE, "tracing was never enabled (MOE_OPT_TRACE)");
+    const int n = L.num_sms * MOE_TRACE_POINTS;
+    if (cap < n) return fail(MOE_E_INVALID, "cap smaller than n_ctas * MOE_TRACE_POINTS");
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    MOE_CUDA_TRY(cudaMemcpy(out, L.trace, (size_t)n * 8, cudaMemcpyDeviceToHost));
+    if (n_ctas) *n_ctas = L.num_sms;
+    return MOE_OK;
+}
+
+moe_status moe_layer_check(moe_layer* layer, uint32_t* bits) {
+    if (!layer) return fail(MOE_E_INVALID, "NULL layer");
+    Layer& L = layer->L;
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    uint32_t v = 0;
+    unsigned* w = fused_error_word(L);
+    MOE_CUDA_TRY(cudaMemcpy(&v, w, 4, cudaMemcpyDeviceToHost));
+    if (bits) *bits = v;
+    if (v) {
+        MOE_CUDA_TRY(cudaMemset(w, 0, 4));
+        return fail(MOE_E_TIMEOUT, "a bounded device-side wait gave up (error bits " + std::to_string(v) + ")");
+    }
     return MOE_OK;
 }
 

@@ -79,6 +79,7 @@ enum KernelKind {
     K_PF_GEMM_DOWN,
     K_PF_COMBINE,
     K_CACHE_FILL,
+    K_DECODE_FUSED,
     K_NUM_KINDS
 };
 
@@ -116,6 +117,15 @@ struct Layer {
     size_t device_bytes = 0;
     int num_sms = 0;
     int occ_gu = 0, occ_down = 0;  // resident CTAs per SM of the decode expert kernels
+
+    // fused single-kernel decode (decode_fused.cu)
+    bool fused_ok = false;
+    int decode_path = MOE_PATH_AUTO;
+    int test_no_publish = 0;
+    unsigned long long* trace = nullptr;  // device [num_sms][MOE_TRACE_POINTS] when tracing is on
+    bool trace_on = false;
+    size_t fused_smem = 0;
+    alignas(16) unsigned char fused_params[512];
 };
 
 // ---- launchers (decode.cu / prefill.cu) -----------------------------------------
@@ -127,6 +137,9 @@ cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32
 cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s);
 cudaError_t decode_kernel_setup(Layer& L);
 cudaError_t prefill_kernel_setup(Layer& L);
+bool fused_setup(Layer& L);
+cudaError_t launch_decode_fused(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s);
+unsigned* fused_error_word(Layer& L);
 
 // Event marks around a launch; no-ops unless profiling was started.
 void prof_begin(Layer& L, int kind, cudaStream_t s);

@@ -40,24 +40,31 @@ def decode_one(ml, spec, x_np):
     return y32.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), yb, y
 
 
-def check_layer(layer, tokens, seed=100):
+PATHS = {"split": moe.MOE_PATH_SPLIT, "fused": moe.MOE_PATH_FUSED}
+
+
+def check_layer(layer, tokens, seed=100, path="fused"):
     spec = layer.spec
     Wr = oracle.router_weights_f64(layer.router)
     errs, flags = [], 0
     with moe.MoELayer(layer) as ml:
+        ml.set_option(moe.MOE_OPT_DECODE_PATH, PATHS[path])
         for t in range(tokens):
             x = si.gen_tokens(seed, t, 1, spec)[0]
             y32, ids, w, yb, _ = decode_one(ml, spec, x)
             err, flagged = compare_token(layer, x, y32, ids, w, Wr=Wr, y_bf16=yb)
             errs.append(err)
             flags += flagged
+        st, bits = ml.check()
+        assert st == 0, bits
     return max(errs), flags
 
 
-def test_tiny_layer_decode():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_tiny_layer_decode(path):
     layer = si.gen_layer(0, 0, si.CONFIGS["tiny"])
-    err, flags = check_layer(layer, 32)
-    print(f"tiny: max normwise err {err:.3e}, near-tie tokens {flags}")
+    err, flags = check_layer(layer, 32, path=path)
+    print(f"tiny/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
 SHAPES = {
@@ -71,31 +78,55 @@ SHAPES = {
 }
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("name", list(SHAPES))
-def test_decode_shapes(name):
+def test_decode_shapes(name, path):
     layer = si.gen_layer(7, 1, SHAPES[name])
-    err, flags = check_layer(layer, 6, seed=7)
-    print(f"{name}: max normwise err {err:.3e}, near-tie tokens {flags}")
+    err, flags = check_layer(layer, 6, seed=7, path=path)
+    print(f"{name}/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
-def test_zero_input_exact():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_zero_input_exact(path):
     spec = si.LayerSpec(hidden=256, inter=128, n_experts=16)
     layer = si.gen_layer(3, 0, spec)
     with moe.MoELayer(layer) as ml:
+        ml.set_option(moe.MOE_OPT_DECODE_PATH, PATHS[path])
         y32, ids, w, yb, _ = decode_one(ml, spec, np.zeros(256, np.uint16))
     assert list(ids) == list(range(8))
     assert np.all(w == np.float32(0.125))
     assert np.all(y32 == 0)
 
 
-def test_bit_reproducible():
+@pytest.mark.parametrize("path", list(PATHS))
+def test_bit_reproducible(path):
     spec = si.CONFIGS["tiny"]
     layer = si.gen_layer(0, 0, spec)
     x = si.gen_tokens(5, 0, 1, spec)[0]
     with moe.MoELayer(layer) as ml:
+        ml.set_option(moe.MOE_OPT_DECODE_PATH, PATHS[path])
         a = decode_one(ml, spec, x)[0]
         b = decode_one(ml, spec, x)[0]
     assert np.array_equal(a, b)
+
+
+def test_fused_wait_runs_out_and_recovers():
+    """Failure detection without a GPU fault: the routing flag is never set, every
+    bounded wait on it gives up, the kernel drains out and the host reads
+    MOE_E_TIMEOUT; the next call runs normally."""
+    spec = si.LayerSpec(hidden=512, inter=256, n_experts=32)
+    layer = si.gen_layer(8, 0, spec)
+    x = si.gen_tokens(8, 0, 1, spec)[0]
+    with moe.MoELayer(layer) as ml:
+        ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_FUSED)
+        ml.set_option(moe.MOE_OPT_TEST_STALL_ROUTING, 1)
+        decode_one(ml, spec, x)
+        st, bits = ml.check()
+        assert st == 5 and bits != 0  # MOE_E_TIMEOUT
+        ml.set_option(moe.MOE_OPT_TEST_STALL_ROUTING, 0)
+        y32, ids, w, yb, _ = decode_one(ml, spec, x)
+        assert ml.check() == (0, 0)
+        compare_token(layer, x, y32, ids, w, y_bf16=yb)
 
 
 def test_host_buffer_entry_matches_device_path():
@@ -157,13 +188,19 @@ def gemma_layer():
     return si.gen_layer(0, 0, si.CONFIGS["gemma_decode"])
 
 
-def test_gemma_scale_decode(gemma_layer):
-    err, flags = check_layer(gemma_layer, 16, seed=0)
-    print(f"gemma: max normwise err {err:.3e}, near-tie tokens {flags}")
+@pytest.mark.parametrize("path", list(PATHS))
+def test_gemma_scale_decode(gemma_layer, path):
+    err, flags = check_layer(gemma_layer, 16, seed=0, path=path)
+    print(f"gemma/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
+
+
+@pytest.fixture(scope="module")
+def glm_layer():
+    return si.gen_layer(0, 0, si.CONFIGS["glm_decode"])
 
 
 @pytest.mark.slow
-def test_glm_scale_decode():
-    layer = si.gen_layer(0, 0, si.CONFIGS["glm_decode"])
-    err, flags = check_layer(layer, 4, seed=0)
-    print(f"glm: max normwise err {err:.3e}, near-tie tokens {flags}")
+@pytest.mark.parametrize("path", list(PATHS))
+def test_glm_scale_decode(glm_layer, path):
+    err, flags = check_layer(glm_layer, 4, seed=0, path=path)
+    print(f"glm/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
