@@ -244,6 +244,14 @@ enum {
  * the grid size. Waits for the device. */
 moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t* n_ctas);
 
+/* Trace of the last three-kernel decode (while MOE_OPT_TRACE is on): out
+ * receives 3 * MOE_TRACE_MAX_CTAS * 4 global-timer stamps (ns), ordered
+ * kernel (router, gate/up, down), CTA, point (start, dependency satisfied,
+ * main work done, end); 0 where a CTA or point did not run. Waits for the
+ * device. cap must be at least 3 * MOE_TRACE_MAX_CTAS * 4. */
+#define MOE_TRACE_MAX_CTAS 1024
+moe_status moe_trace_read_split(moe_layer* layer, uint64_t* out, int32_t cap);
+
 moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value);
 
 /* Wait for the layer's device work, then report device-side failures since

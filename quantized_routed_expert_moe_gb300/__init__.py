@@ -28,7 +28,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_route", "moe_decode", "moe_prefill_chunk",
            "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency",
-           "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read",
+           "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
 MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
@@ -126,6 +126,8 @@ def lib() -> ctypes.CDLL:
             L.moe_layer_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             L.moe_trace_read.restype = st
             L.moe_trace_read.argtypes = [vp, vp, i32, ctypes.POINTER(i32)]
+            L.moe_trace_read_split.restype = st
+            L.moe_trace_read_split.argtypes = [vp, vp, i32]
             L.moe_status_str.restype = ctypes.c_char_p
             L.moe_status_str.argtypes = [st]
             L.moe_last_error.restype = ctypes.c_char_p
@@ -306,6 +308,21 @@ def moe_trace_read(handle, max_ctas: int = 1024):
     n = ctypes.c_int32()
     _check(lib().moe_trace_read(handle, ctypes.cast(buf, ctypes.c_void_p), cap, ctypes.byref(n)), "moe_trace_read")
     return [list(buf[c * MOE_TRACE_POINTS:(c + 1) * MOE_TRACE_POINTS]) for c in range(n.value)]
+
+
+MOE_TRACE_MAX_CTAS = 1024
+SPLIT_TRACE_KERNELS = ("router", "gateup", "down")
+SPLIT_TRACE_POINTS = ("start", "dependency", "main_done", "end")
+
+
+def moe_trace_read_split(handle):
+    """Per-kernel, per-CTA stamps (ns) of the last three-kernel decode: [3][1024][4]."""
+    cap = 3 * MOE_TRACE_MAX_CTAS * 4
+    buf = (ctypes.c_uint64 * cap)()
+    _check(lib().moe_trace_read_split(handle, ctypes.cast(buf, ctypes.c_void_p), cap), "moe_trace_read_split")
+    v = list(buf)
+    return [[v[(kk * MOE_TRACE_MAX_CTAS + c) * 4:(kk * MOE_TRACE_MAX_CTAS + c) * 4 + 4]
+             for c in range(MOE_TRACE_MAX_CTAS)] for kk in range(3)]
 
 
 class MoELayer:

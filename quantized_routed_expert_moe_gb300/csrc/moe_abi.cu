@@ -104,6 +104,7 @@ static void free_layer(Layer& L) {
     f(L.io_y);
     f(L.pf.xp);        // prefill block base
     f(L.trace);
+    f(L.trace_split);
 }
 
 }  // namespace moe
@@ -358,7 +359,7 @@ moe_status moe_route(moe_layer* layer, const void* x, int32_t T, int32_t* ids, f
     DeviceGuard g(L.device);
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = (T == 1) ? launch_route_decode(L, x, s) : launch_route_tokens(L, x, T, s);
+    cudaError_t e = (T == 1) ? launch_route_decode(L, x, s, 1) : launch_route_tokens(L, x, T, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
     const size_t nb = (size_t)T * L.d.top_k * 4;
     MOE_CUDA_TRY(cudaMemcpyAsync(ids, L.ids, nb, cudaMemcpyDeviceToDevice, s));
@@ -379,7 +380,7 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
         if (ef != cudaSuccess) return cuda_fail(ef, "fused decode launch");
         return MOE_OK;
     }
-    cudaError_t e = launch_route_decode(L, x, s);
+    cudaError_t e = launch_route_decode(L, x, s, 0);   // partial logits; the expert kernels select
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     e = launch_experts_decode(L, x, y, y_f32, RUN_ALL, s);
     if (e != cudaSuccess) return cuda_fail(e, "expert launch");
@@ -456,6 +457,9 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
                 const size_t nb = (size_t)L.num_sms * MOE_TRACE_POINTS * 8;
                 MOE_CUDA_TRY(cudaMalloc(&L.trace, nb));
                 MOE_CUDA_TRY(cudaMemset(L.trace, 0, nb));
+                const size_t ns = (size_t)3 * MOE_TRACE_MAX_CTAS * 4 * 8;
+                MOE_CUDA_TRY(cudaMalloc(&L.trace_split, ns));
+                MOE_CUDA_TRY(cudaMemset(L.trace_split, 0, ns));
             }
             L.trace_on = value != 0;
             return MOE_OK;
@@ -474,6 +478,19 @@ moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t*
     MOE_CUDA_TRY(cudaDeviceSynchronize());
     MOE_CUDA_TRY(cudaMemcpy(out, L.trace, (size_t)n * 8, cudaMemcpyDeviceToHost));
     if (n_ctas) *n_ctas = L.num_sms;
+    return MOE_OK;
+}
+
+moe_status moe_trace_read_split(moe_layer* layer, uint64_t* out, int32_t cap) {
+    if (!layer || !out) return fail(MOE_E_INVALID, "NULL argument");
+    Layer& L = layer->L;
+    if (!L.trace_split) return fail(MOE_E_STATE, "tracing was never enabled (MOE_OPT_TRACE)");
+    const int n = 3 * MOE_TRACE_MAX_CTAS * 4;
+    if (cap < n) return fail(MOE_E_INVALID, "cap smaller than 3 * MOE_TRACE_MAX_CTAS * 4");
+    DeviceGuard g(L.device);
+    if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    MOE_CUDA_TRY(cudaMemcpy(out, L.trace_split, (size_t)n * 8, cudaMemcpyDeviceToHost));
     return MOE_OK;
 }
 

@@ -118,25 +118,52 @@ struct Layer {
     int num_sms = 0;
     int occ_gu = 0, occ_down = 0;  // resident CTAs per SM of the decode expert kernels
 
+    // three-kernel decode: programmatic dependent launch between the kernels
+    bool pdl = true;
+
     // fused single-kernel decode (decode_fused.cu)
     bool fused_ok = false;
     int decode_path = MOE_PATH_AUTO;
     int test_no_publish = 0;
     unsigned long long* trace = nullptr;  // device [num_sms][MOE_TRACE_POINTS] when tracing is on
+    unsigned long long* trace_split = nullptr;  // device [3][MOE_TRACE_MAX_CTAS][4]
     bool trace_on = false;
+    unsigned long long* split_trace(int kernel) const {
+        return (trace_on && trace_split) ? trace_split + (size_t)kernel * MOE_TRACE_MAX_CTAS * 4 : nullptr;
+    }
     size_t fused_smem = 0;
     alignas(16) unsigned char fused_params[512];
 };
 
 // ---- launchers (decode.cu / prefill.cu) -----------------------------------------
 
-cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s);
+cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select);
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which,
                                   cudaStream_t s);
 cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s);
 cudaError_t decode_kernel_setup(Layer& L);
+cudaError_t router_kernel_setup(Layer& L);
 cudaError_t prefill_kernel_setup(Layer& L);
+
+// Launch with programmatic dependent launch allowed (the kernel may start
+// before the preceding kernel in the stream completes and must call
+// griddepcontrol.wait before touching that kernel's results).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 bool fused_setup(Layer& L);
 cudaError_t launch_decode_fused(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s);
 unsigned* fused_error_word(Layer& L);

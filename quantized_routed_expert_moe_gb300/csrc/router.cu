@@ -1,0 +1,292 @@
+// Routing: router GEMV/GEMM, exact top-k selection, softmax over the selected
+// experts.
+//
+// Router and exact top-8 selection: TurboFieldfare article, "token
+// generation"; Inferno README, "Current Scope"; Colibri report, section 3.
+// 8-bit router weights: TurboFieldfare article, "execution architecture".
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// ---------------------------------------------------------------------------
+// exact top-k + softmax over the selected logits, one CTA
+// ---------------------------------------------------------------------------
+//
+// Selection is the first k of the experts ordered by (-l_e, e): each round
+// takes the largest remaining logit, the lower index on equal values. NaN
+// logits are treated as -inf so that every round selects a valid expert.
+// ---------------------------------------------------------------------------
+// router GEMV for one token: split over H, last CTA reduces and selects
+// ---------------------------------------------------------------------------
+//
+// Grid (ceil(E/8), splits); warp w of CTA (bx, by) computes the partial logit
+// of expert 8*bx + w over inputs [by*Ls, (by+1)*Ls). With programmatic
+// dependent launch, the weight slice is prefetched into L2 before waiting for
+// the preceding kernel (the activations may come from it); the partials are
+// then reduced in split order by the last CTA to finish, which selects and
+// writes ids, weights and logits. It also clears the per-slot |h| maxima the
+// gate/up kernel of this token accumulates.
+template <bool Q8>
+__global__ void __launch_bounds__(kThreads) k_router_decode(
+    const void* __restrict__ W, const void* __restrict__ x, int x_bf16, int H, int E, int splits,
+    const float* __restrict__ bias, float* __restrict__ part, float* __restrict__ logits,
+    int32_t* __restrict__ ids, float* __restrict__ wts, int k, unsigned* __restrict__ counter,
+    int select, unsigned long long* __restrict__ tr) {
+    extern __shared__ float sm[];
+    __shared__ unsigned s_last;
+    const int cta = blockIdx.y * gridDim.x + blockIdx.x;
+    ktrace(tr, cta, 0);
+    const int Ls = H / splits;
+    const int k0 = blockIdx.y * Ls;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kWarps + warp;
+    // prefetch this warp's weight slice into L2 (constant data)
+    if (e < E && lane == 0) {
+        const uint8_t* src = Q8 ? static_cast<const uint8_t*>(W) + (size_t)e * H + k0
+                                : reinterpret_cast<const uint8_t*>(static_cast<const float*>(W) + (size_t)e * H + k0);
+        const uint32_t bytes = Q8 ? (uint32_t)Ls : (uint32_t)Ls * 4;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+    }
+    pdl_wait();
+    pdl_trigger();
+    ktrace(tr, cta, 1);
+    for (int i4 = threadIdx.x; i4 < Ls / 4; i4 += blockDim.x) {
+        float4 v;
+        if (x_bf16) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + k0) + i4);
+            v = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                            __uint_as_float(w.y & 0xFFFF0000u));
+        } else {
+            v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x) + k0) + i4);
+        }
+        reinterpret_cast<float4*>(sm)[i4] = v;
+    }
+    __syncthreads();
+    if (e < E) {
+        float acc = 0.f;
+        if (!Q8) {
+            const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(W) + (size_t)e * H + k0);
+            const float4* xs = reinterpret_cast<const float4*>(sm);
+            for (int c0 = lane; c0 < Ls / 4; c0 += 32 * 8) {
+                float4 wv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {   // 8 loads in flight per lane
+                    const int c = c0 + 32 * u;
+                    wv[u] = (c < Ls / 4) ? __ldg(row + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < Ls / 4) {
+                        const float4 xv = xs[c];
+                        acc = fmaf(wv[u].x, xv.x, acc);
+                        acc = fmaf(wv[u].y, xv.y, acc);
+                        acc = fmaf(wv[u].z, xv.z, acc);
+                        acc = fmaf(wv[u].w, xv.w, acc);
+                    }
+                }
+            }
+        } else {
+            const uint8_t* codes = static_cast<const uint8_t*>(W) + (size_t)e * H + k0;
+            const uint32_t* meta = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(W) + (size_t)E * H) +
+                                   (size_t)e * (H / 64) + k0 / 64;
+            for (int c0 = lane; c0 < Ls / 16; c0 += 32 * 4) {
+                uint4 qv[4];
+                uint32_t mv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + 32 * u;
+                    qv[u] = (c < Ls / 16) ? ldg_stream(codes + 16 * c) : make_uint4(0u, 0u, 0u, 0u);
+                    mv[u] = (c < Ls / 16) ? __ldg(meta + (c >> 2)) : 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < Ls / 16) {
+                        const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+                        float aq = 0.f, ax = 0.f;
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float xv = sm[16 * c + t];
+                            aq = fmaf(__uint_as_float(0x4B000000u | ((qw[t >> 2] >> (8 * (t & 3))) & 0xFFu)) - 8388608.0f,
+                                      xv, aq);
+                            ax += xv;
+                        }
+                        const float2 sb = meta_to_f2(mv[u]);
+                        acc = fmaf(sb.x, aq, fmaf(sb.y, ax, acc));
+                    }
+                }
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) part[(size_t)blockIdx.y * E + e] = acc;
+    }
+    __syncthreads();
+    ktrace(tr, cta, 2);
+    if (!select) return;   // the decode kernels reduce the partials and select themselves
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(counter, 1u);
+        s_last = (prev == gridDim.x * gridDim.y - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_last) { ktrace(tr, cta, 3); return; }
+    __threadfence();
+    for (int e2 = threadIdx.x; e2 < E; e2 += blockDim.x) {
+        float v[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) v[s] = (s < splits) ? __ldcg(part + (size_t)s * E + e2) : 0.f;   // splits <= 8
+        float l = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) l += v[s];
+        if (bias) l += bias[e2];
+        sm[e2] = l;
+        logits[e2] = l;
+    }
+    __syncthreads();
+    block_topk_softmax(sm, E, k, ids, wts);
+    if (threadIdx.x == 0) *counter = 0u;
+    __syncthreads();
+    ktrace(tr, cta, 3);
+}
+
+// ---------------------------------------------------------------------------
+// router for T tokens: split-K tiles (16 tokens x 64 experts), then per-token top-k
+// ---------------------------------------------------------------------------
+constexpr int RT_T = 16, RT_E = 64, RT_K = 64;
+
+template <bool Q8>
+__global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restrict__ W, const void* __restrict__ x,
+                                                            int x_bf16, int T, int H, int E, int splits,
+                                                            float* __restrict__ part) {
+    __shared__ float xs[RT_T][RT_K + 1];
+    __shared__ __align__(16) float ws[RT_K][RT_E];
+    const int e0 = blockIdx.x * RT_E, t0 = blockIdx.y * RT_T;
+    const int Ls = H / splits, kb = blockIdx.z * Ls;
+    const int tid = threadIdx.x, tt = tid >> 4, te = (tid & 15) * 4;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kc = kb; kc < kb + Ls; kc += RT_K) {
+        for (int i = tid; i < RT_T * RT_K; i += kThreads) {
+            const int r = i / RT_K, c = i % RT_K;
+            xs[r][c] = (t0 + r < T) ? load_act(x, x_bf16, (size_t)(t0 + r) * H + kc + c) : 0.f;
+        }
+        for (int i = tid; i < RT_E * RT_K; i += kThreads) {
+            const int r = i / RT_K, c = i % RT_K;  // r: expert in tile, c: k in chunk
+            float w = 0.f;
+            if (e0 + r < E) {
+                if (!Q8) {
+                    w = __ldg(static_cast<const float*>(W) + (size_t)(e0 + r) * H + kc + c);
+                } else {
+                    const uint8_t* base = static_cast<const uint8_t*>(W);
+                    const uint32_t m = __ldg(reinterpret_cast<const uint32_t*>(base + (size_t)E * H) +
+                                             (size_t)(e0 + r) * (H / 64) + (kc / 64));
+                    const float2 sb = meta_to_f2(m);
+                    w = fmaf((float)base[(size_t)(e0 + r) * H + kc + c], sb.x, sb.y);
+                }
+            }
+            ws[c][r] = w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int c = 0; c < RT_K; ++c) {
+            const float a = xs[tt][c];
+            const float4 w4 = *reinterpret_cast<const float4*>(&ws[c][te]);
+            acc[0] = fmaf(a, w4.x, acc[0]);
+            acc[1] = fmaf(a, w4.y, acc[1]);
+            acc[2] = fmaf(a, w4.z, acc[2]);
+            acc[3] = fmaf(a, w4.w, acc[3]);
+        }
+        __syncthreads();
+    }
+    const int t = t0 + tt;
+    if (t < T)
+        for (int j = 0; j < 4; ++j)
+            if (e0 + te + j < E) part[((size_t)blockIdx.z * T + t) * E + e0 + te + j] = acc[j];
+}
+
+__global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restrict__ part, int splits, int T, int E,
+                                                          const float* __restrict__ bias, float* __restrict__ logits,
+                                                          int32_t* __restrict__ ids, float* __restrict__ wts, int k) {
+    extern __shared__ float sl[];
+    const int t = blockIdx.x;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float v[8];
+#pragma unroll
+        for (int s = 0; s < 8; ++s) v[s] = (s < splits) ? part[((size_t)s * T + t) * E + e] : 0.f;   // splits <= 8
+        float l = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) l += v[s];
+        if (bias) l += bias[e];
+        sl[e] = l;
+        logits[(size_t)t * E + e] = l;
+    }
+    __syncthreads();
+    block_topk_softmax(sl, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+
+static size_t router_smem(const Layer& L) {
+    return (size_t)std::max(L.d.hidden / L.router_splits, L.d.n_experts) * 4;
+}
+
+cudaError_t router_kernel_setup(Layer& L) {
+    cudaError_t e;
+    e = cudaFuncSetAttribute(k_router_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)router_smem(L));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_router_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)router_smem(L));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_topk_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, L.d.n_experts * 4);
+}
+
+cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select) {
+    const auto& d = L.d;
+    dim3 grid((d.n_experts + kWarps - 1) / kWarps, L.router_splits);
+    const int xb = d.act_dtype == MOE_BF16;
+    prof_begin(L, K_ROUTER_DECODE, s);
+    cudaError_t e;
+    if (d.router_fmt == MOE_W_F32)
+        e = launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
+                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
+                       L.ids, L.wts, d.top_k, L.counters, select, L.split_trace(0));
+    else
+        e = launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
+                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
+                       L.ids, L.wts, d.top_k, L.counters, select, L.split_trace(0));
+    prof_end(L, s);
+    return e;
+}
+
+cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) {
+    const auto& d = L.d;
+    const int xb = d.act_dtype == MOE_BF16;
+    const int splits = L.router_splits;
+    dim3 grid((d.n_experts + RT_E - 1) / RT_E, (T + RT_T - 1) / RT_T, splits);
+    if ((d.hidden / splits) % RT_K) return cudaErrorInvalidValue;
+    prof_begin(L, K_ROUTER_TOKENS, s);
+    if (d.router_fmt == MOE_W_F32)
+        k_router_tokens<false><<<grid, kThreads, 0, s>>>(L.router, x, xb, T, d.hidden, d.n_experts, splits,
+                                                         L.logits_part);
+    else
+        k_router_tokens<true><<<grid, kThreads, 0, s>>>(L.router, x, xb, T, d.hidden, d.n_experts, splits,
+                                                        L.logits_part);
+    prof_end(L, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prof_begin(L, K_TOPK_TOKENS, s);
+    k_topk_tokens<<<T, kThreads, d.n_experts * 4, s>>>(L.logits_part, splits, T, d.n_experts, L.router_bias,
+                                                       L.logits, L.ids, L.wts, d.top_k);
+    prof_end(L, s);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
