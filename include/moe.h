@@ -177,6 +177,42 @@ moe_status moe_route(moe_layer* layer, const void* x, int32_t T, int32_t* ids, f
  * experts (MOE_E_TIMEOUT / MOE_E_SOURCE / MOE_E_STATE on failure). */
 moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, void* stream);
 
+/* Largest scratch moe_decode_static_scratch can use on one device, in bytes. */
+#define MOE_STATIC_SCRATCH_BYTES (256u * 1024u)
+
+/* One decode token like moe_decode, with its scratch in a fixed region of the
+ * library's own device image instead of the layer's scratch. The pages have no
+ * counterpart to this call: it serves callers that must not allocate device
+ * memory while they serve tokens. cudaMalloc and cudaFree can synchronise the
+ * whole device and so stall work queued on every other stream; an engine that
+ * has already divided HBM between weights, caches and activations has nothing
+ * left to hand out; and a caching allocator asked for a new block at that
+ * point may have to grow or trim its pool. This call makes no allocation of
+ * any kind, by CUDA, by a library or by the binding above it.
+ *
+ * Arguments, layouts, result and errors are those of moe_decode, with these
+ * differences:
+ *   - The work runs on the split path (router partials, then gate/up and
+ *     down kernels that each select from the partials) whatever the layer's
+ *     MOE_OPT_DECODE_PATH says; streamed layers (cache_slots > 0) get
+ *     MOE_E_UNSUPPORTED.
+ *   - The scratch holds the router's partial logits [splits][E], the logits
+ *     [E], ids [k], weights [k] and the SwiGLU outputs [k + 1][I] (each
+ *     rounded up to 256 bytes). A layer that needs more than
+ *     MOE_STATIC_SCRATCH_BYTES gets MOE_E_INVALID, with the sizes in
+ *     moe_last_error(), before anything is launched.
+ *   - The first call on a device does a one-time set-up with that device
+ *     current: it looks up the region's device address, which may load the
+ *     library's kernels onto the device. Make that first call before any
+ *     stream capture begins on the device.
+ *   - Nothing in the region has to start at zero: each call writes every word
+ *     it later reads, so no clear is issued.
+ *   - There is one region per device, shared by every layer and stream: two
+ *     calls whose work overlaps on the device (other streams, other threads,
+ *     other layers) overwrite each other's scratch. Order them, for example on
+ *     one stream. */
+moe_status moe_decode_static_scratch(moe_layer* layer, const void* x, void* y, float* y_f32, void* stream);
+
 /* A prefill chunk of T tokens (1 <= T <= max_tokens), resident layers.
  *   x: device [T][H]; y: device [T][H] or NULL; y_f32: device fp32 [T][H] or NULL.
  * Row t equals moe_decode of token t up to rounding: the tokens are grouped by

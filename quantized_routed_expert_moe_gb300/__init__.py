@@ -26,12 +26,13 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
-           "moe_layer_device_bytes", "moe_route", "moe_decode", "moe_prefill_chunk",
+           "moe_layer_device_bytes", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
            "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
 MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
+MOE_STATIC_SCRATCH_BYTES = 256 * 1024
 MOE_OPT_DECODE_PATH, MOE_OPT_TEST_STALL_ROUTING, MOE_OPT_TRACE = 1, 2, 3
 MOE_TRACE_POINTS = 10
 TRACE_NAMES = ("start", "x_staged", "router_done", "ids_published", "ids_seen", "gateup_done",
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
             L.moe_route.argtypes = [vp, vp, i32, vp, vp, vp]
             L.moe_decode.restype = st
             L.moe_decode.argtypes = [vp, vp, vp, vp, vp]
+            L.moe_decode_static_scratch.restype = st
+            L.moe_decode_static_scratch.argtypes = [vp, vp, vp, vp, vp]
             L.moe_prefill_chunk.restype = st
             L.moe_prefill_chunk.argtypes = [vp, vp, i32, vp, vp, vp]
             L.moe_decode_tokens_host.restype = st
@@ -247,6 +250,13 @@ def moe_decode(handle, x, y, y_f32=None, stream=None) -> None:
     _check(lib().moe_decode(handle, _addr(x), _addr(y), _addr(y_f32), _stream(stream)), "moe_decode")
 
 
+def moe_decode_static_scratch(handle, x, y, y_f32=None, stream=None) -> None:
+    """moe_decode over the library's fixed per-device scratch region; the
+    library allocates nothing (the caller passes buffers it already owns)."""
+    _check(lib().moe_decode_static_scratch(handle, _addr(x), _addr(y), _addr(y_f32), _stream(stream)),
+           "moe_decode_static_scratch")
+
+
 def moe_prefill_chunk(handle, x, T, y, y_f32=None, stream=None) -> None:
     _check(lib().moe_prefill_chunk(handle, _addr(x), T, _addr(y), _addr(y_f32), _stream(stream)),
            "moe_prefill_chunk")
@@ -361,6 +371,9 @@ class MoELayer:
 
     def decode(self, x, y, y_f32=None, stream=None):
         moe_decode(self.handle, x, y, y_f32, stream)
+
+    def decode_static_scratch(self, x, y, y_f32=None, stream=None):
+        moe_decode_static_scratch(self.handle, x, y, y_f32, stream)
 
     def prefill_chunk(self, x, T, y, y_f32=None, stream=None):
         moe_prefill_chunk(self.handle, x, T, y, y_f32, stream)

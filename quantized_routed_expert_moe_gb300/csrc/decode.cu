@@ -380,4 +380,25 @@ cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32
     return cudaSuccess;
 }
 
+// The same two expert kernels over caller-given scratch: router partials
+// `part` [splits][E] (already written on `s`), selection out (`logits` [E],
+// `ids` [k], `wts` [k]) and SwiGLU outputs `h` [k + 1][I]. No profiling or tracing.
+cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
+                                          float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s) {
+    const auto& d = L.d;
+    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts, ns = k + d.n_shared;
+    const int xb = d.act_dtype == MOE_BF16;
+    const int need = (ns * I + kWarps - 1) / kWarps;
+    const int grid = std::max(1, std::min(need, L.num_sms * L.occ_gu));
+    cudaError_t e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, L.pdl,
+                               (const uint8_t* const*)L.rec_table, part, L.router_splits,
+                               (const float*)L.router_bias, k, E, d.n_shared, x, xb, H, I, h, row_bytes(H), ids, wts,
+                               logits, (unsigned long long*)nullptr);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, L.pdl,
+                      (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias, k, E,
+                      d.n_shared, H, I, (const float*)h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I),
+                      (unsigned long long*)nullptr);
+}
+
 }  // namespace moe

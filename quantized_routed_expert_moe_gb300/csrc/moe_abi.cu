@@ -24,25 +24,6 @@ moe_status cuda_fail(cudaError_t e, const char* what) {
     return MOE_E_CUDA;
 }
 
-// Switches to the layer's device for the duration of a call.
-struct DeviceGuard {
-    int prev = -1;
-    bool ok = false;
-    cudaError_t err = cudaSuccess;
-    explicit DeviceGuard(int dev) {
-        err = cudaGetDevice(&prev);
-        if (err != cudaSuccess) return;
-        if (prev != dev) err = cudaSetDevice(dev);
-        ok = (err == cudaSuccess);
-    }
-    ~DeviceGuard() {
-        if (ok && prev >= 0) {
-            int cur = -1;
-            if (cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
-        }
-    }
-};
-
 static moe_status check_desc(const moe_layer_desc* d) {
     if (!d) return fail(MOE_E_INVALID, "desc is NULL");
     if (d->abi_version != MOE_ABI_VERSION) return fail(MOE_E_INVALID, "abi_version mismatch");

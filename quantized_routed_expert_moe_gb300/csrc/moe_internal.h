@@ -23,6 +23,25 @@ moe_status cuda_fail(cudaError_t e, const char* what);
         if (_e != cudaSuccess) return ::moe::cuda_fail(_e, #expr);    \
     } while (0)
 
+// Makes `dev` current for the guard's lifetime; restores the previous device.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err != cudaSuccess) return;
+        if (prev != dev) err = cudaSetDevice(dev);
+        ok = (err == cudaSuccess);
+    }
+    ~DeviceGuard() {
+        if (ok && prev >= 0) {
+            int cur = -1;
+            if (cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+        }
+    }
+};
+
 // ---- kernel layout of the weights ---------------------------------------------
 //
 // A quantised row of K inputs is stored as one "row record":
@@ -139,6 +158,9 @@ struct Layer {
 
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select);
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
+cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s);
+cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
+                                          float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s);
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which,
                                   cudaStream_t s);
 cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s);

@@ -266,6 +266,23 @@ cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int sel
     return e;
 }
 
+// Partial logits of one token into caller-given scratch `part` [splits][E]
+// (no selection, no counter, no profiling or tracing).
+cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s) {
+    const auto& d = L.d;
+    dim3 grid((d.n_experts + kWarps - 1) / kWarps, L.router_splits);
+    const int xb = d.act_dtype == MOE_BF16;
+    if (d.router_fmt == MOE_W_F32)
+        return launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
+                          d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
+                          (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0,
+                          (unsigned long long*)nullptr);
+    return launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
+                      d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
+                      (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0,
+                      (unsigned long long*)nullptr);
+}
+
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) {
     const auto& d = L.d;
     const int xb = d.act_dtype == MOE_BF16;
