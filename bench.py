@@ -118,12 +118,16 @@ def dist_info():
     return ws, rank, local
 
 
-def kernel_source_sha() -> str:
-    """Hash of the CUDA sources: a stored ncu traffic figure is only used while it matches."""
+KERNEL_SOURCES = {"gateup_decode": ("decode.cu", "common.cuh"), "decode_fused": ("decode_fused.cu", "common.cuh")}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the sources that define `kernel`: a stored ncu traffic figure is
+    only used while it matches."""
     import hashlib
     d = os.path.join(ROOT, "quantized_routed_expert_moe_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -173,14 +177,21 @@ def main():
     ap.add_argument("--replicas", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "fused"],
-                    help="decode implementation (auto: fused single kernel where supported)")
+                    help="decode implementation (auto: the three-kernel split path)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the routed-expert count (a smaller layer of the same shape, for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     spec = si.CONFIGS[args.workload]
+    if args.experts:
+        import dataclasses
+        spec = dataclasses.replace(spec, n_experts=args.experts)
     desc = {"glm_decode": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q4g64 experts, fp32 router",
             "gemma_decode": "Gemma-style decode: H2816 I704 E128 top-8 + 1 shared, q4g64 experts, q8g64 router",
             "tiny": "tiny layer: H512 I256 E32 top-8 + 1 shared, fp32 I/O"}[args.workload]
+    if args.experts:
+        desc = desc.replace(f"E{si.CONFIGS[args.workload].n_experts}", f"E{args.experts}")
     workload = f"{desc}; {args.tokens} sequential single-token decodes per step"
     if args.impl == "reference":
         run_reference(args, spec, workload)
@@ -263,20 +274,20 @@ def main():
             a, b = prof.get(name, (0, 0.0))
             prof[name] = (a + n, b + t)
 
-    # end to end: pinned host inputs -> device, decode, device -> pinned host outputs
+    # end to end through the C ABI with HOST buffers: moe_decode_tokens_host
+    # copies the step's inputs from pinned host memory, decodes the T tokens and
+    # copies the outputs back, then waits for its stream (one layer instance,
+    # itself larger than L2)
+    e2e_layer = reps[0]
     for _ in range(args.warmup):
-        x_dev.copy_(x_host, non_blocking=True)
-        step()
-        y_host.copy_(y_dev, non_blocking=True)
+        e2e_layer.decode_tokens_host(x_host, T, y_host, stream=stream)
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        step()
-        y_host.copy_(y_dev, non_blocking=True)
-        torch.cuda.synchronize()
+        e2e_layer.decode_tokens_host(x_host, T, y_host, stream=stream)
+    torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
 
     mx = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
@@ -316,7 +327,7 @@ def main():
     tf = os.path.join(ROOT, "profiles", f"{dom}_{args.workload}_traffic.json")
     if os.path.exists(tf):
         tj = json.load(open(tf))
-        if tj.get("kernel_source_sha") == kernel_source_sha():
+        if tj.get("kernel_source_sha") == kernel_source_sha(dom):
             traffic = tj.get("bytes_per_launch")
 
     line = {

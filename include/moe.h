@@ -217,8 +217,13 @@ moe_status moe_decode_static_scratch(moe_layer* layer, const void* x, void* y, f
  *   x: device [T][H]; y: device [T][H] or NULL; y_f32: device fp32 [T][H] or NULL.
  * Row t equals moe_decode of token t up to rounding: the tokens are grouped by
  * expert (each distinct expert's weights read once per chunk), run through a
- * grouped GEMM with the dequantised weights as bf16 tensor-core operands and
- * fp32 accumulation, and combined per token in a fixed order. */
+ * grouped GEMM on the tensor cores with fp16 operands (weights dequantised to
+ * fp16 in shared memory, activations and SwiGLU outputs rounded to fp16) and
+ * fp32 accumulation, and combined per token in a fixed order. fp16 rather than
+ * bf16: its 11-bit significand keeps the chunk within the layer tolerance,
+ * which bf16 operands do not. Activations and SwiGLU outputs must lie within
+ * the fp16 range (|v| < 65504). Not available on streamed layers
+ * (MOE_E_UNSUPPORTED). */
 moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y, float* y_f32,
                              void* stream);
 
@@ -249,9 +254,10 @@ moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert);
 /* ---- options and health ----------------------------------------------------------- */
 
 /* Decode implementations (MOE_OPT_DECODE_PATH):
- *   MOE_PATH_AUTO   the fused single-kernel decode when the shape fits it, else
- *                   the three-kernel decode;
- *   MOE_PATH_SPLIT  three kernels: router + top-k, gate/up + SwiGLU, down + combine;
+ *   MOE_PATH_AUTO   the faster of the two on GB300: the three-kernel decode;
+ *   MOE_PATH_SPLIT  three kernels chained with programmatic dependent launch:
+ *                   router partial logits, gate/up + SwiGLU (each CTA selects
+ *                   the top k from the partials), down + combine;
  *   MOE_PATH_FUSED  one persistent cooperative kernel per token (setting it on
  *                   a shape it does not support returns MOE_E_UNSUPPORTED). */
 enum { MOE_PATH_AUTO = 0, MOE_PATH_SPLIT = 1, MOE_PATH_FUSED = 2 };

@@ -180,14 +180,12 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     size_t o_xp = pf.add((size_t)rows * H * 2);
     size_t o_hp = pf.add((size_t)rows * I * 2);
     size_t o_yp = pf.add((size_t)rows * H * 4);
-    size_t o_counts = pf.add((size_t)(E + 2) * 4);
-    size_t o_offs = pf.add((size_t)(E + 3) * 4);
+    size_t o_gexp = pf.add((size_t)(E + 1) * 4);
+    size_t o_goff = pf.add((size_t)(E + 1) * 4);
+    size_t o_gcnt = pf.add((size_t)(E + 1) * 4);
     size_t o_ptok = pf.add((size_t)rows * 4);
     size_t o_pos = pf.add((size_t)T * (k + 1) * 4);
-    const int max_tiles = rows / 16 + E + 2;
-    size_t o_te = pf.add((size_t)max_tiles * 4);
-    size_t o_tr = pf.add((size_t)max_tiles * 4);
-    size_t o_nt = pf.add(16);
+    size_t o_ng = pf.add(16);
 
     size_t need = router_bytes(d) + (size_t)E * 4 + n_rec * L.rec_bytes + (size_t)(E + 1) * 8 +
                   sc.total + (T > 1 ? pf.total : 0);
@@ -299,13 +297,13 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
         L.pf.xp = base + o_xp;
         L.pf.hp = base + o_hp;
         L.pf.yp = reinterpret_cast<float*>(base + o_yp);
-        L.pf.counts = reinterpret_cast<int32_t*>(base + o_counts);
-        L.pf.offsets = reinterpret_cast<int32_t*>(base + o_offs);
+        L.pf.group_expert = reinterpret_cast<int32_t*>(base + o_gexp);
+        L.pf.group_off = reinterpret_cast<int32_t*>(base + o_goff);
+        L.pf.group_cnt = reinterpret_cast<int32_t*>(base + o_gcnt);
         L.pf.perm_token = reinterpret_cast<int32_t*>(base + o_ptok);
         L.pf.pos = reinterpret_cast<int32_t*>(base + o_pos);
-        L.pf.tile_expert = reinterpret_cast<int32_t*>(base + o_te);
-        L.pf.tile_row0 = reinterpret_cast<int32_t*>(base + o_tr);
-        L.pf.n_tiles = reinterpret_cast<int32_t*>(base + o_nt);
+        L.pf.n_groups = reinterpret_cast<int32_t*>(base + o_ng);
+        L.pf.err = reinterpret_cast<unsigned*>(base + o_ng + 4);
         L.pf.max_rows = rows;
     }
     L.device_bytes = need;
@@ -356,7 +354,7 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (L.d.cache_slots > 0) return cache_decode(L, x, y, y_f32, s);
-    if (L.fused_ok && L.decode_path != MOE_PATH_SPLIT) {
+    if (L.fused_ok && L.decode_path == MOE_PATH_FUSED) {
         cudaError_t ef = launch_decode_fused(L, x, y, y_f32, s);
         if (ef != cudaSuccess) return cuda_fail(ef, "fused decode launch");
         return MOE_OK;
@@ -481,12 +479,15 @@ moe_status moe_layer_check(moe_layer* layer, uint32_t* bits) {
     DeviceGuard g(L.device);
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     MOE_CUDA_TRY(cudaDeviceSynchronize());
-    uint32_t v = 0;
+    uint32_t v = 0, vp = 0;
     unsigned* w = fused_error_word(L);
     MOE_CUDA_TRY(cudaMemcpy(&v, w, 4, cudaMemcpyDeviceToHost));
+    if (L.pf.err) MOE_CUDA_TRY(cudaMemcpy(&vp, L.pf.err, 4, cudaMemcpyDeviceToHost));
+    v |= vp;   // the prefill GEMM reports in bits 16 and up
     if (bits) *bits = v;
     if (v) {
         MOE_CUDA_TRY(cudaMemset(w, 0, 4));
+        if (L.pf.err) MOE_CUDA_TRY(cudaMemset(L.pf.err, 0, 4));
         return fail(MOE_E_TIMEOUT, "a bounded device-side wait gave up (error bits " + std::to_string(v) + ")");
     }
     return MOE_OK;

@@ -7,6 +7,8 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+
 #include "moe.h"
 
 namespace moe {
@@ -68,18 +70,22 @@ void pack_expert(int H, int I, const moe_expert& e, uint8_t* dst);
 // ---- layer ------------------------------------------------------------------
 
 struct PrefillScratch {
-    // permutation of the (token, slot) pairs by expert
-    int32_t* counts = nullptr;      // [E + 1]
-    int32_t* offsets = nullptr;     // [E + 2] exclusive scan (+ shared group)
-    int32_t* perm_token = nullptr;  // [T*k + T] token of each permuted row
-    int32_t* pos = nullptr;         // [T][k] permuted row of (t, j)
-    int32_t* tile_expert = nullptr; // work list: expert of each (group, m-tile)
-    int32_t* tile_row0 = nullptr;   // first permuted row of each tile
-    int32_t* n_tiles = nullptr;     // [1]
-    void* xp = nullptr;             // [rows][H] bf16 gathered activations
-    void* hp = nullptr;             // [rows][I] bf16 SwiGLU outputs
-    float* yp = nullptr;            // [rows][H] fp32 expert outputs (unweighted)
+    // permutation of the (token, slot) pairs by expert: groups of rows, one
+    // group per distinct routed expert (ascending id), then the shared group
+    int32_t* group_expert = nullptr;  // [E + 1] record index of each group
+    int32_t* group_off = nullptr;     // [E + 1] first permuted row
+    int32_t* group_cnt = nullptr;     // [E + 1] rows (tokens) in the group
+    int32_t* n_groups = nullptr;      // [1]
+    int32_t* perm_token = nullptr;    // [rows] token of each permuted row
+    int32_t* pos = nullptr;           // [T][k + 1] permuted row of (t, slot j); slot k = shared
+    unsigned* err = nullptr;          // [1] error bits of the grouped GEMM (bounded waits)
+    void* xp = nullptr;               // [rows][H] fp16 gathered activations (8-element blocks permuted)
+    void* hp = nullptr;               // [rows][I] fp16 SwiGLU outputs (same block permutation)
+    float* yp = nullptr;              // [rows][H] fp32 expert outputs (unweighted)
     int max_rows = 0;
+    // TMA descriptors: gate/up codes, gate/up meta, down codes, down meta, xp, hp
+    CUtensorMap tm[6];
+    bool ready = false;
 };
 
 struct CacheState;  // streamed mode (cache.cu)

@@ -1,12 +1,539 @@
-// Prefill chunk path (token permutation, grouped expert GEMM, combine).
+// Prefill chunk path: the T tokens' (token, slot) pairs are grouped by expert,
+// gathered as fp16, run through a grouped GEMM on the tcgen05 tensor cores
+// (gate/up with the SwiGLU in the epilogue, then down) with the 4-bit weights
+// dequantised into shared memory, and combined per token in a fixed order.
+//
+// Grouping follows the "Union" step of the Colibri analysis report (section 2):
+// each distinct expert's weights are read once per chunk however many tokens
+// selected it. The TurboFieldfare article ("token generation") chunks prefill
+// at 128 tokens.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "common.cuh"
 #include "moe_internal.h"
+#include "sm100.cuh"
 
 namespace moe {
+namespace {
 
-cudaError_t prefill_kernel_setup(Layer&) { return cudaSuccess; }
+using namespace bw;
 
-cudaError_t launch_prefill(Layer&, const void*, int, void*, float*, cudaStream_t) {
-    return cudaErrorNotSupported;
+// The dequantiser turns one 32-bit word of codes (8 elements) into four fp16
+// pairs in the order (0,4) (1,5) (2,6) (3,7): masking the nibbles at bits 0
+// and 16, then 4 and 20, and so on. The activation operands (x gathered here,
+// h written by the gate/up epilogue) are stored in the same order within every
+// block of 8 along K, so the products pair up as in the plain dot product.
+__host__ __device__ constexpr int blk_pos(int j) { return ((j & 3) << 1) | (j >> 2); }
+
+// ---------------------------------------------------------------------------
+// permutation (histogram, exclusive scan, stable scatter) -- one CTA
+// ---------------------------------------------------------------------------
+
+constexpr int kPermThreads = 1024;
+
+__global__ void __launch_bounds__(kPermThreads) k_pf_permute(const int32_t* __restrict__ ids, int T, int k, int E,
+                                                             int n_shared, int32_t* __restrict__ gexp,
+                                                             int32_t* __restrict__ goff, int32_t* __restrict__ gcnt,
+                                                             int32_t* __restrict__ n_groups,
+                                                             int32_t* __restrict__ perm_token,
+                                                             int32_t* __restrict__ pos) {
+    __shared__ int s_cnt[1024];
+    __shared__ int s_e[1024];
+    __shared__ int s_start[1024];
+    __shared__ int s_gidx[1024];
+    __shared__ int s_wa[32], s_wb[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = T * k;   // <= 1024
+    s_cnt[tid] = 0;
+    __syncthreads();
+    if (tid < P) {
+        int e = ids[tid];
+        if ((unsigned)e >= (unsigned)E) e = 0;   // a valid selection never needs this
+        s_e[tid] = e;
+        atomicAdd(&s_cnt[e], 1);
+    }
+    __syncthreads();
+    // exclusive scans over experts (thread e): row starts, and group index of
+    // each expert that has rows (groups in ascending expert id)
+    const int c = tid < E ? s_cnt[tid] : 0, nz = c > 0;
+    int a = c, b = nz;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ua = __shfl_up_sync(0xffffffffu, a, o), ub = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) { a += ua; b += ub; }
+    }
+    if (lane == 31) { s_wa[warp] = a; s_wb[warp] = b; }
+    __syncthreads();
+    if (warp == 0) {
+        int wa = s_wa[lane], wb = s_wb[lane];
+        const int ta = wa, tb = wb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ua = __shfl_up_sync(0xffffffffu, wa, o), ub = __shfl_up_sync(0xffffffffu, wb, o);
+            if (lane >= o) { wa += ua; wb += ub; }
+        }
+        s_wa[lane] = wa - ta;   // exclusive prefix of warp totals
+        s_wb[lane] = wb - tb;
+        if (lane == 31) s_gidx[1023] = wb;   // number of routed groups (read below, after the sync)
+    }
+    __syncthreads();
+    const int n_routed = s_gidx[1023];
+    __syncthreads();
+    if (tid < E) {
+        s_start[tid] = a - c + s_wa[warp];
+        s_gidx[tid] = b - nz + s_wb[warp];
+    }
+    __syncthreads();
+    if (tid < P) {
+        // stable: the rank among earlier pairs with the same expert
+        const int e = s_e[tid];
+        int r = 0;
+        for (int q = 0; q < tid; ++q) r += (s_e[q] == e);
+        const int row = s_start[e] + r;
+        const int t = tid / k, j = tid - t * k;
+        perm_token[row] = t;
+        pos[t * (k + 1) + j] = row;
+    }
+    if (tid < E && c > 0) {
+        const int g = s_gidx[tid];
+        gexp[g] = tid;
+        goff[g] = s_start[tid];
+        gcnt[g] = c;
+    }
+    if (n_shared) {
+        for (int t = tid; t < T; t += blockDim.x) {
+            perm_token[P + t] = t;
+            pos[t * (k + 1) + k] = P + t;
+        }
+        if (tid == 0) {
+            gexp[n_routed] = E;
+            goff[n_routed] = P;
+            gcnt[n_routed] = T;
+        }
+    }
+    if (tid == 0) *n_groups = n_routed + (n_shared ? 1 : 0);
+}
+
+// ---------------------------------------------------------------------------
+// gather: xp[row] = fp16(x[perm_token[row]]), blocks of 8 in operand order
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, int x_bf16,
+                                                   const int32_t* __restrict__ perm_token, int rows, int H,
+                                                   uint4* __restrict__ xp) {
+    const int nb = H / 8;
+    const long total = (long)rows * nb;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int row = (int)(idx / nb), blk = (int)(idx - (long)row * nb);
+        const int t = __ldg(perm_token + row);
+        float v[8];
+        if (x_bf16) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + (size_t)t * H) + blk);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                v[2 * q] = __uint_as_float(w[q] << 16);
+                v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+            }
+        } else {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * H) + 2 * blk;
+            const float4 p = __ldg(src), q = __ldg(src + 1);
+            v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
+            v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {   // position 2q holds element q, 2q + 1 holds element q + 4
+            const __half2 h = __floats2half2_rn(v[q], v[q + 4]);
+            o[q] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        xp[idx] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// grouped GEMM on tcgen05
+// ---------------------------------------------------------------------------
+//
+// Work items are (group g, 128-row weight tile mt). One persistent CTA per SM
+// walks the items; per item it computes D[128 weight rows][N tokens] over K in
+// chunks of 64 (one quantisation group):
+//   * a TMA thread copies the chunk's packed codes (128 rows x 32 B) and
+//     (scale, bias) pairs into a raw ring, and the group's token rows of the
+//     fp16 activations (N x 128 B, 128-byte swizzle) into an operand stage;
+//   * 8 dequantiser warps (two threads per weight row) turn the codes into
+//     fp16 w = code * scale + bias (one fp16 fma: correctly rounded) and store
+//     them into the operand stage in the 128-byte-swizzled K-major layout;
+//   * one thread issues tcgen05.mma (M = 128, N = round16(tokens), K = 16) x 4
+//     per chunk into a tensor-memory accumulator (two, alternating by item);
+//   * 4 epilogue warps read the accumulator (warp w owns lanes 32w..32w+31) and
+//     write either h = silu(gate) * up in fp16 (gate/up: the weight tile holds
+//     64 interleaved gate/up row pairs, so lane pairs exchange one shuffle) or
+//     the fp32 expert outputs (down).
+
+constexpr int kStages = 4, kRawStages = 8;
+constexpr int kEpiWarps = 4, kDqWarps = 8;
+constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
+constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr uint32_t kA16 = 128 * 128, kB16 = 128 * 128, kStageBytes = kA16 + kB16;
+constexpr uint32_t kRawCodes = 128 * 32, kRawMeta = 128 * 16, kRaw = kRawCodes + kRawMeta;
+constexpr uint32_t kTmemCols = 256;
+constexpr size_t kBarBytes = 8 * (2 * kStages + 2 * kRawStages + 4) + 16;
+constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kRawStages * kRaw + kBarBytes;
+
+struct GemmArgs {
+    const int32_t* gexp;
+    const int32_t* goff;
+    const int32_t* gcnt;
+    const int32_t* n_groups;
+    int K;          // reduction length (H for gate/up, I for down)
+    int n_mt;       // 128-row weight tiles per expert
+    int rows_out;   // weight rows that exist (2I or H)
+    void* out;      // gate/up: fp16 [rows][I]; down: fp32 [rows][H]
+    int ld_out;
+    unsigned* err;
+};
+
+// error bits (moe_layer_check): bit 16 + role
+enum { ERR_TMA = 1u << 16, ERR_DQ = 1u << 17, ERR_MMA = 1u << 18, ERR_EPI = 1u << 19, ERR_DRAIN = 1u << 20 };
+
+// fp16 pair from two nibbles placed at bits 0..3 and 16..19 of t: code * s + b
+__device__ __forceinline__ uint32_t dq_pair(uint32_t t, uint32_t s2, uint32_t b2) {
+    uint32_t r;
+    asm("{.reg .b32 c; lop3.b32 c, %1, 0x000F000F, 0x64006400, 0xEA;"   // (t & mask) | 1024.0
+        " sub.f16x2 c, c, %4; fma.rn.f16x2 %0, c, %2, %3;}"
+        : "=r"(r)
+        : "r"(t), "r"(s2), "r"(b2), "r"(0x64006400u));
+    return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_constant__ CUtensorMap tm_codes,
+                                                             const __grid_constant__ CUtensorMap tm_meta,
+                                                             const __grid_constant__ CUtensorMap tm_b,
+                                                             const GemmArgs a) {
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    uint8_t* raw = smem + kStages * kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRaw);
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kRawStages + 4);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    const uint32_t b_full = saddr(bars), b_empty = b_full + 8 * kStages;
+    const uint32_t b_rfull = b_empty + 8 * kStages, b_rempty = b_rfull + 8 * kRawStages;
+    const uint32_t b_afull = b_rempty + 8 * kRawStages, b_aempty = b_afull + 16;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(b_full + 8 * s, kDqThreads + 1);
+            mbar_init(b_empty + 8 * s, 1);
+        }
+        for (int r = 0; r < kRawStages; ++r) {
+            mbar_init(b_rfull + 8 * r, 1);
+            mbar_init(b_rempty + 8 * r, kDqThreads);
+        }
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(b_afull + 8 * c, 1);
+            mbar_init(b_aempty + 8 * c, kEpiWarps * 32);
+        }
+        *s_abort = 0;
+        mbar_fence_init();
+    }
+    if (warp == kMmaWarp) tmem_alloc(saddr(s_tmem), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const int n_items = *a.n_groups * a.n_mt;
+    const int nk = a.K / 64;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_codes);
+            tma_prefetch_desc(&tm_meta);
+            tma_prefetch_desc(&tm_b);
+            const uint64_t pol_w = l2_evict_first(), pol_b = l2_evict_last();
+            uint32_t it = 0;
+            for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+                const int g = w / a.n_mt, mt = w - g * a.n_mt;
+                const int e = a.gexp[g], off = a.goff[g], m = a.gcnt[g];
+                const int nb = (m + 15) >> 4;
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    const uint32_t rs = it % kRawStages, s = it % kStages;
+                    mbar_wait(b_rempty + 8 * rs, ((it / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                    mbar_arrive_tx(b_rfull + 8 * rs, kRaw);
+                    const uint32_t rd = saddr(raw + rs * kRaw);
+                    tma_load_3d(rd, &tm_codes, kc * 32, mt * 128, e, b_rfull + 8 * rs, pol_w);
+                    tma_load_3d(rd + kRawCodes, &tm_meta, a.K / 2 + (kc >> 2) * 16, mt * 128, e, b_rfull + 8 * rs,
+                                pol_w);
+                    mbar_wait(b_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                    mbar_arrive_tx(b_full + 8 * s, (uint32_t)nb * 2048u);
+                    const uint32_t bd = saddr(stages + s * kStageBytes + kA16);
+                    for (int j = 0; j < nb; ++j)
+                        tma_load_2d(bd + j * 2048, &tm_b, kc * 64, off + j * 16, b_full + 8 * s, pol_b);
+                }
+            }
+            // copies in flight land before the CTA exits (on the normal path the
+            // consumers have already waited for all of them)
+            const uint32_t n_tail = it < (uint32_t)kRawStages ? it : (uint32_t)kRawStages;
+            for (uint32_t q = it - n_tail; q < it; ++q) {
+                int dummy = 0;
+                mbar_wait(b_rfull + 8 * (q % kRawStages), (q / kRawStages) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
+        const int d = tid - kEpiWarps * 32;
+        const int r = d >> 1, hf = d & 1;
+        uint32_t it = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+            for (int kc = 0; kc < nk; ++kc, ++it) {
+                const uint32_t rs = it % kRawStages, s = it % kStages;
+                mbar_wait(b_rfull + 8 * rs, (it / kRawStages) & 1, s_abort, a.err, ERR_DQ);
+                const uint8_t* rw = raw + rs * kRaw;
+                const uint4 cw = *reinterpret_cast<const uint4*>(rw + r * 32 + hf * 16);
+                const uint32_t mw = *reinterpret_cast<const uint32_t*>(rw + kRawCodes + r * 16 + (kc & 3) * 4);
+                mbar_arrive(b_rempty + 8 * rs);
+                const uint32_t s2 = __byte_perm(mw, 0, 0x1010), b2 = __byte_perm(mw, 0, 0x3232);
+                uint4 o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t v = u4w(cw, j);
+                    o[j] = make_uint4(dq_pair(v, s2, b2), dq_pair(v >> 4, s2, b2), dq_pair(v >> 8, s2, b2),
+                                      dq_pair(v >> 12, s2, b2));
+                }
+                mbar_wait(b_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort, a.err, ERR_DQ);
+                uint8_t* A = stages + s * kStageBytes + r * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(A + ((((hf << 2) | j) ^ (r & 7)) << 4)) = o[j];
+                fence_async_smem();
+                mbar_arrive(b_full + 8 * s);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            uint32_t it = 0, tile = 0;
+            for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++tile) {
+                const int g = w / a.n_mt;
+                const int m = a.gcnt[g];
+                const int N = ((m + 15) >> 4) << 4;
+                const uint32_t idesc = idesc_f16_f32(128, N);
+                const uint32_t acc = tile & 1;
+                mbar_wait(b_aempty + 8 * acc, ((tile >> 1) & 1) ^ 1, s_abort, a.err, ERR_MMA);
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * 128;
+                for (int kc = 0; kc < nk; ++kc, ++it) {
+                    const uint32_t s = it % kStages;
+                    mbar_wait(b_full + 8 * s, (it / kStages) & 1, s_abort, a.err, ERR_MMA);
+                    tc_fence_after();
+                    const uint32_t A = saddr(stages + s * kStageBytes), B = A + kA16;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(d_tmem, desc_sw128(A + kk * 32), desc_sw128(B + kk * 32), idesc, (kc | kk) != 0);
+                    mma_commit(b_empty + 8 * s);
+                }
+                mma_commit(b_afull + 8 * acc);
+            }
+            // every MMA completes before the tensor memory is released
+            if (tile > 0) {
+                int dummy = 0;
+                mbar_wait(b_afull + 8 * ((tile - 1) & 1), ((tile - 1) >> 1) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
+            }
+        }
+        __syncwarp();
+    } else {   // epilogue warps 0..3: tensor-memory lanes 32*warp .. 32*warp + 31
+        const int row = warp * 32 + lane;
+        uint32_t tile = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++tile) {
+            const int g = w / a.n_mt, mt = w - g * a.n_mt;
+            const int off = a.goff[g], m = a.gcnt[g];
+            const int N = ((m + 15) >> 4) << 4;
+            const uint32_t acc = tile & 1;
+            mbar_wait(b_afull + 8 * acc, (tile >> 1) & 1, s_abort, a.err, ERR_EPI);
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + acc * 128;
+            for (int c0 = 0; c0 < N; c0 += 16) {
+                float v[16];
+                tmem_ld16(tb + c0, v);
+                if (MODE == 0) {
+                    const int i = mt * 64 + (row >> 1);
+                    const int ip = (i & ~7) | blk_pos(i & 7);
+                    __half* hp = static_cast<__half*>(a.out);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float up = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                        if (!(row & 1) && c0 + j < m)
+                            hp[(size_t)(off + c0 + j) * a.ld_out + ip] = __float2half_rn(silu_f(v[j]) * up);
+                    }
+                } else {
+                    const int n = mt * 128 + row;
+                    float* yp = static_cast<float*>(a.out);
+                    if (n < a.rows_out) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (c0 + j < m) yp[(size_t)(off + c0 + j) * a.ld_out + n] = v[j];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(b_aempty + 8 * acc);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// combine: y[t] = y_shared[t] + sum_j w[t][j] * y_{S_j}[t], fixed order
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) k_pf_combine(const float* __restrict__ yp, const int32_t* __restrict__ pos,
+                                                    const float* __restrict__ wts, int k, int n_shared, int H,
+                                                    void* __restrict__ y, int y_bf16, float* __restrict__ y32) {
+    const int t = blockIdx.x;
+    const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+    if (n >= H) return;
+    const int32_t* pt = pos + (size_t)t * (k + 1);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (n_shared) acc = __ldcg(reinterpret_cast<const float4*>(yp + (size_t)pt[k] * H + n));
+    for (int j = 0; j < k; ++j) {
+        const float w = wts[(size_t)t * k + j];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(yp + (size_t)pt[j] * H + n));
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+    }
+    const size_t o = (size_t)t * H + n;
+    if (y32) *reinterpret_cast<float4*>(y32 + o) = acc;
+    if (y) {
+        if (y_bf16) {
+            __nv_bfloat16* yb = static_cast<__nv_bfloat16*>(y) + o;
+            yb[0] = __float2bfloat16_rn(acc.x);
+            yb[1] = __float2bfloat16_rn(acc.y);
+            yb[2] = __float2bfloat16_rn(acc.z);
+            yb[3] = __float2bfloat16_rn(acc.w);
+        } else {
+            *reinterpret_cast<float4*>(static_cast<float*>(y) + o) = acc;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps and launches
+// ---------------------------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// rows of packed weights (bytes), one plane per expert record
+bool map_weight_rows(CUtensorMap* tm, const uint8_t* base, size_t row_b, int rows, int recs, size_t rec_b,
+                     uint32_t box_x) {
+    const cuuint64_t dims[3] = {row_b, (cuuint64_t)rows, (cuuint64_t)recs};
+    const cuuint64_t strides[2] = {row_b, rec_b};
+    const cuuint32_t box[3] = {box_x, 128, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encoder()(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp16 activations [rows][K], 16-row x 64-column boxes with the 128-byte swizzle
+bool map_act(CUtensorMap* tm, void* base, int K, int rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t es[2] = {1, 1};
+    return encoder()(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t prefill_kernel_setup(Layer& L) {
+    const auto& d = L.d;
+    if (d.cache_slots > 0 || !L.pf.xp) return cudaSuccess;   // prefill needs resident experts
+    cudaError_t e = cudaFuncSetAttribute(k_pf_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_pf_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    if (e != cudaSuccess) return e;
+    if (!encoder()) return cudaErrorSymbolNotFound;
+    const int H = d.hidden, I = d.inter, recs = d.n_experts + d.n_shared;
+    const uint8_t* gu = L.experts;
+    const uint8_t* dn = L.experts + gu_block_bytes(H, I);
+    bool ok = map_weight_rows(&L.pf.tm[0], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 32) &&
+              map_weight_rows(&L.pf.tm[1], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 16) &&
+              map_weight_rows(&L.pf.tm[2], dn, row_bytes(I), H, recs, L.rec_bytes, 32) &&
+              map_weight_rows(&L.pf.tm[3], dn, row_bytes(I), H, recs, L.rec_bytes, 16) &&
+              map_act(&L.pf.tm[4], L.pf.xp, H, L.pf.max_rows) && map_act(&L.pf.tm[5], L.pf.hp, I, L.pf.max_rows);
+    if (!ok) return cudaErrorInvalidValue;
+    L.pf.ready = true;
+    return cudaSuccess;
+}
+
+cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s) {
+    if (!L.pf.ready) return cudaErrorNotSupported;
+    const auto& d = L.d;
+    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts, ns = d.n_shared;
+    const int xb = d.act_dtype == MOE_BF16;
+    const int P = T * k, rows = P + T * ns;
+    auto& pf = L.pf;
+
+    prof_begin(L, K_PF_PERMUTE, s);
+    k_pf_permute<<<1, kPermThreads, 0, s>>>(L.ids, T, k, E, ns, pf.group_expert, pf.group_off, pf.group_cnt,
+                                            pf.n_groups, pf.perm_token, pf.pos);
+    prof_end(L, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    prof_begin(L, K_PF_GATHER, s);
+    const long blocks = ((long)rows * (H / 8) + 255) / 256;
+    k_pf_gather<<<(int)std::min<long>(blocks, (long)L.num_sms * 8), 256, 0, s>>>(x, xb, pf.perm_token, rows, H,
+                                                                                 static_cast<uint4*>(pf.xp));
+    prof_end(L, s);
+
+    GemmArgs gu{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, H, I / 64, 2 * I, pf.hp, I, pf.err};
+    prof_begin(L, K_PF_GEMM_GU, s);
+    k_pf_gemm<0><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[0], pf.tm[1], pf.tm[4], gu);
+    prof_end(L, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    GemmArgs dn{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, I, (H + 127) / 128, H, pf.yp, H, pf.err};
+    prof_begin(L, K_PF_GEMM_DOWN, s);
+    k_pf_gemm<1><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[2], pf.tm[3], pf.tm[5], dn);
+    prof_end(L, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    prof_begin(L, K_PF_COMBINE, s);
+    k_pf_combine<<<dim3(T, (H / 4 + 255) / 256), 256, 0, s>>>(pf.yp, pf.pos, L.wts, k, ns, H, y, xb, y_f32);
+    prof_end(L, s);
+    return cudaGetLastError();
 }
 
 }  // namespace moe
