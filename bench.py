@@ -166,13 +166,181 @@ def run_reference(args, spec, workload):
     print(json.dumps(line), flush=True)
 
 
+PREFILL_DESC = {
+    "glm_prefill": "GLM-scale prefill chunk: H6144 I2048 E256 top-8 + 1 shared, 128 tokens, "
+                   "router bias from Zipf(1.1) expert popularity (uneven expert loads)",
+    "glm_prefill_dense": "GLM-scale prefill chunk, all 128 tokens on the same 8 experts "
+                         "(router bias +30 on experts 0..7, -30 elsewhere): 9 full 128-token groups",
+}
+
+
+def prefill_layer(workload, seed=0, experts=None):
+    import dataclasses
+    spec = si.CONFIGS["glm_prefill"]
+    if experts:
+        spec = dataclasses.replace(spec, n_experts=experts)
+    layer = si.gen_layer(seed, 0, spec)
+    if workload == "glm_prefill_dense":
+        bias = np.full(layer.spec.n_experts, -30.0, np.float32)
+        bias[:8] = 30.0
+        layer = dataclasses.replace(layer, router_bias=bias)
+    return layer
+
+
+def run_prefill(args):
+    """One step = one 128-token chunk through each of R rotating layer replicas."""
+    ws, rank, local = dist_info()
+    T = 128
+    layer = prefill_layer(args.workload, experts=args.experts)
+    spec = layer.spec
+    workload = PREFILL_DESC[args.workload]
+    if args.experts:
+        workload = workload.replace("E256", f"E{args.experts}")
+    X = si.gen_tokens(1000 * rank, 0, T, spec)
+    flops_gu = 2.0 * T * (spec.top_k + spec.n_shared) * 2 * spec.inter * spec.hidden
+    flops_down = 2.0 * T * (spec.top_k + spec.n_shared) * spec.hidden * spec.inter
+    flops_router = 2.0 * T * spec.n_experts * spec.hidden
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n = 1
+        for _ in range(args.warmup):
+            oracle_sample(layer, X, n)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_sample(layer, X, n)
+        dt = time.perf_counter() - t0
+        v = args.steps * n / dt
+        print(json.dumps({"impl": "reference", "metric": "MoE-layer prefill tokens/s", "value": v, "unit": UNIT,
+                          "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": workload, "tokens_per_step": n},
+                          "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                           "sample": f"{n} token of the chunk per step, fp64 numpy, 1 BLAS thread"},
+                          "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import quantized_routed_expert_moe_gb300 as moe
+    from quantized_routed_expert_moe_gb300 import build as _b
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        _b.build()
+    if ws > 1:
+        dist.barrier()
+    R = args.replicas or 4
+    reps = [moe.MoELayer(layer, device=local, max_tokens=T) for _ in range(R)]
+    x_host = torch.from_numpy(np.ascontiguousarray(X.view(np.int16))).view(torch.bfloat16).pin_memory()
+    x_dev = x_host.to("cuda")
+    y_dev = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device="cuda")
+    y_host = torch.empty((T, spec.hidden), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for r in reps:
+            r.prefill_chunk(x_dev, T, y_dev, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    for r in reps:
+        st, bits = r.check()
+        if st:
+            raise RuntimeError(f"prefill reported device error bits {bits:#x}")
+
+    for r in reps:
+        moe.moe_profile_start(r.handle, 16 * args.steps)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    prof = {}
+    for r in reps:
+        for name, (n, t) in moe.moe_profile_stop(r.handle).items():
+            a, b = prof.get(name, (0, 0.0))
+            prof[name] = (a + n, b + t)
+
+    # end to end: pinned host chunk -> device, prefill, device -> pinned host output
+    for _ in range(args.warmup):
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y_dev, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+
+    mx = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    ms, e2e_s = float(mx[0]), float(mx[1])
+    total_tokens = T * R * args.steps * ws
+    value = total_tokens / (ms / 1e3)
+    _, tflops, peak_kind = peaks()
+    kernels = {k: {"launches": n, "avg_us": t / max(n, 1) * 1e3} for k, (n, t) in prof.items()}
+    n_gu, t_gu = prof.get("prefill_gemm_gateup", (0, 0.0))
+    gu_avg_s = t_gu / max(n_gu, 1) / 1e3
+    achieved = flops_gu / gu_avg_s / 1e12 if n_gu else None
+    chunk_flops = flops_gu + flops_down + flops_router
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": "MoE-layer prefill tokens/s (128-token chunks)", "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": workload, "tokens_per_step": T * R, "layer_replicas": R,
+                   "l2": f"inputs larger than L2: {R} rotating layer replicas",
+                   "parallelism": f"replicas x{ws}"},
+        "chunk_tflops": chunk_flops * R * args.steps * ws / (ms / 1e3) / 1e12,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                     "frac": achieved / tflops if achieved else None, "traffic": None, "kernel": "prefill_gemm_gateup",
+                     "peak_source": f"{peak_kind} bf16_tflops (cuBLAS), burst; fp16 and bf16 share the dense rate",
+                     "algorithmic_flops_per_launch": flops_gu, "avg_launch_us": gu_avg_s * 1e6},
+        "kernels": kernels,
+        "e2e": {"value": total_tokens / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": sum(n for n, _ in prof.values()),
+        "clocks": clk,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="glm_decode", choices=["glm_decode", "gemma_decode", "tiny"])
+    ap.add_argument("--workload", default="glm_decode",
+                    choices=["glm_decode", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense"])
     ap.add_argument("--tokens", type=int, default=1000)
     ap.add_argument("--replicas", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -183,6 +351,9 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    if args.workload.startswith("glm_prefill"):
+        run_prefill(args)
+        return
     spec = si.CONFIGS[args.workload]
     if args.experts:
         import dataclasses

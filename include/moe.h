@@ -286,12 +286,18 @@ enum {
  * the grid size. Waits for the device. */
 moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t* n_ctas);
 
-/* Trace of the last three-kernel decode (while MOE_OPT_TRACE is on): out
- * receives 3 * MOE_TRACE_MAX_CTAS * 4 global-timer stamps (ns), ordered
- * kernel (router, gate/up, down), CTA, point (start, dependency satisfied,
- * main work done, end); 0 where a CTA or point did not run. Waits for the
- * device. cap must be at least 3 * MOE_TRACE_MAX_CTAS * 4. */
+/* Traces of the last three-kernel decode and of the last prefill chunk's two
+ * grouped GEMMs (while MOE_OPT_TRACE is on): out receives
+ * MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4 uint64 values ordered kernel,
+ * CTA, slot; 0 where a CTA or slot did not run. Waits for the device.
+ *   kernels 0..2 (decode router, gate/up, down): global-timer stamps (ns) at
+ *     start, dependency satisfied, main work done, end;
+ *   kernels 3..4 (prefill gate/up GEMM, down GEMM): SM clock cycles spent
+ *     waiting by the copy thread, by one dequantiser thread and by the MMA
+ *     thread, then the CTA's total cycles.
+ * cap must be at least MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4. */
 #define MOE_TRACE_MAX_CTAS 1024
+#define MOE_TRACE_KERNELS 5
 moe_status moe_trace_read_split(moe_layer* layer, uint64_t* out, int32_t cap);
 
 moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value);

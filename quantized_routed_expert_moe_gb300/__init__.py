@@ -321,18 +321,22 @@ def moe_trace_read(handle, max_ctas: int = 1024):
 
 
 MOE_TRACE_MAX_CTAS = 1024
-SPLIT_TRACE_KERNELS = ("router", "gateup", "down")
+MOE_TRACE_KERNELS = 5
+SPLIT_TRACE_KERNELS = ("router", "gateup", "down", "prefill_gemm_gateup", "prefill_gemm_down")
 SPLIT_TRACE_POINTS = ("start", "dependency", "main_done", "end")
+PREFILL_WAIT_ROLES = ("copy", "dequant", "mma", "total")
 
 
 def moe_trace_read_split(handle):
-    """Per-kernel, per-CTA stamps (ns) of the last three-kernel decode: [3][1024][4]."""
-    cap = 3 * MOE_TRACE_MAX_CTAS * 4
+    """[kernel][cta][4]: decode stamps (ns) for kernels 0..2; for the prefill
+    GEMMs (kernels 3..4) the cycles the copy, dequantiser and MMA roles waited
+    and the CTA's total cycles."""
+    cap = MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4
     buf = (ctypes.c_uint64 * cap)()
     _check(lib().moe_trace_read_split(handle, ctypes.cast(buf, ctypes.c_void_p), cap), "moe_trace_read_split")
     v = list(buf)
     return [[v[(kk * MOE_TRACE_MAX_CTAS + c) * 4:(kk * MOE_TRACE_MAX_CTAS + c) * 4 + 4]
-             for c in range(MOE_TRACE_MAX_CTAS)] for kk in range(3)]
+             for c in range(MOE_TRACE_MAX_CTAS)] for kk in range(MOE_TRACE_KERNELS)]
 
 
 class MoELayer:

@@ -436,7 +436,7 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
                 const size_t nb = (size_t)L.num_sms * MOE_TRACE_POINTS * 8;
                 MOE_CUDA_TRY(cudaMalloc(&L.trace, nb));
                 MOE_CUDA_TRY(cudaMemset(L.trace, 0, nb));
-                const size_t ns = (size_t)3 * MOE_TRACE_MAX_CTAS * 4 * 8;
+                const size_t ns = (size_t)MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4 * 8;
                 MOE_CUDA_TRY(cudaMalloc(&L.trace_split, ns));
                 MOE_CUDA_TRY(cudaMemset(L.trace_split, 0, ns));
             }
@@ -464,8 +464,8 @@ moe_status moe_trace_read_split(moe_layer* layer, uint64_t* out, int32_t cap) {
     if (!layer || !out) return fail(MOE_E_INVALID, "NULL argument");
     Layer& L = layer->L;
     if (!L.trace_split) return fail(MOE_E_STATE, "tracing was never enabled (MOE_OPT_TRACE)");
-    const int n = 3 * MOE_TRACE_MAX_CTAS * 4;
-    if (cap < n) return fail(MOE_E_INVALID, "cap smaller than 3 * MOE_TRACE_MAX_CTAS * 4");
+    const int n = MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4;
+    if (cap < n) return fail(MOE_E_INVALID, "cap smaller than MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4");
     DeviceGuard g(L.device);
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     MOE_CUDA_TRY(cudaDeviceSynchronize());

@@ -83,8 +83,9 @@ struct PrefillScratch {
     void* hp = nullptr;               // [rows][I] fp16 SwiGLU outputs (same block permutation)
     float* yp = nullptr;              // [rows][H] fp32 expert outputs (unweighted)
     int max_rows = 0;
-    // TMA descriptors: gate/up codes, gate/up meta, down codes, down meta, xp, hp
-    CUtensorMap tm[6];
+    // TMA descriptors: gate/up codes, gate/up meta, down codes, down meta, then
+    // xp and hp with boxes of 16, 32, 64 and 128 token rows
+    CUtensorMap tm[12];
     bool ready = false;
 };
 
@@ -151,7 +152,7 @@ struct Layer {
     int decode_path = MOE_PATH_AUTO;
     int test_no_publish = 0;
     unsigned long long* trace = nullptr;  // device [num_sms][MOE_TRACE_POINTS] when tracing is on
-    unsigned long long* trace_split = nullptr;  // device [3][MOE_TRACE_MAX_CTAS][4]
+    unsigned long long* trace_split = nullptr;  // device [MOE_TRACE_KERNELS][MOE_TRACE_MAX_CTAS][4]
     bool trace_on = false;
     unsigned long long* split_trace(int kernel) const {
         return (trace_on && trace_split) ? trace_split + (size_t)kernel * MOE_TRACE_MAX_CTAS * 4 : nullptr;

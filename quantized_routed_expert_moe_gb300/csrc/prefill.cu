@@ -161,29 +161,39 @@ __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, i
 // Work items are (group g, 128-row weight tile mt). One persistent CTA per SM
 // walks the items; per item it computes D[128 weight rows][N tokens] over K in
 // chunks of 64 (one quantisation group):
-//   * a TMA thread copies the chunk's packed codes (128 rows x 32 B) and
-//     (scale, bias) pairs into a raw ring, and the group's token rows of the
-//     fp16 activations (N x 128 B, 128-byte swizzle) into an operand stage;
-//   * 8 dequantiser warps (two threads per weight row) turn the codes into
-//     fp16 w = code * scale + bias (one fp16 fma: correctly rounded) and store
-//     them into the operand stage in the 128-byte-swizzled K-major layout;
-//   * one thread issues tcgen05.mma (M = 128, N = round16(tokens), K = 16) x 4
-//     per chunk into a tensor-memory accumulator (two, alternating by item);
+//   * a TMA thread copies the packed codes of 4 chunks (128 rows x 128 B, with
+//     the 128-byte swizzle so that the dequantisers' reads are conflict-free)
+//     and their (scale, bias) pairs (128 rows x 16 B) into a raw ring, and,
+//     per chunk, the group's token rows of the fp16 activations (N x 128 B,
+//     128-byte swizzle) into a shared-memory operand stage;
+//   * 8 dequantiser warps turn the codes into fp16 w = code * scale + bias (one
+//     fp16 fma: correctly rounded) and store them straight into tensor memory
+//     (tcgen05.st): warp w owns tensor-memory lanes 32 (w % 4) .. + 31 (one
+//     weight row each) and half of the chunk's 64 columns of K. The weight
+//     operand never touches shared memory, which leaves the shared-memory
+//     bandwidth to the token operand and the raw codes;
+//   * one thread issues tcgen05.mma (A from tensor memory, B from shared
+//     memory; M = 128, N = round16(tokens), K = 16) x 4 per chunk into a
+//     tensor-memory accumulator (two, alternating by item);
 //   * 4 epilogue warps read the accumulator (warp w owns lanes 32w..32w+31) and
 //     write either h = silu(gate) * up in fp16 (gate/up: the weight tile holds
 //     64 interleaved gate/up row pairs, so lane pairs exchange one shuffle) or
 //     the fp32 expert outputs (down).
+//
+// Tensor memory (512 columns): accumulators at columns 0 and 128; weight
+// operand stages of 32 columns (128 x 64 fp16) from column 256.
 
-constexpr int kStages = 4, kRawStages = 8;
+constexpr int kStages = 8, kRawStages = 4, kChunksPerRaw = 4;
 constexpr int kEpiWarps = 4, kDqWarps = 8;
 constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
 constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
-constexpr int kDqThreads = kDqWarps * 32;
-constexpr uint32_t kA16 = 128 * 128, kB16 = 128 * 128, kStageBytes = kA16 + kB16;
-constexpr uint32_t kRawCodes = 128 * 32, kRawMeta = 128 * 16, kRaw = kRawCodes + kRawMeta;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kB16 = 128 * 128;
+constexpr uint32_t kRawCodes = 128 * 128, kRawMeta = 128 * 16, kRaw = kRawCodes + kRawMeta;
+constexpr uint32_t kTmemCols = 512, kTmemA = 256, kACols = 32;
 constexpr size_t kBarBytes = 8 * (2 * kStages + 2 * kRawStages + 4) + 16;
-constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kRawStages * kRaw + kBarBytes;
+constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kB16 + (size_t)kRawStages * kRaw + kBarBytes;
+static_assert(kRaw % 1024 == 0 && kB16 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(kTmemA + kStages * kACols <= kTmemCols, "weight stages exceed tensor memory");
 
 struct GemmArgs {
     const int32_t* gexp;
@@ -196,6 +206,24 @@ struct GemmArgs {
     void* out;      // gate/up: fp16 [rows][I]; down: fp32 [rows][H]
     int ld_out;
     unsigned* err;
+    unsigned long long* tr;   // [gridDim][4]: wait cycles of copy / dequant / MMA, total cycles; or null
+};
+
+// mbarrier wait that, when tracing, adds the SM clock cycles spent waiting to `acc`
+struct TimedWait {
+    unsigned long long* tr;
+    unsigned long long acc;
+    __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* err,
+                                               unsigned code) {
+        if (!tr) return mbar_wait(bar, parity, abort, err, code);
+        const long long t0 = clock64();
+        const bool ok = mbar_wait(bar, parity, abort, err, code);
+        acc += (unsigned long long)(clock64() - t0);
+        return ok;
+    }
+    __device__ __forceinline__ void store(int slot, unsigned long long v) {
+        if (tr) tr[blockIdx.x * 4 + slot] = v;
+    }
 };
 
 // error bits (moe_layer_check): bit 16 + role
@@ -214,12 +242,15 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t t, uint32_t s2, uint32_t b2
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_constant__ CUtensorMap tm_codes,
                                                              const __grid_constant__ CUtensorMap tm_meta,
-                                                             const __grid_constant__ CUtensorMap tm_b,
+                                                             const __grid_constant__ CUtensorMap tm_b16,
+                                                             const __grid_constant__ CUtensorMap tm_b32,
+                                                             const __grid_constant__ CUtensorMap tm_b64,
+                                                             const __grid_constant__ CUtensorMap tm_b128,
                                                              const GemmArgs a) {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    uint8_t* stages = smem;
-    uint8_t* raw = smem + kStages * kStageBytes;
+    uint8_t* bst = smem;                          // token operand stages
+    uint8_t* raw = smem + kStages * kB16;         // raw code / meta ring
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRaw);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kRawStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
@@ -230,16 +261,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(b_full + 8 * s, kDqThreads + 1);
+            mbar_init(b_full + 8 * s, kDqWarps + 1);
             mbar_init(b_empty + 8 * s, 1);
         }
         for (int r = 0; r < kRawStages; ++r) {
             mbar_init(b_rfull + 8 * r, 1);
-            mbar_init(b_rempty + 8 * r, kDqThreads);
+            mbar_init(b_rempty + 8 * r, kDqWarps);
         }
         for (int c = 0; c < 2; ++c) {
             mbar_init(b_afull + 8 * c, 1);
-            mbar_init(b_aempty + 8 * c, kEpiWarps * 32);
+            mbar_init(b_aempty + 8 * c, kEpiWarps);
         }
         *s_abort = 0;
         mbar_fence_init();
@@ -249,103 +280,153 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    const long long t_start = clock64();
     const int n_items = *a.n_groups * a.n_mt;
     const int nk = a.K / 64;
+    TimedWait tw{a.tr, 0ull};
 
     if (warp == kTmaWarp) {
-        if (lane == 0) {
+        // the whole warp walks the loop (waits included) and one elected lane
+        // issues each copy, so the warp stays converged
+        if (elect_one()) {
             tma_prefetch_desc(&tm_codes);
             tma_prefetch_desc(&tm_meta);
-            tma_prefetch_desc(&tm_b);
-            const uint64_t pol_w = l2_evict_first(), pol_b = l2_evict_last();
-            uint32_t it = 0;
-            for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-                const int g = w / a.n_mt, mt = w - g * a.n_mt;
-                const int e = a.gexp[g], off = a.goff[g], m = a.gcnt[g];
-                const int nb = (m + 15) >> 4;
-                for (int kc = 0; kc < nk; ++kc, ++it) {
-                    const uint32_t rs = it % kRawStages, s = it % kStages;
-                    mbar_wait(b_rempty + 8 * rs, ((it / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+            tma_prefetch_desc(&tm_b16);
+            tma_prefetch_desc(&tm_b32);
+            tma_prefetch_desc(&tm_b64);
+            tma_prefetch_desc(&tm_b128);
+        }
+        __syncwarp();
+        const uint64_t pol_w = l2_evict_first(), pol_b = l2_evict_last();
+        uint32_t it = 0, rit = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+            const int g = w / a.n_mt, mt = w - g * a.n_mt;
+            const int e = a.gexp[g], off = a.goff[g], m = a.gcnt[g];
+            // one copy per chunk: the smallest box of 16, 32, 64 or 128 token rows that holds the group
+            const CUtensorMap* tmb = m <= 16 ? &tm_b16 : m <= 32 ? &tm_b32 : m <= 64 ? &tm_b64 : &tm_b128;
+            const uint32_t b_bytes = (m <= 16 ? 16u : m <= 32 ? 32u : m <= 64 ? 64u : 128u) * 128u;
+            for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
+                const uint32_t rs = rit % kRawStages;
+                tw(b_rempty + 8 * rs, ((rit / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                if (elect_one()) {
                     mbar_arrive_tx(b_rfull + 8 * rs, kRaw);
                     const uint32_t rd = saddr(raw + rs * kRaw);
-                    tma_load_3d(rd, &tm_codes, kc * 32, mt * 128, e, b_rfull + 8 * rs, pol_w);
-                    tma_load_3d(rd + kRawCodes, &tm_meta, a.K / 2 + (kc >> 2) * 16, mt * 128, e, b_rfull + 8 * rs,
-                                pol_w);
-                    mbar_wait(b_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
-                    mbar_arrive_tx(b_full + 8 * s, (uint32_t)nb * 2048u);
-                    const uint32_t bd = saddr(stages + s * kStageBytes + kA16);
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_2d(bd + j * 2048, &tm_b, kc * 64, off + j * 16, b_full + 8 * s, pol_b);
+                    tma_load_3d(rd, &tm_codes, kb * 128, mt * 128, e, b_rfull + 8 * rs, pol_w);
+                    tma_load_3d(rd + kRawCodes, &tm_meta, a.K / 2 + kb * 16, mt * 128, e, b_rfull + 8 * rs, pol_w);
                 }
-            }
-            // copies in flight land before the CTA exits (on the normal path the
-            // consumers have already waited for all of them)
-            const uint32_t n_tail = it < (uint32_t)kRawStages ? it : (uint32_t)kRawStages;
-            for (uint32_t q = it - n_tail; q < it; ++q) {
-                int dummy = 0;
-                mbar_wait(b_rfull + 8 * (q % kRawStages), (q / kRawStages) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
-            }
-        }
-        __syncwarp();
-    } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
-        const int d = tid - kEpiWarps * 32;
-        const int r = d >> 1, hf = d & 1;
-        uint32_t it = 0;
-        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
-            for (int kc = 0; kc < nk; ++kc, ++it) {
-                const uint32_t rs = it % kRawStages, s = it % kStages;
-                mbar_wait(b_rfull + 8 * rs, (it / kRawStages) & 1, s_abort, a.err, ERR_DQ);
-                const uint8_t* rw = raw + rs * kRaw;
-                const uint4 cw = *reinterpret_cast<const uint4*>(rw + r * 32 + hf * 16);
-                const uint32_t mw = *reinterpret_cast<const uint32_t*>(rw + kRawCodes + r * 16 + (kc & 3) * 4);
-                mbar_arrive(b_rempty + 8 * rs);
-                const uint32_t s2 = __byte_perm(mw, 0, 0x1010), b2 = __byte_perm(mw, 0, 0x3232);
-                uint4 o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t v = u4w(cw, j);
-                    o[j] = make_uint4(dq_pair(v, s2, b2), dq_pair(v >> 4, s2, b2), dq_pair(v >> 8, s2, b2),
-                                      dq_pair(v >> 12, s2, b2));
-                }
-                mbar_wait(b_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort, a.err, ERR_DQ);
-                uint8_t* A = stages + s * kStageBytes + r * 128;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(A + ((((hf << 2) | j) ^ (r & 7)) << 4)) = o[j];
-                fence_async_smem();
-                mbar_arrive(b_full + 8 * s);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) {
-            uint32_t it = 0, tile = 0;
-            for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++tile) {
-                const int g = w / a.n_mt;
-                const int m = a.gcnt[g];
-                const int N = ((m + 15) >> 4) << 4;
-                const uint32_t idesc = idesc_f16_f32(128, N);
-                const uint32_t acc = tile & 1;
-                mbar_wait(b_aempty + 8 * acc, ((tile >> 1) & 1) ^ 1, s_abort, a.err, ERR_MMA);
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + acc * 128;
-                for (int kc = 0; kc < nk; ++kc, ++it) {
+                __syncwarp();
+                const int kc1 = min(nk, (kb + 1) * kChunksPerRaw);
+                for (int kc = kb * kChunksPerRaw; kc < kc1; ++kc, ++it) {
                     const uint32_t s = it % kStages;
-                    mbar_wait(b_full + 8 * s, (it / kStages) & 1, s_abort, a.err, ERR_MMA);
-                    tc_fence_after();
-                    const uint32_t A = saddr(stages + s * kStageBytes), B = A + kA16;
+                    tw(b_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                    if (elect_one()) {
+                        mbar_arrive_tx(b_full + 8 * s, b_bytes);
+                        tma_load_2d(saddr(bst + s * kB16), tmb, kc * 64, off, b_full + 8 * s, pol_b);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+        // copies in flight land before the CTA exits (on the normal path the
+        // consumers have already waited for all of them)
+        const uint32_t n_tail = rit < (uint32_t)kRawStages ? rit : (uint32_t)kRawStages;
+        for (uint32_t q = rit - n_tail; q < rit; ++q) {
+            int dummy = 0;
+            mbar_wait(b_rfull + 8 * (q % kRawStages), (q / kRawStages) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
+        }
+        if (lane == 0) tw.store(0, tw.acc);
+    } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
+        // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows), half hf
+        // of each chunk's K (columns 16 hf .. 16 hf + 15 of the stage)
+        const int dw = warp - kEpiWarps, q = dw & 3, hf = dw >> 2;
+        const int r = 32 * q + lane;
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemA + 16 * hf;
+        uint32_t it = 0, rit = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+            for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
+                // one raw block (up to 4 chunks) at a time: all of its codes are
+                // read and converted before any is stored, for instruction-level
+                // parallelism across the chunks
+                const uint32_t rs = rit % kRawStages;
+                tw(b_rfull + 8 * rs, (rit / kRawStages) & 1, s_abort, a.err, ERR_DQ);
+                const uint8_t* rw = raw + rs * kRaw;
+                const uint4 mq = *reinterpret_cast<const uint4*>(rw + kRawCodes + r * 16);
+                const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
+                uint4 cw[kChunksPerRaw];
+#pragma unroll
+                for (int c = 0; c < kChunksPerRaw; ++c) {
+                    // 16-byte unit 2c + hf of row r, at its 128-byte-swizzled place
+                    const int u = (c << 1) | hf;
+                    cw[c] = *reinterpret_cast<const uint4*>(rw + r * 128 + ((u ^ (r & 7)) << 4));
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_rempty + 8 * rs);
+                uint32_t o[kChunksPerRaw][16];
+#pragma unroll
+                for (int c = 0; c < kChunksPerRaw; ++c) {
+                    const uint32_t mw = u4w(mq, c);
+                    const uint32_t s2 = __byte_perm(mw, 0, 0x1010), b2 = __byte_perm(mw, 0, 0x3232);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t v = u4w(cw[c], j);
+                        o[c][4 * j + 0] = dq_pair(v, s2, b2);
+                        o[c][4 * j + 1] = dq_pair(v >> 4, s2, b2);
+                        o[c][4 * j + 2] = dq_pair(v >> 8, s2, b2);
+                        o[c][4 * j + 3] = dq_pair(v >> 12, s2, b2);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < kChunksPerRaw; ++c) {
+                    if (c < nc) {
+                        const uint32_t s = (it + c) % kStages;
+                        tw(b_empty + 8 * s, (((it + c) / kStages) & 1) ^ 1, s_abort, a.err, ERR_DQ);
+                        tc_fence_after();
+                        tmem_st16(ta + s * kACols, o[c]);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    for (int c = 0; c < nc; ++c) mbar_arrive(b_full + 8 * ((it + c) % kStages));
+                it += nc;
+            }
+        }
+        if (dw == 0 && lane == 0) tw.store(1, tw.acc);
+    } else if (warp == kMmaWarp) {
+        // converged warp; one elected lane issues the MMAs and commits
+        uint32_t it = 0, tile = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++tile) {
+            const int g = w / a.n_mt;
+            const int m = a.gcnt[g];
+            const int N = ((m + 15) >> 4) << 4;
+            const uint32_t idesc = idesc_f16_f32(128, N);
+            const uint32_t acc = tile & 1;
+            tw(b_aempty + 8 * acc, ((tile >> 1) & 1) ^ 1, s_abort, a.err, ERR_MMA);
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + acc * 128;
+            for (int kc = 0; kc < nk; ++kc, ++it) {
+                const uint32_t s = it % kStages;
+                tw(b_full + 8 * s, (it / kStages) & 1, s_abort, a.err, ERR_MMA);
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t A = tmem + kTmemA + s * kACols, B = saddr(bst + s * kB16);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_f16(d_tmem, desc_sw128(A + kk * 32), desc_sw128(B + kk * 32), idesc, (kc | kk) != 0);
+                        mma_f16_ta(d_tmem, A + kk * 8, desc_sw128(B + kk * 32), idesc, (kc | kk) != 0);
                     mma_commit(b_empty + 8 * s);
                 }
-                mma_commit(b_afull + 8 * acc);
+                __syncwarp();
             }
-            // every MMA completes before the tensor memory is released
-            if (tile > 0) {
-                int dummy = 0;
-                mbar_wait(b_afull + 8 * ((tile - 1) & 1), ((tile - 1) >> 1) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
-            }
+            if (elect_one()) mma_commit(b_afull + 8 * acc);
+            __syncwarp();
         }
-        __syncwarp();
+        // every MMA completes before the tensor memory is released
+        if (tile > 0) {
+            int dummy = 0;
+            mbar_wait(b_afull + 8 * ((tile - 1) & 1), ((tile - 1) >> 1) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
+        }
+        if (lane == 0) tw.store(2, tw.acc);
     } else {   // epilogue warps 0..3: tensor-memory lanes 32*warp .. 32*warp + 31
         const int row = warp * 32 + lane;
         uint32_t tile = 0;
@@ -354,7 +435,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
             const int off = a.goff[g], m = a.gcnt[g];
             const int N = ((m + 15) >> 4) << 4;
             const uint32_t acc = tile & 1;
-            mbar_wait(b_afull + 8 * acc, (tile >> 1) & 1, s_abort, a.err, ERR_EPI);
+            tw(b_afull + 8 * acc, (tile >> 1) & 1, s_abort, a.err, ERR_EPI);
             tc_fence_after();
             const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + acc * 128;
             for (int c0 = 0; c0 < N; c0 += 16) {
@@ -381,11 +462,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 }
             }
             tc_fence_before();
-            mbar_arrive(b_aempty + 8 * acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_aempty + 8 * acc);
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) tw.store(3, (unsigned long long)(clock64() - t_start));
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -451,21 +534,21 @@ EncodeTiled encoder() {
 
 // rows of packed weights (bytes), one plane per expert record
 bool map_weight_rows(CUtensorMap* tm, const uint8_t* base, size_t row_b, int rows, int recs, size_t rec_b,
-                     uint32_t box_x) {
+                     uint32_t box_x, CUtensorMapSwizzle swz) {
     const cuuint64_t dims[3] = {row_b, (cuuint64_t)rows, (cuuint64_t)recs};
     const cuuint64_t strides[2] = {row_b, rec_b};
     const cuuint32_t box[3] = {box_x, 128, 1};
     const cuuint32_t es[3] = {1, 1, 1};
     return encoder()(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp16 activations [rows][K], 16-row x 64-column boxes with the 128-byte swizzle
-bool map_act(CUtensorMap* tm, void* base, int K, int rows) {
+// fp16 activations [rows][K], `box_rows` x 64-column boxes with the 128-byte swizzle
+bool map_act(CUtensorMap* tm, void* base, int K, int rows, uint32_t box_rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t es[2] = {1, 1};
     return encoder()(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -485,11 +568,15 @@ cudaError_t prefill_kernel_setup(Layer& L) {
     const int H = d.hidden, I = d.inter, recs = d.n_experts + d.n_shared;
     const uint8_t* gu = L.experts;
     const uint8_t* dn = L.experts + gu_block_bytes(H, I);
-    bool ok = map_weight_rows(&L.pf.tm[0], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 32) &&
-              map_weight_rows(&L.pf.tm[1], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 16) &&
-              map_weight_rows(&L.pf.tm[2], dn, row_bytes(I), H, recs, L.rec_bytes, 32) &&
-              map_weight_rows(&L.pf.tm[3], dn, row_bytes(I), H, recs, L.rec_bytes, 16) &&
-              map_act(&L.pf.tm[4], L.pf.xp, H, L.pf.max_rows) && map_act(&L.pf.tm[5], L.pf.hp, I, L.pf.max_rows);
+    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+    bool ok = map_weight_rows(&L.pf.tm[0], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 128, SW) &&
+              map_weight_rows(&L.pf.tm[1], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 16, NS) &&
+              map_weight_rows(&L.pf.tm[2], dn, row_bytes(I), H, recs, L.rec_bytes, 128, SW) &&
+              map_weight_rows(&L.pf.tm[3], dn, row_bytes(I), H, recs, L.rec_bytes, 16, NS) &&
+              true;
+    for (int j = 0; j < 4 && ok; ++j)   // token boxes of 16, 32, 64 and 128 rows
+        ok = map_act(&L.pf.tm[4 + j], L.pf.xp, H, L.pf.max_rows, 16u << j) &&
+             map_act(&L.pf.tm[8 + j], L.pf.hp, I, L.pf.max_rows, 16u << j);
     if (!ok) return cudaErrorInvalidValue;
     L.pf.ready = true;
     return cudaSuccess;
@@ -516,16 +603,20 @@ cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32
                                                                                  static_cast<uint4*>(pf.xp));
     prof_end(L, s);
 
-    GemmArgs gu{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, H, I / 64, 2 * I, pf.hp, I, pf.err};
+    GemmArgs gu{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, H, I / 64, 2 * I, pf.hp, I, pf.err,
+                L.split_trace(3)};
     prof_begin(L, K_PF_GEMM_GU, s);
-    k_pf_gemm<0><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[0], pf.tm[1], pf.tm[4], gu);
+    k_pf_gemm<0><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[0], pf.tm[1], pf.tm[4], pf.tm[5], pf.tm[6],
+                                                             pf.tm[7], gu);
     prof_end(L, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    GemmArgs dn{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, I, (H + 127) / 128, H, pf.yp, H, pf.err};
+    GemmArgs dn{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, I, (H + 127) / 128, H, pf.yp, H, pf.err,
+                L.split_trace(4)};
     prof_begin(L, K_PF_GEMM_DOWN, s);
-    k_pf_gemm<1><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[2], pf.tm[3], pf.tm[5], dn);
+    k_pf_gemm<1><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[2], pf.tm[3], pf.tm[8], pf.tm[9], pf.tm[10],
+                                                             pf.tm[11], dn);
     prof_end(L, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -160,25 +160,33 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
 // ---------------------------------------------------------------------------
 // router for T tokens: split-K tiles (16 tokens x 64 experts), then per-token top-k
 // ---------------------------------------------------------------------------
-constexpr int RT_T = 16, RT_E = 64, RT_K = 64;
+constexpr int RT_T = 32, RT_E = 64, RT_K = 32;
 
+// Tile of 32 tokens x 64 experts over one split's K range, in chunks of 32:
+// x and W are staged transposed (k-major) in shared memory, each thread keeps
+// 2 tokens x 4 experts of fp32 sums, and the next chunk's global loads are in
+// flight while the current chunk is multiplied.
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restrict__ W, const void* __restrict__ x,
                                                             int x_bf16, int T, int H, int E, int splits,
                                                             float* __restrict__ part) {
-    __shared__ float xs[RT_T][RT_K + 1];
-    __shared__ __align__(16) float ws[RT_K][RT_E];
-    const int e0 = blockIdx.x * RT_E, t0 = blockIdx.y * RT_T;
+    __shared__ __align__(16) float xs[RT_K][RT_T + 4];
+    __shared__ __align__(16) float ws[RT_K][RT_E + 4];
+    const int e0 = blockIdx.y * RT_E, t0 = blockIdx.x * RT_T;
     const int Ls = H / splits, kb = blockIdx.z * Ls;
-    const int tid = threadIdx.x, tt = tid >> 4, te = (tid & 15) * 4;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int kc = kb; kc < kb + Ls; kc += RT_K) {
-        for (int i = tid; i < RT_T * RT_K; i += kThreads) {
-            const int r = i / RT_K, c = i % RT_K;
-            xs[r][c] = (t0 + r < T) ? load_act(x, x_bf16, (size_t)(t0 + r) * H + kc + c) : 0.f;
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int c = tid & 31, r0 = tid >> 5;   // staging: k within the chunk, first row
+    float acc[2][4] = {};
+    float vx[RT_T * RT_K / kThreads], vw[RT_E * RT_K / kThreads];
+    auto load = [&](int kc) {
+#pragma unroll
+        for (int j = 0; j < RT_T * RT_K / kThreads; ++j) {
+            const int r = r0 + 8 * j;
+            vx[j] = (t0 + r < T) ? load_act(x, x_bf16, (size_t)(t0 + r) * H + kc + c) : 0.f;
         }
-        for (int i = tid; i < RT_E * RT_K; i += kThreads) {
-            const int r = i / RT_K, c = i % RT_K;  // r: expert in tile, c: k in chunk
+#pragma unroll
+        for (int j = 0; j < RT_E * RT_K / kThreads; ++j) {
+            const int r = r0 + 8 * j;
             float w = 0.f;
             if (e0 + r < E) {
                 if (!Q8) {
@@ -188,27 +196,43 @@ __global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restri
                     const uint32_t m = __ldg(reinterpret_cast<const uint32_t*>(base + (size_t)E * H) +
                                              (size_t)(e0 + r) * (H / 64) + (kc / 64));
                     const float2 sb = meta_to_f2(m);
-                    w = fmaf((float)base[(size_t)(e0 + r) * H + kc + c], sb.x, sb.y);
+                    w = fmaf((float)__ldg(base + (size_t)(e0 + r) * H + kc + c), sb.x, sb.y);
                 }
             }
-            ws[c][r] = w;
+            vw[j] = w;
         }
+    };
+    load(kb);
+    for (int kc = kb; kc < kb + Ls; kc += RT_K) {
+        __syncthreads();   // the previous chunk's reads of xs / ws are done
+#pragma unroll
+        for (int j = 0; j < RT_T * RT_K / kThreads; ++j) xs[c][r0 + 8 * j] = vx[j];
+#pragma unroll
+        for (int j = 0; j < RT_E * RT_K / kThreads; ++j) ws[c][r0 + 8 * j] = vw[j];
         __syncthreads();
+        if (kc + RT_K < kb + Ls) load(kc + RT_K);
 #pragma unroll 8
-        for (int c = 0; c < RT_K; ++c) {
-            const float a = xs[tt][c];
-            const float4 w4 = *reinterpret_cast<const float4*>(&ws[c][te]);
-            acc[0] = fmaf(a, w4.x, acc[0]);
-            acc[1] = fmaf(a, w4.y, acc[1]);
-            acc[2] = fmaf(a, w4.z, acc[2]);
-            acc[3] = fmaf(a, w4.w, acc[3]);
+        for (int q = 0; q < RT_K; ++q) {
+            const float2 a = *reinterpret_cast<const float2*>(&xs[q][2 * ty]);
+            const float4 w4 = *reinterpret_cast<const float4*>(&ws[q][4 * tx]);
+            acc[0][0] = fmaf(a.x, w4.x, acc[0][0]);
+            acc[0][1] = fmaf(a.x, w4.y, acc[0][1]);
+            acc[0][2] = fmaf(a.x, w4.z, acc[0][2]);
+            acc[0][3] = fmaf(a.x, w4.w, acc[0][3]);
+            acc[1][0] = fmaf(a.y, w4.x, acc[1][0]);
+            acc[1][1] = fmaf(a.y, w4.y, acc[1][1]);
+            acc[1][2] = fmaf(a.y, w4.z, acc[1][2]);
+            acc[1][3] = fmaf(a.y, w4.w, acc[1][3]);
         }
-        __syncthreads();
     }
-    const int t = t0 + tt;
-    if (t < T)
-        for (int j = 0; j < 4; ++j)
-            if (e0 + te + j < E) part[((size_t)blockIdx.z * T + t) * E + e0 + te + j] = acc[j];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int t = t0 + 2 * ty + i;
+        if (t < T)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e0 + 4 * tx + j < E) part[((size_t)blockIdx.z * T + t) * E + e0 + 4 * tx + j] = acc[i][j];
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restrict__ part, int splits, int T, int E,
@@ -287,7 +311,7 @@ cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) 
     const auto& d = L.d;
     const int xb = d.act_dtype == MOE_BF16;
     const int splits = L.router_splits;
-    dim3 grid((d.n_experts + RT_E - 1) / RT_E, (T + RT_T - 1) / RT_T, splits);
+    dim3 grid((T + RT_T - 1) / RT_T, (d.n_experts + RT_E - 1) / RT_E, splits);
     if ((d.hidden / splits) % RT_K) return cudaErrorInvalidValue;
     prof_begin(L, K_ROUTER_TOKENS, s);
     if (d.router_fmt == MOE_W_F32)
