@@ -161,6 +161,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     L.device = device;
     L.rec_bytes = record_bytes(d.hidden, d.inter);
     L.router_splits = pick_router_splits(d.hidden);
+    L.router_splits_tok = ((d.hidden / 64) % 16 == 0) ? 16 : L.router_splits;
     cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, device);
 
     const int E = d.n_experts, H = d.hidden, I = d.inter, k = d.top_k, T = d.max_tokens;
@@ -168,7 +169,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
 
     // scratch block layout
     Alloc sc;
-    size_t o_part = sc.add((size_t)L.router_splits * E * 4 * std::max(1, T));
+    size_t o_part = sc.add((size_t)std::max(L.router_splits, L.router_splits_tok) * E * 4 * std::max(1, T));
     size_t o_logits = sc.add((size_t)T * E * 4);
     size_t o_ids = sc.add((size_t)T * k * 4);
     size_t o_w = sc.add((size_t)T * k * 4);

@@ -123,13 +123,14 @@ struct Layer {
     const uint8_t** rec_table = nullptr;  // device [E + 1] record pointer per expert
 
     // decode scratch
-    float* logits_part = nullptr;   // [router_splits][E]
+    float* logits_part = nullptr;   // [max(router_splits, router_splits_tok)][max_tokens][E]
     float* logits = nullptr;        // [max_tokens][E]
     int32_t* ids = nullptr;         // [max_tokens][k]
     float* wts = nullptr;           // [max_tokens][k]
     float* h = nullptr;             // [k + 1][I]
     unsigned* counters = nullptr;   // [8] last-block counters, kept at zero between launches
-    int router_splits = 1;
+    int router_splits = 1;       // split-K of the one-token router
+    int router_splits_tok = 1;   // split-K of the multi-token router (<= 16)
 
     PrefillScratch pf;
     CacheState* cache = nullptr;

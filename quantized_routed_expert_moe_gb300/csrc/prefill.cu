@@ -41,19 +41,23 @@ __global__ void __launch_bounds__(kPermThreads) k_pf_permute(const int32_t* __re
                                                              int32_t* __restrict__ perm_token,
                                                              int32_t* __restrict__ pos) {
     __shared__ int s_cnt[1024];
-    __shared__ int s_e[1024];
     __shared__ int s_start[1024];
     __shared__ int s_gidx[1024];
+    __shared__ uint32_t s_bits[1024][MOE_MAX_CHUNK / 32];   // [expert][token bit]: token selected the expert
     __shared__ int s_wa[32], s_wb[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = T * k;   // <= 1024
     s_cnt[tid] = 0;
+#pragma unroll
+    for (int q = 0; q < MOE_MAX_CHUNK / 32; ++q) s_bits[tid][q] = 0u;
     __syncthreads();
+    int my_e = 0;
     if (tid < P) {
-        int e = ids[tid];
-        if ((unsigned)e >= (unsigned)E) e = 0;   // a valid selection never needs this
-        s_e[tid] = e;
-        atomicAdd(&s_cnt[e], 1);
+        my_e = ids[tid];
+        if ((unsigned)my_e >= (unsigned)E) my_e = 0;   // a valid selection never needs this
+        const int t = tid / k;
+        atomicAdd(&s_cnt[my_e], 1);
+        atomicOr(&s_bits[my_e][t >> 5], 1u << (t & 31));
     }
     __syncthreads();
     // exclusive scans over experts (thread e): row starts, and group index of
@@ -88,12 +92,18 @@ __global__ void __launch_bounds__(kPermThreads) k_pf_permute(const int32_t* __re
     }
     __syncthreads();
     if (tid < P) {
-        // stable: the rank among earlier pairs with the same expert
-        const int e = s_e[tid];
-        int r = 0;
-        for (int q = 0; q < tid; ++q) r += (s_e[q] == e);
-        const int row = s_start[e] + r;
+        // stable: a token selects an expert at most once, so the rank among
+        // earlier pairs with the same expert is the number of earlier tokens
+        // that selected it (bits below t in the expert's token mask)
+        const int e = my_e;
         const int t = tid / k, j = tid - t * k;
+        int r = 0;
+#pragma unroll
+        for (int q = 0; q < MOE_MAX_CHUNK / 32; ++q) {
+            const uint32_t m = s_bits[e][q];
+            r += (q < (t >> 5)) ? __popc(m) : (q == (t >> 5)) ? __popc(m & ((1u << (t & 31)) - 1u)) : 0;
+        }
+        const int row = s_start[e] + r;
         perm_token[row] = t;
         pos[t * (k + 1) + j] = row;
     }

@@ -160,33 +160,36 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
 // ---------------------------------------------------------------------------
 // router for T tokens: split-K tiles (16 tokens x 64 experts), then per-token top-k
 // ---------------------------------------------------------------------------
-constexpr int RT_T = 32, RT_E = 64, RT_K = 32;
+constexpr int RT_T = 32, RT_E = 128, RT_K = 32;
 
-// Tile of 32 tokens x 64 experts over one split's K range, in chunks of 32:
-// x and W are staged transposed (k-major) in shared memory, each thread keeps
-// 2 tokens x 4 experts of fp32 sums, and the next chunk's global loads are in
-// flight while the current chunk is multiplied.
+// Tile of 32 tokens x 128 experts over one split's K range, in chunks of 32:
+// x and W are staged transposed (k-major) in shared memory; thread (ty, tx)
+// keeps the fp32 sums of tokens 4ty..4ty+3 x experts 4tx..4tx+3 (the four x
+// values are one broadcast read per warp), and the next chunk's global loads
+// are in flight while the current chunk is multiplied.
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restrict__ W, const void* __restrict__ x,
                                                             int x_bf16, int T, int H, int E, int splits,
                                                             float* __restrict__ part) {
+    constexpr int NX = RT_T * RT_K / kThreads, NW = RT_E * RT_K / kThreads;   // 4, 16
     __shared__ __align__(16) float xs[RT_K][RT_T + 4];
     __shared__ __align__(16) float ws[RT_K][RT_E + 4];
     const int e0 = blockIdx.y * RT_E, t0 = blockIdx.x * RT_T;
     const int Ls = H / splits, kb = blockIdx.z * Ls;
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int c = tid & 31, r0 = tid >> 5;   // staging: k within the chunk, first row
-    float acc[2][4] = {};
-    float vx[RT_T * RT_K / kThreads], vw[RT_E * RT_K / kThreads];
+    const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;
+    const int c = tid & (RT_K - 1), r0 = tid / RT_K;   // staging: k within the chunk, first row
+    constexpr int RS = kThreads / RT_K;                 // rows per staging pass (8)
+    float acc[4][4] = {};
+    float vx[NX], vw[NW];
     auto load = [&](int kc) {
 #pragma unroll
-        for (int j = 0; j < RT_T * RT_K / kThreads; ++j) {
-            const int r = r0 + 8 * j;
+        for (int j = 0; j < NX; ++j) {
+            const int r = r0 + RS * j;
             vx[j] = (t0 + r < T) ? load_act(x, x_bf16, (size_t)(t0 + r) * H + kc + c) : 0.f;
         }
 #pragma unroll
-        for (int j = 0; j < RT_E * RT_K / kThreads; ++j) {
-            const int r = r0 + 8 * j;
+        for (int j = 0; j < NW; ++j) {
+            const int r = r0 + RS * j;
             float w = 0.f;
             if (e0 + r < E) {
                 if (!Q8) {
@@ -206,28 +209,25 @@ __global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restri
     for (int kc = kb; kc < kb + Ls; kc += RT_K) {
         __syncthreads();   // the previous chunk's reads of xs / ws are done
 #pragma unroll
-        for (int j = 0; j < RT_T * RT_K / kThreads; ++j) xs[c][r0 + 8 * j] = vx[j];
+        for (int j = 0; j < NX; ++j) xs[c][r0 + RS * j] = vx[j];
 #pragma unroll
-        for (int j = 0; j < RT_E * RT_K / kThreads; ++j) ws[c][r0 + 8 * j] = vw[j];
+        for (int j = 0; j < NW; ++j) ws[c][r0 + RS * j] = vw[j];
         __syncthreads();
         if (kc + RT_K < kb + Ls) load(kc + RT_K);
 #pragma unroll 8
         for (int q = 0; q < RT_K; ++q) {
-            const float2 a = *reinterpret_cast<const float2*>(&xs[q][2 * ty]);
+            const float4 a = *reinterpret_cast<const float4*>(&xs[q][4 * ty]);
             const float4 w4 = *reinterpret_cast<const float4*>(&ws[q][4 * tx]);
-            acc[0][0] = fmaf(a.x, w4.x, acc[0][0]);
-            acc[0][1] = fmaf(a.x, w4.y, acc[0][1]);
-            acc[0][2] = fmaf(a.x, w4.z, acc[0][2]);
-            acc[0][3] = fmaf(a.x, w4.w, acc[0][3]);
-            acc[1][0] = fmaf(a.y, w4.x, acc[1][0]);
-            acc[1][1] = fmaf(a.y, w4.y, acc[1][1]);
-            acc[1][2] = fmaf(a.y, w4.z, acc[1][2]);
-            acc[1][3] = fmaf(a.y, w4.w, acc[1][3]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
         }
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int t = t0 + 2 * ty + i;
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + 4 * ty + i;
         if (t < T)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -241,12 +241,12 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
     extern __shared__ float sl[];
     const int t = blockIdx.x;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float v[8];
+        float v[16];
 #pragma unroll
-        for (int s = 0; s < 8; ++s) v[s] = (s < splits) ? part[((size_t)s * T + t) * E + e] : 0.f;   // splits <= 8
+        for (int s = 0; s < 16; ++s) v[s] = (s < splits) ? __ldcg(part + ((size_t)s * T + t) * E + e) : 0.f;   // splits <= 16
         float l = 0.f;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) l += v[s];
+        for (int s = 0; s < 16; ++s) l += v[s];
         if (bias) l += bias[e];
         sl[e] = l;
         logits[(size_t)t * E + e] = l;
@@ -310,7 +310,7 @@ cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, c
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) {
     const auto& d = L.d;
     const int xb = d.act_dtype == MOE_BF16;
-    const int splits = L.router_splits;
+    const int splits = L.router_splits_tok;
     dim3 grid((T + RT_T - 1) / RT_T, (d.n_experts + RT_E - 1) / RT_E, splits);
     if ((d.hidden / splits) % RT_K) return cudaErrorInvalidValue;
     prof_begin(L, K_ROUTER_TOKENS, s);
