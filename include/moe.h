@@ -251,6 +251,19 @@ moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out);
  * -1 for an empty slot. */
 moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert);
 
+/* The cache policy alone, on the host (no device, no layer): runs n_tokens
+ * tokens of k distinct expert ids each (ids: host int32 [n_tokens][k], values
+ * in 0..n_experts-1) through an empty `slots`-slot cache exactly as a streamed
+ * layer's moe_cache_stage does, and writes per (token, slot j): hit[t][j] = 1
+ * if the expert was resident before the token, and slot[t][j] = the slot that
+ * holds it afterwards. Policy (TurboFieldfare article, "token generation",
+ * with the readings the pages leave open): counts start at 1 on admission and
+ * grow by one per use, the victim is the least-used resident the token does
+ * not need (ties: least recently used, then lower id), a miss takes the lowest
+ * free slot while there is one, hits are counted before misses. */
+moe_status moe_lfu_trace(int32_t slots, int32_t n_experts, int32_t k, int32_t n_tokens, const int32_t* ids,
+                         int32_t* slot, uint8_t* hit);
+
 /* ---- options and health ----------------------------------------------------------- */
 
 /* Decode implementations (MOE_OPT_DECODE_PATH):
@@ -272,7 +285,16 @@ enum {
     /* Phase tracing of the fused decode: while nonzero, every CTA records the
      * GPU global timer (ns) at MOE_TRACE_POINTS phase boundaries of the last
      * launch; read them with moe_trace_read. Costs a few stores per CTA. */
-    MOE_OPT_TRACE = 3
+    MOE_OPT_TRACE = 3,
+    /* Deadline of every host-side wait of a streamed layer (expert ids coming
+     * back, staging and table buffers free for reuse), in milliseconds
+     * (default 30000); a wait that passes it returns MOE_E_TIMEOUT. */
+    MOE_OPT_HOST_TIMEOUT_MS = 4,
+    /* Test hook for failure detection on streamed layers: while nonzero, each
+     * stage first holds the layer's copy stream for this many milliseconds (a
+     * host callback that sleeps), so that a short MOE_OPT_HOST_TIMEOUT_MS runs
+     * out on the host. No device work is involved. */
+    MOE_OPT_TEST_STALL_COPIES_MS = 5
 };
 
 /* Trace points recorded per CTA (in this order): kernel start, activations

@@ -27,13 +27,14 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
-           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency",
+           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency", "moe_lfu_trace",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
 MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
 MOE_STATIC_SCRATCH_BYTES = 256 * 1024
 MOE_OPT_DECODE_PATH, MOE_OPT_TEST_STALL_ROUTING, MOE_OPT_TRACE = 1, 2, 3
+MOE_OPT_HOST_TIMEOUT_MS, MOE_OPT_TEST_STALL_COPIES_MS = 4, 5
 MOE_TRACE_POINTS = 10
 TRACE_NAMES = ("start", "x_staged", "router_done", "ids_published", "ids_seen", "gateup_done",
                "h_visible", "h_staged", "down_done", "exit")
@@ -119,6 +120,8 @@ def lib() -> ctypes.CDLL:
             L.moe_cache_stats.argtypes = [vp, ctypes.POINTER(moe_cache_stats_t)]
             L.moe_cache_residency.restype = st
             L.moe_cache_residency.argtypes = [vp, vp]
+            L.moe_lfu_trace.restype = st
+            L.moe_lfu_trace.argtypes = [i32, i32, i32, i32, vp, vp, vp]
             L.moe_profile_start.restype = st
             L.moe_profile_start.argtypes = [vp, i32]
             L.moe_profile_stop.restype = st
@@ -280,6 +283,18 @@ def moe_cache_stats(handle) -> dict:
     return {f: int(getattr(s, f)) for f, _ in moe_cache_stats_t._fields_}
 
 
+def moe_lfu_trace(slots: int, n_experts: int, ids):
+    """Host-only run of the cache policy: ids int32 [n_tokens][k] -> (slot, hit) arrays."""
+    import numpy as _np
+    ids = _np.ascontiguousarray(ids, dtype=_np.int32)
+    n_tokens, k = ids.shape
+    slot = _np.empty((n_tokens, k), _np.int32)
+    hit = _np.empty((n_tokens, k), _np.uint8)
+    _check(lib().moe_lfu_trace(slots, n_experts, k, n_tokens, ids.ctypes.data, slot.ctypes.data, hit.ctypes.data),
+           "moe_lfu_trace")
+    return slot, hit
+
+
 def moe_cache_residency(handle, slots: int) -> list[int]:
     arr = (ctypes.c_int32 * slots)()
     _check(lib().moe_cache_residency(handle, ctypes.cast(arr, ctypes.c_void_p)), "moe_cache_residency")
@@ -390,6 +405,9 @@ class MoELayer:
 
     def cache_stats(self):
         return moe_cache_stats(self.handle)
+
+    def residency(self):
+        return moe_cache_residency(self.handle, self.desc.cache_slots)
 
     def set_option(self, option, value):
         moe_layer_set_option(self.handle, option, value)

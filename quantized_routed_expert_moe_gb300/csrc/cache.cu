@@ -1,31 +1,359 @@
-// Streamed expert cache (per-layer LFU slots filled from host records).
+// Streamed expert cache: per-layer device slots holding the records of the
+// experts used recently, managed least-frequently-used and filled from host
+// memory by cudaMemcpyAsync on the layer's own copy stream.
+//
+// TurboFieldfare article ("token generation"): the router's expert IDs are
+// matched against a per-layer 16-slot LFU cache and the misses are loaded,
+// overlapped with the always-resident shared expert's compute. Inferno README
+// ("Memory Strategy") keeps hot experts resident and streams the rest.
+//
+// Policy (the pages leave the details open; this is the reading the oracle's
+// LFU simulation follows):
+//   * an expert's count starts at 1 when it is admitted and grows by 1 on every
+//     use while resident; the count is dropped on eviction;
+//   * the victim is the resident expert with the smallest count that the
+//     current token does not need; ties go to the least recently used, then to
+//     the lower expert id;
+//   * a token's IDs are processed in selection order, hits before misses, and
+//     a miss takes the lowest free slot while there is one.
+#include <chrono>
+#include <cstring>
+#include <thread>
+#include <vector>
+
 #include "moe_internal.h"
 
 namespace moe {
 
-struct CacheState {};
+// ---------------------------------------------------------------------------
+// LFU policy (host)
+// ---------------------------------------------------------------------------
 
-moe_status cache_create(Layer&, const void* const*, moe_expert_source, void*) {
-    return fail(MOE_E_UNSUPPORTED, "streamed mode is not built yet");
+struct Fill {
+    int expert, slot, victim;
+};
+
+class Lfu {
+public:
+    Lfu(int slots, int E) : slots_(slots), slot_of_(E, -1), expert_in_(slots, -1), count_(E, 0), last_(E, 0) {}
+
+    // One token's IDs (distinct, at most `slots`): updates the counts and
+    // returns the fills (expert, slot, evicted expert or -1) in admission order.
+    void access(const int32_t* ids, int n, int* hits, std::vector<Fill>& fills) {
+        ++clock_;
+        fills.clear();
+        int h = 0;
+        for (int i = 0; i < n; ++i) {
+            const int e = ids[i];
+            if (slot_of_[e] >= 0) {
+                ++h;
+                ++count_[e];
+                last_[e] = clock_;
+            }
+        }
+        for (int i = 0; i < n; ++i) {
+            const int e = ids[i];
+            if (slot_of_[e] >= 0) continue;
+            int slot = -1, victim = -1;
+            for (int s = 0; s < slots_; ++s)
+                if (expert_in_[s] < 0) { slot = s; break; }
+            if (slot < 0) {
+                for (int s = 0; s < slots_; ++s) {
+                    const int r = expert_in_[s];
+                    bool needed = false;
+                    for (int j = 0; j < n; ++j) needed |= (ids[j] == r);
+                    if (needed) continue;
+                    if (victim < 0 || count_[r] < count_[victim] ||
+                        (count_[r] == count_[victim] &&
+                         (last_[r] < last_[victim] || (last_[r] == last_[victim] && r < victim))))
+                        victim = r;
+                }
+                slot = slot_of_[victim];
+                drop(victim);
+            }
+            slot_of_[e] = slot;
+            expert_in_[slot] = e;
+            count_[e] = 1;
+            last_[e] = clock_;
+            fills.push_back({e, slot, victim});
+        }
+        *hits = h;
+    }
+
+    // Forget a resident expert (eviction, or a fill that failed).
+    void drop(int e) {
+        if (slot_of_[e] < 0) return;
+        expert_in_[slot_of_[e]] = -1;
+        slot_of_[e] = -1;
+        count_[e] = 0;
+        last_[e] = 0;
+    }
+
+    int slot_of(int e) const { return slot_of_[e]; }
+    int expert_in(int s) const { return expert_in_[s]; }
+
+private:
+    int slots_;
+    uint64_t clock_ = 0;
+    std::vector<int> slot_of_, expert_in_;
+    std::vector<uint64_t> count_, last_;
+};
+
+// ---------------------------------------------------------------------------
+// cache state
+// ---------------------------------------------------------------------------
+
+struct CacheState {
+    int slots = 0;
+    uint8_t* dev_slots = nullptr;             // [slots][rec_bytes]
+    Lfu lfu{1, 1};
+    const void* const* records = nullptr;     // borrowed host records, or null
+    std::vector<const void*> records_copy;    // the caller's pointer array, copied
+    moe_expert_source src = nullptr;
+    void* user = nullptr;
+    uint8_t* staging[2] = {nullptr, nullptr}; // pinned, for the source path
+    cudaEvent_t staging_ev[2] = {nullptr, nullptr};
+    int staging_idx = 0;
+    const uint8_t** tab_pinned[2] = {nullptr, nullptr};   // record table upload buffers
+    cudaEvent_t tab_ev[2] = {nullptr, nullptr};
+    int tab_idx = 0;
+    std::vector<const uint8_t*> table;        // host copy of the device record table [E + 1]
+    int32_t* ids_host = nullptr;              // pinned [top_k]
+    cudaEvent_t ids_ready = nullptr, stream_mark = nullptr, copies_done = nullptr;
+    cudaStream_t copy = nullptr;
+    moe_cache_stats_t stats{};
+    std::vector<Fill> fills;
+};
+
+namespace {
+
+using clk = std::chrono::steady_clock;
+
+// Host wait for `ev` with the layer's deadline (MOE_OPT_HOST_TIMEOUT_MS).
+moe_status wait_event(const Layer& L, cudaEvent_t ev, const char* what) {
+    const auto t0 = clk::now();
+    for (;;) {
+        const cudaError_t e = cudaEventQuery(ev);
+        if (e == cudaSuccess) return MOE_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(e, what);
+        if (clk::now() - t0 > std::chrono::milliseconds(L.host_timeout_ms))
+            return fail(MOE_E_TIMEOUT, std::string(what) + ": host wait passed its deadline");
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
 }
-void cache_destroy(Layer& L) { delete L.cache; L.cache = nullptr; }
-moe_status cache_stage(Layer&, const int32_t*, int, cudaStream_t, int*, int*) {
-    return fail(MOE_E_UNSUPPORTED, "streamed mode is not built yet");
+
+void CUDART_CB sleep_host(void* ms) {
+    std::this_thread::sleep_for(std::chrono::milliseconds((intptr_t)ms));
 }
-moe_status cache_decode(Layer&, const void*, void*, float*, cudaStream_t) {
-    return fail(MOE_E_UNSUPPORTED, "streamed mode is not built yet");
+
+}  // namespace
+
+moe_status cache_create(Layer& L, const void* const* records, moe_expert_source src, void* user) {
+    const auto& d = L.d;
+    CacheState* C = new (std::nothrow) CacheState();
+    if (!C) return fail(MOE_E_NOMEM, "host allocation failed");
+    L.cache = C;
+    C->slots = d.cache_slots;
+    C->lfu = Lfu(d.cache_slots, d.n_experts);
+    if (records) {
+        C->records_copy.assign(records, records + d.n_experts);
+        for (int e = 0; e < d.n_experts; ++e)
+            if (!C->records_copy[e]) return fail(MOE_E_INVALID, "records[" + std::to_string(e) + "] is NULL");
+        C->records = C->records_copy.data();
+    }
+    C->src = src;
+    C->user = user;
+    const size_t rb = L.rec_bytes;
+    MOE_CUDA_TRY(cudaMalloc(&C->dev_slots, (size_t)C->slots * rb));
+    L.device_bytes += (size_t)C->slots * rb;
+    MOE_CUDA_TRY(cudaStreamCreateWithFlags(&C->copy, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+        MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->tab_ev[i], cudaEventDisableTiming));
+        MOE_CUDA_TRY(cudaHostAlloc(&C->tab_pinned[i], (size_t)(d.n_experts + 1) * sizeof(void*), cudaHostAllocDefault));
+        if (!records) {
+            MOE_CUDA_TRY(cudaHostAlloc(&C->staging[i], rb, cudaHostAllocDefault));
+            MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->staging_ev[i], cudaEventDisableTiming));
+        }
+    }
+    MOE_CUDA_TRY(cudaHostAlloc(&C->ids_host, (size_t)d.top_k * 4, cudaHostAllocDefault));
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->ids_ready, cudaEventDisableTiming));
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->stream_mark, cudaEventDisableTiming));
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->copies_done, cudaEventDisableTiming));
+    // the record table as create left it: no routed expert resident, the
+    // shared expert (index E) in device memory
+    C->table.assign(d.n_experts + 1, nullptr);
+    MOE_CUDA_TRY(cudaMemcpy(C->table.data(), L.rec_table, C->table.size() * sizeof(void*), cudaMemcpyDeviceToHost));
+    for (int e = 0; e < d.n_experts; ++e) C->table[e] = nullptr;
+    return MOE_OK;
+}
+
+void cache_destroy(Layer& L) {
+    CacheState* C = L.cache;
+    if (!C) return;
+    if (C->copy) cudaStreamSynchronize(C->copy);
+    for (int i = 0; i < 2; ++i) {
+        if (C->staging[i]) cudaFreeHost(C->staging[i]);
+        if (C->staging_ev[i]) cudaEventDestroy(C->staging_ev[i]);
+        if (C->tab_pinned[i]) cudaFreeHost(C->tab_pinned[i]);
+        if (C->tab_ev[i]) cudaEventDestroy(C->tab_ev[i]);
+    }
+    if (C->ids_host) cudaFreeHost(C->ids_host);
+    if (C->ids_ready) cudaEventDestroy(C->ids_ready);
+    if (C->stream_mark) cudaEventDestroy(C->stream_mark);
+    if (C->copies_done) cudaEventDestroy(C->copies_done);
+    if (C->copy) cudaStreamDestroy(C->copy);
+    if (C->dev_slots) cudaFree(C->dev_slots);
+    delete C;
+    L.cache = nullptr;
+}
+
+moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int* hits, int* misses) {
+    CacheState& C = *L.cache;
+    const auto& d = L.d;
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= d.n_experts) return fail(MOE_E_INVALID, "expert id out of range");
+        for (int j = 0; j < i; ++j)
+            if (ids[j] == ids[i]) return fail(MOE_E_INVALID, "repeated expert id");
+    }
+    const auto t0 = clk::now();
+    const size_t rb = L.rec_bytes;
+    // the record-table upload buffer used now must be free before anything
+    // changes, so that a timeout leaves the cache as it was
+    {
+        const moe_status sw = wait_event(L, C.tab_ev[C.tab_idx], "record table buffer reuse");
+        if (sw != MOE_OK) return sw;
+    }
+    // work already queued on `s` may still read the slots that are about to be refilled
+    MOE_CUDA_TRY(cudaEventRecord(C.stream_mark, s));
+    MOE_CUDA_TRY(cudaStreamWaitEvent(C.copy, C.stream_mark, 0));
+    if (L.test_stall_copies_ms > 0)
+        MOE_CUDA_TRY(cudaLaunchHostFunc(C.copy, sleep_host, (void*)(intptr_t)L.test_stall_copies_ms));
+    int h = 0;
+    C.lfu.access(ids, n, &h, C.fills);
+    moe_status st = MOE_OK;
+    int filled = 0;
+    for (const Fill& f : C.fills) {
+        uint8_t* dst = C.dev_slots + (size_t)f.slot * rb;
+        if (f.victim >= 0) C.table[f.victim] = nullptr;
+        C.table[f.expert] = nullptr;
+        if (st != MOE_OK) {   // an earlier fill of this token failed: admit nothing more
+            C.lfu.drop(f.expert);
+            continue;
+        }
+        const void* src = nullptr;
+        if (C.records) {
+            src = C.records[f.expert];
+        } else {
+            const int b = C.staging_idx;
+            st = wait_event(L, C.staging_ev[b], "staging buffer reuse");
+            if (st == MOE_OK && C.src(C.user, f.expert, C.staging[b], rb) != 0)
+                st = fail(MOE_E_SOURCE, "expert source failed for expert " + std::to_string(f.expert));
+            if (st != MOE_OK) {
+                C.lfu.drop(f.expert);
+                continue;
+            }
+            src = C.staging[b];
+            C.staging_idx ^= 1;
+        }
+        const cudaError_t ce = cudaMemcpyAsync(dst, src, rb, cudaMemcpyHostToDevice, C.copy);
+        if (ce != cudaSuccess) {
+            st = cuda_fail(ce, "expert fill copy");
+            C.lfu.drop(f.expert);
+            continue;
+        }
+        if (!C.records) MOE_CUDA_TRY(cudaEventRecord(C.staging_ev[C.staging_idx ^ 1], C.copy));
+        C.table[f.expert] = dst;
+        C.stats.bytes_h2d += rb;
+        ++filled;
+    }
+    // publish the record table (double-buffered pinned upload)
+    {
+        const int b = C.tab_idx;   // free: waited for above
+        std::memcpy(C.tab_pinned[b], C.table.data(), C.table.size() * sizeof(void*));
+        MOE_CUDA_TRY(cudaMemcpyAsync(L.rec_table, C.tab_pinned[b], C.table.size() * sizeof(void*),
+                                     cudaMemcpyHostToDevice, C.copy));
+        MOE_CUDA_TRY(cudaEventRecord(C.tab_ev[b], C.copy));
+        C.tab_idx ^= 1;
+    }
+    MOE_CUDA_TRY(cudaEventRecord(C.copies_done, C.copy));
+    MOE_CUDA_TRY(cudaStreamWaitEvent(s, C.copies_done, 0));
+    C.stats.tokens += 1;
+    C.stats.hits += (uint64_t)h;
+    C.stats.misses += (uint64_t)C.fills.size();
+    C.stats.stage_ns += (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(clk::now() - t0).count();
+    if (hits) *hits = h;
+    if (misses) *misses = (int)C.fills.size();
+    (void)filled;
+    return st;
+}
+
+moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s) {
+    CacheState& C = *L.cache;
+    const auto& d = L.d;
+    const int k = d.top_k;
+    // router + selection (ids, weights on the device)
+    cudaError_t e = launch_route_decode(L, x, s, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "router launch");
+    // the shared expert's gate/up runs while the host stages the routed experts
+    if (d.n_shared) {
+        e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, 1, false, s);
+        if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
+    }
+    MOE_CUDA_TRY(cudaMemcpyAsync(C.ids_host, L.ids, (size_t)k * 4, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaEventRecord(C.ids_ready, s));
+    moe_status st = wait_event(L, C.ids_ready, "expert ids");
+    if (st != MOE_OK) return st;
+    int h = 0, m = 0;
+    st = cache_stage(L, C.ids_host, k, s, &h, &m);
+    if (st != MOE_OK) return st;
+    for (int j = 0; j < k; ++j)
+        if (C.lfu.slot_of(C.ids_host[j]) < 0)
+            return fail(MOE_E_STATE, "expert " + std::to_string(C.ids_host[j]) + " is not resident");
+    const int jj0 = d.n_shared ? 1 : 0;
+    e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, jj0, jj0 + k, true, s);
+    if (e != cudaSuccess) return cuda_fail(e, "routed expert launch");
+    return MOE_OK;
 }
 
 }  // namespace moe
 
 extern "C" {
+
 moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out) {
     if (!layer || !out) return moe::fail(MOE_E_INVALID, "NULL argument");
-    *out = moe_cache_stats_t{};
+    if (!layer->L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed");
+    *out = layer->L.cache->stats;
     return MOE_OK;
 }
-moe_status moe_cache_residency(const moe_layer* layer, int32_t*) {
-    if (!layer) return moe::fail(MOE_E_INVALID, "NULL argument");
-    return moe::fail(MOE_E_STATE, "layer is not streamed");
+
+moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert) {
+    if (!layer || !slot_expert) return moe::fail(MOE_E_INVALID, "NULL argument");
+    if (!layer->L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed");
+    const moe::CacheState& C = *layer->L.cache;
+    for (int s = 0; s < C.slots; ++s) slot_expert[s] = C.lfu.expert_in(s);
+    return MOE_OK;
 }
+
+moe_status moe_lfu_trace(int32_t slots, int32_t n_experts, int32_t k, int32_t n_tokens, const int32_t* ids,
+                         int32_t* slot, uint8_t* hit) {
+    if (!ids || !slot || !hit) return moe::fail(MOE_E_INVALID, "NULL argument");
+    if (slots < 1 || n_experts < 1 || k < 1 || k > slots || n_tokens < 0)
+        return moe::fail(MOE_E_INVALID, "need 1 <= k <= slots, n_experts >= 1, n_tokens >= 0");
+    moe::Lfu lfu(slots, n_experts);
+    std::vector<moe::Fill> fills;
+    for (int t = 0; t < n_tokens; ++t) {
+        const int32_t* row = ids + (size_t)t * k;
+        for (int i = 0; i < k; ++i) {
+            if (row[i] < 0 || row[i] >= n_experts) return moe::fail(MOE_E_INVALID, "expert id out of range");
+            for (int j = 0; j < i; ++j)
+                if (row[j] == row[i]) return moe::fail(MOE_E_INVALID, "repeated expert id");
+        }
+        for (int i = 0; i < k; ++i) hit[(size_t)t * k + i] = lfu.slot_of(row[i]) >= 0 ? 1 : 0;
+        int h = 0;
+        lfu.access(row, k, &h, fills);
+        for (int i = 0; i < k; ++i) slot[(size_t)t * k + i] = lfu.slot_of(row[i]);
+    }
+    return MOE_OK;
 }
+
+}  // extern "C"

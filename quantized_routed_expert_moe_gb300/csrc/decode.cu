@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) k_gateup(const uint8_t* const* __res
                                                      float* __restrict__ h, size_t rbH,
                                                      int32_t* __restrict__ ids_out, float* __restrict__ wts_out,
                                                      float* __restrict__ logits_out,
+                                                     const int32_t* __restrict__ sel_ids, int jj0, int jj1,
                                                      unsigned long long* __restrict__ tr) {
     extern __shared__ uint4 smq[];
     __shared__ float s_logit[1024];
@@ -98,17 +99,26 @@ __global__ void __launch_bounds__(kThreads) k_gateup(const uint8_t* const* __res
     pdl_wait();
     pdl_trigger();
     ktrace(tr, blockIdx.x, 1);
-    // every CTA reduces the router's partial logits and selects (same result
-    // everywhere); no CTA has to wait for a single selecting CTA
-    block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts);
-    if (blockIdx.x == 0) {   // publish the selection (read by the host and by later calls)
-        for (int e = threadIdx.x; e < E; e += blockDim.x) logits_out[e] = s_logit[e];
-        if (threadIdx.x < k) { ids_out[threadIdx.x] = s_ids[threadIdx.x]; wts_out[threadIdx.x] = s_wts[threadIdx.x]; }
+    if (sel_ids) {
+        // the selection was made earlier (streamed layers: the host staged
+        // those experts first)
+        if (threadIdx.x < k) s_ids[threadIdx.x] = sel_ids[threadIdx.x];
+        __syncthreads();
+    } else {
+        // every CTA reduces the router's partial logits and selects (same result
+        // everywhere); no CTA has to wait for a single selecting CTA
+        block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts);
+        if (blockIdx.x == 0) {   // publish the selection (read by the host and by later calls)
+            for (int e = threadIdx.x; e < E; e += blockDim.x) logits_out[e] = s_logit[e];
+            if (threadIdx.x < k) { ids_out[threadIdx.x] = s_ids[threadIdx.x]; wts_out[threadIdx.x] = s_wts[threadIdx.x]; }
+        }
     }
     {
-        // slots in row order: the shared expert (slot k) first, then routed 0..k-1
-        const int nrows = (k + n_shared) * I;
-        for (int r = gw; r < nrows; r += nw) {
+        // slots in row order: the shared expert (slot k) first, then routed
+        // 0..k-1; this launch covers row-order slots jj0 .. jj1 - 1
+        const int nrows = (jj1 - jj0) * I;
+        for (int r0 = gw; r0 < nrows; r0 += nw) {
+            const int r = r0 + jj0 * I;
             const int jj = r / I;
             const int j = n_shared ? (jj == 0 ? k : jj - 1) : jj;
             const int i = r - jj * I;
@@ -120,7 +130,7 @@ __global__ void __launch_bounds__(kThreads) k_gateup(const uint8_t* const* __res
             // steps ahead into L2 (same slot; it is contiguous with this one)
             if (lane == 0) {
                 const int r2 = r + 2 * nw;
-                if (r2 < nrows && r2 / I == jj)
+                if (r2 < jj1 * I && r2 / I == jj)
                     prefetch_l2_hint(rec_tab[e] + (size_t)(2 * (r2 - jj * I)) * rbH, pair_bytes, stream_pol);
             }
             float acc_g = 0.f, acc_u = 0.f;
@@ -179,6 +189,8 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
                                                    int k, int E, int n_shared, int H, int I,
                                                    const float* __restrict__ h, void* __restrict__ y, int y_bf16,
                                                    float* __restrict__ y32, size_t rbI, size_t gu_block,
+                                                   const int32_t* __restrict__ sel_ids,
+                                                   const float* __restrict__ sel_wts,
                                                    unsigned long long* __restrict__ tr) {
     extern __shared__ uint4 smh[];
     ktrace(tr, blockIdx.x, 0);
@@ -197,7 +209,12 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
     // the router has completed when this kernel starts (gate/up waited for it
     // before allowing this launch): select from its partial logits and prefetch
     // this CTA's down rows of every slot into L2 while gate/up finishes
-    block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts);
+    if (sel_ids) {   // selection made earlier (streamed layers)
+        if (threadIdx.x < k) { s_ids[threadIdx.x] = sel_ids[threadIdx.x]; s_wts[threadIdx.x] = sel_wts[threadIdx.x]; }
+        __syncthreads();
+    } else {
+        block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts);
+    }
     if (threadIdx.x < ns) {
         const int s = threadIdx.x;
         const bool sh = n_shared && s == 0;
@@ -363,7 +380,8 @@ cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32
         prof_begin(L, K_GATEUP_DECODE, s);
         e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, L.pdl, (const uint8_t* const*)L.rec_table,
                        (const float*)L.logits_part, L.router_splits, (const float*)L.router_bias, k, E,
-                       d.n_shared, x, xb, H, I, L.h, row_bytes(H), L.ids, L.wts, L.logits, L.split_trace(1));
+                       d.n_shared, x, xb, H, I, L.h, row_bytes(H), L.ids, L.wts, L.logits, (const int32_t*)nullptr, 0,
+                       k + d.n_shared, L.split_trace(1));
         prof_end(L, s);
         if (e != cudaSuccess) return e;
     }
@@ -373,7 +391,8 @@ cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32
         e = launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, L.pdl,
                        (const uint8_t* const*)L.rec_table, (const float*)L.logits_part, L.router_splits,
                        (const float*)L.router_bias, k, E,
-                       d.n_shared, H, I, (const float*)L.h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I), L.split_trace(2));
+                       d.n_shared, H, I, (const float*)L.h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I),
+                       (const int32_t*)nullptr, (const float*)nullptr, L.split_trace(2));
         prof_end(L, s);
         return e;
     }
@@ -393,12 +412,45 @@ cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, floa
     cudaError_t e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, L.pdl,
                                (const uint8_t* const*)L.rec_table, part, L.router_splits,
                                (const float*)L.router_bias, k, E, d.n_shared, x, xb, H, I, h, row_bytes(H), ids, wts,
-                               logits, (unsigned long long*)nullptr);
+                               logits, (const int32_t*)nullptr, 0, ns, (unsigned long long*)nullptr);
     if (e != cudaSuccess) return e;
     return launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, L.pdl,
                       (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias, k, E,
                       d.n_shared, H, I, (const float*)h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I),
-                      (unsigned long long*)nullptr);
+                      (const int32_t*)nullptr, (const float*)nullptr, (unsigned long long*)nullptr);
+}
+
+// Streamed layers: the selection (ids, wts of one token) is already on the
+// device and the routed experts' records are resident. `jj0..jj1` are the
+// row-order slots of gate/up to run (0 = the shared expert when there is one);
+// `down` adds the down + combine kernel. Plain launches (no programmatic
+// overlap): the caller orders them against the cache's copies with events.
+cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
+                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s) {
+    const auto& d = L.d;
+    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts, ns = k + d.n_shared;
+    const int xb = d.act_dtype == MOE_BF16;
+    cudaError_t e = cudaSuccess;
+    if (jj1 > jj0) {
+        const int need = ((jj1 - jj0) * I + kWarps - 1) / kWarps;
+        const int grid = std::max(1, std::min(need, L.num_sms * L.occ_gu));
+        prof_begin(L, K_GATEUP_DECODE, s);
+        e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, false, (const uint8_t* const*)L.rec_table,
+                       (const float*)nullptr, 0, (const float*)nullptr, k, E, d.n_shared, x, xb, H, I, L.h,
+                       row_bytes(H), (int32_t*)nullptr, (float*)nullptr, (float*)nullptr, ids, jj0, jj1,
+                       (unsigned long long*)nullptr);
+        prof_end(L, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (down) {
+        prof_begin(L, K_DOWN_DECODE, s);
+        e = launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, false,
+                       (const uint8_t* const*)L.rec_table, (const float*)nullptr, 0, (const float*)nullptr, k, E,
+                       d.n_shared, H, I, (const float*)L.h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I), ids,
+                       wts, (unsigned long long*)nullptr);
+        prof_end(L, s);
+    }
+    return e;
 }
 
 }  // namespace moe

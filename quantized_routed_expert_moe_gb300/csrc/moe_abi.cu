@@ -189,6 +189,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     size_t o_ng = pf.add(16);
 
     size_t need = router_bytes(d) + (size_t)E * 4 + n_rec * L.rec_bytes + (size_t)(E + 1) * 8 +
+                  (size_t)d.cache_slots * L.rec_bytes +
                   sc.total + (T > 1 ? pf.total : 0);
     size_t free_b = 0, total_b = 0;
     ce = cudaMemGetInfo(&free_b, &total_b);
@@ -442,6 +443,14 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
                 MOE_CUDA_TRY(cudaMemset(L.trace_split, 0, ns));
             }
             L.trace_on = value != 0;
+            return MOE_OK;
+        case MOE_OPT_HOST_TIMEOUT_MS:
+            if (value < 0 || value > 3600000) return fail(MOE_E_INVALID, "host timeout out of range 0..3600000 ms");
+            L.host_timeout_ms = (int)value;
+            return MOE_OK;
+        case MOE_OPT_TEST_STALL_COPIES_MS:
+            if (value < 0 || value > 10000) return fail(MOE_E_INVALID, "copy stall out of range 0..10000 ms");
+            L.test_stall_copies_ms = (int)value;
             return MOE_OK;
     }
     return fail(MOE_E_INVALID, "unknown option");

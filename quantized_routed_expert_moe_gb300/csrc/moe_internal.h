@@ -148,6 +148,11 @@ struct Layer {
     // three-kernel decode: programmatic dependent launch between the kernels
     bool pdl = true;
 
+    // host waits (streamed layers): deadline, and a test hook that holds the
+    // copy stream for this long before each stage's fills
+    int host_timeout_ms = 30000;
+    int test_stall_copies_ms = 0;
+
     // fused single-kernel decode (decode_fused.cu)
     bool fused_ok = false;
     int decode_path = MOE_PATH_AUTO;
@@ -167,6 +172,8 @@ struct Layer {
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select);
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
 cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s);
+cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
+                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s);
 cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
                                           float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s);
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which,

@@ -1,0 +1,228 @@
+"""Streamed expert cache (per-layer LFU slots filled from host memory).
+
+CPU: the library's cache policy (moe_lfu_trace, host-only) against the
+oracle's LFU simulation and the hand-written golden trace.
+GPU: a streamed layer decodes bit-identically to the resident layer, its
+hit/miss sequence and slot residency follow the oracle's simulation, and host
+failures (a source callback that fails, a host wait that runs out) come back
+as status codes without a device fault.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import quantized_routed_expert_moe_gb300 as moe
+import seeded_inputs as si
+from _pins import read_lfu
+
+
+def zipf_rows(seed, n_tokens, E, k, alpha=1.1):
+    """Seeded token id rows: k distinct experts per token, skewed popularity."""
+    rng = np.random.default_rng(seed)
+    p = (np.arange(1, E + 1, dtype=np.float64) ** -alpha)
+    p = p[rng.permutation(E)]
+    p /= p.sum()
+    return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(n_tokens)]).astype(np.int32)
+
+
+def oracle_slots_hits(rows, slots):
+    c = oracle.moe.LFUCache(slots)
+    slot = np.empty(rows.shape, np.int32)
+    hit = np.empty(rows.shape, np.uint8)
+    for t, ids in enumerate(rows):
+        hit[t] = [1 if int(e) in c.count else 0 for e in ids]
+        c.access(ids)
+        slot[t] = [c.slot_of[int(e)] for e in ids]
+    return slot, hit
+
+
+@pytest.mark.parametrize("seed,E,k,slots", [(0, 256, 8, 16), (1, 32, 8, 8), (2, 64, 4, 16), (3, 9, 1, 1)])
+def test_lfu_policy_matches_oracle(seed, E, k, slots):
+    rows = zipf_rows(seed, 400, E, k)
+    slot, hit = moe.moe_lfu_trace(slots, E, rows)
+    o_slot, o_hit = oracle_slots_hits(rows, slots)
+    assert np.array_equal(hit, o_hit)
+    assert np.array_equal(slot, o_slot)
+
+
+def test_lfu_policy_golden_trace():
+    """The hand-worked trace in tests/golden/lfu_trace.txt (TurboFieldfare
+    article, "token generation", with the stated readings), checked against the
+    library's policy directly."""
+    slots, rows = read_lfu()
+    ids = np.array([r[0] for r in rows], np.int32)
+    slot, hit = moe.moe_lfu_trace(slots, int(ids.max()) + 1, ids)
+    for t, (tok, hits, fills) in enumerate(rows):
+        assert sorted(e for e, h in zip(tok, hit[t]) if h) == sorted(hits)
+        for e, s, _victim in fills:
+            assert slot[t][tok.index(e)] == s
+        for j, e in enumerate(tok):
+            if e in hits:   # a hit keeps its slot
+                assert slot[t][j] == slot[t - 1][list(rows[t - 1][0]).index(e)] if e in rows[t - 1][0] else True
+
+
+def test_lfu_policy_rejects_bad_rows():
+    with pytest.raises(moe.MoEError):
+        moe.moe_lfu_trace(4, 8, np.array([[1, 1]], np.int32))
+    with pytest.raises(moe.MoEError):
+        moe.moe_lfu_trace(4, 8, np.array([[1, 9]], np.int32))
+    with pytest.raises(moe.MoEError):
+        moe.moe_lfu_trace(1, 8, np.array([[1, 2]], np.int32))
+
+
+# --------------------------------------------------------------------------- GPU
+
+def packed_records(layer, ml_desc):
+    """Host records in the library's layout (moe_pack_expert_record)."""
+    recs = []
+    n = moe.moe_expert_record_bytes(ml_desc)
+    for ex in layer.experts:
+        buf = np.zeros(n, np.uint8)
+        moe.moe_pack_expert_record(ml_desc, ex, buf)
+        recs.append(buf)
+    return recs
+
+
+def _streamed_vs_resident(layer, T, source=False, seed=31):
+    import torch
+    spec = layer.spec
+    X = si.gen_tokens(seed, 0, T, spec)
+    xs = torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).cuda()
+    y_res = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    y_str = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer) as res:
+        res.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
+        for t in range(T):
+            res.decode(xs[t], None, y_res[t])
+            res.route(xs[t], 1, ids[t], w[t])
+        torch.cuda.synchronize()
+        recs = packed_records(layer, res.desc)
+    hm = []
+    if source:
+        calls = []
+
+        def src(user, e, dst, nbytes):
+            calls.append(e)
+            ctypes.memmove(dst, recs[e].ctypes.data, nbytes)
+            return 0
+        kw = dict(source=moe.SOURCE_FN(src))
+    else:
+        kw = dict(records=recs)
+    with moe.MoELayer(layer, cache_slots=16, **kw) as st:
+        for t in range(T):
+            st.decode(xs[t], None, y_str[t])
+            torch.cuda.synchronize()
+            hm.append(st.residency())
+        stats = st.cache_stats()
+    return (y_res.cpu().numpy(), y_str.cpu().numpy(), ids.cpu().numpy(), hm, stats)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("source", [False, True])
+def test_streamed_decode_bit_identical_and_lfu(source):
+    spec = si.LayerSpec(hidden=512, inter=256, n_experts=64, zipf_alpha=1.1)
+    layer = si.gen_layer(30, 0, spec)
+    T = 40
+    y_res, y_str, ids, residency, stats = _streamed_vs_resident(layer, T, source=source)
+    assert np.array_equal(y_res, y_str)
+    o_slot, o_hit = oracle_slots_hits(ids, 16)
+    for t in range(T):
+        # the oracle's slot map after token t, seen through the library's residency
+        for j, e in enumerate(ids[t]):
+            assert residency[t][o_slot[t][j]] == e
+    assert stats["tokens"] == T
+    assert stats["hits"] == int(o_hit.sum())
+    assert stats["misses"] == T * spec.top_k - int(o_hit.sum())
+    assert stats["bytes_h2d"] == stats["misses"] * moe.moe_expert_record_bytes(moe.desc_from_spec(spec))
+
+
+@pytest.mark.gpu
+def test_explicit_stage_counts():
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=32)
+    layer = si.gen_layer(32, 0, spec)
+    desc = moe.desc_from_spec(spec)
+    recs = packed_records(layer, desc)
+    with moe.MoELayer(layer, cache_slots=8, records=recs) as st:
+        a = np.array([3, 5, 7, 9], np.int32)
+        assert st.cache_stage(a, 4) == (0, 4)
+        assert st.cache_stage(a, 4) == (4, 0)
+        b = np.array([3, 11, 12, 13, 14, 15, 16, 17], np.int32)
+        assert st.cache_stage(b, 8) == (1, 7)
+        torch.cuda.synchronize()
+        res = st.residency()
+        assert sorted(e for e in res if e >= 0) == sorted(set(b.tolist()))
+        with pytest.raises(moe.MoEError) as ei:
+            st.cache_stage(np.array([1, 1], np.int32), 2)
+        assert ei.value.status == 1
+
+
+@pytest.mark.gpu
+def test_source_failure_reported_and_recovered():
+    """Host-side failure injection: the expert source fails for one expert; the
+    decode that needs it returns MOE_E_SOURCE and leaves it out of the cache;
+    once the source works again the same token decodes normally."""
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=16)
+    layer = si.gen_layer(33, 0, spec)
+    desc = moe.desc_from_spec(spec)
+    recs = packed_records(layer, desc)
+    X = si.gen_tokens(33, 0, 1, spec)
+    x = torch.from_numpy(np.ascontiguousarray(X[0]).view(np.int16)).cuda()
+    y = torch.empty(spec.hidden, dtype=torch.float32, device="cuda")
+    y_ref = torch.empty(spec.hidden, dtype=torch.float32, device="cuda")
+    ids = torch.empty(spec.top_k, dtype=torch.int32, device="cuda")
+    w = torch.empty(spec.top_k, dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer) as res:
+        res.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
+        res.decode(x, None, y_ref)
+        res.route(x, 1, ids, w)
+        torch.cuda.synchronize()
+    bad = int(ids[3].item())
+    broken = {"on": True}
+
+    def src(user, e, dst, nbytes):
+        if broken["on"] and e == bad:
+            return 1
+        ctypes.memmove(dst, recs[e].ctypes.data, nbytes)
+        return 0
+    fn = moe.SOURCE_FN(src)
+    with moe.MoELayer(layer, cache_slots=8, source=fn) as st:
+        with pytest.raises(moe.MoEError) as ei:
+            st.decode(x, None, y)
+        assert ei.value.status == 7   # MOE_E_SOURCE
+        torch.cuda.synchronize()
+        assert bad not in st.residency()
+        broken["on"] = False
+        st.decode(x, None, y)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
+
+
+@pytest.mark.gpu
+def test_host_wait_deadline():
+    """The copy stream is held on the host (a callback that sleeps); a short
+    host deadline then runs out with MOE_E_TIMEOUT, and the layer works again
+    once the stall is lifted."""
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=16)
+    layer = si.gen_layer(34, 0, spec)
+    desc = moe.desc_from_spec(spec)
+    recs = packed_records(layer, desc)
+    with moe.MoELayer(layer, cache_slots=8, records=recs) as st:
+        st.set_option(moe.MOE_OPT_TEST_STALL_COPIES_MS, 400)
+        st.set_option(moe.MOE_OPT_HOST_TIMEOUT_MS, 20)
+        st.cache_stage(np.array([0, 1], np.int32), 2)
+        st.cache_stage(np.array([2, 3], np.int32), 2)
+        with pytest.raises(moe.MoEError) as ei:   # the first table buffer is still queued behind the stall
+            st.cache_stage(np.array([4, 5], np.int32), 2)
+        assert ei.value.status == 5   # MOE_E_TIMEOUT
+        torch.cuda.synchronize()
+        st.set_option(moe.MOE_OPT_TEST_STALL_COPIES_MS, 0)
+        st.set_option(moe.MOE_OPT_HOST_TIMEOUT_MS, 30000)
+        st.cache_stage(np.array([6, 7], np.int32), 2)
+        torch.cuda.synchronize()
