@@ -333,6 +333,148 @@ def run_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+def run_streamed(args):
+    """Streamed decode through a stack of GLM-scale layers, each with a 16-slot
+    LFU device cache filled from pinned host records. One step = one token
+    through every layer; between layers the activation is renormalised
+    (x <- bf16(y / rms(y)), a weightless stand-in for the rest of the model) so
+    that each layer's routing depends on the previous layer's output.
+
+    Routed expert records come from an alias pool of `pool` distinct records in
+    pinned host memory (layer l's expert e uses pool record (l * E + e) * 2654435761
+    mod pool): the full stack (75 x 256 records, 407 GB) does not fit in host
+    memory; the host-to-device traffic per miss is the same."""
+    ws, rank, local = dist_info()
+    spec = si.CONFIGS["glm_prefill"]   # GLM shape with Zipf(1.1) router bias
+    E, Lc, P = spec.n_experts, args.layers, args.pool
+    workload = (f"streamed GLM-scale decode: {Lc} layers of H6144 I2048 E256 top-8 + 1 shared, 16-slot LFU cache "
+                f"per layer, Zipf(1.1) routing bias per layer, {P}-record alias pool in pinned host memory")
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        layer = si.gen_layer(0, 0, spec)
+        X = si.gen_tokens(0, 0, 2, spec)
+        for _ in range(args.warmup):
+            oracle_sample(layer, X, 1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_sample(layer, X, 1)
+        dt = time.perf_counter() - t0
+        v = args.steps / dt / Lc   # one token through every layer
+        print(json.dumps({"impl": "reference", "metric": "streamed MoE decode tokens/s", "value": v, "unit": UNIT,
+                          "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": dt / args.steps * 1e3 * Lc, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": workload, "tokens_per_step": 1},
+                          "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                           "sample": "one layer-token per step, scaled to the layer count"},
+                          "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import quantized_routed_expert_moe_gb300 as moe
+    from quantized_routed_expert_moe_gb300 import build as _b
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        _b.build()
+    if ws > 1:
+        dist.barrier()
+    desc = moe.desc_from_spec(spec, cache_slots=16)
+    rb = moe.moe_expert_record_bytes(desc)
+    pool = torch.empty((P, rb), dtype=torch.uint8).pin_memory()
+    pool_np = pool.numpy()
+    for p in range(P):
+        moe.moe_pack_expert_record(desc, si.gen_expert(0, 1000, p, spec), pool_np[p])
+    stack = []
+    for l in range(Lc):
+        recs = [pool[((l * E + e) * 2654435761) % P] for e in range(E)]
+        lay = si.Layer(spec, si.gen_router(0, l, spec), [], si.gen_expert(0, l, E, spec),
+                       si.gen_router_bias(0, l, spec), 0, l)
+        stack.append(moe.MoELayer(lay, device=local, cache_slots=16, records=recs))
+    X0 = si.gen_tokens(1000 * rank, 0, args.warmup + args.steps, spec)
+    x_host = torch.from_numpy(np.ascontiguousarray(X0.view(np.int16))).view(torch.bfloat16).pin_memory()
+    x = torch.empty(spec.hidden, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(spec.hidden, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def token(i):
+        x.copy_(x_host[i], non_blocking=True)
+        for ml in stack:
+            ml.decode(x, None, y, stream=stream)
+            x.copy_((y * torch.rsqrt(torch.mean(y * y) + 1e-12)).to(torch.bfloat16))
+
+    for i in range(args.warmup):
+        token(i)
+    torch.cuda.synchronize()
+    s0 = [ml.cache_stats() for ml in stack]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        token(args.warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    s1 = [ml.cache_stats() for ml in stack]
+    hits = sum(b["hits"] - a["hits"] for a, b in zip(s0, s1))
+    misses = sum(b["misses"] - a["misses"] for a, b in zip(s0, s1))
+    h2d = sum(b["bytes_h2d"] - a["bytes_h2d"] for a, b in zip(s0, s1))
+    # pinned host -> device copy peak on this box, for the fraction
+    big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    dst.copy_(big, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(4):
+        dst.copy_(big, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_peak = 4 * (1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9
+    mx = torch.tensor([ms, wall], dtype=torch.float64, device="cuda")
+    if ws > 1:
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    ms, wall = float(mx[0]), float(mx[1])
+    value = args.steps * ws / (ms / 1e3)
+    for ml in stack:
+        ml.close()
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    h2d_gbs = h2d / (ms / 1e3) / 1e9
+    line = {
+        "metric": "streamed MoE decode tokens/s (every layer of the stack per token)", "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload, "tokens_per_step": 1, "layers": Lc, "pool_records": P,
+                   "record_bytes": rb, "parallelism": f"replicas x{ws}"},
+        "hit_rate": hits / max(hits + misses, 1),
+        "h2d_gbs": h2d_gbs,
+        "roofline": {"bound": "h2d", "achieved": h2d_gbs, "peak": h2d_peak, "unit": "GB/s",
+                     "frac": h2d_gbs / h2d_peak, "traffic": None, "kernel": "cache fills (cudaMemcpyAsync)",
+                     "peak_source": "measured here: pinned 1 GiB host-to-device copy"},
+        "e2e": {"value": args.steps * ws / wall, "unit": UNIT, "h2d_bytes_per_step": spec.hidden * 2 + h2d / args.steps,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": None,
+        "clocks": clk,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -340,7 +482,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="glm_decode",
-                    choices=["glm_decode", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense"])
+                    choices=["glm_decode", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense", "glm_streamed"])
+    ap.add_argument("--layers", type=int, default=75, help="glm_streamed: layers in the stack")
+    ap.add_argument("--pool", type=int, default=256,
+                    help="glm_streamed: distinct expert records in pinned host memory (alias pool)")
     ap.add_argument("--tokens", type=int, default=1000)
     ap.add_argument("--replicas", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -353,6 +498,9 @@ def main():
 
     if args.workload.startswith("glm_prefill"):
         run_prefill(args)
+        return
+    if args.workload == "glm_streamed":
+        run_streamed(args)
         return
     spec = si.CONFIGS[args.workload]
     if args.experts:

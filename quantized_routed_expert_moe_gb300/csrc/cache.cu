@@ -136,9 +136,12 @@ moe_status wait_event(const Layer& L, cudaEvent_t ev, const char* what) {
         const cudaError_t e = cudaEventQuery(ev);
         if (e == cudaSuccess) return MOE_OK;
         if (e != cudaErrorNotReady) return cuda_fail(e, what);
-        if (clk::now() - t0 > std::chrono::milliseconds(L.host_timeout_ms))
+        const auto waited = clk::now() - t0;
+        if (waited > std::chrono::milliseconds(L.host_timeout_ms))
             return fail(MOE_E_TIMEOUT, std::string(what) + ": host wait passed its deadline");
-        std::this_thread::sleep_for(std::chrono::microseconds(20));
+        // a decode token's round trip is tens of microseconds: spin first,
+        // then give the core back
+        if (waited > std::chrono::milliseconds(2)) std::this_thread::sleep_for(std::chrono::microseconds(50));
     }
 }
 
