@@ -300,7 +300,8 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
 // Two stages without block-wide rounds: every warp selects the top k of its
 // contiguous range of experts (k rounds of a warp argmax), then warp 0 selects
 // the top k of the <= 8 * k candidates. The union of the per-range top-k holds
-// the global top-k, so the result is the same selection. E <= 1024, 8 warps.
+// the global top-k, so the result is the same selection. E <= 1024, at least
+// 8 warps (warps beyond the eighth only join the barriers).
 __device__ __forceinline__ void block_topk_softmax(const float* sl, int E, int k, int32_t* ids_out, float* w_out) {
     __shared__ float c_v[8 * MOE_MAX_TOP_K];
     __shared__ int c_i[8 * MOE_MAX_TOP_K];
@@ -316,7 +317,7 @@ __device__ __forceinline__ void block_topk_softmax(const float* sl, int E, int k
         const float t = live[m] ? sl[e] : -INFINITY;
         v[m] = (t != t) ? -INFINITY : t;
     }
-    for (int r = 0; r < k; ++r) {
+    for (int r = 0; r < k && warp < 8; ++r) {   // warps 8 and up (larger blocks) take no range
         float bv = -INFINITY;
         int bi = INT_MAX;
 #pragma unroll

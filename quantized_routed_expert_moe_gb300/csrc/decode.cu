@@ -19,6 +19,7 @@
 // architecture".
 #include "common.cuh"
 #include "moe_internal.h"
+#include "sm100.cuh"
 
 namespace moe {
 
@@ -64,38 +65,62 @@ __device__ void stage_vector_q16(const void* x, int x_bf16, bool cg, int K, uint
 // ---------------------------------------------------------------------------
 //
 // h[j][i] = silu(gate_i . x) * (up_i . x) for slot j (routed slots 0..k-1 in
-// selection order, the shared expert at slot k). One warp per (slot, row i);
-// lane l takes half-groups l, l + 32, ... of both rows.
-__global__ void __launch_bounds__(kThreads) k_gateup(const uint8_t* const* __restrict__ rec_tab,
-                                                     const float* __restrict__ part, int splits,
-                                                     const float* __restrict__ bias, int k, int E, int n_shared,
-                                                     const void* __restrict__ x, int x_bf16, int H, int I,
-                                                     float* __restrict__ h, size_t rbH,
-                                                     int32_t* __restrict__ ids_out, float* __restrict__ wts_out,
-                                                     float* __restrict__ logits_out,
-                                                     const int32_t* __restrict__ sel_ids, int jj0, int jj1,
-                                                     unsigned long long* __restrict__ tr) {
+// selection order, the shared expert at slot k). Rows are taken in "row order":
+// the shared expert's rows first, then the routed slots, i ascending; CTA c owns
+// rows [c R, (c + 1) R) of that order (R a multiple of 32), one or two
+// contiguous runs of (gate row i, up row i) pairs in the weight records.
+//
+// One warp per row pair at a time: each lane issues all of its 128-bit loads of
+// both rows (half-groups l, l + 32, ...) before it computes, and lane 0 pulls the
+// pair kGuAhead steps ahead into L2, so that HBM sees many independent requests
+// (a burst of plain loads reaches the copy roofline; bulk copies through
+// shared memory do not, for bursts this short). The codes are multiplied with
+// the 16-bit fixed-point activations by dp4a. The CTA ends by quantising its
+// SwiGLU outputs into the down kernel's staged form, which the down kernel
+// copies as it is.
+
+constexpr int kGuThreads = 256;
+constexpr int kGuWarps = kGuThreads / 32;
+constexpr int kGuAhead = 3;   // row pairs per warp pulled into L2 ahead of use
+
+// The q16 SwiGLU output block (global, and the down kernel's shared-memory
+// copy of it) for ns slots in row order: runs hq[ns][4][I/32] (uint4), then the
+// inverse scales inv[ns][I/32], then the half-group sums X[ns][I/32].
+__host__ __device__ inline size_t hq_block_bytes(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
+
+// expert (record index) of row-order slot jj
+__device__ __forceinline__ int row_slot_expert(int jj, int k, int E, int n_shared, const int32_t* s_ids) {
+    const int j = n_shared ? (jj == 0 ? k : jj - 1) : jj;
+    if (j == k) return E;
+    const int e = s_ids[j];
+    return ((unsigned)e < (unsigned)E) ? e : 0;   // a valid selection never needs the clamp
+}
+
+__global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* __restrict__ rec_tab,
+                                                         const float* __restrict__ part, int splits,
+                                                         const float* __restrict__ bias, int k, int E, int n_shared,
+                                                         const void* __restrict__ x, int x_bf16, int H, int I,
+                                                         size_t rbH, int R, void* __restrict__ hout, int copies,
+                                                         int32_t* __restrict__ ids_out, float* __restrict__ wts_out,
+                                                         float* __restrict__ logits_out,
+                                                         const int32_t* __restrict__ sel_ids, int jj0, int jj1,
+                                                         unsigned long long* __restrict__ tr) {
     extern __shared__ uint4 smq[];
     __shared__ float s_logit[1024];
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
     __shared__ float s_wts[MOE_MAX_TOP_K];
-    ktrace(tr, blockIdx.x, 0);
-    const int HG = H / 32;
+    const int HG = H / 32, IG = I / 32, ns = k + n_shared;
     uint4* xq = smq;                                                   // [4][HG]
     float* Iv = reinterpret_cast<float*>(smq + 4 * HG);                // [HG] 2^-f
     float* Xx = Iv + HG;                                               // [HG]
+    float* hbuf = Xx + HG;                                             // [R]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ktrace(tr, blockIdx.x, 0);
     stage_vector_q16(x, x_bf16, false, H, xq, Iv, Xx);
     __syncthreads();
     ktrace(tr, blockIdx.x, 2);
-    const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
-    const int M = (HG + 31) / 32;
-    const uint64_t stream_pol = policy_evict_first();
-    const uint32_t pair_bytes = (uint32_t)(2 * rbH);
 
-    // The router's last CTA is latency-bound (atomics, partial logits, top-k);
-    // weight traffic started before it finishes slows it by more than it
-    // hides, so the weight rows (shared and routed) are all read after it.
+    // no weight traffic before the selection is known
     pdl_wait();
     pdl_trigger();
     ktrace(tr, blockIdx.x, 1);
@@ -113,65 +138,108 @@ __global__ void __launch_bounds__(kThreads) k_gateup(const uint8_t* const* __res
             if (threadIdx.x < k) { ids_out[threadIdx.x] = s_ids[threadIdx.x]; wts_out[threadIdx.x] = s_wts[threadIdx.x]; }
         }
     }
-    {
-        // slots in row order: the shared expert (slot k) first, then routed
-        // 0..k-1; this launch covers row-order slots jj0 .. jj1 - 1
-        const int nrows = (jj1 - jj0) * I;
-        for (int r0 = gw; r0 < nrows; r0 += nw) {
-            const int r = r0 + jj0 * I;
-            const int jj = r / I;
-            const int j = n_shared ? (jj == 0 ? k : jj - 1) : jj;
-            const int i = r - jj * I;
-            int e = j == k ? E : s_ids[j];
-            if ((unsigned)e >= (unsigned)E && j < k) e = 0;  // a valid selection never needs this
-            const uint8_t* g = rec_tab[e] + (size_t)(2 * i) * rbH;
-            const uint8_t* u = g + rbH;
-            // keep HBM busy across this warp's compute: pull the row pair two
-            // steps ahead into L2 (same slot; it is contiguous with this one)
-            if (lane == 0) {
-                const int r2 = r + 2 * nw;
-                if (r2 < jj1 * I && r2 / I == jj)
-                    prefetch_l2_hint(rec_tab[e] + (size_t)(2 * (r2 - jj * I)) * rbH, pair_bytes, stream_pol);
-            }
-            float acc_g = 0.f, acc_u = 0.f;
-            for (int m0 = 0; m0 < M; m0 += kGuBlock) {
-                uint4 cg[kGuBlock], cu[kGuBlock];
-                uint32_t mg[kGuBlock], mu[kGuBlock];
-#pragma unroll
-                for (int mm = 0; mm < kGuBlock; ++mm) {
-                    const int hg = lane + 32 * (m0 + mm);
-                    if (m0 + mm < M && hg < HG) {
-                        cg[mm] = ldg_stream_hint(g + 16 * hg, stream_pol);
-                        cu[mm] = ldg_stream_hint(u + 16 * hg, stream_pol);
-                        mg[mm] = ldg_u32_hint(g + H / 2 + 4 * (hg >> 1), stream_pol);
-                        mu[mm] = ldg_u32_hint(u + H / 2 + 4 * (hg >> 1), stream_pol);
-                    }
-                }
-#pragma unroll
-                for (int mm = 0; mm < kGuBlock; ++mm) {
-                    const int hg = lane + 32 * (m0 + mm);
-                    if (m0 + mm < M && hg < HG) {
-                        int gh = 0, gl = 0, uh = 0, ul = 0;
-#pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            const uint4 xs = xq[wi * HG + hg];
-                            word_dp4a(u4w(cg[mm], wi), xs, gh, gl);
-                            word_dp4a(u4w(cu[mm], wi), xs, uh, ul);
-                        }
-                        const float iv = Iv[hg], xs = Xx[hg];
-                        const float2 sg = meta_to_f2(mg[mm]), su = meta_to_f2(mu[mm]);
-                        acc_g = fmaf(sg.x, (float)(gh * 256 + gl) * iv, fmaf(sg.y, xs, acc_g));
-                        acc_u = fmaf(su.x, (float)(uh * 256 + ul) * iv, fmaf(su.y, xs, acc_u));
-                    }
-                }
-            }
-            const float gv = warp_sum(acc_g);
-            const float uv = warp_sum(acc_u);
-            if (lane == 0) h[(size_t)j * I + i] = silu_f(gv) * uv;
+
+    const int NR = (jj1 - jj0) * I;
+    const int rbeg = blockIdx.x * R;
+    const int np = max(0, min(R, NR - rbeg));   // row pairs of this CTA
+    const uint64_t pol = policy_evict_first();
+    const uint32_t pair_b = (uint32_t)(2 * rbH);
+    auto pair_ptr = [&](int p) {
+        const int r = jj0 * I + rbeg + p;
+        const int jj = r / I, i = r - jj * I;
+        return rec_tab[row_slot_expert(jj, k, E, n_shared, s_ids)] + (size_t)2 * i * rbH;
+    };
+    // the first kGuAhead pairs of every warp, then one more per step
+    if (lane == 0)
+        for (int a = 0; a < kGuAhead; ++a) {
+            const int p = warp + a * kGuWarps;
+            if (p < np) prefetch_l2_hint(pair_ptr(p), pair_b, pol);
         }
+    const int M = (HG + 31) / 32;
+    for (int p = warp; p < np; p += kGuWarps) {
+        if (lane == 0) {
+            const int pa = p + kGuAhead * kGuWarps;
+            if (pa < np) prefetch_l2_hint(pair_ptr(pa), pair_b, pol);
+        }
+        const uint8_t* g = pair_ptr(p);
+        const uint8_t* u = g + rbH;
+        float acc_g = 0.f, acc_u = 0.f;
+        for (int m0 = 0; m0 < M; m0 += kGuBlock) {
+            uint4 cg[kGuBlock], cu[kGuBlock];
+            uint32_t mg[kGuBlock], mu[kGuBlock];
+#pragma unroll
+            for (int mm = 0; mm < kGuBlock; ++mm) {
+                const int hg = lane + 32 * (m0 + mm);
+                if (m0 + mm < M && hg < HG) {
+                    cg[mm] = ldg_stream_hint(g + 16 * hg, pol);
+                    cu[mm] = ldg_stream_hint(u + 16 * hg, pol);
+                    mg[mm] = ldg_u32_hint(g + H / 2 + 4 * (hg >> 1), pol);
+                    mu[mm] = ldg_u32_hint(u + H / 2 + 4 * (hg >> 1), pol);
+                }
+            }
+#pragma unroll
+            for (int mm = 0; mm < kGuBlock; ++mm) {
+                const int hg = lane + 32 * (m0 + mm);
+                if (m0 + mm < M && hg < HG) {
+                    int gh = 0, gl = 0, uh = 0, ul = 0;
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint4 xs = xq[wi * HG + hg];
+                        word_dp4a(u4w(cg[mm], wi), xs, gh, gl);
+                        word_dp4a(u4w(cu[mm], wi), xs, uh, ul);
+                    }
+                    const float iv = Iv[hg], xs = Xx[hg];
+                    const float2 sg = meta_to_f2(mg[mm]), su = meta_to_f2(mu[mm]);
+                    acc_g = fmaf(sg.x, (float)(gh * 256 + gl) * iv, fmaf(sg.y, xs, acc_g));
+                    acc_u = fmaf(su.x, (float)(uh * 256 + ul) * iv, fmaf(su.y, xs, acc_u));
+                }
+            }
+        }
+        const float gv = warp_sum(acc_g);
+        const float uv = warp_sum(acc_u);
+        if (lane == 0) hbuf[p] = silu_f(gv) * uv;
     }
     __syncthreads();
     ktrace(tr, blockIdx.x, 3);
+    // the CTA's SwiGLU outputs in the down kernel's staged form; a half-group
+    // (32 rows) never straddles CTAs or slots
+    // (written `copies` times: the down kernel's CTAs all read the whole block,
+    // and spreading them over several copies spreads the reads over L2)
+    const int nrun = np / 8;
+    const size_t blk = hq_block_bytes(ns, I);
+    for (int rb = warp * 32; rb < ((nrun + 31) / 32) * 32; rb += blockDim.x) {
+        const int rr = rb + lane;
+        const bool valid = rr < nrun;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = valid ? hbuf[8 * rr + i] : 0.f;
+        const int r0 = jj0 * I + rbeg + 8 * (valid ? rr : 0);
+        const int jj = r0 / I, run = (r0 - jj * I) / 8;
+        // quantise once (the run, its half-group's scale and sum) ...
+        float m = 0.f, sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { m = fmaxf(m, fabsf(v[i])); sum += v[i]; }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        const float sc = q16_scale(m);
+        const uint4 qv = quant_run(v, sc);
+        // ... and store it into every replica
+        if (valid) {
+            const int hg = run >> 2, wi = run & 3;
+            for (int c = 0; c < copies; ++c) {
+                uint8_t* base = static_cast<uint8_t*>(hout) + (size_t)c * blk;
+                uint4* hq = reinterpret_cast<uint4*>(base);
+                float* hinv = reinterpret_cast<float*>(hq + (size_t)ns * 4 * IG);
+                float* hX = hinv + ns * IG;
+                hq[(size_t)jj * 4 * IG + wi * IG + hg] = qv;
+                if (wi == 0) { hinv[jj * IG + hg] = 1.0f / sc; hX[jj * IG + hg] = sum; }
+            }
+        }
+    }
+    // the down kernel reads the block with a bulk copy (the async proxy)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -187,10 +255,11 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
                                                    const float* __restrict__ part, int splits,
                                                    const float* __restrict__ bias,
                                                    int k, int E, int n_shared, int H, int I,
-                                                   const float* __restrict__ h, void* __restrict__ y, int y_bf16,
+                                                   const void* __restrict__ hblk, int copies, void* __restrict__ y,
+                                                   int y_bf16,
                                                    float* __restrict__ y32, size_t rbI, size_t gu_block,
                                                    const int32_t* __restrict__ sel_ids,
-                                                   const float* __restrict__ sel_wts,
+                                                   const float* __restrict__ sel_wts, unsigned* __restrict__ err,
                                                    unsigned long long* __restrict__ tr) {
     extern __shared__ uint4 smh[];
     ktrace(tr, blockIdx.x, 0);
@@ -201,20 +270,33 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
     float* ypart = Xh + ns * IG;                                         // [ns][kDownMaxRows]
     __shared__ const uint8_t* s_rows[MOE_MAX_TOP_K + 1];
     __shared__ float s_w[MOE_MAX_TOP_K + 1];
-    __shared__ float s_logit[1024];
+    __shared__ __align__(8) uint64_t s_hbar;
+    __shared__ int s_abort;
+    if (threadIdx.x == 0) {
+        bw::mbar_init(bw::saddr(&s_hbar), 1);
+        s_abort = 0;
+        bw::mbar_fence_init();
+    }
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
     __shared__ float s_wts[MOE_MAX_TOP_K];
     const int own0 = (int)((long long)H * blockIdx.x / gridDim.x);
     const int own1 = (int)((long long)H * (blockIdx.x + 1) / gridDim.x);
-    // the router has completed when this kernel starts (gate/up waited for it
-    // before allowing this launch): select from its partial logits and prefetch
-    // this CTA's down rows of every slot into L2 while gate/up finishes
-    if (sel_ids) {   // selection made earlier (streamed layers)
-        if (threadIdx.x < k) { s_ids[threadIdx.x] = sel_ids[threadIdx.x]; s_wts[threadIdx.x] = sel_wts[threadIdx.x]; }
-        __syncthreads();
-    } else {
-        block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts);
+    pdl_wait();     // gate/up complete: the selection it published and the staged SwiGLU outputs are final
+    pdl_trigger();  // the next token's router may start prefetching its weights
+    ktrace(tr, blockIdx.x, 1);
+    // every slot's SwiGLU outputs, already in the staged form gate/up wrote:
+    // one bulk copy into shared memory, in flight while the selection is read
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)hq_block_bytes(ns, I);
+        bw::mbar_arrive_tx(bw::saddr(&s_hbar), bytes);
+        const uint8_t* src = static_cast<const uint8_t*>(hblk) + (size_t)(blockIdx.x % copies) * bytes;
+        bw::bulk_load(bw::saddr(smh), src, bytes, bw::saddr(&s_hbar), policy_evict_first());
     }
+    if (threadIdx.x < k) {   // the selection (gate/up's CTA 0 published it; streamed layers pass their own)
+        s_ids[threadIdx.x] = sel_ids[threadIdx.x];
+        s_wts[threadIdx.x] = sel_wts[threadIdx.x];
+    }
+    __syncthreads();
     if (threadIdx.x < ns) {
         const int s = threadIdx.x;
         const bool sh = n_shared && s == 0;
@@ -224,46 +306,8 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
         const uint8_t* base = rec_tab[e] + gu_block;
         s_rows[s] = base;
         s_w[s] = sh ? 1.0f : s_wts[j];
-        if (own1 > own0)
-            prefetch_l2_hint(base + (size_t)own0 * rbI, (uint32_t)((own1 - own0) * rbI), policy_evict_last());
     }
-    pdl_wait();     // gate/up complete: h is final
-    pdl_trigger();  // the next token's router may start prefetching its weights
-    ktrace(tr, blockIdx.x, 1);
-    // stage every slot's h (shared first, then routed in selection order); all
-    // of a thread's loads are issued before any is used (one L2 round trip)
-    {
-        const int warp0 = threadIdx.x >> 5, lane0 = threadIdx.x & 31;
-        const int nrun = I / 8, total = ns * nrun;
-        const int rounds = (total + blockDim.x - 1) / blockDim.x;   // warp-uniform
-        for (int rb0 = 0; rb0 < rounds; rb0 += 4) {
-            float v[4][8];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int idx = (rb0 + u) * blockDim.x + warp0 * 32 + lane0;
-                const bool valid = rb0 + u < rounds && idx < total;
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
-                if (valid) {
-                    const int s = idx / nrun, r = idx - s * nrun;
-                    const int j = (n_shared && s == 0) ? k : s - n_shared;
-                    const float4* src = reinterpret_cast<const float4*>(h + (size_t)j * I) + 2 * r;
-                    a = __ldcg(src);
-                    c = __ldcg(src + 1);
-                }
-                v[u][0] = a.x; v[u][1] = a.y; v[u][2] = a.z; v[u][3] = a.w;
-                v[u][4] = c.x; v[u][5] = c.y; v[u][6] = c.z; v[u][7] = c.w;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (rb0 + u >= rounds) break;   // uniform across the block
-                const int idx = (rb0 + u) * blockDim.x + warp0 * 32 + lane0;
-                const bool valid = idx < total;
-                const int s = valid ? idx / nrun : 0, r = valid ? idx - s * nrun : 0;
-                // a half-group's four runs are in four consecutive lanes (nrun % 4 == 0)
-                stage_q16_run(v[u], valid, r, IG, hq + (size_t)s * 4 * IG, Iv + s * IG, Xh + s * IG);
-            }
-        }
-    }
+    bw::mbar_wait(bw::saddr(&s_hbar), 0, &s_abort, err, 1u << 27);
     __syncthreads();
     ktrace(tr, blockIdx.x, 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -342,7 +386,15 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
 // launchers
 // ---------------------------------------------------------------------------
 
-static size_t gu_smem(int H) { return (size_t)H * 2 + (size_t)(H / 32) * 8; }
+static int round32(int v) { return (v + 31) / 32 * 32; }
+// rows one gate/up CTA owns for NR rows: a multiple of 32, spread over every resident CTA
+static int gu_rows(const Layer& L, int NR) {
+    return std::max(32, round32((NR + L.num_sms * L.occ_gu - 1) / (L.num_sms * L.occ_gu)));
+}
+static size_t gu_smem_for(const Layer& L, int R) {
+    const int H = L.d.hidden;
+    return (size_t)H * 2 + (size_t)(H / 32) * 8 + (size_t)R * 4;
+}
 static size_t down_smem(int I, int ns) {
     return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8 + (size_t)ns * kDownMaxRows * 4;
 }
@@ -352,11 +404,13 @@ cudaError_t decode_kernel_setup(Layer& L) {
     const int H = L.d.hidden, I = L.d.inter, ns = L.d.top_k + L.d.n_shared;
     cudaError_t e = router_kernel_setup(L);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu_smem(H));
+    const int R1 = round32((ns * I + L.num_sms - 1) / L.num_sms);   // rows per CTA at one CTA per SM (upper bound)
+    L.gu_smem = gu_smem_for(L, R1);
+    e = cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.gu_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)down_smem(I, ns));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, k_gateup, kThreads, gu_smem(H));
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, k_gateup, kGuThreads, L.gu_smem);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, k_down, kThreads, down_smem(I, ns));
     if (e != cudaSuccess) return e;
@@ -369,30 +423,46 @@ cudaError_t decode_kernel_setup(Layer& L) {
     return cudaSuccess;
 }
 
-cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which, cudaStream_t s) {
+// gate/up over row-order slots jj0..jj1-1 (sel_ids null: select from `part`)
+static cudaError_t launch_gateup(Layer& L, const void* x, const float* part, void* hblk, int copies, int32_t* ids_out,
+                                 float* wts_out, float* logits_out, const int32_t* sel_ids, int jj0, int jj1,
+                                 bool pdl, unsigned long long* tr, cudaStream_t s) {
     const auto& d = L.d;
-    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts;
-    const int xb = d.act_dtype == MOE_BF16;
+    const int NR = (jj1 - jj0) * d.inter;
+    const int R = gu_rows(L, NR);
+    const int grid = (NR + R - 1) / R;
+    return launch_pdl(k_gateup, dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s, pdl,
+                      (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias, d.top_k,
+                      d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
+                      row_bytes(d.hidden), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1, tr);
+}
+
+static cudaError_t launch_down(Layer& L, const float* part, const void* hblk, int copies, void* y, float* y_f32,
+                               const int32_t* sel_ids, const float* sel_wts, bool pdl, unsigned long long* tr,
+                               cudaStream_t s) {
+    const auto& d = L.d;
+    const int ns = d.top_k + d.n_shared;
+    return launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(d.inter, ns), s, pdl,
+                      (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias,
+                      d.top_k, d.n_experts, d.n_shared, d.hidden, d.inter, hblk, copies, y,
+                      d.act_dtype == MOE_BF16 ? 1 : 0,
+                      y_f32, row_bytes(d.inter), gu_block_bytes(d.hidden, d.inter), sel_ids, sel_wts,
+                      fused_error_word(L), tr);
+}
+
+cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which, cudaStream_t s) {
+    const int ns = L.d.top_k + L.d.n_shared;
     cudaError_t e;
     if (which & (RUN_ROUTED_GU | RUN_SHARED_GU)) {
-        const int need = ((k + d.n_shared) * I + kWarps - 1) / kWarps;
-        const int grid = std::max(1, std::min(need, L.num_sms * L.occ_gu));
         prof_begin(L, K_GATEUP_DECODE, s);
-        e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, L.pdl, (const uint8_t* const*)L.rec_table,
-                       (const float*)L.logits_part, L.router_splits, (const float*)L.router_bias, k, E,
-                       d.n_shared, x, xb, H, I, L.h, row_bytes(H), L.ids, L.wts, L.logits, (const int32_t*)nullptr, 0,
-                       k + d.n_shared, L.split_trace(1));
+        e = launch_gateup(L, x, L.logits_part, L.h, L.h_copies, L.ids, L.wts, L.logits, nullptr, 0, ns, L.pdl,
+                          L.split_trace(1), s);
         prof_end(L, s);
         if (e != cudaSuccess) return e;
     }
     if (which & RUN_DOWN) {
-        const int ns = k + d.n_shared;
         prof_begin(L, K_DOWN_DECODE, s);
-        e = launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, L.pdl,
-                       (const uint8_t* const*)L.rec_table, (const float*)L.logits_part, L.router_splits,
-                       (const float*)L.router_bias, k, E,
-                       d.n_shared, H, I, (const float*)L.h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I),
-                       (const int32_t*)nullptr, (const float*)nullptr, L.split_trace(2));
+        e = launch_down(L, L.logits_part, L.h, L.h_copies, y, y_f32, L.ids, L.wts, L.pdl, L.split_trace(2), s);
         prof_end(L, s);
         return e;
     }
@@ -401,23 +471,14 @@ cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32
 
 // The same two expert kernels over caller-given scratch: router partials
 // `part` [splits][E] (already written on `s`), selection out (`logits` [E],
-// `ids` [k], `wts` [k]) and SwiGLU outputs `h` [k + 1][I]. No profiling or tracing.
+// `ids` [k], `wts` [k]) and the staged SwiGLU outputs `h` (at least
+// hq_block_bytes(k + n_shared, I) bytes). No profiling or tracing.
 cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
                                           float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s) {
-    const auto& d = L.d;
-    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts, ns = k + d.n_shared;
-    const int xb = d.act_dtype == MOE_BF16;
-    const int need = (ns * I + kWarps - 1) / kWarps;
-    const int grid = std::max(1, std::min(need, L.num_sms * L.occ_gu));
-    cudaError_t e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, L.pdl,
-                               (const uint8_t* const*)L.rec_table, part, L.router_splits,
-                               (const float*)L.router_bias, k, E, d.n_shared, x, xb, H, I, h, row_bytes(H), ids, wts,
-                               logits, (const int32_t*)nullptr, 0, ns, (unsigned long long*)nullptr);
+    const int ns = L.d.top_k + L.d.n_shared;
+    cudaError_t e = launch_gateup(L, x, part, h, 1, ids, wts, logits, nullptr, 0, ns, L.pdl, nullptr, s);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, L.pdl,
-                      (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias, k, E,
-                      d.n_shared, H, I, (const float*)h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I),
-                      (const int32_t*)nullptr, (const float*)nullptr, (unsigned long long*)nullptr);
+    return launch_down(L, part, h, 1, y, y_f32, ids, wts, L.pdl, nullptr, s);
 }
 
 // Streamed layers: the selection (ids, wts of one token) is already on the
@@ -427,27 +488,16 @@ cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, floa
 // overlap): the caller orders them against the cache's copies with events.
 cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
                                       const float* wts, int jj0, int jj1, bool down, cudaStream_t s) {
-    const auto& d = L.d;
-    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts, ns = k + d.n_shared;
-    const int xb = d.act_dtype == MOE_BF16;
     cudaError_t e = cudaSuccess;
     if (jj1 > jj0) {
-        const int need = ((jj1 - jj0) * I + kWarps - 1) / kWarps;
-        const int grid = std::max(1, std::min(need, L.num_sms * L.occ_gu));
         prof_begin(L, K_GATEUP_DECODE, s);
-        e = launch_pdl(k_gateup, dim3(grid), dim3(kThreads), gu_smem(H), s, false, (const uint8_t* const*)L.rec_table,
-                       (const float*)nullptr, 0, (const float*)nullptr, k, E, d.n_shared, x, xb, H, I, L.h,
-                       row_bytes(H), (int32_t*)nullptr, (float*)nullptr, (float*)nullptr, ids, jj0, jj1,
-                       (unsigned long long*)nullptr);
+        e = launch_gateup(L, x, nullptr, L.h, L.h_copies, nullptr, nullptr, nullptr, ids, jj0, jj1, false, nullptr, s);
         prof_end(L, s);
         if (e != cudaSuccess) return e;
     }
     if (down) {
         prof_begin(L, K_DOWN_DECODE, s);
-        e = launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(I, ns), s, false,
-                       (const uint8_t* const*)L.rec_table, (const float*)nullptr, 0, (const float*)nullptr, k, E,
-                       d.n_shared, H, I, (const float*)L.h, y, xb, y_f32, row_bytes(I), gu_block_bytes(H, I), ids,
-                       wts, (unsigned long long*)nullptr);
+        e = launch_down(L, nullptr, L.h, L.h_copies, y, y_f32, ids, wts, false, nullptr, s);
         prof_end(L, s);
     }
     return e;

@@ -173,7 +173,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     size_t o_logits = sc.add((size_t)T * E * 4);
     size_t o_ids = sc.add((size_t)T * k * 4);
     size_t o_w = sc.add((size_t)T * k * 4);
-    size_t o_h = sc.add((size_t)(k + 1) * I * 4);
+    size_t o_h = sc.add(std::max((size_t)(k + 1) * I * 4, (size_t)kHCopies * hq_block_bytes_host(k + d.n_shared, I)));
     size_t o_cnt = sc.add(64 * 4);
     // prefill block layout
     const int rows = T * k + T * d.n_shared;
@@ -290,6 +290,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
         L.ids = reinterpret_cast<int32_t*>(base + o_ids);
         L.wts = reinterpret_cast<float*>(base + o_w);
         L.h = reinterpret_cast<float*>(base + o_h);
+        L.h_copies = kHCopies;
         L.counters = reinterpret_cast<unsigned*>(base + o_cnt);
     }
     if (T > 1) {

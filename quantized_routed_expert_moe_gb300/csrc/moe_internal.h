@@ -127,7 +127,8 @@ struct Layer {
     float* logits = nullptr;        // [max_tokens][E]
     int32_t* ids = nullptr;         // [max_tokens][k]
     float* wts = nullptr;           // [max_tokens][k]
-    float* h = nullptr;             // [k + 1][I]
+    float* h = nullptr;             // staged SwiGLU outputs: h_copies replicas of the q16 block
+    int h_copies = 1;
     unsigned* counters = nullptr;   // [8] last-block counters, kept at zero between launches
     int router_splits = 1;       // split-K of the one-token router
     int router_splits_tok = 1;   // split-K of the multi-token router (<= 16)
@@ -144,6 +145,7 @@ struct Layer {
     size_t device_bytes = 0;
     int num_sms = 0;
     int occ_gu = 0, occ_down = 0;  // resident CTAs per SM of the decode expert kernels
+    size_t gu_smem = 0;            // gate/up dynamic shared memory (upper bound)
 
     // three-kernel decode: programmatic dependent launch between the kernels
     bool pdl = true;
@@ -174,6 +176,9 @@ cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
 cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s);
 cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
                                       const float* wts, int jj0, int jj1, bool down, cudaStream_t s);
+// staged SwiGLU output block (q16 runs, inverse scales, sums) of ns slots
+inline size_t hq_block_bytes_host(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
+constexpr int kHCopies = 16;   // replicas of that block the decode kernels use
 cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
                                           float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s);
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which,

@@ -102,6 +102,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
         "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
         : "memory");
 }
+// Contiguous bulk copy global -> shared (both 16-byte aligned, size a multiple
+// of 16); completion is counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
 // Make this thread's ordinary shared-memory stores visible to the async proxy
 // (the tensor cores read operands through it).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
