@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, i
 // operand stages of 32 columns (128 x 64 fp16) from column 256.
 
 constexpr int kStages = 8, kRawStages = 4, kChunksPerRaw = 4;
-constexpr int kEpiWarps = 4, kDqWarps = 8;
+constexpr int kEpiWarps = 4, kDqWarps = 16;
+constexpr int kDqParts = kDqWarps / 4;   // K parts of a chunk per tensor-memory lane quarter
 constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
 constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kB16 = 128 * 128;
@@ -346,11 +347,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
         }
         if (lane == 0) tw.store(0, tw.acc);
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
-        // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows), half hf
-        // of each chunk's K (columns 16 hf .. 16 hf + 15 of the stage)
-        const int dw = warp - kEpiWarps, q = dw & 3, hf = dw >> 2;
+        // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows) and
+        // part pt of each chunk's K (16 elements: columns 8 pt .. 8 pt + 7)
+        const int dw = warp - kEpiWarps, q = dw & 3, pt = dw >> 2;
         const int r = 32 * q + lane;
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemA + 16 * hf;
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemA + 8 * pt;
         uint32_t it = 0, rit = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
             for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
@@ -362,23 +363,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 const uint8_t* rw = raw + rs * kRaw;
                 const uint4 mq = *reinterpret_cast<const uint4*>(rw + kRawCodes + r * 16);
                 const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
-                uint4 cw[kChunksPerRaw];
+                uint2 cw[kChunksPerRaw];
 #pragma unroll
                 for (int c = 0; c < kChunksPerRaw; ++c) {
-                    // 16-byte unit 2c + hf of row r, at its 128-byte-swizzled place
-                    const int u = (c << 1) | hf;
-                    cw[c] = *reinterpret_cast<const uint4*>(rw + r * 128 + ((u ^ (r & 7)) << 4));
+                    // bytes 8 pt .. 8 pt + 7 of chunk c (16-byte unit 2c + pt / 2),
+                    // at their 128-byte-swizzled place
+                    const int u = (c << 1) | (pt >> 1);
+                    cw[c] = *reinterpret_cast<const uint2*>(rw + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (pt & 1));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_rempty + 8 * rs);
-                uint32_t o[kChunksPerRaw][16];
+                uint32_t o[kChunksPerRaw][8];
 #pragma unroll
                 for (int c = 0; c < kChunksPerRaw; ++c) {
                     const uint32_t mw = u4w(mq, c);
                     const uint32_t s2 = __byte_perm(mw, 0, 0x1010), b2 = __byte_perm(mw, 0, 0x3232);
+                    const uint32_t vw[2] = {cw[c].x, cw[c].y};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t v = u4w(cw[c], j);
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t v = vw[j];
                         o[c][4 * j + 0] = dq_pair(v, s2, b2);
                         o[c][4 * j + 1] = dq_pair(v >> 4, s2, b2);
                         o[c][4 * j + 2] = dq_pair(v >> 8, s2, b2);
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                         const uint32_t s = (it + c) % kStages;
                         tw(b_empty + 8 * s, (((it + c) / kStages) & 1) ^ 1, s_abort, a.err, ERR_DQ);
                         tc_fence_after();
-                        tmem_st16(ta + s * kACols, o[c]);
+                        tmem_st8(ta + s * kACols, o[c]);
                     }
                 }
                 tmem_wait_st();
