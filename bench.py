@@ -132,6 +132,17 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(vals, device):
+    """Elementwise maximum of `vals` over every rank of the default process
+    group (the values themselves when there is one rank)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
 def oracle_sample(layer, X, n_tokens):
     """Time the fp64 oracle on n_tokens tokens; returns tokens/s."""
     import oracle
@@ -294,10 +305,7 @@ def run_prefill(args):
         torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
 
-    mx = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-    ms, e2e_s = float(mx[0]), float(mx[1])
+    ms, e2e_s = max_over_ranks([ms, e2e_s], "cuda")
     total_tokens = T * R * args.steps * ws
     value = total_tokens / (ms / 1e3)
     _, tflops, peak_kind = peaks()
@@ -443,10 +451,7 @@ def run_streamed(args):
     e1.record(stream)
     torch.cuda.synchronize()
     h2d_peak = 4 * (1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9
-    mx = torch.tensor([ms, wall], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-    ms, wall = float(mx[0]), float(mx[1])
+    ms, wall = max_over_ranks([ms, wall], "cuda")
     value = args.steps * ws / (ms / 1e3)
     for ml in stack:
         ml.close()
@@ -609,10 +614,7 @@ def main():
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
 
-    mx = torch.tensor([ms, e2e_s], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-    ms, e2e_s = float(mx[0]), float(mx[1])
+    ms, e2e_s = max_over_ranks([ms, e2e_s], "cuda")
     total_tokens = T * args.steps * ws
     value = total_tokens / (ms / 1e3)
     e2e = total_tokens / e2e_s
