@@ -71,17 +71,16 @@ __device__ void stage_vector_q16(const void* x, int x_bf16, bool cg, int K, uint
 // contiguous runs of (gate row i, up row i) pairs in the weight records.
 //
 // One warp per row pair at a time: each lane issues all of its 128-bit loads of
-// both rows (half-groups l, l + 32, ...) before it computes, and lane 0 pulls the
-// pair kGuAhead steps ahead into L2, so that HBM sees many independent requests
-// (a burst of plain loads reaches the copy roofline; bulk copies through
-// shared memory do not, for bursts this short). The codes are multiplied with
+// both rows (half-groups l, l + 32, ...) before it computes, so that HBM sees
+// many independent requests (a burst of plain loads reaches the copy roofline;
+// bulk copies through shared memory do not, for bursts this short, and bulk L2
+// prefetches of the next pairs measured slower than none). The codes are multiplied with
 // the 16-bit fixed-point activations by dp4a. The CTA ends by quantising its
 // SwiGLU outputs into the down kernel's staged form, which the down kernel
 // copies as it is.
 
 constexpr int kGuThreads = 256;
 constexpr int kGuWarps = kGuThreads / 32;
-constexpr int kGuAhead = 3;   // row pairs per warp pulled into L2 ahead of use
 
 // The q16 SwiGLU output block (global, and the down kernel's shared-memory
 // copy of it) for ns slots in row order: runs hq[ns][4][I/32] (uint4), then the
@@ -149,18 +148,9 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
         const int jj = r / I, i = r - jj * I;
         return rec_tab[row_slot_expert(jj, k, E, n_shared, s_ids)] + (size_t)2 * i * rbH;
     };
-    // the first kGuAhead pairs of every warp, then one more per step
-    if (lane == 0)
-        for (int a = 0; a < kGuAhead; ++a) {
-            const int p = warp + a * kGuWarps;
-            if (p < np) prefetch_l2_hint(pair_ptr(p), pair_b, pol);
-        }
     const int M = (HG + 31) / 32;
     for (int p = warp; p < np; p += kGuWarps) {
-        if (lane == 0) {
-            const int pa = p + kGuAhead * kGuWarps;
-            if (pa < np) prefetch_l2_hint(pair_ptr(pa), pair_b, pol);
-        }
+
         const uint8_t* g = pair_ptr(p);
         const uint8_t* u = g + rbH;
         float acc_g = 0.f, acc_u = 0.f;
