@@ -269,8 +269,10 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
     }
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
     __shared__ float s_wts[MOE_MAX_TOP_K];
-    const int own0 = (int)((long long)H * blockIdx.x / gridDim.x);
-    const int own1 = (int)((long long)H * (blockIdx.x + 1) / gridDim.x);
+    // whole quads of rows per CTA (a partial quad costs a full work item)
+    const int nquads_all = (H + kDownRows - 1) / kDownRows;
+    const int own0 = kDownRows * (int)((long long)nquads_all * blockIdx.x / gridDim.x);
+    const int own1 = min(H, kDownRows * (int)((long long)nquads_all * (blockIdx.x + 1) / gridDim.x));
     pdl_wait();     // gate/up complete: the selection it published and the staged SwiGLU outputs are final
     pdl_trigger();  // the next token's router may start prefetching its weights
     ktrace(tr, blockIdx.x, 1);
@@ -406,7 +408,7 @@ cudaError_t decode_kernel_setup(Layer& L) {
     if (e != cudaSuccess) return e;
     if (L.occ_gu < 1 || L.occ_down < 1) return cudaErrorInvalidConfiguration;
     // rows owned by one down CTA must fit its partial-sum buffer
-    while ((H + down_grid(L) - 1) / down_grid(L) > kDownMaxRows) {
+    while (kDownRows * (((H + kDownRows - 1) / kDownRows + down_grid(L) - 1) / down_grid(L)) > kDownMaxRows) {
         if (L.occ_down >= 64) return cudaErrorInvalidConfiguration;
         ++L.occ_down;   // more (smaller) CTAs per SM are launched in waves
     }
