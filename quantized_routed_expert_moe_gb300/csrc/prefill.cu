@@ -455,14 +455,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 float v[16];
                 tmem_ld16(tb + c0, v);
                 if (MODE == 0) {
+                    // lanes 2p and 2p + 1 hold gate and up of pair i for these 16
+                    // tokens; the even lane finishes the even tokens and the odd
+                    // lane the odd ones, after one exchange per token pair
                     const int i = mt * 64 + (row >> 1);
                     const int ip = (i & ~7) | blk_pos(i & 7);
-                    __half* hp = static_cast<__half*>(a.out);
+                    const bool odd = row & 1;
+                    __half* hp = static_cast<__half*>(a.out) + ip;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float up = __shfl_xor_sync(0xffffffffu, v[j], 1);
-                        if (!(row & 1) && c0 + j < m)
-                            hp[(size_t)(off + c0 + j) * a.ld_out + ip] = __float2half_rn(silu_f(v[j]) * up);
+                    for (int q = 0; q < 8; ++q) {
+                        const float got = __shfl_xor_sync(0xffffffffu, odd ? v[2 * q] : v[2 * q + 1], 1);
+                        const float g = odd ? got : v[2 * q], u = odd ? v[2 * q + 1] : got;
+                        const int col = c0 + 2 * q + (odd ? 1 : 0);
+                        // fp16 result: the fast exponential and division are well inside its rounding
+                        const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
+                        if (col < m) hp[(size_t)(off + col) * a.ld_out] = __float2half_rn(h);
                     }
                 } else {
                     const int n = mt * 128 + row;
