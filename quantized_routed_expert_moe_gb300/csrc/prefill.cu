@@ -170,30 +170,35 @@ __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, i
 //
 // Work items are (group g, 128-row weight tile mt). One persistent CTA per SM
 // walks the items; per item it computes D[128 weight rows][N tokens] over K in
-// chunks of 64 (one quantisation group):
-//   * a TMA thread copies the packed codes of 4 chunks (128 rows x 128 B, with
+// chunks of 64 (one quantisation group), 4 chunks (one raw block) at a time:
+//   * a TMA thread copies the packed codes of a block (128 rows x 128 B, with
 //     the 128-byte swizzle so that the dequantisers' reads are conflict-free)
-//     and their (scale, bias) pairs (128 rows x 16 B) into a raw ring, and,
-//     per chunk, the group's token rows of the fp16 activations (N x 128 B,
-//     128-byte swizzle) into a shared-memory operand stage;
-//   * 8 dequantiser warps turn the codes into fp16 w = code * scale + bias (one
-//     fp16 fma: correctly rounded) and store them straight into tensor memory
-//     (tcgen05.st): warp w owns tensor-memory lanes 32 (w % 4) .. + 31 (one
-//     weight row each) and half of the chunk's 64 columns of K. The weight
-//     operand never touches shared memory, which leaves the shared-memory
-//     bandwidth to the token operand and the raw codes;
+//     and their (scale, bias) pairs (128 rows x 16 B) into a raw ring, and the
+//     group's token rows of the fp16 activations for the block's chunks (N x
+//     128 B each, 128-byte swizzle) into a shared-memory operand slot;
+//   * 16 dequantiser warps turn the codes into fp16 w = code * scale + bias
+//     (one fp16 fma: correctly rounded) and store them straight into tensor
+//     memory (tcgen05.st): warp w owns tensor-memory lanes 32 (w % 4) .. + 31
+//     (one weight row each) and a quarter of each chunk's 64 columns of K. The
+//     weight operand never touches shared memory: stores from the SM's threads
+//     into shared memory slow the tensor core's operand reads, copies by the
+//     TMA unit and stores into tensor memory do not;
 //   * one thread issues tcgen05.mma (A from tensor memory, B from shared
-//     memory; M = 128, N = round16(tokens), K = 16) x 4 per chunk into a
+//     memory; M = 128, N = round16(tokens), K = 16), 16 per block, into a
 //     tensor-memory accumulator (two, alternating by item);
 //   * 4 epilogue warps read the accumulator (warp w owns lanes 32w..32w+31) and
 //     write either h = silu(gate) * up in fp16 (gate/up: the weight tile holds
-//     64 interleaved gate/up row pairs, so lane pairs exchange one shuffle) or
-//     the fp32 expert outputs (down).
+//     64 interleaved gate/up row pairs) or the fp32 expert outputs (down).
+// Operand slots change hands a block at a time (one barrier wait and one commit
+// per 16 MMAs): the MMA thread shares its scheduler with four dequantiser warps
+// that keep it busy, and per-chunk hand-offs left the tensor core idle.
 //
 // Tensor memory (512 columns): accumulators at columns 0 and 128; weight
-// operand stages of 32 columns (128 x 64 fp16) from column 256.
+// operand stages of 32 columns (128 x 64 fp16) from column 256, two slots of
+// four.
 
 constexpr int kStages = 8, kRawStages = 4, kChunksPerRaw = 4;
+constexpr int kBatchSlots = kStages / kChunksPerRaw;   // operand stages are handed over a raw block at a time
 constexpr int kEpiWarps = 4, kDqWarps = 16;
 constexpr int kDqParts = kDqWarps / 4;   // K parts of a chunk per tensor-memory lane quarter
 constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
@@ -240,13 +245,25 @@ struct TimedWait {
 // error bits (moe_layer_check): bit 16 + role
 enum { ERR_TMA = 1u << 16, ERR_DQ = 1u << 17, ERR_MMA = 1u << 18, ERR_EPI = 1u << 19, ERR_DRAIN = 1u << 20 };
 
-// fp16 pair from two nibbles placed at bits 0..3 and 16..19 of t: code * s + b
+// fp16 pair from two nibbles placed at bits 0..3 and 16..19 of t: code * s + b.
+// The nibble becomes the low mantissa bits of 1024.0 (unit in the last place 1),
+// so subtracting 1024 leaves the code exactly.
 __device__ __forceinline__ uint32_t dq_pair(uint32_t t, uint32_t s2, uint32_t b2) {
     uint32_t r;
     asm("{.reg .b32 c; lop3.b32 c, %1, 0x000F000F, 0x64006400, 0xEA;"   // (t & mask) | 1024.0
         " sub.f16x2 c, c, %4; fma.rn.f16x2 %0, c, %2, %3;}"
         : "=r"(r)
         : "r"(t), "r"(s2), "r"(b2), "r"(0x64006400u));
+    return r;
+}
+// The same for nibbles at bits 4..7 and 20..23, without a shift: there they are
+// mantissa bits 4..7, which in 64.0 (unit in the last place 1/16) weigh 1 each.
+__device__ __forceinline__ uint32_t dq_pair_hi(uint32_t t, uint32_t s2, uint32_t b2) {
+    uint32_t r;
+    asm("{.reg .b32 c; lop3.b32 c, %1, 0x00F000F0, 0x54005400, 0xEA;"   // (t & mask) | 64.0
+        " sub.f16x2 c, c, %4; fma.rn.f16x2 %0, c, %2, %3;}"
+        : "=r"(r)
+        : "r"(t), "r"(s2), "r"(b2), "r"(0x54005400u));
     return r;
 }
 
@@ -271,7 +288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kBatchSlots; ++s) {
             mbar_init(b_full + 8 * s, kDqWarps + 1);
             mbar_init(b_empty + 8 * s, 1);
         }
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
         }
         __syncwarp();
         const uint64_t pol_w = l2_evict_first(), pol_b = l2_evict_last();
-        uint32_t it = 0, rit = 0;
+        uint32_t rit = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
             const int g = w / a.n_mt, mt = w - g * a.n_mt;
             const int e = a.gexp[g], off = a.goff[g], m = a.gcnt[g];
@@ -326,16 +343,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                     tma_load_3d(rd + kRawCodes, &tm_meta, a.K / 2 + kb * 16, mt * 128, e, b_rfull + 8 * rs, pol_w);
                 }
                 __syncwarp();
-                const int kc1 = min(nk, (kb + 1) * kChunksPerRaw);
-                for (int kc = kb * kChunksPerRaw; kc < kc1; ++kc, ++it) {
-                    const uint32_t s = it % kStages;
-                    tw(b_empty + 8 * s, ((it / kStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
-                    if (elect_one()) {
-                        mbar_arrive_tx(b_full + 8 * s, b_bytes);
-                        tma_load_2d(saddr(bst + s * kB16), tmb, kc * 64, off, b_full + 8 * s, pol_b);
-                    }
-                    __syncwarp();
+                // the block's token tiles, into the operand slot the MMA thread has released
+                const uint32_t bs = rit % kBatchSlots;
+                const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
+                tw(b_empty + 8 * bs, ((rit / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                if (elect_one()) {
+                    mbar_arrive_tx(b_full + 8 * bs, (uint32_t)nc * b_bytes);
+                    for (int c = 0; c < nc; ++c)
+                        tma_load_2d(saddr(bst + (bs * kChunksPerRaw + c) * kB16), tmb, (kc0 + c) * 64, off,
+                                    b_full + 8 * bs, pol_b);
                 }
+                __syncwarp();
             }
         }
         // copies in flight land before the CTA exits (on the normal path the
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
         const int dw = warp - kEpiWarps, q = dw & 3, pt = dw >> 2;
         const int r = 32 * q + lane;
         const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemA + 8 * pt;
-        uint32_t it = 0, rit = 0;
+        uint32_t rit = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
             for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
                 // one raw block (up to 4 chunks) at a time: all of its codes are
@@ -381,34 +399,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                     const uint32_t vw[2] = {cw[c].x, cw[c].y};
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const uint32_t v = vw[j];
+                        const uint32_t v = vw[j], v8 = v >> 8;
                         o[c][4 * j + 0] = dq_pair(v, s2, b2);
-                        o[c][4 * j + 1] = dq_pair(v >> 4, s2, b2);
-                        o[c][4 * j + 2] = dq_pair(v >> 8, s2, b2);
-                        o[c][4 * j + 3] = dq_pair(v >> 12, s2, b2);
+                        o[c][4 * j + 1] = dq_pair_hi(v, s2, b2);
+                        o[c][4 * j + 2] = dq_pair(v8, s2, b2);
+                        o[c][4 * j + 3] = dq_pair_hi(v8, s2, b2);
                     }
                 }
+                const uint32_t bs = rit % kBatchSlots;
+                tw(b_empty + 8 * bs, ((rit / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_DQ);
+                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < kChunksPerRaw; ++c) {
-                    if (c < nc) {
-                        const uint32_t s = (it + c) % kStages;
-                        tw(b_empty + 8 * s, (((it + c) / kStages) & 1) ^ 1, s_abort, a.err, ERR_DQ);
-                        tc_fence_after();
-                        tmem_st8(ta + s * kACols, o[c]);
-                    }
-                }
+                for (int c = 0; c < kChunksPerRaw; ++c)
+                    if (c < nc) tmem_st8(ta + (bs * kChunksPerRaw + c) * kACols, o[c]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    for (int c = 0; c < nc; ++c) mbar_arrive(b_full + 8 * ((it + c) % kStages));
-                it += nc;
+                if (lane == 0) mbar_arrive(b_full + 8 * bs);
             }
         }
         if (dw == 0 && lane == 0) tw.store(1, tw.acc);
     } else if (warp == kMmaWarp) {
         // converged warp; one elected lane issues the MMAs and commits
-        uint32_t it = 0, tile = 0;
+        uint32_t bt = 0, tile = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x, ++tile) {
             const int g = w / a.n_mt;
             const int m = a.gcnt[g];
@@ -418,16 +431,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
             tw(b_aempty + 8 * acc, ((tile >> 1) & 1) ^ 1, s_abort, a.err, ERR_MMA);
             tc_fence_after();
             const uint32_t d_tmem = tmem + acc * 128;
-            for (int kc = 0; kc < nk; ++kc, ++it) {
-                const uint32_t s = it % kStages;
-                tw(b_full + 8 * s, (it / kStages) & 1, s_abort, a.err, ERR_MMA);
+            for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++bt) {
+                // one wait and one commit per block of up to 4 chunks (16 MMAs)
+                const uint32_t bs = bt % kBatchSlots;
+                const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
+                tw(b_full + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);
                 tc_fence_after();
                 if (elect_one()) {
-                    const uint32_t A = tmem + kTmemA + s * kACols, B = saddr(bst + s * kB16);
+                    for (int c = 0; c < nc; ++c) {
+                        const uint32_t A = tmem + kTmemA + (bs * kChunksPerRaw + c) * kACols;
+                        const uint32_t B = saddr(bst + (bs * kChunksPerRaw + c) * kB16);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_f16_ta(d_tmem, A + kk * 8, desc_sw128(B + kk * 32), idesc, (kc | kk) != 0);
-                    mma_commit(b_empty + 8 * s);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16_ta(d_tmem, A + kk * 8, desc_sw128(B + kk * 32), idesc, ((kc0 + c) | kk) != 0);
+                    }
+                    mma_commit(b_empty + 8 * bs);
                 }
                 __syncwarp();
             }
