@@ -171,11 +171,13 @@ __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, i
 // Work items are (group g, 128-row weight tile mt). One persistent CTA per SM
 // walks the items; per item it computes D[128 weight rows][N tokens] over K in
 // chunks of 64 (one quantisation group), 4 chunks (one raw block) at a time:
-//   * a TMA thread copies the packed codes of a block (128 rows x 128 B, with
+//   * one TMA thread copies the packed codes of a block (128 rows x 128 B, with
 //     the 128-byte swizzle so that the dequantisers' reads are conflict-free)
-//     and their (scale, bias) pairs (128 rows x 16 B) into a raw ring, and the
-//     group's token rows of the fp16 activations for the block's chunks (N x
-//     128 B each, 128-byte swizzle) into a shared-memory operand slot;
+//     and their (scale, bias) pairs (128 rows x 16 B) into a raw ring, as far
+//     ahead as the ring allows; another copies the group's token rows of the
+//     fp16 activations for the block's chunks (N x 128 B each, 128-byte
+//     swizzle) into a shared-memory operand slot once the MMA thread has
+//     released it (one thread for both kept the raw ring from running ahead);
 //   * 16 dequantiser warps turn the codes into fp16 w = code * scale + bias
 //     (one fp16 fma: correctly rounded) and store them straight into tensor
 //     memory (tcgen05.st): warp w owns tensor-memory lanes 32 (w % 4) .. + 31
@@ -201,7 +203,7 @@ constexpr int kStages = 8, kRawStages = 4, kChunksPerRaw = 4;
 constexpr int kBatchSlots = kStages / kChunksPerRaw;   // operand stages are handed over a raw block at a time
 constexpr int kEpiWarps = 4, kDqWarps = 16;
 constexpr int kDqParts = kDqWarps / 4;   // K parts of a chunk per tensor-memory lane quarter
-constexpr int kTmaWarp = kEpiWarps + kDqWarps, kMmaWarp = kTmaWarp + 1;
+constexpr int kTmaWarp = kEpiWarps + kDqWarps, kTokWarp = kTmaWarp + 1, kMmaWarp = kTokWarp + 1;
 constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kB16 = 128 * 128;
 constexpr uint32_t kRawCodes = 128 * 128, kRawMeta = 128 * 16, kRaw = kRawCodes + kRawMeta;
@@ -314,25 +316,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     TimedWait tw{a.tr, 0ull};
 
     if (warp == kTmaWarp) {
-        // the whole warp walks the loop (waits included) and one elected lane
-        // issues each copy, so the warp stays converged
+        // raw codes and (scale, bias) pairs, as far ahead as the raw ring allows.
+        // The whole warp walks the loop (waits included) and one elected lane
+        // issues each copy, so the warp stays converged.
         if (elect_one()) {
             tma_prefetch_desc(&tm_codes);
             tma_prefetch_desc(&tm_meta);
-            tma_prefetch_desc(&tm_b16);
-            tma_prefetch_desc(&tm_b32);
-            tma_prefetch_desc(&tm_b64);
-            tma_prefetch_desc(&tm_b128);
         }
         __syncwarp();
-        const uint64_t pol_w = l2_evict_first(), pol_b = l2_evict_last();
+        const uint64_t pol_w = l2_evict_first();
         uint32_t rit = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
             const int g = w / a.n_mt, mt = w - g * a.n_mt;
-            const int e = a.gexp[g], off = a.goff[g], m = a.gcnt[g];
-            // one copy per chunk: the smallest box of 16, 32, 64 or 128 token rows that holds the group
-            const CUtensorMap* tmb = m <= 16 ? &tm_b16 : m <= 32 ? &tm_b32 : m <= 64 ? &tm_b64 : &tm_b128;
-            const uint32_t b_bytes = (m <= 16 ? 16u : m <= 32 ? 32u : m <= 64 ? 64u : 128u) * 128u;
+            const int e = a.gexp[g];
             for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
                 const uint32_t rs = rit % kRawStages;
                 tw(b_rempty + 8 * rs, ((rit / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
@@ -341,17 +337,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                     const uint32_t rd = saddr(raw + rs * kRaw);
                     tma_load_3d(rd, &tm_codes, kb * 128, mt * 128, e, b_rfull + 8 * rs, pol_w);
                     tma_load_3d(rd + kRawCodes, &tm_meta, a.K / 2 + kb * 16, mt * 128, e, b_rfull + 8 * rs, pol_w);
-                }
-                __syncwarp();
-                // the block's token tiles, into the operand slot the MMA thread has released
-                const uint32_t bs = rit % kBatchSlots;
-                const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
-                tw(b_empty + 8 * bs, ((rit / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_TMA);
-                if (elect_one()) {
-                    mbar_arrive_tx(b_full + 8 * bs, (uint32_t)nc * b_bytes);
-                    for (int c = 0; c < nc; ++c)
-                        tma_load_2d(saddr(bst + (bs * kChunksPerRaw + c) * kB16), tmb, (kc0 + c) * 64, off,
-                                    b_full + 8 * bs, pol_b);
                 }
                 __syncwarp();
             }
@@ -364,6 +349,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
             mbar_wait(b_rfull + 8 * (q % kRawStages), (q / kRawStages) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
         }
         if (lane == 0) tw.store(0, tw.acc);
+    } else if (warp == kTokWarp) {
+        // the group's token tiles of a block, into the operand slot the MMA thread has released
+        if (elect_one()) {
+            tma_prefetch_desc(&tm_b16);
+            tma_prefetch_desc(&tm_b32);
+            tma_prefetch_desc(&tm_b64);
+            tma_prefetch_desc(&tm_b128);
+        }
+        __syncwarp();
+        const uint64_t pol_b = l2_evict_last();
+        uint32_t bt = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+            const int g = w / a.n_mt;
+            const int off = a.goff[g], m = a.gcnt[g];
+            // one copy per chunk: the smallest box of 16, 32, 64 or 128 token rows that holds the group
+            const CUtensorMap* tmb = m <= 16 ? &tm_b16 : m <= 32 ? &tm_b32 : m <= 64 ? &tm_b64 : &tm_b128;
+            const uint32_t b_bytes = (m <= 16 ? 16u : m <= 32 ? 32u : m <= 64 ? 64u : 128u) * 128u;
+            for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++bt) {
+                const uint32_t bs = bt % kBatchSlots;
+                const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
+                tw(b_empty + 8 * bs, ((bt / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                if (elect_one()) {
+                    mbar_arrive_tx(b_full + 8 * bs, (uint32_t)nc * b_bytes);
+                    for (int c = 0; c < nc; ++c)
+                        tma_load_2d(saddr(bst + (bs * kChunksPerRaw + c) * kB16), tmb, (kc0 + c) * 64, off,
+                                    b_full + 8 * bs, pol_b);
+                }
+                __syncwarp();
+            }
+        }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
         // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows) and
         // part pt of each chunk's K (16 elements: columns 8 pt .. 8 pt + 7)
