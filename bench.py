@@ -625,6 +625,57 @@ def main():
             a, b = prof.get(name, (0, 0.0))
             prof[name] = (a + n, b + t)
 
+    # per-token intervals: one step again with an event after every token. The
+    # events sit between consecutive tokens' kernels (they block the overlap of
+    # the next token's router prologue with this token's tail), so these are an
+    # upper bound on the per-token time of the timed region.
+    tev = [torch.cuda.Event(enable_timing=True) for _ in range(T + 1)]
+    torch.cuda.synchronize()
+    tev[0].record(stream)
+    for t in range(T):
+        st = dec(handles[t % R], xb + t * row, yb + t * row, None, sp)
+        if st:
+            raise moe.MoEError(st, "moe_decode", moe.moe_last_error())
+        tev[t + 1].record(stream)
+    torch.cuda.synchronize()
+    lat = np.array([tev[t].elapsed_time(tev[t + 1]) * 1e3 for t in range(T)])
+    latency = {"p50": float(np.percentile(lat, 50)), "p95": float(np.percentile(lat, 95)),
+               "p99": float(np.percentile(lat, 99)), "max": float(lat.max()), "unit": "us",
+               "note": "interval between events recorded after consecutive tokens of one step"}
+
+    # the same step captured once into a CUDA graph and replayed K times
+    graph = None
+    try:
+        gstream = torch.cuda.Stream()
+        gstream.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gstream):
+            gsp = gstream.cuda_stream
+            step_g = lambda: [dec(handles[t % R], xb + t * row, yb + t * row, None, gsp) for t in range(T)]
+            step_g()   # untimed warm-up on the capture stream
+            gstream.synchronize()
+            with torch.cuda.graph(g, stream=gstream):
+                codes = step_g()
+        if any(codes):
+            raise RuntimeError(f"moe_decode returned {max(codes)} during capture")
+        stream.wait_stream(gstream)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        gev0, gev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gev0.record(torch.cuda.current_stream())
+        for _ in range(args.steps):
+            g.replay()
+        gev1.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        gms = gev0.elapsed_time(gev1)
+        graph = {"value": T * args.steps / (gms / 1e3), "unit": UNIT, "ms_per_step": gms / args.steps,
+                 "note": "one step (T decodes, rotating replicas) captured once, replayed K times"}
+        del g
+    except Exception as exc:   # reported, not fatal: the plain timed region above is the headline
+        graph = {"error": str(exc).splitlines()[0][:200]}
+        torch.cuda.synchronize()
+
     # end to end through the C ABI with HOST buffers: moe_decode_tokens_host
     # copies the step's inputs from pinned host memory, decodes the T tokens and
     # copies the outputs back, then waits for its stream (one layer instance,
@@ -698,6 +749,8 @@ def main():
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
         "gpu_launches": launches,
+        "per_token_latency": latency,
+        "graph": graph,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
