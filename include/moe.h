@@ -123,8 +123,10 @@ typedef struct {
 
 /* Create a layer on CUDA device `device`.
  *   router:       host, required. Copied and repacked; the caller may free it after.
- *   router_bias:  host fp32 [E] or NULL. Added to the logits before selection
- *                 and before the softmax.
+ *   router_bias:  host fp32 [E] or NULL. With softmax scoring (the default)
+ *                 it is added to the logits before selection and before the
+ *                 softmax; with sigmoid scoring (moe_layer_set_router_scoring)
+ *                 it is added to the sigmoid scores for the selection only.
  *   shared:       host, required iff n_shared == 1.
  *   experts:      host array of E experts, required when cache_slots == 0
  *                 (copied, repacked into the kernel layout in device memory).
@@ -158,13 +160,45 @@ moe_status moe_pack_expert_record(const moe_layer_desc* desc, const moe_expert* 
 /* Device bytes the layer holds (weights + slots + scratch). */
 size_t moe_layer_device_bytes(const moe_layer* layer);
 
+/* ---- router scoring ---------------------------------------------------------- */
+
+/* How router logits become a selection and routing weights. */
+enum {
+    /* softmax top-k (the default): key_e = l_e + bias_e; the k largest keys
+     * (ties to the lower index) are selected and weighted by the softmax of
+     * their keys, renormalised over the selection. */
+    MOE_SCORE_SOFTMAX = 0,
+    /* sigmoid top-k, the DeepSeek-V3-style router of the Colibri README
+     * ("What's implemented": sigmoid router, noaux_tc,
+     * routed_scaling_factor): s_e = 1 / (1 + exp(-l_e)); key_e = s_e + bias_e,
+     * the bias steering the selection only; the k largest keys (ties to the
+     * lower index, all experts in one group) are selected and weighted by
+     * w_j = routed_scaling * s_j / sum over the selection of s. */
+    MOE_SCORE_SIGMOID = 1
+};
+
+/* Set the layer's router scoring (default MOE_SCORE_SOFTMAX, scaling 1).
+ * routed_scaling must be finite and positive; it multiplies the sigmoid
+ * weights and is ignored for softmax. The layer's router_bias (moe_layer_create)
+ * is the bias_e above. Applies to every later moe_route, moe_decode,
+ * moe_decode_static_scratch and moe_prefill_chunk call; set it before the
+ * first of them (the call does not wait for work in flight). The fused decode
+ * path supports softmax only: with MOE_SCORE_SIGMOID the layer runs the split
+ * path, and setting MOE_OPT_DECODE_PATH to MOE_PATH_FUSED afterwards returns
+ * MOE_E_UNSUPPORTED (as does this call, with MOE_SCORE_SIGMOID, while the
+ * fused path is selected). Errors: MOE_E_INVALID for a NULL layer, an unknown
+ * scoring or a bad routed_scaling. */
+moe_status moe_layer_set_router_scoring(moe_layer* layer, int32_t scoring, float routed_scaling);
+
 /* ---- compute --------------------------------------------------------------- */
 
 /* Router only, for T tokens (1 <= T <= max_tokens).
  *   x:   device [T][H] of act_dtype.
- *   ids: device int32 [T][top_k], selection order (descending logit, ties to lower index).
- *   w:   device fp32 [T][top_k], softmax over the selected logits.
- * Router GEMV/GEMM with fp32 accumulation; top-k and softmax in fp32. */
+ *   ids: device int32 [T][top_k], selection order (descending key, ties to lower index).
+ *   w:   device fp32 [T][top_k], the routing weights of the layer's scoring
+ *        (moe_layer_set_router_scoring): softmax over the selected keys, or the
+ *        scaled, renormalised sigmoid scores.
+ * Router GEMV/GEMM with fp32 accumulation; selection and weights in fp32. */
 moe_status moe_route(moe_layer* layer, const void* x, int32_t T, int32_t* ids, float* w, void* stream);
 
 /* One decode token.

@@ -9,11 +9,12 @@ Every function states the passage of the pages it follows. The pages are:
   * "Colibri" analysis report -- section 2 "Exact Architecture and Data-Flow
     Reconstruction" (Route / Union / Place / Overlap) and section 3 (exact
     routing);
-  * Colibri README -- "What's implemented" (batch-union MoE, dequant-on-use).
+  * Colibri README -- "What's implemented" (batch-union MoE, dequant-on-use,
+    the DeepSeek-V3-style sigmoid router).
 
 What the pages leave open is filled with the plainest reading, recorded where
 it is used (nibble order, softmax renormalised over the selected experts,
-ties to the lower index, LFU details).
+ties to the lower index, LFU details, the sigmoid router's bias and scaling).
 
 Everything here is computed in float64 with numpy; no blocking, fusion or
 reordering beyond the definitions. Parity status: every function below is
@@ -136,6 +137,65 @@ def routing_weights(l_sel: np.ndarray) -> np.ndarray:
     return e / e.sum()
 
 
+def sigmoid_scores(l: np.ndarray) -> np.ndarray:
+    """s_e = 1 / (1 + exp(-l_e)), in float64.
+
+    Colibri README, "What's implemented": the model's router is a
+    DeepSeek-V3-style sigmoid router (noaux_tc, routed_scaling_factor). The
+    pages name it only; the reading used here: each expert's score is the
+    logistic function of its logit.
+    """
+    return 1.0 / (1.0 + np.exp(-np.asarray(l, dtype=np.float64)))
+
+
+def sigmoid_keys(s: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
+    """Selection keys of the sigmoid router: key_e = s_e + bias_e.
+
+    Reading of "noaux_tc" (Colibri README, "What's implemented"): the
+    per-expert bias steers which experts are selected and takes no part in the
+    routing weights; all experts form one group.
+    """
+    key = np.asarray(s, dtype=np.float64).copy()
+    if bias is not None:
+        key = key + np.asarray(bias, dtype=np.float32).astype(np.float64)
+    return key
+
+
+def routing_weights_sigmoid(s_sel: np.ndarray, routed_scaling: float) -> np.ndarray:
+    """w_j = routed_scaling * s_j / sum_j' s_j' over the selected experts.
+
+    Colibri README, "What's implemented" (routed_scaling_factor). Reading: the
+    selected sigmoid scores (without the bias) are renormalised to sum to one
+    and then multiplied by the scaling factor.
+    """
+    s_sel = np.asarray(s_sel, dtype=np.float64)
+    return float(routed_scaling) * s_sel / s_sel.sum()
+
+
+def route_keys(layer, l: np.ndarray) -> tuple[np.ndarray, np.ndarray | None]:
+    """(selection keys, sigmoid scores or None) for the layer's router scoring.
+
+    softmax scoring: the keys are the logits with the bias already added by
+    ``router_logits``. sigmoid scoring: ``l`` must be the unbiased logits.
+    """
+    if getattr(layer.spec, "router_score", "softmax") == "sigmoid":
+        sc = sigmoid_scores(l)
+        return sigmoid_keys(sc, layer.router_bias), sc
+    return np.asarray(l, dtype=np.float64), None
+
+
+def _weights(layer, key: np.ndarray, sc: np.ndarray | None, ids: np.ndarray) -> np.ndarray:
+    if sc is None:
+        return routing_weights(key[ids])
+    return routing_weights_sigmoid(sc[ids], layer.spec.routed_scaling)
+
+
+def _logits(layer, Wr: np.ndarray, x64: np.ndarray) -> np.ndarray:
+    """The router logits: biased for softmax scoring, unbiased for sigmoid."""
+    sigmoid = getattr(layer.spec, "router_score", "softmax") == "sigmoid"
+    return router_logits(Wr, x64, None if sigmoid else layer.router_bias)
+
+
 # ---------------------------------------------------------------------------
 # expert FFN and the layer
 # ---------------------------------------------------------------------------
@@ -175,11 +235,13 @@ def _x_f64(layer, x) -> np.ndarray:
 
 
 def route_token(layer, x64: np.ndarray, Wr: np.ndarray | None = None) -> RouteInfo:
+    """Selection and weights of one token under the layer's router scoring
+    (gap: between the k-th and (k+1)-th selection keys)."""
     if Wr is None:
         Wr = router_weights_f64(layer.router)
-    l = router_logits(Wr, x64, layer.router_bias)
-    ids, gap = select_topk(l, layer.spec.top_k)
-    w = routing_weights(l[ids])
+    key, sc = route_keys(layer, _logits(layer, Wr, x64))
+    ids, gap = select_topk(key, layer.spec.top_k)
+    w = _weights(layer, key, sc, ids)
     scale = float(np.max(np.abs(Wr * x64[None, :]).sum(axis=1)))
     return RouteInfo(ids, w, gap, scale)
 
@@ -193,7 +255,8 @@ def moe_token(layer, x, ids: np.ndarray | None = None, Wr: np.ndarray | None = N
     section 2: Route, then the experts. The shared expert is unweighted.
 
     ``ids`` overrides the selection (used when the GPU's fp32 logits resolve a
-    near-tie the other way; the weights are then the softmax over those ids).
+    near-tie the other way; the weights are then those of the layer's scoring
+    over those ids).
     Returns (y float64 [H], RouteInfo).
     """
     x64 = _x_f64(layer, x)
@@ -201,9 +264,9 @@ def moe_token(layer, x, ids: np.ndarray | None = None, Wr: np.ndarray | None = N
         Wr = router_weights_f64(layer.router)
     info = route_token(layer, x64, Wr)
     if ids is not None:
-        l = router_logits(Wr, x64, layer.router_bias)
+        key, sc = route_keys(layer, _logits(layer, Wr, x64))
         ids = np.asarray(ids, dtype=np.int64)
-        info = RouteInfo(ids, routing_weights(l[ids]), info.gap, info.scale)
+        info = RouteInfo(ids, _weights(layer, key, sc, ids), info.gap, info.scale)
     y = np.zeros(layer.spec.hidden, dtype=np.float64)
     if layer.shared is not None:
         y += expert_ffn(layer.shared, x64)

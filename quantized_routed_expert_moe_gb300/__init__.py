@@ -26,12 +26,13 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
-           "moe_layer_device_bytes", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
+           "moe_layer_device_bytes", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
            "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency", "moe_lfu_trace",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
 MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_STATIC_SCRATCH_BYTES = 256 * 1024
 MOE_OPT_DECODE_PATH, MOE_OPT_TEST_STALL_ROUTING, MOE_OPT_TRACE = 1, 2, 3
 MOE_OPT_HOST_TIMEOUT_MS, MOE_OPT_TEST_STALL_COPIES_MS = 4, 5
@@ -128,6 +129,8 @@ def lib() -> ctypes.CDLL:
             L.moe_profile_stop.argtypes = [vp, ctypes.POINTER(moe_kernel_time), i32, ctypes.POINTER(i32)]
             L.moe_layer_set_option.restype = st
             L.moe_layer_set_option.argtypes = [vp, i32, ctypes.c_int64]
+            L.moe_layer_set_router_scoring.restype = st
+            L.moe_layer_set_router_scoring.argtypes = [vp, i32, ctypes.c_float]
             L.moe_layer_check.restype = st
             L.moe_layer_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             L.moe_trace_read.restype = st
@@ -318,6 +321,10 @@ def moe_layer_set_option(handle, option: int, value: int) -> None:
     _check(lib().moe_layer_set_option(handle, option, value), "moe_layer_set_option")
 
 
+def moe_layer_set_router_scoring(handle, scoring: int, routed_scaling: float = 1.0) -> None:
+    _check(lib().moe_layer_set_router_scoring(handle, scoring, routed_scaling), "moe_layer_set_router_scoring")
+
+
 def moe_layer_check(handle) -> tuple[int, int]:
     """(status, error bits) of device-side bounded waits since the last check."""
     bits = ctypes.c_uint32()
@@ -367,6 +374,8 @@ class MoELayer:
         self.handle = moe_layer_create(self.desc, layer.router, layer.router_bias, layer.shared,
                                        None if cache_slots else layer.experts, records=records,
                                        source=source, device=device)
+        if getattr(layer.spec, "router_score", "softmax") == "sigmoid":
+            moe_layer_set_router_scoring(self.handle, MOE_SCORE_SIGMOID, layer.spec.routed_scaling)
 
     def close(self):
         if getattr(self, "handle", None):
@@ -411,6 +420,9 @@ class MoELayer:
 
     def set_option(self, option, value):
         moe_layer_set_option(self.handle, option, value)
+
+    def set_router_scoring(self, scoring, routed_scaling=1.0):
+        moe_layer_set_router_scoring(self.handle, scoring, routed_scaling)
 
     def check(self):
         return moe_layer_check(self.handle)

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "moe.h"
+#include "route_mode.h"
 
 namespace moe {
 
@@ -297,12 +298,26 @@ __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
     }
 }
 
+// Selection key of one expert from its logit l and bias b (b = 0 without a
+// bias). softmax: the biased logit. sigmoid (DeepSeek-V3-style router of the
+// Colibri README, "What's implemented"): the score s = 1 / (1 + e^-l), written
+// to *score, plus the bias, which steers the selection only.
+__device__ __forceinline__ float route_key(float l, float b, RouteMode m, float* score) {
+    if (!m.sigmoid) return l + b;
+    const float sc = 1.0f / (1.0f + expf(-l));
+    *score = sc;
+    return sc + b;
+}
+
 // Two stages without block-wide rounds: every warp selects the top k of its
 // contiguous range of experts (k rounds of a warp argmax), then warp 0 selects
 // the top k of the <= 8 * k candidates. The union of the per-range top-k holds
 // the global top-k, so the result is the same selection. E <= 1024, at least
 // 8 warps (warps beyond the eighth only join the barriers).
-__device__ __forceinline__ void block_topk_softmax(const float* sl, int E, int k, int32_t* ids_out, float* w_out) {
+// Weights: the softmax over the selected keys, or, when `score` is given
+// (sigmoid scoring), scale * score_j / sum over the selection of score.
+__device__ __forceinline__ void block_topk_softmax(const float* sl, int E, int k, int32_t* ids_out, float* w_out,
+                                                   const float* score = nullptr, float scale = 1.0f) {
     __shared__ float c_v[8 * MOE_MAX_TOP_K];
     __shared__ int c_i[8 * MOE_MAX_TOP_K];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -363,24 +378,31 @@ __device__ __forceinline__ void block_topk_softmax(const float* sl, int E, int k
                 if (cl[m] && ci[m] == bi) cl[m] = false;
         }
         if (lane == 0) {
-            // softmax over the selected logits; the first selected is the maximum
+            // softmax over the selected keys (the first selected is the
+            // maximum), or the selected sigmoid scores renormalised and scaled
             float ex[MOE_MAX_TOP_K], den = 0.f;
 #pragma unroll
             for (int r = 0; r < MOE_MAX_TOP_K; ++r)
-                if (r < k) { ex[r] = expf(sel_l[r] - sel_l[0]); den += ex[r]; }
+                if (r < k) {
+                    ex[r] = score ? score[sel_i[r]] : expf(sel_l[r] - sel_l[0]);
+                    den += ex[r];
+                }
+            const float mul = score ? scale : 1.0f;
 #pragma unroll
             for (int r = 0; r < MOE_MAX_TOP_K; ++r)
-                if (r < k) { ids_out[r] = sel_i[r]; w_out[r] = ex[r] / den; }
+                if (r < k) { ids_out[r] = sel_i[r]; w_out[r] = ex[r] / den * mul; }
         }
     }
 }
 
 
 // Sum the router's partial logits part[s][e] (s < splits <= 8, fixed order),
-// add the bias, and select: logits into sl[E] (shared), ids / weights into
-// ids_out / w_out (shared or global). All 256 threads; E <= 1024.
+// apply the layer's scoring and bias, and select: selection keys into sl[E]
+// and, for sigmoid scoring, the scores into ss[E] (both shared), ids /
+// weights into ids_out / w_out (shared or global). All 256 threads; E <= 1024.
 __device__ __forceinline__ void block_select(const float* part, int splits, int E, const float* bias, int k,
-                                             float* sl, int32_t* ids_out, float* w_out) {
+                                             float* sl, int32_t* ids_out, float* w_out, RouteMode mode,
+                                             float* ss) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float v[8];
 #pragma unroll
@@ -388,11 +410,10 @@ __device__ __forceinline__ void block_select(const float* part, int splits, int 
         float l = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s) l += v[s];
-        if (bias) l += __ldg(bias + e);
-        sl[e] = l;
+        sl[e] = route_key(l, bias ? __ldg(bias + e) : 0.f, mode, ss + e);
     }
     __syncthreads();
-    block_topk_softmax(sl, E, k, ids_out, w_out);
+    block_topk_softmax(sl, E, k, ids_out, w_out, mode.sigmoid ? ss : nullptr, mode.scale);
     __syncthreads();
 }
 

@@ -103,9 +103,10 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
                                                          int32_t* __restrict__ ids_out, float* __restrict__ wts_out,
                                                          float* __restrict__ logits_out,
                                                          const int32_t* __restrict__ sel_ids, int jj0, int jj1,
-                                                         unsigned long long* __restrict__ tr) {
+                                                         RouteMode mode, unsigned long long* __restrict__ tr) {
     extern __shared__ uint4 smq[];
     __shared__ float s_logit[1024];
+    __shared__ float s_score[1024];
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
     __shared__ float s_wts[MOE_MAX_TOP_K];
     const int HG = H / 32, IG = I / 32, ns = k + n_shared;
@@ -131,7 +132,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
     } else {
         // every CTA reduces the router's partial logits and selects (same result
         // everywhere); no CTA has to wait for a single selecting CTA
-        block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts);
+        block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts, mode, s_score);
         if (blockIdx.x == 0) {   // publish the selection (read by the host and by later calls)
             for (int e = threadIdx.x; e < E; e += blockDim.x) logits_out[e] = s_logit[e];
             if (threadIdx.x < k) { ids_out[threadIdx.x] = s_ids[threadIdx.x]; wts_out[threadIdx.x] = s_wts[threadIdx.x]; }
@@ -426,7 +427,8 @@ static cudaError_t launch_gateup(Layer& L, const void* x, const float* part, voi
     return launch_pdl(k_gateup, dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s, pdl,
                       (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias, d.top_k,
                       d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
-                      row_bytes(d.hidden), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1, tr);
+                      row_bytes(d.hidden), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1,
+                      L.route_mode(), tr);
 }
 
 static cudaError_t launch_down(Layer& L, const float* part, const void* hblk, int copies, void* y, float* y_f32,

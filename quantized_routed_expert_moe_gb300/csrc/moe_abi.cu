@@ -1,6 +1,7 @@
 // C ABI entry points: layer lifetime, argument checks, scratch, dispatch.
 #include <algorithm>
 #include <chrono>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -419,6 +420,19 @@ moe_status moe_decode_tokens_host(moe_layer* layer, const void* x_host, int32_t 
     return MOE_OK;
 }
 
+moe_status moe_layer_set_router_scoring(moe_layer* layer, int32_t scoring, float routed_scaling) {
+    if (!layer) return fail(MOE_E_INVALID, "NULL layer");
+    Layer& L = layer->L;
+    if (scoring != MOE_SCORE_SOFTMAX && scoring != MOE_SCORE_SIGMOID) return fail(MOE_E_INVALID, "unknown router scoring");
+    if (!(routed_scaling > 0.0f) || !std::isfinite(routed_scaling))
+        return fail(MOE_E_INVALID, "routed_scaling must be finite and positive");
+    if (scoring == MOE_SCORE_SIGMOID && L.decode_path == MOE_PATH_FUSED)
+        return fail(MOE_E_UNSUPPORTED, "the fused decode supports softmax router scoring only");
+    L.router_scoring = scoring;
+    L.routed_scaling = routed_scaling;
+    return MOE_OK;
+}
+
 moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value) {
     if (!layer) return fail(MOE_E_INVALID, "NULL layer");
     Layer& L = layer->L;
@@ -428,6 +442,8 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
                 return fail(MOE_E_INVALID, "unknown decode path");
             if (value == MOE_PATH_FUSED && !L.fused_ok)
                 return fail(MOE_E_UNSUPPORTED, "the fused decode does not support this layer's shape or mode");
+            if (value == MOE_PATH_FUSED && L.router_scoring != MOE_SCORE_SOFTMAX)
+                return fail(MOE_E_UNSUPPORTED, "the fused decode supports softmax router scoring only");
             L.decode_path = (int)value;
             return MOE_OK;
         case MOE_OPT_TEST_STALL_ROUTING:

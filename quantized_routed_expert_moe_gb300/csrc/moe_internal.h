@@ -10,6 +10,7 @@
 #include <cuda.h>
 
 #include "moe.h"
+#include "route_mode.h"
 
 namespace moe {
 
@@ -117,6 +118,9 @@ struct Layer {
     // router
     void* router = nullptr;         // fp32 [E][H], or 8-bit codes + meta
     float* router_bias = nullptr;   // fp32 [E] or null
+    int router_scoring = MOE_SCORE_SOFTMAX;   // moe_layer_set_router_scoring
+    float routed_scaling = 1.0f;
+    RouteMode route_mode() const { return RouteMode{router_scoring == MOE_SCORE_SIGMOID ? 1 : 0, routed_scaling}; }
 
     // experts (resident mode): (E + n_shared) records; the shared expert is index E
     uint8_t* experts = nullptr;

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     const void* __restrict__ W, const void* __restrict__ x, int x_bf16, int H, int E, int splits,
     const float* __restrict__ bias, float* __restrict__ part, float* __restrict__ logits,
     int32_t* __restrict__ ids, float* __restrict__ wts, int k, unsigned* __restrict__ counter,
-    int select, unsigned long long* __restrict__ tr) {
+    int select, RouteMode mode, unsigned long long* __restrict__ tr) {
     extern __shared__ float sm[];
     __shared__ unsigned s_last;
     const int cta = blockIdx.y * gridDim.x + blockIdx.x;
@@ -146,12 +146,13 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
         float l = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s) l += v[s];
-        if (bias) l += bias[e2];
-        sm[e2] = l;
-        logits[e2] = l;
+        // keys in sm[0, E), sigmoid scores in sm[E, 2E)
+        const float key = route_key(l, bias ? bias[e2] : 0.f, mode, sm + E + e2);
+        sm[e2] = key;
+        logits[e2] = key;
     }
     __syncthreads();
-    block_topk_softmax(sm, E, k, ids, wts);
+    block_topk_softmax(sm, E, k, ids, wts, mode.sigmoid ? sm + E : nullptr, mode.scale);
     if (threadIdx.x == 0) *counter = 0u;
     __syncthreads();
     ktrace(tr, cta, 3);
@@ -237,8 +238,9 @@ __global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restri
 
 __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restrict__ part, int splits, int T, int E,
                                                           const float* __restrict__ bias, float* __restrict__ logits,
-                                                          int32_t* __restrict__ ids, float* __restrict__ wts, int k) {
-    extern __shared__ float sl[];
+                                                          int32_t* __restrict__ ids, float* __restrict__ wts, int k,
+                                                          RouteMode mode) {
+    extern __shared__ float sl[];   // keys [E], then sigmoid scores [E]
     const int t = blockIdx.x;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float v[16];
@@ -247,12 +249,13 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
         float l = 0.f;
 #pragma unroll
         for (int s = 0; s < 16; ++s) l += v[s];
-        if (bias) l += bias[e];
-        sl[e] = l;
-        logits[(size_t)t * E + e] = l;
+        const float key = route_key(l, bias ? bias[e] : 0.f, mode, sl + E + e);
+        sl[e] = key;
+        logits[(size_t)t * E + e] = key;
     }
     __syncthreads();
-    block_topk_softmax(sl, E, k, ids + (size_t)t * k, wts + (size_t)t * k);
+    block_topk_softmax(sl, E, k, ids + (size_t)t * k, wts + (size_t)t * k, mode.sigmoid ? sl + E : nullptr,
+                       mode.scale);
 }
 
 // ---------------------------------------------------------------------------
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
 // ---------------------------------------------------------------------------
 
 static size_t router_smem(const Layer& L) {
-    return (size_t)std::max(L.d.hidden / L.router_splits, L.d.n_experts) * 4;
+    return (size_t)std::max(L.d.hidden / L.router_splits, 2 * L.d.n_experts) * 4;   // x slice, or keys + scores
 }
 
 cudaError_t router_kernel_setup(Layer& L) {
@@ -269,7 +272,7 @@ cudaError_t router_kernel_setup(Layer& L) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_router_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)router_smem(L));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_topk_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, L.d.n_experts * 4);
+    return cudaFuncSetAttribute(k_topk_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * L.d.n_experts * 4);
 }
 
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select) {
@@ -281,11 +284,11 @@ cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int sel
     if (d.router_fmt == MOE_W_F32)
         e = launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                        d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.split_trace(0));
+                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), L.split_trace(0));
     else
         e = launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                        d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.split_trace(0));
+                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), L.split_trace(0));
     prof_end(L, s);
     return e;
 }
@@ -299,11 +302,11 @@ cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, c
     if (d.router_fmt == MOE_W_F32)
         return launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                           d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
-                          (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0,
+                          (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
                           (unsigned long long*)nullptr);
     return launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
-                      (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0,
+                      (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
                       (unsigned long long*)nullptr);
 }
 
@@ -324,8 +327,8 @@ cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     prof_begin(L, K_TOPK_TOKENS, s);
-    k_topk_tokens<<<T, kThreads, d.n_experts * 4, s>>>(L.logits_part, splits, T, d.n_experts, L.router_bias,
-                                                       L.logits, L.ids, L.wts, d.top_k);
+    k_topk_tokens<<<T, kThreads, 2 * d.n_experts * 4, s>>>(L.logits_part, splits, T, d.n_experts, L.router_bias,
+                                                           L.logits, L.ids, L.wts, d.top_k, L.route_mode());
     prof_end(L, s);
     return cudaGetLastError();
 }

@@ -39,6 +39,7 @@ TAG_EXPERT_CODES = 2
 TAG_EXPERT_SCALE = 3
 TAG_TOKENS = 4
 TAG_BIAS_PERM = 5
+TAG_SCORE_BIAS = 6
 
 MAT_GATE, MAT_UP, MAT_DOWN = 0, 1, 2
 
@@ -209,6 +210,9 @@ class LayerSpec:
     act: str = "bf16"             # "bf16" | "f32"
     zipf_alpha: float | None = None   # router bias from skewed popularity
     router_sd: float = 0.02
+    router_score: str = "softmax"     # "softmax" | "sigmoid"
+    routed_scaling: float = 1.0       # sigmoid scoring: multiplies the routing weights
+    score_bias_sd: float | None = None   # sigmoid scoring: selection bias N(0, sd) per expert
 
     def expert_bytes(self) -> int:
         """Canonical bytes of one 4-bit group-64 expert: 3*H*I*(1/2 + 4/64)."""
@@ -247,7 +251,10 @@ def gen_router(seed: int, layer: int, spec: LayerSpec) -> Router:
 
 
 def gen_router_bias(seed: int, layer: int, spec: LayerSpec) -> np.ndarray | None:
-    """ln p_e with p_e proportional to rank_e ** -alpha (rank a seeded permutation of 1..E)."""
+    """ln p_e with p_e proportional to rank_e ** -alpha (rank a seeded permutation of 1..E);
+    with sigmoid scoring and score_bias_sd, a seeded N(0, sd) bias per expert instead."""
+    if spec.router_score == "sigmoid" and spec.score_bias_sd is not None:
+        return normal_f32(key(seed, TAG_SCORE_BIAS, layer), spec.n_experts, spec.score_bias_sd)
     if spec.zipf_alpha is None:
         return None
     E = spec.n_experts

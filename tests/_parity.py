@@ -8,7 +8,11 @@ Tolerances:
     for validity and the output is compared with the oracle run on the GPU's
     selection. TAU = 2^-16 bounds the fp32 summation error of the router
     (< 200 sequential fp32 additions per partial sum, each within 2^-24).
-  * routing weights: absolute 1e-5 (fp32 softmax of fp32 logits).
+    With sigmoid scoring the keys are s + bias: a key moves by at most a
+    quarter of its logit's error plus SIGMOID_EPS = 2^-20 for the fp32
+    exponential, division and addition.
+  * routing weights: absolute 1e-5 (fp32 softmax of fp32 logits, or fp32
+    sigmoid scores renormalised and scaled).
   * layer output: max_i |y_i - yhat_i| / max_i |yhat_i| <= 2e-3 per token on
     the fp32 output, and the bf16 output equals the fp32 output rounded to
     nearest even.
@@ -20,6 +24,7 @@ import numpy as np
 import oracle
 
 TAU = 2.0 ** -16
+SIGMOID_EPS = 2.0 ** -20
 REL_TOL = 2e-3
 W_TOL = 1e-5
 
@@ -35,13 +40,17 @@ def check_selection(layer, x, ids_gpu, Wr=None):
     if Wr is None:
         Wr = oracle.router_weights_f64(layer.router)
     x64 = oracle.moe._x_f64(layer, x)
-    l = oracle.router_logits(Wr, x64, layer.router_bias)
+    sigmoid = getattr(layer.spec, "router_score", "softmax") == "sigmoid"
+    # selection keys: biased logits, or sigmoid scores plus the bias
+    l, _ = oracle.route_keys(layer, oracle.moe._logits(layer, Wr, x64))
     k = layer.spec.top_k
     ids_o, _ = oracle.select_topk(l, k)
     sigma = float(np.max(np.abs(Wr * x64[None, :]).sum(axis=1)))
-    if layer.router_bias is not None:
+    if layer.router_bias is not None and not sigmoid:
         sigma += float(np.max(np.abs(layer.router_bias)))
-    tau = TAU * sigma
+    # a sigmoid key moves by at most 1/4 of its logit's error, plus the fp32
+    # rounding of the exponential, the division and the bias addition
+    tau = TAU * sigma * 0.25 + SIGMOID_EPS if sigmoid else TAU * sigma
     ids_g = [int(v) for v in ids_gpu]
     if ids_g == [int(v) for v in ids_o]:
         return ids_o, False

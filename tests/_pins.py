@@ -282,12 +282,18 @@ def _py_layer(layer, x):
         R = [[int(q.codes[e, i]) * f16(q.scale[e, i // 64]) + f16(q.bias[e, i // 64])
               for i in range(H)] for e in range(E)]
     l = [sum(R[e][i] * xv[i] for i in range(H)) for e in range(E)]
-    if layer.router_bias is not None:
-        l = [l[e] + float(layer.router_bias[e]) for e in range(E)]
-    S = sorted(range(E), key=lambda e: (-l[e], e))[:k]
-    m = max(l[e] for e in S)
-    z = sum(math.exp(l[e] - m) for e in S)
-    w = [math.exp(l[e] - m) / z for e in S]
+    bias = [0.0] * E if layer.router_bias is None else [float(b) for b in layer.router_bias]
+    if getattr(layer.spec, "router_score", "softmax") == "sigmoid":
+        sc = [1.0 / (1.0 + math.exp(-v)) for v in l]
+        S = sorted(range(E), key=lambda e: (-(sc[e] + bias[e]), e))[:k]
+        z = sum(sc[e] for e in S)
+        w = [layer.spec.routed_scaling * sc[e] / z for e in S]
+    else:
+        l = [l[e] + bias[e] for e in range(E)]
+        S = sorted(range(E), key=lambda e: (-l[e], e))[:k]
+        m = max(l[e] for e in S)
+        z = sum(math.exp(l[e] - m) for e in S)
+        w = [math.exp(l[e] - m) / z for e in S]
     y = ffn(layer.shared, xv)
     for j, e in enumerate(S):
         fe = ffn(layer.experts[e], xv)
@@ -353,7 +359,89 @@ def pin_lfu_trace():
         assert [tuple(v) for v in f] == fills, (ids, f, fills)
 
 
+def read_sigmoid_cases():
+    """Hand-worked sigmoid router cases (tests/golden/sigmoid_router.txt)."""
+    cases, cur = [], None
+    for raw in open(os.path.join(GOLDEN, "sigmoid_router.txt")):
+        line = raw.strip()
+        if not line or line.startswith("#"):
+            continue
+        tok = line.split()
+        if tok[0] == "case":
+            cur = {"name": tok[1], "bias": {}}
+            cases.append(cur)
+        elif tok[0] == "k":
+            cur["k"] = int(tok[1])
+        elif tok[0] == "scale":
+            cur["scale"] = Fraction(tok[1])
+        elif tok[0] == "logit":
+            lg = {}
+            for t in tok[1:]:
+                e, v = t.split("=")
+                if v == "0":
+                    lg[int(e)] = 0.0
+                else:
+                    sign = -1.0 if v.startswith("-") else 1.0
+                    lg[int(e)] = sign * math.log(float(Fraction(v.lstrip("-").split(":")[1])))
+            cur["logits"] = np.array([lg[e] for e in range(len(lg))])
+        elif tok[0] == "bias":
+            for t in tok[1:]:
+                e, v = t.split("=")
+                cur["bias"][int(e)] = float(v)
+        elif tok[0] == "ids":
+            cur["ids"] = [int(v) for v in tok[1:]]
+        elif tok[0] == "w":
+            cur["w"] = [Fraction(v) for v in tok[1:]]
+    for c in cases:
+        E = len(c["logits"])
+        c["bias"] = np.array([c["bias"].get(e, 0.0) for e in range(E)], np.float32)
+    return cases
+
+
+def _sigmoid_layer(seed=14, E=10, k=3, H=64, I=64, scale=2.5, bias_sd=0.05):
+    spec = LayerSpec(hidden=H, inter=I, n_experts=E, top_k=k, act="f32", router_score="sigmoid",
+                     routed_scaling=scale, score_bias_sd=bias_sd)
+    return si.gen_layer(seed, 0, spec)
+
+
+def pin_sigmoid_router_golden():
+    """The sigmoid scoring steps against the hand-worked cases."""
+    for c in read_sigmoid_cases():
+        layer = Layer(LayerSpec(hidden=64, inter=64, n_experts=len(c["logits"]), top_k=c["k"],
+                                router_score="sigmoid", routed_scaling=float(c["scale"])),
+                      None, [], None, router_bias=c["bias"])
+        key, sc = oracle.moe.route_keys(layer, c["logits"])
+        ids, _ = oracle.select_topk(key, c["k"])
+        assert list(ids) == c["ids"], (c["name"], list(ids))
+        w = oracle.moe._weights(layer, key, sc, ids)
+        assert np.allclose(w, [float(v) for v in c["w"]], rtol=0, atol=1e-14), (c["name"], w)
+
+
+def pin_sigmoid_layer_pure_python():
+    """A tiny sigmoid-scored layer equals the pure-Python restatement; the weights
+    sum to the scaling factor; without a bias the selection is the softmax one."""
+    for seed, scale in ((14, 2.5), (15, 1.0)):
+        layer = _sigmoid_layer(seed=seed, scale=scale)
+        for t in range(3):
+            x = si.gen_tokens(seed, t, 1, layer.spec)[0]
+            y, info = oracle.moe_token(layer, x)
+            yp, S, w = _py_layer(layer, x)
+            assert list(info.ids) == S
+            assert np.allclose(info.weights, w, rtol=0, atol=1e-14)
+            assert abs(info.weights.sum() - scale) < 1e-12
+            assert np.allclose(y, yp, rtol=1e-11, atol=1e-14)
+    layer = _sigmoid_layer(seed=16, bias_sd=None)
+    soft = Layer(LayerSpec(hidden=64, inter=64, n_experts=10, top_k=3, act="f32"), layer.router,
+                 layer.experts, layer.shared)
+    for t in range(5):
+        x = si.gen_tokens(16, t, 1, layer.spec)[0]
+        _, a = oracle.moe_token(layer, x)
+        _, b = oracle.moe_token(soft, x)
+        assert list(a.ids) == list(b.ids)
+
+
 ALL_PINS = [pin_dequant_q4_table, pin_dequant_q8_table, pin_format_sizes,
             pin_zero_input_routing, pin_topk_is_full_sort, pin_routing_weights,
             pin_silu, pin_ffn_closed_form, pin_dense_brute_force, pin_pure_python,
-            pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace]
+            pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace, pin_sigmoid_router_golden,
+            pin_sigmoid_layer_pure_python]

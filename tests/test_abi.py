@@ -59,6 +59,12 @@ def test_invalid_descriptors_rejected_before_cuda():
     assert spec.hidden == 512
 
 
+def test_router_scoring_null_layer_rejected():
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_layer_set_router_scoring(None, moe.MOE_SCORE_SIGMOID, 2.5)
+    assert ei.value.status == 1
+
+
 def test_no_cpu_fallback_without_gpu():
     import torch
     if torch.cuda.is_available():

@@ -23,7 +23,8 @@ def test_pin(pin):
 
 _real = {name: getattr(om, name) for name in
          ("dequant_q4g64", "dequant_q8g64", "routing_weights", "select_topk",
-          "silu", "expert_ffn", "router_logits", "moe_token")}
+          "silu", "expert_ffn", "router_logits", "moe_token", "sigmoid_keys",
+          "routing_weights_sigmoid", "route_keys", "sigmoid_scores")}
 
 
 def _deq_swapped_nibbles(codes, scale, bias):
@@ -105,6 +106,23 @@ def _token_no_shared(layer, x, ids=None, Wr=None):
     return y, info
 
 
+def _sig_bias_dropped(s, bias):
+    return _real["sigmoid_keys"](s, None)
+
+
+def _sig_not_scaled(s_sel, routed_scaling):
+    return _real["routing_weights_sigmoid"](s_sel, 1.0)
+
+
+def _sig_weights_from_keys(layer, l):
+    key, sc = _real["route_keys"](layer, l)
+    return key, (None if sc is None else key)
+
+
+def _sig_is_tanh(l):
+    return np.tanh(np.asarray(l, np.float64))
+
+
 MISTAKES = {
     "nibble order swapped": ("dequant_q4g64", _deq_swapped_nibbles),
     "bias sign flipped": ("dequant_q4g64", _deq_bias_sign),
@@ -118,6 +136,10 @@ MISTAKES = {
     "router bias dropped": ("router_logits", _logits_no_bias),
     "shared expert weighted": ("moe_token", _token_weighted_shared),
     "shared expert dropped": ("moe_token", _token_no_shared),
+    "sigmoid selection bias dropped": ("sigmoid_keys", _sig_bias_dropped),
+    "sigmoid weights not scaled": ("routing_weights_sigmoid", _sig_not_scaled),
+    "sigmoid bias in the weights": ("route_keys", _sig_weights_from_keys),
+    "sigmoid replaced by tanh": ("sigmoid_scores", _sig_is_tanh),
 }
 
 
