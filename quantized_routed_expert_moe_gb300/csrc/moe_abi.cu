@@ -162,7 +162,10 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     L.device = device;
     L.rec_bytes = record_bytes(d.hidden, d.inter);
     L.router_splits = pick_router_splits(d.hidden);
-    L.router_splits_tok = ((d.hidden / 64) % 16 == 0) ? 16 : L.router_splits;
+    // prefill router GEMM: enough K-splits for two CTAs per SM at 128 tokens
+    // (each split a whole number of 64-wide groups)
+    L.router_splits_tok = ((d.hidden / 64) % kMaxTokSplits == 0) ? kMaxTokSplits
+                          : ((d.hidden / 64) % 16 == 0) ? 16 : L.router_splits;
     cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, device);
 
     const int E = d.n_experts, H = d.hidden, I = d.inter, k = d.top_k, T = d.max_tokens;

@@ -182,6 +182,9 @@ cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y
                                       const float* wts, int jj0, int jj1, bool down, cudaStream_t s);
 // staged SwiGLU output block (q16 runs, inverse scales, sums) of ns slots
 inline size_t hq_block_bytes_host(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
+// K-splits of the prefill router GEMM: at most this many partial logit sets
+// are summed (in a fixed order) per token.
+constexpr int kMaxTokSplits = 32;
 constexpr int kHCopies = 16;   // replicas of that block the decode kernels use
 cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
                                           float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s);

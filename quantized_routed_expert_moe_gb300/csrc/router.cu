@@ -161,25 +161,25 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
 // ---------------------------------------------------------------------------
 // router for T tokens: split-K tiles (16 tokens x 64 experts), then per-token top-k
 // ---------------------------------------------------------------------------
-constexpr int RT_T = 32, RT_E = 128, RT_K = 32;
+constexpr int RT_T = 32, RT_E = 128, RT_K = 64;
 
-// Tile of 32 tokens x 128 experts over one split's K range, in chunks of 32:
+// Tile of 32 tokens x 128 experts over one split's K range, in chunks of 64:
 // x and W are staged transposed (k-major) in shared memory; thread (ty, tx)
 // keeps the fp32 sums of tokens 4ty..4ty+3 x experts 4tx..4tx+3 (the four x
 // values are one broadcast read per warp), and the next chunk's global loads
 // are in flight while the current chunk is multiplied.
 template <bool Q8>
-__global__ void __launch_bounds__(kThreads) k_router_tokens(const void* __restrict__ W, const void* __restrict__ x,
+__global__ void __launch_bounds__(kThreads, 2) k_router_tokens(const void* __restrict__ W, const void* __restrict__ x,
                                                             int x_bf16, int T, int H, int E, int splits,
                                                             float* __restrict__ part) {
-    constexpr int NX = RT_T * RT_K / kThreads, NW = RT_E * RT_K / kThreads;   // 4, 16
+    constexpr int NX = RT_T * RT_K / kThreads, NW = RT_E * RT_K / kThreads;   // 8, 32
     __shared__ __align__(16) float xs[RT_K][RT_T + 4];
     __shared__ __align__(16) float ws[RT_K][RT_E + 4];
     const int e0 = blockIdx.y * RT_E, t0 = blockIdx.x * RT_T;
     const int Ls = H / splits, kb = blockIdx.z * Ls;
     const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;
     const int c = tid & (RT_K - 1), r0 = tid / RT_K;   // staging: k within the chunk, first row
-    constexpr int RS = kThreads / RT_K;                 // rows per staging pass (8)
+    constexpr int RS = kThreads / RT_K;                 // rows per staging pass (4)
     float acc[4][4] = {};
     float vx[NX], vw[NW];
     auto load = [&](int kc) {
@@ -243,12 +243,12 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
     extern __shared__ float sl[];   // keys [E], then sigmoid scores [E]
     const int t = blockIdx.x;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float v[16];
+        float v[kMaxTokSplits];
 #pragma unroll
-        for (int s = 0; s < 16; ++s) v[s] = (s < splits) ? __ldcg(part + ((size_t)s * T + t) * E + e) : 0.f;   // splits <= 16
+        for (int s = 0; s < kMaxTokSplits; ++s) v[s] = (s < splits) ? __ldcg(part + ((size_t)s * T + t) * E + e) : 0.f;
         float l = 0.f;
 #pragma unroll
-        for (int s = 0; s < 16; ++s) l += v[s];
+        for (int s = 0; s < kMaxTokSplits; ++s) l += v[s];
         const float key = route_key(l, bias ? bias[e] : 0.f, mode, sl + E + e);
         sl[e] = key;
         logits[(size_t)t * E + e] = key;
