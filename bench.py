@@ -183,6 +183,8 @@ def run_reference(args, spec, workload):
 
 
 PREFILL_DESC = {
+    "glm_verify": "GLM-scale verify batches: H6144 I2048 E256 top-8 + 1 shared, T tokens per batch through the "
+                  "batch-union path (each distinct expert read once per batch), router bias from Zipf(1.1)",
     "glm_prefill": "GLM-scale prefill chunk: H6144 I2048 E256 top-8 + 1 shared, 128 tokens, "
                    "router bias from Zipf(1.1) expert popularity (uneven expert loads)",
     "glm_prefill_dense": "GLM-scale prefill chunk, all 128 tokens on the same 8 experts "
@@ -206,10 +208,12 @@ def prefill_layer(workload, seed=0, experts=None):
 def run_prefill(args):
     """One step = one 128-token chunk through each of R rotating layer replicas."""
     ws, rank, local = dist_info()
-    T = 128
+    T = args.chunk or (4 if args.workload == "glm_verify" else 128)
     layer = prefill_layer(args.workload, experts=args.experts)
     spec = layer.spec
     workload = PREFILL_DESC[args.workload]
+    if args.workload == "glm_verify":
+        workload = workload.replace("T tokens", f"{T} tokens")
     if args.experts:
         workload = workload.replace("E256", f"E{args.experts}")
     X = si.gen_tokens(1000 * rank, 0, T, spec)
@@ -348,7 +352,7 @@ def run_prefill(args):
             dist.destroy_process_group()
         return
     line = {
-        "metric": "MoE-layer prefill tokens/s (128-token chunks)", "value": value, "unit": UNIT, "n_gpus": ws,
+        "metric": f"MoE-layer prefill tokens/s ({T}-token chunks)", "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": workload, "tokens_per_step": T * R, "layer_replicas": R,
@@ -507,6 +511,124 @@ def run_streamed(args):
     print(json.dumps(line), flush=True)
 
 
+def h2d_peak_gbs(stream):
+    """Pinned host -> device copy bandwidth of this machine (1 GiB copies)."""
+    import torch
+    big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    dst.copy_(big, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(4):
+        dst.copy_(big, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del big, dst
+    return 4 * (1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+
+def run_streamed_prefill(args):
+    """Prefill chunks on one streamed GLM-scale layer: the chunk's distinct
+    experts pass through the 16-slot cache in waves (batch union), routed
+    records from a pinned alias pool. One step = one distinct 128-token chunk."""
+    ws, rank, local = dist_info()
+    spec = si.CONFIGS["glm_prefill"]
+    E, P = spec.n_experts, args.pool
+    T = args.chunk or 128
+    workload = (f"streamed GLM-scale prefill: H6144 I2048 E256 top-8 + 1 shared, {T}-token chunks, 16-slot cache, "
+                f"Zipf(1.1) routing bias, {P}-record alias pool in pinned host memory")
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        layer = si.gen_layer(0, 0, spec)
+        X = si.gen_tokens(0, 0, 2, spec)
+        for _ in range(args.warmup):
+            oracle_sample(layer, X, 1)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_sample(layer, X, 1)
+        v = args.steps / (time.perf_counter() - t0)
+        print(json.dumps({"impl": "reference", "metric": f"streamed MoE-layer prefill tokens/s ({T}-token chunks)",
+                          "value": v, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 / v, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic", "config": {"workload": workload, "tokens_per_step": 1},
+                          "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                           "sample": "one token per step through the fp64 oracle"},
+                          "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    import torch
+    import quantized_routed_expert_moe_gb300 as moe
+    from quantized_routed_expert_moe_gb300 import build as _b
+    torch.cuda.set_device(local)
+    if rank == 0:
+        _b.build()
+    desc = moe.desc_from_spec(spec, cache_slots=16, max_tokens=T)
+    rb = moe.moe_expert_record_bytes(desc)
+    pool = torch.empty((P, rb), dtype=torch.uint8).pin_memory()
+    pool_np = pool.numpy()
+    for p in range(P):
+        moe.moe_pack_expert_record(desc, si.gen_expert(0, 1000, p, spec), pool_np[p])
+    recs = [pool[(e * 2654435761) % P] for e in range(E)]
+    lay = si.Layer(spec, si.gen_router(0, 0, spec), [], si.gen_expert(0, 0, E, spec), si.gen_router_bias(0, 0, spec))
+    ml = moe.MoELayer(lay, device=local, max_tokens=T, cache_slots=16, records=recs)
+    n_chunks = args.warmup + args.steps
+    X = si.gen_tokens(1000 * rank, 0, T * n_chunks, spec).reshape(n_chunks, T, spec.hidden)
+    x_host = torch.from_numpy(np.ascontiguousarray(X.view(np.int16))).view(torch.bfloat16).pin_memory()
+    x_dev = x_host.to("cuda")
+    y = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        ml.prefill_chunk(x_dev[i], T, y, stream=stream)
+    torch.cuda.synchronize()
+    s0 = ml.cache_stats()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        ml.prefill_chunk(x_dev[args.warmup + i], T, y, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    s1 = ml.cache_stats()
+    st, bits = ml.check()
+    if st:
+        raise RuntimeError(f"streamed prefill reported device error bits {bits:#x}")
+    ml.close()
+    hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+    h2d = s1["bytes_h2d"] - s0["bytes_h2d"]
+    waves = s1["tokens"] - s0["tokens"]
+    peak = h2d_peak_gbs(stream)
+    h2d_gbs = h2d / (ms / 1e3) / 1e9
+    value = T * args.steps / (ms / 1e3)
+    if rank != 0:
+        return
+    line = {
+        "metric": f"streamed MoE-layer prefill tokens/s ({T}-token chunks)", "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": workload, "tokens_per_step": T, "pool_records": P, "record_bytes": rb,
+                   "parallelism": f"replicas x{ws}"},
+        "waves_per_chunk": waves / args.steps,
+        "hit_rate": hits / max(hits + misses, 1),
+        "h2d_gbs": h2d_gbs,
+        "roofline": {"bound": "h2d", "achieved": h2d_gbs, "peak": peak, "unit": "GB/s", "frac": h2d_gbs / peak,
+                     "traffic": None, "kernel": "cache fills (cudaMemcpyAsync) between the waves' GEMMs",
+                     "peak_source": "measured here: pinned 1 GiB host-to-device copy"},
+        "e2e": {"value": T * args.steps / wall, "unit": UNIT,
+                "h2d_bytes_per_step": T * spec.hidden * 2 + h2d / args.steps, "d2h_bytes_per_step": 0},
+        "gpu_launches": None,
+        "clocks": clk,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -514,11 +636,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="glm_decode",
-                    choices=["glm_decode", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense", "glm_streamed"])
+                    choices=["glm_decode", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense", "glm_verify",
+                             "glm_streamed", "glm_streamed_prefill"])
     ap.add_argument("--layers", type=int, default=75, help="glm_streamed: layers in the stack")
     ap.add_argument("--pool", type=int, default=256,
                     help="glm_streamed: distinct expert records in pinned host memory (alias pool)")
     ap.add_argument("--tokens", type=int, default=1000)
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="tokens per prefill chunk / verify batch (default 128; glm_verify: 4)")
     ap.add_argument("--replicas", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "fused"],
@@ -528,11 +653,14 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
-    if args.workload.startswith("glm_prefill"):
+    if args.workload.startswith("glm_prefill") or args.workload == "glm_verify":
         run_prefill(args)
         return
     if args.workload == "glm_streamed":
         run_streamed(args)
+        return
+    if args.workload == "glm_streamed_prefill":
+        run_streamed_prefill(args)
         return
     spec = si.CONFIGS[args.workload]
     if args.experts:

@@ -256,8 +256,15 @@ moe_status moe_decode_static_scratch(moe_layer* layer, const void* x, void* y, f
  * fp32 accumulation, and combined per token in a fixed order. fp16 rather than
  * bf16: its 11-bit significand keeps the chunk within the layer tolerance,
  * which bf16 operands do not. Activations and SwiGLU outputs must lie within
- * the fp16 range (|v| < 65504). Not available on streamed layers
- * (MOE_E_UNSUPPORTED). */
+ * the fp16 range (|v| < 65504).
+ * Streamed layers (cache_slots > 0) run the chunk as a batch union through the
+ * cache (Colibri report section 2, "Union"): the chunk's distinct routed
+ * experts are staged in waves, first those already resident, then the others
+ * at most cache_slots at a time, and each wave's groups are computed from the
+ * slots. Each wave is one moe_cache_stage (the host waits for the chunk's
+ * routing, with the layer's deadline), so a failing source returns
+ * MOE_E_SOURCE and a deadline MOE_E_TIMEOUT. The output equals that of the
+ * same layer held resident, bit for bit. */
 moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y, float* y_f32,
                              void* stream);
 

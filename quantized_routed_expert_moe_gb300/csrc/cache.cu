@@ -290,6 +290,12 @@ moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int*
     return st;
 }
 
+int cache_slot_of(const Layer& L, int expert) { return L.cache->lfu.slot_of(expert); }
+
+const uint8_t* cache_slots_base(const Layer& L) { return L.cache->dev_slots; }
+
+moe_status host_wait_event(const Layer& L, cudaEvent_t ev, const char* what) { return wait_event(L, ev, what); }
+
 moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s) {
     CacheState& C = *L.cache;
     const auto& d = L.d;

@@ -85,6 +85,11 @@ static void free_layer(Layer& L) {
     f(L.io_x);
     f(L.io_y);
     f(L.pf.xp);        // prefill block base
+    f(L.pf.waves_dev);
+    if (L.pf.groups_host) cudaFreeHost(L.pf.groups_host);
+    if (L.pf.waves_host) cudaFreeHost(L.pf.waves_host);
+    if (L.pf.groups_ready) cudaEventDestroy(L.pf.groups_ready);
+    if (L.pf.waves_free) cudaEventDestroy(L.pf.waves_free);
     f(L.trace);
     f(L.trace_split);
 }
@@ -322,6 +327,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
 
     if (d.cache_slots > 0) {
         st = cache_create(L, records, source, source_user);
+        if (st == MOE_OK && T > 1) st = prefill_cache_setup(L);
         if (st != MOE_OK) { std::string m = g_last_error; free_layer(L); delete layer; return fail(st, m); }
     }
 #undef TRY_ALLOC
@@ -379,14 +385,13 @@ moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y
     if (!y && !y_f32) return fail(MOE_E_INVALID, "y and y_f32 are both NULL");
     Layer& L = layer->L;
     if (T < 1 || T > L.d.max_tokens) return fail(MOE_E_INVALID, "T out of range 1..max_tokens");
-    if (L.d.cache_slots > 0)
-        return fail(MOE_E_UNSUPPORTED, "prefill on a streamed layer: stage experts and decode per token");
     DeviceGuard g(L.device);
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 1) return moe_decode(layer, x, y, y_f32, stream);
     cudaError_t e = launch_route_tokens(L, x, T, s);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
+    if (L.d.cache_slots > 0) return launch_prefill_streamed(L, x, T, y, y_f32, s);
     e = launch_prefill(L, x, T, y, y_f32, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return MOE_OK;

@@ -85,9 +85,18 @@ struct PrefillScratch {
     float* yp = nullptr;              // [rows][H] fp32 expert outputs (unweighted)
     int max_rows = 0;
     // TMA descriptors: gate/up codes, gate/up meta, down codes, down meta, then
-    // xp and hp with boxes of 16, 32, 64 and 128 token rows
-    CUtensorMap tm[12];
+    // xp and hp with boxes of 16, 32, 64 and 128 token rows; on streamed layers
+    // 12..15 are the four weight maps over the cache slots
+    CUtensorMap tm[16];
     bool ready = false;
+    // streamed layers: the chunk's groups read back to the host, and the group
+    // lists of the staging waves ([n, expert or slot x n, off x n, cnt x n] per
+    // wave, waves back to back), in pinned host memory and on the device
+    int32_t* groups_host = nullptr;   // pinned [1 + 3 (E + 1)]
+    int32_t* waves_host = nullptr;    // pinned [4 (E + 2)]
+    int32_t* waves_dev = nullptr;     // device [4 (E + 2)]
+    cudaEvent_t groups_ready = nullptr, waves_free = nullptr;
+    uint64_t waves = 0;               // staging waves run by streamed prefill chunks
 };
 
 struct CacheState;  // streamed mode (cache.cu)
@@ -231,6 +240,14 @@ moe_status cache_create(Layer& L, const void* const* records, moe_expert_source 
 void cache_destroy(Layer& L);
 moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int* hits, int* misses);
 moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s);
+int cache_slot_of(const Layer& L, int expert);   // slot holding `expert`, -1 when not resident
+const uint8_t* cache_slots_base(const Layer& L); // device [cache_slots][rec_bytes]
+// host wait for `ev` with the layer's deadline (MOE_OPT_HOST_TIMEOUT_MS)
+moe_status host_wait_event(const Layer& L, cudaEvent_t ev, const char* what);
+// prefill chunk on a streamed layer (router already launched): waves through the cache
+moe_status launch_prefill_streamed(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s);
+// streamed layers: tensor maps over the cache slots and the pinned buffers (after cache_create)
+moe_status prefill_cache_setup(Layer& L);
 
 }  // namespace moe
 

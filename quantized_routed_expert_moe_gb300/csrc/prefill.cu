@@ -11,6 +11,8 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "moe_internal.h"
@@ -612,72 +614,214 @@ bool map_act(CUtensorMap* tm, void* base, int K, int rows, uint32_t box_rows) {
 
 cudaError_t prefill_kernel_setup(Layer& L) {
     const auto& d = L.d;
-    if (d.cache_slots > 0 || !L.pf.xp) return cudaSuccess;   // prefill needs resident experts
+    if (!L.pf.xp) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k_pf_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_pf_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     if (!encoder()) return cudaErrorSymbolNotFound;
-    const int H = d.hidden, I = d.inter, recs = d.n_experts + d.n_shared;
+    const int H = d.hidden, I = d.inter;
+    // device records: every expert and the shared one (resident layers), or
+    // the shared one alone (streamed layers: routed experts live in the cache slots)
+    const int recs = d.cache_slots > 0 ? d.n_shared : d.n_experts + d.n_shared;
     const uint8_t* gu = L.experts;
     const uint8_t* dn = L.experts + gu_block_bytes(H, I);
     const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
-    bool ok = map_weight_rows(&L.pf.tm[0], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 128, SW) &&
-              map_weight_rows(&L.pf.tm[1], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 16, NS) &&
-              map_weight_rows(&L.pf.tm[2], dn, row_bytes(I), H, recs, L.rec_bytes, 128, SW) &&
-              map_weight_rows(&L.pf.tm[3], dn, row_bytes(I), H, recs, L.rec_bytes, 16, NS) &&
-              true;
+    bool ok = recs == 0 ||
+              (map_weight_rows(&L.pf.tm[0], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 128, SW) &&
+               map_weight_rows(&L.pf.tm[1], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 16, NS) &&
+               map_weight_rows(&L.pf.tm[2], dn, row_bytes(I), H, recs, L.rec_bytes, 128, SW) &&
+               map_weight_rows(&L.pf.tm[3], dn, row_bytes(I), H, recs, L.rec_bytes, 16, NS));
     for (int j = 0; j < 4 && ok; ++j)   // token boxes of 16, 32, 64 and 128 rows
         ok = map_act(&L.pf.tm[4 + j], L.pf.xp, H, L.pf.max_rows, 16u << j) &&
              map_act(&L.pf.tm[8 + j], L.pf.hp, I, L.pf.max_rows, 16u << j);
     if (!ok) return cudaErrorInvalidValue;
-    L.pf.ready = true;
+    L.pf.ready = d.cache_slots == 0;   // streamed layers: once the slot maps exist
     return cudaSuccess;
 }
 
-cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s) {
-    if (!L.pf.ready) return cudaErrorNotSupported;
+moe_status prefill_cache_setup(Layer& L) {
     const auto& d = L.d;
-    const int H = d.hidden, I = d.inter, k = d.top_k, E = d.n_experts, ns = d.n_shared;
-    const int xb = d.act_dtype == MOE_BF16;
-    const int P = T * k, rows = P + T * ns;
     auto& pf = L.pf;
+    if (!pf.xp) return MOE_OK;
+    const int H = d.hidden, I = d.inter, E = d.n_experts;
+    const uint8_t* slots = cache_slots_base(L);
+    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint8_t* dn = slots + gu_block_bytes(H, I);
+    const bool ok = map_weight_rows(&pf.tm[12], slots, row_bytes(H), 2 * I, d.cache_slots, L.rec_bytes, 128, SW) &&
+                    map_weight_rows(&pf.tm[13], slots, row_bytes(H), 2 * I, d.cache_slots, L.rec_bytes, 16, NS) &&
+                    map_weight_rows(&pf.tm[14], dn, row_bytes(I), H, d.cache_slots, L.rec_bytes, 128, SW) &&
+                    map_weight_rows(&pf.tm[15], dn, row_bytes(I), H, d.cache_slots, L.rec_bytes, 16, NS);
+    if (!ok) return fail(MOE_E_CUDA, "tensor maps over the cache slots");
+    MOE_CUDA_TRY(cudaHostAlloc(&pf.groups_host, (size_t)(1 + 3 * (E + 1)) * 4, cudaHostAllocDefault));
+    MOE_CUDA_TRY(cudaHostAlloc(&pf.waves_host, (size_t)4 * (E + 2) * 4, cudaHostAllocDefault));
+    MOE_CUDA_TRY(cudaMalloc(&pf.waves_dev, (size_t)4 * (E + 2) * 4));
+    L.device_bytes += (size_t)4 * (E + 2) * 4;
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&pf.groups_ready, cudaEventDisableTiming));
+    MOE_CUDA_TRY(cudaEventCreateWithFlags(&pf.waves_free, cudaEventDisableTiming));
+    MOE_CUDA_TRY(cudaEventRecord(pf.waves_free, 0));
+    pf.ready = true;
+    return MOE_OK;
+}
 
+namespace {
+
+// permute the chunk's (token, slot) pairs by expert and gather the activations
+cudaError_t launch_permute_gather(Layer& L, const void* x, int T, cudaStream_t s) {
+    const auto& d = L.d;
+    const int H = d.hidden, k = d.top_k, E = d.n_experts, ns = d.n_shared;
+    const int rows = T * k + T * ns;
+    auto& pf = L.pf;
     prof_begin(L, K_PF_PERMUTE, s);
     k_pf_permute<<<1, kPermThreads, 0, s>>>(L.ids, T, k, E, ns, pf.group_expert, pf.group_off, pf.group_cnt,
                                             pf.n_groups, pf.perm_token, pf.pos);
     prof_end(L, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-
     prof_begin(L, K_PF_GATHER, s);
     const long blocks = ((long)rows * (H / 8) + 255) / 256;
-    k_pf_gather<<<(int)std::min<long>(blocks, (long)L.num_sms * 8), 256, 0, s>>>(x, xb, pf.perm_token, rows, H,
-                                                                                 static_cast<uint4*>(pf.xp));
-    prof_end(L, s);
-
-    GemmArgs gu{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, H, I / 64, 2 * I, pf.hp, I, pf.err,
-                L.split_trace(3)};
-    prof_begin(L, K_PF_GEMM_GU, s);
-    k_pf_gemm<0><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[0], pf.tm[1], pf.tm[4], pf.tm[5], pf.tm[6],
-                                                             pf.tm[7], gu);
-    prof_end(L, s);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    GemmArgs dn{pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, I, (H + 127) / 128, H, pf.yp, H, pf.err,
-                L.split_trace(4)};
-    prof_begin(L, K_PF_GEMM_DOWN, s);
-    k_pf_gemm<1><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[2], pf.tm[3], pf.tm[8], pf.tm[9], pf.tm[10],
-                                                             pf.tm[11], dn);
-    prof_end(L, s);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    prof_begin(L, K_PF_COMBINE, s);
-    k_pf_combine<<<dim3(T, (H / 4 + 255) / 256), 256, 0, s>>>(pf.yp, pf.pos, L.wts, k, ns, H, y, xb, y_f32);
+    k_pf_gather<<<(int)std::min<long>(blocks, (long)L.num_sms * 8), 256, 0, s>>>(
+        x, d.act_dtype == MOE_BF16 ? 1 : 0, pf.perm_token, rows, H, static_cast<uint4*>(pf.xp));
     prof_end(L, s);
     return cudaGetLastError();
+}
+
+// gate/up + SwiGLU and down GEMMs over a list of groups; `wmap` selects the
+// weight maps (0: device records, 12: cache slots); group g's expert field is
+// the record (or slot) index the maps address
+cudaError_t launch_gemm_pair(Layer& L, int wmap, const int32_t* gexp, const int32_t* goff, const int32_t* gcnt,
+                             const int32_t* n_groups, cudaStream_t s) {
+    const auto& d = L.d;
+    const int H = d.hidden, I = d.inter;
+    auto& pf = L.pf;
+    GemmArgs gu{gexp, goff, gcnt, n_groups, H, I / 64, 2 * I, pf.hp, I, pf.err, L.split_trace(3)};
+    prof_begin(L, K_PF_GEMM_GU, s);
+    k_pf_gemm<0><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[wmap + 0], pf.tm[wmap + 1], pf.tm[4], pf.tm[5],
+                                                             pf.tm[6], pf.tm[7], gu);
+    prof_end(L, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    GemmArgs dn{gexp, goff, gcnt, n_groups, I, (H + 127) / 128, H, pf.yp, H, pf.err, L.split_trace(4)};
+    prof_begin(L, K_PF_GEMM_DOWN, s);
+    k_pf_gemm<1><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[wmap + 2], pf.tm[wmap + 3], pf.tm[8], pf.tm[9],
+                                                             pf.tm[10], pf.tm[11], dn);
+    prof_end(L, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(Layer& L, int T, void* y, float* y_f32, cudaStream_t s) {
+    const auto& d = L.d;
+    const int H = d.hidden;
+    prof_begin(L, K_PF_COMBINE, s);
+    k_pf_combine<<<dim3(T, (H / 4 + 255) / 256), 256, 0, s>>>(L.pf.yp, L.pf.pos, L.wts, d.top_k, d.n_shared, H, y,
+                                                              d.act_dtype == MOE_BF16 ? 1 : 0, y_f32);
+    prof_end(L, s);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s) {
+    if (!L.pf.ready) return cudaErrorNotSupported;
+    auto& pf = L.pf;
+    cudaError_t e = launch_permute_gather(L, x, T, s);
+    if (e != cudaSuccess) return e;
+    e = launch_gemm_pair(L, 0, pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, s);
+    if (e != cudaSuccess) return e;
+    return launch_combine(L, T, y, y_f32, s);
+}
+
+// Batch union through the cache (Colibri report section 2, "Union": each
+// distinct expert of a batch is loaded once and applied to every row that
+// routes to it; Colibri README, "What's implemented": batch-union MoE in
+// prefill). The chunk's distinct routed experts pass through the layer's
+// cache slots in waves: first the experts already resident (no copies), then
+// the rest, at most cache_slots at a time. Each wave is one moe_cache_stage
+// (the LFU counts one use per expert per wave), then the grouped GEMMs run on
+// that wave's groups with the weight maps over the slots. The shared expert's
+// group runs first, from its device record, while the first copies are in
+// flight. Every group's rows are computed exactly as on a resident layer, so
+// the chunk's output is the same bit for bit.
+moe_status launch_prefill_streamed(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s) {
+    auto& pf = L.pf;
+    if (!pf.ready) return fail(MOE_E_UNSUPPORTED, "prefill scratch missing (max_tokens == 1)");
+    const auto& d = L.d;
+    const int E = d.n_experts, ns = d.n_shared, S = d.cache_slots;
+    MOE_CUDA_TRY(launch_permute_gather(L, x, T, s));
+    // the groups, read back (count, then expert / offset / size arrays)
+    int32_t* gh = pf.groups_host;
+    MOE_CUDA_TRY(cudaMemcpyAsync(gh, pf.n_groups, 4, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(gh + 1, pf.group_expert, (size_t)(E + 1) * 4, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(gh + 1 + (E + 1), pf.group_off, (size_t)(E + 1) * 4, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(gh + 1 + 2 * (E + 1), pf.group_cnt, (size_t)(E + 1) * 4, cudaMemcpyDeviceToHost, s));
+    MOE_CUDA_TRY(cudaEventRecord(pf.groups_ready, s));
+    moe_status st = host_wait_event(L, pf.groups_ready, "prefill groups");
+    if (st != MOE_OK) return st;
+    // the previous chunk's wave-list uploads have run before the pinned lists are rewritten
+    st = host_wait_event(L, pf.waves_free, "wave list buffer reuse");
+    if (st != MOE_OK) return st;
+    const int ng = gh[0];
+    const int32_t* gexp = gh + 1;
+    const int32_t* goff = gh + 1 + (E + 1);
+    const int32_t* gcnt = gh + 1 + 2 * (E + 1);
+    const int nr = ng - ns;   // routed groups (ascending expert id); the shared group is last
+    if (nr < 0 || nr > E) return fail(MOE_E_STATE, "prefill group count out of range");
+    int32_t* wh = pf.waves_host;
+    int32_t* wd = pf.waves_dev;
+    int o = 0;   // next free int in the wave lists
+    // one wave list: [n, index x n, off x n, cnt x n], uploaded on `s`, then the GEMMs
+    auto run_wave = [&](int wmap, const int* gsel, int n, const int32_t* index) -> moe_status {
+        int32_t* w = wh + o;
+        w[0] = n;
+        for (int i = 0; i < n; ++i) {
+            w[1 + i] = index[i];
+            w[1 + n + i] = goff[gsel[i]];
+            w[1 + 2 * n + i] = gcnt[gsel[i]];
+        }
+        const int len = 1 + 3 * n;
+        MOE_CUDA_TRY(cudaMemcpyAsync(wd + o, w, (size_t)len * 4, cudaMemcpyHostToDevice, s));
+        MOE_CUDA_TRY(launch_gemm_pair(L, wmap, wd + o + 1, wd + o + 1 + n, wd + o + 1 + 2 * n, wd + o, s));
+        o += len;
+        ++pf.waves;
+        return MOE_OK;
+    };
+    if (ns) {
+        const int gs = ng - 1;
+        const int32_t rec0 = 0;   // the shared expert is the layer's only device record
+        st = run_wave(0, &gs, 1, &rec0);
+        if (st != MOE_OK) return st;
+    }
+    // waves: the resident experts first, then the others in ascending id
+    std::vector<int> order;
+    order.reserve(nr);
+    for (int g = 0; g < nr; ++g)
+        if (cache_slot_of(L, gexp[g]) >= 0) order.push_back(g);
+    const int n_res = (int)order.size();
+    for (int g = 0; g < nr; ++g)
+        if (cache_slot_of(L, gexp[g]) < 0) order.push_back(g);
+    std::vector<int32_t> ids, slot;
+    for (int w0 = 0; w0 < nr;) {
+        // the resident experts form the first wave (at most S of them by construction)
+        const int w1 = (w0 == 0 && n_res > 0) ? n_res : std::min(nr, w0 + S);
+        const int n = w1 - w0;
+        ids.resize(n);
+        slot.resize(n);
+        for (int i = 0; i < n; ++i) ids[i] = gexp[order[w0 + i]];
+        st = cache_stage(L, ids.data(), n, s, nullptr, nullptr);
+        if (st != MOE_OK) break;
+        for (int i = 0; i < n; ++i) {
+            slot[i] = cache_slot_of(L, ids[i]);
+            if (slot[i] < 0) st = fail(MOE_E_STATE, "expert " + std::to_string(ids[i]) + " is not resident");
+        }
+        if (st != MOE_OK) break;
+        st = run_wave(12, order.data() + w0, n, slot.data());
+        if (st != MOE_OK) break;
+        w0 = w1;
+    }
+    MOE_CUDA_TRY(cudaEventRecord(pf.waves_free, s));
+    if (st != MOE_OK) return st;
+    MOE_CUDA_TRY(launch_combine(L, T, y, y_f32, s));
+    return MOE_OK;
 }
 
 }  // namespace moe

@@ -226,3 +226,101 @@ def test_host_wait_deadline():
         st.set_option(moe.MOE_OPT_HOST_TIMEOUT_MS, 30000)
         st.cache_stage(np.array([6, 7], np.int32), 2)
         torch.cuda.synchronize()
+
+
+# --------------------------------------------------------------------------- streamed prefill (batch union)
+
+def _prefill(ml, spec, xd, T):
+    y = torch_empty(T * spec.hidden)
+    y32 = torch_empty(T * spec.hidden)
+    ml.prefill_chunk(xd, T, y, y32)
+    import torch
+    torch.cuda.synchronize()
+    st, bits = ml.check()
+    assert st == 0, hex(bits)
+    return y32.cpu().numpy().reshape(T, spec.hidden)
+
+
+def torch_empty(n):
+    import torch
+    return torch.empty(n, dtype=torch.float32, device="cuda")
+
+
+def _waves(resident_before, distinct, slots):
+    """The library's wave order: resident experts first, then the rest in
+    ascending id, at most `slots` per wave."""
+    res = [e for e in distinct if e in resident_before]
+    rest = [e for e in distinct if e not in resident_before]
+    waves = [res] if res else []
+    for i in range(0, len(rest), slots):
+        waves.append(rest[i:i + slots])
+    return waves
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("slots,T,E", [(16, 64, 64), (8, 24, 32), (8, 3, 16)])
+def test_streamed_prefill_bit_identical_and_lfu(slots, T, E):
+    """A prefill chunk on a streamed layer (batch union through the cache in
+    waves) equals the resident layer's chunk bit for bit, over two chunks (the
+    second finds experts resident); slot residency follows the oracle's LFU run
+    over the same waves."""
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=E, zipf_alpha=1.1, act="f32")
+    layer = si.gen_layer(35, 0, spec)
+    chunks = [si.gen_tokens(35 + c, 0, T, spec) for c in range(2)]
+    xs = [torch.from_numpy(np.ascontiguousarray(X, np.float32)).cuda() for X in chunks]
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, max_tokens=T) as res:
+        want = [_prefill(res, spec, xd, T) for xd in xs]
+        sel = []
+        for xd in xs:
+            res.route(xd, T, ids, w)
+            torch.cuda.synchronize()
+            sel.append(ids.cpu().numpy().copy())
+        recs = packed_records(layer, res.desc)
+    sim = oracle.moe.LFUCache(slots)
+    with moe.MoELayer(layer, max_tokens=T, cache_slots=slots, records=recs) as st:
+        for c, xd in enumerate(xs):
+            got = _prefill(st, spec, xd, T)
+            assert np.array_equal(got, want[c])
+            distinct = sorted(set(int(e) for e in sel[c].reshape(-1)))
+            before = set(sim.count)
+            for wv in _waves(before, distinct, slots):
+                sim.access(np.array(wv, np.int64))
+            residency = st.residency()
+            for e, s in sim.slot_of.items():
+                assert residency[s] == e
+            assert sum(1 for e in residency if e >= 0) == len(sim.slot_of)
+
+
+@pytest.mark.gpu
+def test_streamed_prefill_source_failure():
+    """A source that fails during a chunk's waves returns MOE_E_SOURCE; once
+    it works again the chunk is computed as on the resident layer."""
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=16, act="f32")
+    layer = si.gen_layer(36, 0, spec)
+    T = 8
+    X = si.gen_tokens(36, 0, T, spec)
+    xd = torch.from_numpy(np.ascontiguousarray(X, np.float32)).cuda()
+    with moe.MoELayer(layer, max_tokens=T) as res:
+        want = _prefill(res, spec, xd, T)
+        recs = packed_records(layer, res.desc)
+    broken = {"on": True}
+
+    def src(user, e, dst, nbytes):
+        if broken["on"] and e % 3 == 1:
+            return 1
+        ctypes.memmove(dst, recs[e].ctypes.data, nbytes)
+        return 0
+    fn = moe.SOURCE_FN(src)
+    with moe.MoELayer(layer, max_tokens=T, cache_slots=8, source=fn) as st:
+        y = torch_empty(T * spec.hidden)
+        with pytest.raises(moe.MoEError) as ei:
+            st.prefill_chunk(xd, T, y, y)
+        assert ei.value.status == 7   # MOE_E_SOURCE
+        torch.cuda.synchronize()
+        broken["on"] = False
+        got = _prefill(st, spec, xd, T)
+        assert np.array_equal(got, want)
