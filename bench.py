@@ -387,7 +387,8 @@ def run_streamed(args):
     spec = si.CONFIGS["glm_prefill"]   # GLM shape with Zipf(1.1) router bias
     E, Lc, P = spec.n_experts, args.layers, args.pool
     workload = (f"streamed GLM-scale decode: {Lc} layers of H6144 I2048 E256 top-8 + 1 shared, 16-slot LFU cache "
-                f"per layer, Zipf(1.1) routing bias per layer, {P}-record alias pool in pinned host memory")
+                f"per layer, Zipf(1.1) routing bias per layer, {P}-record alias pool in pinned host memory; "
+                f"chain: {args.chain}; router lookahead: {'on' if args.lookahead else 'off'}")
     if args.impl == "reference":
         if rank != 0:
             return
@@ -441,16 +442,28 @@ def run_streamed(args):
     y = torch.empty(spec.hidden, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    def chain(y):
+        if args.chain == "norm":   # the layer output, renormalised
+            return (y * torch.rsqrt(torch.mean(y * y) + 1e-12)).to(torch.bfloat16)
+        # a residual-stream stand-in: the layer adds its output at a quarter of
+        # the stream's RMS, and the sum is renormalised
+        h = x.float() + 0.25 * y * torch.rsqrt(torch.mean(y * y) + 1e-12)
+        return (h * torch.rsqrt(torch.mean(h * h) + 1e-12)).to(torch.bfloat16)
+
     def token(i):
         x.copy_(x_host[i], non_blocking=True)
-        for ml in stack:
+        for li, ml in enumerate(stack):
+            if args.lookahead and li + 1 < Lc:
+                # the next layer's router on this layer's input: stage its predicted experts now
+                stack[li + 1].cache_prefetch(x, stream=stream)
             ml.decode(x, None, y, stream=stream)
-            x.copy_((y * torch.rsqrt(torch.mean(y * y) + 1e-12)).to(torch.bfloat16))
+            x.copy_(chain(y))
 
     for i in range(args.warmup):
         token(i)
     torch.cuda.synchronize()
     s0 = [ml.cache_stats() for ml in stack]
+    p0 = [ml.prefetch_stats() for ml in stack]
     clocks = ClockSampler(local)
     clocks.start()
     if ws > 1:
@@ -467,9 +480,11 @@ def run_streamed(args):
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     s1 = [ml.cache_stats() for ml in stack]
+    pf = [{key: b[key] - a[key] for key in b} for a, b in zip(p0, [ml.prefetch_stats() for ml in stack])]
     hits = sum(b["hits"] - a["hits"] for a, b in zip(s0, s1))
     misses = sum(b["misses"] - a["misses"] for a, b in zip(s0, s1))
-    h2d = sum(b["bytes_h2d"] - a["bytes_h2d"] for a, b in zip(s0, s1))
+    # fills for misses and fills for predictions
+    h2d = sum(b["bytes_h2d"] - a["bytes_h2d"] for a, b in zip(s0, s1)) + sum(p["bytes_h2d"] for p in pf)
     # pinned host -> device copy peak on this machine, for the fraction
     big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
     dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
@@ -499,6 +514,8 @@ def run_streamed(args):
                    "record_bytes": rb, "parallelism": f"replicas x{ws}"},
         "hit_rate": hits / max(hits + misses, 1),
         "h2d_gbs": h2d_gbs,
+        "lookahead": {"calls": sum(p["calls"] for p in pf), "predicted_resident": sum(p["resident"] for p in pf),
+                      "fills": sum(p["fills"] for p in pf), "bytes_h2d": sum(p["bytes_h2d"] for p in pf)},
         "roofline": {"bound": "h2d", "achieved": h2d_gbs, "peak": h2d_peak, "unit": "GB/s",
                      "frac": h2d_gbs / h2d_peak, "traffic": None, "kernel": "cache fills (cudaMemcpyAsync)",
                      "peak_source": "measured here: pinned 1 GiB host-to-device copy"},
@@ -642,6 +659,10 @@ def main():
     ap.add_argument("--pool", type=int, default=256,
                     help="glm_streamed: distinct expert records in pinned host memory (alias pool)")
     ap.add_argument("--tokens", type=int, default=1000)
+    ap.add_argument("--chain", default="norm", choices=["norm", "residual"],
+                    help="glm_streamed: how one layer's output becomes the next layer's input")
+    ap.add_argument("--lookahead", action="store_true",
+                    help="glm_streamed: stage each next layer's predicted experts (moe_cache_prefetch)")
     ap.add_argument("--chunk", type=int, default=None,
                     help="tokens per prefill chunk / verify batch (default 128; glm_verify: 4)")
     ap.add_argument("--replicas", type=int, default=None)

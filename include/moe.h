@@ -285,6 +285,31 @@ moe_status moe_decode_tokens_host(moe_layer* layer, const void* x_host, int32_t 
 moe_status moe_cache_stage(moe_layer* layer, const int32_t* ids, int32_t n, void* stream,
                            int32_t* n_hits, int32_t* n_misses);
 
+/* Router lookahead (Colibri analysis report, caching and prefetch: the state
+ * entering layer L, passed through the routing function of layer L + 1,
+ * predicts that layer's experts one layer ahead, and the predicted weights are
+ * loaded while layer L computes). Call it on the NEXT layer (streamed) with
+ * the CURRENT layer's input x (device, [H] act_dtype), before running the
+ * current layer. Once the work already queued on `stream` is done, the next
+ * layer's router runs on x on the layer's copy stream. The host waits for the
+ * predicted ids (the layer's deadline applies), then copies the predicted
+ * experts that are not resident into slots on the copy stream. `stream` does
+ * not wait for these copies; the layer's next moe_decode / moe_prefill_chunk
+ * does.
+ * Policy: a predicted expert is admitted with a use count of 0 (a later use
+ * counts as a hit); residents keep their counts and recency; victims are
+ * chosen as in moe_cache_stage, outside the prediction.
+ * n_resident / n_fills (may be NULL): predicted experts already resident, and
+ * copies issued. Errors: MOE_E_UNSUPPORTED on a resident layer, MOE_E_SOURCE
+ * if the source fails (that expert is left out), MOE_E_TIMEOUT. */
+moe_status moe_cache_prefetch(moe_layer* layer, const void* x, void* stream, int32_t* n_resident,
+                              int32_t* n_fills);
+
+/* Lookahead counters since creation: out4 = {calls, predicted experts already
+ * resident, fills, bytes copied for fills}. Prefetch fills are not counted in
+ * moe_cache_stats. */
+moe_status moe_cache_prefetch_stats(const moe_layer* layer, uint64_t* out4);
+
 /* Counters since creation. */
 moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out);
 

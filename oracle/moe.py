@@ -377,6 +377,45 @@ class LFUCache:
         return hits, fills
 
 
+    def prefetch(self, ids) -> tuple[list[int], list[tuple[int, int, int]]]:
+        """Admit a prediction (router lookahead).
+
+        Colibri analysis report, caching and prefetch: passing the state that
+        enters layer L through the router of layer L + 1 predicts that
+        layer's experts one layer ahead, and the predicted weights are loaded
+        while layer L computes. Readings (the page describes the prediction,
+        not its bookkeeping): a predicted expert that is not resident is
+        admitted with count 0, since it has not been used; residents keep
+        their counts and recency; victims follow the same rule as ``access``,
+        taken outside the prediction. Returns (predicted experts already
+        resident, fills).
+        """
+        ids = [int(e) for e in ids]
+        assert len(set(ids)) == len(ids) <= self.slots
+        self.clock += 1
+        pred = set(ids)
+        resident = [e for e in ids if e in self.count]
+        fills = []
+        for e in ids:
+            if e in self.count:
+                continue
+            if len(self.count) < self.slots:
+                used = set(self.slot_of.values())
+                slot = min(s for s in range(self.slots) if s not in used)
+                victim = -1
+            else:
+                cands = [r for r in self.count if r not in pred]
+                victim = min(cands, key=lambda r: (self.count[r], self.last[r], r))
+                slot = self.slot_of.pop(victim)
+                del self.count[victim]
+                del self.last[victim]
+            self.count[e] = 0
+            self.last[e] = self.clock
+            self.slot_of[e] = slot
+            fills.append((e, slot, victim))
+        return resident, fills
+
+
 def lfu_trace(id_rows, slots: int):
     """Hit/miss trace of a sequence of tokens through one LFU cache."""
     c = LFUCache(slots)

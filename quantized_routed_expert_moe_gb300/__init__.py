@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
-           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_stats", "moe_cache_residency", "moe_lfu_trace",
+           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_lfu_trace",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
@@ -117,6 +117,10 @@ def lib() -> ctypes.CDLL:
             L.moe_decode_tokens_host.argtypes = [vp, vp, i32, vp, vp]
             L.moe_cache_stage.restype = st
             L.moe_cache_stage.argtypes = [vp, vp, i32, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            L.moe_cache_prefetch.restype = st
+            L.moe_cache_prefetch.argtypes = [vp, vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            L.moe_cache_prefetch_stats.restype = st
+            L.moe_cache_prefetch_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
             L.moe_cache_stats.restype = st
             L.moe_cache_stats.argtypes = [vp, ctypes.POINTER(moe_cache_stats_t)]
             L.moe_cache_residency.restype = st
@@ -273,6 +277,20 @@ def moe_decode_tokens_host(handle, x_host, T, y_host, stream=None) -> None:
            "moe_decode_tokens_host")
 
 
+def moe_cache_prefetch(handle, x, stream=None) -> tuple[int, int]:
+    """Router lookahead on a streamed layer; returns (predicted already resident, fills issued)."""
+    r, f = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().moe_cache_prefetch(handle, _addr(x), _stream(stream), ctypes.byref(r), ctypes.byref(f)),
+           "moe_cache_prefetch")
+    return r.value, f.value
+
+
+def moe_cache_prefetch_stats(handle) -> dict:
+    out = (ctypes.c_uint64 * 4)()
+    _check(lib().moe_cache_prefetch_stats(handle, out), "moe_cache_prefetch_stats")
+    return {"calls": out[0], "resident": out[1], "fills": out[2], "bytes_h2d": out[3]}
+
+
 def moe_cache_stage(handle, ids, n, stream=None) -> tuple[int, int]:
     h, m = ctypes.c_int32(), ctypes.c_int32()
     _check(lib().moe_cache_stage(handle, _addr(ids), n, _stream(stream), ctypes.byref(h), ctypes.byref(m)),
@@ -411,6 +429,12 @@ class MoELayer:
 
     def cache_stage(self, ids, n, stream=None):
         return moe_cache_stage(self.handle, ids, n, stream)
+
+    def cache_prefetch(self, x, stream=None):
+        return moe_cache_prefetch(self.handle, x, stream)
+
+    def prefetch_stats(self):
+        return moe_cache_prefetch_stats(self.handle)
 
     def cache_stats(self):
         return moe_cache_stats(self.handle)

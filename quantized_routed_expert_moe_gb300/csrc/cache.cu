@@ -80,6 +80,46 @@ public:
         *hits = h;
     }
 
+    // A prediction (router lookahead): admits each predicted expert that is
+    // not resident, with count 0 (it has not been used yet), and leaves the
+    // residents' counts and recency alone. Victims as in access: the least
+    // used resident outside the prediction, ties to the least recently used,
+    // then the lower id.
+    void prefetch(const int32_t* ids, int n, int* resident, std::vector<Fill>& fills) {
+        ++clock_;
+        fills.clear();
+        int r0 = 0;
+        for (int i = 0; i < n; ++i) r0 += slot_of_[ids[i]] >= 0;
+        for (int i = 0; i < n; ++i) {
+            const int e = ids[i];
+            if (slot_of_[e] >= 0) continue;
+            int slot = -1, victim = -1;
+            for (int s = 0; s < slots_; ++s)
+                if (expert_in_[s] < 0) { slot = s; break; }
+            if (slot < 0) {
+                for (int s = 0; s < slots_; ++s) {
+                    const int r = expert_in_[s];
+                    bool predicted = false;
+                    for (int j = 0; j < n; ++j) predicted |= (ids[j] == r);
+                    if (predicted) continue;
+                    if (victim < 0 || count_[r] < count_[victim] ||
+                        (count_[r] == count_[victim] &&
+                         (last_[r] < last_[victim] || (last_[r] == last_[victim] && r < victim))))
+                        victim = r;
+                }
+                if (victim < 0) break;   // every slot holds a predicted expert
+                slot = slot_of_[victim];
+                drop(victim);
+            }
+            slot_of_[e] = slot;
+            expert_in_[slot] = e;
+            count_[e] = 0;
+            last_[e] = clock_;
+            fills.push_back({e, slot, victim});
+        }
+        *resident = r0;
+    }
+
     // Forget a resident expert (eviction, or a fill that failed).
     void drop(int e) {
         if (slot_of_[e] < 0) return;
@@ -123,6 +163,7 @@ struct CacheState {
     cudaStream_t copy = nullptr;
     moe_cache_stats_t stats{};
     std::vector<Fill> fills;
+    uint64_t pf_calls = 0, pf_resident = 0, pf_fills = 0, pf_bytes = 0;   // router lookahead
 };
 
 namespace {
@@ -210,6 +251,8 @@ void cache_destroy(Layer& L) {
     L.cache = nullptr;
 }
 
+moe_status fill_slots(Layer& L, int& filled, bool prefetch);
+
 moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int* hits, int* misses) {
     CacheState& C = *L.cache;
     const auto& d = L.d;
@@ -219,7 +262,6 @@ moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int*
             if (ids[j] == ids[i]) return fail(MOE_E_INVALID, "repeated expert id");
     }
     const auto t0 = clk::now();
-    const size_t rb = L.rec_bytes;
     // the record-table upload buffer used now must be free before anything
     // changes, so that a timeout leaves the cache as it was
     {
@@ -233,8 +275,35 @@ moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int*
         MOE_CUDA_TRY(cudaLaunchHostFunc(C.copy, sleep_host, (void*)(intptr_t)L.test_stall_copies_ms));
     int h = 0;
     C.lfu.access(ids, n, &h, C.fills);
-    moe_status st = MOE_OK;
     int filled = 0;
+    moe_status st = fill_slots(L, filled, false);
+    // publish the record table (double-buffered pinned upload)
+    {
+        const int b = C.tab_idx;   // free: waited for above
+        std::memcpy(C.tab_pinned[b], C.table.data(), C.table.size() * sizeof(void*));
+        MOE_CUDA_TRY(cudaMemcpyAsync(L.rec_table, C.tab_pinned[b], C.table.size() * sizeof(void*),
+                                     cudaMemcpyHostToDevice, C.copy));
+        MOE_CUDA_TRY(cudaEventRecord(C.tab_ev[b], C.copy));
+        C.tab_idx ^= 1;
+    }
+    MOE_CUDA_TRY(cudaEventRecord(C.copies_done, C.copy));
+    MOE_CUDA_TRY(cudaStreamWaitEvent(s, C.copies_done, 0));
+    C.stats.tokens += 1;
+    C.stats.hits += (uint64_t)h;
+    C.stats.misses += (uint64_t)C.fills.size();
+    C.stats.stage_ns += (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(clk::now() - t0).count();
+    if (hits) *hits = h;
+    if (misses) *misses = (int)C.fills.size();
+    return st;
+}
+
+// The copies of C.fills on the copy stream (the slots' previous readers are
+// already ordered before them); a failing fill leaves its expert, and the
+// ones after it, out of the cache.
+moe_status fill_slots(Layer& L, int& filled, bool prefetch) {
+    CacheState& C = *L.cache;
+    const size_t rb = L.rec_bytes;
+    moe_status st = MOE_OK;
     for (const Fill& f : C.fills) {
         uint8_t* dst = C.dev_slots + (size_t)f.slot * rb;
         if (f.victim >= 0) C.table[f.victim] = nullptr;
@@ -266,27 +335,51 @@ moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int*
         }
         if (!C.records) MOE_CUDA_TRY(cudaEventRecord(C.staging_ev[C.staging_idx ^ 1], C.copy));
         C.table[f.expert] = dst;
-        C.stats.bytes_h2d += rb;
+        (prefetch ? C.pf_bytes : C.stats.bytes_h2d) += rb;
         ++filled;
     }
-    // publish the record table (double-buffered pinned upload)
+    return st;
+}
+
+// Router lookahead (Colibri analysis report, caching and prefetch: the state
+// entering layer L, passed through the router of layer L + 1, predicts that
+// layer's experts one layer ahead, and the predicted weights are loaded while
+// layer L computes). On this (next) layer: its router runs on `x` on the copy
+// stream once the work queued on `s` so far is done, the predicted ids come
+// back to the host, and the predicted experts that are not resident are
+// copied into slots on the copy stream. `s` does not wait for those copies;
+// the layer's next stage (its next decode or prefill chunk) does.
+moe_status cache_prefetch(Layer& L, const void* x, cudaStream_t s, int* resident, int* fills) {
+    CacheState& C = *L.cache;
+    const int k = L.d.top_k;
     {
-        const int b = C.tab_idx;   // free: waited for above
+        const moe_status sw = wait_event(L, C.tab_ev[C.tab_idx], "record table buffer reuse");
+        if (sw != MOE_OK) return sw;
+    }
+    MOE_CUDA_TRY(cudaEventRecord(C.stream_mark, s));
+    MOE_CUDA_TRY(cudaStreamWaitEvent(C.copy, C.stream_mark, 0));
+    cudaError_t e = launch_route_decode(L, x, C.copy, 1);
+    if (e != cudaSuccess) return cuda_fail(e, "lookahead router launch");
+    MOE_CUDA_TRY(cudaMemcpyAsync(C.ids_host, L.ids, (size_t)k * 4, cudaMemcpyDeviceToHost, C.copy));
+    MOE_CUDA_TRY(cudaEventRecord(C.ids_ready, C.copy));
+    moe_status st = wait_event(L, C.ids_ready, "predicted expert ids");
+    if (st != MOE_OK) return st;
+    int r = 0, filled = 0;
+    C.lfu.prefetch(C.ids_host, k, &r, C.fills);
+    st = fill_slots(L, filled, true);
+    {
+        const int b = C.tab_idx;
         std::memcpy(C.tab_pinned[b], C.table.data(), C.table.size() * sizeof(void*));
         MOE_CUDA_TRY(cudaMemcpyAsync(L.rec_table, C.tab_pinned[b], C.table.size() * sizeof(void*),
                                      cudaMemcpyHostToDevice, C.copy));
         MOE_CUDA_TRY(cudaEventRecord(C.tab_ev[b], C.copy));
         C.tab_idx ^= 1;
     }
-    MOE_CUDA_TRY(cudaEventRecord(C.copies_done, C.copy));
-    MOE_CUDA_TRY(cudaStreamWaitEvent(s, C.copies_done, 0));
-    C.stats.tokens += 1;
-    C.stats.hits += (uint64_t)h;
-    C.stats.misses += (uint64_t)C.fills.size();
-    C.stats.stage_ns += (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(clk::now() - t0).count();
-    if (hits) *hits = h;
-    if (misses) *misses = (int)C.fills.size();
-    (void)filled;
+    C.pf_calls += 1;
+    C.pf_resident += (uint64_t)r;
+    C.pf_fills += (uint64_t)filled;
+    if (resident) *resident = r;
+    if (fills) *fills = (int)C.fills.size();
     return st;
 }
 
@@ -327,6 +420,32 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
 }  // namespace moe
 
 extern "C" {
+
+moe_status moe_cache_prefetch(moe_layer* layer, const void* x, void* stream, int32_t* n_resident,
+                              int32_t* n_fills) {
+    if (!layer || !x) return moe::fail(MOE_E_INVALID, "NULL argument");
+    moe::Layer& L = layer->L;
+    if (!L.cache) return moe::fail(MOE_E_UNSUPPORTED, "router lookahead needs a streamed layer (cache_slots > 0)");
+    moe::DeviceGuard g(L.device);
+    if (!g.ok) return moe::cuda_fail(g.err, "cudaSetDevice");
+    int r = 0, f = 0;
+    const moe_status st = moe::cache_prefetch(L, x, static_cast<cudaStream_t>(stream), &r, &f);
+    if (n_resident) *n_resident = r;
+    if (n_fills) *n_fills = f;
+    return st;
+}
+
+moe_status moe_cache_prefetch_stats(const moe_layer* layer, uint64_t* out4) {
+    if (!layer || !out4) return moe::fail(MOE_E_INVALID, "NULL argument");
+    const moe::Layer& L = layer->L;
+    if (!L.cache) return moe::fail(MOE_E_UNSUPPORTED, "not a streamed layer");
+    const moe::CacheState& C = *L.cache;
+    out4[0] = C.pf_calls;
+    out4[1] = C.pf_resident;
+    out4[2] = C.pf_fills;
+    out4[3] = C.pf_bytes;
+    return MOE_OK;
+}
 
 moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out) {
     if (!layer || !out) return moe::fail(MOE_E_INVALID, "NULL argument");

@@ -77,6 +77,25 @@ def read_lfu():
     return slots, rows
 
 
+def read_lfu_prefetch():
+    """(slots, [(op, ids, hits_or_resident, fills)]) from lfu_prefetch.txt."""
+    slots, rows = None, []
+    for raw in open(os.path.join(GOLDEN, "lfu_prefetch.txt")):
+        line = raw.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("slots"):
+            slots = int(line.split()[1])
+            continue
+        head, mid, fills = [p.strip() for p in line.split("|")]
+        op, ids = head.split()
+        m = mid.split()[1]
+        m = [] if m == "-" else [int(v) for v in m.split(",")]
+        f = [tuple(int(v) for v in t.split(":")) for t in fills.split()[1:]]
+        rows.append((op, [int(v) for v in ids.split(",")], m, f))
+    return slots, rows
+
+
 # ---------------------------------------------------------------------------
 # small layers built by hand
 # ---------------------------------------------------------------------------
@@ -350,6 +369,15 @@ def pin_bf16_input():
     assert list(oracle.bf16_bits_to_f64(np.array([0x3FC0, 0xC0A0], np.uint16))) == [1.5, -5.0]
 
 
+def pin_lfu_prefetch_trace():
+    slots, rows = read_lfu_prefetch()
+    c = oracle.LFUCache(slots)
+    for op, ids, want, fills in rows:
+        got, f = (c.access if op == "token" else c.prefetch)(ids)
+        assert got == want, (op, ids, got, want)
+        assert [tuple(v) for v in f] == fills, (op, ids, f, fills)
+
+
 def pin_lfu_trace():
     slots, rows = read_lfu()
     c = oracle.LFUCache(slots)
@@ -443,5 +471,6 @@ def pin_sigmoid_layer_pure_python():
 ALL_PINS = [pin_dequant_q4_table, pin_dequant_q8_table, pin_format_sizes,
             pin_zero_input_routing, pin_topk_is_full_sort, pin_routing_weights,
             pin_silu, pin_ffn_closed_form, pin_dense_brute_force, pin_pure_python,
-            pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace, pin_sigmoid_router_golden,
+            pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace, pin_lfu_prefetch_trace,
+            pin_sigmoid_router_golden,
             pin_sigmoid_layer_pure_python]

@@ -324,3 +324,56 @@ def test_streamed_prefill_source_failure():
         broken["on"] = False
         got = _prefill(st, spec, xd, T)
         assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------------------------- router lookahead
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("exact", [True, False])
+def test_lookahead_prefetch(exact):
+    """moe_cache_prefetch stages a prediction; the decode that follows finds the
+    predicted experts resident. With the token's own input as the prediction
+    every routed expert is a hit; with the previous token's input some are.
+    Outputs equal the resident layer's bit for bit, and the slots follow the
+    oracle's LFU run of the same predictions and tokens."""
+    import torch
+    spec = si.LayerSpec(hidden=512, inter=256, n_experts=64, zipf_alpha=1.1)
+    layer = si.gen_layer(37, 0, spec)
+    T, k = 24, spec.top_k
+    y_res, _, ids, _, _ = _streamed_vs_resident(layer, T, seed=37)
+    X = si.gen_tokens(37, 0, T, spec)
+    xs = torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).cuda()
+    with moe.MoELayer(layer, max_tokens=T) as res:
+        recs = packed_records(layer, res.desc)
+        # the selection each prediction input gives (the router of this layer)
+        pid = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        pw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        res.route(xs, T, pid, pw)
+        torch.cuda.synchronize()
+        pred_ids = pid.cpu().numpy()
+    y = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    sim = oracle.moe.LFUCache(16)
+    with moe.MoELayer(layer, cache_slots=16, records=recs) as st:
+        with moe.MoELayer(layer) as plain:
+            with pytest.raises(moe.MoEError) as ei:
+                plain.cache_prefetch(xs[0])
+            assert ei.value.status == 2   # MOE_E_UNSUPPORTED on a resident layer
+        for t in range(T):
+            src = t if exact else max(t - 1, 0)
+            s0 = st.cache_stats()
+            r, f = st.cache_prefetch(xs[src])
+            want_r, want_f = sim.prefetch(pred_ids[src])
+            assert (r, f) == (len(want_r), len(want_f))
+            st.decode(xs[t], None, y[t])
+            torch.cuda.synchronize()
+            h, _ = sim.access(ids[t])
+            s1 = st.cache_stats()
+            assert s1["hits"] - s0["hits"] == len(h)
+            if exact:
+                assert len(h) == k
+            residency = st.residency()
+            for e, s in sim.slot_of.items():
+                assert residency[s] == e
+        ps = st.prefetch_stats()
+        assert ps["calls"] == T
+    assert np.array_equal(y.cpu().numpy(), y_res)

@@ -119,6 +119,22 @@ def _sig_weights_from_keys(layer, l):
     return key, (None if sc is None else key)
 
 
+class _LfuPrefetchCountsUse(om.LFUCache):
+    def prefetch(self, ids):
+        r, f = super().prefetch(ids)
+        for e, _, _ in f:
+            self.count[e] = 1
+        return r, f
+
+
+class _LfuPrefetchRefreshes(om.LFUCache):
+    def prefetch(self, ids):
+        r, f = super().prefetch(ids)
+        for e in r:
+            self.last[e] = self.clock
+        return r, f
+
+
 def _sig_is_tanh(l):
     return np.tanh(np.asarray(l, np.float64))
 
@@ -140,6 +156,8 @@ MISTAKES = {
     "sigmoid weights not scaled": ("routing_weights_sigmoid", _sig_not_scaled),
     "sigmoid bias in the weights": ("route_keys", _sig_weights_from_keys),
     "sigmoid replaced by tanh": ("sigmoid_scores", _sig_is_tanh),
+    "prediction admitted as a use": ("LFUCache", _LfuPrefetchCountsUse),
+    "prediction refreshes residents": ("LFUCache", _LfuPrefetchRefreshes),
 }
 
 
