@@ -442,13 +442,15 @@ def run_streamed(args):
     y = torch.empty(spec.hidden, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    H = spec.hidden
+    rms_norm = torch.nn.functional.rms_norm
+
     def chain(y):
         if args.chain == "norm":   # the layer output, renormalised
-            return (y * torch.rsqrt(torch.mean(y * y) + 1e-12)).to(torch.bfloat16)
+            return rms_norm(y, (H,), eps=1e-12)
         # a residual-stream stand-in: the layer adds its output at a quarter of
         # the stream's RMS, and the sum is renormalised
-        h = x.float() + 0.25 * y * torch.rsqrt(torch.mean(y * y) + 1e-12)
-        return (h * torch.rsqrt(torch.mean(h * h) + 1e-12)).to(torch.bfloat16)
+        return rms_norm(torch.add(x.float(), rms_norm(y, (H,), eps=1e-12), alpha=0.25), (H,), eps=1e-12)
 
     def token(i):
         x.copy_(x_host[i], non_blocking=True)
@@ -457,7 +459,7 @@ def run_streamed(args):
                 # the next layer's router on this layer's input: stage its predicted experts now
                 stack[li + 1].cache_prefetch(x, stream=stream)
             ml.decode(x, None, y, stream=stream)
-            x.copy_(chain(y))
+            x.copy_(chain(y))   # bf16 rounding in the copy
 
     for i in range(args.warmup):
         token(i)

@@ -164,6 +164,7 @@ struct CacheState {
     moe_cache_stats_t stats{};
     std::vector<Fill> fills;
     uint64_t pf_calls = 0, pf_resident = 0, pf_fills = 0, pf_bytes = 0;   // router lookahead
+    bool copies_pending = false;   // copies (lookahead fills) the caller's stream has not waited for
 };
 
 namespace {
@@ -268,13 +269,23 @@ moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int*
         const moe_status sw = wait_event(L, C.tab_ev[C.tab_idx], "record table buffer reuse");
         if (sw != MOE_OK) return sw;
     }
+    int h = 0;
+    C.lfu.access(ids, n, &h, C.fills);
+    if (C.fills.empty() && !C.copies_pending) {
+        // every expert resident and no copy in flight: the slots and the
+        // record table already hold what the kernels read
+        C.stats.tokens += 1;
+        C.stats.hits += (uint64_t)h;
+        C.stats.stage_ns += (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(clk::now() - t0).count();
+        if (hits) *hits = h;
+        if (misses) *misses = 0;
+        return MOE_OK;
+    }
     // work already queued on `s` may still read the slots that are about to be refilled
     MOE_CUDA_TRY(cudaEventRecord(C.stream_mark, s));
     MOE_CUDA_TRY(cudaStreamWaitEvent(C.copy, C.stream_mark, 0));
     if (L.test_stall_copies_ms > 0)
         MOE_CUDA_TRY(cudaLaunchHostFunc(C.copy, sleep_host, (void*)(intptr_t)L.test_stall_copies_ms));
-    int h = 0;
-    C.lfu.access(ids, n, &h, C.fills);
     int filled = 0;
     moe_status st = fill_slots(L, filled, false);
     // publish the record table (double-buffered pinned upload)
@@ -288,6 +299,7 @@ moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int*
     }
     MOE_CUDA_TRY(cudaEventRecord(C.copies_done, C.copy));
     MOE_CUDA_TRY(cudaStreamWaitEvent(s, C.copies_done, 0));
+    C.copies_pending = false;
     C.stats.tokens += 1;
     C.stats.hits += (uint64_t)h;
     C.stats.misses += (uint64_t)C.fills.size();
@@ -367,13 +379,14 @@ moe_status cache_prefetch(Layer& L, const void* x, cudaStream_t s, int* resident
     int r = 0, filled = 0;
     C.lfu.prefetch(C.ids_host, k, &r, C.fills);
     st = fill_slots(L, filled, true);
-    {
+    if (!C.fills.empty()) {
         const int b = C.tab_idx;
         std::memcpy(C.tab_pinned[b], C.table.data(), C.table.size() * sizeof(void*));
         MOE_CUDA_TRY(cudaMemcpyAsync(L.rec_table, C.tab_pinned[b], C.table.size() * sizeof(void*),
                                      cudaMemcpyHostToDevice, C.copy));
         MOE_CUDA_TRY(cudaEventRecord(C.tab_ev[b], C.copy));
         C.tab_idx ^= 1;
+        C.copies_pending = true;
     }
     C.pf_calls += 1;
     C.pf_resident += (uint64_t)r;
