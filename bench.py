@@ -55,8 +55,9 @@ def algorithmic_bytes(spec: si.LayerSpec):
     router = spec.n_experts * spec.hidden * 4 if spec.router_fmt == "f32" else \
         spec.n_experts * spec.hidden + spec.n_experts * spec.hidden // 64 * 4
     ns = spec.top_k + spec.n_shared
-    gu = ns * 2 * spec.inter * (spec.hidden // 2 + spec.hidden // 16)
-    down = ns * spec.hidden * (spec.inter // 2 + spec.inter // 16)
+    b = spec.expert_bits
+    gu = ns * 2 * spec.inter * (spec.hidden * b // 8 + spec.hidden // 16)
+    down = ns * spec.hidden * (spec.inter * b // 8 + spec.inter // 16)
     return router + gu + down, gu, down, router
 
 
@@ -655,7 +656,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="glm_decode",
-                    choices=["glm_decode", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense", "glm_verify",
+                    choices=["glm_decode", "glm_decode_q2", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense", "glm_verify",
                              "glm_streamed", "glm_streamed_prefill"])
     ap.add_argument("--layers", type=int, default=75, help="glm_streamed: layers in the stack")
     ap.add_argument("--pool", type=int, default=256,
@@ -690,6 +691,7 @@ def main():
         import dataclasses
         spec = dataclasses.replace(spec, n_experts=args.experts)
     desc = {"glm_decode": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q4g64 experts, fp32 router",
+            "glm_decode_q2": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q2g64 experts, fp32 router",
             "gemma_decode": "Gemma-style decode: H2816 I704 E128 top-8 + 1 shared, q4g64 experts, q8g64 router",
             "tiny": "tiny layer: H512 I256 E32 top-8 + 1 shared, fp32 I/O"}[args.workload]
     if args.experts:
@@ -714,7 +716,7 @@ def main():
     if ws > 1:
         dist.barrier()
 
-    R = args.replicas or {"glm_decode": 4, "gemma_decode": 16, "tiny": 64}[args.workload]
+    R = args.replicas or {"glm_decode": 4, "glm_decode_q2": 4, "gemma_decode": 16, "tiny": 64}[args.workload]
     layer = si.gen_layer(0, 0, spec)
     reps = [moe.MoELayer(layer, device=local) for _ in range(R)]
     path = {"auto": moe.MOE_PATH_AUTO, "split": moe.MOE_PATH_SPLIT, "fused": moe.MOE_PATH_FUSED}[args.path]
@@ -868,7 +870,7 @@ def main():
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        n_cpu = {"glm_decode": 6, "gemma_decode": 60, "tiny": 400}[args.workload]
+        n_cpu = {"glm_decode": 6, "glm_decode_q2": 6, "gemma_decode": 60, "tiny": 400}[args.workload]
         v = oracle_sample(layer, X, n_cpu)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n_cpu} tokens of the same layer through the fp64 numpy oracle, 1 BLAS thread"}

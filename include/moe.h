@@ -64,10 +64,11 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
-typedef enum { MOE_W_F32 = 0, MOE_W_Q8G64 = 1, MOE_W_Q4G64 = 2 } moe_wfmt;
+typedef enum { MOE_W_F32 = 0, MOE_W_Q8G64 = 1, MOE_W_Q4G64 = 2, MOE_W_Q2G64 = 3 } moe_wfmt;
 
 /* Affine group-64 matrix [N][K] in canonical storage (host memory):
  *   codes: 4-bit: uint8 [N][K/2], element k in byte k/2, low nibble for even k;
+ *          2-bit: uint8 [N][K/4], element k in byte k/4 at bits 2*(k%4) (low bits first);
  *          8-bit: uint8 [N][K];
  *   scale, bias: IEEE binary16 bit patterns [N][K/64];
  *   element (n, k) = code(n, k) * scale[n][k/64] + bias[n][k/64]. */
@@ -77,7 +78,8 @@ typedef struct {
     const uint16_t* bias;
 } moe_qmat;
 
-/* One expert: gate [I][H], up [I][H], down [H][I], all 4-bit group-64. */
+/* One expert: gate [I][H], up [I][H], down [H][I], all in the layer's
+ * expert_fmt (4-bit or 2-bit group-64). */
 typedef struct {
     moe_qmat gate, up, down;
 } moe_expert;
@@ -97,7 +99,8 @@ typedef struct {
     int32_t top_k;         /* 1..MOE_MAX_TOP_K */
     int32_t n_shared;      /* 0 or 1 */
     int32_t router_fmt;    /* MOE_W_F32 or MOE_W_Q8G64 */
-    int32_t expert_fmt;    /* MOE_W_Q4G64 */
+    int32_t expert_fmt;    /* MOE_W_Q4G64, or MOE_W_Q2G64 (2-bit experts: decode only; moe_prefill_chunk
+                              with T > 1 and the fused decode path return MOE_E_UNSUPPORTED) */
     int32_t group;         /* 64 */
     int32_t act_dtype;     /* MOE_F32 or MOE_BF16: dtype of x and y */
     int32_t max_tokens;    /* largest T for moe_route / moe_prefill_chunk, 1..MOE_MAX_CHUNK */

@@ -9,7 +9,7 @@ seeded input generator, which holds no arithmetic of the method).
 See ``oracle.moe`` for the functions and the passages each one follows.
 """
 from .moe import (  # noqa: F401
-    f16_bits_to_f64, bf16_bits_to_f64, dequant_q4g64, dequant_q8g64,
+    f16_bits_to_f64, bf16_bits_to_f64, dequant_q4g64, dequant_q2g64, dequant_q8g64,
     router_weights_f64, router_logits, select_topk, routing_weights, silu,
     expert_ffn, moe_token, moe_tokens, RouteInfo, LFUCache, lfu_trace,
     layer_dense_f64, sigmoid_scores, sigmoid_keys, routing_weights_sigmoid, route_keys,

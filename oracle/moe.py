@@ -63,6 +63,27 @@ def dequant_q4g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.
     return q * s + b
 
 
+def dequant_q2g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """Affine group-64 2-bit dequantisation, W[n][k] = code(n,k) * s[n][k//64] + b[n][k//64].
+
+    Inferno README ("Model"): the routed experts of the GLM-5.2 file it runs are
+    2-bit (Q2); Colibri README ("What's implemented"): packed int2 kernels with
+    dequant-on-use. Neither prints the layout; the reading here is the 2-bit
+    sibling of the 4-bit format: codes row-major [N][K/4] bytes, element k at
+    bits 2*(k % 4) of byte k//4 (low bits first); scale and bias binary16
+    [N][K/64]. The fp64 result is exact.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    N, quarter_k = codes.shape
+    K = 4 * quarter_k
+    q = np.empty((N, K), dtype=np.float64)
+    for j in range(4):
+        q[:, j::4] = (codes >> (2 * j)) & 0x03
+    s = np.repeat(f16_bits_to_f64(scale).reshape(N, K // 64), 64, axis=1)
+    b = np.repeat(f16_bits_to_f64(bias).reshape(N, K // 64), 64, axis=1)
+    return q * s + b
+
+
 def dequant_q8g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
     """Affine group-64 8-bit dequantisation, W[n][k] = code(n,k) * s[n][k//64] + b[n][k//64].
 
@@ -212,6 +233,8 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 
 def _deq(m) -> np.ndarray:
+    if getattr(m, "bits", 4) == 2:
+        return dequant_q2g64(m.codes, m.scale, m.bias)
     return dequant_q4g64(m.codes, m.scale, m.bias)
 
 

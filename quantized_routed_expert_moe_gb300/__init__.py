@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(PKG, "_build", "libmoe_gb300.so")
 
 MOE_ABI_VERSION = 1
 MOE_F32, MOE_BF16 = 0, 1
-MOE_W_F32, MOE_W_Q8G64, MOE_W_Q4G64 = 0, 1, 2
+MOE_W_F32, MOE_W_Q8G64, MOE_W_Q4G64, MOE_W_Q2G64 = 0, 1, 2, 3
 STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOMEM",
           4: "MOE_E_CUDA", 5: "MOE_E_TIMEOUT", 6: "MOE_E_STATE", 7: "MOE_E_SOURCE"}
 
@@ -197,15 +197,16 @@ def _expert(e) -> moe_expert:
 
 
 def make_desc(hidden, inter, n_experts, top_k=8, n_shared=1, router_fmt="f32", act="bf16",
-              max_tokens=1, cache_slots=0) -> moe_layer_desc:
+              max_tokens=1, cache_slots=0, expert_bits=4) -> moe_layer_desc:
     return moe_layer_desc(MOE_ABI_VERSION, hidden, inter, n_experts, top_k, n_shared,
-                          MOE_W_F32 if router_fmt == "f32" else MOE_W_Q8G64, MOE_W_Q4G64, 64,
+                          MOE_W_F32 if router_fmt == "f32" else MOE_W_Q8G64,
+                          MOE_W_Q2G64 if expert_bits == 2 else MOE_W_Q4G64, 64,
                           MOE_BF16 if act == "bf16" else MOE_F32, max_tokens, cache_slots)
 
 
 def desc_from_spec(spec, max_tokens=1, cache_slots=0) -> moe_layer_desc:
     return make_desc(spec.hidden, spec.inter, spec.n_experts, spec.top_k, spec.n_shared,
-                     spec.router_fmt, spec.act, max_tokens, cache_slots)
+                     spec.router_fmt, spec.act, max_tokens, cache_slots, getattr(spec, "expert_bits", 4))
 
 
 def moe_expert_record_bytes(desc: moe_layer_desc) -> int:

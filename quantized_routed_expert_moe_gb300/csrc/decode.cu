@@ -95,6 +95,64 @@ __device__ __forceinline__ int row_slot_expert(int jj, int k, int E, int n_share
     return ((unsigned)e < (unsigned)E) ? e : 0;   // a valid selection never needs the clamp
 }
 
+// 16 two-bit codes of one kernel-layout word (two runs of 8: one code per byte
+// in each of (w >> 2f) & 0x03030303) against the staged runs xa, xb.
+__device__ __forceinline__ void word2_dp4a(uint32_t w, const uint4 xa, const uint4 xb, int& ah, int& al) {
+    const uint32_t ea = w & 0x03030303u, oa = (w >> 2) & 0x03030303u;
+    const uint32_t eb = (w >> 4) & 0x03030303u, ob = (w >> 6) & 0x03030303u;
+    ah = __dp4a((int)ea, (int)xa.x, ah);
+    ah = __dp4a((int)oa, (int)xa.y, ah);
+    al = __dp4a((int)ea, (int)xa.z, al);
+    al = __dp4a((int)oa, (int)xa.w, al);
+    ah = __dp4a((int)eb, (int)xb.x, ah);
+    ah = __dp4a((int)ob, (int)xb.y, ah);
+    al = __dp4a((int)eb, (int)xb.z, al);
+    al = __dp4a((int)ob, (int)xb.w, al);
+}
+
+// One 64-code group of 2-bit codes (16 bytes: words 0-1 are half-group 2G,
+// words 2-3 half-group 2G + 1) against the staged activations: the group's
+// contribution s * (D_0 + D_1) + b * (X_0 + X_1).
+__device__ __forceinline__ float group2_dot(const uint4 c, uint32_t meta, const uint4* xq, int HG, int G,
+                                            const float* Iv, const float* Xx, float acc) {
+    int h0 = 0, l0 = 0, h1 = 0, l1 = 0;
+    const int a = 2 * G, b = 2 * G + 1;
+    word2_dp4a(c.x, xq[0 * HG + a], xq[1 * HG + a], h0, l0);
+    word2_dp4a(c.y, xq[2 * HG + a], xq[3 * HG + a], h0, l0);
+    word2_dp4a(c.z, xq[0 * HG + b], xq[1 * HG + b], h1, l1);
+    word2_dp4a(c.w, xq[2 * HG + b], xq[3 * HG + b], h1, l1);
+    const float2 sb = meta_to_f2(meta);
+    const float d = (float)(h0 * 256 + l0) * Iv[a] + (float)(h1 * 256 + l1) * Iv[b];
+    return fmaf(sb.x, d, fmaf(sb.y, Xx[a] + Xx[b], acc));
+}
+
+// The same for a gate row and an up row at once, sharing the staged activations.
+__device__ __forceinline__ void group2_dot_gu(const uint4 cg, const uint4 cu, uint32_t mg, uint32_t mu,
+                                              const uint4* xq, int HG, int G, const float* Iv, const float* Xx,
+                                              float& acc_g, float& acc_u) {
+    int gh0 = 0, gl0 = 0, gh1 = 0, gl1 = 0, uh0 = 0, ul0 = 0, uh1 = 0, ul1 = 0;
+    const int a = 2 * G, b = 2 * G + 1;
+    {
+        const uint4 x0 = xq[0 * HG + a], x1 = xq[1 * HG + a], x2 = xq[2 * HG + a], x3 = xq[3 * HG + a];
+        word2_dp4a(cg.x, x0, x1, gh0, gl0);
+        word2_dp4a(cg.y, x2, x3, gh0, gl0);
+        word2_dp4a(cu.x, x0, x1, uh0, ul0);
+        word2_dp4a(cu.y, x2, x3, uh0, ul0);
+    }
+    {
+        const uint4 x0 = xq[0 * HG + b], x1 = xq[1 * HG + b], x2 = xq[2 * HG + b], x3 = xq[3 * HG + b];
+        word2_dp4a(cg.z, x0, x1, gh1, gl1);
+        word2_dp4a(cg.w, x2, x3, gh1, gl1);
+        word2_dp4a(cu.z, x0, x1, uh1, ul1);
+        word2_dp4a(cu.w, x2, x3, uh1, ul1);
+    }
+    const float ia = Iv[a], ib = Iv[b], xs = Xx[a] + Xx[b];
+    const float2 sg = meta_to_f2(mg), su = meta_to_f2(mu);
+    acc_g = fmaf(sg.x, (float)(gh0 * 256 + gl0) * ia + (float)(gh1 * 256 + gl1) * ib, fmaf(sg.y, xs, acc_g));
+    acc_u = fmaf(su.x, (float)(uh0 * 256 + ul0) * ia + (float)(uh1 * 256 + ul1) * ib, fmaf(su.y, xs, acc_u));
+}
+
+template <int BITS>
 __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* __restrict__ rec_tab,
                                                          const float* __restrict__ part, int splits,
                                                          const float* __restrict__ bias, int k, int E, int n_shared,
@@ -149,6 +207,55 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
         const int jj = r / I, i = r - jj * I;
         return rec_tab[row_slot_expert(jj, k, E, n_shared, s_ids)] + (size_t)2 * i * rbH;
     };
+    if constexpr (BITS == 2) {
+        // a lane takes whole groups of 64 codes (16 bytes each); a warp works
+        // on two row pairs at a time, so that it keeps as many bytes in flight
+        // as with 4-bit codes
+        constexpr int B2 = kGuBlock / 2;
+        const int GH = HG / 2, M2 = (GH + 31) / 32;
+        for (int p0 = warp; p0 < np; p0 += 2 * kGuWarps) {
+            const uint8_t* g[2];
+            bool live[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int p = p0 + q * kGuWarps;
+                live[q] = p < np;
+                g[q] = pair_ptr(live[q] ? p : p0);
+            }
+            float acc_g[2] = {0.f, 0.f}, acc_u[2] = {0.f, 0.f};
+            for (int m0 = 0; m0 < M2; m0 += B2) {
+                uint4 cg[2][B2], cu[2][B2];
+                uint32_t mg[2][B2], mu[2][B2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int mm = 0; mm < B2; ++mm) {
+                        const int G = lane + 32 * (m0 + mm);
+                        if (live[q] && m0 + mm < M2 && G < GH) {
+                            cg[q][mm] = ldg_stream_hint(g[q] + 16 * G, pol);
+                            cu[q][mm] = ldg_stream_hint(g[q] + rbH + 16 * G, pol);
+                            mg[q][mm] = ldg_u32_hint(g[q] + H / 4 + 4 * G, pol);
+                            mu[q][mm] = ldg_u32_hint(g[q] + rbH + H / 4 + 4 * G, pol);
+                        }
+                    }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int mm = 0; mm < B2; ++mm) {
+                        const int G = lane + 32 * (m0 + mm);
+                        if (live[q] && m0 + mm < M2 && G < GH)
+                            group2_dot_gu(cg[q][mm], cu[q][mm], mg[q][mm], mu[q][mm], xq, HG, G, Iv, Xx, acc_g[q],
+                                          acc_u[q]);
+                    }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float gv = warp_sum(acc_g[q]);
+                const float uv = warp_sum(acc_u[q]);
+                if (live[q] && lane == 0) hbuf[p0 + q * kGuWarps] = silu_f(gv) * uv;
+            }
+        }
+    } else {
     const int M = (HG + 31) / 32;
     for (int p = warp; p < np; p += kGuWarps) {
 
@@ -190,6 +297,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
         const float uv = warp_sum(acc_u);
         if (lane == 0) hbuf[p] = silu_f(gv) * uv;
     }
+    }   // BITS == 4
     __syncthreads();
     ktrace(tr, blockIdx.x, 3);
     // the CTA's SwiGLU outputs in the down kernel's staged form; a half-group
@@ -242,6 +350,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
 // (staged once per CTA in 16-bit fixed point per half-group), keeping the
 // results per (slot, row); the rows are then combined in a fixed order:
 // shared expert first (weight 1), then the routed slots in selection order.
+template <int BITS>
 __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restrict__ rec_tab,
                                                    const float* __restrict__ part, int splits,
                                                    const float* __restrict__ bias,
@@ -307,6 +416,64 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
     const int own = own1 - own0;
     const int nquad = (own + kDownRows - 1) / kDownRows;
     const int M = (IG + 31) / 32;
+    if constexpr (BITS == 2) {
+        // a lane takes whole groups of 64 codes (16 bytes each); a warp works
+        // on two items at a time, so that it keeps as many bytes in flight as
+        // with 4-bit codes
+        const int GI = IG / 2, nit = nquad * ns;
+        for (int it0 = warp; it0 < nit; it0 += 2 * kWarps) {
+            const uint8_t* rr[2][kDownRows];
+            int s2[2], n0s[2], nrs[2];
+            bool live[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int it = it0 + j * kWarps;
+                live[j] = it < nit;
+                const int itv = live[j] ? it : it0;
+                const int q = itv / ns;
+                s2[j] = itv - q * ns;
+                n0s[j] = own0 + q * kDownRows;
+                nrs[j] = min(kDownRows, own1 - n0s[j]);
+#pragma unroll
+                for (int r = 0; r < kDownRows; ++r) rr[j][r] = s_rows[s2[j]] + (size_t)(n0s[j] + min(r, nrs[j] - 1)) * rbI;
+            }
+            float acc[2][kDownRows];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int r = 0; r < kDownRows; ++r) acc[j][r] = 0.f;
+            for (int G = lane; G < GI; G += 32) {
+                uint4 c[2][kDownRows];
+                uint32_t mt[2][kDownRows];
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int r = 0; r < kDownRows; ++r)
+                        if (live[j]) {
+                            c[j][r] = ldg_stream(rr[j][r] + 16 * G);
+                            mt[j][r] = ldg_u32(rr[j][r] + I / 4 + 4 * G);
+                        }
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (live[j]) {
+                        const uint4* xs = hq + (size_t)s2[j] * 4 * IG;
+#pragma unroll
+                        for (int r = 0; r < kDownRows; ++r)
+                            acc[j][r] = group2_dot(c[j][r], mt[j][r], xs, IG, G, Iv + s2[j] * IG, Xh + s2[j] * IG,
+                                                   acc[j][r]);
+                    }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float d[kDownRows];
+#pragma unroll
+                for (int r = 0; r < kDownRows; ++r) d[r] = warp_sum(acc[j][r]);
+#pragma unroll
+                for (int r = 0; r < kDownRows; ++r)
+                    if (live[j] && lane == r && r < nrs[j]) ypart[s2[j] * kDownMaxRows + (n0s[j] - own0) + r] = d[r];
+            }
+        }
+    } else
     for (int it = warp; it < nquad * ns; it += kWarps) {
         const int q = it / ns, s = it - q * ns;
         const int n0 = own0 + q * kDownRows, nr = min(kDownRows, own1 - n0);
@@ -399,13 +566,15 @@ cudaError_t decode_kernel_setup(Layer& L) {
     if (e != cudaSuccess) return e;
     const int R1 = round32((ns * I + L.num_sms - 1) / L.num_sms);   // rows per CTA at one CTA per SM (upper bound)
     L.gu_smem = gu_smem_for(L, R1);
-    e = cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.gu_smem);
+    const void* gu = L.wbits == 2 ? (const void*)k_gateup<2> : (const void*)k_gateup<4>;
+    const void* dn = L.wbits == 2 ? (const void*)k_down<2> : (const void*)k_down<4>;
+    e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.gu_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)down_smem(I, ns));
+    e = cudaFuncSetAttribute(dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)down_smem(I, ns));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, k_gateup, kGuThreads, L.gu_smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, gu, kGuThreads, L.gu_smem);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, k_down, kThreads, down_smem(I, ns));
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, dn, kThreads, down_smem(I, ns));
     if (e != cudaSuccess) return e;
     if (L.occ_gu < 1 || L.occ_down < 1) return cudaErrorInvalidConfiguration;
     // rows owned by one down CTA must fit its partial-sum buffer
@@ -424,10 +593,10 @@ static cudaError_t launch_gateup(Layer& L, const void* x, const float* part, voi
     const int NR = (jj1 - jj0) * d.inter;
     const int R = gu_rows(L, NR);
     const int grid = (NR + R - 1) / R;
-    return launch_pdl(k_gateup, dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s, pdl,
-                      (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias, d.top_k,
-                      d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
-                      row_bytes(d.hidden), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1,
+    return launch_pdl(L.wbits == 2 ? k_gateup<2> : k_gateup<4>, dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s,
+                      pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias,
+                      d.top_k, d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
+                      row_bytes(d.hidden, L.wbits), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1,
                       L.route_mode(), tr);
 }
 
@@ -436,12 +605,11 @@ static cudaError_t launch_down(Layer& L, const float* part, const void* hblk, in
                                cudaStream_t s) {
     const auto& d = L.d;
     const int ns = d.top_k + d.n_shared;
-    return launch_pdl(k_down, dim3(down_grid(L)), dim3(kThreads), down_smem(d.inter, ns), s, pdl,
-                      (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias,
-                      d.top_k, d.n_experts, d.n_shared, d.hidden, d.inter, hblk, copies, y,
-                      d.act_dtype == MOE_BF16 ? 1 : 0,
-                      y_f32, row_bytes(d.inter), gu_block_bytes(d.hidden, d.inter), sel_ids, sel_wts,
-                      fused_error_word(L), tr);
+    return launch_pdl(L.wbits == 2 ? k_down<2> : k_down<4>, dim3(down_grid(L)), dim3(kThreads),
+                      down_smem(d.inter, ns), s, pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits,
+                      (const float*)L.router_bias, d.top_k, d.n_experts, d.n_shared, d.hidden, d.inter, hblk, copies,
+                      y, d.act_dtype == MOE_BF16 ? 1 : 0, y_f32, row_bytes(d.inter, L.wbits),
+                      gu_block_bytes(d.hidden, d.inter, L.wbits), sel_ids, sel_wts, fused_error_word(L), tr);
 }
 
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which, cudaStream_t s) {

@@ -38,7 +38,8 @@ static moe_status check_desc(const moe_layer_desc* d) {
     if (d->n_shared != 0 && d->n_shared != 1) return fail(MOE_E_INVALID, "n_shared must be 0 or 1");
     if (d->router_fmt != MOE_W_F32 && d->router_fmt != MOE_W_Q8G64)
         return fail(MOE_E_UNSUPPORTED, "router_fmt must be MOE_W_F32 or MOE_W_Q8G64");
-    if (d->expert_fmt != MOE_W_Q4G64) return fail(MOE_E_UNSUPPORTED, "expert_fmt must be MOE_W_Q4G64");
+    if (d->expert_fmt != MOE_W_Q4G64 && d->expert_fmt != MOE_W_Q2G64)
+        return fail(MOE_E_UNSUPPORTED, "expert_fmt must be MOE_W_Q4G64 or MOE_W_Q2G64");
     if (d->group != MOE_GROUP) return fail(MOE_E_UNSUPPORTED, "group must be 64");
     if (d->act_dtype != MOE_F32 && d->act_dtype != MOE_BF16) return fail(MOE_E_INVALID, "act_dtype");
     if (d->max_tokens < 1 || d->max_tokens > MOE_MAX_CHUNK)
@@ -118,7 +119,7 @@ const char* moe_last_error(void) { return g_last_error.c_str(); }
 
 size_t moe_expert_record_bytes(const moe_layer_desc* desc) {
     if (check_desc(desc) != MOE_OK) return 0;
-    return record_bytes(desc->hidden, desc->inter);
+    return record_bytes(desc->hidden, desc->inter, desc->expert_fmt == MOE_W_Q2G64 ? 2 : 4);
 }
 
 moe_status moe_pack_expert_record(const moe_layer_desc* desc, const moe_expert* expert, void* dst) {
@@ -128,7 +129,8 @@ moe_status moe_pack_expert_record(const moe_layer_desc* desc, const moe_expert* 
     const moe_qmat* m[3] = {&expert->gate, &expert->up, &expert->down};
     for (auto q : m)
         if (!q->codes || !q->scale || !q->bias) return fail(MOE_E_INVALID, "expert matrix pointer is NULL");
-    pack_expert(desc->hidden, desc->inter, *expert, static_cast<uint8_t*>(dst));
+    pack_expert(desc->hidden, desc->inter, desc->expert_fmt == MOE_W_Q2G64 ? 2 : 4, *expert,
+                static_cast<uint8_t*>(dst));
     return MOE_OK;
 }
 
@@ -165,7 +167,8 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     Layer& L = layer->L;
     L.d = d;
     L.device = device;
-    L.rec_bytes = record_bytes(d.hidden, d.inter);
+    L.wbits = d.expert_fmt == MOE_W_Q2G64 ? 2 : 4;
+    L.rec_bytes = record_bytes(d.hidden, d.inter, L.wbits);
     L.router_splits = pick_router_splits(d.hidden);
     // prefill router GEMM: enough K-splits for two CTAs per SM at 128 tokens
     // (each split a whole number of 64-wide groups)
@@ -263,7 +266,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
             if (r >= 2) e2 = cudaEventSynchronize(ev[b]);
             if (e2 != cudaSuccess) break;
             const moe_expert* src = (d.cache_slots == 0 && r < (size_t)E) ? &experts[r] : shared;
-            pack_expert(H, I, *src, stage[b]);
+            pack_expert(H, I, L.wbits, *src, stage[b]);
             e2 = cudaMemcpyAsync(L.experts + r * rb, stage[b], rb, cudaMemcpyHostToDevice, cs);
             if (e2 == cudaSuccess) e2 = cudaEventRecord(ev[b], cs);
         }
@@ -321,13 +324,13 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     L.device_bytes = need;
 
     TRY_CUDA(decode_kernel_setup(L));
-    if (T > 1) TRY_CUDA(prefill_kernel_setup(L));
-    L.fused_ok = fused_setup(L);
+    if (T > 1 && L.wbits == 4) TRY_CUDA(prefill_kernel_setup(L));
+    L.fused_ok = L.wbits == 4 && fused_setup(L);
     cudaGetLastError();  // a rejected fused configuration leaves no sticky error
 
     if (d.cache_slots > 0) {
         st = cache_create(L, records, source, source_user);
-        if (st == MOE_OK && T > 1) st = prefill_cache_setup(L);
+        if (st == MOE_OK && T > 1 && L.wbits == 4) st = prefill_cache_setup(L);
         if (st != MOE_OK) { std::string m = g_last_error; free_layer(L); delete layer; return fail(st, m); }
     }
 #undef TRY_ALLOC
@@ -389,6 +392,7 @@ moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 1) return moe_decode(layer, x, y, y_f32, stream);
+    if (L.wbits != 4) return fail(MOE_E_UNSUPPORTED, "prefill chunks need 4-bit experts (decode token by token)");
     cudaError_t e = launch_route_tokens(L, x, T, s);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     if (L.d.cache_slots > 0) return launch_prefill_streamed(L, x, T, y, y_f32, s);

@@ -48,8 +48,12 @@ struct DeviceGuard {
 // ---- kernel layout of the weights ---------------------------------------------
 //
 // A quantised row of K inputs is stored as one "row record":
-//   [ codes: K/2 bytes, canonical nibble order (element k in byte k/2, low
-//     nibble for even k) ]
+//   [ codes: 4-bit experts: K/2 bytes, canonical nibble order (element k in
+//     byte k/2, low nibble for even k). 2-bit experts: K/4 bytes; per group
+//     of 64, 4 words of 16 codes; word w holds elements 16w + j, j < 16, with
+//     byte i, bits 2f: f = 0: j = 2i, f = 1: j = 2i + 1, f = 2: j = 8 + 2i,
+//     f = 3: j = 9 + 2i (so that (word >> 2f) & 0x03030303 is the even or
+//     odd half of one run of 8, one code per byte) ]
 //   [ meta: K/64 pairs (scale, bias) as two binary16 values, scale first;
 //     zero-padded to a multiple of 16 bytes ]
 // so one row is a single contiguous, 16-byte aligned run of bytes.
@@ -62,11 +66,13 @@ struct DeviceGuard {
 // (scale, bias) binary16 pairs.
 
 inline size_t row_meta_bytes(int K) { return ((size_t)(K / 64) * 4 + 15) / 16 * 16; }
-inline size_t row_bytes(int K) { return (size_t)K / 2 + row_meta_bytes(K); }
-inline size_t gu_block_bytes(int H, int I) { return 2 * (size_t)I * row_bytes(H); }
-inline size_t record_bytes(int H, int I) { return gu_block_bytes(H, I) + (size_t)H * row_bytes(I); }
+inline size_t row_bytes(int K, int bits = 4) { return (size_t)K * bits / 8 + row_meta_bytes(K); }
+inline size_t gu_block_bytes(int H, int I, int bits = 4) { return 2 * (size_t)I * row_bytes(H, bits); }
+inline size_t record_bytes(int H, int I, int bits = 4) {
+    return gu_block_bytes(H, I, bits) + (size_t)H * row_bytes(I, bits);
+}
 
-void pack_expert(int H, int I, const moe_expert& e, uint8_t* dst);
+void pack_expert(int H, int I, int bits, const moe_expert& e, uint8_t* dst);
 
 // ---- layer ------------------------------------------------------------------
 
@@ -171,6 +177,7 @@ struct Layer {
     // fused single-kernel decode (decode_fused.cu)
     bool fused_ok = false;
     int decode_path = MOE_PATH_AUTO;
+    int wbits = 4;   // expert code width: 4 (MOE_W_Q4G64) or 2 (MOE_W_Q2G64)
     int test_no_publish = 0;
     unsigned long long* trace = nullptr;  // device [num_sms][MOE_TRACE_POINTS] when tracing is on
     unsigned long long* trace_split = nullptr;  // device [MOE_TRACE_KERNELS][MOE_TRACE_MAX_CTAS][4]

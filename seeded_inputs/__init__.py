@@ -161,7 +161,8 @@ def encode_q8g64(w: np.ndarray):
 class QMat:
     """Affine group-64 matrix [N][K] in canonical storage.
 
-    codes: uint8 [N][K/2] (4-bit, low nibble = even k) or [N][K] (8-bit);
+    codes: uint8 [N][K/2] (4-bit, low nibble = even k), [N][K/4] (2-bit,
+    element k at bits 2 (k % 4) of byte k/4) or [N][K] (8-bit);
     scale, bias: uint16 binary16 bit patterns [N][K/64].
     """
     codes: np.ndarray
@@ -213,11 +214,12 @@ class LayerSpec:
     router_score: str = "softmax"     # "softmax" | "sigmoid"
     routed_scaling: float = 1.0       # sigmoid scoring: multiplies the routing weights
     score_bias_sd: float | None = None   # sigmoid scoring: selection bias N(0, sd) per expert
+    expert_bits: int = 4              # 4 (q4g64) or 2 (q2g64) expert codes
 
     def expert_bytes(self) -> int:
-        """Canonical bytes of one 4-bit group-64 expert: 3*H*I*(1/2 + 4/64)."""
+        """Canonical bytes of one group-64 expert: 3*H*I*(bits/8 + 4/64)."""
         w = 3 * self.hidden * self.inter
-        return w // 2 + 2 * 2 * (w // 64)
+        return w * self.expert_bits // 8 + 2 * 2 * (w // 64)
 
 
 def gen_qmat4(seed: int, layer: int, expert: int, mat: int, N: int, K: int) -> QMat:
@@ -231,12 +233,24 @@ def gen_qmat4(seed: int, layer: int, expert: int, mat: int, N: int, K: int) -> Q
     return QMat(codes, scale.reshape(N, K // 64), bias.reshape(N, K // 64), 4, N, K)
 
 
+def gen_qmat2(seed: int, layer: int, expert: int, mat: int, N: int, K: int) -> QMat:
+    """2-bit codes uniform on 0..3 (four per seeded byte), scales as for 4 bits,
+    bias = -2 * scale (exact in binary16: sign flip, exponent + 1)."""
+    assert K % 64 == 0 and N > 0
+    codes = stream_bytes(key(seed, TAG_EXPERT_CODES, layer, expert, mat), N * K // 4).reshape(N, K // 4)
+    scale = f16_uniform(key(seed, TAG_EXPERT_SCALE, layer, expert, mat), N * K // 64, 0.002, 0.02)
+    assert np.all(((scale >> 10) & 0x1F) >= 1) and np.all(((scale >> 10) & 0x1F) <= 29)
+    bias = (scale + np.uint16(1 << 10)) | np.uint16(0x8000)
+    return QMat(codes, scale.reshape(N, K // 64), bias.reshape(N, K // 64), 2, N, K)
+
+
 def gen_expert(seed: int, layer: int, expert: int, spec: LayerSpec) -> Expert:
     """Expert ``expert`` of layer ``layer``; index ``n_experts`` is the shared expert."""
     H, I = spec.hidden, spec.inter
-    return Expert(gate=gen_qmat4(seed, layer, expert, MAT_GATE, I, H),
-                  up=gen_qmat4(seed, layer, expert, MAT_UP, I, H),
-                  down=gen_qmat4(seed, layer, expert, MAT_DOWN, H, I))
+    gen = gen_qmat2 if spec.expert_bits == 2 else gen_qmat4
+    return Expert(gate=gen(seed, layer, expert, MAT_GATE, I, H),
+                  up=gen(seed, layer, expert, MAT_UP, I, H),
+                  down=gen(seed, layer, expert, MAT_DOWN, H, I))
 
 
 def gen_router(seed: int, layer: int, spec: LayerSpec) -> Router:
@@ -304,6 +318,8 @@ CONFIGS = {
     "tiny": LayerSpec(hidden=512, inter=256, n_experts=32, act="f32"),
     # GLM-scale single-layer decode: H6144 I2048 E256, bf16 activations
     "glm_decode": LayerSpec(hidden=6144, inter=2048, n_experts=256),
+    # the same shape with 2-bit experts
+    "glm_decode_q2": LayerSpec(hidden=6144, inter=2048, n_experts=256, expert_bits=2),
     # Gemma-style decode: H2816 I704 E128, 8-bit group-64 router
     "gemma_decode": LayerSpec(hidden=2816, inter=704, n_experts=128, router_fmt="q8g64"),
     # 128-token prefill chunk on the GLM-scale layer with skewed popularity bias

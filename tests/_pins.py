@@ -144,6 +144,46 @@ def pin_dequant_q4_table():
             assert Fraction(float(W[0, k])) == v, (case["name"], k, float(W[0, k]), float(v))
 
 
+def pin_dequant_q2_table():
+    """Hand-worked 2-bit rows (golden/q2g64_dequant.txt) must come out exactly."""
+    for case in _read_cases(os.path.join(GOLDEN, "q2g64_dequant.txt")):
+        K = 128
+        codes = np.zeros((1, K // 4), np.uint8)
+        for i, v in case["bytes"].items():
+            codes[0, i] = v
+        sc = np.zeros((1, K // 64), np.uint16)
+        bi = np.zeros((1, K // 64), np.uint16)
+        for g, (s, b) in case["groups"].items():
+            sc[0, g], bi[0, g] = s, b
+        W = oracle.dequant_q2g64(codes, sc, bi)
+        for k, v in case["expect"].items():
+            assert Fraction(float(W[0, k])) == v, (case["name"], k, float(W[0, k]), float(v))
+
+
+def pin_q2_layer():
+    """A tiny 2-bit layer equals the pure-Python restatement; constant codes
+    give the closed form of the 4-bit case with code - 2 = 1 (code 3, bias -2s)."""
+    spec = LayerSpec(hidden=128, inter=64, n_experts=6, top_k=2, act="f32", expert_bits=2)
+    layer = si.gen_layer(17, 0, spec)
+    for t in range(2):
+        x = si.gen_tokens(17, t, 1, spec)[0]
+        y, info = oracle.moe_token(layer, x)
+        yp, S, w = _py_layer(layer, x)
+        assert list(info.ids) == S
+        assert np.allclose(y, yp, rtol=1e-11, atol=1e-14)
+    H, I, s = 128, 64, 2.0 ** -7
+    q = lambda N, K: QMat(np.full((N, K // 4), 0xFF, np.uint8), np.full((N, K // 64), 0x2000, np.uint16),
+                          np.full((N, K // 64), 0xA400, np.uint16), 2, N, K)
+    ex = Expert(q(I, H), q(I, H), q(H, I))
+    lay = Layer(LayerSpec(hidden=H, inter=I, n_experts=4, top_k=2, act="f32", expert_bits=2),
+                Router("f32", w=np.zeros((4, H), np.float32)), [ex] * 4, ex)
+    x = si.gen_tokens(18, 0, 1, LayerSpec(hidden=H, inter=I, n_experts=4, act="f32"))[0]
+    g = s * float(np.sum(x.astype(np.float64)))
+    h = g / (1 + math.exp(-g)) * g
+    y, _ = oracle.moe_token(lay, x)
+    assert np.allclose(y, 2.0 * I * s * h, rtol=1e-12, atol=0)
+
+
 def pin_dequant_q8_table():
     for case in _read_cases(os.path.join(GOLDEN, "q8g64_dequant.txt")):
         K = 128
@@ -280,8 +320,11 @@ def _py_layer(layer, x):
         return -v if bits & 0x8000 else v
 
     def w4(q, n, kk):
-        byte = int(q.codes[n, kk // 2])
-        c = (byte >> 4) if kk % 2 else (byte & 15)
+        if getattr(q, "bits", 4) == 2:
+            c = (int(q.codes[n, kk // 4]) >> (2 * (kk % 4))) & 3
+        else:
+            byte = int(q.codes[n, kk // 2])
+            c = (byte >> 4) if kk % 2 else (byte & 15)
         return c * f16(q.scale[n, kk // 64]) + f16(q.bias[n, kk // 64])
 
     def matvec(q, v):
@@ -468,7 +511,7 @@ def pin_sigmoid_layer_pure_python():
         assert list(a.ids) == list(b.ids)
 
 
-ALL_PINS = [pin_dequant_q4_table, pin_dequant_q8_table, pin_format_sizes,
+ALL_PINS = [pin_dequant_q4_table, pin_dequant_q2_table, pin_q2_layer, pin_dequant_q8_table, pin_format_sizes,
             pin_zero_input_routing, pin_topk_is_full_sort, pin_routing_weights,
             pin_silu, pin_ffn_closed_form, pin_dense_brute_force, pin_pure_python,
             pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace, pin_lfu_prefetch_trace,

@@ -92,6 +92,41 @@ def _expected_record(e, H, I):
     return b"".join(parts)
 
 
+def _expected_record_q2(e, H, I):
+    """The documented 2-bit kernel layout, built independently with numpy: per
+    word of 16 codes, byte i holds elements 2i, 2i+1, 8+2i, 9+2i at bits 0, 2, 4, 6."""
+    def rowrec(q, n, K):
+        c = np.zeros(K, np.uint8)
+        for j in range(4):
+            c[j::4] = (q.codes[n] >> (2 * j)) & 3
+        c = c.reshape(K // 16, 16)
+        out = np.zeros((K // 16, 4), np.uint8)
+        for i in range(4):
+            out[:, i] = c[:, 2 * i] | (c[:, 2 * i + 1] << 2) | (c[:, 8 + 2 * i] << 4) | (c[:, 9 + 2 * i] << 6)
+        meta = np.stack([q.scale[n], q.bias[n]], axis=1).astype(np.uint16).tobytes()
+        return out.tobytes() + meta + b"\0" * (-(len(meta)) % 16)
+    parts = []
+    for i in range(I):
+        parts.append(rowrec(e.gate, i, H))
+        parts.append(rowrec(e.up, i, H))
+    for n in range(H):
+        parts.append(rowrec(e.down, n, I))
+    return b"".join(parts)
+
+
+@pytest.mark.parametrize("H,I", [(128, 64), (192, 320)])
+def test_record_packing_q2(H, I):
+    spec = si.LayerSpec(hidden=H, inter=I, n_experts=8, act="f32", expert_bits=2)
+    e = si.gen_expert(5, 0, 1, spec)
+    d = moe.desc_from_spec(spec)
+    n = moe.moe_expert_record_bytes(d)
+    want = _expected_record_q2(e, H, I)
+    assert n == len(want)
+    buf = np.zeros(n, np.uint8)
+    moe.moe_pack_expert_record(d, e, buf)
+    assert buf.tobytes() == want
+
+
 @pytest.mark.parametrize("H,I", [(128, 64), (192, 320), (512, 256)])
 def test_record_packing(H, I):
     spec = si.LayerSpec(hidden=H, inter=I, n_experts=8)

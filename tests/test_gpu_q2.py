@@ -1,0 +1,134 @@
+"""2-bit experts (affine group-64, codes 0..3) on the GPU against the fp64 oracle.
+
+Inferno README ("Model": 2-bit routed experts) and Colibri README ("What's
+implemented": packed int2, dequant-on-use), with the storage reading in
+tests/golden/q2g64_dequant.txt. Decode (split path), the allocation-free
+decode and a streamed layer are covered; prefill chunks and the fused path
+refuse 2-bit layers with MOE_E_UNSUPPORTED.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_routed_expert_moe_gb300 as moe
+import seeded_inputs as si
+from _parity import compare_token
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from quantized_routed_expert_moe_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def q2(spec):
+    return dataclasses.replace(spec, expert_bits=2)
+
+
+SHAPES = {
+    "tiny_f32": q2(si.CONFIGS["tiny"]),
+    "bf16_mid": q2(si.LayerSpec(hidden=512, inter=320, n_experts=64, zipf_alpha=1.1)),
+    "q8_router_ragged": q2(si.LayerSpec(hidden=320, inter=128, n_experts=40, router_fmt="q8g64")),
+    "top1": q2(si.LayerSpec(hidden=192, inter=64, n_experts=9, top_k=1, act="f32")),
+    "E1024": q2(si.LayerSpec(hidden=256, inter=256, n_experts=1024)),
+    "no_shared_wide": q2(si.LayerSpec(hidden=1088, inter=704, n_experts=24, top_k=6, n_shared=0)),
+}
+
+
+def to_dev(X, spec):
+    if spec.act == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).cuda()
+    return torch.from_numpy(np.ascontiguousarray(X, dtype=np.float32)).cuda()
+
+
+def run_decode(ml, spec, X, static=False):
+    T, H, k = len(X), spec.hidden, spec.top_k
+    xd = to_dev(X, spec)
+    yd = torch.bfloat16 if spec.act == "bf16" else torch.float32
+    y = torch.empty((T, H), dtype=yd, device="cuda")
+    y32 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    for t in range(T):
+        (ml.decode_static_scratch if static else ml.decode)(xd[t], y[t], y32[t])
+        ml.route(xd[t], 1, ids[t], w[t])
+    torch.cuda.synchronize()
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16) if spec.act == "bf16" else None
+    return y32.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), yb
+
+
+def check_rows(layer, X, y32, ids, w, yb):
+    Wr = oracle.router_weights_f64(layer.router)
+    errs, flags = [], 0
+    for t in range(len(X)):
+        err, fl = compare_token(layer, X[t], y32[t], ids[t], w[t], Wr=Wr, y_bf16=None if yb is None else yb[t])
+        errs.append(err)
+        flags += fl
+    return max(errs), flags
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_q2_decode(name):
+    spec = SHAPES[name]
+    layer = si.gen_layer(51, 0, spec)
+    X = si.gen_tokens(51, 0, 10, spec)
+    with moe.MoELayer(layer) as ml:
+        y32, ids, w, yb = run_decode(ml, spec, X)
+        st, bits = ml.check()
+        assert st == 0, hex(bits)
+    err, flags = check_rows(layer, X, y32, ids, w, yb)
+    print(f"{name}: max normwise err {err:.3e}, near-tie tokens {flags}")
+
+
+def test_q2_static_scratch_and_reproducible():
+    spec = SHAPES["bf16_mid"]
+    layer = si.gen_layer(52, 0, spec)
+    X = si.gen_tokens(52, 0, 6, spec)
+    with moe.MoELayer(layer) as ml:
+        a = run_decode(ml, spec, X)
+        b = run_decode(ml, spec, X)
+        c = run_decode(ml, spec, X, static=True)
+    assert np.array_equal(a[0], b[0])
+    check_rows(layer, X, *c)
+
+
+def test_q2_streamed_layer_bit_identical():
+    spec = q2(si.LayerSpec(hidden=256, inter=128, n_experts=32, zipf_alpha=1.1))
+    layer = si.gen_layer(53, 0, spec)
+    X = si.gen_tokens(53, 0, 12, spec)
+    with moe.MoELayer(layer) as res:
+        want = run_decode(res, spec, X)[0]
+        n = moe.moe_expert_record_bytes(res.desc)
+        recs = []
+        for ex in layer.experts:
+            buf = np.zeros(n, np.uint8)
+            moe.moe_pack_expert_record(res.desc, ex, buf)
+            recs.append(buf)
+    xd = to_dev(X, spec)
+    y32 = torch.empty((len(X), spec.hidden), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, cache_slots=16, records=recs) as st:
+        for t in range(len(X)):
+            st.decode(xd[t], None, y32[t])
+            torch.cuda.synchronize()
+    assert np.array_equal(y32.cpu().numpy(), want)
+
+
+def test_q2_refused_paths():
+    spec = SHAPES["tiny_f32"]
+    layer = si.gen_layer(54, 0, spec)
+    X = si.gen_tokens(54, 0, 4, spec)
+    with moe.MoELayer(layer, max_tokens=4) as ml:
+        with pytest.raises(moe.MoEError) as ei:
+            ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_FUSED)
+        assert ei.value.status == 2
+        xd = to_dev(X.reshape(-1), spec)
+        y = torch.empty(4 * spec.hidden, dtype=torch.float32, device="cuda")
+        with pytest.raises(moe.MoEError) as ei:
+            ml.prefill_chunk(xd, 4, y)
+        assert ei.value.status == 2

@@ -22,7 +22,7 @@ def test_pin(pin):
 # --- planted mistakes --------------------------------------------------------
 
 _real = {name: getattr(om, name) for name in
-         ("dequant_q4g64", "dequant_q8g64", "routing_weights", "select_topk",
+         ("dequant_q4g64", "dequant_q2g64", "dequant_q8g64", "routing_weights", "select_topk",
           "silu", "expert_ffn", "router_logits", "moe_token", "sigmoid_keys",
           "routing_weights_sigmoid", "route_keys", "sigmoid_scores")}
 
@@ -106,6 +106,16 @@ def _token_no_shared(layer, x, ids=None, Wr=None):
     return y, info
 
 
+def _deq2_fields_reversed(codes, scale, bias):
+    codes = np.asarray(codes, np.uint8)
+    rev = ((codes & 0x03) << 6) | ((codes & 0x0C) << 2) | ((codes & 0x30) >> 2) | ((codes & 0xC0) >> 6)
+    return _real["dequant_q2g64"](rev.astype(np.uint8), scale, bias)
+
+
+def _deq2_row_reversed(codes, scale, bias):
+    return _real["dequant_q2g64"](codes, scale, bias)[:, ::-1]
+
+
 def _sig_bias_dropped(s, bias):
     return _real["sigmoid_keys"](s, None)
 
@@ -152,6 +162,8 @@ MISTAKES = {
     "router bias dropped": ("router_logits", _logits_no_bias),
     "shared expert weighted": ("moe_token", _token_weighted_shared),
     "shared expert dropped": ("moe_token", _token_no_shared),
+    "2-bit fields read high bits first": ("dequant_q2g64", _deq2_fields_reversed),
+    "2-bit row reversed": ("dequant_q2g64", _deq2_row_reversed),
     "sigmoid selection bias dropped": ("sigmoid_keys", _sig_bias_dropped),
     "sigmoid weights not scaled": ("routing_weights_sigmoid", _sig_not_scaled),
     "sigmoid bias in the weights": ("route_keys", _sig_weights_from_keys),
