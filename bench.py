@@ -437,6 +437,8 @@ def run_streamed(args):
         lay = si.Layer(spec, si.gen_router(0, l, spec), [], si.gen_expert(0, l, E, spec),
                        si.gen_router_bias(0, l, spec), 0, l)
         stack.append(moe.MoELayer(lay, device=local, cache_slots=16, records=recs))
+    for li in range(Lc):   # each layer warms the next one's router into L2
+        stack[li].set_next(stack[(li + 1) % Lc])
     X0 = si.gen_tokens(1000 * rank, 0, args.warmup + args.steps, spec)
     x_host = torch.from_numpy(np.ascontiguousarray(X0.view(np.int16))).view(torch.bfloat16).pin_memory()
     x = torch.empty(spec.hidden, dtype=torch.bfloat16, device="cuda")

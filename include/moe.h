@@ -163,6 +163,13 @@ moe_status moe_pack_expert_record(const moe_layer_desc* desc, const moe_expert* 
 /* Device bytes the layer holds (weights + slots + scratch). */
 size_t moe_layer_device_bytes(const moe_layer* layer);
 
+/* The layer that runs after `layer` (same device; NULL clears it). While
+ * `layer` decodes, its gate/up kernel prefetches `next`'s router weights into
+ * L2, so that the next layer's router reads them from L2 rather than HBM. A
+ * hint only: results do not depend on it. `next` must stay alive while it is
+ * set. Errors: MOE_E_INVALID for a NULL layer or a layer on another device. */
+moe_status moe_layer_set_next(moe_layer* layer, const moe_layer* next);
+
 /* ---- router scoring ---------------------------------------------------------- */
 
 /* How router logits become a selection and routing weights. */

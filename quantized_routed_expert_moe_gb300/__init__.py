@@ -26,7 +26,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
-           "moe_layer_device_bytes", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
+           "moe_layer_device_bytes", "moe_layer_set_next", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
            "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_lfu_trace",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
@@ -133,6 +133,8 @@ def lib() -> ctypes.CDLL:
             L.moe_profile_stop.argtypes = [vp, ctypes.POINTER(moe_kernel_time), i32, ctypes.POINTER(i32)]
             L.moe_layer_set_option.restype = st
             L.moe_layer_set_option.argtypes = [vp, i32, ctypes.c_int64]
+            L.moe_layer_set_next.restype = st
+            L.moe_layer_set_next.argtypes = [vp, vp]
             L.moe_layer_set_router_scoring.restype = st
             L.moe_layer_set_router_scoring.argtypes = [vp, i32, ctypes.c_float]
             L.moe_layer_check.restype = st
@@ -340,6 +342,10 @@ def moe_layer_set_option(handle, option: int, value: int) -> None:
     _check(lib().moe_layer_set_option(handle, option, value), "moe_layer_set_option")
 
 
+def moe_layer_set_next(handle, next_handle) -> None:
+    _check(lib().moe_layer_set_next(handle, next_handle), "moe_layer_set_next")
+
+
 def moe_layer_set_router_scoring(handle, scoring: int, routed_scaling: float = 1.0) -> None:
     _check(lib().moe_layer_set_router_scoring(handle, scoring, routed_scaling), "moe_layer_set_router_scoring")
 
@@ -445,6 +451,9 @@ class MoELayer:
 
     def set_option(self, option, value):
         moe_layer_set_option(self.handle, option, value)
+
+    def set_next(self, other):
+        moe_layer_set_next(self.handle, other.handle if other is not None else None)
 
     def set_router_scoring(self, scoring, routed_scaling=1.0):
         moe_layer_set_router_scoring(self.handle, scoring, routed_scaling)

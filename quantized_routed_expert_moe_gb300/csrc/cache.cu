@@ -16,6 +16,7 @@
 //     the lower expert id;
 //   * a token's IDs are processed in selection order, hits before misses, and
 //     a miss takes the lowest free slot while there is one.
+#include <atomic>
 #include <chrono>
 #include <cstring>
 #include <thread>
@@ -165,6 +166,13 @@ struct CacheState {
     std::vector<Fill> fills;
     uint64_t pf_calls = 0, pf_resident = 0, pf_fills = 0, pf_bytes = 0;   // router lookahead
     bool copies_pending = false;   // copies (lookahead fills) the caller's stream has not waited for
+    // the router's selection published into host-mapped memory: ids, then a
+    // sequence number the host polls (speculative decode)
+    int32_t* pub_ids = nullptr;    // host view [top_k]
+    unsigned* pub_seq = nullptr;   // host view [1]
+    int32_t* pub_ids_dev = nullptr;
+    unsigned* pub_seq_dev = nullptr;
+    unsigned seq = 0;
 };
 
 namespace {
@@ -184,6 +192,27 @@ moe_status wait_event(const Layer& L, cudaEvent_t ev, const char* what) {
         // a decode token's round trip is tens of microseconds: spin first,
         // then give the core back
         if (waited > std::chrono::milliseconds(2)) std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+// Host wait until the router has published sequence number `want` into
+// host-mapped memory (deadline as for events); then the ids are visible.
+moe_status wait_published(const Layer& L, const volatile unsigned* seq, unsigned want) {
+    const auto t0 = clk::now();
+    for (;;) {
+        if (*seq == want) {
+            std::atomic_thread_fence(std::memory_order_acquire);
+            return MOE_OK;
+        }
+        const auto waited = clk::now() - t0;
+        if (waited > std::chrono::milliseconds(L.host_timeout_ms))
+            return fail(MOE_E_TIMEOUT, "expert ids: host wait passed its deadline");
+        if (waited > std::chrono::milliseconds(2)) {
+            // a failed launch never publishes: report it instead of waiting out the deadline
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_fail(e, "expert ids");
+            std::this_thread::sleep_for(std::chrono::microseconds(50));
+        }
     }
 }
 
@@ -221,6 +250,11 @@ moe_status cache_create(Layer& L, const void* const* records, moe_expert_source 
         }
     }
     MOE_CUDA_TRY(cudaHostAlloc(&C->ids_host, (size_t)d.top_k * 4, cudaHostAllocDefault));
+    MOE_CUDA_TRY(cudaHostAlloc(&C->pub_ids, (size_t)d.top_k * 4, cudaHostAllocMapped));
+    MOE_CUDA_TRY(cudaHostAlloc(&C->pub_seq, 64, cudaHostAllocMapped));
+    *C->pub_seq = 0;
+    MOE_CUDA_TRY(cudaHostGetDevicePointer((void**)&C->pub_ids_dev, C->pub_ids, 0));
+    MOE_CUDA_TRY(cudaHostGetDevicePointer((void**)&C->pub_seq_dev, C->pub_seq, 0));
     MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->ids_ready, cudaEventDisableTiming));
     MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->stream_mark, cudaEventDisableTiming));
     MOE_CUDA_TRY(cudaEventCreateWithFlags(&C->copies_done, cudaEventDisableTiming));
@@ -243,6 +277,8 @@ void cache_destroy(Layer& L) {
         if (C->tab_ev[i]) cudaEventDestroy(C->tab_ev[i]);
     }
     if (C->ids_host) cudaFreeHost(C->ids_host);
+    if (C->pub_ids) cudaFreeHost(C->pub_ids);
+    if (C->pub_seq) cudaFreeHost(C->pub_seq);
     if (C->ids_ready) cudaEventDestroy(C->ids_ready);
     if (C->stream_mark) cudaEventDestroy(C->stream_mark);
     if (C->copies_done) cudaEventDestroy(C->copies_done);
@@ -406,26 +442,48 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
     CacheState& C = *L.cache;
     const auto& d = L.d;
     const int k = d.top_k;
-    // router + selection (ids, weights on the device)
-    cudaError_t e = launch_route_decode(L, x, s, 1);
+    const int jj0 = d.n_shared ? 1 : 0;
+    // Speculative launch: every expert (shared and routed) runs right after
+    // the router, from the record table as it stands. If the token needs an
+    // expert that is not resident, its record is null there and the kernels do
+    // nothing; the host then stages and launches again. With every expert
+    // resident (the common case) the host's wait for the ids overlaps the
+    // experts' compute. The router publishes the ids straight into
+    // host-mapped memory, so no copy sits between it and the experts. Not
+    // while a lookahead's copies are in flight (their slots are not ready
+    // yet): then the shared expert's gate/up alone runs while the host stages.
+    const bool spec = !C.copies_pending && L.test_stall_copies_ms == 0;
+    const unsigned want = ++C.seq;
+    cudaError_t e = spec ? launch_route_decode(L, x, s, 1, C.pub_ids_dev, C.pub_seq_dev, want)
+                         : launch_route_decode(L, x, s, 1);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
-    // the shared expert's gate/up runs while the host stages the routed experts
-    if (d.n_shared) {
-        e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, 1, false, s);
-        if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
+    moe_status st = MOE_OK;
+    if (spec) {
+        e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, jj0 + k, true, s);
+        if (e != cudaSuccess) return cuda_fail(e, "expert launch");
+        st = wait_published(L, C.pub_seq, want);
+        if (st != MOE_OK) return st;
+        for (int j = 0; j < k; ++j) C.ids_host[j] = ((volatile int32_t*)C.pub_ids)[j];
+    } else {
+        if (d.n_shared) {
+            e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, 1, false, s);
+            if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
+        }
+        MOE_CUDA_TRY(cudaMemcpyAsync(C.ids_host, L.ids, (size_t)k * 4, cudaMemcpyDeviceToHost, s));
+        MOE_CUDA_TRY(cudaEventRecord(C.ids_ready, s));
+        st = wait_event(L, C.ids_ready, "expert ids");
+        if (st != MOE_OK) return st;
     }
-    MOE_CUDA_TRY(cudaMemcpyAsync(C.ids_host, L.ids, (size_t)k * 4, cudaMemcpyDeviceToHost, s));
-    MOE_CUDA_TRY(cudaEventRecord(C.ids_ready, s));
-    moe_status st = wait_event(L, C.ids_ready, "expert ids");
-    if (st != MOE_OK) return st;
     int h = 0, m = 0;
     st = cache_stage(L, C.ids_host, k, s, &h, &m);
     if (st != MOE_OK) return st;
     for (int j = 0; j < k; ++j)
         if (C.lfu.slot_of(C.ids_host[j]) < 0)
             return fail(MOE_E_STATE, "expert " + std::to_string(C.ids_host[j]) + " is not resident");
-    const int jj0 = d.n_shared ? 1 : 0;
-    e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, jj0, jj0 + k, true, s);
+    if (spec && m == 0) return MOE_OK;   // the speculative launch had every expert
+    // after a speculative launch that met a miss every slot runs again;
+    // otherwise the shared expert's gate/up has run already
+    e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, spec ? 0 : jj0, jj0 + k, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "routed expert launch");
     return MOE_OK;
 }

@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
                                                          int32_t* __restrict__ ids_out, float* __restrict__ wts_out,
                                                          float* __restrict__ logits_out,
                                                          const int32_t* __restrict__ sel_ids, int jj0, int jj1,
-                                                         RouteMode mode, unsigned long long* __restrict__ tr) {
+                                                         RouteMode mode, const uint8_t* pf, size_t pf_bytes,
+                                                         unsigned long long* __restrict__ tr) {
     extern __shared__ uint4 smq[];
     __shared__ float s_logit[1024];
     __shared__ float s_score[1024];
@@ -174,6 +175,14 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
     float* hbuf = Xx + HG;                                             // [R]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ktrace(tr, blockIdx.x, 0);
+    if (pf && threadIdx.x == 0) {
+        // the next layer's router weights into L2 (moe_layer_set_next): this
+        // CTA's share, in 16-byte multiples, no later than 64 KB a request
+        const size_t per = (pf_bytes / gridDim.x + 15) / 16 * 16;
+        const size_t b0 = per * blockIdx.x, b1 = min(pf_bytes, b0 + per);
+        for (size_t o = b0; o < b1; o += 65536)
+            prefetch_l2(pf + o, (uint32_t)min((size_t)65536, b1 - o));
+    }
     stage_vector_q16(x, x_bf16, false, H, xq, Iv, Xx);
     __syncthreads();
     ktrace(tr, blockIdx.x, 2);
@@ -187,6 +196,17 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
         // those experts first)
         if (threadIdx.x < k) s_ids[threadIdx.x] = sel_ids[threadIdx.x];
         __syncthreads();
+        // streamed layers: a launch made before the host has staged this
+        // token's experts finds a missing expert's record null and does
+        // nothing (the host launches again once every expert is resident)
+        __shared__ int s_skip;
+        if (threadIdx.x == 0) {
+            int bad = 0;
+            for (int jj = jj0; jj < jj1; ++jj) bad |= rec_tab[row_slot_expert(jj, k, E, n_shared, s_ids)] == nullptr;
+            s_skip = bad;
+        }
+        __syncthreads();
+        if (s_skip) return;
     } else {
         // every CTA reduces the router's partial logits and selects (same result
         // everywhere); no CTA has to wait for a single selecting CTA
@@ -371,10 +391,11 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
     __shared__ const uint8_t* s_rows[MOE_MAX_TOP_K + 1];
     __shared__ float s_w[MOE_MAX_TOP_K + 1];
     __shared__ __align__(8) uint64_t s_hbar;
-    __shared__ int s_abort;
+    __shared__ int s_abort, s_skip;
     if (threadIdx.x == 0) {
         bw::mbar_init(bw::saddr(&s_hbar), 1);
         s_abort = 0;
+        s_skip = 0;
         bw::mbar_fence_init();
     }
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
@@ -405,12 +426,17 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
         const int j = sh ? k : s - n_shared;
         int e = sh ? E : s_ids[j];
         if ((unsigned)e > (unsigned)E) e = 0;
-        const uint8_t* base = rec_tab[e] + gu_block;
-        s_rows[s] = base;
+        const uint8_t* rec = rec_tab[e];
+        if (!rec) s_skip = 1;   // streamed layer, expert not resident yet: see below
+        s_rows[s] = rec + gu_block;
         s_w[s] = sh ? 1.0f : s_wts[j];
     }
     bw::mbar_wait(bw::saddr(&s_hbar), 0, &s_abort, err, 1u << 27);
     __syncthreads();
+    // a launch made before the host staged this token's experts (streamed
+    // layers) does nothing once the staged copy has landed; the host launches
+    // again when every expert is resident
+    if (s_skip) return;
     ktrace(tr, blockIdx.x, 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int own = own1 - own0;
@@ -597,7 +623,7 @@ static cudaError_t launch_gateup(Layer& L, const void* x, const float* part, voi
                       pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias,
                       d.top_k, d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
                       row_bytes(d.hidden, L.wbits), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1,
-                      L.route_mode(), tr);
+                      L.route_mode(), (const uint8_t*)L.next_router, L.next_router_bytes, tr);
 }
 
 static cudaError_t launch_down(Layer& L, const float* part, const void* hblk, int copies, void* y, float* y_f32,

@@ -231,6 +231,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
 
     // router
     TRY_ALLOC(L.router, router_bytes(d));
+    L.router_nbytes = router_bytes(d);
     if (d.router_fmt == MOE_W_F32) {
         TRY_CUDA(cudaMemcpy(L.router, router->w, (size_t)E * H * 4, cudaMemcpyHostToDevice));
     } else {
@@ -429,6 +430,20 @@ moe_status moe_decode_tokens_host(moe_layer* layer, const void* x_host, int32_t 
     }
     MOE_CUDA_TRY(cudaMemcpyAsync(y_host, L.io_y, row * T, cudaMemcpyDeviceToHost, s));
     MOE_CUDA_TRY(cudaStreamSynchronize(s));
+    return MOE_OK;
+}
+
+moe_status moe_layer_set_next(moe_layer* layer, const moe_layer* next) {
+    if (!layer) return fail(MOE_E_INVALID, "NULL layer");
+    Layer& L = layer->L;
+    if (!next) {
+        L.next_router = nullptr;
+        L.next_router_bytes = 0;
+        return MOE_OK;
+    }
+    if (next->L.device != L.device) return fail(MOE_E_INVALID, "next layer is on another device");
+    L.next_router = next->L.router;
+    L.next_router_bytes = next->L.router_nbytes / 16 * 16;   // the prefetch moves multiples of 16 bytes
     return MOE_OK;
 }
 

@@ -132,6 +132,11 @@ struct Layer {
 
     // router
     void* router = nullptr;         // fp32 [E][H], or 8-bit codes + meta
+    size_t router_nbytes = 0;
+    // moe_layer_set_next: the router weights of the layer that runs next,
+    // warmed into L2 by this layer's gate/up kernel (nullable)
+    const void* next_router = nullptr;
+    size_t next_router_bytes = 0;
     float* router_bias = nullptr;   // fp32 [E] or null
     int router_scoring = MOE_SCORE_SOFTMAX;   // moe_layer_set_router_scoring
     float routed_scaling = 1.0f;
@@ -191,7 +196,10 @@ struct Layer {
 
 // ---- launchers (decode.cu / prefill.cu) -----------------------------------------
 
-cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select);
+// ids_pub / seq_pub (host-mapped, nullable): with select, the ids are also
+// written there and then seq, for a host that polls instead of copying
+cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select, int32_t* ids_pub = nullptr,
+                                unsigned* seq_pub = nullptr, unsigned seq = 0);
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
 cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s);
 cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,

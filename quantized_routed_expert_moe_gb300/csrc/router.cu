@@ -38,7 +38,8 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     const void* __restrict__ W, const void* __restrict__ x, int x_bf16, int H, int E, int splits,
     const float* __restrict__ bias, float* __restrict__ part, float* __restrict__ logits,
     int32_t* __restrict__ ids, float* __restrict__ wts, int k, unsigned* __restrict__ counter,
-    int select, RouteMode mode, unsigned long long* __restrict__ tr) {
+    int select, RouteMode mode, int32_t* ids_pub, unsigned* seq_pub, unsigned seq,
+    unsigned long long* __restrict__ tr) {
     extern __shared__ float sm[];
     __shared__ unsigned s_last;
     const int cta = blockIdx.y * gridDim.x + blockIdx.x;
@@ -153,6 +154,13 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     }
     __syncthreads();
     block_topk_softmax(sm, E, k, ids, wts, mode.sigmoid ? sm + E : nullptr, mode.scale);
+    // streamed layers: the selection straight into host-mapped memory, then
+    // its sequence number (thread 0 wrote the ids itself)
+    if (threadIdx.x == 0 && ids_pub) {
+        for (int r = 0; r < k; ++r) ids_pub[r] = ids[r];
+        __threadfence_system();
+        *(volatile unsigned*)seq_pub = seq;
+    }
     if (threadIdx.x == 0) *counter = 0u;
     __syncthreads();
     ktrace(tr, cta, 3);
@@ -275,7 +283,8 @@ cudaError_t router_kernel_setup(Layer& L) {
     return cudaFuncSetAttribute(k_topk_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * L.d.n_experts * 4);
 }
 
-cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select) {
+cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select, int32_t* ids_pub,
+                                unsigned* seq_pub, unsigned seq) {
     const auto& d = L.d;
     dim3 grid((d.n_experts + kWarps - 1) / kWarps, L.router_splits);
     const int xb = d.act_dtype == MOE_BF16;
@@ -284,11 +293,13 @@ cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int sel
     if (d.router_fmt == MOE_W_F32)
         e = launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                        d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), L.split_trace(0));
+                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq,
+                       L.split_trace(0));
     else
         e = launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                        d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), L.split_trace(0));
+                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq,
+                       L.split_trace(0));
     prof_end(L, s);
     return e;
 }
@@ -303,11 +314,11 @@ cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, c
         return launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                           d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
                           (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
-                          (unsigned long long*)nullptr);
+                          (int32_t*)nullptr, (unsigned*)nullptr, 0u, (unsigned long long*)nullptr);
     return launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
                       (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
-                      (unsigned long long*)nullptr);
+                      (int32_t*)nullptr, (unsigned*)nullptr, 0u, (unsigned long long*)nullptr);
 }
 
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) {

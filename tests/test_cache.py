@@ -377,3 +377,47 @@ def test_lookahead_prefetch(exact):
         ps = st.prefetch_stats()
         assert ps["calls"] == T
     assert np.array_equal(y.cpu().numpy(), y_res)
+
+
+@pytest.mark.gpu
+def test_set_next_changes_no_result():
+    """moe_layer_set_next (the next layer's router warmed into L2) is a hint:
+    two chained layers, resident and streamed, give the same bits with it."""
+    import torch
+    spec = si.LayerSpec(hidden=512, inter=256, n_experts=32)
+    lays = [si.gen_layer(38, l, spec) for l in range(2)]
+    X = si.gen_tokens(38, 0, 6, spec)
+    xs = torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).cuda()
+
+    def run(mls, link):
+        if link:
+            mls[0].set_next(mls[1])
+            mls[1].set_next(mls[0])
+        y = torch.empty((len(X), spec.hidden), dtype=torch.float32, device="cuda")
+        yb = torch.empty(spec.hidden, dtype=torch.bfloat16, device="cuda")
+        for t in range(len(X)):
+            mls[0].decode(xs[t], yb, None)
+            mls[1].decode(yb.view(torch.int16), None, y[t])
+        torch.cuda.synchronize()
+        return y.cpu().numpy()
+
+    with moe.MoELayer(lays[0]) as a, moe.MoELayer(lays[1]) as b:
+        plain = run([a, b], False)
+    with moe.MoELayer(lays[0]) as a, moe.MoELayer(lays[1]) as b:
+        linked = run([a, b], True)
+        with pytest.raises(moe.MoEError):
+            moe.moe_layer_set_next(None, b.handle)
+    assert np.array_equal(plain, linked)
+    recs = []
+    for lay in lays:
+        d = moe.desc_from_spec(spec, cache_slots=16)
+        r = []
+        for ex in lay.experts:
+            buf = np.zeros(moe.moe_expert_record_bytes(d), np.uint8)
+            moe.moe_pack_expert_record(d, ex, buf)
+            r.append(buf)
+        recs.append(r)
+    with moe.MoELayer(lays[0], cache_slots=16, records=recs[0]) as a, \
+            moe.MoELayer(lays[1], cache_slots=16, records=recs[1]) as b:
+        streamed = run([a, b], True)
+    assert np.array_equal(plain, streamed)
