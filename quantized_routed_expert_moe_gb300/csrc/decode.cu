@@ -152,7 +152,7 @@ __device__ __forceinline__ void group2_dot_gu(const uint4 cg, const uint4 cu, ui
     acc_u = fmaf(su.x, (float)(uh0 * 256 + ul0) * ia + (float)(uh1 * 256 + ul1) * ib, fmaf(su.y, xs, acc_u));
 }
 
-template <int BITS>
+template <int BITS, int NQ = 1>
 __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* __restrict__ rec_tab,
                                                          const float* __restrict__ part, int splits,
                                                          const float* __restrict__ bias, int k, int E, int n_shared,
@@ -276,47 +276,70 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
             }
         }
     } else {
-    const int M = (HG + 31) / 32;
-    for (int p = warp; p < np; p += kGuWarps) {
-
-        const uint8_t* g = pair_ptr(p);
-        const uint8_t* u = g + rbH;
-        float acc_g = 0.f, acc_u = 0.f;
-        for (int m0 = 0; m0 < M; m0 += kGuBlock) {
-            uint4 cg[kGuBlock], cu[kGuBlock];
-            uint32_t mg[kGuBlock], mu[kGuBlock];
+        // 4-bit codes. A warp works on NQ row pairs at a time, and each lane
+        // issues all loads of its kGuBlock / NQ half-groups of every row
+        // before it computes. Short rows (at most kGuBlock / 2 half-groups
+        // per lane) take two pairs at a time (NQ = 2), so that as many bytes
+        // are in flight per warp as with long rows.
+        {
+            constexpr int BQ = kGuBlock / NQ;
+            const int M = (HG + 31) / 32;
+            for (int p0 = warp; p0 < np; p0 += NQ * kGuWarps) {
+                const uint8_t* g[NQ];
+                bool live[NQ];
 #pragma unroll
-            for (int mm = 0; mm < kGuBlock; ++mm) {
-                const int hg = lane + 32 * (m0 + mm);
-                if (m0 + mm < M && hg < HG) {
-                    cg[mm] = ldg_stream_hint(g + 16 * hg, pol);
-                    cu[mm] = ldg_stream_hint(u + 16 * hg, pol);
-                    mg[mm] = ldg_u32_hint(g + H / 2 + 4 * (hg >> 1), pol);
-                    mu[mm] = ldg_u32_hint(u + H / 2 + 4 * (hg >> 1), pol);
+                for (int q = 0; q < NQ; ++q) {
+                    const int p = p0 + q * kGuWarps;
+                    live[q] = p < np;
+                    g[q] = pair_ptr(live[q] ? p : p0);
                 }
-            }
+                float acc_g[NQ], acc_u[NQ];
 #pragma unroll
-            for (int mm = 0; mm < kGuBlock; ++mm) {
-                const int hg = lane + 32 * (m0 + mm);
-                if (m0 + mm < M && hg < HG) {
-                    int gh = 0, gl = 0, uh = 0, ul = 0;
+                for (int q = 0; q < NQ; ++q) acc_g[q] = acc_u[q] = 0.f;
+                for (int m0 = 0; m0 < M; m0 += BQ) {
+                    uint4 cg[NQ][BQ], cu[NQ][BQ];
+                    uint32_t mg[NQ][BQ], mu[NQ][BQ];
 #pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const uint4 xs = xq[wi * HG + hg];
-                        word_dp4a(u4w(cg[mm], wi), xs, gh, gl);
-                        word_dp4a(u4w(cu[mm], wi), xs, uh, ul);
-                    }
-                    const float iv = Iv[hg], xs = Xx[hg];
-                    const float2 sg = meta_to_f2(mg[mm]), su = meta_to_f2(mu[mm]);
-                    acc_g = fmaf(sg.x, (float)(gh * 256 + gl) * iv, fmaf(sg.y, xs, acc_g));
-                    acc_u = fmaf(su.x, (float)(uh * 256 + ul) * iv, fmaf(su.y, xs, acc_u));
+                    for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                        for (int mm = 0; mm < BQ; ++mm) {
+                            const int hg = lane + 32 * (m0 + mm);
+                            if (live[q] && m0 + mm < M && hg < HG) {
+                                const uint8_t* u = g[q] + rbH;
+                                cg[q][mm] = ldg_stream_hint(g[q] + 16 * hg, pol);
+                                cu[q][mm] = ldg_stream_hint(u + 16 * hg, pol);
+                                mg[q][mm] = ldg_u32_hint(g[q] + H / 2 + 4 * (hg >> 1), pol);
+                                mu[q][mm] = ldg_u32_hint(u + H / 2 + 4 * (hg >> 1), pol);
+                            }
+                        }
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                        for (int mm = 0; mm < BQ; ++mm) {
+                            const int hg = lane + 32 * (m0 + mm);
+                            if (live[q] && m0 + mm < M && hg < HG) {
+                                int gh = 0, gl = 0, uh = 0, ul = 0;
+#pragma unroll
+                                for (int wi = 0; wi < 4; ++wi) {
+                                    const uint4 xs = xq[wi * HG + hg];
+                                    word_dp4a(u4w(cg[q][mm], wi), xs, gh, gl);
+                                    word_dp4a(u4w(cu[q][mm], wi), xs, uh, ul);
+                                }
+                                const float iv = Iv[hg], xs = Xx[hg];
+                                const float2 sg = meta_to_f2(mg[q][mm]), su = meta_to_f2(mu[q][mm]);
+                                acc_g[q] = fmaf(sg.x, (float)(gh * 256 + gl) * iv, fmaf(sg.y, xs, acc_g[q]));
+                                acc_u[q] = fmaf(su.x, (float)(uh * 256 + ul) * iv, fmaf(su.y, xs, acc_u[q]));
+                            }
+                        }
+                }
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const float gv = warp_sum(acc_g[q]);
+                    const float uv = warp_sum(acc_u[q]);
+                    if (live[q] && lane == 0) hbuf[p0 + q * kGuWarps] = silu_f(gv) * uv;
                 }
             }
         }
-        const float gv = warp_sum(acc_g);
-        const float uv = warp_sum(acc_u);
-        if (lane == 0) hbuf[p] = silu_f(gv) * uv;
-    }
     }   // BITS == 4
     __syncthreads();
     ktrace(tr, blockIdx.x, 3);
@@ -370,7 +393,7 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
 // (staged once per CTA in 16-bit fixed point per half-group), keeping the
 // results per (slot, row); the rows are then combined in a fixed order:
 // shared expert first (weight 1), then the routed slots in selection order.
-template <int BITS>
+template <int BITS, int J = 1>
 __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restrict__ rec_tab,
                                                    const float* __restrict__ part, int splits,
                                                    const float* __restrict__ bias,
@@ -499,60 +522,89 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
                     if (live[j] && lane == r && r < nrs[j]) ypart[s2[j] * kDownMaxRows + (n0s[j] - own0) + r] = d[r];
             }
         }
-    } else
-    for (int it = warp; it < nquad * ns; it += kWarps) {
-        const int q = it / ns, s = it - q * ns;
-        const int n0 = own0 + q * kDownRows, nr = min(kDownRows, own1 - n0);
-        const uint8_t* rr[kDownRows];
+    } else {
+        // 4-bit codes. A warp works on J items at a time, and each lane issues
+        // the loads of MB half-groups of every row of them before it computes.
+        // Short rows (one half-group per lane) take two items at a time
+        // (J = 2), so that as many bytes are in flight per warp as with long
+        // rows.
+        {
+            constexpr int MB = 2 / J;
+            const int nit = nquad * ns;
+            for (int it0 = warp; it0 < nit; it0 += J * kWarps) {
+                const uint8_t* rr[J][kDownRows];
+                int s2[J], n0s[J], nrs[J];
+                bool live[J];
 #pragma unroll
-        for (int r = 0; r < kDownRows; ++r) rr[r] = s_rows[s] + (size_t)(n0 + min(r, nr - 1)) * rbI;
-        const uint4* xs = hq + (size_t)s * 4 * IG;
-        const float* ivs = Iv + s * IG;
-        const float* xsum = Xh + s * IG;
-        float acc[kDownRows];
+                for (int j = 0; j < J; ++j) {
+                    const int it = it0 + j * kWarps;
+                    live[j] = it < nit;
+                    const int itv = live[j] ? it : it0;
+                    const int q = itv / ns;
+                    s2[j] = itv - q * ns;
+                    n0s[j] = own0 + q * kDownRows;
+                    nrs[j] = min(kDownRows, own1 - n0s[j]);
 #pragma unroll
-        for (int r = 0; r < kDownRows; ++r) acc[r] = 0.f;
-        for (int m = 0; m < M; m += 2) {
-            uint4 c[2][kDownRows];
-            uint32_t mt[2][kDownRows];
+                    for (int r = 0; r < kDownRows; ++r)
+                        rr[j][r] = s_rows[s2[j]] + (size_t)(n0s[j] + min(r, nrs[j] - 1)) * rbI;
+                }
+                float acc[J][kDownRows];
 #pragma unroll
-            for (int mm = 0; mm < 2; ++mm) {
-                const int hg = lane + 32 * (m + mm);
+                for (int j = 0; j < J; ++j)
 #pragma unroll
-                for (int r = 0; r < kDownRows; ++r)
-                    if (m + mm < M && hg < IG) {
-                        c[mm][r] = ldg_stream(rr[r] + 16 * hg);
-                        mt[mm][r] = ldg_u32(rr[r] + I / 2 + 4 * (hg >> 1));
-                    }
-            }
+                    for (int r = 0; r < kDownRows; ++r) acc[j][r] = 0.f;
+                for (int m = 0; m < M; m += MB) {
+                    uint4 c[J][MB][kDownRows];
+                    uint32_t mt[J][MB][kDownRows];
 #pragma unroll
-            for (int mm = 0; mm < 2; ++mm) {
-                const int hg = lane + 32 * (m + mm);
-                if (m + mm < M && hg < IG) {
-                    int ah[kDownRows], al[kDownRows];
+                    for (int j = 0; j < J; ++j)
 #pragma unroll
-                    for (int r = 0; r < kDownRows; ++r) ah[r] = al[r] = 0;
+                        for (int mm = 0; mm < MB; ++mm) {
+                            const int hg = lane + 32 * (m + mm);
 #pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const uint4 xv = xs[wi * IG + hg];
+                            for (int r = 0; r < kDownRows; ++r)
+                                if (live[j] && m + mm < M && hg < IG) {
+                                    c[j][mm][r] = ldg_stream(rr[j][r] + 16 * hg);
+                                    mt[j][mm][r] = ldg_u32(rr[j][r] + I / 2 + 4 * (hg >> 1));
+                                }
+                        }
 #pragma unroll
-                        for (int r = 0; r < kDownRows; ++r) word_dp4a(u4w(c[mm][r], wi), xv, ah[r], al[r]);
-                    }
-                    const float iv = ivs[hg], xx = xsum[hg];
+                    for (int j = 0; j < J; ++j)
 #pragma unroll
-                    for (int r = 0; r < kDownRows; ++r) {
-                        const float2 sb = meta_to_f2(mt[mm][r]);
-                        acc[r] = fmaf(sb.x, (float)(ah[r] * 256 + al[r]) * iv, fmaf(sb.y, xx, acc[r]));
-                    }
+                        for (int mm = 0; mm < MB; ++mm) {
+                            const int hg = lane + 32 * (m + mm);
+                            if (live[j] && m + mm < M && hg < IG) {
+                                const uint4* xs = hq + (size_t)s2[j] * 4 * IG;
+                                int ah[kDownRows], al[kDownRows];
+#pragma unroll
+                                for (int r = 0; r < kDownRows; ++r) ah[r] = al[r] = 0;
+#pragma unroll
+                                for (int wi = 0; wi < 4; ++wi) {
+                                    const uint4 xv = xs[wi * IG + hg];
+#pragma unroll
+                                    for (int r = 0; r < kDownRows; ++r)
+                                        word_dp4a(u4w(c[j][mm][r], wi), xv, ah[r], al[r]);
+                                }
+                                const float iv = Iv[s2[j] * IG + hg], xx = Xh[s2[j] * IG + hg];
+#pragma unroll
+                                for (int r = 0; r < kDownRows; ++r) {
+                                    const float2 sb = meta_to_f2(mt[j][mm][r]);
+                                    acc[j][r] = fmaf(sb.x, (float)(ah[r] * 256 + al[r]) * iv, fmaf(sb.y, xx, acc[j][r]));
+                                }
+                            }
+                        }
+                }
+#pragma unroll
+                for (int j = 0; j < J; ++j) {
+                    float d[kDownRows];
+#pragma unroll
+                    for (int r = 0; r < kDownRows; ++r) d[r] = warp_sum(acc[j][r]);
+#pragma unroll
+                    for (int r = 0; r < kDownRows; ++r)
+                        if (live[j] && lane == r && r < nrs[j]) ypart[s2[j] * kDownMaxRows + (n0s[j] - own0) + r] = d[r];
                 }
             }
         }
-        float d[kDownRows];
-#pragma unroll
-        for (int r = 0; r < kDownRows; ++r) d[r] = warp_sum(acc[r]);
-#pragma unroll
-        for (int r = 0; r < kDownRows; ++r)
-            if (lane == r && r < nr) ypart[s * kDownMaxRows + (n0 - own0) + r] = d[r];
     }
     __syncthreads();
     for (int n = own0 + threadIdx.x; n < own1; n += blockDim.x) {
@@ -586,14 +638,28 @@ static size_t down_smem(int I, int ns) {
 }
 static int down_grid(const Layer& L) { return L.num_sms * L.occ_down; }
 
+using GuKernel = decltype(&k_gateup<4, 1>);
+using DownKernel = decltype(&k_down<4, 1>);
+// 4-bit rows of at most kGuBlock / 2 half-groups per lane (H <= 3072): two
+// row pairs per warp at a time; down rows of one half-group per lane
+// (I <= 1024): two items per warp at a time
+static GuKernel gu_kernel(const Layer& L) {
+    if (L.wbits == 2) return k_gateup<2, 1>;
+    return (L.d.hidden / 32 + 31) / 32 <= kGuBlock / 2 ? k_gateup<4, 2> : k_gateup<4, 1>;
+}
+static DownKernel down_kernel(const Layer& L) {
+    if (L.wbits == 2) return k_down<2, 1>;
+    return (L.d.inter / 32 + 31) / 32 == 1 ? k_down<4, 2> : k_down<4, 1>;
+}
+
 cudaError_t decode_kernel_setup(Layer& L) {
     const int H = L.d.hidden, I = L.d.inter, ns = L.d.top_k + L.d.n_shared;
     cudaError_t e = router_kernel_setup(L);
     if (e != cudaSuccess) return e;
     const int R1 = round32((ns * I + L.num_sms - 1) / L.num_sms);   // rows per CTA at one CTA per SM (upper bound)
     L.gu_smem = gu_smem_for(L, R1);
-    const void* gu = L.wbits == 2 ? (const void*)k_gateup<2> : (const void*)k_gateup<4>;
-    const void* dn = L.wbits == 2 ? (const void*)k_down<2> : (const void*)k_down<4>;
+    const void* gu = (const void*)gu_kernel(L);
+    const void* dn = (const void*)down_kernel(L);
     e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.gu_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)down_smem(I, ns));
@@ -619,7 +685,7 @@ static cudaError_t launch_gateup(Layer& L, const void* x, const float* part, voi
     const int NR = (jj1 - jj0) * d.inter;
     const int R = gu_rows(L, NR);
     const int grid = (NR + R - 1) / R;
-    return launch_pdl(L.wbits == 2 ? k_gateup<2> : k_gateup<4>, dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s,
+    return launch_pdl(gu_kernel(L), dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s,
                       pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias,
                       d.top_k, d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
                       row_bytes(d.hidden, L.wbits), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1,
@@ -631,7 +697,7 @@ static cudaError_t launch_down(Layer& L, const float* part, const void* hblk, in
                                cudaStream_t s) {
     const auto& d = L.d;
     const int ns = d.top_k + d.n_shared;
-    return launch_pdl(L.wbits == 2 ? k_down<2> : k_down<4>, dim3(down_grid(L)), dim3(kThreads),
+    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(kThreads),
                       down_smem(d.inter, ns), s, pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits,
                       (const float*)L.router_bias, d.top_k, d.n_experts, d.n_shared, d.hidden, d.inter, hblk, copies,
                       y, d.act_dtype == MOE_BF16 ? 1 : 0, y_f32, row_bytes(d.inter, L.wbits),
