@@ -389,7 +389,8 @@ def run_streamed(args):
     E, Lc, P = spec.n_experts, args.layers, args.pool
     workload = (f"streamed GLM-scale decode: {Lc} layers of H6144 I2048 E256 top-8 + 1 shared, 16-slot LFU cache "
                 f"per layer, Zipf(1.1) routing bias per layer, {P}-record alias pool in pinned host memory; "
-                f"chain: {args.chain}; router lookahead: {'on' if args.lookahead else 'off'}")
+                f"chain: {args.chain}; router lookahead: {'on' if args.lookahead else 'off'}; "
+                f"cache managed on the {'device' if args.device_cache else 'host'}")
     if args.impl == "reference":
         if rank != 0:
             return
@@ -439,6 +440,8 @@ def run_streamed(args):
         stack.append(moe.MoELayer(lay, device=local, cache_slots=16, records=recs))
     for li in range(Lc):   # each layer warms the next one's router into L2
         stack[li].set_next(stack[(li + 1) % Lc])
+        if args.device_cache:   # LFU step and fills on the device, no host round trip per layer
+            stack[li].set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
     X0 = si.gen_tokens(1000 * rank, 0, args.warmup + args.steps, spec)
     x_host = torch.from_numpy(np.ascontiguousarray(X0.view(np.int16))).view(torch.bfloat16).pin_memory()
     x = torch.empty(spec.hidden, dtype=torch.bfloat16, device="cuda")
@@ -490,6 +493,47 @@ def run_streamed(args):
     misses = sum(b["misses"] - a["misses"] for a, b in zip(s0, s1))
     # fills for misses and fills for predictions
     h2d = sum(b["bytes_h2d"] - a["bytes_h2d"] for a, b in zip(s0, s1)) + sum(p["bytes_h2d"] for p in pf)
+    graph = None
+    if args.device_cache:
+        # the same steps with each token's pass through the stack captured once
+        # as a CUDA graph (no host work per layer at all), replayed per token
+        try:
+            x_in = torch.empty_like(x)
+            gs = torch.cuda.Stream()
+            gs.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+
+            def token_g():
+                x.copy_(x_in)
+                for ml in stack:
+                    ml.decode(x, None, y, stream=gs)
+                    x.copy_(chain(y))
+            with torch.cuda.stream(gs):
+                x_in.copy_(x_host[0], non_blocking=True)
+                token_g()
+                gs.synchronize()
+                with torch.cuda.graph(g, stream=gs):
+                    token_g()
+            stream.wait_stream(gs)
+            for i in range(args.warmup):
+                x_in.copy_(x_host[i], non_blocking=True)
+                g.replay()
+            torch.cuda.synchronize()
+            gev0, gev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            gev0.record(stream)
+            for i in range(args.steps):
+                x_in.copy_(x_host[args.warmup + i], non_blocking=True)
+                g.replay()
+            gev1.record(stream)
+            torch.cuda.synchronize()
+            gms = gev0.elapsed_time(gev1)
+            graph = {"value": args.steps / (gms / 1e3), "unit": UNIT, "ms_per_step": gms / args.steps,
+                     "note": "each token through the stack captured once as a CUDA graph, replayed per token "
+                             "(the same tokens as the timed steps)"}
+            del g
+        except Exception as exc:   # reported, not fatal
+            graph = {"error": str(exc).splitlines()[0][:200]}
+            torch.cuda.synchronize()
     # pinned host -> device copy peak on this machine, for the fraction
     big = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
     dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
@@ -519,6 +563,7 @@ def run_streamed(args):
                    "record_bytes": rb, "parallelism": f"replicas x{ws}"},
         "hit_rate": hits / max(hits + misses, 1),
         "h2d_gbs": h2d_gbs,
+        "graph": graph,
         "lookahead": {"calls": sum(p["calls"] for p in pf), "predicted_resident": sum(p["resident"] for p in pf),
                       "fills": sum(p["fills"] for p in pf), "bytes_h2d": sum(p["bytes_h2d"] for p in pf)},
         "roofline": {"bound": "h2d", "achieved": h2d_gbs, "peak": h2d_peak, "unit": "GB/s",
@@ -668,6 +713,8 @@ def main():
                     help="glm_streamed: how one layer's output becomes the next layer's input")
     ap.add_argument("--lookahead", action="store_true",
                     help="glm_streamed: stage each next layer's predicted experts (moe_cache_prefetch)")
+    ap.add_argument("--device-cache", action="store_true",
+                    help="glm_streamed: device-managed caches (MOE_OPT_CACHE_DEVICE); also times the token as a CUDA graph")
     ap.add_argument("--chunk", type=int, default=None,
                     help="tokens per prefill chunk / verify batch (default 128; glm_verify: 4)")
     ap.add_argument("--replicas", type=int, default=None)
@@ -682,6 +729,8 @@ def main():
     if args.workload.startswith("glm_prefill") or args.workload == "glm_verify":
         run_prefill(args)
         return
+    if args.workload == "glm_streamed" and args.device_cache and args.lookahead:
+        ap.error("--lookahead stages on the host; it does not combine with --device-cache")
     if args.workload == "glm_streamed":
         run_streamed(args)
         return

@@ -370,7 +370,24 @@ enum {
      * stage first holds the layer's copy stream for this many milliseconds (a
      * host callback that sleeps), so that a short MOE_OPT_HOST_TIMEOUT_MS runs
      * out on the host. No device work is involved. */
-    MOE_OPT_TEST_STALL_COPIES_MS = 5
+    MOE_OPT_TEST_STALL_COPIES_MS = 5,
+    /* Device-managed cache of a streamed layer (0: off, the default; 1: on).
+     * While on, moe_decode makes no host round trip: the router's selecting
+     * block runs the LFU step (the same policy as host staging, on the same
+     * state), a copy kernel moves the missing records from host memory into
+     * their slots, reading them through their device mapping, and the expert
+     * kernels follow; a decode can be captured in a CUDA graph. Needs borrowed
+     * records (records != NULL at create) in page-locked host memory, 16-byte
+     * aligned (else MOE_E_UNSUPPORTED / MOE_E_INVALID). Switching on waits for
+     * the layer's host copies; switching off synchronises the device and
+     * hands the state back to the host. While on, moe_cache_stage,
+     * moe_cache_prefetch and streamed moe_prefill_chunk return MOE_E_STATE;
+     * moe_cache_stats and moe_cache_residency synchronise the device and
+     * report the device state (stage_ns does not grow). A token whose ids
+     * found no victim slot (impossible while top_k <= cache_slots) sets a bit
+     * that moe_layer_check reports. TurboFieldfare article ("token
+     * generation"): the 16-slot LFU cache and its misses loaded per token. */
+    MOE_OPT_CACHE_DEVICE = 6
 };
 
 /* Trace points recorded per CTA (in this order): kernel start, activations

@@ -35,7 +35,7 @@ MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_STATIC_SCRATCH_BYTES = 256 * 1024
 MOE_OPT_DECODE_PATH, MOE_OPT_TEST_STALL_ROUTING, MOE_OPT_TRACE = 1, 2, 3
-MOE_OPT_HOST_TIMEOUT_MS, MOE_OPT_TEST_STALL_COPIES_MS = 4, 5
+MOE_OPT_HOST_TIMEOUT_MS, MOE_OPT_TEST_STALL_COPIES_MS, MOE_OPT_CACHE_DEVICE = 4, 5, 6
 MOE_TRACE_POINTS = 10
 TRACE_NAMES = ("start", "x_staged", "router_done", "ids_published", "ids_seen", "gateup_done",
                "h_visible", "h_staged", "down_done", "exit")

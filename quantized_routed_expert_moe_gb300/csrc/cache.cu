@@ -16,12 +16,14 @@
 //     the lower expert id;
 //   * a token's IDs are processed in selection order, hits before misses, and
 //     a miss takes the lowest free slot while there is one.
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <cstring>
 #include <thread>
 #include <vector>
 
+#include "common.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -132,6 +134,24 @@ public:
 
     int slot_of(int e) const { return slot_of_[e]; }
     int expert_in(int s) const { return expert_in_[s]; }
+    uint64_t count(int e) const { return count_[e]; }
+    uint64_t last(int e) const { return last_[e]; }
+    uint64_t clock() const { return clock_; }
+
+    // Replace the state by a per-slot one (the device-managed cache's).
+    void load(const int32_t* expert_in, const uint32_t* count, const uint32_t* last, uint64_t clock) {
+        std::fill(slot_of_.begin(), slot_of_.end(), -1);
+        std::fill(count_.begin(), count_.end(), 0);
+        std::fill(last_.begin(), last_.end(), 0);
+        for (int s = 0; s < slots_; ++s) {
+            expert_in_[s] = expert_in[s];
+            if (expert_in[s] < 0) continue;
+            slot_of_[expert_in[s]] = s;
+            count_[expert_in[s]] = count[s];
+            last_[expert_in[s]] = last[s];
+        }
+        clock_ = clock;
+    }
 
 private:
     int slots_;
@@ -173,6 +193,11 @@ struct CacheState {
     int32_t* pub_ids_dev = nullptr;
     unsigned* pub_seq_dev = nullptr;
     unsigned seq = 0;
+    // device-managed mode (MOE_OPT_CACHE_DEVICE): the LFU state lives in
+    // dev_state, the host copies above are stale until the mode is left
+    bool device = false;
+    void* dev_state = nullptr;
+    DevCacheArgs dca;
 };
 
 namespace {
@@ -284,6 +309,7 @@ void cache_destroy(Layer& L) {
     if (C->copies_done) cudaEventDestroy(C->copies_done);
     if (C->copy) cudaStreamDestroy(C->copy);
     if (C->dev_slots) cudaFree(C->dev_slots);
+    if (C->dev_state) cudaFree(C->dev_state);
     delete C;
     L.cache = nullptr;
 }
@@ -293,6 +319,7 @@ moe_status fill_slots(Layer& L, int& filled, bool prefetch);
 moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int* hits, int* misses) {
     CacheState& C = *L.cache;
     const auto& d = L.d;
+    if (C.device) return fail(MOE_E_STATE, "the cache is device-managed (MOE_OPT_CACHE_DEVICE): host staging is off");
     for (int i = 0; i < n; ++i) {
         if (ids[i] < 0 || ids[i] >= d.n_experts) return fail(MOE_E_INVALID, "expert id out of range");
         for (int j = 0; j < i; ++j)
@@ -400,6 +427,7 @@ moe_status fill_slots(Layer& L, int& filled, bool prefetch) {
 moe_status cache_prefetch(Layer& L, const void* x, cudaStream_t s, int* resident, int* fills) {
     CacheState& C = *L.cache;
     const int k = L.d.top_k;
+    if (C.device) return fail(MOE_E_STATE, "the cache is device-managed (MOE_OPT_CACHE_DEVICE): host staging is off");
     {
         const moe_status sw = wait_event(L, C.tab_ev[C.tab_idx], "record table buffer reuse");
         if (sw != MOE_OK) return sw;
@@ -438,11 +466,153 @@ const uint8_t* cache_slots_base(const Layer& L) { return L.cache->dev_slots; }
 
 moe_status host_wait_event(const Layer& L, cudaEvent_t ev, const char* what) { return wait_event(L, ev, what); }
 
+// ---------------------------------------------------------------------------
+// device-managed mode
+// ---------------------------------------------------------------------------
+
+constexpr int kFillThreads = 256;
+
+// Copy the records the router's LFU step admitted (fills: n, then (expert,
+// slot) pairs) from host memory, read through its device mapping, into their
+// slots: each thread moves 16-byte units, 8 in flight. Nothing to do on an
+// all-hit token.
+__global__ void __launch_bounds__(kFillThreads) k_cache_fill(const int32_t* fills, const uint8_t* const* src,
+                                                             uint8_t* slots, unsigned long long rb) {
+    pdl_wait();      // the router's LFU step is complete
+    pdl_trigger();
+    const int n = fills[0];
+    const size_t units = rb / 16, stride = (size_t)gridDim.x * blockDim.x;
+    for (int f = 0; f < n; ++f) {
+        const uint4* from = reinterpret_cast<const uint4*>(src[fills[1 + 2 * f]]);
+        uint4* to = reinterpret_cast<uint4*>(slots + (size_t)fills[2 + 2 * f] * rb);
+        for (size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < units; i0 += 8 * stride) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const size_t i = i0 + u * stride;
+                if (i < units) v[u] = from[i];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const size_t i = i0 + u * stride;
+                if (i < units) to[i] = v[u];
+            }
+        }
+    }
+}
+
+bool cache_is_device(const Layer& L) { return L.cache && L.cache->device; }
+
+// On: the host LFU state goes to the device (after any host copies in flight
+// have landed), and every decode runs its LFU step and fills on the device.
+// Off: the device state comes back (after the device is idle) and host staging
+// resumes from it. Needs borrowed records in page-locked host memory, 16-byte
+// aligned: a source callback cannot run on the device.
+moe_status cache_set_device(Layer& L, bool on) {
+    CacheState& C = *L.cache;
+    const int E = L.d.n_experts, S = C.slots;
+    if (on == C.device) return MOE_OK;
+    if (on) {
+        if (!C.records)
+            return fail(MOE_E_UNSUPPORTED, "a device-managed cache needs borrowed host records, not a source callback");
+        if (L.rec_bytes % 16) return fail(MOE_E_UNSUPPORTED, "record size is not a multiple of 16 bytes");
+        std::vector<const uint8_t*> src(E);
+        for (int e = 0; e < E; ++e) {
+            void* p = nullptr;
+            if (cudaHostGetDevicePointer(&p, const_cast<void*>(C.records[e]), 0) != cudaSuccess) {
+                cudaGetLastError();
+                return fail(MOE_E_UNSUPPORTED, "record " + std::to_string(e) +
+                                                   " is not in page-locked host memory the device can read");
+            }
+            if (reinterpret_cast<uintptr_t>(p) % 16)
+                return fail(MOE_E_INVALID, "record " + std::to_string(e) + " is not 16-byte aligned");
+            src[e] = static_cast<const uint8_t*>(p);
+        }
+        if (!C.dev_state) {
+            // slot_expert, slot_count, slot_last [S] | clock | fills [1 + 2 MOE_MAX_TOP_K] | stats [4] (8-aligned) | src [E]
+            const size_t words = 3 * (size_t)S + 1 + 1 + 2 * MOE_MAX_TOP_K;
+            const size_t stats_off = (words * 4 + 7) / 8 * 8, src_off = stats_off + 4 * 8;
+            MOE_CUDA_TRY(cudaMalloc(&C.dev_state, src_off + (size_t)E * sizeof(void*)));
+            uint8_t* b = static_cast<uint8_t*>(C.dev_state);
+            C.dca.slot_expert = reinterpret_cast<int32_t*>(b);
+            C.dca.slot_count = reinterpret_cast<uint32_t*>(b) + S;
+            C.dca.slot_last = reinterpret_cast<uint32_t*>(b) + 2 * S;
+            C.dca.clock = reinterpret_cast<uint32_t*>(b) + 3 * S;
+            C.dca.fills = reinterpret_cast<int32_t*>(b) + 3 * S + 1;
+            C.dca.stats = reinterpret_cast<unsigned long long*>(b + stats_off);
+            C.dca.src = reinterpret_cast<const uint8_t* const*>(b + src_off);
+            C.dca.rec_table = (const uint8_t**)L.rec_table;
+            C.dca.slots_base = C.dev_slots;
+            C.dca.rb = L.rec_bytes;
+            C.dca.slots = S;
+            C.dca.err = fused_error_word(L);
+        }
+        // host copies (lookahead fills, table uploads) land first
+        MOE_CUDA_TRY(cudaStreamSynchronize(C.copy));
+        C.copies_pending = false;
+        std::vector<int32_t> se(S);
+        std::vector<uint32_t> cnt(S), last(S);
+        for (int s = 0; s < S; ++s) {
+            se[s] = C.lfu.expert_in(s);
+            cnt[s] = se[s] < 0 ? 0u : (uint32_t)C.lfu.count(se[s]);
+            last[s] = se[s] < 0 ? 0u : (uint32_t)C.lfu.last(se[s]);
+        }
+        const uint32_t clk = (uint32_t)C.lfu.clock();
+        const int32_t zero_fills = 0;
+        const unsigned long long zero_stats[4] = {0, 0, 0, 0};
+        MOE_CUDA_TRY(cudaMemcpy(C.dca.slot_expert, se.data(), S * 4, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemcpy(C.dca.slot_count, cnt.data(), S * 4, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemcpy(C.dca.slot_last, last.data(), S * 4, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemcpy(C.dca.clock, &clk, 4, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemcpy(C.dca.fills, &zero_fills, 4, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemcpy(C.dca.stats, zero_stats, sizeof zero_stats, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemcpy((void*)C.dca.src, src.data(), (size_t)E * sizeof(void*), cudaMemcpyHostToDevice));
+        C.device = true;
+        return MOE_OK;
+    }
+    // off: every decode already queued has run
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    std::vector<int32_t> se(S);
+    std::vector<uint32_t> cnt(S), last(S);
+    uint32_t clk = 0;
+    unsigned long long st[4];
+    MOE_CUDA_TRY(cudaMemcpy(se.data(), C.dca.slot_expert, S * 4, cudaMemcpyDeviceToHost));
+    MOE_CUDA_TRY(cudaMemcpy(cnt.data(), C.dca.slot_count, S * 4, cudaMemcpyDeviceToHost));
+    MOE_CUDA_TRY(cudaMemcpy(last.data(), C.dca.slot_last, S * 4, cudaMemcpyDeviceToHost));
+    MOE_CUDA_TRY(cudaMemcpy(&clk, C.dca.clock, 4, cudaMemcpyDeviceToHost));
+    MOE_CUDA_TRY(cudaMemcpy(st, C.dca.stats, sizeof st, cudaMemcpyDeviceToHost));
+    C.lfu.load(se.data(), cnt.data(), last.data(), clk);
+    C.stats.tokens += st[0];
+    C.stats.hits += st[1];
+    C.stats.misses += st[2];
+    C.stats.bytes_h2d += st[3];
+    // the host mirror of the record table (the device's already matches)
+    for (int e = 0; e < E; ++e) C.table[e] = nullptr;
+    for (int s = 0; s < S; ++s)
+        if (se[s] >= 0) C.table[se[s]] = C.dev_slots + (size_t)s * L.rec_bytes;
+    C.device = false;
+    return MOE_OK;
+}
+
 moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s) {
     CacheState& C = *L.cache;
     const auto& d = L.d;
     const int k = d.top_k;
     const int jj0 = d.n_shared ? 1 : 0;
+    if (C.device) {
+        // no host step: the router's selecting block runs the LFU step, the
+        // fill kernel copies the misses, the experts read the updated table
+        cudaError_t e = launch_route_decode(L, x, s, 1, nullptr, nullptr, 0, &C.dca);
+        if (e != cudaSuccess) return cuda_fail(e, "router launch");
+        prof_begin(L, K_CACHE_FILL, s);
+        e = launch_pdl(k_cache_fill, dim3(2 * L.num_sms), dim3(kFillThreads), 0, s, L.pdl,
+                       (const int32_t*)C.dca.fills, C.dca.src, C.dca.slots_base, (unsigned long long)L.rec_bytes);
+        prof_end(L, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cache fill launch");
+        e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, jj0 + k, true, s, true);
+        if (e != cudaSuccess) return cuda_fail(e, "expert launch");
+        return MOE_OK;
+    }
     // Speculative launch: every expert (shared and routed) runs right after
     // the router, from the record table as it stands. If the token needs an
     // expert that is not resident, its record is null there and the kernels do
@@ -521,7 +691,19 @@ moe_status moe_cache_prefetch_stats(const moe_layer* layer, uint64_t* out4) {
 moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out) {
     if (!layer || !out) return moe::fail(MOE_E_INVALID, "NULL argument");
     if (!layer->L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed");
-    *out = layer->L.cache->stats;
+    const moe::CacheState& C = *layer->L.cache;
+    *out = C.stats;
+    if (C.device) {   // plus the device's counts so far (every decode queued included)
+        moe::DeviceGuard g(layer->L.device);
+        if (!g.ok) return moe::cuda_fail(g.err, "cudaSetDevice");
+        MOE_CUDA_TRY(cudaDeviceSynchronize());
+        unsigned long long st[4];
+        MOE_CUDA_TRY(cudaMemcpy(st, C.dca.stats, sizeof st, cudaMemcpyDeviceToHost));
+        out->tokens += st[0];
+        out->hits += st[1];
+        out->misses += st[2];
+        out->bytes_h2d += st[3];
+    }
     return MOE_OK;
 }
 
@@ -529,6 +711,13 @@ moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert) {
     if (!layer || !slot_expert) return moe::fail(MOE_E_INVALID, "NULL argument");
     if (!layer->L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed");
     const moe::CacheState& C = *layer->L.cache;
+    if (C.device) {
+        moe::DeviceGuard g(layer->L.device);
+        if (!g.ok) return moe::cuda_fail(g.err, "cudaSetDevice");
+        MOE_CUDA_TRY(cudaDeviceSynchronize());
+        MOE_CUDA_TRY(cudaMemcpy(slot_expert, C.dca.slot_expert, (size_t)C.slots * 4, cudaMemcpyDeviceToHost));
+        return MOE_OK;
+    }
     for (int s = 0; s < C.slots; ++s) slot_expert[s] = C.lfu.expert_in(s);
     return MOE_OK;
 }

@@ -741,17 +741,18 @@ cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, floa
 // `down` adds the down + combine kernel. Plain launches (no programmatic
 // overlap): the caller orders them against the cache's copies with events.
 cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
-                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s) {
+                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s, bool pdl) {
     cudaError_t e = cudaSuccess;
     if (jj1 > jj0) {
         prof_begin(L, K_GATEUP_DECODE, s);
-        e = launch_gateup(L, x, nullptr, L.h, L.h_copies, nullptr, nullptr, nullptr, ids, jj0, jj1, false, nullptr, s);
+        e = launch_gateup(L, x, nullptr, L.h, L.h_copies, nullptr, nullptr, nullptr, ids, jj0, jj1, pdl && L.pdl,
+                          nullptr, s);
         prof_end(L, s);
         if (e != cudaSuccess) return e;
     }
     if (down) {
         prof_begin(L, K_DOWN_DECODE, s);
-        e = launch_down(L, nullptr, L.h, L.h_copies, y, y_f32, ids, wts, false, nullptr, s);
+        e = launch_down(L, nullptr, L.h, L.h_copies, y, y_f32, ids, wts, pdl && L.pdl, nullptr, s);
         prof_end(L, s);
     }
     return e;

@@ -396,7 +396,12 @@ moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y
     if (L.wbits != 4) return fail(MOE_E_UNSUPPORTED, "prefill chunks need 4-bit experts (decode token by token)");
     cudaError_t e = launch_route_tokens(L, x, T, s);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
-    if (L.d.cache_slots > 0) return launch_prefill_streamed(L, x, T, y, y_f32, s);
+    if (L.d.cache_slots > 0) {
+        if (cache_is_device(L))
+            return fail(MOE_E_STATE, "the cache is device-managed (MOE_OPT_CACHE_DEVICE): streamed prefill stages on "
+                                     "the host; switch the option off first");
+        return launch_prefill_streamed(L, x, T, y, y_f32, s);
+    }
     e = launch_prefill(L, x, T, y, y_f32, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return MOE_OK;
@@ -496,6 +501,13 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
             if (value < 0 || value > 10000) return fail(MOE_E_INVALID, "copy stall out of range 0..10000 ms");
             L.test_stall_copies_ms = (int)value;
             return MOE_OK;
+        case MOE_OPT_CACHE_DEVICE: {
+            if (value != 0 && value != 1) return fail(MOE_E_INVALID, "MOE_OPT_CACHE_DEVICE takes 0 or 1");
+            if (!L.cache) return fail(MOE_E_STATE, "layer is not streamed (cache_slots == 0)");
+            DeviceGuard g(L.device);
+            if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
+            return cache_set_device(L, value != 0);
+        }
     }
     return fail(MOE_E_INVALID, "unknown option");
 }

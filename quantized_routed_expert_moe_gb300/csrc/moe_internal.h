@@ -106,6 +106,26 @@ struct PrefillScratch {
 };
 
 struct CacheState;  // streamed mode (cache.cu)
+
+// Device-managed cache (MOE_OPT_CACHE_DEVICE): the LFU state of a streamed
+// layer in device memory, kept per slot (an expert's count and last use are
+// dropped on eviction, so only residents carry any), updated by the router's
+// selecting block, and the fills it decides, which k_cache_fill copies from
+// host-mapped records. All pointers are device pointers.
+struct DevCacheArgs {
+    int32_t* slot_expert = nullptr;     // [slots] expert held, -1 when free
+    uint32_t* slot_count = nullptr;     // [slots] uses since admission
+    uint32_t* slot_last = nullptr;      // [slots] clock of the last use
+    uint32_t* clock = nullptr;          // [1] tokens seen
+    int32_t* fills = nullptr;           // [1 + 2 MOE_MAX_TOP_K]: n, then (expert, slot) pairs
+    unsigned long long* stats = nullptr;   // [4] tokens, hits, misses, bytes
+    const uint8_t** rec_table = nullptr;   // the layer's record table [E + 1]
+    const uint8_t* const* src = nullptr;   // [E] device views of the host records
+    uint8_t* slots_base = nullptr;      // [slots][rb]
+    unsigned long long rb = 0;          // record bytes
+    int slots = 0;
+    unsigned* err = nullptr;            // error word (bit 26: no victim found)
+};
 struct Profiler;    // per-kernel event timing (profile.cu)
 
 // Kernel kinds for per-kernel timing.
@@ -198,12 +218,14 @@ struct Layer {
 
 // ids_pub / seq_pub (host-mapped, nullable): with select, the ids are also
 // written there and then seq, for a host that polls instead of copying
+// dc (nullable): the selecting block also runs the device-managed cache's LFU step
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select, int32_t* ids_pub = nullptr,
-                                unsigned* seq_pub = nullptr, unsigned seq = 0);
+                                unsigned* seq_pub = nullptr, unsigned seq = 0, const DevCacheArgs* dc = nullptr);
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
 cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s);
+// pdl: both launches may start early (the preceding kernel in `s` must be ours)
 cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
-                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s);
+                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s, bool pdl = false);
 // staged SwiGLU output block (q16 runs, inverse scales, sums) of ns slots
 inline size_t hq_block_bytes_host(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
 // K-splits of the prefill router GEMM: at most this many partial logit sets
@@ -255,6 +277,9 @@ moe_status cache_create(Layer& L, const void* const* records, moe_expert_source 
 void cache_destroy(Layer& L);
 moe_status cache_stage(Layer& L, const int32_t* ids, int n, cudaStream_t s, int* hits, int* misses);
 moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s);
+// MOE_OPT_CACHE_DEVICE: hand the LFU state to the device (on) or back to the host (off)
+moe_status cache_set_device(Layer& L, bool on);
+bool cache_is_device(const Layer& L);
 int cache_slot_of(const Layer& L, int expert);   // slot holding `expert`, -1 when not resident
 const uint8_t* cache_slots_base(const Layer& L); // device [cache_slots][rec_bytes]
 // host wait for `ev` with the layer's deadline (MOE_OPT_HOST_TIMEOUT_MS)

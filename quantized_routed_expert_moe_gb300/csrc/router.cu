@@ -7,6 +7,8 @@
 #include <cfloat>
 #include <climits>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "moe_internal.h"
 
@@ -33,12 +35,79 @@ constexpr int kWarps = kThreads / 32;
 // then reduced in split order by the last CTA to finish, which selects and
 // writes ids, weights and logits. It also clears the per-slot |h| maxima the
 // gate/up kernel of this token accumulates.
+// One token's access to a device-managed cache (thread 0, on the slot state
+// the block staged in shared memory: se expert, sc count, sl last use). The
+// policy is the host's (cache.cu) step for step, with the counts and last uses
+// kept per slot:
+//   * hits first, in selection order: count + 1, last use = this token;
+//   * then each miss in selection order takes the lowest free slot, else the
+//     slot of the resident with the smallest count that this token does not
+//     need (ties: the least recently used, then the lower expert id), and
+//     enters with count 1;
+//   * the record table points each admitted expert at its slot and forgets the
+//     evicted one; the fill list and the statistics are written for the copy
+//     kernel and the host.
+__device__ void dev_lfu_access(const DevCacheArgs& dc, const int32_t* ids_g, int n, int32_t* se, uint32_t* sc,
+                               uint32_t* sl) {
+    int32_t ids[MOE_MAX_TOP_K];
+    for (int i = 0; i < n; ++i) ids[i] = ids_g[i];
+    const int S = dc.slots;
+    const uint32_t clk = *dc.clock + 1u;
+    *dc.clock = clk;
+    int hits = 0, nf = 0;
+    for (int i = 0; i < n; ++i)
+        for (int s = 0; s < S; ++s)
+            if (se[s] == ids[i]) {
+                ++hits;
+                sc[s] += 1u;
+                sl[s] = clk;
+            }
+    for (int i = 0; i < n; ++i) {
+        const int e = ids[i];
+        bool resident = false;
+        for (int s = 0; s < S; ++s) resident |= se[s] == e;
+        if (resident) continue;
+        int slot = -1;
+        for (int s = 0; s < S && slot < 0; ++s)
+            if (se[s] < 0) slot = s;
+        if (slot < 0) {
+            int vs = -1;
+            for (int s = 0; s < S; ++s) {
+                const int r = se[s];
+                bool needed = false;
+                for (int j = 0; j < n; ++j) needed |= ids[j] == r;
+                if (needed) continue;
+                if (vs < 0 || sc[s] < sc[vs] || (sc[s] == sc[vs] && (sl[s] < sl[vs] || (sl[s] == sl[vs] && r < se[vs]))))
+                    vs = s;
+            }
+            if (vs < 0) {   // cannot happen while a token's ids fit the slots
+                atomicOr(dc.err, 1u << 26);
+                break;
+            }
+            dc.rec_table[se[vs]] = nullptr;
+            slot = vs;
+        }
+        se[slot] = e;
+        sc[slot] = 1u;
+        sl[slot] = clk;
+        dc.rec_table[e] = dc.slots_base + (size_t)slot * dc.rb;
+        dc.fills[1 + 2 * nf] = e;
+        dc.fills[2 + 2 * nf] = slot;
+        ++nf;
+    }
+    dc.fills[0] = nf;
+    dc.stats[0] += 1ull;
+    dc.stats[1] += (unsigned long long)hits;
+    dc.stats[2] += (unsigned long long)nf;
+    dc.stats[3] += (unsigned long long)nf * dc.rb;
+}
+
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads) k_router_decode(
     const void* __restrict__ W, const void* __restrict__ x, int x_bf16, int H, int E, int splits,
     const float* __restrict__ bias, float* __restrict__ part, float* __restrict__ logits,
     int32_t* __restrict__ ids, float* __restrict__ wts, int k, unsigned* __restrict__ counter,
-    int select, RouteMode mode, int32_t* ids_pub, unsigned* seq_pub, unsigned seq,
+    int select, RouteMode mode, int32_t* ids_pub, unsigned* seq_pub, unsigned seq, DevCacheArgs dc,
     unsigned long long* __restrict__ tr) {
     extern __shared__ float sm[];
     __shared__ unsigned s_last;
@@ -161,6 +230,27 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
         __threadfence_system();
         *(volatile unsigned*)seq_pub = seq;
     }
+    // device-managed cache: the LFU step for this token's ids (thread 0 wrote
+    // them), on the slot state staged in shared memory and written back
+    if (dc.slot_expert) {
+        int32_t* se = reinterpret_cast<int32_t*>(sm);
+        uint32_t* sc = reinterpret_cast<uint32_t*>(sm) + dc.slots;
+        uint32_t* sl = sc + dc.slots;
+        __syncthreads();   // the selection is done with sm
+        for (int s2 = threadIdx.x; s2 < dc.slots; s2 += blockDim.x) {
+            se[s2] = dc.slot_expert[s2];
+            sc[s2] = dc.slot_count[s2];
+            sl[s2] = dc.slot_last[s2];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) dev_lfu_access(dc, ids, k, se, sc, sl);
+        __syncthreads();
+        for (int s2 = threadIdx.x; s2 < dc.slots; s2 += blockDim.x) {
+            dc.slot_expert[s2] = se[s2];
+            dc.slot_count[s2] = sc[s2];
+            dc.slot_last[s2] = sl[s2];
+        }
+    }
     if (threadIdx.x == 0) *counter = 0u;
     __syncthreads();
     ktrace(tr, cta, 3);
@@ -271,7 +361,8 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
 // ---------------------------------------------------------------------------
 
 static size_t router_smem(const Layer& L) {
-    return (size_t)std::max(L.d.hidden / L.router_splits, 2 * L.d.n_experts) * 4;   // x slice, or keys + scores
+    // x slice, or keys + scores, or a device-managed cache's slot state
+    return (size_t)std::max({L.d.hidden / L.router_splits, 2 * L.d.n_experts, 3 * L.d.cache_slots}) * 4;
 }
 
 cudaError_t router_kernel_setup(Layer& L) {
@@ -284,7 +375,8 @@ cudaError_t router_kernel_setup(Layer& L) {
 }
 
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select, int32_t* ids_pub,
-                                unsigned* seq_pub, unsigned seq) {
+                                unsigned* seq_pub, unsigned seq, const DevCacheArgs* dc) {
+    const DevCacheArgs dca = dc ? *dc : DevCacheArgs{};
     const auto& d = L.d;
     dim3 grid((d.n_experts + kWarps - 1) / kWarps, L.router_splits);
     const int xb = d.act_dtype == MOE_BF16;
@@ -293,12 +385,12 @@ cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int sel
     if (d.router_fmt == MOE_W_F32)
         e = launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                        d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq,
+                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq, dca,
                        L.split_trace(0));
     else
         e = launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                        d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq,
+                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq, dca,
                        L.split_trace(0));
     prof_end(L, s);
     return e;
@@ -314,11 +406,11 @@ cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, c
         return launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                           d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
                           (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
-                          (int32_t*)nullptr, (unsigned*)nullptr, 0u, (unsigned long long*)nullptr);
+                          (int32_t*)nullptr, (unsigned*)nullptr, 0u, DevCacheArgs{}, (unsigned long long*)nullptr);
     return launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
                       (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
-                      (int32_t*)nullptr, (unsigned*)nullptr, 0u, (unsigned long long*)nullptr);
+                      (int32_t*)nullptr, (unsigned*)nullptr, 0u, DevCacheArgs{}, (unsigned long long*)nullptr);
 }
 
 cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) {

@@ -421,3 +421,167 @@ def test_set_next_changes_no_result():
             moe.MoELayer(lays[1], cache_slots=16, records=recs[1]) as b:
         streamed = run([a, b], True)
     assert np.array_equal(plain, streamed)
+
+
+# ---- device-managed cache (MOE_OPT_CACHE_DEVICE) ------------------------------------
+
+def pinned_records(recs):
+    """The records copied into page-locked host memory: a device-managed cache
+    reads them through their device mapping."""
+    import torch
+    out = []
+    for r in recs:
+        t = torch.empty(len(r), dtype=torch.uint8).pin_memory()
+        t.numpy()[:] = r
+        out.append(t)
+    return out
+
+
+def _resident(layer, xs):
+    import torch
+    T, spec = xs.shape[0], layer.spec
+    y = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer) as res:
+        for t in range(T):
+            res.decode(xs[t], None, y[t])
+            res.route(xs[t], 1, ids[t], w[t])
+        torch.cuda.synchronize()
+        recs = packed_records(layer, res.desc)
+    return y.cpu().numpy(), ids.cpu().numpy(), recs
+
+
+def _tokens(spec, seed, T):
+    import torch
+    X = si.gen_tokens(seed, 0, T, spec)
+    return torch.from_numpy(np.ascontiguousarray(X).view(np.int16)).cuda()
+
+
+@pytest.mark.gpu
+def test_device_cache_bit_identical_and_lfu():
+    """Each token's LFU step and fills run on the device; the outputs equal the
+    resident layer's bit for bit and the slot map after every token is the
+    oracle's."""
+    import torch
+    spec = si.LayerSpec(hidden=512, inter=256, n_experts=64, zipf_alpha=1.1)
+    layer = si.gen_layer(30, 0, spec)
+    T = 40
+    xs = _tokens(spec, 31, T)
+    y_res, ids, recs = _resident(layer, xs)
+    y = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    residency = []
+    with moe.MoELayer(layer, cache_slots=16, records=pinned_records(recs)) as st:
+        st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        for t in range(T):
+            st.decode(xs[t], None, y[t])
+            residency.append(st.residency())   # synchronises
+        stats = st.cache_stats()
+        assert st.check() == (0, 0)
+    assert np.array_equal(y_res, y.cpu().numpy())
+    o_slot, o_hit = oracle_slots_hits(ids, 16)
+    for t in range(T):
+        for j, e in enumerate(ids[t]):
+            assert residency[t][o_slot[t][j]] == e
+    assert stats["tokens"] == T
+    assert stats["hits"] == int(o_hit.sum())
+    assert stats["misses"] == T * spec.top_k - int(o_hit.sum())
+    assert stats["bytes_h2d"] == stats["misses"] * moe.moe_expert_record_bytes(moe.desc_from_spec(spec))
+
+
+@pytest.mark.gpu
+def test_device_cache_switch_queue_and_graph():
+    """Host staging, then device-managed tokens queued with no host wait, host
+    staging again, then device-managed decodes replayed from a CUDA graph: one
+    LFU run throughout (the oracle's), outputs bit-identical to resident."""
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=32, top_k=4, zipf_alpha=1.1)
+    layer = si.gen_layer(32, 0, spec)
+    T = 40
+    xs = _tokens(spec, 33, T)
+    y_res, ids, recs = _resident(layer, xs)
+    slots = 8
+    y = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, cache_slots=slots, records=pinned_records(recs)) as st:
+        for t in range(0, 10):                      # host staging
+            st.decode(xs[t], None, y[t])
+        st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        for t in range(10, 22):                     # queued, no synchronisation
+            st.decode(xs[t], None, y[t])
+        st.set_option(moe.MOE_OPT_CACHE_DEVICE, 0)
+        mid = st.residency()
+        for t in range(22, 28):                     # host staging again
+            st.decode(xs[t], None, y[t])
+        st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        x_in = torch.empty_like(xs[0])
+        y_out = torch.empty(spec.hidden, dtype=torch.float32, device="cuda")
+        x_in.copy_(xs[28])
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            st.decode(x_in, None, y_out, stream=gs.cuda_stream)   # token 28, outside the graph
+            gs.synchronize()
+            y[28].copy_(y_out)
+            gs.synchronize()
+            with torch.cuda.graph(g, stream=gs):
+                st.decode(x_in, None, y_out, stream=gs.cuda_stream)
+        torch.cuda.current_stream().wait_stream(gs)
+        for t in range(29, T):                      # graph replays
+            x_in.copy_(xs[t])
+            g.replay()
+            y[t].copy_(y_out)
+        torch.cuda.synchronize()
+        final = st.residency()
+        stats = st.cache_stats()
+        assert st.check() == (0, 0)
+        del g
+    assert np.array_equal(y_res, y.cpu().numpy())
+    o_slot, o_hit = oracle_slots_hits(ids, slots)
+    for j, e in enumerate(ids[21]):
+        assert mid[o_slot[21][j]] == e
+    for j, e in enumerate(ids[T - 1]):
+        assert final[o_slot[T - 1][j]] == e
+    assert stats["tokens"] == T
+    assert stats["hits"] == int(o_hit.sum())
+    assert stats["misses"] == T * spec.top_k - int(o_hit.sum())
+
+
+@pytest.mark.gpu
+def test_device_cache_refusals():
+    """A source callback cannot run on the device; while the cache is
+    device-managed, host staging, lookahead and streamed prefill refuse with
+    MOE_E_STATE; a resident layer has no cache to manage."""
+    import torch
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=16, top_k=4)
+    layer = si.gen_layer(34, 0, spec)
+    xs = _tokens(spec, 35, 4)
+    _, _, recs = _resident(layer, xs)
+
+    def src(user, e, dst, nbytes):
+        ctypes.memmove(dst, recs[e].ctypes.data, nbytes)
+        return 0
+    with moe.MoELayer(layer, cache_slots=8, source=moe.SOURCE_FN(src)) as st:
+        with pytest.raises(moe.MoEError) as ei:
+            st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        assert ei.value.status == 2
+    with moe.MoELayer(layer, cache_slots=8, records=pinned_records(recs), max_tokens=4) as st:
+        st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        ids = np.array([0, 1, 2, 3], np.int32)
+        with pytest.raises(moe.MoEError) as ei:
+            st.cache_stage(ids, 4)
+        assert ei.value.status == 6
+        with pytest.raises(moe.MoEError) as ei:
+            st.cache_prefetch(xs[0])
+        assert ei.value.status == 6
+        y = torch.empty(4 * spec.hidden, dtype=torch.float32, device="cuda")
+        with pytest.raises(moe.MoEError) as ei:
+            st.prefill_chunk(xs.reshape(-1), 4, y)
+        assert ei.value.status == 6
+        with pytest.raises(moe.MoEError) as ei:
+            st.set_option(moe.MOE_OPT_CACHE_DEVICE, 2)
+        assert ei.value.status == 1
+    with moe.MoELayer(layer) as res:
+        with pytest.raises(moe.MoEError) as ei:
+            res.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        assert ei.value.status == 6
