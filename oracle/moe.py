@@ -363,6 +363,33 @@ class LFUCache:
         self.last: dict[int, int] = {}
         self.slot_of: dict[int, int] = {}
         self.clock = 0
+        self.pinned: frozenset = frozenset()
+        self.usage: dict[int, int] = {}
+
+    def pin(self, experts) -> None:
+        """Replace the set of pinned experts (the learning cache).
+
+        Colibri README, "Self-learning cache" / "The learning cache": the
+        engine records which experts the usage routes to and pins the hottest
+        ones in spare memory. Readings (the page gives the idea, not the
+        bookkeeping): a pinned expert is always resident outside the LFU
+        slots, so its lookups are hits that leave the LFU state alone; pinning
+        an expert that holds a slot frees that slot (its count and recency are
+        dropped); an expert that stops being pinned is not resident until a
+        token stages it again. Pinning is not a token: the clock stays.
+        """
+        new = frozenset(int(e) for e in experts)
+        for e in new:
+            if e in self.count:
+                del self.slot_of[e]
+                del self.count[e]
+                del self.last[e]
+        self.pinned = new
+
+    def hottest(self, n: int) -> list[int]:
+        """The n experts used most often so far (ties: the lower id first)."""
+        order = sorted(self.usage, key=lambda e: (-self.usage[e], e))
+        return order[:n]
 
     def access(self, ids) -> tuple[list[int], list[tuple[int, int, int]]]:
         """Process one token's expert IDs.
@@ -371,17 +398,21 @@ class LFUCache:
         or -1) in the order the misses are admitted.
         """
         ids = [int(e) for e in ids]
-        assert len(set(ids)) == len(ids) <= self.slots
+        assert len(set(ids)) == len(ids)
+        assert len([e for e in ids if e not in self.pinned]) <= self.slots
         self.clock += 1
         need = set(ids)
         hits, fills = [], []
         for e in ids:
-            if e in self.count:
+            self.usage[e] = self.usage.get(e, 0) + 1
+            if e in self.pinned:
+                hits.append(e)
+            elif e in self.count:
                 hits.append(e)
                 self.count[e] += 1
                 self.last[e] = self.clock
         for e in ids:
-            if e in self.count:
+            if e in self.count or e in self.pinned:
                 continue
             if len(self.count) < self.slots:
                 used = set(self.slot_of.values())
@@ -414,13 +445,14 @@ class LFUCache:
         resident, fills).
         """
         ids = [int(e) for e in ids]
-        assert len(set(ids)) == len(ids) <= self.slots
+        assert len(set(ids)) == len(ids)
+        assert len([e for e in ids if e not in self.pinned]) <= self.slots
         self.clock += 1
         pred = set(ids)
-        resident = [e for e in ids if e in self.count]
+        resident = [e for e in ids if e in self.count or e in self.pinned]
         fills = []
         for e in ids:
-            if e in self.count:
+            if e in self.count or e in self.pinned:
                 continue
             if len(self.count) < self.slots:
                 used = set(self.slot_of.values())

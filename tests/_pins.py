@@ -96,6 +96,31 @@ def read_lfu_prefetch():
     return slots, rows
 
 
+def read_lfu_pinned():
+    """(slots, [(op, args...)]) from lfu_pinned.txt: ("token", ids, hits,
+    fills), ("pin", ids) or ("hottest", n, ids)."""
+    slots, rows = None, []
+    for raw in open(os.path.join(GOLDEN, "lfu_pinned.txt")):
+        line = raw.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("slots"):
+            slots = int(line.split()[1])
+            continue
+        parts = [p.strip() for p in line.split("|")]
+        op, arg = parts[0].split()
+        ints = lambda v: [] if v == "-" else [int(u) for u in v.split(",")]
+        if op == "pin":
+            rows.append(("pin", ints(arg)))
+        elif op == "hottest":
+            rows.append(("hottest", int(arg), ints(parts[1])))
+        else:
+            h = ints(parts[1].split()[1])
+            f = [tuple(int(u) for u in t.split(":")) for t in parts[2].split()[1:]]
+            rows.append(("token", ints(arg), h, f))
+    return slots, rows
+
+
 # ---------------------------------------------------------------------------
 # small layers built by hand
 # ---------------------------------------------------------------------------
@@ -421,6 +446,20 @@ def pin_lfu_prefetch_trace():
         assert [tuple(v) for v in f] == fills, (op, ids, f, fills)
 
 
+def pin_lfu_pinned_trace():
+    slots, rows = read_lfu_pinned()
+    c = oracle.LFUCache(slots)
+    for row in rows:
+        if row[0] == "pin":
+            c.pin(row[1])
+        elif row[0] == "hottest":
+            assert c.hottest(row[1]) == row[2], (row, c.hottest(row[1]))
+        else:
+            h, f = c.access(row[1])
+            assert h == row[2], (row, h)
+            assert [tuple(v) for v in f] == row[3], (row, f)
+
+
 def pin_lfu_trace():
     slots, rows = read_lfu()
     c = oracle.LFUCache(slots)
@@ -515,5 +554,6 @@ ALL_PINS = [pin_dequant_q4_table, pin_dequant_q2_table, pin_q2_layer, pin_dequan
             pin_zero_input_routing, pin_topk_is_full_sort, pin_routing_weights,
             pin_silu, pin_ffn_closed_form, pin_dense_brute_force, pin_pure_python,
             pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace, pin_lfu_prefetch_trace,
+            pin_lfu_pinned_trace,
             pin_sigmoid_router_golden,
             pin_sigmoid_layer_pure_python]

@@ -145,6 +145,33 @@ class _LfuPrefetchRefreshes(om.LFUCache):
         return r, f
 
 
+class _LfuPinnedCountsUse(om.LFUCache):
+    """a pinned expert also enters an LFU slot when used"""
+    def access(self, ids):
+        pinned, self.pinned = self.pinned, frozenset()
+        try:
+            return super().access(ids)
+        finally:
+            self.pinned = pinned
+
+
+class _LfuPinKeepsSlot(om.LFUCache):
+    """pinning leaves the expert's slot taken"""
+    def pin(self, experts):
+        self.pinned = frozenset(int(e) for e in experts)
+
+
+class _LfuUnpinKeepsResident(om.LFUCache):
+    """an unpinned expert stays resident (a new pin only adds experts)"""
+    def pin(self, experts):
+        super().pin(set(int(e) for e in experts) | set(self.pinned))
+
+
+class _LfuHottestTiesHigh(om.LFUCache):
+    def hottest(self, n):
+        return sorted(self.usage, key=lambda e: (-self.usage[e], -e))[:n]
+
+
 def _sig_is_tanh(l):
     return np.tanh(np.asarray(l, np.float64))
 
@@ -170,6 +197,10 @@ MISTAKES = {
     "sigmoid replaced by tanh": ("sigmoid_scores", _sig_is_tanh),
     "prediction admitted as a use": ("LFUCache", _LfuPrefetchCountsUse),
     "prediction refreshes residents": ("LFUCache", _LfuPrefetchRefreshes),
+    "pinned expert enters the LFU": ("LFUCache", _LfuPinnedCountsUse),
+    "pinning keeps the slot": ("LFUCache", _LfuPinKeepsSlot),
+    "unpinned expert stays resident": ("LFUCache", _LfuUnpinKeepsResident),
+    "hottest ties to the higher id": ("LFUCache", _LfuHottestTiesHigh),
 }
 
 
