@@ -390,7 +390,8 @@ def run_streamed(args):
     workload = (f"streamed GLM-scale decode: {Lc} layers of H6144 I2048 E256 top-8 + 1 shared, 16-slot LFU cache "
                 f"per layer, Zipf(1.1) routing bias per layer, {P}-record alias pool in pinned host memory; "
                 f"chain: {args.chain}; router lookahead: {'on' if args.lookahead else 'off'}; "
-                f"cache managed on the {'device' if args.device_cache else 'host'}")
+                f"cache managed on the {'device' if args.device_cache else 'host'}; "
+                f"pinned hottest per layer: {args.pin}" + (f" (usage learned over {args.learn} tokens)" if args.pin else ""))
     if args.impl == "reference":
         if rank != 0:
             return
@@ -458,8 +459,8 @@ def run_streamed(args):
         # the stream's RMS, and the sum is renormalised
         return rms_norm(torch.add(x.float(), rms_norm(y, (H,), eps=1e-12), alpha=0.25), (H,), eps=1e-12)
 
-    def token(i):
-        x.copy_(x_host[i], non_blocking=True)
+    def token(i, src=None):
+        x.copy_((x_host if src is None else src)[i], non_blocking=True)
         for li, ml in enumerate(stack):
             if args.lookahead and li + 1 < Lc:
                 # the next layer's router on this layer's input: stage its predicted experts now
@@ -467,6 +468,16 @@ def run_streamed(args):
             ml.decode(x, None, y, stream=stream)
             x.copy_(chain(y))   # bf16 rounding in the copy
 
+    if args.pin:
+        # the learning cache: record which experts a run of tokens (a seeded
+        # stream of their own) routes to, then pin each layer's hottest
+        XL = si.gen_tokens(1000 * rank + 500, 0, args.learn, spec)
+        xl_host = torch.from_numpy(np.ascontiguousarray(XL.view(np.int16))).view(torch.bfloat16).pin_memory()
+        for i in range(args.learn):
+            token(i, xl_host)
+        torch.cuda.synchronize()
+        for ml in stack:
+            ml.pin_hottest(args.pin)
     for i in range(args.warmup):
         token(i)
     torch.cuda.synchronize()
@@ -713,6 +724,9 @@ def main():
                     help="glm_streamed: how one layer's output becomes the next layer's input")
     ap.add_argument("--lookahead", action="store_true",
                     help="glm_streamed: stage each next layer's predicted experts (moe_cache_prefetch)")
+    ap.add_argument("--pin", type=int, default=0,
+                    help="glm_streamed: pin each layer's N most used experts after --learn tokens (learning cache)")
+    ap.add_argument("--learn", type=int, default=32, help="glm_streamed: tokens whose routing --pin learns from")
     ap.add_argument("--device-cache", action="store_true",
                     help="glm_streamed: device-managed caches (MOE_OPT_CACHE_DEVICE); also times the token as a CUDA graph")
     ap.add_argument("--chunk", type=int, default=None,

@@ -327,6 +327,28 @@ moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out);
  * -1 for an empty slot. */
 moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert);
 
+/* The learning cache (Colibri README, "Self-learning cache": the engine records
+ * which experts the usage routes to and pins the hottest in spare memory).
+ *
+ * moe_cache_usage: counts (host uint64 [n_experts]) of how often each expert was
+ * selected on this streamed layer since creation: every decode token's ids and
+ * every expert of every streamed-prefill wave; lookahead predictions do not
+ * count. In device-managed mode it synchronises the device first.
+ *
+ * moe_cache_pin: replaces the set of pinned experts by experts[0..n) (host
+ * int32, distinct, 0 <= id < n_experts; n = 0 unpins all). Pinned experts are
+ * copied once into device memory beside the cache slots (n records more) and
+ * stay resident: their lookups are hits that leave the LFU state alone. An
+ * expert pinned while it held a slot frees the slot; an unpinned expert is not
+ * resident until a token stages it. Not a token (the LFU clock stays). Copies
+ * come from the borrowed records or the source callback. Synchronises the
+ * device (slots move); MOE_E_INVALID for bad ids, MOE_E_STATE on a resident
+ * layer, MOE_E_SOURCE / MOE_E_CUDA if a copy fails (the previous state is
+ * kept). Choosing the set (e.g. the hottest by moe_cache_usage, ties to the
+ * lower id) is the caller's. */
+moe_status moe_cache_usage(const moe_layer* layer, uint64_t* counts);
+moe_status moe_cache_pin(moe_layer* layer, const int32_t* experts, int32_t n);
+
 /* The cache policy alone, on the host (no device, no layer): runs n_tokens
  * tokens of k distinct expert ids each (ids: host int32 [n_tokens][k], values
  * in 0..n_experts-1) through an empty `slots`-slot cache exactly as a streamed

@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_layer_set_next", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
-           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_lfu_trace",
+           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_cache_usage", "moe_cache_pin", "moe_lfu_trace",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
@@ -125,6 +125,10 @@ def lib() -> ctypes.CDLL:
             L.moe_cache_stats.argtypes = [vp, ctypes.POINTER(moe_cache_stats_t)]
             L.moe_cache_residency.restype = st
             L.moe_cache_residency.argtypes = [vp, vp]
+            L.moe_cache_usage.restype = st
+            L.moe_cache_usage.argtypes = [vp, vp]
+            L.moe_cache_pin.restype = st
+            L.moe_cache_pin.argtypes = [vp, vp, ctypes.c_int32]
             L.moe_lfu_trace.restype = st
             L.moe_lfu_trace.argtypes = [i32, i32, i32, i32, vp, vp, vp]
             L.moe_profile_start.restype = st
@@ -325,6 +329,22 @@ def moe_cache_residency(handle, slots: int) -> list[int]:
     return list(arr)
 
 
+def moe_cache_usage(handle, n_experts: int):
+    """Per-expert selection counts of a streamed layer (numpy uint64 [n_experts])."""
+    import numpy as np
+    out = np.zeros(n_experts, np.uint64)
+    _check(lib().moe_cache_usage(handle, ctypes.c_void_p(out.ctypes.data)), "moe_cache_usage")
+    return out
+
+
+def moe_cache_pin(handle, experts) -> None:
+    """Pin these experts (the learning cache); an empty list unpins all."""
+    import numpy as np
+    ids = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
+    _check(lib().moe_cache_pin(handle, ctypes.c_void_p(ids.ctypes.data) if len(ids) else None, len(ids)),
+           "moe_cache_pin")
+
+
 def moe_profile_start(handle, max_launches: int) -> None:
     _check(lib().moe_profile_start(handle, max_launches), "moe_profile_start")
 
@@ -448,6 +468,19 @@ class MoELayer:
 
     def residency(self):
         return moe_cache_residency(self.handle, self.desc.cache_slots)
+
+    def cache_usage(self):
+        return moe_cache_usage(self.handle, self.desc.n_experts)
+
+    def cache_pin(self, experts):
+        moe_cache_pin(self.handle, experts)
+
+    def pin_hottest(self, n):
+        """Pin the n most used experts so far (ties: the lower id first)."""
+        import numpy as np
+        use = self.cache_usage()
+        order = sorted(range(len(use)), key=lambda e: (-int(use[e]), e))
+        self.cache_pin(np.array(order[:n], np.int32))
 
     def set_option(self, option, value):
         moe_layer_set_option(self.handle, option, value)

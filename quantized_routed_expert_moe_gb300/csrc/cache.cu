@@ -38,7 +38,8 @@ struct Fill {
 
 class Lfu {
 public:
-    Lfu(int slots, int E) : slots_(slots), slot_of_(E, -1), expert_in_(slots, -1), count_(E, 0), last_(E, 0) {}
+    Lfu(int slots, int E)
+        : slots_(slots), slot_of_(E, -1), expert_in_(slots, -1), count_(E, 0), last_(E, 0), pinned_(E, 0), usage_(E, 0) {}
 
     // One token's IDs (distinct, at most `slots`): updates the counts and
     // returns the fills (expert, slot, evicted expert or -1) in admission order.
@@ -48,7 +49,10 @@ public:
         int h = 0;
         for (int i = 0; i < n; ++i) {
             const int e = ids[i];
-            if (slot_of_[e] >= 0) {
+            ++usage_[e];
+            if (pinned_[e]) {   // served outside the slots; the LFU state stays
+                ++h;
+            } else if (slot_of_[e] >= 0) {
                 ++h;
                 ++count_[e];
                 last_[e] = clock_;
@@ -56,7 +60,7 @@ public:
         }
         for (int i = 0; i < n; ++i) {
             const int e = ids[i];
-            if (slot_of_[e] >= 0) continue;
+            if (slot_of_[e] >= 0 || pinned_[e]) continue;
             int slot = -1, victim = -1;
             for (int s = 0; s < slots_; ++s)
                 if (expert_in_[s] < 0) { slot = s; break; }
@@ -92,10 +96,10 @@ public:
         ++clock_;
         fills.clear();
         int r0 = 0;
-        for (int i = 0; i < n; ++i) r0 += slot_of_[ids[i]] >= 0;
+        for (int i = 0; i < n; ++i) r0 += slot_of_[ids[i]] >= 0 || pinned_[ids[i]];
         for (int i = 0; i < n; ++i) {
             const int e = ids[i];
-            if (slot_of_[e] >= 0) continue;
+            if (slot_of_[e] >= 0 || pinned_[e]) continue;
             int slot = -1, victim = -1;
             for (int s = 0; s < slots_; ++s)
                 if (expert_in_[s] < 0) { slot = s; break; }
@@ -132,6 +136,22 @@ public:
         last_[e] = 0;
     }
 
+    // The learning cache (Colibri README, "Self-learning cache"): a new set
+    // of pinned experts, resident outside the slots. An expert pinned while it
+    // holds a slot leaves the slot; an unpinned one is not resident until a
+    // token stages it. Not a token: the clock stays.
+    void pin(const int32_t* ids, int n) {
+        std::fill(pinned_.begin(), pinned_.end(), 0);
+        for (int i = 0; i < n; ++i) {
+            drop(ids[i]);
+            pinned_[ids[i]] = 1;
+        }
+    }
+    bool pinned(int e) const { return pinned_[e] != 0; }
+    // selections of each expert so far (tokens and prefill waves; not predictions)
+    uint64_t usage(int e) const { return usage_[e]; }
+    void add_usage(int e, uint64_t v) { usage_[e] += v; }
+
     int slot_of(int e) const { return slot_of_[e]; }
     int expert_in(int s) const { return expert_in_[s]; }
     uint64_t count(int e) const { return count_[e]; }
@@ -158,6 +178,8 @@ private:
     uint64_t clock_ = 0;
     std::vector<int> slot_of_, expert_in_;
     std::vector<uint64_t> count_, last_;
+    std::vector<char> pinned_;
+    std::vector<uint64_t> usage_;
 };
 
 // ---------------------------------------------------------------------------
@@ -198,6 +220,9 @@ struct CacheState {
     bool device = false;
     void* dev_state = nullptr;
     DevCacheArgs dca;
+    // pinned experts: pinned[i] lives at dev_slots + (slots + i) * rec_bytes
+    std::vector<int32_t> pinned;
+    std::vector<int32_t> pin_index;   // [E] index into pinned, or -1
 };
 
 namespace {
@@ -254,6 +279,7 @@ moe_status cache_create(Layer& L, const void* const* records, moe_expert_source 
     L.cache = C;
     C->slots = d.cache_slots;
     C->lfu = Lfu(d.cache_slots, d.n_experts);
+    C->pin_index.assign(d.n_experts, -1);
     if (records) {
         C->records_copy.assign(records, records + d.n_experts);
         for (int e = 0; e < d.n_experts; ++e)
@@ -460,9 +486,15 @@ moe_status cache_prefetch(Layer& L, const void* x, cudaStream_t s, int* resident
     return st;
 }
 
-int cache_slot_of(const Layer& L, int expert) { return L.cache->lfu.slot_of(expert); }
+int cache_slot_of(const Layer& L, int expert) {
+    const CacheState& C = *L.cache;
+    const int p = C.pin_index[expert];
+    return p >= 0 ? C.slots + p : C.lfu.slot_of(expert);
+}
 
 const uint8_t* cache_slots_base(const Layer& L) { return L.cache->dev_slots; }
+
+int cache_slot_count(const Layer& L) { return L.cache->slots + (int)L.cache->pinned.size(); }
 
 moe_status host_wait_event(const Layer& L, cudaEvent_t ev, const char* what) { return wait_event(L, ev, what); }
 
@@ -529,10 +561,12 @@ moe_status cache_set_device(Layer& L, bool on) {
             src[e] = static_cast<const uint8_t*>(p);
         }
         if (!C.dev_state) {
-            // slot_expert, slot_count, slot_last [S] | clock | fills [1 + 2 MOE_MAX_TOP_K] | stats [4] (8-aligned) | src [E]
+            // slot_expert, slot_count, slot_last [S] | clock | fills [1 + 2 MOE_MAX_TOP_K] | stats [4] (8-aligned)
+            // | src [E] | usage [E] | pinned flags [E]
             const size_t words = 3 * (size_t)S + 1 + 1 + 2 * MOE_MAX_TOP_K;
             const size_t stats_off = (words * 4 + 7) / 8 * 8, src_off = stats_off + 4 * 8;
-            MOE_CUDA_TRY(cudaMalloc(&C.dev_state, src_off + (size_t)E * sizeof(void*)));
+            const size_t usage_off = src_off + (size_t)E * sizeof(void*), pin_off = usage_off + (size_t)E * 8;
+            MOE_CUDA_TRY(cudaMalloc(&C.dev_state, pin_off + (size_t)E));
             uint8_t* b = static_cast<uint8_t*>(C.dev_state);
             C.dca.slot_expert = reinterpret_cast<int32_t*>(b);
             C.dca.slot_count = reinterpret_cast<uint32_t*>(b) + S;
@@ -541,8 +575,9 @@ moe_status cache_set_device(Layer& L, bool on) {
             C.dca.fills = reinterpret_cast<int32_t*>(b) + 3 * S + 1;
             C.dca.stats = reinterpret_cast<unsigned long long*>(b + stats_off);
             C.dca.src = reinterpret_cast<const uint8_t* const*>(b + src_off);
+            C.dca.usage = reinterpret_cast<unsigned long long*>(b + usage_off);
+            C.dca.pinned = b + pin_off;
             C.dca.rec_table = (const uint8_t**)L.rec_table;
-            C.dca.slots_base = C.dev_slots;
             C.dca.rb = L.rec_bytes;
             C.dca.slots = S;
             C.dca.err = fused_error_word(L);
@@ -567,6 +602,11 @@ moe_status cache_set_device(Layer& L, bool on) {
         MOE_CUDA_TRY(cudaMemcpy(C.dca.fills, &zero_fills, 4, cudaMemcpyHostToDevice));
         MOE_CUDA_TRY(cudaMemcpy(C.dca.stats, zero_stats, sizeof zero_stats, cudaMemcpyHostToDevice));
         MOE_CUDA_TRY(cudaMemcpy((void*)C.dca.src, src.data(), (size_t)E * sizeof(void*), cudaMemcpyHostToDevice));
+        std::vector<uint8_t> pin(E);
+        for (int e = 0; e < E; ++e) pin[e] = C.lfu.pinned(e) ? 1 : 0;
+        MOE_CUDA_TRY(cudaMemcpy((void*)C.dca.pinned, pin.data(), (size_t)E, cudaMemcpyHostToDevice));
+        MOE_CUDA_TRY(cudaMemset(C.dca.usage, 0, (size_t)E * 8));
+        C.dca.slots_base = C.dev_slots;   // the slots may have moved (pinning)
         C.device = true;
         return MOE_OK;
     }
@@ -581,16 +621,88 @@ moe_status cache_set_device(Layer& L, bool on) {
     MOE_CUDA_TRY(cudaMemcpy(last.data(), C.dca.slot_last, S * 4, cudaMemcpyDeviceToHost));
     MOE_CUDA_TRY(cudaMemcpy(&clk, C.dca.clock, 4, cudaMemcpyDeviceToHost));
     MOE_CUDA_TRY(cudaMemcpy(st, C.dca.stats, sizeof st, cudaMemcpyDeviceToHost));
+    std::vector<unsigned long long> use(E);
+    MOE_CUDA_TRY(cudaMemcpy(use.data(), C.dca.usage, (size_t)E * 8, cudaMemcpyDeviceToHost));
     C.lfu.load(se.data(), cnt.data(), last.data(), clk);
+    for (int e = 0; e < E; ++e) C.lfu.add_usage(e, use[e]);
     C.stats.tokens += st[0];
     C.stats.hits += st[1];
     C.stats.misses += st[2];
     C.stats.bytes_h2d += st[3];
-    // the host mirror of the record table (the device's already matches)
-    for (int e = 0; e < E; ++e) C.table[e] = nullptr;
-    for (int s = 0; s < S; ++s)
-        if (se[s] >= 0) C.table[se[s]] = C.dev_slots + (size_t)s * L.rec_bytes;
+    // the host mirror of the record table (the device's already matches):
+    // LFU residents and pinned experts
+    for (int e = 0; e < E; ++e) {
+        const int sl = cache_slot_of(L, e);
+        C.table[e] = sl < 0 ? nullptr : C.dev_slots + (size_t)sl * L.rec_bytes;
+    }
     C.device = false;
+    return MOE_OK;
+}
+
+// The learning cache (Colibri README, "Self-learning cache": the engine records
+// which experts the usage routes to and pins the hottest in spare memory).
+// A new pinned set: the records are copied into a slot array that now holds
+// the LFU slots followed by the pinned experts, the record table points at
+// them, and the LFU forgets them (an expert pinned while it held a slot frees
+// the slot). Synchronises the device; a failed copy leaves everything as it was.
+moe_status cache_pin(Layer& L, const int32_t* ids, int n) {
+    CacheState& C = *L.cache;
+    const int E = L.d.n_experts, S = C.slots;
+    const size_t rb = L.rec_bytes;
+    if (n < 0 || n > E) return fail(MOE_E_INVALID, "n out of range 0..n_experts");
+    if (n > 0 && !ids) return fail(MOE_E_INVALID, "NULL ids");
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= E) return fail(MOE_E_INVALID, "expert id out of range");
+        for (int j = 0; j < i; ++j)
+            if (ids[j] == ids[i]) return fail(MOE_E_INVALID, "repeated expert id");
+    }
+    const bool was_device = C.device;
+    if (was_device) {
+        const moe_status st = cache_set_device(L, false);
+        if (st != MOE_OK) return st;
+    }
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    MOE_CUDA_TRY(cudaStreamSynchronize(C.copy));
+    C.copies_pending = false;
+    uint8_t* nb = nullptr;
+    MOE_CUDA_TRY(cudaMalloc(&nb, (size_t)(S + n) * rb));
+    moe_status st = MOE_OK;
+    cudaError_t ce = cudaMemcpy(nb, C.dev_slots, (size_t)S * rb, cudaMemcpyDeviceToDevice);
+    if (ce != cudaSuccess) st = cuda_fail(ce, "slot move");
+    for (int i = 0; i < n && st == MOE_OK; ++i) {
+        const void* src = nullptr;
+        if (C.records) {
+            src = C.records[ids[i]];
+        } else if (C.src(C.user, ids[i], C.staging[0], rb) != 0) {
+            st = fail(MOE_E_SOURCE, "expert source failed for expert " + std::to_string(ids[i]));
+            break;
+        } else {
+            src = C.staging[0];
+        }
+        ce = cudaMemcpy(nb + (size_t)(S + i) * rb, src, rb, cudaMemcpyHostToDevice);
+        if (ce != cudaSuccess) st = cuda_fail(ce, "pinned expert copy");
+    }
+    if (st != MOE_OK) {
+        cudaFree(nb);
+        if (was_device) cache_set_device(L, true);
+        return st;
+    }
+    C.lfu.pin(ids, n);
+    cudaFree(C.dev_slots);
+    L.device_bytes = L.device_bytes - (size_t)(S + C.pinned.size()) * rb + (size_t)(S + n) * rb;
+    C.dev_slots = nb;
+    C.pinned.assign(ids, ids + n);
+    std::fill(C.pin_index.begin(), C.pin_index.end(), -1);
+    for (int i = 0; i < n; ++i) C.pin_index[ids[i]] = i;
+    // the record table: LFU residents, then pinned experts (the shared expert's entry stays)
+    for (int e = 0; e < E; ++e) {
+        const int sl = cache_slot_of(L, e);
+        C.table[e] = sl < 0 ? nullptr : nb + (size_t)sl * rb;
+    }
+    MOE_CUDA_TRY(cudaMemcpy(L.rec_table, C.table.data(), C.table.size() * sizeof(void*), cudaMemcpyHostToDevice));
+    st = prefill_cache_maps(L);
+    if (st != MOE_OK) return st;
+    if (was_device) return cache_set_device(L, true);
     return MOE_OK;
 }
 
@@ -648,7 +760,7 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
     st = cache_stage(L, C.ids_host, k, s, &h, &m);
     if (st != MOE_OK) return st;
     for (int j = 0; j < k; ++j)
-        if (C.lfu.slot_of(C.ids_host[j]) < 0)
+        if (cache_slot_of(L, C.ids_host[j]) < 0)
             return fail(MOE_E_STATE, "expert " + std::to_string(C.ids_host[j]) + " is not resident");
     if (spec && m == 0) return MOE_OK;   // the speculative launch had every expert
     // after a speculative launch that met a miss every slot runs again;
@@ -703,6 +815,33 @@ moe_status moe_cache_stats(const moe_layer* layer, moe_cache_stats_t* out) {
         out->hits += st[1];
         out->misses += st[2];
         out->bytes_h2d += st[3];
+    }
+    return MOE_OK;
+}
+
+moe_status moe_cache_pin(moe_layer* layer, const int32_t* experts, int32_t n) {
+    if (!layer) return moe::fail(MOE_E_INVALID, "NULL layer");
+    moe::Layer& L = layer->L;
+    if (!L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed (cache_slots == 0)");
+    moe::DeviceGuard g(L.device);
+    if (!g.ok) return moe::cuda_fail(g.err, "cudaSetDevice");
+    return moe::cache_pin(L, experts, n);
+}
+
+moe_status moe_cache_usage(const moe_layer* layer, uint64_t* counts) {
+    if (!layer || !counts) return moe::fail(MOE_E_INVALID, "NULL argument");
+    const moe::Layer& L = layer->L;
+    if (!L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed (cache_slots == 0)");
+    const moe::CacheState& C = *L.cache;
+    const int E = L.d.n_experts;
+    for (int e = 0; e < E; ++e) counts[e] = C.lfu.usage(e);
+    if (C.device) {   // plus the device's counts so far (every decode queued included)
+        moe::DeviceGuard g(L.device);
+        if (!g.ok) return moe::cuda_fail(g.err, "cudaSetDevice");
+        MOE_CUDA_TRY(cudaDeviceSynchronize());
+        std::vector<unsigned long long> use(E);
+        MOE_CUDA_TRY(cudaMemcpy(use.data(), C.dca.usage, (size_t)E * 8, cudaMemcpyDeviceToHost));
+        for (int e = 0; e < E; ++e) counts[e] += use[e];
     }
     return MOE_OK;
 }

@@ -121,6 +121,8 @@ struct DevCacheArgs {
     unsigned long long* stats = nullptr;   // [4] tokens, hits, misses, bytes
     const uint8_t** rec_table = nullptr;   // the layer's record table [E + 1]
     const uint8_t* const* src = nullptr;   // [E] device views of the host records
+    const uint8_t* pinned = nullptr;    // [E] 1: pinned (resident outside the slots, never in the LFU)
+    unsigned long long* usage = nullptr;   // [E] selections since the state came to the device
     uint8_t* slots_base = nullptr;      // [slots][rb]
     unsigned long long rb = 0;          // record bytes
     int slots = 0;
@@ -280,8 +282,11 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
 // MOE_OPT_CACHE_DEVICE: hand the LFU state to the device (on) or back to the host (off)
 moe_status cache_set_device(Layer& L, bool on);
 bool cache_is_device(const Layer& L);
+// tensor maps of the streamed prefill over the slots (LFU slots, then pinned experts)
+moe_status prefill_cache_maps(Layer& L);
 int cache_slot_of(const Layer& L, int expert);   // slot holding `expert`, -1 when not resident
-const uint8_t* cache_slots_base(const Layer& L); // device [cache_slots][rec_bytes]
+const uint8_t* cache_slots_base(const Layer& L); // device [cache_slot_count][rec_bytes]
+int cache_slot_count(const Layer& L);            // LFU slots + pinned experts
 // host wait for `ev` with the layer's deadline (MOE_OPT_HOST_TIMEOUT_MS)
 moe_status host_wait_event(const Layer& L, cudaEvent_t ev, const char* what);
 // prefill chunk on a streamed layer (router already launched): waves through the cache

@@ -640,19 +640,30 @@ cudaError_t prefill_kernel_setup(Layer& L) {
     return cudaSuccess;
 }
 
+moe_status prefill_cache_maps(Layer& L) {
+    const auto& d = L.d;
+    auto& pf = L.pf;
+    if (!pf.xp) return MOE_OK;
+    const int H = d.hidden, I = d.inter;
+    const uint8_t* slots = cache_slots_base(L);
+    const int n = cache_slot_count(L);   // LFU slots, then pinned experts
+    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint8_t* dn = slots + gu_block_bytes(H, I);
+    const bool ok = map_weight_rows(&pf.tm[12], slots, row_bytes(H), 2 * I, n, L.rec_bytes, 128, SW) &&
+                    map_weight_rows(&pf.tm[13], slots, row_bytes(H), 2 * I, n, L.rec_bytes, 16, NS) &&
+                    map_weight_rows(&pf.tm[14], dn, row_bytes(I), H, n, L.rec_bytes, 128, SW) &&
+                    map_weight_rows(&pf.tm[15], dn, row_bytes(I), H, n, L.rec_bytes, 16, NS);
+    if (!ok) return fail(MOE_E_CUDA, "tensor maps over the cache slots");
+    return MOE_OK;
+}
+
 moe_status prefill_cache_setup(Layer& L) {
     const auto& d = L.d;
     auto& pf = L.pf;
     if (!pf.xp) return MOE_OK;
-    const int H = d.hidden, I = d.inter, E = d.n_experts;
-    const uint8_t* slots = cache_slots_base(L);
-    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
-    const uint8_t* dn = slots + gu_block_bytes(H, I);
-    const bool ok = map_weight_rows(&pf.tm[12], slots, row_bytes(H), 2 * I, d.cache_slots, L.rec_bytes, 128, SW) &&
-                    map_weight_rows(&pf.tm[13], slots, row_bytes(H), 2 * I, d.cache_slots, L.rec_bytes, 16, NS) &&
-                    map_weight_rows(&pf.tm[14], dn, row_bytes(I), H, d.cache_slots, L.rec_bytes, 128, SW) &&
-                    map_weight_rows(&pf.tm[15], dn, row_bytes(I), H, d.cache_slots, L.rec_bytes, 16, NS);
-    if (!ok) return fail(MOE_E_CUDA, "tensor maps over the cache slots");
+    const int E = d.n_experts;
+    const moe_status sm = prefill_cache_maps(L);
+    if (sm != MOE_OK) return sm;
     MOE_CUDA_TRY(cudaHostAlloc(&pf.groups_host, (size_t)(1 + 3 * (E + 1)) * 4, cudaHostAllocDefault));
     MOE_CUDA_TRY(cudaHostAlloc(&pf.waves_host, (size_t)4 * (E + 2) * 4, cudaHostAllocDefault));
     MOE_CUDA_TRY(cudaMalloc(&pf.waves_dev, (size_t)4 * (E + 2) * 4));
@@ -801,7 +812,8 @@ moe_status launch_prefill_streamed(Layer& L, const void* x, int T, void* y, floa
         if (cache_slot_of(L, gexp[g]) < 0) order.push_back(g);
     std::vector<int32_t> ids, slot;
     for (int w0 = 0; w0 < nr;) {
-        // the resident experts form the first wave (at most S of them by construction)
+        // the resident experts form the first wave (at most S in the LFU slots, plus
+        // the pinned ones)
         const int w1 = (w0 == 0 && n_res > 0) ? n_res : std::min(nr, w0 + S);
         const int n = w1 - w0;
         ids.resize(n);

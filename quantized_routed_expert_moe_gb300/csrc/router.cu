@@ -39,6 +39,7 @@ constexpr int kWarps = kThreads / 32;
 // the block staged in shared memory: se expert, sc count, sl last use). The
 // policy is the host's (cache.cu) step for step, with the counts and last uses
 // kept per slot:
+//   * a pinned expert (the learning cache) is a hit that leaves the state alone;
 //   * hits first, in selection order: count + 1, last use = this token;
 //   * then each miss in selection order takes the lowest free slot, else the
 //     slot of the resident with the smallest count that this token does not
@@ -55,6 +56,12 @@ __device__ void dev_lfu_access(const DevCacheArgs& dc, const int32_t* ids_g, int
     const uint32_t clk = *dc.clock + 1u;
     *dc.clock = clk;
     int hits = 0, nf = 0;
+    bool pin[MOE_MAX_TOP_K];
+    for (int i = 0; i < n; ++i) {
+        dc.usage[ids[i]] += 1ull;
+        pin[i] = dc.pinned[ids[i]] != 0;
+        hits += pin[i];   // pinned (learning cache): served outside the slots
+    }
     for (int i = 0; i < n; ++i)
         for (int s = 0; s < S; ++s)
             if (se[s] == ids[i]) {
@@ -64,6 +71,7 @@ __device__ void dev_lfu_access(const DevCacheArgs& dc, const int32_t* ids_g, int
             }
     for (int i = 0; i < n; ++i) {
         const int e = ids[i];
+        if (pin[i]) continue;
         bool resident = false;
         for (int s = 0; s < S; ++s) resident |= se[s] == e;
         if (resident) continue;

@@ -585,3 +585,120 @@ def test_device_cache_refusals():
         with pytest.raises(moe.MoEError) as ei:
             res.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
         assert ei.value.status == 6
+
+
+# ---- the learning cache (usage counts, pinned experts) -------------------------------
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("device", [False, True])
+def test_learning_cache_pin_hottest(device):
+    """Usage counts equal the oracle's; pinning the hottest experts (the
+    oracle's choice, ties to the lower id) keeps the outputs bit-identical to
+    the resident layer's; pinned lookups hit and leave the LFU alone, so the
+    slot map follows the oracle's run with the same pins, through a re-pin and
+    an unpin; host-managed and device-managed alike."""
+    import torch
+    spec = si.LayerSpec(hidden=512, inter=256, n_experts=64, zipf_alpha=1.1)
+    layer = si.gen_layer(36, 0, spec)
+    T = 48
+    xs = _tokens(spec, 37, T)
+    y_res, ids, recs = _resident(layer, xs)
+    slots = 8
+    sim = oracle.moe.LFUCache(slots)
+    hits = misses = 0
+    y = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, cache_slots=slots, records=pinned_records(recs)) as st:
+        if device:
+            st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        for t in range(T):
+            if t == 16:
+                use = st.cache_usage()
+                want = np.zeros(spec.n_experts, np.uint64)
+                for e, n in sim.usage.items():
+                    want[e] = n
+                assert np.array_equal(use, want)
+                hot = sim.hottest(6)
+                st.pin_hottest(6)
+                sim.pin(hot)
+            if t == 30:   # a new set: some stay, some leave, some come
+                new = sim.hottest(10)[4:]
+                st.cache_pin(np.array(new, np.int32))
+                sim.pin(new)
+            if t == 40:
+                st.cache_pin([])
+                sim.pin([])
+            st.decode(xs[t], None, y[t])
+            h, f = sim.access(ids[t])
+            hits += len(h)
+            misses += len(f)
+            res = st.residency()
+            for e, s in sim.slot_of.items():
+                assert res[s] == e, (t, e, s, res)
+            assert sum(1 for e in res if e >= 0) == len(sim.slot_of)
+        stats = st.cache_stats()
+        assert st.check() == (0, 0)
+    assert np.array_equal(y_res, y.cpu().numpy())
+    assert stats["tokens"] == T
+    assert stats["hits"] == hits
+    assert stats["misses"] == misses
+
+
+@pytest.mark.gpu
+def test_learning_cache_streamed_prefill():
+    """A prefill chunk on a streamed layer with pinned experts: the pinned ones
+    join the first (resident) wave, the output equals the resident layer's bit
+    for bit, and the LFU follows the oracle's run over the same waves."""
+    import torch
+    T, E, slots = 24, 32, 8
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=E, zipf_alpha=1.1, act="f32")
+    layer = si.gen_layer(38, 0, spec)
+    chunks = [si.gen_tokens(38 + c, 0, T, spec) for c in range(2)]
+    xs = [torch.from_numpy(np.ascontiguousarray(X, np.float32)).cuda() for X in chunks]
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, max_tokens=T) as res:
+        want = [_prefill(res, spec, xd, T) for xd in xs]
+        sel = []
+        for xd in xs:
+            res.route(xd, T, ids, w)
+            torch.cuda.synchronize()
+            sel.append(ids.cpu().numpy().copy())
+        recs = packed_records(layer, res.desc)
+    sim = oracle.moe.LFUCache(slots)
+    with moe.MoELayer(layer, max_tokens=T, cache_slots=slots, records=recs) as st:
+        for c, xd in enumerate(xs):
+            if c == 1:   # pin the hottest after the first chunk
+                hot = sim.hottest(5)
+                st.pin_hottest(5)
+                sim.pin(hot)
+            got = _prefill(st, spec, xd, T)
+            assert np.array_equal(got, want[c])
+            distinct = sorted(set(int(e) for e in sel[c].reshape(-1)))
+            for wv in _waves(set(sim.count) | set(sim.pinned), distinct, slots):
+                sim.access(np.array(wv, np.int64))
+            residency = st.residency()
+            for e, s in sim.slot_of.items():
+                assert residency[s] == e
+            assert sum(1 for e in residency if e >= 0) == len(sim.slot_of)
+        use = st.cache_usage()
+    assert [int(use[e]) for e in range(E)] == [sim.usage.get(e, 0) for e in range(E)]
+
+
+@pytest.mark.gpu
+def test_learning_cache_refusals():
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=16, top_k=4)
+    layer = si.gen_layer(39, 0, spec)
+    xs = _tokens(spec, 40, 2)
+    _, _, recs = _resident(layer, xs)
+    with moe.MoELayer(layer, cache_slots=8, records=recs) as st:
+        for bad in ([1, 1], [16], [-1]):
+            with pytest.raises(moe.MoEError) as ei:
+                st.cache_pin(bad)
+            assert ei.value.status == 1
+    with moe.MoELayer(layer) as res:
+        with pytest.raises(moe.MoEError) as ei:
+            res.cache_pin([0])
+        assert ei.value.status == 6
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_cache_usage(res.handle, spec.n_experts)
+        assert ei.value.status == 6
