@@ -221,7 +221,6 @@ __global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* 
     const int rbeg = blockIdx.x * R;
     const int np = max(0, min(R, NR - rbeg));   // row pairs of this CTA
     const uint64_t pol = policy_evict_first();
-    const uint32_t pair_b = (uint32_t)(2 * rbH);
     auto pair_ptr = [&](int p) {
         const int r = jj0 * I + rbeg + p;
         const int jj = r / I, i = r - jj * I;

@@ -204,7 +204,6 @@ __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, i
 constexpr int kStages = 8, kRawStages = 4, kChunksPerRaw = 4;
 constexpr int kBatchSlots = kStages / kChunksPerRaw;   // operand stages are handed over a raw block at a time
 constexpr int kEpiWarps = 4, kDqWarps = 16;
-constexpr int kDqParts = kDqWarps / 4;   // K parts of a chunk per tensor-memory lane quarter
 constexpr int kTmaWarp = kEpiWarps + kDqWarps, kTokWarp = kTmaWarp + 1, kMmaWarp = kTokWarp + 1;
 constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kB16 = 128 * 128;
