@@ -402,8 +402,10 @@ enum {
      * records (records != NULL at create) in page-locked host memory, 16-byte
      * aligned (else MOE_E_UNSUPPORTED / MOE_E_INVALID). Switching on waits for
      * the layer's host copies; switching off synchronises the device and
-     * hands the state back to the host. While on, moe_cache_stage,
-     * moe_cache_prefetch and streamed moe_prefill_chunk return MOE_E_STATE;
+     * hands the state back to the host. While on, moe_cache_stage and
+     * moe_cache_prefetch return MOE_E_STATE; a streamed moe_prefill_chunk
+     * hands the state to the host for the chunk's staging waves and back after
+     * it (synchronising the device twice);
      * moe_cache_stats and moe_cache_residency synchronise the device and
      * report the device state (stage_ns does not grow). A token whose ids
      * found no victim slot (impossible while top_k <= cache_slots) sets a bit

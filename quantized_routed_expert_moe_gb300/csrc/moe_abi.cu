@@ -397,10 +397,15 @@ moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y
     cudaError_t e = launch_route_tokens(L, x, T, s);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     if (L.d.cache_slots > 0) {
-        if (cache_is_device(L))
-            return fail(MOE_E_STATE, "the cache is device-managed (MOE_OPT_CACHE_DEVICE): streamed prefill stages on "
-                                     "the host; switch the option off first");
-        return launch_prefill_streamed(L, x, T, y, y_f32, s);
+        if (!cache_is_device(L)) return launch_prefill_streamed(L, x, T, y, y_f32, s);
+        // device-managed cache: a chunk's waves are staged by the host, so the
+        // LFU state comes to the host for the chunk and goes back after it (two
+        // synchronisations, against a chunk of milliseconds); one LFU run throughout
+        moe_status st = cache_set_device(L, false);
+        if (st != MOE_OK) return st;
+        st = launch_prefill_streamed(L, x, T, y, y_f32, s);
+        const moe_status back = cache_set_device(L, true);
+        return st != MOE_OK ? st : back;
     }
     e = launch_prefill(L, x, T, y, y_f32, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");

@@ -550,8 +550,8 @@ def test_device_cache_switch_queue_and_graph():
 @pytest.mark.gpu
 def test_device_cache_refusals():
     """A source callback cannot run on the device; while the cache is
-    device-managed, host staging, lookahead and streamed prefill refuse with
-    MOE_E_STATE; a resident layer has no cache to manage."""
+    device-managed, host staging and lookahead refuse with MOE_E_STATE; a
+    resident layer has no cache to manage."""
     import torch
     spec = si.LayerSpec(hidden=256, inter=128, n_experts=16, top_k=4)
     layer = si.gen_layer(34, 0, spec)
@@ -573,10 +573,6 @@ def test_device_cache_refusals():
         assert ei.value.status == 6
         with pytest.raises(moe.MoEError) as ei:
             st.cache_prefetch(xs[0])
-        assert ei.value.status == 6
-        y = torch.empty(4 * spec.hidden, dtype=torch.float32, device="cuda")
-        with pytest.raises(moe.MoEError) as ei:
-            st.prefill_chunk(xs.reshape(-1), 4, y)
         assert ei.value.status == 6
         with pytest.raises(moe.MoEError) as ei:
             st.set_option(moe.MOE_OPT_CACHE_DEVICE, 2)
@@ -702,3 +698,54 @@ def test_learning_cache_refusals():
         with pytest.raises(moe.MoEError) as ei:
             moe.moe_cache_usage(res.handle, spec.n_experts)
         assert ei.value.status == 6
+
+
+@pytest.mark.gpu
+def test_device_cache_with_streamed_prefill():
+    """Device-managed decodes, a streamed prefill chunk (its waves staged on the
+    host, the state handed over and back), then device-managed decodes again:
+    one LFU run (the oracle's), outputs bit-identical to the resident layer."""
+    import torch
+    T, E, slots = 24, 32, 8
+    spec = si.LayerSpec(hidden=256, inter=128, n_experts=E, zipf_alpha=1.1, act="f32")
+    layer = si.gen_layer(41, 0, spec)
+    Xd = si.gen_tokens(41, 0, 12, spec)
+    Xp = si.gen_tokens(42, 0, T, spec)
+    xd = torch.from_numpy(np.ascontiguousarray(Xd, np.float32)).cuda()
+    xp = torch.from_numpy(np.ascontiguousarray(Xp, np.float32)).cuda()
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    y_dec = torch.empty((12, spec.hidden), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, max_tokens=T) as res:
+        want_p = _prefill(res, spec, xp, T)
+        for t in range(12):
+            res.decode(xd[t], None, y_dec[t])
+        res.route(xp, T, ids, w)
+        torch.cuda.synchronize()
+        sel_p = ids.cpu().numpy().copy()
+        res.route(xd, 12, ids[:12], w[:12])
+        torch.cuda.synchronize()
+        sel_d = ids[:12].cpu().numpy().copy()
+        want_d = y_dec.cpu().numpy()
+        recs = packed_records(layer, res.desc)
+    sim = oracle.moe.LFUCache(slots)
+    got_d = torch.empty((12, spec.hidden), dtype=torch.float32, device="cuda")
+    with moe.MoELayer(layer, max_tokens=T, cache_slots=slots, records=pinned_records(recs)) as st:
+        st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
+        for t in range(6):
+            st.decode(xd[t], None, got_d[t])
+            sim.access(sel_d[t])
+        got_p = _prefill(st, spec, xp, T)
+        distinct = sorted(set(int(e) for e in sel_p.reshape(-1)))
+        for wv in _waves(set(sim.count) | set(sim.pinned), distinct, slots):
+            sim.access(np.array(wv, np.int64))
+        for t in range(6, 12):
+            st.decode(xd[t], None, got_d[t])
+            sim.access(sel_d[t])
+        res_final = st.residency()
+        assert st.check() == (0, 0)
+    assert np.array_equal(got_p, want_p)
+    assert np.array_equal(got_d.cpu().numpy(), want_d)
+    for e, s_ in sim.slot_of.items():
+        assert res_final[s_] == e
+    assert sum(1 for e in res_final if e >= 0) == len(sim.slot_of)
