@@ -289,13 +289,17 @@ namespace moe {
 // Selection is the first k of the experts ordered by (-l_e, e): the largest
 // logit first, the lower index on equal values; NaN logits count as -inf so
 // every round selects a valid expert.
+// The warp's largest (bv, lowest bi among equal bv), in two warp reductions:
+// the key as an unsigned integer of the same order (-0 taken as +0, so that
+// equal floats stay equal), its maximum, then the smallest index holding it.
+// bv is never NaN here; bi is at most INT_MAX.
 __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
+    const uint32_t u = __float_as_uint(bv + 0.0f);
+    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t mi = __reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)bi : 0xffffffffu);
+    bv = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
+    bi = (int)mi;
 }
 
 // Selection key of one expert from its logit l and bias b (b = 0 without a
