@@ -362,6 +362,16 @@ moe_status moe_cache_pin(moe_layer* layer, const int32_t* experts, int32_t n);
 moe_status moe_lfu_trace(int32_t slots, int32_t n_experts, int32_t k, int32_t n_tokens, const int32_t* ids,
                          int32_t* slot, uint8_t* hit);
 
+/* The same host-only run with the learning cache: experts pinned[0..n_pinned)
+ * (distinct, in range) are pinned before the first token, as moe_cache_pin
+ * does. A pinned expert is a hit that leaves the LFU state alone; its slot[t][j]
+ * is slots + its index in `pinned` (where moe_cache_pin places it). usage
+ * (nullable, uint64 [n_experts]) receives each expert's selection count, as
+ * moe_cache_usage reports it. Colibri README, "Self-learning cache". */
+moe_status moe_lfu_trace_pinned(int32_t slots, int32_t n_experts, int32_t k, int32_t n_tokens, const int32_t* ids,
+                                const int32_t* pinned, int32_t n_pinned, int32_t* slot, uint8_t* hit,
+                                uint64_t* usage);
+
 /* ---- options and health ----------------------------------------------------------- */
 
 /* Decode implementations (MOE_OPT_DECODE_PATH):

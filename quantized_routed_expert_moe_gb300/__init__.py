@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_layer_set_next", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
-           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_cache_usage", "moe_cache_pin", "moe_lfu_trace",
+           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_cache_usage", "moe_cache_pin", "moe_lfu_trace", "moe_lfu_trace_pinned",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
@@ -131,6 +131,8 @@ def lib() -> ctypes.CDLL:
             L.moe_cache_pin.argtypes = [vp, vp, ctypes.c_int32]
             L.moe_lfu_trace.restype = st
             L.moe_lfu_trace.argtypes = [i32, i32, i32, i32, vp, vp, vp]
+            L.moe_lfu_trace_pinned.restype = st
+            L.moe_lfu_trace_pinned.argtypes = [i32, i32, i32, i32, vp, vp, i32, vp, vp, vp]
             L.moe_profile_start.restype = st
             L.moe_profile_start.argtypes = [vp, i32]
             L.moe_profile_stop.restype = st
@@ -321,6 +323,21 @@ def moe_lfu_trace(slots: int, n_experts: int, ids):
     _check(lib().moe_lfu_trace(slots, n_experts, k, n_tokens, ids.ctypes.data, slot.ctypes.data, hit.ctypes.data),
            "moe_lfu_trace")
     return slot, hit
+
+
+def moe_lfu_trace_pinned(slots: int, n_experts: int, ids, pinned):
+    """Host-only run of the cache policy with pinned experts: -> (slot, hit, usage)."""
+    import numpy as _np
+    ids = _np.ascontiguousarray(ids, dtype=_np.int32)
+    pin = _np.ascontiguousarray(_np.asarray(pinned, dtype=_np.int32))
+    n_tokens, k = ids.shape
+    slot = _np.empty((n_tokens, k), _np.int32)
+    hit = _np.empty((n_tokens, k), _np.uint8)
+    usage = _np.zeros(n_experts, _np.uint64)
+    _check(lib().moe_lfu_trace_pinned(slots, n_experts, k, n_tokens, ids.ctypes.data,
+                                      pin.ctypes.data if len(pin) else None, len(pin), slot.ctypes.data,
+                                      hit.ctypes.data, usage.ctypes.data), "moe_lfu_trace_pinned")
+    return slot, hit, usage
 
 
 def moe_cache_residency(handle, slots: int) -> list[int]:

@@ -883,4 +883,41 @@ moe_status moe_lfu_trace(int32_t slots, int32_t n_experts, int32_t k, int32_t n_
     return MOE_OK;
 }
 
+moe_status moe_lfu_trace_pinned(int32_t slots, int32_t n_experts, int32_t k, int32_t n_tokens, const int32_t* ids,
+                                const int32_t* pinned, int32_t n_pinned, int32_t* slot, uint8_t* hit,
+                                uint64_t* usage) {
+    if (!ids || !slot || !hit || (n_pinned > 0 && !pinned)) return moe::fail(MOE_E_INVALID, "NULL argument");
+    if (slots < 1 || n_experts < 1 || k < 1 || k > slots || n_tokens < 0)
+        return moe::fail(MOE_E_INVALID, "need 1 <= k <= slots, n_experts >= 1, n_tokens >= 0");
+    if (n_pinned < 0 || n_pinned > n_experts) return moe::fail(MOE_E_INVALID, "n_pinned out of range 0..n_experts");
+    std::vector<int32_t> pin_index(n_experts, -1);
+    for (int i = 0; i < n_pinned; ++i) {
+        if (pinned[i] < 0 || pinned[i] >= n_experts) return moe::fail(MOE_E_INVALID, "pinned id out of range");
+        if (pin_index[pinned[i]] >= 0) return moe::fail(MOE_E_INVALID, "repeated pinned id");
+        pin_index[pinned[i]] = i;
+    }
+    moe::Lfu lfu(slots, n_experts);
+    lfu.pin(pinned, n_pinned);
+    std::vector<moe::Fill> fills;
+    for (int t = 0; t < n_tokens; ++t) {
+        const int32_t* row = ids + (size_t)t * k;
+        for (int i = 0; i < k; ++i) {
+            if (row[i] < 0 || row[i] >= n_experts) return moe::fail(MOE_E_INVALID, "expert id out of range");
+            for (int j = 0; j < i; ++j)
+                if (row[j] == row[i]) return moe::fail(MOE_E_INVALID, "repeated expert id");
+        }
+        for (int i = 0; i < k; ++i)
+            hit[(size_t)t * k + i] = (lfu.pinned(row[i]) || lfu.slot_of(row[i]) >= 0) ? 1 : 0;
+        int h = 0;
+        lfu.access(row, k, &h, fills);
+        for (int i = 0; i < k; ++i) {
+            const int p = pin_index[row[i]];
+            slot[(size_t)t * k + i] = p >= 0 ? slots + p : lfu.slot_of(row[i]);
+        }
+    }
+    if (usage)
+        for (int e = 0; e < n_experts; ++e) usage[e] = lfu.usage(e);
+    return MOE_OK;
+}
+
 }  // extern "C"

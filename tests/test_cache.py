@@ -74,6 +74,50 @@ def test_lfu_policy_rejects_bad_rows():
 
 # --------------------------------------------------------------------------- GPU
 
+def oracle_pinned_run(rows, slots, pinned, n_experts):
+    c = oracle.moe.LFUCache(slots)
+    c.pin(pinned)
+    pin_at = {int(e): i for i, e in enumerate(pinned)}
+    slot = np.empty(rows.shape, np.int32)
+    hit = np.empty(rows.shape, np.uint8)
+    for t, ids in enumerate(rows):
+        hit[t] = [1 if (int(e) in c.count or int(e) in c.pinned) else 0 for e in ids]
+        c.access(ids)
+        slot[t] = [slots + pin_at[int(e)] if int(e) in pin_at else c.slot_of[int(e)] for e in ids]
+    usage = np.array([c.usage.get(e, 0) for e in range(n_experts)], np.uint64)
+    return slot, hit, usage, c
+
+
+@pytest.mark.parametrize("seed,E,k,slots,n_pin", [(0, 256, 8, 16, 16), (1, 32, 8, 8, 5), (2, 64, 4, 16, 60),
+                                                  (3, 9, 1, 1, 3), (4, 64, 8, 8, 0)])
+def test_lfu_pinned_policy_matches_oracle(seed, E, k, slots, n_pin):
+    """The library's host policy with pinned experts (the learning cache: the
+    hottest of a learning run, as moe_cache_pin places them) against the
+    oracle's, on seeded Zipf traces: hits, slots and usage counts."""
+    learn = zipf_rows(seed + 100, 200, E, k)
+    sim = oracle.moe.LFUCache(slots)
+    for ids in learn:
+        sim.access(ids)
+    pinned = np.array(sim.hottest(n_pin), np.int32)
+    rows = zipf_rows(seed, 400, E, k)
+    slot, hit, usage = moe.moe_lfu_trace_pinned(slots, E, rows, pinned)
+    o_slot, o_hit, o_usage, c = oracle_pinned_run(rows, slots, pinned, E)
+    assert np.array_equal(hit, o_hit)
+    assert np.array_equal(slot, o_slot)
+    assert np.array_equal(usage, o_usage)
+    if n_pin:
+        pinned_hits = sum(int(e) in c.pinned for e in rows.reshape(-1))
+        assert pinned_hits > 0 and int(hit.sum()) >= pinned_hits
+
+
+def test_lfu_pinned_rejects_bad_pins():
+    rows = np.array([[1, 2]], np.int32)
+    for bad in ([3, 3], [8], [-1]):
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_lfu_trace_pinned(4, 8, rows, bad)
+        assert ei.value.status == 1
+
+
 def packed_records(layer, ml_desc):
     """Host records in the library's layout (moe_pack_expert_record)."""
     recs = []
