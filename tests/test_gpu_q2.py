@@ -98,7 +98,8 @@ def test_q2_static_scratch_and_reproducible():
     check_rows(layer, X, *c)
 
 
-def test_q2_streamed_layer_bit_identical():
+@pytest.mark.parametrize("device", [False, True])
+def test_q2_streamed_layer_bit_identical(device):
     spec = q2(si.LayerSpec(hidden=256, inter=128, n_experts=32, zipf_alpha=1.1))
     layer = si.gen_layer(53, 0, spec)
     X = si.gen_tokens(53, 0, 12, spec)
@@ -112,10 +113,20 @@ def test_q2_streamed_layer_bit_identical():
             recs.append(buf)
     xd = to_dev(X, spec)
     y32 = torch.empty((len(X), spec.hidden), dtype=torch.float32, device="cuda")
+    if device:   # the device-managed cache reads page-locked records through their mapping
+        pinned = []
+        for r in recs:
+            t_ = torch.empty(len(r), dtype=torch.uint8).pin_memory()
+            t_.numpy()[:] = r
+            pinned.append(t_)
+        recs = pinned
     with moe.MoELayer(layer, cache_slots=16, records=recs) as st:
+        if device:
+            st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
         for t in range(len(X)):
             st.decode(xd[t], None, y32[t])
             torch.cuda.synchronize()
+        assert st.check() == (0, 0)
     assert np.array_equal(y32.cpu().numpy(), want)
 
 

@@ -127,9 +127,11 @@ def test_sigmoid_prefill_chunk(name):
     print(f"prefill {name}: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
-def test_sigmoid_streamed_layer_bit_identical():
+@pytest.mark.parametrize("device", [False, True])
+def test_sigmoid_streamed_layer_bit_identical(device):
     """A streamed layer selects in the router kernel's last block: same output
-    as the resident layer, bit for bit."""
+    as the resident layer, bit for bit, with the cache managed on the host or
+    on the device."""
     spec = sig(si.LayerSpec(hidden=256, inter=128, n_experts=32))
     layer = si.gen_layer(44, 0, spec)
     T = 10
@@ -146,11 +148,24 @@ def test_sigmoid_streamed_layer_bit_identical():
     xd = to_dev(X, spec)
     y = torch.empty((T, spec.hidden), dtype=torch.bfloat16, device="cuda")
     y32 = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
+    if device:
+        recs = [pinned_copy(r) for r in recs]
     with moe.MoELayer(layer, cache_slots=16, records=recs) as st:
+        if device:
+            st.set_option(moe.MOE_OPT_CACHE_DEVICE, 1)
         for t in range(T):
             st.decode(xd[t], y[t], y32[t])
             torch.cuda.synchronize()
+        assert st.check() == (0, 0)
     assert np.array_equal(y32.cpu().numpy(), y_res)
+
+
+def pinned_copy(r):
+    """A record in page-locked host memory (the device-managed cache reads it
+    through its mapping)."""
+    t = torch.empty(len(r), dtype=torch.uint8).pin_memory()
+    t.numpy()[:] = r
+    return t
 
 
 def test_sigmoid_option_errors():
