@@ -32,6 +32,35 @@ def test_every_declared_symbol_is_exported():
     assert sorted(moe.EXPORTS) == names
 
 
+def header_constants():
+    """Integer constants of include/moe.h: enumerators with explicit values and
+    #defines of integer expressions."""
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {n: int(v) for n, v in re.findall(r"\b(MOE_[A-Z0-9_]+)\s*=\s*(-?[0-9]+)\b", text)}
+    for n, expr in re.findall(r"#define\s+(MOE_[A-Z0-9_]+)\s+([0-9()*+ u]+)\s*$", text, flags=re.M):
+        out[n] = int(eval(expr.replace("u", "")))
+    return out
+
+
+def test_binding_constants_match_header():
+    """The binding's constants (option ids, formats, paths, limits) equal the
+    header's, so a call from Python means what the header documents."""
+    consts = header_constants()
+    for must in ("MOE_OPT_CACHE_DEVICE", "MOE_OPT_DECODE_PATH", "MOE_W_Q2G64", "MOE_MAX_TOP_K",
+                 "MOE_STATIC_SCRATCH_BYTES", "MOE_SCORE_SIGMOID"):
+        assert must in consts, must
+    checked = 0
+    for name, value in consts.items():
+        if hasattr(moe, name):
+            assert getattr(moe, name) == value, (name, getattr(moe, name), value)
+            checked += 1
+    assert checked >= 15
+    # the status values the tests compare against as literals
+    assert (consts["MOE_OK"], consts["MOE_E_INVALID"], consts["MOE_E_UNSUPPORTED"], consts["MOE_E_TIMEOUT"],
+            consts["MOE_E_STATE"], consts["MOE_E_SOURCE"]) == (0, 1, 2, 5, 6, 7)
+
+
 def test_status_strings():
     for code, name in moe.STATUS.items():
         assert moe.moe_status_str(code) == name
