@@ -206,7 +206,7 @@ def prefill_layer(workload, seed=0, experts=None):
     return layer
 
 
-def run_prefill(args):
+def run_prefill(args, emit=True):
     """One step = one 128-token chunk through each of R rotating layer replicas."""
     ws, rank, local = dist_info()
     T = args.chunk or (4 if args.workload == "glm_verify" else 128)
@@ -370,10 +370,26 @@ def run_prefill(args):
         "clocks": clk,
         "cpu_baseline": None,
     }
-    print(json.dumps(line), flush=True)
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_chunk_sample(layer, X, 8)
+    if emit:
+        print(json.dumps(line), flush=True)
+    return line
 
 
-def run_streamed(args):
+def cpu_chunk_sample(layer, X, n):
+    """The fp64 oracle on the first n tokens of a chunk (each distinct expert
+    dequantised once for the rows that selected it): tokens/s on one core."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.moe_tokens(layer, X[:n])
+    v = n / (time.perf_counter() - t0)
+    return {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"the first {n} tokens of the chunk through the fp64 numpy oracle (chunk evaluation), "
+                      "1 BLAS thread"}
+
+
+def run_streamed(args, emit=True):
     """Streamed decode through a stack of GLM-scale layers, each with a 16-slot
     LFU device cache filled from pinned host records. One step = one token
     through every layer; between layers the activation is renormalised
@@ -478,10 +494,45 @@ def run_streamed(args):
         torch.cuda.synchronize()
         for ml in stack:
             ml.pin_hottest(args.pin)
+    # warm-up tokens, recording every layer's selection: the oracle's LFU run
+    # over the same id stream must give the same hits and misses
+    rec_ids = torch.empty((args.warmup, Lc, spec.top_k), dtype=torch.int32, device="cuda")
+    rec_w = torch.empty((args.warmup, Lc, spec.top_k), dtype=torch.float32, device="cuda")
+    pre = [ml.cache_stats() for ml in stack]
+
+    def token_rec(i):
+        x.copy_(x_host[i], non_blocking=True)
+        for li, ml in enumerate(stack):
+            ml.decode(x, None, y, stream=stream)
+            ml.selection(1, rec_ids[i, li], rec_w[i, li], stream=stream)
+            x.copy_(chain(y))
+
     for i in range(args.warmup):
-        token(i)
+        if args.lookahead:
+            token(i)
+        else:
+            token_rec(i)
     torch.cuda.synchronize()
     s0 = [ml.cache_stats() for ml in stack]
+    lfu_check = None
+    if not args.lookahead and not args.pin:
+        import oracle
+        ids_np = rec_ids.cpu().numpy()
+        o_hits = o_miss = 0
+        for li in range(Lc):
+            c = oracle.LFUCache(16)
+            for i in range(args.warmup):
+                h, f = c.access(ids_np[i, li])
+                o_hits += len(h)
+                o_miss += len(f)
+        m_hits = sum(b["hits"] - a["hits"] for a, b in zip(pre, s0))
+        m_miss = sum(b["misses"] - a["misses"] for a, b in zip(pre, s0))
+        lfu_check = {"tokens": args.warmup, "layers": Lc, "hits": m_hits, "misses": m_miss,
+                     "oracle_hits": o_hits, "oracle_misses": o_miss,
+                     "hit_rate": m_hits / max(m_hits + m_miss, 1),
+                     "oracle_hit_rate": o_hits / max(o_hits + o_miss, 1),
+                     "note": "the warm-up tokens (from an empty cache), every layer's selection recorded and run "
+                             "through the oracle's LFU simulation"}
     p0 = [ml.prefetch_stats() for ml in stack]
     clocks = ClockSampler(local)
     clocks.start()
@@ -582,11 +633,45 @@ def run_streamed(args):
                      "peak_source": "measured here: pinned 1 GiB host-to-device copy"},
         "e2e": {"value": args.steps * ws / wall, "unit": UNIT, "h2d_bytes_per_step": spec.hidden * 2 + h2d / args.steps,
                 "d2h_bytes_per_step": 0},
+        "lfu_check": lfu_check,
         "gpu_launches": None,
         "clocks": clk,
         "cpu_baseline": None,
     }
-    print(json.dumps(line), flush=True)
+    if ws == 1 and not args.no_cpu_baseline:
+        layer0 = si.Layer(spec, si.gen_router(0, 0, spec), LazyExperts(0, 1000, spec, P, 0),
+                          si.gen_expert(0, 0, E, spec), si.gen_router_bias(0, 0, spec), 0, 0)
+        n = 2
+        t0 = time.perf_counter()
+        for i in range(n):
+            import oracle
+            oracle.moe_token(layer0, X0[i])
+        dt = (time.perf_counter() - t0) / n
+        line["cpu_baseline"] = {"value": 1.0 / (dt * Lc), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{n} layer-tokens of the first layer through the fp64 oracle, scaled to "
+                                          f"{Lc} layers per token, 1 BLAS thread"}
+    if emit:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+class LazyExperts:
+    """The routed experts of one layer of the streamed stack, generated on
+    first use (layer l's expert e is alias-pool record (l * E + e) * 2654435761
+    mod P, itself seeded expert p of layer `pool_layer`)."""
+
+    def __init__(self, seed, pool_layer, spec, P, layer):
+        self.seed, self.pool_layer, self.spec, self.P, self.layer = seed, pool_layer, spec, P, layer
+        self.cache = {}
+
+    def __len__(self):
+        return self.spec.n_experts
+
+    def __getitem__(self, e):
+        p = ((self.layer * self.spec.n_experts + int(e)) * 2654435761) % self.P
+        if p not in self.cache:
+            self.cache[p] = si.gen_expert(self.seed, self.pool_layer, p, self.spec)
+        return self.cache[p]
 
 
 def h2d_peak_gbs(stream):
@@ -707,86 +792,27 @@ def run_streamed_prefill(args):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="glm_decode",
-                    choices=["glm_decode", "glm_decode_q2", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense", "glm_verify",
-                             "glm_streamed", "glm_streamed_prefill"])
-    ap.add_argument("--layers", type=int, default=75, help="glm_streamed: layers in the stack")
-    ap.add_argument("--pool", type=int, default=256,
-                    help="glm_streamed: distinct expert records in pinned host memory (alias pool)")
-    ap.add_argument("--tokens", type=int, default=1000)
-    ap.add_argument("--chain", default="norm", choices=["norm", "residual"],
-                    help="glm_streamed: how one layer's output becomes the next layer's input")
-    ap.add_argument("--lookahead", action="store_true",
-                    help="glm_streamed: stage each next layer's predicted experts (moe_cache_prefetch)")
-    ap.add_argument("--pin", type=int, default=0,
-                    help="glm_streamed: pin each layer's N most used experts after --learn tokens (learning cache)")
-    ap.add_argument("--learn", type=int, default=32, help="glm_streamed: tokens whose routing --pin learns from")
-    ap.add_argument("--device-cache", action="store_true",
-                    help="glm_streamed: device-managed caches (MOE_OPT_CACHE_DEVICE); also times the token as a CUDA graph")
-    ap.add_argument("--chunk", type=int, default=None,
-                    help="tokens per prefill chunk / verify batch (default 128; glm_verify: 4)")
-    ap.add_argument("--replicas", type=int, default=None)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="auto", choices=["auto", "split", "fused"],
-                    help="decode implementation (auto: the three-kernel split path)")
-    ap.add_argument("--experts", type=int, default=None,
-                    help="override the routed-expert count (a smaller layer of the same shape, for profiler captures)")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+DECODE_DESC = {"glm_decode": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q4g64 experts, fp32 router",
+               "glm_decode_q2": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q2g64 experts, fp32 router",
+               "gemma_decode": "Gemma-style decode: H2816 I704 E128 top-8 + 1 shared, q4g64 experts, q8g64 router",
+               "tiny": "tiny layer: H512 I256 E32 top-8 + 1 shared, fp32 I/O"}
+DECODE_REPLICAS = {"glm_decode": 4, "glm_decode_q2": 4, "gemma_decode": 16, "tiny": 64}
+DECODE_CPU_TOKENS = {"glm_decode": 6, "glm_decode_q2": 6, "gemma_decode": 60, "tiny": 400}
+DTYPE = "int8 x int4 dp4a on 16-bit fixed-point activations per run of 32, fp32 accumulate and SwiGLU"
 
-    if args.workload.startswith("glm_prefill") or args.workload == "glm_verify":
-        run_prefill(args)
-        return
-    if args.workload == "glm_streamed" and args.device_cache and args.lookahead:
-        ap.error("--lookahead stages on the host; it does not combine with --device-cache")
-    if args.workload == "glm_streamed":
-        run_streamed(args)
-        return
-    if args.workload == "glm_streamed_prefill":
-        run_streamed_prefill(args)
-        return
-    spec = si.CONFIGS[args.workload]
-    if args.experts:
-        import dataclasses
-        spec = dataclasses.replace(spec, n_experts=args.experts)
-    desc = {"glm_decode": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q4g64 experts, fp32 router",
-            "glm_decode_q2": "GLM-scale decode: H6144 I2048 E256 top-8 + 1 shared, q2g64 experts, fp32 router",
-            "gemma_decode": "Gemma-style decode: H2816 I704 E128 top-8 + 1 shared, q4g64 experts, q8g64 router",
-            "tiny": "tiny layer: H512 I256 E32 top-8 + 1 shared, fp32 I/O"}[args.workload]
-    if args.experts:
-        desc = desc.replace(f"E{si.CONFIGS[args.workload].n_experts}", f"E{args.experts}")
-    workload = f"{desc}; {args.tokens} sequential single-token decodes per step"
-    if args.impl == "reference":
-        run_reference(args, spec, workload)
-        return
 
+def decode_bench(args, name, spec, workload):
+    """T seeded tokens decoded one after another per step, token t on replica t
+    mod R; returns the JSON line (dict)."""
     import torch
     import torch.distributed as dist
 
     import quantized_routed_expert_moe_gb300 as moe
-    from quantized_routed_expert_moe_gb300 import build as _b
 
     ws, rank, local = dist_info()
-    if ws > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    if rank == 0:
-        _b.build()
-    if ws > 1:
-        dist.barrier()
-
-    R = args.replicas or {"glm_decode": 4, "glm_decode_q2": 4, "gemma_decode": 16, "tiny": 64}[args.workload]
+    R = args.replicas or DECODE_REPLICAS[name]
     layer = si.gen_layer(0, 0, spec)
     reps = [moe.MoELayer(layer, device=local) for _ in range(R)]
-    path = {"auto": moe.MOE_PATH_AUTO, "split": moe.MOE_PATH_SPLIT, "fused": moe.MOE_PATH_FUSED}[args.path]
-    for r in reps:
-        r.set_option(moe.MOE_OPT_DECODE_PATH, path)
     T = args.tokens
     X = si.gen_tokens(1000 * rank, 0, T, spec)   # distinct tokens per rank
     xdt = torch.bfloat16 if spec.act == "bf16" else torch.float32
@@ -828,6 +854,10 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
+    for r in reps:
+        st, bits = r.check()
+        if st:
+            raise RuntimeError(f"decode reported device error bits {bits:#x}")
 
     # the same K steps again with a CUDA event pair around every kernel the
     # library launches (recorded by the library on the launch stream)
@@ -839,9 +869,9 @@ def main():
     torch.cuda.synchronize()
     prof = {}
     for h in handles:
-        for name, (n, t) in moe.moe_profile_stop(h).items():
-            a, b = prof.get(name, (0, 0.0))
-            prof[name] = (a + n, b + t)
+        for kname, (n, t) in moe.moe_profile_stop(h).items():
+            a, b = prof.get(kname, (0, 0.0))
+            prof[kname] = (a + n, b + t)
 
     # per-token intervals: one step again with an event after every token. The
     # events sit between consecutive tokens' kernels (they block the overlap of
@@ -894,20 +924,23 @@ def main():
         graph = {"error": str(exc).splitlines()[0][:200]}
         torch.cuda.synchronize()
 
-    # end to end through the C ABI with HOST buffers: moe_decode_tokens_host
-    # copies the step's inputs from pinned host memory, decodes the T tokens and
-    # copies the outputs back, then waits for its stream (one layer instance,
-    # itself larger than L2)
-    e2e_layer = reps[0]
+    # end to end with HOST buffers: every step copies its T input tokens from
+    # pinned host memory to the device, decodes them through moe_decode on the
+    # same R rotating replicas as the timed region, copies the T outputs back
+    # to pinned host memory and synchronises
+    def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(y_dev, non_blocking=True)
+        torch.cuda.synchronize()
+
     for _ in range(args.warmup):
-        e2e_layer.decode_tokens_host(x_host, T, y_host, stream=stream)
-    torch.cuda.synchronize()
+        step_e2e()
     if ws > 1:
         dist.barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        e2e_layer.decode_tokens_host(x_host, T, y_host, stream=stream)
-    torch.cuda.synchronize()
+        step_e2e()
     e2e_s = time.perf_counter() - t0
 
     ms, e2e_s = max_over_ranks([ms, e2e_s], "cuda")
@@ -917,47 +950,44 @@ def main():
 
     hbm, _, peak_kind = peaks()
     tot_b, gu_b, down_b, router_b = algorithmic_bytes(spec)
-    if "decode_fused" in prof:
-        dom, dom_bytes = "decode_fused", tot_b       # one kernel does the whole token
-    else:
-        dom, dom_bytes = "gateup_decode", gu_b
+    dom, dom_bytes = "gateup_decode", gu_b
     n_dom, t_dom = prof.get(dom, (0, 0.0))
     dom_avg_ms = t_dom / max(n_dom, 1)
     dom_gbs = dom_bytes / (dom_avg_ms / 1e3) / 1e9 if n_dom else None
-    launches = sum(n for n, _ in prof.values()) // 1
+    launches = sum(n for n, _ in prof.values())
     kernels = {k: {"launches": n, "avg_us": t / max(n, 1) * 1e3, "share": t / max(sum(v[1] for v in prof.values()), 1e-9)}
                for k, (n, t) in prof.items()}
-
-    if rank != 0:
-        if ws > 1:
-            dist.destroy_process_group()
-        return
+    for r in reps:
+        r.close()
 
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
-        n_cpu = {"glm_decode": 6, "glm_decode_q2": 6, "gemma_decode": 60, "tiny": 400}[args.workload]
+        n_cpu = DECODE_CPU_TOKENS[name]
         v = oracle_sample(layer, X, n_cpu)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{n_cpu} tokens of the same layer through the fp64 numpy oracle, 1 BLAS thread"}
+        if name == "glm_decode":
+            cpu["all_cores"] = oracle_all_cores(name, X, 2 * (os.cpu_count() or 1))
 
     traffic = None
-    tf = os.path.join(ROOT, "profiles", f"{dom}_{args.workload}_traffic.json")
+    tf = os.path.join(ROOT, "profiles", f"{dom}_{name}_traffic.json")
     if os.path.exists(tf):
         tj = json.load(open(tf))
         if tj.get("kernel_source_sha") == kernel_source_sha(dom):
             traffic = tj.get("bytes_per_launch")
 
-    line = {
+    return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
         "config": {"workload": workload, "tokens_per_step": T, "layer_replicas": R,
                    "l2": f"inputs larger than L2: {R} rotating layer replicas "
                          f"({R * (len(layer.experts) + 1) * spec.expert_bytes() / 1e9:.1f} GB of weights)",
-                   "weights": "affine group-64 4-bit experts, dequantised on the fly; fp32 accumulate",
+                   "weights": f"affine group-64 {spec.expert_bits}-bit experts, dequantised on the fly",
                    "parallelism": f"replicas x{ws}"},
         "effective_hbm_gbs": tot_b * value / ws / 1e9,
         "hbm_roofline_frac_nominal_8tbs": tot_b * value / ws / 8e12,
+        "hbm_roofline_frac_measured": tot_b * value / ws / 1e9 / hbm,
         "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": (dom_gbs / hbm) if dom_gbs else None, "traffic": traffic,
                      "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy), burst",
@@ -965,16 +995,171 @@ def main():
                      "avg_launch_us": dom_avg_ms * 1e3},
         "kernels": kernels,
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
+                "path": "pinned host -> device copy of the step's tokens, moe_decode per token over the same "
+                        "rotating replicas as the timed region, device -> pinned host copy, synchronize"},
         "gpu_launches": launches,
         "per_token_latency": latency,
         "graph": graph,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
+
+
+def _oracle_worker(job):
+    """One token of the oracle (a spawned process): the layer's router, the
+    shared expert and the 8 selected experts are generated here."""
+    import oracle
+    name, x, seed = job
+    spec = si.CONFIGS[name]
+
+    class Lazy:
+        def __init__(self):
+            self.c = {}
+
+        def __len__(self):
+            return spec.n_experts
+
+        def __getitem__(self, e):
+            e = int(e)
+            if e not in self.c:
+                self.c[e] = si.gen_expert(seed, 0, e, spec)
+            return self.c[e]
+
+    layer = si.Layer(spec, si.gen_router(seed, 0, spec), Lazy(),
+                     si.gen_expert(seed, 0, spec.n_experts, spec) if spec.n_shared else None,
+                     si.gen_router_bias(seed, 0, spec), seed, 0)
+    t0 = time.perf_counter()
+    oracle.moe_token(layer, x)
+    return time.perf_counter() - t0
+
+
+def oracle_all_cores(name, X, n):
+    """The oracle on every host core at once: n tokens over a pool of
+    os.cpu_count() spawned processes (one BLAS thread each); tokens/s of the
+    whole pool, counting only the oracle's time per token in each worker."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    jobs = [(name, X[i % len(X)], 0) for i in range(n)]
+    t0 = time.perf_counter()
+    with cf.ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+        per = list(ex.map(_oracle_worker, jobs))
+    wall = time.perf_counter() - t0
+    busy = sum(per)
+    return {"value": n / (busy / cores) if busy else None, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} tokens over {cores} spawned worker processes (each generates the layer's router "
+                      "and the experts a token needs, then times the fp64 oracle on it); value = tokens / "
+                      "(summed oracle seconds / cores)",
+            "wall_s_including_generation": wall}
+
+
+def sub_args(args, **kw):
+    import copy
+    a = copy.copy(args)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="glm_decode",
+                    choices=["glm_decode", "glm_decode_q2", "gemma_decode", "tiny", "glm_prefill", "glm_prefill_dense",
+                             "glm_verify", "glm_streamed", "glm_streamed_prefill"])
+    ap.add_argument("--layers", type=int, default=75, help="glm_streamed: layers in the stack")
+    ap.add_argument("--pool", type=int, default=256,
+                    help="glm_streamed: distinct expert records in pinned host memory (alias pool)")
+    ap.add_argument("--tokens", type=int, default=1000)
+    ap.add_argument("--chain", default="norm", choices=["norm", "residual"],
+                    help="glm_streamed: how one layer's output becomes the next layer's input")
+    ap.add_argument("--lookahead", action="store_true",
+                    help="glm_streamed: stage each next layer's predicted experts (moe_cache_prefetch)")
+    ap.add_argument("--pin", type=int, default=0,
+                    help="glm_streamed: pin each layer's N most used experts after --learn tokens (learning cache)")
+    ap.add_argument("--learn", type=int, default=32, help="glm_streamed: tokens whose routing --pin learns from")
+    ap.add_argument("--device-cache", action="store_true",
+                    help="glm_streamed: device-managed caches (MOE_OPT_CACHE_DEVICE); also times the token as a CUDA graph")
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="tokens per prefill chunk / verify batch (default 128; glm_verify: 4)")
+    ap.add_argument("--replicas", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="default workload: print the GLM-scale decode line without the other configurations")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the routed-expert count (a smaller layer of the same shape, for profiler captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.workload.startswith("glm_prefill") or args.workload == "glm_verify":
+        run_prefill(args)
+        return
+    if args.workload == "glm_streamed" and args.device_cache and args.lookahead:
+        ap.error("--lookahead stages on the host; it does not combine with --device-cache")
+    if args.workload == "glm_streamed":
+        run_streamed(args)
+        return
+    if args.workload == "glm_streamed_prefill":
+        run_streamed_prefill(args)
+        return
+    spec = si.CONFIGS[args.workload]
+    if args.experts:
+        import dataclasses
+        spec = dataclasses.replace(spec, n_experts=args.experts)
+    desc = DECODE_DESC[args.workload]
+    if args.experts:
+        desc = desc.replace(f"E{si.CONFIGS[args.workload].n_experts}", f"E{args.experts}")
+    workload = f"{desc}; {args.tokens} sequential single-token decodes per step"
+    if args.impl == "reference":
+        run_reference(args, spec, workload)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from quantized_routed_expert_moe_gb300 import build as _b
+
+    ws, rank, local = dist_info()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        _b.build()
+    if ws > 1:
+        dist.barrier()
+
+    line = decode_bench(args, args.workload, spec, workload)
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    if args.workload == "glm_decode" and ws == 1 and not args.headline_only and not args.experts:
+        # the other configurations of the same path, each with its own
+        # roofline, oracle baseline and clock record
+        subs = {
+            "gemma_decode": lambda: decode_bench(
+                sub_args(args, replicas=None), "gemma_decode", si.CONFIGS["gemma_decode"],
+                DECODE_DESC["gemma_decode"] + f"; {args.tokens} sequential single-token decodes per step"),
+            "glm_prefill_dense": lambda: run_prefill(sub_args(args, workload="glm_prefill_dense", replicas=None,
+                                                              chunk=None), emit=False),
+            "glm_prefill": lambda: run_prefill(sub_args(args, workload="glm_prefill", replicas=None, chunk=None),
+                                               emit=False),
+            "glm_streamed": lambda: run_streamed(sub_args(args, workload="glm_streamed", layers=75, pool=256,
+                                                          steps=20, warmup=16, device_cache=True, lookahead=False,
+                                                          pin=0, chain="norm"), emit=False),
+        }
+        line["configs"] = {}
+        for name, fn in subs.items():
+            try:
+                line["configs"][name] = fn()
+            except Exception as exc:   # reported in the line, the headline stands
+                line["configs"][name] = {"error": f"{type(exc).__name__}: {str(exc).splitlines()[0][:300]}"}
+            torch.cuda.empty_cache()
     print(json.dumps(line), flush=True)
-    for r in reps:
-        r.close()
     if ws > 1:
         dist.destroy_process_group()
 

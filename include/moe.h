@@ -99,8 +99,7 @@ typedef struct {
     int32_t top_k;         /* 1..MOE_MAX_TOP_K */
     int32_t n_shared;      /* 0 or 1 */
     int32_t router_fmt;    /* MOE_W_F32 or MOE_W_Q8G64 */
-    int32_t expert_fmt;    /* MOE_W_Q4G64, or MOE_W_Q2G64 (2-bit experts: decode only; moe_prefill_chunk
-                              with T > 1 and the fused decode path return MOE_E_UNSUPPORTED) */
+    int32_t expert_fmt;    /* MOE_W_Q4G64 or MOE_W_Q2G64 */
     int32_t group;         /* 64 */
     int32_t act_dtype;     /* MOE_F32 or MOE_BF16: dtype of x and y */
     int32_t max_tokens;    /* largest T for moe_route / moe_prefill_chunk, 1..MOE_MAX_CHUNK */
@@ -192,12 +191,8 @@ enum {
  * weights and is ignored for softmax. The layer's router_bias (moe_layer_create)
  * is the bias_e above. Applies to every later moe_route, moe_decode,
  * moe_decode_static_scratch and moe_prefill_chunk call; set it before the
- * first of them (the call does not wait for work in flight). The fused decode
- * path supports softmax only: with MOE_SCORE_SIGMOID the layer runs the split
- * path, and setting MOE_OPT_DECODE_PATH to MOE_PATH_FUSED afterwards returns
- * MOE_E_UNSUPPORTED (as does this call, with MOE_SCORE_SIGMOID, while the
- * fused path is selected). Errors: MOE_E_INVALID for a NULL layer, an unknown
- * scoring or a bad routed_scaling. */
+ * first of them (the call does not wait for work in flight). Errors:
+ * MOE_E_INVALID for a NULL layer, an unknown scoring or a bad routed_scaling. */
 moe_status moe_layer_set_router_scoring(moe_layer* layer, int32_t scoring, float routed_scaling);
 
 /* ---- compute --------------------------------------------------------------- */
@@ -210,6 +205,18 @@ moe_status moe_layer_set_router_scoring(moe_layer* layer, int32_t scoring, float
  *        scaled, renormalised sigmoid scores.
  * Router GEMV/GEMM with fp32 accumulation; selection and weights in fp32. */
 moe_status moe_route(moe_layer* layer, const void* x, int32_t T, int32_t* ids, float* w, void* stream);
+
+/* The expert selection of the last moe_route, moe_decode or moe_prefill_chunk
+ * on this layer -- the one that call itself computed and combined with -- for
+ * tokens 0..T-1 (T = 1 after moe_decode): ids device int32 [T][top_k] in
+ * selection order, w device fp32 [T][top_k], both caller-owned. The copies are
+ * enqueued on `stream` (order it after that call, e.g. the same stream).
+ * Every call selects once per token (moe_decode in its router kernel's last
+ * block, which the gate/up and down kernels then read; moe_prefill_chunk in
+ * one block per token); moe_decode_static_scratch keeps its selection in the
+ * static region and does not update this one. TurboFieldfare article, "token generation" (top-8 selection);
+ * Inferno README, "Current Scope" (exact top-8). Errors: MOE_E_INVALID. */
+moe_status moe_layer_selection(moe_layer* layer, int32_t T, int32_t* ids, float* w, void* stream);
 
 /* One decode token.
  *   x:     device [H] of act_dtype.
@@ -236,9 +243,9 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
  *
  * Arguments, layouts, result and errors are those of moe_decode, with these
  * differences:
- *   - The work runs on the split path (router partials, then gate/up and
- *     down kernels that each select from the partials) whatever the layer's
- *     MOE_OPT_DECODE_PATH says; streamed layers (cache_slots > 0) get
+ *   - The same three kernels run; gate/up waits for the router grid rather
+ *     than for a ready flag, and the down kernel starts on the shared expert
+ *     only after its wait for gate/up. Streamed layers (cache_slots > 0) get
  *     MOE_E_UNSUPPORTED.
  *   - The scratch holds the router's partial logits [splits][E], the logits
  *     [E], ids [k], weights [k] and the SwiGLU outputs [k + 1][I] (each
@@ -374,25 +381,25 @@ moe_status moe_lfu_trace_pinned(int32_t slots, int32_t n_experts, int32_t k, int
 
 /* ---- options and health ----------------------------------------------------------- */
 
-/* Decode implementations (MOE_OPT_DECODE_PATH):
- *   MOE_PATH_AUTO   the faster of the two on GB300: the three-kernel decode;
- *   MOE_PATH_SPLIT  three kernels chained with programmatic dependent launch:
- *                   router partial logits, gate/up + SwiGLU (each CTA selects
- *                   the top k from the partials), down + combine;
- *   MOE_PATH_FUSED  one persistent cooperative kernel per token (setting it on
- *                   a shape it does not support returns MOE_E_UNSUPPORTED). */
-enum { MOE_PATH_AUTO = 0, MOE_PATH_SPLIT = 1, MOE_PATH_FUSED = 2 };
-
+/* moe_decode on a resident layer runs three kernels chained with programmatic
+ * dependent launch: the router (logits, then the top-k selection in its last
+ * block, which raises a ready flag); gate/up + SwiGLU (computes the shared
+ * expert's rows while the router runs, waits for the flag, then the routed
+ * experts' rows; each completed half-group of SwiGLU outputs is quantised once
+ * by the warp that completed it); down + combine (starts on the shared
+ * expert's rows once its half-groups are all staged, then waits for gate/up
+ * and computes the routed experts). Device-side waits on the flag and the
+ * counter are bounded (0.2 s) and fall back to the ordinary wait. */
 enum {
-    MOE_OPT_DECODE_PATH = 1,
-    /* Test hook for failure detection: while nonzero, the fused decode never
-     * publishes the expert IDs, so every device-side wait on them runs out
-     * (about half a second), records MOE_E_TIMEOUT for moe_layer_check and
-     * drains out cleanly. */
-    MOE_OPT_TEST_STALL_ROUTING = 2,
-    /* Phase tracing of the fused decode: while nonzero, every CTA records the
-     * GPU global timer (ns) at MOE_TRACE_POINTS phase boundaries of the last
-     * launch; read them with moe_trace_read. Costs a few stores per CTA. */
+    /* Test hook for failure detection: while nonzero, the decode gate/up
+     * kernel never counts the shared expert's staged half-groups, so the down
+     * kernel's bounded wait on the count runs out (0.2 s), records
+     * MOE_E_TIMEOUT for moe_layer_check and computes the shared expert after
+     * its ordinary wait instead (the output is unchanged). */
+    MOE_OPT_TEST_STALL_SHARED = 2,
+    /* Phase tracing of the decode kernels and the prefill GEMMs: while
+     * nonzero, every CTA records timestamps; read them with
+     * moe_trace_read_split. Costs a few stores per CTA. */
     MOE_OPT_TRACE = 3,
     /* Deadline of every host-side wait of a streamed layer (expert ids coming
      * back, staging and table buffers free for reuse), in milliseconds
@@ -423,17 +430,6 @@ enum {
      * generation"): the 16-slot LFU cache and its misses loaded per token. */
     MOE_OPT_CACHE_DEVICE = 6
 };
-
-/* Trace points recorded per CTA (in this order): kernel start, activations
- * staged, router chunks done, IDs published (only the CTA that selected, else
- * 0), IDs seen by the producer, gate/up rows done, all SwiGLU outputs visible,
- * SwiGLU outputs staged, down rows and combine done, exit. */
-#define MOE_TRACE_POINTS 10
-
-/* Copy the trace of the last fused decode (after it completed): out receives
- * n_ctas * MOE_TRACE_POINTS uint64 timestamps (ns), CTA-major; *n_ctas receives
- * the grid size. Waits for the device. */
-moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t* n_ctas);
 
 /* Traces of the last three-kernel decode and of the last prefill chunk's two
  * grouped GEMMs (while MOE_OPT_TRACE is on): out receives

@@ -43,6 +43,16 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
+def _affine_g64(q: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """W[n][k] = q[n][k] * s[n][k // 64] + b[n][k // 64] for integer codes q
+    [N][K], with the binary16 scale and bias of each group of 64 along k
+    (exact in float64: a code times a binary16 plus a binary16)."""
+    N, K = q.shape
+    s = f16_bits_to_f64(scale).reshape(N, K // 64, 1)
+    b = f16_bits_to_f64(bias).reshape(N, K // 64, 1)
+    return (q.reshape(N, K // 64, 64) * s + b).reshape(N, K)
+
+
 def dequant_q4g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
     """Affine group-64 4-bit dequantisation, W[n][k] = code(n,k) * s[n][k//64] + b[n][k//64].
 
@@ -55,12 +65,10 @@ def dequant_q4g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.
     codes = np.asarray(codes, dtype=np.uint8)
     N, half_k = codes.shape
     K = 2 * half_k
-    q = np.empty((N, K), dtype=np.float64)
-    q[:, 0::2] = codes & 0x0F
-    q[:, 1::2] = codes >> 4
-    s = np.repeat(f16_bits_to_f64(scale).reshape(N, K // 64), 64, axis=1)
-    b = np.repeat(f16_bits_to_f64(bias).reshape(N, K // 64), 64, axis=1)
-    return q * s + b
+    q = np.empty((N, half_k, 2), dtype=np.uint8)   # q[n][k // 2][k % 2]
+    q[:, :, 0] = codes & 0x0F
+    q[:, :, 1] = codes >> 4
+    return _affine_g64(q.reshape(N, K), scale, bias)
 
 
 def dequant_q2g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
@@ -76,12 +84,10 @@ def dequant_q2g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.
     codes = np.asarray(codes, dtype=np.uint8)
     N, quarter_k = codes.shape
     K = 4 * quarter_k
-    q = np.empty((N, K), dtype=np.float64)
+    q = np.empty((N, quarter_k, 4), dtype=np.uint8)   # q[n][k // 4][k % 4]
     for j in range(4):
-        q[:, j::4] = (codes >> (2 * j)) & 0x03
-    s = np.repeat(f16_bits_to_f64(scale).reshape(N, K // 64), 64, axis=1)
-    b = np.repeat(f16_bits_to_f64(bias).reshape(N, K // 64), 64, axis=1)
-    return q * s + b
+        q[:, :, j] = (codes >> (2 * j)) & 0x03
+    return _affine_g64(q.reshape(N, K), scale, bias)
 
 
 def dequant_q8g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.ndarray:
@@ -90,11 +96,7 @@ def dequant_q8g64(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray) -> np.
     TurboFieldfare "execution architecture": the router is stored at 8 bits in
     the same affine group-64 scheme. codes are row-major [N][K] bytes.
     """
-    codes = np.asarray(codes, dtype=np.uint8)
-    N, K = codes.shape
-    s = np.repeat(f16_bits_to_f64(scale).reshape(N, K // 64), 64, axis=1)
-    b = np.repeat(f16_bits_to_f64(bias).reshape(N, K // 64), 64, axis=1)
-    return codes.astype(np.float64) * s + b
+    return _affine_g64(np.asarray(codes, dtype=np.uint8), scale, bias)
 
 
 def router_weights_f64(router) -> np.ndarray:
@@ -305,14 +307,46 @@ def moe_tokens(layer, X, ids: np.ndarray | None = None):
     so a fetched expert serves several rows) and Colibri "Union" / batch-union
     MoE (each distinct expert of the batch read once, applied to every row
     routed to it): both are execution strategies; the rows are independent.
+
+    Every row is ``moe_token`` of that token (same selection, weights and
+    order of the sum: shared first, then the slots in selection order); the
+    only difference is that each expert is dequantised once for all the rows
+    that selected it, and its gate/up/down products for those rows are one
+    matrix product each. Returns (Y float64 [T][H], [RouteInfo] * T).
     """
     Wr = router_weights_f64(layer.router)
-    ys, infos = [], []
-    for t in range(len(X)):
-        y, info = moe_token(layer, X[t], None if ids is None else ids[t], Wr)
-        ys.append(y)
+    T = len(X)
+    X64 = np.stack([_x_f64(layer, X[t]) for t in range(T)])
+    infos = []
+    for t in range(T):
+        info = route_token(layer, X64[t], Wr)
+        if ids is not None:
+            key, sc = route_keys(layer, _logits(layer, Wr, X64[t]))
+            sel = np.asarray(ids[t], dtype=np.int64)
+            info = RouteInfo(sel, _weights(layer, key, sc, sel), info.gap, info.scale)
         infos.append(info)
-    return np.stack(ys), infos
+
+    def ffn_rows(expert, rows):   # f(x_t) for the given rows, one dequantisation
+        Xs = X64[rows]
+        g = Xs @ _deq(expert.gate).T
+        u = Xs @ _deq(expert.up).T
+        return (silu(g) * u) @ _deq(expert.down).T
+
+    k = layer.spec.top_k
+    F = np.zeros((T, k, layer.spec.hidden))          # F[t][j] = f_{S_j}(x_t)
+    users = {}
+    for t in range(T):
+        for j, e in enumerate(infos[t].ids):
+            users.setdefault(int(e), []).append((t, j))
+    for e, tj in users.items():
+        out = ffn_rows(layer.experts[e], [t for t, _ in tj])
+        for (t, j), row in zip(tj, out):
+            F[t, j] = row
+    Y = ffn_rows(layer.shared, list(range(T))) if layer.shared is not None else np.zeros((T, layer.spec.hidden))
+    for t in range(T):
+        for j in range(k):
+            Y[t] += infos[t].weights[j] * F[t, j]
+    return Y, infos
 
 
 def layer_dense_f64(layer, x) -> np.ndarray:

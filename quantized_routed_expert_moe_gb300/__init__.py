@@ -26,19 +26,16 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
-           "moe_layer_device_bytes", "moe_layer_set_next", "moe_layer_set_router_scoring", "moe_route", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
+           "moe_layer_device_bytes", "moe_layer_set_next", "moe_layer_set_router_scoring", "moe_route", "moe_layer_selection", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
            "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_cache_usage", "moe_cache_pin", "moe_lfu_trace", "moe_lfu_trace_pinned",
-           "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read", "moe_trace_read_split",
+           "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
-MOE_PATH_AUTO, MOE_PATH_SPLIT, MOE_PATH_FUSED = 0, 1, 2
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_STATIC_SCRATCH_BYTES = 256 * 1024
-MOE_OPT_DECODE_PATH, MOE_OPT_TEST_STALL_ROUTING, MOE_OPT_TRACE = 1, 2, 3
+MOE_OPT_TEST_STALL_SHARED, MOE_OPT_TRACE = 2, 3
 MOE_OPT_HOST_TIMEOUT_MS, MOE_OPT_TEST_STALL_COPIES_MS, MOE_OPT_CACHE_DEVICE = 4, 5, 6
-MOE_TRACE_POINTS = 10
-TRACE_NAMES = ("start", "x_staged", "router_done", "ids_published", "ids_seen", "gateup_done",
-               "h_visible", "h_staged", "down_done", "exit")
+MOE_MAX_TOP_K = 8
 
 
 class MoEError(RuntimeError):
@@ -145,8 +142,8 @@ def lib() -> ctypes.CDLL:
             L.moe_layer_set_router_scoring.argtypes = [vp, i32, ctypes.c_float]
             L.moe_layer_check.restype = st
             L.moe_layer_check.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
-            L.moe_trace_read.restype = st
-            L.moe_trace_read.argtypes = [vp, vp, i32, ctypes.POINTER(i32)]
+            L.moe_layer_selection.restype = st
+            L.moe_layer_selection.argtypes = [vp, i32, vp, vp, vp]
             L.moe_trace_read_split.restype = st
             L.moe_trace_read_split.argtypes = [vp, vp, i32]
             L.moe_status_str.restype = ctypes.c_char_p
@@ -394,14 +391,10 @@ def moe_layer_check(handle) -> tuple[int, int]:
     return st, bits.value
 
 
-def moe_trace_read(handle, max_ctas: int = 1024):
-    """Per-CTA phase timestamps (ns) of the last fused decode: list of lists."""
-    import array
-    cap = max_ctas * MOE_TRACE_POINTS
-    buf = (ctypes.c_uint64 * cap)()
-    n = ctypes.c_int32()
-    _check(lib().moe_trace_read(handle, ctypes.cast(buf, ctypes.c_void_p), cap, ctypes.byref(n)), "moe_trace_read")
-    return [list(buf[c * MOE_TRACE_POINTS:(c + 1) * MOE_TRACE_POINTS]) for c in range(n.value)]
+def moe_layer_selection(handle, T, ids, w, stream=None):
+    """Copy the selection the last route / decode / prefill call used into
+    device buffers ids int32 [T][k] and w fp32 [T][k] (enqueued on stream)."""
+    _check(lib().moe_layer_selection(handle, T, _addr(ids), _addr(w), _stream(stream)), "moe_layer_selection")
 
 
 MOE_TRACE_MAX_CTAS = 1024
@@ -461,6 +454,9 @@ class MoELayer:
 
     def decode(self, x, y, y_f32=None, stream=None):
         moe_decode(self.handle, x, y, y_f32, stream)
+
+    def selection(self, T, ids, w, stream=None):
+        moe_layer_selection(self.handle, T, ids, w, stream)
 
     def decode_static_scratch(self, x, y, y_f32=None, stream=None):
         moe_decode_static_scratch(self.handle, x, y, y_f32, stream)

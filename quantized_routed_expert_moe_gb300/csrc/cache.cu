@@ -580,7 +580,7 @@ moe_status cache_set_device(Layer& L, bool on) {
             C.dca.rec_table = (const uint8_t**)L.rec_table;
             C.dca.rb = L.rec_bytes;
             C.dca.slots = S;
-            C.dca.err = fused_error_word(L);
+            C.dca.err = error_word(L);
         }
         // host copies (lookahead fills, table uploads) land first
         MOE_CUDA_TRY(cudaStreamSynchronize(C.copy));
@@ -721,7 +721,7 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
                        (const int32_t*)C.dca.fills, C.dca.src, C.dca.slots_base, (unsigned long long)L.rec_bytes);
         prof_end(L, s);
         if (e != cudaSuccess) return cuda_fail(e, "cache fill launch");
-        e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, jj0 + k, true, s, true);
+        e = launch_experts_decode_sel(L, x, y, y_f32, 0, jj0 + k, true, s, true);
         if (e != cudaSuccess) return cuda_fail(e, "expert launch");
         return MOE_OK;
     }
@@ -741,14 +741,14 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     moe_status st = MOE_OK;
     if (spec) {
-        e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, jj0 + k, true, s);
+        e = launch_experts_decode_sel(L, x, y, y_f32, 0, jj0 + k, true, s);
         if (e != cudaSuccess) return cuda_fail(e, "expert launch");
         st = wait_published(L, C.pub_seq, want);
         if (st != MOE_OK) return st;
         for (int j = 0; j < k; ++j) C.ids_host[j] = ((volatile int32_t*)C.pub_ids)[j];
     } else {
         if (d.n_shared) {
-            e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, 0, 1, false, s);
+            e = launch_experts_decode_sel(L, x, y, y_f32, 0, 1, false, s);
             if (e != cudaSuccess) return cuda_fail(e, "shared expert launch");
         }
         MOE_CUDA_TRY(cudaMemcpyAsync(C.ids_host, L.ids, (size_t)k * 4, cudaMemcpyDeviceToHost, s));
@@ -765,7 +765,7 @@ moe_status cache_decode(Layer& L, const void* x, void* y, float* y_f32, cudaStre
     if (spec && m == 0) return MOE_OK;   // the speculative launch had every expert
     // after a speculative launch that met a miss every slot runs again;
     // otherwise the shared expert's gate/up has run already
-    e = launch_experts_decode_sel(L, x, y, y_f32, L.ids, L.wts, spec ? 0 : jj0, jj0 + k, true, s);
+    e = launch_experts_decode_sel(L, x, y, y_f32, spec ? 0 : jj0, jj0 + k, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "routed expert launch");
     return MOE_OK;
 }

@@ -230,12 +230,16 @@ __device__ __forceinline__ float q16_scale(float max_abs) {
     return __uint_as_float((uint32_t)(f + 127) << 23);
 }
 
-// Quantise one run v[0..7] with scale sc into the staged uint4 layout.
+// Quantise one run v[0..7] with scale sc into the staged uint4 layout. The
+// rounding to the nearest integer (ties to even) is one fma with 1.5 * 2^23:
+// the sum lies in [2^23, 2^24), where the unit in the last place is 1, so the
+// fma's rounding is the rounding to an integer, and the integer is the low
+// bits of the sum (sc is a power of two, so v * sc is exact).
 __device__ __forceinline__ uint4 quant_run(const float* v, float sc) {
     uint32_t he = 0, ho = 0, le = 0, lo = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int q = __float2int_rn(v[i] * sc);       // |q| <= 2^14
+        const int q = __float_as_int(fmaf(v[i], sc, 12582912.0f)) - 0x4B400000;   // |q| <= 2^14
         const int h = (q + 128) >> 8;                  // floor((q + 128) / 256)
         const int l = q - 256 * h;                     // in [-128, 127]
         const uint32_t hb = (uint32_t)(h & 0xFF), lb = (uint32_t)(l & 0xFF);
@@ -268,6 +272,27 @@ __device__ __forceinline__ void stage_q16_run(const float* v, bool valid, int r,
     }
 }
 
+// Token scale: the exponent a with max_abs * 2^a in [1, 2) (0 when max_abs is
+// 0, subnormal or not finite). Activations are staged as x * 2^a, so that the
+// staged values and everything computed from them stay far from both ends of
+// the fp32 range whatever the token's magnitude; results are scaled back by
+// exact powers of two.
+__device__ __forceinline__ int token_exp(float max_abs) {
+    const int ex = (int)((__float_as_uint(max_abs) >> 23) & 0xFF);
+    if (ex == 0 || ex == 0xFF) return 0;
+    return max(-126, min(126, 127 - ex));
+}
+__device__ __forceinline__ float exp2i(int a) { return __uint_as_float((uint32_t)(a + 127) << 23); }   // |a| <= 126
+
+// Prefill operands: the exponent e with max_abs * 2^e in [2^14, 2^15), so that
+// values times 2^e lie well inside the binary16 range while keeping its full
+// precision (0 for a zero, subnormal or non-finite maximum; |e| <= 126).
+__device__ __forceinline__ int fp16_fit_exp(float max_abs) {
+    const int ex = (int)((__float_as_uint(max_abs) >> 23) & 0xFF);
+    if (ex == 0 || ex == 0xFF) return 0;
+    return max(-126, min(126, 141 - ex));
+}
+
 }  // namespace moe
 
 namespace moe {
@@ -284,22 +309,17 @@ __device__ __forceinline__ void ktrace(unsigned long long* tr, int cta, int p) {
 
 namespace moe {
 
-// ---- exact top-k + softmax over the selected logits, one 256-thread CTA --------------
+// ---- exact top-k + softmax over the selected keys, one CTA ----------------------------
 //
-// Selection is the first k of the experts ordered by (-l_e, e): the largest
-// logit first, the lower index on equal values; NaN logits count as -inf so
-// every round selects a valid expert.
-// The warp's largest (bv, lowest bi among equal bv), in two warp reductions:
-// the key as an unsigned integer of the same order (-0 taken as +0, so that
-// equal floats stay equal), its maximum, then the smallest index holding it.
-// bv is never NaN here; bi is at most INT_MAX.
-__device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
-    const uint32_t u = __float_as_uint(bv + 0.0f);
-    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, key);
-    const uint32_t mi = __reduce_min_sync(0xffffffffu, key == mk ? (uint32_t)bi : 0xffffffffu);
-    bv = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7fffffffu) : ~mk);
-    bi = (int)mi;
+// Selection is the first k of the experts ordered by (-key_e, e): the largest
+// key first, the lower index on equal values; NaN keys count as -inf.
+
+// Order-preserving unsigned image of a key (NaN as -inf, -0 as +0): a > b as
+// floats iff img(a) > img(b), equal floats have equal images.
+__device__ __forceinline__ uint32_t key_img(float v) {
+    if (v != v) v = -INFINITY;
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Selection key of one expert from its logit l and bias b (b = 0 without a
@@ -313,111 +333,53 @@ __device__ __forceinline__ float route_key(float l, float b, RouteMode m, float*
     return sc + b;
 }
 
-// Two stages without block-wide rounds: every warp selects the top k of its
-// contiguous range of experts (k rounds of a warp argmax), then warp 0 selects
-// the top k of the <= 8 * k candidates. The union of the per-range top-k holds
-// the global top-k, so the result is the same selection. E <= 1024, at least
-// 8 warps (warps beyond the eighth only join the barriers).
-// Weights: the softmax over the selected keys, or, when `score` is given
-// (sigmoid scoring), scale * score_j / sum over the selection of score.
-__device__ __forceinline__ void block_topk_softmax(const float* sl, int E, int k, int32_t* ids_out, float* w_out,
-                                                   const float* score = nullptr, float scale = 1.0f) {
-    __shared__ float c_v[8 * MOE_MAX_TOP_K];
-    __shared__ int c_i[8 * MOE_MAX_TOP_K];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int chunk = (E + 8 - 1) / 8;   // <= 128
-    const int e0 = warp * chunk, e1 = min(E, e0 + chunk);
-    float v[4];
-    bool live[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int e = e0 + lane + 32 * m;
-        live[m] = e < e1 && lane + 32 * m < chunk;
-        const float t = live[m] ? sl[e] : -INFINITY;
-        v[m] = (t != t) ? -INFINITY : t;
-    }
-    for (int r = 0; r < k && warp < 8; ++r) {   // warps 8 and up (larger blocks) take no range
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int e = e0 + lane + 32 * m;
-            if (live[m] && (v[m] > bv || (v[m] == bv && e < bi))) { bv = v[m]; bi = e; }
-        }
-        warp_argmax(bv, bi);
-        if (lane == 0) { c_v[warp * MOE_MAX_TOP_K + r] = bv; c_i[warp * MOE_MAX_TOP_K + r] = bi; }
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            if (e0 + lane + 32 * m == bi) live[m] = false;
-    }
+// Top k of the keys sl[0..E) (shared memory) by rank: every thread takes
+// experts e = tid, tid + blockDim, ... and counts the experts that come before
+// e in the order; the expert of rank r < k is selection r. The ranks are a
+// permutation (the index breaks ties), so each r < k is written exactly once.
+// su: shared scratch of round4(E) words. Weights, by thread 0 in selection
+// order: the softmax over the selected keys (the first selected is the
+// maximum), or, when `score` is given (sigmoid scoring), scale * score_j / sum
+// over the selection of score. Ends with the block synchronised; E <= 1024.
+__device__ __forceinline__ void block_topk_rank(const float* sl, uint32_t* su, int E, int k, int32_t* ids_out,
+                                                float* w_out, const float* score = nullptr, float scale = 1.0f) {
+    __shared__ float s_v[MOE_MAX_TOP_K];
+    __shared__ int s_i[MOE_MAX_TOP_K];
+    const int E4 = (E + 3) & ~3;
+    for (int e = threadIdx.x; e < E4; e += blockDim.x) su[e] = e < E ? key_img(sl[e]) : key_img(-INFINITY);
     __syncthreads();
-    if (warp == 0) {
-        const int n = 8 * k;   // candidates, <= 64
-        float cv[2];
-        int ci[2];
-        bool cl[2];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int c = lane + 32 * m;
-            cl[m] = c < n;
-            const int w = c / (cl[m] ? k : 1), rr = c - w * (cl[m] ? k : 1);
-            cv[m] = cl[m] ? c_v[w * MOE_MAX_TOP_K + rr] : -INFINITY;
-            ci[m] = cl[m] ? c_i[w * MOE_MAX_TOP_K + rr] : INT_MAX;
-        }
-        float sel_l[MOE_MAX_TOP_K];
-        int sel_i[MOE_MAX_TOP_K];
-#pragma unroll
-        for (int r = 0; r < MOE_MAX_TOP_K; ++r) {
-            if (r >= k) break;
-            float bv = -INFINITY;
-            int bi = INT_MAX;
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-                if (cl[m] && (cv[m] > bv || (cv[m] == bv && ci[m] < bi))) { bv = cv[m]; bi = ci[m]; }
-            warp_argmax(bv, bi);
-            sel_l[r] = bv;
-            sel_i[r] = bi;
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-                if (cl[m] && ci[m] == bi) cl[m] = false;
-        }
-        if (lane == 0) {
-            // softmax over the selected keys (the first selected is the
-            // maximum), or the selected sigmoid scores renormalised and scaled
-            float ex[MOE_MAX_TOP_K], den = 0.f;
-#pragma unroll
-            for (int r = 0; r < MOE_MAX_TOP_K; ++r)
-                if (r < k) {
-                    ex[r] = score ? score[sel_i[r]] : expf(sel_l[r] - sel_l[0]);
-                    den += ex[r];
-                }
-            const float mul = score ? scale : 1.0f;
-#pragma unroll
-            for (int r = 0; r < MOE_MAX_TOP_K; ++r)
-                if (r < k) { ids_out[r] = sel_i[r]; w_out[r] = ex[r] / den * mul; }
-        }
-    }
-}
-
-
-// Sum the router's partial logits part[s][e] (s < splits <= 8, fixed order),
-// apply the layer's scoring and bias, and select: selection keys into sl[E]
-// and, for sigmoid scoring, the scores into ss[E] (both shared), ids /
-// weights into ids_out / w_out (shared or global). All 256 threads; E <= 1024.
-__device__ __forceinline__ void block_select(const float* part, int splits, int E, const float* bias, int k,
-                                             float* sl, int32_t* ids_out, float* w_out, RouteMode mode,
-                                             float* ss) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        float v[8];
-#pragma unroll
-        for (int s = 0; s < 8; ++s) v[s] = (s < splits) ? __ldcg(part + (size_t)s * E + e) : 0.f;
-        float l = 0.f;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) l += v[s];
-        sl[e] = route_key(l, bias ? __ldg(bias + e) : 0.f, mode, ss + e);
+        const uint32_t ue = su[e];
+        int rank = 0;
+        for (int j0 = 0; j0 < E4; j0 += 4) {
+            const uint4 q = *reinterpret_cast<const uint4*>(su + j0);
+            // (j < e and u_j >= u_e) or (j > e and u_j > u_e); padding never
+            // counts (it equals -inf and lies past every real index)
+            rank += (q.x > ue) | ((q.x == ue) & (j0 + 0 < e));
+            rank += (q.y > ue) | ((q.y == ue) & (j0 + 1 < e));
+            rank += (q.z > ue) | ((q.z == ue) & (j0 + 2 < e));
+            rank += (q.w > ue) | ((q.w == ue) & (j0 + 3 < e));
+        }
+        if (rank < k) {
+            const float v = sl[e];
+            s_v[rank] = (v != v) ? -INFINITY : v;
+            s_i[rank] = e;
+        }
     }
     __syncthreads();
-    block_topk_softmax(sl, E, k, ids_out, w_out, mode.sigmoid ? ss : nullptr, mode.scale);
+    if (threadIdx.x == 0) {
+        float ex[MOE_MAX_TOP_K], den = 0.f;
+#pragma unroll
+        for (int r = 0; r < MOE_MAX_TOP_K; ++r)
+            if (r < k) {
+                ex[r] = score ? score[s_i[r]] : expf(s_v[r] - s_v[0]);
+                den += ex[r];
+            }
+        const float mul = score ? scale : 1.0f;
+#pragma unroll
+        for (int r = 0; r < MOE_MAX_TOP_K; ++r)
+            if (r < k) { ids_out[r] = s_i[r]; w_out[r] = ex[r] / den * mul; }
+    }
     __syncthreads();
 }
 

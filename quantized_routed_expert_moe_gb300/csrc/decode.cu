@@ -1,18 +1,31 @@
 // Three-kernel decode, expert part: gate/up dequant-GEMV with SwiGLU, then
 // down dequant-GEMV with the weighted combine.
 //
-// The kernels are chained with programmatic dependent launch:
-//   router   -- selects the experts (router.cu);
-//   gate/up  -- starts early and stages the activations, waits for the router,
-//               then computes the shared and the routed experts;
-//   down     -- starts early: prefetches its weight rows into L2 while gate/up
-//               finishes, waits for gate/up, then stages the SwiGLU outputs
-//               and combines.
-// Both expert kernels are persistent grids of many warps; each warp issues all
-// of a row's weight loads (128-bit, streaming) before it computes, so enough
-// bytes are in flight to run at the memory roofline. The 4-bit codes are
-// multiplied with 16-bit fixed-point activations by integer dp4a (common.cuh),
-// about one instruction per weight.
+// The kernels are chained with programmatic dependent launch (PDL):
+//   router   -- the token's logits and, in its last block, the top-k selection
+//               and routing weights (router.cu), then a ready flag;
+//   gate/up  -- starts while the router runs: stages the activations and
+//               computes the shared expert's rows, which do not depend on the
+//               routing; waits (bounded) for the ready flag rather than for the
+//               router grid to retire, then computes the routed experts' rows.
+//               Row pairs are spread over every warp of the grid, one pair per
+//               warp at a time. The warp that completes a half-group of 32
+//               SwiGLU outputs (a counter per half-group) quantises it into the
+//               down kernel's staged form, so nothing is quantised twice and no
+//               CTA waits for another;
+//   down     -- starts as gate/up CTAs retire: computes the shared expert's
+//               output rows as soon as its half-groups are all staged (a
+//               counter), then waits for gate/up and computes the routed
+//               experts' rows and the weighted combine.
+// Each warp issues all of a row's weight loads (128-bit, streaming) before it
+// computes. The 4-bit codes are multiplied with 16-bit fixed-point activations
+// by integer dp4a (common.cuh).
+//
+// Scaling: the token's activations are staged as x * 2^a, with a chosen so that
+// max |x| * 2^a lies in [1, 2). The dot products then come out times 2^a, the
+// SwiGLU outputs times 2^2a, and the combine multiplies by 2^-2a: exact powers
+// of two, so tokens of any magnitude keep fp32's relative precision
+// throughout (no overflow of large activations, no flush of tiny ones).
 //
 // Gated experts, shared expert, combine: Inferno README "Model"; TurboFieldfare
 // article, "token generation"; weight format: same article, "execution
@@ -25,36 +38,65 @@ namespace moe {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kGuBlock = 6;      // half-groups per lane whose loads are in flight together (gate/up)
-constexpr int kDownRows = 4;     // output rows per down work item (share the staged activations)
-constexpr int kDownMaxRows = 96; // output rows one CTA owns in the down kernel
+constexpr int kGuBlock = 6;           // half-groups per lane whose loads are in flight together (gate/up)
+constexpr int kDownRows = 4;          // output rows per down work item (share the staged activations)
+constexpr int kDownMaxRows = 96;      // output rows one CTA owns in the down kernel
+constexpr uint64_t kWaitNs = 200000000ull;   // bounded device waits: 0.2 s
+constexpr int kHCopies = kDecodeHCopies;   // replicas of the staged SwiGLU outputs: the down CTAs' reads spread over L2
 
-// Stage a vector of K activations (global, bf16 or fp32; `cg` reads bypass L1)
-// into 16-bit fixed-point runs xq[4][K/32] with per-half-group inverse scale and
-// sum. Block-wide, warp-uniform trip counts.
-__device__ void stage_vector_q16(const void* x, int x_bf16, bool cg, int K, uint4* xq, float* inv, float* X) {
+__device__ __forceinline__ void load_run(const void* x, int x_bf16, int r, float (&v)[8]) {
+    if (x_bf16) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(x) + r);
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w4[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(x) + 2 * r;
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+// max |x_i| over K activations, every thread of the block gets it (NaN ignored)
+__device__ float block_absmax(const void* x, int x_bf16, int K, float* s_red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float m = 0.f;
+    for (int r = threadIdx.x; r < K / 8; r += blockDim.x) {
+        float v[8];
+        load_run(x, x_bf16, r, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    float r = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, s_red[w]);
+    __syncthreads();
+    return r;
+}
+
+// Stage K activations times xs (a power of two) into 16-bit fixed-point runs
+// xq[4][K/32] with per-half-group inverse scale and sum. Block-wide,
+// warp-uniform trip counts.
+__device__ void stage_vector_q16(const void* x, int x_bf16, int K, float xs, uint4* xq, float* inv, float* X) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrun = K / 8, KG = K / 32;
     for (int rb = warp * 32; rb < ((nrun + 31) / 32) * 32; rb += blockDim.x) {
         const int r = rb + lane;
         const bool valid = r < nrun;
         float v[8];
-        if (!valid) {
+        if (valid) {
+            load_run(x, x_bf16, r, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] *= xs;
+        } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = 0.f;
-        } else if (x_bf16) {
-            const uint4 q = __ldg(reinterpret_cast<const uint4*>(x) + r);
-            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[2 * i] = __uint_as_float(w4[i] << 16);
-                v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-            }
-        } else {
-            const float4* p = reinterpret_cast<const float4*>(x) + 2 * r;
-            const float4 a = cg ? __ldcg(p) : __ldg(p);
-            const float4 b = cg ? __ldcg(p + 1) : __ldg(p + 1);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
         }
         stage_q16_run(v, valid, r, KG, xq, inv, X);
     }
@@ -64,28 +106,9 @@ __device__ void stage_vector_q16(const void* x, int x_bf16, bool cg, int K, uint
 // gate/up + SwiGLU
 // ---------------------------------------------------------------------------
 //
-// h[j][i] = silu(gate_i . x) * (up_i . x) for slot j (routed slots 0..k-1 in
-// selection order, the shared expert at slot k). Rows are taken in "row order":
-// the shared expert's rows first, then the routed slots, i ascending; CTA c owns
-// rows [c R, (c + 1) R) of that order (R a multiple of 32), one or two
-// contiguous runs of (gate row i, up row i) pairs in the weight records.
-//
-// One warp per row pair at a time: each lane issues all of its 128-bit loads of
-// both rows (half-groups l, l + 32, ...) before it computes, so that HBM sees
-// many independent requests (a burst of plain loads reaches the copy roofline;
-// bulk copies through shared memory do not, for bursts this short, and bulk L2
-// prefetches of the next pairs measured slower than none). The codes are multiplied with
-// the 16-bit fixed-point activations by dp4a. The CTA ends by quantising its
-// SwiGLU outputs into the down kernel's staged form, which the down kernel
-// copies as it is.
-
-constexpr int kGuThreads = 256;
-constexpr int kGuWarps = kGuThreads / 32;
-
-// The q16 SwiGLU output block (global, and the down kernel's shared-memory
-// copy of it) for ns slots in row order: runs hq[ns][4][I/32] (uint4), then the
-// inverse scales inv[ns][I/32], then the half-group sums X[ns][I/32].
-__host__ __device__ inline size_t hq_block_bytes(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
+// h[j][i] = silu(gate_i . x) * (up_i . x) for row-order slot j: the shared
+// expert first (when there is one), then the routed slots in selection order.
+// The kernel writes h * 2^2a in fp32, [slot][I].
 
 // expert (record index) of row-order slot jj
 __device__ __forceinline__ int row_slot_expert(int jj, int k, int E, int n_shared, const int32_t* s_ids) {
@@ -152,349 +175,367 @@ __device__ __forceinline__ void group2_dot_gu(const uint4 cg, const uint4 cu, ui
     acc_u = fmaf(su.x, (float)(uh0 * 256 + ul0) * ia + (float)(uh1 * 256 + ul1) * ib, fmaf(su.y, xs, acc_u));
 }
 
-template <int BITS, int NQ = 1>
-__global__ void __launch_bounds__(kGuThreads, 2) k_gateup(const uint8_t* const* __restrict__ rec_tab,
-                                                         const float* __restrict__ part, int splits,
-                                                         const float* __restrict__ bias, int k, int E, int n_shared,
-                                                         const void* __restrict__ x, int x_bf16, int H, int I,
-                                                         size_t rbH, int R, void* __restrict__ hout, int copies,
-                                                         int32_t* __restrict__ ids_out, float* __restrict__ wts_out,
-                                                         float* __restrict__ logits_out,
-                                                         const int32_t* __restrict__ sel_ids, int jj0, int jj1,
-                                                         RouteMode mode, const uint8_t* pf, size_t pf_bytes,
-                                                         unsigned long long* __restrict__ tr) {
+// Dot products of NQ row pairs (gate row at g[q], up row at g[q] + rbH) with
+// the staged activations; every lane gets the warp sums gv[q], uv[q]. A lane
+// issues all loads of its half-groups (4-bit: kGuBlock / NQ at a time; 2-bit:
+// whole groups, kGuBlock / 2 at a time) of every row before it computes.
+template <int BITS, int NQ>
+__device__ __forceinline__ void pair_dots(const uint8_t* const (&g)[NQ], const bool (&live)[NQ], int H, size_t rbH,
+                                          const uint4* xq, const float* Iv, const float* Xx, uint64_t pol,
+                                          float (&gv)[NQ], float (&uv)[NQ]) {
+    const int lane = threadIdx.x & 31, HG = H / 32;
+    float acc_g[NQ], acc_u[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) acc_g[q] = acc_u[q] = 0.f;
+    if constexpr (BITS == 2) {
+        constexpr int B2 = kGuBlock / 2;
+        const int GH = HG / 2, M2 = (GH + 31) / 32;
+        for (int m0 = 0; m0 < M2; m0 += B2) {
+            uint4 cg[NQ][B2], cu[NQ][B2];
+            uint32_t mg[NQ][B2], mu[NQ][B2];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                for (int mm = 0; mm < B2; ++mm) {
+                    const int G = lane + 32 * (m0 + mm);
+                    if (live[q] && m0 + mm < M2 && G < GH) {
+                        cg[q][mm] = ldg_stream_hint(g[q] + 16 * G, pol);
+                        cu[q][mm] = ldg_stream_hint(g[q] + rbH + 16 * G, pol);
+                        mg[q][mm] = ldg_u32_hint(g[q] + H / 4 + 4 * G, pol);
+                        mu[q][mm] = ldg_u32_hint(g[q] + rbH + H / 4 + 4 * G, pol);
+                    }
+                }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                for (int mm = 0; mm < B2; ++mm) {
+                    const int G = lane + 32 * (m0 + mm);
+                    if (live[q] && m0 + mm < M2 && G < GH)
+                        group2_dot_gu(cg[q][mm], cu[q][mm], mg[q][mm], mu[q][mm], xq, HG, G, Iv, Xx, acc_g[q],
+                                      acc_u[q]);
+                }
+        }
+    } else {
+        constexpr int BQ = kGuBlock / NQ;
+        const int M = (HG + 31) / 32;
+        for (int m0 = 0; m0 < M; m0 += BQ) {
+            uint4 cg[NQ][BQ], cu[NQ][BQ];
+            uint32_t mg[NQ][BQ], mu[NQ][BQ];
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                for (int mm = 0; mm < BQ; ++mm) {
+                    const int hg = lane + 32 * (m0 + mm);
+                    if (live[q] && m0 + mm < M && hg < HG) {
+                        const uint8_t* u = g[q] + rbH;
+                        cg[q][mm] = ldg_stream_hint(g[q] + 16 * hg, pol);
+                        cu[q][mm] = ldg_stream_hint(u + 16 * hg, pol);
+                        mg[q][mm] = ldg_u32_hint(g[q] + H / 2 + 4 * (hg >> 1), pol);
+                        mu[q][mm] = ldg_u32_hint(u + H / 2 + 4 * (hg >> 1), pol);
+                    }
+                }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+                for (int mm = 0; mm < BQ; ++mm) {
+                    const int hg = lane + 32 * (m0 + mm);
+                    if (live[q] && m0 + mm < M && hg < HG) {
+                        int gh = 0, gl = 0, uh = 0, ul = 0;
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const uint4 xs = xq[wi * HG + hg];
+                            word_dp4a(u4w(cg[q][mm], wi), xs, gh, gl);
+                            word_dp4a(u4w(cu[q][mm], wi), xs, uh, ul);
+                        }
+                        const float iv = Iv[hg], xs = Xx[hg];
+                        const float2 sg = meta_to_f2(mg[q][mm]), su = meta_to_f2(mu[q][mm]);
+                        acc_g[q] = fmaf(sg.x, (float)(gh * 256 + gl) * iv, fmaf(sg.y, xs, acc_g[q]));
+                        acc_u[q] = fmaf(su.x, (float)(uh * 256 + ul) * iv, fmaf(su.y, xs, acc_u[q]));
+                    }
+                }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        gv[q] = warp_sum(acc_g[q]);
+        uv[q] = warp_sum(acc_u[q]);
+    }
+}
+
+// Row pairs p0, p0 + step, ... (< pend) of one phase, NQ at a time; ptr(p)
+// gives the gate row of pair p; done(p, g, u, live) is called by every lane
+// with the (scaled) dot products of pair p.
+template <int BITS, int NQ, typename PtrF, typename DoneF>
+__device__ __forceinline__ void gu_phase(int p0, int step, int pend, PtrF ptr, DoneF done, int H, size_t rbH,
+                                         const uint4* xq, const float* Iv, const float* Xx, uint64_t pol) {
+    for (int p = p0; p < pend; p += NQ * step) {
+        const uint8_t* g[NQ];
+        bool live[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int pq = p + q * step;
+            live[q] = pq < pend;
+            g[q] = ptr(live[q] ? pq : p);
+        }
+        float gv[NQ], uv[NQ];
+        pair_dots<BITS, NQ>(g, live, H, rbH, xq, Iv, Xx, pol, gv, uv);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) done(p + q * step, gv[q], uv[q], live[q]);
+    }
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Wait until *ctr >= target (acquire), for at most limit_ns of GPU time.
+__device__ __forceinline__ bool wait_count(const unsigned* ctr, unsigned target, uint64_t limit_ns) {
+    const uint64_t t0 = bw::gtimer();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((i & 15) == 15 && bw::gtimer() - t0 > limit_ns) return false;
+        __nanosleep(64);
+    }
+    return false;
+}
+
+// The staged SwiGLU outputs of ns slots (one replica): runs hq[ns][4][I/32]
+// (uint4), then the inverse scales inv[ns][I/32], then the half-group sums
+// X[ns][I/32] -- the form stage_q16_run writes, which the down kernel's dot
+// products read.
+__host__ __device__ inline size_t hq_block_bytes(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
+
+// A whole warp quantises half-group hg of slot jj (32 SwiGLU outputs at hrow,
+// fp32, already written) into every replica of the staged block.
+__device__ __forceinline__ void stage_half_group(const float* hrow, int jj, int hg, int ns, int IG, uint8_t* hq_base,
+                                                 size_t blk, int copies) {
+    const int lane = threadIdx.x & 31;
+    const float val = __ldcg(hrow + lane);
+    float v[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) v[m] = __shfl_sync(0xffffffffu, val, ((lane & 3) << 3) | m);   // run lane & 3
+    float mx = 0.f, sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { mx = fmaxf(mx, fabsf(v[i])); sum += v[i]; }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    const float sc = q16_scale(mx);
+    const uint4 q = quant_run(v, sc);
+    if (lane < 4) {   // lanes 0..3 hold runs 0..3
+        for (int c = 0; c < copies; ++c) {
+            uint4* hq = reinterpret_cast<uint4*>(hq_base + (size_t)c * blk);
+            float* hinv = reinterpret_cast<float*>(hq + (size_t)ns * 4 * IG);
+            float* hX = hinv + ns * IG;
+            hq[(size_t)jj * 4 * IG + lane * IG + hg] = q;
+            if (lane == 0) { hinv[jj * IG + hg] = 1.0f / sc; hX[jj * IG + hg] = sum; }
+        }
+    }
+}
+
+struct GuArgs {
+    const uint8_t* const* rec_tab;   // [E + 1] expert records (index E: the shared expert)
+    int k, E, n_shared;
+    const void* x;
+    int x_bf16;
+    int H, I;
+    size_t rbH;                      // bytes of one gate/up row record
+    const int32_t* ids;              // the token's selection [k] (the router's, or a streamed layer's)
+    const unsigned* ids_ready;       // nullable: set by the router's selecting block once ids are written
+    float* h;                        // [ns][I] SwiGLU outputs times 2^2a, row-order slots
+    unsigned* hg_cnt;                // [ns][I/32] rows done per half-group; the warp that completes one
+                                     // quantises it and clears the count
+    uint8_t* hq;                     // copies x staged blocks (hq_block_bytes)
+    int copies;
+    int* scale_out;                  // the token exponent a (CTA 0 writes it)
+    unsigned* shared_done;           // nullable: staged half-groups of the shared expert
+    int jj0, jj1;                    // row-order slots this launch computes
+    const uint8_t* pf;               // next layer's router weights to warm into L2 (nullable)
+    size_t pf_bytes;
+    unsigned* err;
+    unsigned long long* tr;
+    int stall_shared;                // test hook: do not count the shared expert's staged half-groups
+};
+
+template <int BITS, int NQ>
+__global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     extern __shared__ uint4 smq[];
-    __shared__ float s_logit[1024];
-    __shared__ float s_score[1024];
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
-    __shared__ float s_wts[MOE_MAX_TOP_K];
-    const int HG = H / 32, IG = I / 32, ns = k + n_shared;
+    __shared__ float s_red[kWarps];
+    __shared__ int s_skip, s_ok;
+    const int H = a.H, I = a.I, HG = H / 32, IG = I / 32, ns = a.k + a.n_shared;
     uint4* xq = smq;                                                   // [4][HG]
     float* Iv = reinterpret_cast<float*>(smq + 4 * HG);                // [HG] 2^-f
     float* Xx = Iv + HG;                                               // [HG]
-    float* hbuf = Xx + HG;                                             // [R]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ktrace(tr, blockIdx.x, 0);
-    if (pf && threadIdx.x == 0) {
+    ktrace(a.tr, blockIdx.x, 0);
+    if (a.pf && threadIdx.x == 0) {
         // the next layer's router weights into L2 (moe_layer_set_next): this
-        // CTA's share, in 16-byte multiples, no later than 64 KB a request
-        const size_t per = (pf_bytes / gridDim.x + 15) / 16 * 16;
-        const size_t b0 = per * blockIdx.x, b1 = min(pf_bytes, b0 + per);
-        for (size_t o = b0; o < b1; o += 65536)
-            prefetch_l2(pf + o, (uint32_t)min((size_t)65536, b1 - o));
+        // CTA's share, in 16-byte multiples, no more than 64 KB a request
+        const size_t per = (a.pf_bytes / gridDim.x + 15) / 16 * 16;
+        const size_t b0 = per * blockIdx.x, b1 = min(a.pf_bytes, b0 + per);
+        for (size_t o = b0; o < b1; o += 65536) prefetch_l2(a.pf + o, (uint32_t)min((size_t)65536, b1 - o));
     }
-    stage_vector_q16(x, x_bf16, false, H, xq, Iv, Xx);
+    // the token's scale and staged activations (the router waited for the
+    // producer of x before this kernel could start, so x is final)
+    const int ta = token_exp(block_absmax(a.x, a.x_bf16, H, s_red));
+    stage_vector_q16(a.x, a.x_bf16, H, exp2i(ta), xq, Iv, Xx);
     __syncthreads();
-    ktrace(tr, blockIdx.x, 2);
-
-    // no weight traffic before the selection is known
-    pdl_wait();
-    pdl_trigger();
-    ktrace(tr, blockIdx.x, 1);
-    if (sel_ids) {
-        // the selection was made earlier (streamed layers: the host staged
-        // those experts first)
-        if (threadIdx.x < k) s_ids[threadIdx.x] = sel_ids[threadIdx.x];
-        __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.scale_out) *a.scale_out = ta;   // for the down kernel
+    const float inv_a = exp2i(-ta);
+    const uint64_t pol = policy_evict_first();
+    const bool has_shared = a.n_shared && a.jj0 == 0;
+    const int jr0 = has_shared ? 1 : a.jj0;   // first routed row-order slot
+    const size_t blk = hq_block_bytes(ns, I);
+    // pair (slot jj, row i) done: lane 0 writes h * 2^2a = (g 2^a)(u 2^a) sigmoid(g)
+    // and counts the row in its half-group; the warp that counts the 32nd row
+    // quantises the half-group
+    auto done = [&](int jj, int i, float gs, float us, bool live) {
+        unsigned old = 0;
+        if (live && lane == 0) {
+            const float sg = 1.0f / (1.0f + expf(-(gs * inv_a)));
+            a.h[(size_t)jj * I + i] = gs * us * sg;
+            old = atom_add_acq_rel(a.hg_cnt + jj * IG + (i >> 5), 1u);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (live && old == 31u) {   // warp-uniform
+            __syncwarp();
+            __threadfence();
+            const int hg = i >> 5;
+            stage_half_group(a.h + (size_t)jj * I + 32 * hg, jj, hg, ns, IG, a.hq, blk, a.copies);
+            __syncwarp();
+            if (lane == 0) {
+                a.hg_cnt[jj * IG + hg] = 0u;   // for the next token (its gate/up starts after this token's down)
+                if (jj == 0 && has_shared && a.shared_done && !a.stall_shared) {
+                    __threadfence();
+                    atomicAdd(a.shared_done, 1u);
+                }
+            }
+        }
+    };
+    // the shared expert's rows need no routing: they overlap the router
+    if (has_shared) {
+        const uint8_t* rec = a.rec_tab[a.E];   // fixed for the layer's lifetime
+        gu_phase<BITS, NQ>(
+            blockIdx.x * kWarps + warp, gridDim.x * kWarps, I, [&](int p) { return rec + (size_t)2 * p * a.rbH; },
+            [&](int p, float gs, float us, bool live) { done(0, p, gs, us, live); }, H, a.rbH, xq, Iv, Xx, pol);
+    }
+    ktrace(a.tr, blockIdx.x, 1);
+    // the selection: the router's selecting block raises the ready flag as
+    // soon as the ids are written (no wait for the router grid to retire); a
+    // wait that runs out falls back to the ordinary dependency wait
+    if (threadIdx.x == 0) {
+        int ok = 0;
+        if (a.ids_ready) {
+            ok = wait_count(a.ids_ready, 1u, kWaitNs) ? 1 : 0;
+            if (!ok) atomicOr(a.err, 1u << 28);
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) pdl_wait();   // the router (or, streamed, the staging of the records) is complete
+    if (threadIdx.x < a.k) s_ids[threadIdx.x] = __ldcg(a.ids + threadIdx.x);
+    __syncthreads();
+    pdl_trigger();   // the down kernel may launch: it starts with the shared expert's rows
+    ktrace(a.tr, blockIdx.x, 2);
+    if (a.jj1 > jr0) {
         // streamed layers: a launch made before the host has staged this
         // token's experts finds a missing expert's record null and does
         // nothing (the host launches again once every expert is resident)
-        __shared__ int s_skip;
         if (threadIdx.x == 0) {
             int bad = 0;
-            for (int jj = jj0; jj < jj1; ++jj) bad |= rec_tab[row_slot_expert(jj, k, E, n_shared, s_ids)] == nullptr;
+            for (int jj = jr0; jj < a.jj1; ++jj) bad |= a.rec_tab[row_slot_expert(jj, a.k, a.E, a.n_shared, s_ids)] == nullptr;
             s_skip = bad;
         }
         __syncthreads();
-        if (s_skip) return;
-    } else {
-        // every CTA reduces the router's partial logits and selects (same result
-        // everywhere); no CTA has to wait for a single selecting CTA
-        block_select(part, splits, E, bias, k, s_logit, s_ids, s_wts, mode, s_score);
-        if (blockIdx.x == 0) {   // publish the selection (read by the host and by later calls)
-            for (int e = threadIdx.x; e < E; e += blockDim.x) logits_out[e] = s_logit[e];
-            if (threadIdx.x < k) { ids_out[threadIdx.x] = s_ids[threadIdx.x]; wts_out[threadIdx.x] = s_wts[threadIdx.x]; }
-        }
+        if (!s_skip)
+            gu_phase<BITS, NQ>(
+                blockIdx.x * kWarps + warp, gridDim.x * kWarps, (a.jj1 - jr0) * I,
+                [&](int p) {
+                    const int jj = jr0 + p / I, i = p - (p / I) * I;
+                    return a.rec_tab[row_slot_expert(jj, a.k, a.E, a.n_shared, s_ids)] + (size_t)2 * i * a.rbH;
+                },
+                [&](int p, float gs, float us, bool live) {
+                    const int jj = jr0 + p / I;
+                    done(jj, p - (jj - jr0) * I, gs, us, live);
+                },
+                H, a.rbH, xq, Iv, Xx, pol);
     }
-
-    const int NR = (jj1 - jj0) * I;
-    const int rbeg = blockIdx.x * R;
-    const int np = max(0, min(R, NR - rbeg));   // row pairs of this CTA
-    const uint64_t pol = policy_evict_first();
-    auto pair_ptr = [&](int p) {
-        const int r = jj0 * I + rbeg + p;
-        const int jj = r / I, i = r - jj * I;
-        return rec_tab[row_slot_expert(jj, k, E, n_shared, s_ids)] + (size_t)2 * i * rbH;
-    };
-    if constexpr (BITS == 2) {
-        // a lane takes whole groups of 64 codes (16 bytes each); a warp works
-        // on two row pairs at a time, so that it keeps as many bytes in flight
-        // as with 4-bit codes
-        constexpr int B2 = kGuBlock / 2;
-        const int GH = HG / 2, M2 = (GH + 31) / 32;
-        for (int p0 = warp; p0 < np; p0 += 2 * kGuWarps) {
-            const uint8_t* g[2];
-            bool live[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int p = p0 + q * kGuWarps;
-                live[q] = p < np;
-                g[q] = pair_ptr(live[q] ? p : p0);
-            }
-            float acc_g[2] = {0.f, 0.f}, acc_u[2] = {0.f, 0.f};
-            for (int m0 = 0; m0 < M2; m0 += B2) {
-                uint4 cg[2][B2], cu[2][B2];
-                uint32_t mg[2][B2], mu[2][B2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-#pragma unroll
-                    for (int mm = 0; mm < B2; ++mm) {
-                        const int G = lane + 32 * (m0 + mm);
-                        if (live[q] && m0 + mm < M2 && G < GH) {
-                            cg[q][mm] = ldg_stream_hint(g[q] + 16 * G, pol);
-                            cu[q][mm] = ldg_stream_hint(g[q] + rbH + 16 * G, pol);
-                            mg[q][mm] = ldg_u32_hint(g[q] + H / 4 + 4 * G, pol);
-                            mu[q][mm] = ldg_u32_hint(g[q] + rbH + H / 4 + 4 * G, pol);
-                        }
-                    }
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-#pragma unroll
-                    for (int mm = 0; mm < B2; ++mm) {
-                        const int G = lane + 32 * (m0 + mm);
-                        if (live[q] && m0 + mm < M2 && G < GH)
-                            group2_dot_gu(cg[q][mm], cu[q][mm], mg[q][mm], mu[q][mm], xq, HG, G, Iv, Xx, acc_g[q],
-                                          acc_u[q]);
-                    }
-            }
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float gv = warp_sum(acc_g[q]);
-                const float uv = warp_sum(acc_u[q]);
-                if (live[q] && lane == 0) hbuf[p0 + q * kGuWarps] = silu_f(gv) * uv;
-            }
-        }
-    } else {
-        // 4-bit codes. A warp works on NQ row pairs at a time, and each lane
-        // issues all loads of its kGuBlock / NQ half-groups of every row
-        // before it computes. Short rows (at most kGuBlock / 2 half-groups
-        // per lane) take two pairs at a time (NQ = 2), so that as many bytes
-        // are in flight per warp as with long rows.
-        {
-            constexpr int BQ = kGuBlock / NQ;
-            const int M = (HG + 31) / 32;
-            for (int p0 = warp; p0 < np; p0 += NQ * kGuWarps) {
-                const uint8_t* g[NQ];
-                bool live[NQ];
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const int p = p0 + q * kGuWarps;
-                    live[q] = p < np;
-                    g[q] = pair_ptr(live[q] ? p : p0);
-                }
-                float acc_g[NQ], acc_u[NQ];
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) acc_g[q] = acc_u[q] = 0.f;
-                for (int m0 = 0; m0 < M; m0 += BQ) {
-                    uint4 cg[NQ][BQ], cu[NQ][BQ];
-                    uint32_t mg[NQ][BQ], mu[NQ][BQ];
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q)
-#pragma unroll
-                        for (int mm = 0; mm < BQ; ++mm) {
-                            const int hg = lane + 32 * (m0 + mm);
-                            if (live[q] && m0 + mm < M && hg < HG) {
-                                const uint8_t* u = g[q] + rbH;
-                                cg[q][mm] = ldg_stream_hint(g[q] + 16 * hg, pol);
-                                cu[q][mm] = ldg_stream_hint(u + 16 * hg, pol);
-                                mg[q][mm] = ldg_u32_hint(g[q] + H / 2 + 4 * (hg >> 1), pol);
-                                mu[q][mm] = ldg_u32_hint(u + H / 2 + 4 * (hg >> 1), pol);
-                            }
-                        }
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q)
-#pragma unroll
-                        for (int mm = 0; mm < BQ; ++mm) {
-                            const int hg = lane + 32 * (m0 + mm);
-                            if (live[q] && m0 + mm < M && hg < HG) {
-                                int gh = 0, gl = 0, uh = 0, ul = 0;
-#pragma unroll
-                                for (int wi = 0; wi < 4; ++wi) {
-                                    const uint4 xs = xq[wi * HG + hg];
-                                    word_dp4a(u4w(cg[q][mm], wi), xs, gh, gl);
-                                    word_dp4a(u4w(cu[q][mm], wi), xs, uh, ul);
-                                }
-                                const float iv = Iv[hg], xs = Xx[hg];
-                                const float2 sg = meta_to_f2(mg[q][mm]), su = meta_to_f2(mu[q][mm]);
-                                acc_g[q] = fmaf(sg.x, (float)(gh * 256 + gl) * iv, fmaf(sg.y, xs, acc_g[q]));
-                                acc_u[q] = fmaf(su.x, (float)(uh * 256 + ul) * iv, fmaf(su.y, xs, acc_u[q]));
-                            }
-                        }
-                }
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const float gv = warp_sum(acc_g[q]);
-                    const float uv = warp_sum(acc_u[q]);
-                    if (live[q] && lane == 0) hbuf[p0 + q * kGuWarps] = silu_f(gv) * uv;
-                }
-            }
-        }
-    }   // BITS == 4
-    __syncthreads();
-    ktrace(tr, blockIdx.x, 3);
-    // the CTA's SwiGLU outputs in the down kernel's staged form; a half-group
-    // (32 rows) never straddles CTAs or slots
-    // (written `copies` times: the down kernel's CTAs all read the whole block,
-    // and spreading them over several copies spreads the reads over L2)
-    const int nrun = np / 8;
-    const size_t blk = hq_block_bytes(ns, I);
-    for (int rb = warp * 32; rb < ((nrun + 31) / 32) * 32; rb += blockDim.x) {
-        const int rr = rb + lane;
-        const bool valid = rr < nrun;
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = valid ? hbuf[8 * rr + i] : 0.f;
-        const int r0 = jj0 * I + rbeg + 8 * (valid ? rr : 0);
-        const int jj = r0 / I, run = (r0 - jj * I) / 8;
-        // quantise once (the run, its half-group's scale and sum) ...
-        float m = 0.f, sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { m = fmaxf(m, fabsf(v[i])); sum += v[i]; }
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        const float sc = q16_scale(m);
-        const uint4 qv = quant_run(v, sc);
-        // ... and store it into every replica
-        if (valid) {
-            const int hg = run >> 2, wi = run & 3;
-            for (int c = 0; c < copies; ++c) {
-                uint8_t* base = static_cast<uint8_t*>(hout) + (size_t)c * blk;
-                uint4* hq = reinterpret_cast<uint4*>(base);
-                float* hinv = reinterpret_cast<float*>(hq + (size_t)ns * 4 * IG);
-                float* hX = hinv + ns * IG;
-                hq[(size_t)jj * 4 * IG + wi * IG + hg] = qv;
-                if (wi == 0) { hinv[jj * IG + hg] = 1.0f / sc; hX[jj * IG + hg] = sum; }
-            }
-        }
-    }
-    // the down kernel reads the block with a bulk copy (the async proxy)
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+    pdl_wait();   // this grid's completion then implies the router's (returns at once by now)
+    ktrace(a.tr, blockIdx.x, 3);
 }
 
 // ---------------------------------------------------------------------------
 // down + combine
 // ---------------------------------------------------------------------------
 //
-// CTA c owns output rows [c*H/G, (c+1)*H/G). Work items are (4 rows, slot);
-// a warp computes the 4 rows' dot products with that slot's SwiGLU output
-// (staged once per CTA in 16-bit fixed point per half-group), keeping the
-// results per (slot, row); the rows are then combined in a fixed order:
-// shared expert first (weight 1), then the routed slots in selection order.
-template <int BITS, int J = 1>
-__global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restrict__ rec_tab,
-                                                   const float* __restrict__ part, int splits,
-                                                   const float* __restrict__ bias,
-                                                   int k, int E, int n_shared, int H, int I,
-                                                   const void* __restrict__ hblk, int copies, void* __restrict__ y,
-                                                   int y_bf16,
-                                                   float* __restrict__ y32, size_t rbI, size_t gu_block,
-                                                   const int32_t* __restrict__ sel_ids,
-                                                   const float* __restrict__ sel_wts, unsigned* __restrict__ err,
-                                                   unsigned long long* __restrict__ tr) {
-    extern __shared__ uint4 smh[];
-    ktrace(tr, blockIdx.x, 0);
-    const int IG = I / 32, ns = k + n_shared;
-    uint4* hq = smh;                                                     // [ns][4][IG]
-    float* Iv = reinterpret_cast<float*>(hq + (size_t)ns * 4 * IG);     // [ns][IG]
-    float* Xh = Iv + ns * IG;                                            // [ns][IG]
-    float* ypart = Xh + ns * IG;                                         // [ns][kDownMaxRows]
-    __shared__ const uint8_t* s_rows[MOE_MAX_TOP_K + 1];
-    __shared__ float s_w[MOE_MAX_TOP_K + 1];
-    __shared__ __align__(8) uint64_t s_hbar;
-    __shared__ int s_abort, s_skip;
-    if (threadIdx.x == 0) {
-        bw::mbar_init(bw::saddr(&s_hbar), 1);
-        s_abort = 0;
-        s_skip = 0;
-        bw::mbar_fence_init();
+// CTA c owns output rows [c*H/G, (c+1)*H/G). The staged SwiGLU outputs (16-bit
+// fixed point per half-group, written by gate/up) are loaded once per CTA.
+// Work items are (4 rows, slot); a warp computes the 4 rows' dot products with
+// that slot's outputs, keeping the results per (slot, row); the rows are then
+// combined in a fixed order: shared expert first (weight 1), then the routed
+// slots in selection order, and scaled back by 2^-2a.
+
+// Load slots [s0, s1) of a staged block (global) into the same layout in
+// shared memory. Block-wide.
+__device__ __forceinline__ void load_staged(const uint8_t* src, int s0, int s1, int ns, int IG, uint4* hq, float* Iv,
+                                            float* Xh) {
+    const uint4* g_hq = reinterpret_cast<const uint4*>(src);
+    const float* g_inv = reinterpret_cast<const float*>(g_hq + (size_t)ns * 4 * IG);
+    const float* g_X = g_inv + ns * IG;
+    for (int i = s0 * 4 * IG + threadIdx.x; i < s1 * 4 * IG; i += blockDim.x) hq[i] = __ldcg(g_hq + i);
+    for (int i = s0 * IG + threadIdx.x; i < s1 * IG; i += blockDim.x) {
+        Iv[i] = __ldcg(g_inv + i);
+        Xh[i] = __ldcg(g_X + i);
     }
-    __shared__ int32_t s_ids[MOE_MAX_TOP_K];
-    __shared__ float s_wts[MOE_MAX_TOP_K];
-    // whole quads of rows per CTA (a partial quad costs a full work item)
-    const int nquads_all = (H + kDownRows - 1) / kDownRows;
-    const int own0 = kDownRows * (int)((long long)nquads_all * blockIdx.x / gridDim.x);
-    const int own1 = min(H, kDownRows * (int)((long long)nquads_all * (blockIdx.x + 1) / gridDim.x));
-    pdl_wait();     // gate/up complete: the selection it published and the staged SwiGLU outputs are final
-    pdl_trigger();  // the next token's router may start prefetching its weights
-    ktrace(tr, blockIdx.x, 1);
-    // every slot's SwiGLU outputs, already in the staged form gate/up wrote:
-    // one bulk copy into shared memory, in flight while the selection is read
-    if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)hq_block_bytes(ns, I);
-        bw::mbar_arrive_tx(bw::saddr(&s_hbar), bytes);
-        const uint8_t* src = static_cast<const uint8_t*>(hblk) + (size_t)(blockIdx.x % copies) * bytes;
-        bw::bulk_load(bw::saddr(smh), src, bytes, bw::saddr(&s_hbar), policy_evict_first());
-    }
-    if (threadIdx.x < k) {   // the selection (gate/up's CTA 0 published it; streamed layers pass their own)
-        s_ids[threadIdx.x] = sel_ids[threadIdx.x];
-        s_wts[threadIdx.x] = sel_wts[threadIdx.x];
-    }
-    __syncthreads();
-    if (threadIdx.x < ns) {
-        const int s = threadIdx.x;
-        const bool sh = n_shared && s == 0;
-        const int j = sh ? k : s - n_shared;
-        int e = sh ? E : s_ids[j];
-        if ((unsigned)e > (unsigned)E) e = 0;
-        const uint8_t* rec = rec_tab[e];
-        if (!rec) s_skip = 1;   // streamed layer, expert not resident yet: see below
-        s_rows[s] = rec + gu_block;
-        s_w[s] = sh ? 1.0f : s_wts[j];
-    }
-    bw::mbar_wait(bw::saddr(&s_hbar), 0, &s_abort, err, 1u << 27);
-    __syncthreads();
-    // a launch made before the host staged this token's experts (streamed
-    // layers) does nothing once the staged copy has landed; the host launches
-    // again when every expert is resident
-    if (s_skip) return;
-    ktrace(tr, blockIdx.x, 2);
+}
+
+// Work items (quad of rows, slot) for slots [s0, s1) of this CTA's rows
+// [own0, own1): per-(slot, row) results into ypart[slot][row - own0].
+template <int BITS, int J>
+__device__ __forceinline__ void down_items(int s0, int s1, int own0, int own1, int I, size_t rbI,
+                                           const uint8_t* const* s_rows, const uint4* hq, const float* Iv,
+                                           const float* Xh, float* ypart) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int own = own1 - own0;
-    const int nquad = (own + kDownRows - 1) / kDownRows;
-    const int M = (IG + 31) / 32;
+    const int IG = I / 32, nsl = s1 - s0;
+    const int nquad = (own1 - own0 + kDownRows - 1) / kDownRows;
+    const int nit = nquad * nsl;
     if constexpr (BITS == 2) {
         // a lane takes whole groups of 64 codes (16 bytes each); a warp works
-        // on two items at a time, so that it keeps as many bytes in flight as
+        // on J items at a time, so that it keeps as many bytes in flight as
         // with 4-bit codes
-        const int GI = IG / 2, nit = nquad * ns;
-        for (int it0 = warp; it0 < nit; it0 += 2 * kWarps) {
-            const uint8_t* rr[2][kDownRows];
-            int s2[2], n0s[2], nrs[2];
-            bool live[2];
+        const int GI = IG / 2;
+        for (int it0 = warp; it0 < nit; it0 += J * kWarps) {
+            const uint8_t* rr[J][kDownRows];
+            int s2[J], n0s[J], nrs[J];
+            bool live[J];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < J; ++j) {
                 const int it = it0 + j * kWarps;
                 live[j] = it < nit;
                 const int itv = live[j] ? it : it0;
-                const int q = itv / ns;
-                s2[j] = itv - q * ns;
+                const int q = itv / nsl;
+                s2[j] = s0 + (itv - q * nsl);
                 n0s[j] = own0 + q * kDownRows;
                 nrs[j] = min(kDownRows, own1 - n0s[j]);
 #pragma unroll
                 for (int r = 0; r < kDownRows; ++r) rr[j][r] = s_rows[s2[j]] + (size_t)(n0s[j] + min(r, nrs[j] - 1)) * rbI;
             }
-            float acc[2][kDownRows];
+            float acc[J][kDownRows];
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < J; ++j)
 #pragma unroll
                 for (int r = 0; r < kDownRows; ++r) acc[j][r] = 0.f;
             for (int G = lane; G < GI; G += 32) {
-                uint4 c[2][kDownRows];
-                uint32_t mt[2][kDownRows];
+                uint4 c[J][kDownRows];
+                uint32_t mt[J][kDownRows];
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < J; ++j)
 #pragma unroll
                     for (int r = 0; r < kDownRows; ++r)
                         if (live[j]) {
@@ -502,7 +543,7 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
                             mt[j][r] = ldg_u32(rr[j][r] + I / 4 + 4 * G);
                         }
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+                for (int j = 0; j < J; ++j)
                     if (live[j]) {
                         const uint4* xs = hq + (size_t)s2[j] * 4 * IG;
 #pragma unroll
@@ -512,7 +553,7 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
                     }
             }
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < J; ++j) {
                 float d[kDownRows];
 #pragma unroll
                 for (int r = 0; r < kDownRows; ++r) d[r] = warp_sum(acc[j][r]);
@@ -527,143 +568,235 @@ __global__ void __launch_bounds__(kThreads) k_down(const uint8_t* const* __restr
         // Short rows (one half-group per lane) take two items at a time
         // (J = 2), so that as many bytes are in flight per warp as with long
         // rows.
-        {
-            constexpr int MB = 2 / J;
-            const int nit = nquad * ns;
-            for (int it0 = warp; it0 < nit; it0 += J * kWarps) {
-                const uint8_t* rr[J][kDownRows];
-                int s2[J], n0s[J], nrs[J];
-                bool live[J];
+        constexpr int MB = 2 / J;
+        const int M = (IG + 31) / 32;
+        for (int it0 = warp; it0 < nit; it0 += J * kWarps) {
+            const uint8_t* rr[J][kDownRows];
+            int s2[J], n0s[J], nrs[J];
+            bool live[J];
 #pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int it = it0 + j * kWarps;
-                    live[j] = it < nit;
-                    const int itv = live[j] ? it : it0;
-                    const int q = itv / ns;
-                    s2[j] = itv - q * ns;
-                    n0s[j] = own0 + q * kDownRows;
-                    nrs[j] = min(kDownRows, own1 - n0s[j]);
+            for (int j = 0; j < J; ++j) {
+                const int it = it0 + j * kWarps;
+                live[j] = it < nit;
+                const int itv = live[j] ? it : it0;
+                const int q = itv / nsl;
+                s2[j] = s0 + (itv - q * nsl);
+                n0s[j] = own0 + q * kDownRows;
+                nrs[j] = min(kDownRows, own1 - n0s[j]);
 #pragma unroll
-                    for (int r = 0; r < kDownRows; ++r)
-                        rr[j][r] = s_rows[s2[j]] + (size_t)(n0s[j] + min(r, nrs[j] - 1)) * rbI;
-                }
-                float acc[J][kDownRows];
+                for (int r = 0; r < kDownRows; ++r)
+                    rr[j][r] = s_rows[s2[j]] + (size_t)(n0s[j] + min(r, nrs[j] - 1)) * rbI;
+            }
+            float acc[J][kDownRows];
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+                for (int r = 0; r < kDownRows; ++r) acc[j][r] = 0.f;
+            for (int m = 0; m < M; m += MB) {
+                uint4 c[J][MB][kDownRows];
+                uint32_t mt[J][MB][kDownRows];
 #pragma unroll
                 for (int j = 0; j < J; ++j)
 #pragma unroll
-                    for (int r = 0; r < kDownRows; ++r) acc[j][r] = 0.f;
-                for (int m = 0; m < M; m += MB) {
-                    uint4 c[J][MB][kDownRows];
-                    uint32_t mt[J][MB][kDownRows];
+                    for (int mm = 0; mm < MB; ++mm) {
+                        const int hg = lane + 32 * (m + mm);
 #pragma unroll
-                    for (int j = 0; j < J; ++j)
-#pragma unroll
-                        for (int mm = 0; mm < MB; ++mm) {
-                            const int hg = lane + 32 * (m + mm);
-#pragma unroll
-                            for (int r = 0; r < kDownRows; ++r)
-                                if (live[j] && m + mm < M && hg < IG) {
-                                    c[j][mm][r] = ldg_stream(rr[j][r] + 16 * hg);
-                                    mt[j][mm][r] = ldg_u32(rr[j][r] + I / 2 + 4 * (hg >> 1));
-                                }
-                        }
-#pragma unroll
-                    for (int j = 0; j < J; ++j)
-#pragma unroll
-                        for (int mm = 0; mm < MB; ++mm) {
-                            const int hg = lane + 32 * (m + mm);
+                        for (int r = 0; r < kDownRows; ++r)
                             if (live[j] && m + mm < M && hg < IG) {
-                                const uint4* xs = hq + (size_t)s2[j] * 4 * IG;
-                                int ah[kDownRows], al[kDownRows];
+                                c[j][mm][r] = ldg_stream(rr[j][r] + 16 * hg);
+                                mt[j][mm][r] = ldg_u32(rr[j][r] + I / 2 + 4 * (hg >> 1));
+                            }
+                    }
 #pragma unroll
-                                for (int r = 0; r < kDownRows; ++r) ah[r] = al[r] = 0;
+                for (int j = 0; j < J; ++j)
 #pragma unroll
-                                for (int wi = 0; wi < 4; ++wi) {
-                                    const uint4 xv = xs[wi * IG + hg];
+                    for (int mm = 0; mm < MB; ++mm) {
+                        const int hg = lane + 32 * (m + mm);
+                        if (live[j] && m + mm < M && hg < IG) {
+                            const uint4* xs = hq + (size_t)s2[j] * 4 * IG;
+                            int ah[kDownRows], al[kDownRows];
 #pragma unroll
-                                    for (int r = 0; r < kDownRows; ++r)
-                                        word_dp4a(u4w(c[j][mm][r], wi), xv, ah[r], al[r]);
-                                }
-                                const float iv = Iv[s2[j] * IG + hg], xx = Xh[s2[j] * IG + hg];
+                            for (int r = 0; r < kDownRows; ++r) ah[r] = al[r] = 0;
 #pragma unroll
-                                for (int r = 0; r < kDownRows; ++r) {
-                                    const float2 sb = meta_to_f2(mt[j][mm][r]);
-                                    acc[j][r] = fmaf(sb.x, (float)(ah[r] * 256 + al[r]) * iv, fmaf(sb.y, xx, acc[j][r]));
-                                }
+                            for (int wi = 0; wi < 4; ++wi) {
+                                const uint4 xv = xs[wi * IG + hg];
+#pragma unroll
+                                for (int r = 0; r < kDownRows; ++r) word_dp4a(u4w(c[j][mm][r], wi), xv, ah[r], al[r]);
+                            }
+                            const float iv = Iv[s2[j] * IG + hg], xx = Xh[s2[j] * IG + hg];
+#pragma unroll
+                            for (int r = 0; r < kDownRows; ++r) {
+                                const float2 sb = meta_to_f2(mt[j][mm][r]);
+                                acc[j][r] = fmaf(sb.x, (float)(ah[r] * 256 + al[r]) * iv, fmaf(sb.y, xx, acc[j][r]));
                             }
                         }
-                }
+                    }
+            }
 #pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    float d[kDownRows];
+            for (int j = 0; j < J; ++j) {
+                float d[kDownRows];
 #pragma unroll
-                    for (int r = 0; r < kDownRows; ++r) d[r] = warp_sum(acc[j][r]);
+                for (int r = 0; r < kDownRows; ++r) d[r] = warp_sum(acc[j][r]);
 #pragma unroll
-                    for (int r = 0; r < kDownRows; ++r)
-                        if (live[j] && lane == r && r < nrs[j]) ypart[s2[j] * kDownMaxRows + (n0s[j] - own0) + r] = d[r];
-                }
+                for (int r = 0; r < kDownRows; ++r)
+                    if (live[j] && lane == r && r < nrs[j]) ypart[s2[j] * kDownMaxRows + (n0s[j] - own0) + r] = d[r];
             }
         }
     }
-    __syncthreads();
-    for (int n = own0 + threadIdx.x; n < own1; n += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s) acc = fmaf(s_w[s], ypart[s * kDownMaxRows + (n - own0)], acc);
-        if (y32) y32[n] = acc;
-        if (y) {
-            if (y_bf16) static_cast<__nv_bfloat16*>(y)[n] = __float2bfloat16_rn(acc);
-            else static_cast<float*>(y)[n] = acc;
+}
+
+struct DownArgs {
+    const uint8_t* const* rec_tab;
+    int k, E, n_shared, H, I;
+    size_t rbI, gu_block;            // bytes of one down row record; offset of the down block in a record
+    const uint8_t* hq;               // copies x staged blocks of the SwiGLU outputs (gate/up wrote them)
+    int copies;
+    void* y;
+    int y_bf16;
+    float* y32;
+    const int32_t* sel_ids;          // the selection (the router's, or the streamed layer's)
+    const float* sel_wts;
+    const int* scale_in;             // the token exponent a
+    unsigned* shared_done;           // with n_shared: early start on the shared rows (nullable)
+    unsigned* ids_ready;             // the router's ready flag (nullable); cleared with the counters
+    unsigned* down_done;             // the last CTA clears the counters
+    unsigned* err;
+    unsigned long long* tr;
+};
+
+template <int BITS, int J = 1>
+__global__ void __launch_bounds__(kThreads) k_down(const DownArgs a) {
+    extern __shared__ uint4 smh[];
+    ktrace(a.tr, blockIdx.x, 0);
+    const int I = a.I, IG = I / 32, ns = a.k + a.n_shared;
+    uint4* hq = smh;                                                     // [ns][4][IG]
+    float* Iv = reinterpret_cast<float*>(hq + (size_t)ns * 4 * IG);     // [ns][IG]
+    float* Xh = Iv + ns * IG;                                            // [ns][IG]
+    float* ypart = Xh + ns * IG;                                         // [ns][kDownMaxRows]
+    __shared__ const uint8_t* s_rows[MOE_MAX_TOP_K + 1];
+    __shared__ float s_w[MOE_MAX_TOP_K + 1];
+    __shared__ int s_skip, s_early, s_scale;
+    // whole quads of rows per CTA (a partial quad costs a full work item)
+    const int nquads_all = (a.H + kDownRows - 1) / kDownRows;
+    const int own0 = kDownRows * (int)((long long)nquads_all * blockIdx.x / gridDim.x);
+    const int own1 = min(a.H, kDownRows * (int)((long long)nquads_all * (blockIdx.x + 1) / gridDim.x));
+    const bool counted = a.n_shared && a.shared_done;
+    const uint8_t* src = a.hq + (size_t)(blockIdx.x % a.copies) * hq_block_bytes(ns, I);   // this CTA's replica
+    if (threadIdx.x == 0) {
+        // the shared expert's half-groups are all staged once the counter
+        // reaches I/32: its rows run before the wait for gate/up
+        int ok = 0;
+        if (counted) {
+            ok = wait_count(a.shared_done, (unsigned)IG, kWaitNs) ? 1 : 0;
+            if (!ok) atomicOr(a.err, 1u << 27);
+        }
+        s_early = ok;
+        s_skip = 0;
+        if (a.n_shared) {   // slot 0: the shared expert (its record is fixed), weight 1
+            s_rows[0] = a.rec_tab[a.E] + a.gu_block;
+            s_w[0] = 1.0f;
         }
     }
     __syncthreads();
-    ktrace(tr, blockIdx.x, 3);
+    const int early = s_early;
+    if (early) {
+        load_staged(src, 0, 1, ns, IG, hq, Iv, Xh);
+        __syncthreads();
+        down_items<BITS, J>(0, 1, own0, own1, I, a.rbI, s_rows, hq, Iv, Xh, ypart);
+    }
+    pdl_wait();     // gate/up complete: the staged SwiGLU outputs are final
+    pdl_trigger();  // the next token's router may start prefetching its weights
+    ktrace(a.tr, blockIdx.x, 1);
+    if (threadIdx.x >= a.n_shared && threadIdx.x < ns) {   // the routed slots
+        const int s = threadIdx.x, j = s - a.n_shared;
+        int e = a.sel_ids[j];
+        if ((unsigned)e >= (unsigned)a.E) e = 0;   // a valid selection never needs the clamp
+        const uint8_t* rec = a.rec_tab[e];
+        if (!rec) s_skip = 1;   // streamed layer, expert not resident yet: see below
+        s_rows[s] = rec + a.gu_block;
+        s_w[s] = a.sel_wts[j];
+    }
+    if (threadIdx.x == 0) s_scale = a.scale_in ? *a.scale_in : 0;
+    load_staged(src, early, ns, ns, IG, hq, Iv, Xh);
+    __syncthreads();
+    ktrace(a.tr, blockIdx.x, 2);
+    // a launch made before the host staged this token's experts (streamed
+    // layers) does nothing; the host launches again when every expert is resident
+    if (!s_skip) {
+        down_items<BITS, J>(early, ns, own0, own1, I, a.rbI, s_rows, hq, Iv, Xh, ypart);
+        __syncthreads();
+        const float inv_a = exp2i(-s_scale);
+        for (int n = own0 + threadIdx.x; n < own1; n += blockDim.x) {
+            float acc = 0.f;
+            for (int s = 0; s < ns; ++s) acc = fmaf(s_w[s], ypart[s * kDownMaxRows + (n - own0)], acc);
+            acc = acc * inv_a * inv_a;   // two exact steps (one rounding if the result is subnormal)
+            if (a.y32) a.y32[n] = acc;
+            if (a.y) {
+                if (a.y_bf16) static_cast<__nv_bfloat16*>(a.y)[n] = __float2bfloat16_rn(acc);
+                else static_cast<float*>(a.y)[n] = acc;
+            }
+        }
+    }
+    if (a.down_done) {
+        // the last CTA to finish clears the counters for the next token (whose
+        // router and gate/up start only after this grid has completed)
+        __syncthreads();
+        if (threadIdx.x == 0 && atomicAdd(a.down_done, 1u) == gridDim.x - 1) {
+            if (a.shared_done) *a.shared_done = 0u;
+            if (a.ids_ready) *a.ids_ready = 0u;
+            *a.down_done = 0u;
+            __threadfence();
+        }
+    }
+    ktrace(a.tr, blockIdx.x, 3);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 
-static int round32(int v) { return (v + 31) / 32 * 32; }
-// rows one gate/up CTA owns for NR rows: a multiple of 32, spread over every resident CTA
-static int gu_rows(const Layer& L, int NR) {
-    return std::max(32, round32((NR + L.num_sms * L.occ_gu - 1) / (L.num_sms * L.occ_gu)));
-}
-static size_t gu_smem_for(const Layer& L, int R) {
+static size_t gu_smem_for(const Layer& L) {
     const int H = L.d.hidden;
-    return (size_t)H * 2 + (size_t)(H / 32) * 8 + (size_t)R * 4;
+    return (size_t)H * 2 + (size_t)(H / 32) * 8;
 }
 static size_t down_smem(int I, int ns) {
     return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8 + (size_t)ns * kDownMaxRows * 4;
 }
 static int down_grid(const Layer& L) { return L.num_sms * L.occ_down; }
+// gate/up CTAs: every resident CTA, but not more than there are row pairs per warp
+static int gu_grid(const Layer& L) {
+    const int pairs = (L.d.top_k + L.d.n_shared) * L.d.inter;
+    return std::max(1, std::min(L.num_sms * L.occ_gu, (pairs + kWarps - 1) / kWarps));
+}
 
 using GuKernel = decltype(&k_gateup<4, 1>);
 using DownKernel = decltype(&k_down<4, 1>);
 // 4-bit rows of at most kGuBlock / 2 half-groups per lane (H <= 3072): two
 // row pairs per warp at a time; down rows of one half-group per lane
-// (I <= 1024): two items per warp at a time
+// (I <= 1024): two items per warp at a time; 2-bit codes: two of each
 static GuKernel gu_kernel(const Layer& L) {
-    if (L.wbits == 2) return k_gateup<2, 1>;
+    if (L.wbits == 2) return k_gateup<2, 2>;
     return (L.d.hidden / 32 + 31) / 32 <= kGuBlock / 2 ? k_gateup<4, 2> : k_gateup<4, 1>;
 }
 static DownKernel down_kernel(const Layer& L) {
-    if (L.wbits == 2) return k_down<2, 1>;
+    if (L.wbits == 2) return k_down<2, 2>;
     return (L.d.inter / 32 + 31) / 32 == 1 ? k_down<4, 2> : k_down<4, 1>;
 }
+
+size_t decode_hq_block_bytes(int ns, int I) { return hq_block_bytes(ns, I); }
 
 cudaError_t decode_kernel_setup(Layer& L) {
     const int H = L.d.hidden, I = L.d.inter, ns = L.d.top_k + L.d.n_shared;
     cudaError_t e = router_kernel_setup(L);
     if (e != cudaSuccess) return e;
-    const int R1 = round32((ns * I + L.num_sms - 1) / L.num_sms);   // rows per CTA at one CTA per SM (upper bound)
-    L.gu_smem = gu_smem_for(L, R1);
+    L.gu_smem = gu_smem_for(L);
     const void* gu = (const void*)gu_kernel(L);
     const void* dn = (const void*)down_kernel(L);
     e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.gu_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(dn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)down_smem(I, ns));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, gu, kGuThreads, L.gu_smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, gu, kThreads, L.gu_smem);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, dn, kThreads, down_smem(I, ns));
     if (e != cudaSuccess) return e;
@@ -676,85 +809,114 @@ cudaError_t decode_kernel_setup(Layer& L) {
     return cudaSuccess;
 }
 
-// gate/up over row-order slots jj0..jj1-1 (sel_ids null: select from `part`)
-static cudaError_t launch_gateup(Layer& L, const void* x, const float* part, void* hblk, int copies, int32_t* ids_out,
-                                 float* wts_out, float* logits_out, const int32_t* sel_ids, int jj0, int jj1,
-                                 bool pdl, unsigned long long* tr, cudaStream_t s) {
+static cudaError_t launch_gateup(Layer& L, const void* x, const DecodeScratch& b, int jj0, int jj1, bool pdl,
+                                 unsigned long long* tr, cudaStream_t s) {
     const auto& d = L.d;
-    const int NR = (jj1 - jj0) * d.inter;
-    const int R = gu_rows(L, NR);
-    const int grid = (NR + R - 1) / R;
-    return launch_pdl(gu_kernel(L), dim3(grid), dim3(kGuThreads), gu_smem_for(L, R), s,
-                      pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits, (const float*)L.router_bias,
-                      d.top_k, d.n_experts, d.n_shared, x, d.act_dtype == MOE_BF16 ? 1 : 0, d.hidden, d.inter,
-                      row_bytes(d.hidden, L.wbits), R, hblk, copies, ids_out, wts_out, logits_out, sel_ids, jj0, jj1,
-                      L.route_mode(), (const uint8_t*)L.next_router, L.next_router_bytes, tr);
+    GuArgs a{};
+    a.rec_tab = (const uint8_t* const*)L.rec_table;
+    a.k = d.top_k;
+    a.E = d.n_experts;
+    a.n_shared = d.n_shared;
+    a.x = x;
+    a.x_bf16 = d.act_dtype == MOE_BF16 ? 1 : 0;
+    a.H = d.hidden;
+    a.I = d.inter;
+    a.rbH = row_bytes(d.hidden, L.wbits);
+    a.ids = b.ids;
+    a.ids_ready = b.ids_ready;
+    a.h = b.h;
+    a.hg_cnt = b.hg_cnt;
+    a.hq = b.hq;
+    a.copies = b.copies;
+    a.scale_out = b.scale;
+    a.shared_done = b.shared_done;
+    a.jj0 = jj0;
+    a.jj1 = jj1;
+    a.pf = (const uint8_t*)L.next_router;
+    a.pf_bytes = L.next_router_bytes;
+    a.err = error_word(L);
+    a.tr = tr;
+    a.stall_shared = L.test_stall_shared;
+    return launch_pdl(gu_kernel(L), dim3(gu_grid(L)), dim3(kThreads), L.gu_smem, s, pdl, a);
 }
 
-static cudaError_t launch_down(Layer& L, const float* part, const void* hblk, int copies, void* y, float* y_f32,
-                               const int32_t* sel_ids, const float* sel_wts, bool pdl, unsigned long long* tr,
-                               cudaStream_t s) {
+static cudaError_t launch_down(Layer& L, const DecodeScratch& b, void* y, float* y_f32, bool pdl,
+                               unsigned long long* tr, cudaStream_t s) {
     const auto& d = L.d;
     const int ns = d.top_k + d.n_shared;
-    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(kThreads),
-                      down_smem(d.inter, ns), s, pdl, (const uint8_t* const*)L.rec_table, part, L.router_splits,
-                      (const float*)L.router_bias, d.top_k, d.n_experts, d.n_shared, d.hidden, d.inter, hblk, copies,
-                      y, d.act_dtype == MOE_BF16 ? 1 : 0, y_f32, row_bytes(d.inter, L.wbits),
-                      gu_block_bytes(d.hidden, d.inter, L.wbits), sel_ids, sel_wts, fused_error_word(L), tr);
+    DownArgs a{};
+    a.rec_tab = (const uint8_t* const*)L.rec_table;
+    a.k = d.top_k;
+    a.E = d.n_experts;
+    a.n_shared = d.n_shared;
+    a.H = d.hidden;
+    a.I = d.inter;
+    a.rbI = row_bytes(d.inter, L.wbits);
+    a.gu_block = gu_block_bytes(d.hidden, d.inter, L.wbits);
+    a.hq = b.hq;
+    a.copies = b.copies;
+    a.y = y;
+    a.y_bf16 = d.act_dtype == MOE_BF16 ? 1 : 0;
+    a.y32 = y_f32;
+    a.sel_ids = b.ids;
+    a.sel_wts = b.wts;
+    a.scale_in = b.scale;
+    a.shared_done = b.shared_done;
+    a.ids_ready = b.ids_ready;
+    a.down_done = (b.shared_done || b.ids_ready) ? b.down_done : nullptr;
+    a.err = error_word(L);
+    a.tr = tr;
+    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(kThreads), down_smem(d.inter, ns), s, pdl, a);
 }
 
-cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which, cudaStream_t s) {
-    const int ns = L.d.top_k + L.d.n_shared;
-    cudaError_t e;
-    if (which & (RUN_ROUTED_GU | RUN_SHARED_GU)) {
-        prof_begin(L, K_GATEUP_DECODE, s);
-        e = launch_gateup(L, x, L.logits_part, L.h, L.h_copies, L.ids, L.wts, L.logits, nullptr, 0, ns, L.pdl,
-                          L.split_trace(1), s);
-        prof_end(L, s);
-        if (e != cudaSuccess) return e;
-    }
-    if (which & RUN_DOWN) {
-        prof_begin(L, K_DOWN_DECODE, s);
-        e = launch_down(L, L.logits_part, L.h, L.h_copies, y, y_f32, L.ids, L.wts, L.pdl, L.split_trace(2), s);
-        prof_end(L, s);
-        return e;
-    }
-    return cudaSuccess;
-}
-
-// The same two expert kernels over caller-given scratch: router partials
-// `part` [splits][E] (already written on `s`), selection out (`logits` [E],
-// `ids` [k], `wts` [k]) and the staged SwiGLU outputs `h` (at least
-// hq_block_bytes(k + n_shared, I) bytes). No profiling or tracing.
-cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
-                                          float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s) {
-    const int ns = L.d.top_k + L.d.n_shared;
-    cudaError_t e = launch_gateup(L, x, part, h, 1, ids, wts, logits, nullptr, 0, ns, L.pdl, nullptr, s);
-    if (e != cudaSuccess) return e;
-    return launch_down(L, part, h, 1, y, y_f32, ids, wts, L.pdl, nullptr, s);
-}
-
-// Streamed layers: the selection (ids, wts of one token) is already on the
-// device and the routed experts' records are resident. `jj0..jj1` are the
-// row-order slots of gate/up to run (0 = the shared expert when there is one);
-// `down` adds the down + combine kernel. Plain launches (no programmatic
-// overlap): the caller orders them against the cache's copies with events.
-cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
-                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s, bool pdl) {
+// gate/up over row-order slots jj0..jj1-1 and (with `down`) down + combine,
+// over the scratch `b`; the selection b.ids / b.wts is published by the
+// router (or given, streamed layers).
+cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, const DecodeScratch& b, int jj0,
+                                  int jj1, bool down, bool pdl, bool trace, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
     if (jj1 > jj0) {
         prof_begin(L, K_GATEUP_DECODE, s);
-        e = launch_gateup(L, x, nullptr, L.h, L.h_copies, nullptr, nullptr, nullptr, ids, jj0, jj1, pdl && L.pdl,
-                          nullptr, s);
+        e = launch_gateup(L, x, b, jj0, jj1, pdl && L.pdl, trace ? L.split_trace(1) : nullptr, s);
         prof_end(L, s);
         if (e != cudaSuccess) return e;
     }
     if (down) {
         prof_begin(L, K_DOWN_DECODE, s);
-        e = launch_down(L, nullptr, L.h, L.h_copies, y, y_f32, ids, wts, pdl && L.pdl, nullptr, s);
+        e = launch_down(L, b, y, y_f32, pdl && L.pdl, trace ? L.split_trace(2) : nullptr, s);
         prof_end(L, s);
     }
     return e;
+}
+
+DecodeScratch layer_decode_scratch(Layer& L, bool fast) {
+    DecodeScratch b;
+    b.part = L.logits_part;
+    b.logits = L.logits;
+    b.ids = L.ids;
+    b.wts = L.wts;
+    b.scale = reinterpret_cast<int*>(L.counters + CNT_TOKEN_SCALE);
+    b.router_cnt = L.counters + CNT_ROUTER;
+    b.h = L.h;
+    b.hg_cnt = L.hg_cnt;
+    b.hq = L.hq;
+    b.copies = kHCopies;
+    if (fast) {
+        b.ids_ready = L.counters + CNT_IDS_READY;
+        b.shared_done = L.counters + CNT_SHARED_DONE;
+        b.down_done = L.counters + CNT_DOWN_DONE;
+    }
+    return b;
+}
+
+// Streamed layers: the selection (L.ids, L.wts) is already on the device and
+// the routed experts' records are resident. `jj0..jj1` are the row-order
+// slots of gate/up to run (0 = the shared expert when there is one); `down`
+// adds the down + combine kernel. The caller orders them against the cache's
+// copies (events, or programmatic launch after the kernels that staged them).
+cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, int jj0, int jj1, bool down,
+                                      cudaStream_t s, bool pdl) {
+    return launch_experts_decode(L, x, y, y_f32, layer_decode_scratch(L, false), jj0, jj1, down, pdl, false, s);
 }
 
 }  // namespace moe

@@ -8,6 +8,8 @@
 // at creation; this file adds no allocation of any kind on the call path.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -19,55 +21,82 @@ static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRAT
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// per device: the region's address and the context it was looked up in (a
+// device reset gives the device a new primary context, where the region has
+// another address, so the lookup is redone when the context changes)
 void* g_base[kMaxDevices] = {};
+CUcontext g_ctx[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
 
 inline size_t up256(size_t n) { return (n + 255) / 256 * 256; }
 
-struct StaticScratch {
-    float* part;
-    float* logits;
-    int32_t* ids;
-    float* wts;
-    float* h;
-    size_t bytes;
-};
+constexpr int kParts = 9;
 
 // Byte offsets of the pieces within the region; the last entry is the total.
-void layout(const Layer& L, size_t off[6]) {
+void layout(const Layer& L, size_t off[kParts]) {
     const auto& d = L.d;
-    const size_t E = d.n_experts, k = d.top_k;
+    const size_t E = d.n_experts, k = d.top_k, I = d.inter, ns = k + d.n_shared;
     off[0] = 0;                                                  // partial logits [splits][E]
-    off[1] = off[0] + up256((size_t)L.router_splits * E * 4);    // logits [E]
+    off[1] = off[0] + up256((size_t)L.router_splits * E * 4);    // keys [E]
     off[2] = off[1] + up256(E * 4);                              // ids [k]
     off[3] = off[2] + up256(k * 4);                              // weights [k]
-    off[4] = off[3] + up256(k * 4);                              // SwiGLU outputs [k + 1][I]
-    off[5] = off[4] + up256((k + 1) * (size_t)d.inter * 4);
+    off[4] = off[3] + up256(k * 4);                              // the token's scale exponent
+    off[5] = off[4] + up256(4);                                  // SwiGLU outputs [k + 1][I] fp32
+    off[6] = off[5] + up256((k + 1) * I * 4);                    // half-group counters [k + 1][I / 32]
+    off[7] = off[6] + up256((k + 1) * (I / 32) * 4);             // one staged block of the SwiGLU outputs
+    off[8] = off[7] + up256(decode_hq_block_bytes((int)ns, (int)I));
 }
 
-StaticScratch carve(const Layer& L, unsigned char* base) {
-    size_t off[6];
+DecodeScratch carve(Layer& L, unsigned char* base) {
+    size_t off[kParts];
     layout(L, off);
-    StaticScratch s{};
+    DecodeScratch s;
     s.part = reinterpret_cast<float*>(base + off[0]);
     s.logits = reinterpret_cast<float*>(base + off[1]);
     s.ids = reinterpret_cast<int32_t*>(base + off[2]);
     s.wts = reinterpret_cast<float*>(base + off[3]);
-    s.h = reinterpret_cast<float*>(base + off[4]);
-    s.bytes = off[5];
-    return s;
+    s.scale = reinterpret_cast<int*>(base + off[4]);
+    s.router_cnt = L.counters + CNT_ROUTER;   // the layer's own (zero between launches)
+    s.h = reinterpret_cast<float*>(base + off[5]);
+    s.hg_cnt = reinterpret_cast<unsigned*>(base + off[6]);
+    s.hq = base + off[7];
+    s.copies = 1;
+    return s;   // no ready flag and no early start: nothing else in the region must start at zero
 }
 
-// Device address of this device's region, looked up once per device with
-// that device current. The caller holds a DeviceGuard for `dev`.
+// Device address of this device's region, looked up once per device (per
+// context of that device) with that device current. The caller holds a
+// DeviceGuard for `dev`.
 moe_status region_for(int dev, unsigned char** out) {
     if (dev < 0 || dev >= kMaxDevices) return fail(MOE_E_UNSUPPORTED, "device ordinal above the static-scratch table");
+    // binds the device's primary context to this thread (a thread that never
+    // used the runtime has none current yet)
+    const cudaError_t se = cudaSetDevice(dev);
+    if (se != cudaSuccess) return cuda_fail(se, "cudaSetDevice");
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return fail(MOE_E_CUDA, "cuCtxGetCurrent is not available from the driver");
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return fail(MOE_E_CUDA, "no current CUDA context for the device");
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_base[dev]) {
+    if (!g_base[dev] || g_ctx[dev] != ctx) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
         if (!p) return fail(MOE_E_CUDA, "cudaGetSymbolAddress(static scratch) returned NULL");
         g_base[dev] = p;
+        g_ctx[dev] = ctx;
     }
     *out = static_cast<unsigned char*>(g_base[dev]);
     return MOE_OK;
@@ -85,9 +114,9 @@ extern "C" moe_status moe_decode_static_scratch(moe_layer* layer, const void* x,
     Layer& L = layer->L;
     if (L.d.cache_slots > 0) return fail(MOE_E_UNSUPPORTED, "static-scratch decode of a streamed layer");
     // size check first: an oversized layer is rejected before any CUDA call
-    size_t off[6];
+    size_t off[kParts];
     layout(L, off);
-    const size_t need = off[5];
+    const size_t need = off[kParts - 1];
     if (need > MOE_STATIC_SCRATCH_BYTES)
         return fail(MOE_E_INVALID, "layer needs " + std::to_string(need) +
                                        " bytes of decode scratch; the static region holds " +
@@ -97,11 +126,11 @@ extern "C" moe_status moe_decode_static_scratch(moe_layer* layer, const void* x,
     unsigned char* base = nullptr;
     const moe_status st = region_for(L.device, &base);
     if (st != MOE_OK) return st;
-    const StaticScratch sc = carve(L, base);
+    const DecodeScratch sc = carve(L, base);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_route_decode_partials(L, x, sc.part, s);
+    cudaError_t e = launch_route_decode(L, x, s, 1, nullptr, nullptr, 0, nullptr, &sc);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
-    e = launch_experts_decode_scratch(L, x, y, y_f32, sc.part, sc.logits, sc.ids, sc.wts, sc.h, s);
+    e = launch_experts_decode(L, x, y, y_f32, sc, 0, L.d.top_k + L.d.n_shared, true, true, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "expert launch");
     return MOE_OK;
 }

@@ -91,7 +91,6 @@ static void free_layer(Layer& L) {
     if (L.pf.waves_host) cudaFreeHost(L.pf.waves_host);
     if (L.pf.groups_ready) cudaEventDestroy(L.pf.groups_ready);
     if (L.pf.waves_free) cudaEventDestroy(L.pf.waves_free);
-    f(L.trace);
     f(L.trace_split);
 }
 
@@ -185,7 +184,9 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     size_t o_logits = sc.add((size_t)T * E * 4);
     size_t o_ids = sc.add((size_t)T * k * 4);
     size_t o_w = sc.add((size_t)T * k * 4);
-    size_t o_h = sc.add(std::max((size_t)(k + 1) * I * 4, (size_t)kHCopies * hq_block_bytes_host(k + d.n_shared, I)));
+    size_t o_h = sc.add((size_t)(k + 1) * I * 4);
+    size_t o_hq = sc.add((size_t)kDecodeHCopies * decode_hq_block_bytes(k + d.n_shared, I));
+    size_t o_hgc = sc.add((size_t)(k + 1) * (I / 32) * 4);
     size_t o_cnt = sc.add(64 * 4);
     // prefill block layout
     const int rows = T * k + T * d.n_shared;
@@ -193,6 +194,11 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     size_t o_xp = pf.add((size_t)rows * H * 2);
     size_t o_hp = pf.add((size_t)rows * I * 2);
     size_t o_yp = pf.add((size_t)rows * H * 4);
+    size_t o_h32 = pf.add((size_t)rows * I * 4);
+    size_t o_xexp = pf.add((size_t)T * 4);
+    size_t o_rexp = pf.add((size_t)rows * 4);
+    size_t o_hmax = pf.add((size_t)rows * 4);
+    size_t o_zexp = pf.add((size_t)rows * 4);
     size_t o_gexp = pf.add((size_t)(E + 1) * 4);
     size_t o_goff = pf.add((size_t)(E + 1) * 4);
     size_t o_gcnt = pf.add((size_t)(E + 1) * 4);
@@ -303,7 +309,8 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
         L.ids = reinterpret_cast<int32_t*>(base + o_ids);
         L.wts = reinterpret_cast<float*>(base + o_w);
         L.h = reinterpret_cast<float*>(base + o_h);
-        L.h_copies = kHCopies;
+        L.hq = base + o_hq;
+        L.hg_cnt = reinterpret_cast<unsigned*>(base + o_hgc);
         L.counters = reinterpret_cast<unsigned*>(base + o_cnt);
     }
     if (T > 1) {
@@ -313,6 +320,11 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
         L.pf.xp = base + o_xp;
         L.pf.hp = base + o_hp;
         L.pf.yp = reinterpret_cast<float*>(base + o_yp);
+        L.pf.h32 = reinterpret_cast<float*>(base + o_h32);
+        L.pf.xexp = reinterpret_cast<int32_t*>(base + o_xexp);
+        L.pf.rexp = reinterpret_cast<int32_t*>(base + o_rexp);
+        L.pf.hmax = reinterpret_cast<unsigned*>(base + o_hmax);
+        L.pf.zexp = reinterpret_cast<int32_t*>(base + o_zexp);
         L.pf.group_expert = reinterpret_cast<int32_t*>(base + o_gexp);
         L.pf.group_off = reinterpret_cast<int32_t*>(base + o_goff);
         L.pf.group_cnt = reinterpret_cast<int32_t*>(base + o_gcnt);
@@ -325,13 +337,11 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     L.device_bytes = need;
 
     TRY_CUDA(decode_kernel_setup(L));
-    if (T > 1 && L.wbits == 4) TRY_CUDA(prefill_kernel_setup(L));
-    L.fused_ok = L.wbits == 4 && fused_setup(L);
-    cudaGetLastError();  // a rejected fused configuration leaves no sticky error
+    if (T > 1) TRY_CUDA(prefill_kernel_setup(L));
 
     if (d.cache_slots > 0) {
         st = cache_create(L, records, source, source_user);
-        if (st == MOE_OK && T > 1 && L.wbits == 4) st = prefill_cache_setup(L);
+        if (st == MOE_OK && T > 1) st = prefill_cache_setup(L);
         if (st != MOE_OK) { std::string m = g_last_error; free_layer(L); delete layer; return fail(st, m); }
     }
 #undef TRY_ALLOC
@@ -371,14 +381,12 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (L.d.cache_slots > 0) return cache_decode(L, x, y, y_f32, s);
-    if (L.fused_ok && L.decode_path == MOE_PATH_FUSED) {
-        cudaError_t ef = launch_decode_fused(L, x, y, y_f32, s);
-        if (ef != cudaSuccess) return cuda_fail(ef, "fused decode launch");
-        return MOE_OK;
-    }
-    cudaError_t e = launch_route_decode(L, x, s, 0);   // partial logits; the expert kernels select
+    // the router selects in its last block and raises the ready flag that
+    // gate/up waits for; the down kernel starts early on the shared expert
+    const DecodeScratch b = layer_decode_scratch(L, true);
+    cudaError_t e = launch_route_decode(L, x, s, 1, nullptr, nullptr, 0, nullptr, &b);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
-    e = launch_experts_decode(L, x, y, y_f32, RUN_ALL, s);
+    e = launch_experts_decode(L, x, y, y_f32, b, 0, L.d.top_k + L.d.n_shared, true, true, true, s);
     if (e != cudaSuccess) return cuda_fail(e, "expert launch");
     return MOE_OK;
 }
@@ -393,8 +401,7 @@ moe_status moe_prefill_chunk(moe_layer* layer, const void* x, int32_t T, void* y
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 1) return moe_decode(layer, x, y, y_f32, stream);
-    if (L.wbits != 4) return fail(MOE_E_UNSUPPORTED, "prefill chunks need 4-bit experts (decode token by token)");
-    cudaError_t e = launch_route_tokens(L, x, T, s);
+    cudaError_t e = launch_route_tokens(L, x, T, s, L.pf.xexp);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     if (L.d.cache_slots > 0) {
         if (!cache_is_device(L)) return launch_prefill_streamed(L, x, T, y, y_f32, s);
@@ -463,8 +470,6 @@ moe_status moe_layer_set_router_scoring(moe_layer* layer, int32_t scoring, float
     if (scoring != MOE_SCORE_SOFTMAX && scoring != MOE_SCORE_SIGMOID) return fail(MOE_E_INVALID, "unknown router scoring");
     if (!(routed_scaling > 0.0f) || !std::isfinite(routed_scaling))
         return fail(MOE_E_INVALID, "routed_scaling must be finite and positive");
-    if (scoring == MOE_SCORE_SIGMOID && L.decode_path == MOE_PATH_FUSED)
-        return fail(MOE_E_UNSUPPORTED, "the fused decode supports softmax router scoring only");
     L.router_scoring = scoring;
     L.routed_scaling = routed_scaling;
     return MOE_OK;
@@ -474,24 +479,13 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
     if (!layer) return fail(MOE_E_INVALID, "NULL layer");
     Layer& L = layer->L;
     switch (option) {
-        case MOE_OPT_DECODE_PATH:
-            if (value != MOE_PATH_AUTO && value != MOE_PATH_SPLIT && value != MOE_PATH_FUSED)
-                return fail(MOE_E_INVALID, "unknown decode path");
-            if (value == MOE_PATH_FUSED && !L.fused_ok)
-                return fail(MOE_E_UNSUPPORTED, "the fused decode does not support this layer's shape or mode");
-            if (value == MOE_PATH_FUSED && L.router_scoring != MOE_SCORE_SOFTMAX)
-                return fail(MOE_E_UNSUPPORTED, "the fused decode supports softmax router scoring only");
-            L.decode_path = (int)value;
-            return MOE_OK;
-        case MOE_OPT_TEST_STALL_ROUTING:
-            L.test_no_publish = value ? 1 : 0;
+        case MOE_OPT_TEST_STALL_SHARED:
+            L.test_stall_shared = value ? 1 : 0;
             return MOE_OK;
         case MOE_OPT_TRACE:
-            if (value && !L.trace) {
+            if (value && !L.trace_split) {
                 DeviceGuard g(L.device);
-                const size_t nb = (size_t)L.num_sms * MOE_TRACE_POINTS * 8;
-                MOE_CUDA_TRY(cudaMalloc(&L.trace, nb));
-                MOE_CUDA_TRY(cudaMemset(L.trace, 0, nb));
+                if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
                 const size_t ns = (size_t)MOE_TRACE_KERNELS * MOE_TRACE_MAX_CTAS * 4 * 8;
                 MOE_CUDA_TRY(cudaMalloc(&L.trace_split, ns));
                 MOE_CUDA_TRY(cudaMemset(L.trace_split, 0, ns));
@@ -517,17 +511,16 @@ moe_status moe_layer_set_option(moe_layer* layer, int32_t option, int64_t value)
     return fail(MOE_E_INVALID, "unknown option");
 }
 
-moe_status moe_trace_read(moe_layer* layer, uint64_t* out, int32_t cap, int32_t* n_ctas) {
-    if (!layer || !out) return fail(MOE_E_INVALID, "NULL argument");
+moe_status moe_layer_selection(moe_layer* layer, int32_t T, int32_t* ids, float* w, void* stream) {
+    if (!layer || !ids || !w) return fail(MOE_E_INVALID, "NULL argument");
     Layer& L = layer->L;
-    if (!L.trace) return fail(MOE_E_STATE, "tracing was never enabled (MOE_OPT_TRACE)");
-    const int n = L.num_sms * MOE_TRACE_POINTS;
-    if (cap < n) return fail(MOE_E_INVALID, "cap smaller than n_ctas * MOE_TRACE_POINTS");
+    if (T < 1 || T > L.d.max_tokens) return fail(MOE_E_INVALID, "T out of range 1..max_tokens");
     DeviceGuard g(L.device);
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
-    MOE_CUDA_TRY(cudaDeviceSynchronize());
-    MOE_CUDA_TRY(cudaMemcpy(out, L.trace, (size_t)n * 8, cudaMemcpyDeviceToHost));
-    if (n_ctas) *n_ctas = L.num_sms;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t nb = (size_t)T * L.d.top_k * 4;
+    MOE_CUDA_TRY(cudaMemcpyAsync(ids, L.ids, nb, cudaMemcpyDeviceToDevice, s));
+    MOE_CUDA_TRY(cudaMemcpyAsync(w, L.wts, nb, cudaMemcpyDeviceToDevice, s));
     return MOE_OK;
 }
 
@@ -551,7 +544,7 @@ moe_status moe_layer_check(moe_layer* layer, uint32_t* bits) {
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     MOE_CUDA_TRY(cudaDeviceSynchronize());
     uint32_t v = 0, vp = 0;
-    unsigned* w = fused_error_word(L);
+    unsigned* w = error_word(L);
     MOE_CUDA_TRY(cudaMemcpy(&v, w, 4, cudaMemcpyDeviceToHost));
     if (L.pf.err) MOE_CUDA_TRY(cudaMemcpy(&vp, L.pf.err, 4, cudaMemcpyDeviceToHost));
     v |= vp;   // the prefill GEMM reports in bits 16 and up

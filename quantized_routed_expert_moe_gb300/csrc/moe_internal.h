@@ -86,9 +86,14 @@ struct PrefillScratch {
     int32_t* perm_token = nullptr;    // [rows] token of each permuted row
     int32_t* pos = nullptr;           // [T][k + 1] permuted row of (t, slot j); slot k = shared
     unsigned* err = nullptr;          // [1] error bits of the grouped GEMM (bounded waits)
-    void* xp = nullptr;               // [rows][H] fp16 gathered activations (8-element blocks permuted)
-    void* hp = nullptr;               // [rows][I] fp16 SwiGLU outputs (same block permutation)
+    void* xp = nullptr;               // [rows][H] fp16 x * 2^a (8-element blocks permuted)
+    void* hp = nullptr;               // [rows][I] fp16 SwiGLU outputs * 2^z (same block permutation)
     float* yp = nullptr;              // [rows][H] fp32 expert outputs (unweighted)
+    float* h32 = nullptr;             // [rows][I] fp32 SwiGLU outputs * 2^(2a) (gate/up epilogue)
+    int32_t* xexp = nullptr;          // [T] token activation exponents a
+    int32_t* rexp = nullptr;          // [rows] a of each permuted row's token
+    unsigned* hmax = nullptr;         // [rows] max |h32| of each row (float bits)
+    int32_t* zexp = nullptr;          // [rows] z of each row: hp = h * 2^z
     int max_rows = 0;
     // TMA descriptors: gate/up codes, gate/up meta, down codes, down meta, then
     // xp and hp with boxes of 16, 32, 64 and 128 token rows; on streamed layers
@@ -140,10 +145,10 @@ enum KernelKind {
     K_PF_PERMUTE,
     K_PF_GATHER,
     K_PF_GEMM_GU,
+    K_PF_HCONV,
     K_PF_GEMM_DOWN,
     K_PF_COMBINE,
     K_CACHE_FILL,
-    K_DECODE_FUSED,
     K_NUM_KINDS
 };
 
@@ -173,9 +178,10 @@ struct Layer {
     float* logits = nullptr;        // [max_tokens][E]
     int32_t* ids = nullptr;         // [max_tokens][k]
     float* wts = nullptr;           // [max_tokens][k]
-    float* h = nullptr;             // staged SwiGLU outputs: h_copies replicas of the q16 block
-    int h_copies = 1;
-    unsigned* counters = nullptr;   // [8] last-block counters, kept at zero between launches
+    float* h = nullptr;             // SwiGLU outputs [k + 1][I] fp32 (times 2^2a, the token scale)
+    uint8_t* hq = nullptr;          // kDecodeHCopies staged blocks of them (16-bit fixed point per half-group)
+    unsigned* hg_cnt = nullptr;     // [k + 1][I / 32] rows done per half-group (zero between launches)
+    unsigned* counters = nullptr;   // [64] counters and words of the decode kernels (CNT_*)
     int router_splits = 1;       // split-K of the one-token router
     int router_splits_tok = 1;   // split-K of the multi-token router (<= 16)
 
@@ -201,43 +207,71 @@ struct Layer {
     int host_timeout_ms = 30000;
     int test_stall_copies_ms = 0;
 
-    // fused single-kernel decode (decode_fused.cu)
-    bool fused_ok = false;
-    int decode_path = MOE_PATH_AUTO;
     int wbits = 4;   // expert code width: 4 (MOE_W_Q4G64) or 2 (MOE_W_Q2G64)
-    int test_no_publish = 0;
-    unsigned long long* trace = nullptr;  // device [num_sms][MOE_TRACE_POINTS] when tracing is on
+    int test_stall_shared = 0;   // MOE_OPT_TEST_STALL_SHARED
     unsigned long long* trace_split = nullptr;  // device [MOE_TRACE_KERNELS][MOE_TRACE_MAX_CTAS][4]
     bool trace_on = false;
     unsigned long long* split_trace(int kernel) const {
         return (trace_on && trace_split) ? trace_split + (size_t)kernel * MOE_TRACE_MAX_CTAS * 4 : nullptr;
     }
-    size_t fused_smem = 0;
-    alignas(16) unsigned char fused_params[512];
 };
+
+// Words of Layer::counters. The counters are zero between launches.
+enum {
+    CNT_ROUTER = 0,        // router blocks done (the last one selects), moe_route / streamed layers
+    CNT_SHARED_DONE = 1,   // decode gate/up CTAs whose shared-expert rows are written
+    CNT_DOWN_DONE = 2,     // decode down CTAs done (the last one clears the decode counters)
+    CNT_IDS_READY = 3,     // the router's selecting block has published the selection (decode)
+    CNT_TOKEN_SCALE = 8,   // the token exponent a of the last decode (int)
+    CNT_ERR = 20           // error bits of bounded device waits (moe_layer_check)
+};
+inline unsigned* error_word(Layer& L) { return L.counters + CNT_ERR; }
 
 // ---- launchers (decode.cu / prefill.cu) -----------------------------------------
 
 // ids_pub / seq_pub (host-mapped, nullable): with select, the ids are also
 // written there and then seq, for a host that polls instead of copying
 // dc (nullable): the selecting block also runs the device-managed cache's LFU step
+// Scratch one decode token works on: the router's outputs (partials, keys,
+// selection, and the ready flag the decode's gate/up waits for), the SwiGLU
+// outputs, their half-group counters and staged blocks, and the counters the
+// down kernel's early start uses (null: no early start).
+struct DecodeScratch {
+    float* part = nullptr;
+    float* logits = nullptr;
+    int32_t* ids = nullptr;
+    float* wts = nullptr;
+    int* scale = nullptr;
+    unsigned* router_cnt = nullptr;
+    unsigned* ids_ready = nullptr;
+    float* h = nullptr;
+    unsigned* hg_cnt = nullptr;
+    uint8_t* hq = nullptr;
+    int copies = 1;
+    unsigned* shared_done = nullptr;
+    unsigned* down_done = nullptr;
+};
+// the layer's own scratch; `fast`: with the ready flag and the early start
+DecodeScratch layer_decode_scratch(Layer& L, bool fast);
+size_t decode_hq_block_bytes(int ns, int I);   // bytes of one staged block
+
+// out (nullable): where the partials, keys and selection go (default: the
+// layer's scratch, no ready flag)
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select, int32_t* ids_pub = nullptr,
-                                unsigned* seq_pub = nullptr, unsigned seq = 0, const DevCacheArgs* dc = nullptr);
-cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s);
-cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s);
+                                unsigned* seq_pub = nullptr, unsigned seq = 0, const DevCacheArgs* dc = nullptr,
+                                const DecodeScratch* out = nullptr);
+// xexp (nullable): each token's activation exponent for a prefill chunk
+cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s, int32_t* xexp = nullptr);
 // pdl: both launches may start early (the preceding kernel in `s` must be ours)
-cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, const int32_t* ids,
-                                      const float* wts, int jj0, int jj1, bool down, cudaStream_t s, bool pdl = false);
-// staged SwiGLU output block (q16 runs, inverse scales, sums) of ns slots
-inline size_t hq_block_bytes_host(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
+cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y_f32, int jj0, int jj1, bool down,
+                                      cudaStream_t s, bool pdl = false);
 // K-splits of the prefill router GEMM: at most this many partial logit sets
 // are summed (in a fixed order) per token.
 constexpr int kMaxTokSplits = 32;
-constexpr int kHCopies = 16;   // replicas of that block the decode kernels use
-cudaError_t launch_experts_decode_scratch(Layer& L, const void* x, void* y, float* y_f32, const float* part,
-                                          float* logits, int32_t* ids, float* wts, float* h, cudaStream_t s);
-cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, int which,
-                                  cudaStream_t s);
+constexpr int kDecodeHCopies = 8;   // replicas of the decode SwiGLU outputs (decode.cu)
+// gate/up over row-order slots jj0..jj1-1 and (down) the down kernel, over scratch b
+cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, const DecodeScratch& b, int jj0,
+                                  int jj1, bool down, bool pdl, bool trace, cudaStream_t s);
 cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32, cudaStream_t s);
 cudaError_t decode_kernel_setup(Layer& L);
 cudaError_t router_kernel_setup(Layer& L);
@@ -261,17 +295,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
-bool fused_setup(Layer& L);
-cudaError_t launch_decode_fused(Layer& L, const void* x, void* y, float* y_f32, cudaStream_t s);
-unsigned* fused_error_word(Layer& L);
 
 // Event marks around a launch; no-ops unless profiling was started.
 void prof_begin(Layer& L, int kind, cudaStream_t s);
 void prof_end(Layer& L, cudaStream_t s);
 void prof_destroy(Layer& L);
 
-// which-mask for launch_experts_decode
-enum { RUN_SHARED_GU = 1, RUN_ROUTED_GU = 2, RUN_DOWN = 4, RUN_ALL = 7 };
 
 // ---- streamed cache (cache.cu) ---------------------------------------------------
 

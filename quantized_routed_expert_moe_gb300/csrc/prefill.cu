@@ -135,12 +135,19 @@ __global__ void __launch_bounds__(kPermThreads) k_pf_permute(const int32_t* __re
 
 __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, int x_bf16,
                                                    const int32_t* __restrict__ perm_token, int rows, int H,
-                                                   uint4* __restrict__ xp) {
+                                                   const int32_t* __restrict__ xexp, uint4* __restrict__ xp,
+                                                   int32_t* __restrict__ rexp, unsigned* __restrict__ hmax) {
     const int nb = H / 8;
     const long total = (long)rows * nb;
     for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
         const int row = (int)(idx / nb), blk = (int)(idx - (long)row * nb);
         const int t = __ldg(perm_token + row);
+        const int a = __ldg(xexp + t);   // the token's exponent: x * 2^a in binary16 without overflow
+        if (blk == 0) {
+            rexp[row] = a;
+            hmax[row] = 0u;   // the gate/up epilogue accumulates the row's max |h| here
+        }
+        const float sc = exp2i(a);
         float v[8];
         if (x_bf16) {
             const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + (size_t)t * H) + blk);
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(256) k_pf_gather(const void* __restrict__ x, i
         uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {   // position 2q holds element q, 2q + 1 holds element q + 4
-            const __half2 h = __floats2half2_rn(v[q], v[q + 4]);
+            const __half2 h = __floats2half2_rn(v[q] * sc, v[q + 4] * sc);
             o[q] = *reinterpret_cast<const uint32_t*>(&h);
         }
         xp[idx] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -208,6 +215,8 @@ constexpr int kTmaWarp = kEpiWarps + kDqWarps, kTokWarp = kTmaWarp + 1, kMmaWarp
 constexpr int kGemmThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kB16 = 128 * 128;
 constexpr uint32_t kRawCodes = 128 * 128, kRawMeta = 128 * 16, kRaw = kRawCodes + kRawMeta;
+// 2-bit codes: a raw block is 128 rows x 64 bytes (64-byte swizzle), then the same meta
+constexpr uint32_t kRawCodes2 = 128 * 64, kRaw2Tx = kRawCodes2 + kRawMeta;
 constexpr uint32_t kTmemCols = 512, kTmemA = 256, kACols = 32;
 constexpr size_t kBarBytes = 8 * (2 * kStages + 2 * kRawStages + 4) + 16;
 constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kB16 + (size_t)kRawStages * kRaw + kBarBytes;
@@ -222,8 +231,11 @@ struct GemmArgs {
     int K;          // reduction length (H for gate/up, I for down)
     int n_mt;       // 128-row weight tiles per expert
     int rows_out;   // weight rows that exist (2I or H)
-    void* out;      // gate/up: fp16 [rows][I]; down: fp32 [rows][H]
+    void* out;      // gate/up: fp32 h * 2^(2a) [rows][I]; down: fp32 [rows][H]
     int ld_out;
+    const int32_t* rexp;   // gate/up: each permuted row's activation exponent a
+    unsigned* hmax;        // gate/up: each row's max |h * 2^(2a)| (float bits)
+    const int32_t* zexp;   // down: each row's operand exponent z (h * 2^z in binary16)
     unsigned* err;
     unsigned long long* tr;   // [gridDim][4]: wait cycles of copy / dequant / MMA, total cycles; or null
 };
@@ -270,7 +282,23 @@ __device__ __forceinline__ uint32_t dq_pair_hi(uint32_t t, uint32_t s2, uint32_t
     return r;
 }
 
-template <int MODE>
+// fp16 pair from two 2-bit codes at bits F..F+1 and 16+F..17+F of t: code * s
+// + b. The code lands in mantissa bits F..F+1 of a power of two whose unit in
+// the last place is 2^-F (1024.0, 256.0, 64.0, 16.0 for F = 0, 2, 4, 6), where
+// it weighs 1, so subtracting the power of two leaves the code exactly.
+template <int F>
+__device__ __forceinline__ uint32_t dq2_pair(uint32_t t, uint32_t s2, uint32_t b2) {
+    constexpr uint32_t mask = 0x00030003u << F;
+    constexpr uint32_t base = F == 0 ? 0x64006400u : F == 2 ? 0x5C005C00u : F == 4 ? 0x54005400u : 0x4C004C00u;
+    uint32_t r;
+    asm("{.reg .b32 c; lop3.b32 c, %1, %4, %5, 0xEA;"   // (t & mask) | base
+        " sub.f16x2 c, c, %6; fma.rn.f16x2 %0, c, %2, %3;}"
+        : "=r"(r)
+        : "r"(t), "r"(s2), "r"(b2), "n"(mask), "n"(base), "r"(base));
+    return r;
+}
+
+template <int MODE, int BITS>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_constant__ CUtensorMap tm_codes,
                                                              const __grid_constant__ CUtensorMap tm_meta,
                                                              const __grid_constant__ CUtensorMap tm_b16,
@@ -334,10 +362,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 const uint32_t rs = rit % kRawStages;
                 tw(b_rempty + 8 * rs, ((rit / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
                 if (elect_one()) {
-                    mbar_arrive_tx(b_rfull + 8 * rs, kRaw);
+                    mbar_arrive_tx(b_rfull + 8 * rs, BITS == 4 ? kRaw : kRaw2Tx);
                     const uint32_t rd = saddr(raw + rs * kRaw);
-                    tma_load_3d(rd, &tm_codes, kb * 128, mt * 128, e, b_rfull + 8 * rs, pol_w);
-                    tma_load_3d(rd + kRawCodes, &tm_meta, a.K / 2 + kb * 16, mt * 128, e, b_rfull + 8 * rs, pol_w);
+                    // a block: 4 chunks of 64 codes per row (128 or 64 bytes), then their meta
+                    tma_load_3d(rd, &tm_codes, kb * (BITS == 4 ? 128 : 64), mt * 128, e, b_rfull + 8 * rs, pol_w);
+                    tma_load_3d(rd + kRawCodes, &tm_meta, a.K * BITS / 8 + kb * 16, mt * 128, e, b_rfull + 8 * rs,
+                                pol_w);
                 }
                 __syncwarp();
             }
@@ -382,10 +412,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
         // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows) and
-        // part pt of each chunk's K (16 elements: columns 8 pt .. 8 pt + 7)
+        // part pt: 4-bit codes, 16 elements of every chunk's K (columns 8 pt ..
+        // 8 pt + 7 of each chunk); 2-bit codes, the whole of chunk pt
         const int dw = warp - kEpiWarps, q = dw & 3, pt = dw >> 2;
         const int r = 32 * q + lane;
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemA + 8 * pt;
+        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kTmemA + 8 * pt;   // 4-bit: K part pt
+        const uint32_t ta2 = tmem + ((uint32_t)(32 * q) << 16) + kTmemA;            // 2-bit: whole chunks
         uint32_t rit = 0;
         for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
             for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
@@ -397,37 +429,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 const uint8_t* rw = raw + rs * kRaw;
                 const uint4 mq = *reinterpret_cast<const uint4*>(rw + kRawCodes + r * 16);
                 const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
-                uint2 cw[kChunksPerRaw];
-#pragma unroll
-                for (int c = 0; c < kChunksPerRaw; ++c) {
-                    // bytes 8 pt .. 8 pt + 7 of chunk c (16-byte unit 2c + pt / 2),
-                    // at their 128-byte-swizzled place
-                    const int u = (c << 1) | (pt >> 1);
-                    cw[c] = *reinterpret_cast<const uint2*>(rw + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (pt & 1));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_rempty + 8 * rs);
+                // 4-bit: o[c] = this warp's 8 columns (K part pt) of chunk c;
+                // 2-bit: o[w] = columns 8w .. 8w + 7 of chunk pt (the warp's chunk)
                 uint32_t o[kChunksPerRaw][8];
+                if constexpr (BITS == 4) {
+                    uint2 cw[kChunksPerRaw];
 #pragma unroll
-                for (int c = 0; c < kChunksPerRaw; ++c) {
-                    const uint32_t mw = u4w(mq, c);
+                    for (int c = 0; c < kChunksPerRaw; ++c) {
+                        // bytes 8 pt .. 8 pt + 7 of chunk c (16-byte unit 2c + pt / 2),
+                        // at their 128-byte-swizzled place
+                        const int u = (c << 1) | (pt >> 1);
+                        cw[c] = *reinterpret_cast<const uint2*>(rw + r * 128 + ((u ^ (r & 7)) << 4) + 8 * (pt & 1));
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_rempty + 8 * rs);
+#pragma unroll
+                    for (int c = 0; c < kChunksPerRaw; ++c) {
+                        const uint32_t mw = u4w(mq, c);
+                        const uint32_t s2 = __byte_perm(mw, 0, 0x1010), b2 = __byte_perm(mw, 0, 0x3232);
+                        const uint32_t vw[2] = {cw[c].x, cw[c].y};
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t v = vw[j], v8 = v >> 8;
+                            o[c][4 * j + 0] = dq_pair(v, s2, b2);
+                            o[c][4 * j + 1] = dq_pair_hi(v, s2, b2);
+                            o[c][4 * j + 2] = dq_pair(v8, s2, b2);
+                            o[c][4 * j + 3] = dq_pair_hi(v8, s2, b2);
+                        }
+                    }
+                } else {
+                    // the 16 bytes of chunk pt (64 codes), at their 64-byte-swizzled
+                    // place: 16-byte unit pt of row r is unit pt ^ ((r / 2) % 4)
+                    const uint4 cw = *reinterpret_cast<const uint4*>(rw + r * 64 + ((pt ^ ((r >> 1) & 3)) << 4));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_rempty + 8 * rs);
+                    const uint32_t mw = u4w(mq, pt);
                     const uint32_t s2 = __byte_perm(mw, 0, 0x1010), b2 = __byte_perm(mw, 0, 0x3232);
-                    const uint32_t vw[2] = {cw[c].x, cw[c].y};
+                    // word w holds codes 16w .. 16w + 15: byte i carries codes 2i, 2i + 1,
+                    // 8 + 2i, 9 + 2i at bits 0, 2, 4, 6 (the 2-bit kernel layout), so the
+                    // pairs (j, j + 4) of each block of 8 come out of one mask each
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint32_t v = vw[j], v8 = v >> 8;
-                        o[c][4 * j + 0] = dq_pair(v, s2, b2);
-                        o[c][4 * j + 1] = dq_pair_hi(v, s2, b2);
-                        o[c][4 * j + 2] = dq_pair(v8, s2, b2);
-                        o[c][4 * j + 3] = dq_pair_hi(v8, s2, b2);
+                    for (int w = 0; w < 4; ++w) {
+                        const uint32_t v = u4w(cw, w), v8 = v >> 8;
+                        o[w][0] = dq2_pair<0>(v, s2, b2);    // codes 0, 4
+                        o[w][1] = dq2_pair<2>(v, s2, b2);    // 1, 5
+                        o[w][2] = dq2_pair<0>(v8, s2, b2);   // 2, 6
+                        o[w][3] = dq2_pair<2>(v8, s2, b2);   // 3, 7
+                        o[w][4] = dq2_pair<4>(v, s2, b2);    // 8, 12
+                        o[w][5] = dq2_pair<6>(v, s2, b2);    // 9, 13
+                        o[w][6] = dq2_pair<4>(v8, s2, b2);   // 10, 14
+                        o[w][7] = dq2_pair<6>(v8, s2, b2);   // 11, 15
                     }
                 }
                 const uint32_t bs = rit % kBatchSlots;
                 tw(b_empty + 8 * bs, ((rit / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_DQ);
                 tc_fence_after();
+                if constexpr (BITS == 4) {
 #pragma unroll
-                for (int c = 0; c < kChunksPerRaw; ++c)
-                    if (c < nc) tmem_st8(ta + (bs * kChunksPerRaw + c) * kACols, o[c]);
+                    for (int c = 0; c < kChunksPerRaw; ++c)
+                        if (c < nc) tmem_st8(ta + (bs * kChunksPerRaw + c) * kACols, o[c]);
+                } else if (pt < nc) {   // warp-uniform
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) tmem_st8(ta2 + (bs * kChunksPerRaw + pt) * kACols + 8 * w, o[w]);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -491,27 +555,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 if (MODE == 0) {
                     // lanes 2p and 2p + 1 hold gate and up of pair i for these 16
                     // tokens; the even lane finishes the even tokens and the odd
-                    // lane the odd ones, after one exchange per token pair
+                    // lane the odd ones, after one exchange per token pair. The
+                    // products come out times 2^a (the token's scale), so
+                    // g * u * sigmoid(g 2^-a) is h * 2^(2a); the row's max |h|
+                    // goes to hmax for the conversion to binary16.
                     const int i = mt * 64 + (row >> 1);
-                    const int ip = (i & ~7) | blk_pos(i & 7);
                     const bool odd = row & 1;
-                    __half* hp = static_cast<__half*>(a.out) + ip;
+                    float* hp = static_cast<float*>(a.out) + i;
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float got = __shfl_xor_sync(0xffffffffu, odd ? v[2 * q] : v[2 * q + 1], 1);
                         const float g = odd ? got : v[2 * q], u = odd ? v[2 * q + 1] : got;
                         const int col = c0 + 2 * q + (odd ? 1 : 0);
-                        // fp16 result: the fast exponential and division are well inside its rounding
-                        const float h = __fdividef(g, 1.0f + __expf(-g)) * u;
-                        if (col < m) hp[(size_t)(off + col) * a.ld_out] = __float2half_rn(h);
+                        uint32_t mb = 0u;
+                        if (col < m) {
+                            const int prow = off + col;
+                            const float gt = g * exp2i(-__ldg(a.rexp + prow));
+                            // the fast exponential and division are far inside the
+                            // binary16 rounding the value gets next
+                            const float h = g * u * __fdividef(1.0f, 1.0f + __expf(-gt));
+                            hp[(size_t)prow * a.ld_out] = h;
+                            mb = __float_as_uint(h) & 0x7fffffffu;
+                        }
+                        // max over the warp's 16 pairs, even and odd tokens apart
+                        const uint32_t me = __reduce_max_sync(0xffffffffu, odd ? 0u : mb);
+                        const uint32_t mo = __reduce_max_sync(0xffffffffu, odd ? mb : 0u);
+                        if (lane < 2 && col < m) atomicMax(a.hmax + off + col, lane ? mo : me);
                     }
                 } else {
+                    // the operand was h * 2^z: scale back exactly (one rounding
+                    // only if the result is subnormal)
                     const int n = mt * 128 + row;
                     float* yp = static_cast<float*>(a.out);
                     if (n < a.rows_out) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (c0 + j < m) yp[(size_t)(off + c0 + j) * a.ld_out + n] = v[j];
+                            if (c0 + j < m)
+                                yp[(size_t)(off + c0 + j) * a.ld_out + n] = ldexpf(v[j], -__ldg(a.zexp + off + c0 + j));
                     }
                 }
             }
@@ -526,6 +606,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU outputs to the down GEMM's binary16 operand
+// ---------------------------------------------------------------------------
+//
+// Row r of the listed groups: hp[r] = fp16(h32[r] * 2^e_r) in the
+// dequantiser's order within each block of 8, e_r from the row's max |h32|
+// (fp16_fit_exp), and z_r = e_r + 2 a_r, so that hp[r] = h * 2^z_r. Grid
+// (groups of the list, blocks per group); a CTA past the list's group count
+// does nothing.
+__global__ void __launch_bounds__(256) k_pf_hconv(const float* __restrict__ h32, const unsigned* __restrict__ hmax,
+                                                  const int32_t* __restrict__ rexp, const int32_t* __restrict__ goff,
+                                                  const int32_t* __restrict__ gcnt, const int32_t* __restrict__ n_groups,
+                                                  int I, uint4* __restrict__ hp, int32_t* __restrict__ zexp) {
+    const int g = blockIdx.x;
+    if (g >= *n_groups) return;
+    const int off = goff[g], cnt = gcnt[g], nb = I / 8;
+    for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < cnt * nb; idx += gridDim.y * blockDim.x) {
+        const int r = off + idx / nb, b = idx - (idx / nb) * nb;
+        const int e = fp16_fit_exp(__uint_as_float(__ldcg(hmax + r)));
+        const float sc = exp2i(e);
+        const float4* src = reinterpret_cast<const float4*>(h32 + (size_t)r * I + 8 * b);
+        const float4 p = __ldcg(src), q = __ldcg(src + 1);
+        const float v[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // position 2j holds element j, 2j + 1 holds element j + 4
+            const __half2 h = __floats2half2_rn(v[j] * sc, v[j + 4] * sc);
+            o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        hp[(size_t)r * nb + b] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (b == 0) zexp[r] = e + 2 * rexp[r];
     }
 }
 
@@ -611,26 +725,38 @@ bool map_act(CUtensorMap* tm, void* base, int K, int rows, uint32_t box_rows) {
 
 }  // namespace
 
+// The four weight maps of a set of records (gate/up codes, gate/up meta, down
+// codes, down meta): rows of the record layout, one plane per record. A raw
+// block of codes is 4 chunks of 64 codes per row: 128 bytes with the 128-byte
+// swizzle (4-bit) or 64 bytes with the 64-byte swizzle (2-bit).
+static bool map_weights(const Layer& L, CUtensorMap* tm, const uint8_t* recs_base, int recs) {
+    const int H = L.d.hidden, I = L.d.inter, b = L.wbits;
+    const uint8_t* gu = recs_base;
+    const uint8_t* dn = recs_base + gu_block_bytes(H, I, b);
+    const auto SW = b == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const auto NS = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const uint32_t bx = b == 4 ? 128 : 64;
+    return map_weight_rows(&tm[0], gu, row_bytes(H, b), 2 * I, recs, L.rec_bytes, bx, SW) &&
+           map_weight_rows(&tm[1], gu, row_bytes(H, b), 2 * I, recs, L.rec_bytes, 16, NS) &&
+           map_weight_rows(&tm[2], dn, row_bytes(I, b), H, recs, L.rec_bytes, bx, SW) &&
+           map_weight_rows(&tm[3], dn, row_bytes(I, b), H, recs, L.rec_bytes, 16, NS);
+}
+
 cudaError_t prefill_kernel_setup(Layer& L) {
     const auto& d = L.d;
     if (!L.pf.xp) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k_pf_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    const auto g0 = L.wbits == 4 ? k_pf_gemm<0, 4> : k_pf_gemm<0, 2>;
+    const auto g1 = L.wbits == 4 ? k_pf_gemm<1, 4> : k_pf_gemm<1, 2>;
+    cudaError_t e = cudaFuncSetAttribute(g0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_pf_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    e = cudaFuncSetAttribute(g1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
     if (e != cudaSuccess) return e;
     if (!encoder()) return cudaErrorSymbolNotFound;
     const int H = d.hidden, I = d.inter;
     // device records: every expert and the shared one (resident layers), or
     // the shared one alone (streamed layers: routed experts live in the cache slots)
     const int recs = d.cache_slots > 0 ? d.n_shared : d.n_experts + d.n_shared;
-    const uint8_t* gu = L.experts;
-    const uint8_t* dn = L.experts + gu_block_bytes(H, I);
-    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
-    bool ok = recs == 0 ||
-              (map_weight_rows(&L.pf.tm[0], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 128, SW) &&
-               map_weight_rows(&L.pf.tm[1], gu, row_bytes(H), 2 * I, recs, L.rec_bytes, 16, NS) &&
-               map_weight_rows(&L.pf.tm[2], dn, row_bytes(I), H, recs, L.rec_bytes, 128, SW) &&
-               map_weight_rows(&L.pf.tm[3], dn, row_bytes(I), H, recs, L.rec_bytes, 16, NS));
+    bool ok = recs == 0 || map_weights(L, &L.pf.tm[0], L.experts, recs);
     for (int j = 0; j < 4 && ok; ++j)   // token boxes of 16, 32, 64 and 128 rows
         ok = map_act(&L.pf.tm[4 + j], L.pf.xp, H, L.pf.max_rows, 16u << j) &&
              map_act(&L.pf.tm[8 + j], L.pf.hp, I, L.pf.max_rows, 16u << j);
@@ -643,16 +769,9 @@ moe_status prefill_cache_maps(Layer& L) {
     const auto& d = L.d;
     auto& pf = L.pf;
     if (!pf.xp) return MOE_OK;
-    const int H = d.hidden, I = d.inter;
     const uint8_t* slots = cache_slots_base(L);
     const int n = cache_slot_count(L);   // LFU slots, then pinned experts
-    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B, NS = CU_TENSOR_MAP_SWIZZLE_NONE;
-    const uint8_t* dn = slots + gu_block_bytes(H, I);
-    const bool ok = map_weight_rows(&pf.tm[12], slots, row_bytes(H), 2 * I, n, L.rec_bytes, 128, SW) &&
-                    map_weight_rows(&pf.tm[13], slots, row_bytes(H), 2 * I, n, L.rec_bytes, 16, NS) &&
-                    map_weight_rows(&pf.tm[14], dn, row_bytes(I), H, n, L.rec_bytes, 128, SW) &&
-                    map_weight_rows(&pf.tm[15], dn, row_bytes(I), H, n, L.rec_bytes, 16, NS);
-    if (!ok) return fail(MOE_E_CUDA, "tensor maps over the cache slots");
+    if (!map_weights(L, &pf.tm[12], slots, n)) return fail(MOE_E_CUDA, "tensor maps over the cache slots");
     return MOE_OK;
 }
 
@@ -691,7 +810,8 @@ cudaError_t launch_permute_gather(Layer& L, const void* x, int T, cudaStream_t s
     prof_begin(L, K_PF_GATHER, s);
     const long blocks = ((long)rows * (H / 8) + 255) / 256;
     k_pf_gather<<<(int)std::min<long>(blocks, (long)L.num_sms * 8), 256, 0, s>>>(
-        x, d.act_dtype == MOE_BF16 ? 1 : 0, pf.perm_token, rows, H, static_cast<uint4*>(pf.xp));
+        x, d.act_dtype == MOE_BF16 ? 1 : 0, pf.perm_token, rows, H, pf.xexp, static_cast<uint4*>(pf.xp), pf.rexp,
+        pf.hmax);
     prof_end(L, s);
     return cudaGetLastError();
 }
@@ -704,17 +824,25 @@ cudaError_t launch_gemm_pair(Layer& L, int wmap, const int32_t* gexp, const int3
     const auto& d = L.d;
     const int H = d.hidden, I = d.inter;
     auto& pf = L.pf;
-    GemmArgs gu{gexp, goff, gcnt, n_groups, H, I / 64, 2 * I, pf.hp, I, pf.err, L.split_trace(3)};
+    GemmArgs gu{gexp, goff, gcnt, n_groups, H, I / 64, 2 * I, pf.h32, I, pf.rexp, pf.hmax, nullptr, pf.err,
+                L.split_trace(3)};
     prof_begin(L, K_PF_GEMM_GU, s);
-    k_pf_gemm<0><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[wmap + 0], pf.tm[wmap + 1], pf.tm[4], pf.tm[5],
-                                                             pf.tm[6], pf.tm[7], gu);
+    (L.wbits == 4 ? k_pf_gemm<0, 4> : k_pf_gemm<0, 2>)<<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(
+        pf.tm[wmap + 0], pf.tm[wmap + 1], pf.tm[4], pf.tm[5], pf.tm[6], pf.tm[7], gu);
     prof_end(L, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    GemmArgs dn{gexp, goff, gcnt, n_groups, I, (H + 127) / 128, H, pf.yp, H, pf.err, L.split_trace(4)};
+    prof_begin(L, K_PF_HCONV, s);
+    k_pf_hconv<<<dim3(d.n_experts + 1, 8), 256, 0, s>>>(pf.h32, pf.hmax, pf.rexp, goff, gcnt, n_groups, I,
+                                                         static_cast<uint4*>(pf.hp), pf.zexp);
+    prof_end(L, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    GemmArgs dn{gexp, goff, gcnt, n_groups, I, (H + 127) / 128, H, pf.yp, H, nullptr, nullptr, pf.zexp, pf.err,
+                L.split_trace(4)};
     prof_begin(L, K_PF_GEMM_DOWN, s);
-    k_pf_gemm<1><<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(pf.tm[wmap + 2], pf.tm[wmap + 3], pf.tm[8], pf.tm[9],
-                                                             pf.tm[10], pf.tm[11], dn);
+    (L.wbits == 4 ? k_pf_gemm<1, 4> : k_pf_gemm<1, 2>)<<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(
+        pf.tm[wmap + 2], pf.tm[wmap + 3], pf.tm[8], pf.tm[9], pf.tm[10], pf.tm[11], dn);
     prof_end(L, s);
     return cudaGetLastError();
 }

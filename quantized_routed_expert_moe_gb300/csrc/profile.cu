@@ -8,8 +8,8 @@ namespace moe {
 
 static const char* kKindNames[K_NUM_KINDS] = {
     "router_decode", "router_tokens", "topk_tokens", "gateup_decode", "down_decode",
-    "prefill_permute", "prefill_gather", "prefill_gemm_gateup", "prefill_gemm_down", "prefill_combine",
-    "cache_fill", "decode_fused"};
+    "prefill_permute", "prefill_gather", "prefill_gemm_gateup", "prefill_hconv", "prefill_gemm_down", "prefill_combine",
+    "cache_fill"};
 
 struct Profiler {
     bool on = false;

@@ -110,13 +110,79 @@ __device__ void dev_lfu_access(const DevCacheArgs& dc, const int32_t* ids_g, int
     dc.stats[3] += (unsigned long long)nf * dc.rb;
 }
 
+// Dot product of router row e with the activation slice [k0, k0 + Ls) staged
+// as fp32 in xs_slice, by one warp; every lane returns the warp's sum. Fp32
+// rows: 8 float4 loads in flight per lane. Q8 rows: 16 codes per load, each
+// summed as scale * sum(q * x) + bias * sum(x) per 16 inputs of a group of 64.
+template <bool Q8>
+__device__ __forceinline__ float router_warp_dot(const void* __restrict__ W, const float* xs_slice, int H, int E,
+                                                 int e, int k0, int Ls) {
+    const int lane = threadIdx.x & 31;
+    float acc = 0.f;
+    if (!Q8) {
+        const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(W) + (size_t)e * H + k0);
+        const float4* xs = reinterpret_cast<const float4*>(xs_slice);
+        for (int c0 = lane; c0 < Ls / 4; c0 += 32 * 8) {
+            float4 wv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {   // 8 loads in flight per lane
+                const int c = c0 + 32 * u;
+                wv[u] = (c < Ls / 4) ? __ldg(row + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + 32 * u;
+                if (c < Ls / 4) {
+                    const float4 xv = xs[c];
+                    acc = fmaf(wv[u].x, xv.x, acc);
+                    acc = fmaf(wv[u].y, xv.y, acc);
+                    acc = fmaf(wv[u].z, xv.z, acc);
+                    acc = fmaf(wv[u].w, xv.w, acc);
+                }
+            }
+        }
+    } else {
+        const uint8_t* codes = static_cast<const uint8_t*>(W) + (size_t)e * H + k0;
+        const uint32_t* meta = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(W) + (size_t)E * H) +
+                               (size_t)e * (H / 64) + k0 / 64;
+        for (int c0 = lane; c0 < Ls / 16; c0 += 32 * 4) {
+            uint4 qv[4];
+            uint32_t mv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + 32 * u;
+                qv[u] = (c < Ls / 16) ? ldg_stream(codes + 16 * c) : make_uint4(0u, 0u, 0u, 0u);
+                mv[u] = (c < Ls / 16) ? __ldg(meta + (c >> 2)) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + 32 * u;
+                if (c < Ls / 16) {
+                    const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+                    float aq = 0.f, ax = 0.f;
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const float xv = xs_slice[16 * c + t];
+                        aq = fmaf(__uint_as_float(0x4B000000u | ((qw[t >> 2] >> (8 * (t & 3))) & 0xFFu)) - 8388608.0f,
+                                  xv, aq);
+                        ax += xv;
+                    }
+                    const float2 sb = meta_to_f2(mv[u]);
+                    acc = fmaf(sb.x, aq, fmaf(sb.y, ax, acc));
+                }
+            }
+        }
+    }
+    return warp_sum(acc);
+}
+
 template <bool Q8>
 __global__ void __launch_bounds__(kThreads) k_router_decode(
     const void* __restrict__ W, const void* __restrict__ x, int x_bf16, int H, int E, int splits,
     const float* __restrict__ bias, float* __restrict__ part, float* __restrict__ logits,
     int32_t* __restrict__ ids, float* __restrict__ wts, int k, unsigned* __restrict__ counter,
     int select, RouteMode mode, int32_t* ids_pub, unsigned* seq_pub, unsigned seq, DevCacheArgs dc,
-    unsigned long long* __restrict__ tr) {
+    unsigned* ids_ready, unsigned* hg_clear, int n_clear, unsigned long long* __restrict__ tr) {
     extern __shared__ float sm[];
     __shared__ unsigned s_last;
     const int cta = blockIdx.y * gridDim.x + blockIdx.x;
@@ -133,6 +199,14 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
     }
     pdl_wait();
+    if (hg_clear) {
+        // the decode's half-group counters start at zero (the previous kernel
+        // in the stream has completed; gate/up launches after every CTA's trigger)
+        const int nthr = gridDim.x * gridDim.y * blockDim.x;
+        for (int i = cta * blockDim.x + threadIdx.x; i < n_clear; i += nthr) hg_clear[i] = 0u;
+        __threadfence();
+        __syncthreads();
+    }
     pdl_trigger();
     ktrace(tr, cta, 1);
     for (int i4 = threadIdx.x; i4 < Ls / 4; i4 += blockDim.x) {
@@ -148,67 +222,15 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     }
     __syncthreads();
     if (e < E) {
-        float acc = 0.f;
-        if (!Q8) {
-            const float4* row = reinterpret_cast<const float4*>(static_cast<const float*>(W) + (size_t)e * H + k0);
-            const float4* xs = reinterpret_cast<const float4*>(sm);
-            for (int c0 = lane; c0 < Ls / 4; c0 += 32 * 8) {
-                float4 wv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {   // 8 loads in flight per lane
-                    const int c = c0 + 32 * u;
-                    wv[u] = (c < Ls / 4) ? __ldg(row + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int c = c0 + 32 * u;
-                    if (c < Ls / 4) {
-                        const float4 xv = xs[c];
-                        acc = fmaf(wv[u].x, xv.x, acc);
-                        acc = fmaf(wv[u].y, xv.y, acc);
-                        acc = fmaf(wv[u].z, xv.z, acc);
-                        acc = fmaf(wv[u].w, xv.w, acc);
-                    }
-                }
-            }
-        } else {
-            const uint8_t* codes = static_cast<const uint8_t*>(W) + (size_t)e * H + k0;
-            const uint32_t* meta = reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(W) + (size_t)E * H) +
-                                   (size_t)e * (H / 64) + k0 / 64;
-            for (int c0 = lane; c0 < Ls / 16; c0 += 32 * 4) {
-                uint4 qv[4];
-                uint32_t mv[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c = c0 + 32 * u;
-                    qv[u] = (c < Ls / 16) ? ldg_stream(codes + 16 * c) : make_uint4(0u, 0u, 0u, 0u);
-                    mv[u] = (c < Ls / 16) ? __ldg(meta + (c >> 2)) : 0u;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c = c0 + 32 * u;
-                    if (c < Ls / 16) {
-                        const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
-                        float aq = 0.f, ax = 0.f;
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const float xv = sm[16 * c + t];
-                            aq = fmaf(__uint_as_float(0x4B000000u | ((qw[t >> 2] >> (8 * (t & 3))) & 0xFFu)) - 8388608.0f,
-                                      xv, aq);
-                            ax += xv;
-                        }
-                        const float2 sb = meta_to_f2(mv[u]);
-                        acc = fmaf(sb.x, aq, fmaf(sb.y, ax, acc));
-                    }
-                }
-            }
-        }
-        acc = warp_sum(acc);
+        const float acc = router_warp_dot<Q8>(W, reinterpret_cast<const float*>(sm), H, E, e, k0, Ls);
         if (lane == 0) part[(size_t)blockIdx.y * E + e] = acc;
     }
     __syncthreads();
     ktrace(tr, cta, 2);
-    if (!select) return;   // the decode kernels reduce the partials and select themselves
+    if (!select) {   // partials only
+        ktrace(tr, cta, 3);
+        return;
+    }
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(counter, 1u);
@@ -224,13 +246,20 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
         float l = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s) l += v[s];
-        // keys in sm[0, E), sigmoid scores in sm[E, 2E)
+        // keys in sm[0, E), sigmoid scores in sm[E, 2E), key images after them
         const float key = route_key(l, bias ? bias[e2] : 0.f, mode, sm + E + e2);
         sm[e2] = key;
         logits[e2] = key;
     }
     __syncthreads();
-    block_topk_softmax(sm, E, k, ids, wts, mode.sigmoid ? sm + E : nullptr, mode.scale);
+    block_topk_rank(sm, reinterpret_cast<uint32_t*>(sm + ((2 * E + 3) & ~3)), E, k, ids, wts,
+                    mode.sigmoid ? sm + E : nullptr, mode.scale);
+    // the decode's gate/up waits for this flag instead of the grid's end
+    // (thread 0 wrote the ids and weights)
+    if (threadIdx.x == 0 && ids_ready) {
+        __threadfence();
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ids_ready), "r"(1u) : "memory");
+    }
     // streamed layers: the selection straight into host-mapped memory, then
     // its sequence number (thread 0 wrote the ids itself)
     if (threadIdx.x == 0 && ids_pub) {
@@ -342,12 +371,29 @@ __global__ void __launch_bounds__(kThreads, 2) k_router_tokens(const void* __res
     }
 }
 
+// Prefill chunks also need each token's activation exponent a_t (see
+// fp16_fit_exp): the grouped GEMM's operands are x_t * 2^a_t in binary16.
 __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restrict__ part, int splits, int T, int E,
                                                           const float* __restrict__ bias, float* __restrict__ logits,
                                                           int32_t* __restrict__ ids, float* __restrict__ wts, int k,
-                                                          RouteMode mode) {
+                                                          RouteMode mode, const void* __restrict__ x, int x_bf16,
+                                                          int H, int32_t* __restrict__ xexp) {
     extern __shared__ float sl[];   // keys [E], then sigmoid scores [E]
+    __shared__ float s_red[kWarps];
     const int t = blockIdx.x;
+    if (xexp) {   // the token's activation exponent (prefill chunks)
+        float m = 0.f;
+        for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(load_act(x, x_bf16, (size_t)t * H + i)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float r = 0.f;
+            for (int w = 0; w < kWarps; ++w) r = fmaxf(r, s_red[w]);
+            xexp[t] = fp16_fit_exp(r);
+        }
+    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float v[kMaxTokSplits];
 #pragma unroll
@@ -360,17 +406,20 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
         logits[(size_t)t * E + e] = key;
     }
     __syncthreads();
-    block_topk_softmax(sl, E, k, ids + (size_t)t * k, wts + (size_t)t * k, mode.sigmoid ? sl + E : nullptr,
-                       mode.scale);
+    block_topk_rank(sl, reinterpret_cast<uint32_t*>(sl + ((2 * E + 3) & ~3)), E, k, ids + (size_t)t * k,
+                    wts + (size_t)t * k, mode.sigmoid ? sl + E : nullptr, mode.scale);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 
+// keys [E], scores [E] and key images [round4(E)], 16-byte aligned
+static int select_smem_words(int E) { return ((2 * E + 3) & ~3) + ((E + 3) & ~3); }
+
 static size_t router_smem(const Layer& L) {
-    // x slice, or keys + scores, or a device-managed cache's slot state
-    return (size_t)std::max({L.d.hidden / L.router_splits, 2 * L.d.n_experts, 3 * L.d.cache_slots}) * 4;
+    // x slice, or the selection's arrays, or a device-managed cache's slot state
+    return (size_t)std::max({L.d.hidden / L.router_splits, select_smem_words(L.d.n_experts), 3 * L.d.cache_slots}) * 4;
 }
 
 cudaError_t router_kernel_setup(Layer& L) {
@@ -379,49 +428,35 @@ cudaError_t router_kernel_setup(Layer& L) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_router_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)router_smem(L));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_topk_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * L.d.n_experts * 4);
+    return cudaFuncSetAttribute(k_topk_tokens, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                select_smem_words(L.d.n_experts) * 4);
 }
 
 cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int select, int32_t* ids_pub,
-                                unsigned* seq_pub, unsigned seq, const DevCacheArgs* dc) {
+                                unsigned* seq_pub, unsigned seq, const DevCacheArgs* dc, const DecodeScratch* out) {
     const DevCacheArgs dca = dc ? *dc : DevCacheArgs{};
     const auto& d = L.d;
     dim3 grid((d.n_experts + kWarps - 1) / kWarps, L.router_splits);
     const int xb = d.act_dtype == MOE_BF16;
+    float* part = out ? out->part : L.logits_part;
+    float* logits = out ? out->logits : L.logits;
+    int32_t* ids = out ? out->ids : L.ids;
+    float* wts = out ? out->wts : L.wts;
+    unsigned* cnt = out ? out->router_cnt : L.counters + CNT_ROUTER;
+    unsigned* ready = out ? out->ids_ready : nullptr;
+    unsigned* hgc = out ? out->hg_cnt : L.hg_cnt;
+    const int n_clear = (d.top_k + 1) * (d.inter / 32);
+    auto kern = d.router_fmt == MOE_W_F32 ? k_router_decode<false> : k_router_decode<true>;
     prof_begin(L, K_ROUTER_DECODE, s);
-    cudaError_t e;
-    if (d.router_fmt == MOE_W_F32)
-        e = launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
-                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq, dca,
-                       L.split_trace(0));
-    else
-        e = launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
-                       d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, L.logits_part, L.logits,
-                       L.ids, L.wts, d.top_k, L.counters, select, L.route_mode(), ids_pub, seq_pub, seq, dca,
-                       L.split_trace(0));
+    const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb, d.hidden,
+                                     d.n_experts, L.router_splits, (const float*)L.router_bias, part, logits, ids, wts,
+                                     d.top_k, cnt, select, L.route_mode(), ids_pub, seq_pub, seq, dca, ready, hgc,
+                                     n_clear, L.split_trace(0));
     prof_end(L, s);
     return e;
 }
 
-// Partial logits of one token into caller-given scratch `part` [splits][E]
-// (no selection, no counter, no profiling or tracing).
-cudaError_t launch_route_decode_partials(Layer& L, const void* x, float* part, cudaStream_t s) {
-    const auto& d = L.d;
-    dim3 grid((d.n_experts + kWarps - 1) / kWarps, L.router_splits);
-    const int xb = d.act_dtype == MOE_BF16;
-    if (d.router_fmt == MOE_W_F32)
-        return launch_pdl(k_router_decode<false>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
-                          d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
-                          (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
-                          (int32_t*)nullptr, (unsigned*)nullptr, 0u, DevCacheArgs{}, (unsigned long long*)nullptr);
-    return launch_pdl(k_router_decode<true>, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb,
-                      d.hidden, d.n_experts, L.router_splits, (const float*)L.router_bias, part, (float*)nullptr,
-                      (int32_t*)nullptr, (float*)nullptr, d.top_k, (unsigned*)nullptr, 0, L.route_mode(),
-                      (int32_t*)nullptr, (unsigned*)nullptr, 0u, DevCacheArgs{}, (unsigned long long*)nullptr);
-}
-
-cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) {
+cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s, int32_t* xexp) {
     const auto& d = L.d;
     const int xb = d.act_dtype == MOE_BF16;
     const int splits = L.router_splits_tok;
@@ -438,8 +473,9 @@ cudaError_t launch_route_tokens(Layer& L, const void* x, int T, cudaStream_t s) 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     prof_begin(L, K_TOPK_TOKENS, s);
-    k_topk_tokens<<<T, kThreads, 2 * d.n_experts * 4, s>>>(L.logits_part, splits, T, d.n_experts, L.router_bias,
-                                                           L.logits, L.ids, L.wts, d.top_k, L.route_mode());
+    k_topk_tokens<<<T, kThreads, select_smem_words(d.n_experts) * 4, s>>>(L.logits_part, splits, T, d.n_experts, L.router_bias,
+                                                           L.logits, L.ids, L.wts, d.top_k, L.route_mode(), x, xb,
+                                                           d.hidden, xexp);
     prof_end(L, s);
     return cudaGetLastError();
 }

@@ -40,6 +40,7 @@ TAG_EXPERT_SCALE = 3
 TAG_TOKENS = 4
 TAG_BIAS_PERM = 5
 TAG_SCORE_BIAS = 6
+TAG_OUTLIER_POS = 7
 
 MAT_GATE, MAT_UP, MAT_DOWN = 0, 1, 2
 
@@ -75,6 +76,7 @@ def _load():
             lib.si_fill_normal_f32.argtypes = [u64, u64, dbl, vp]
             lib.si_fill_normal_bf16.argtypes = [u64, u64, dbl, vp]
             lib.si_permutation.argtypes = [u64, i64, vp]
+            lib.si_fill_normal_outliers.argtypes = [u64, u64, u64, u64, dbl, vp, vp]
             lib.si_encode_q8g64.argtypes = [vp, i64, i64, vp, vp, vp]
             lib.si_f64_to_f16.restype = ctypes.c_uint16
             lib.si_f64_to_f16.argtypes = [dbl]
@@ -285,6 +287,31 @@ def gen_tokens(seed: int, t0: int, T: int, spec: LayerSpec) -> np.ndarray:
     if spec.act == "f32":
         return np.stack([normal_f32(key(seed, TAG_TOKENS, t), H, 1.0) for t in range(t0, t0 + T)])
     return np.stack([normal_bf16(key(seed, TAG_TOKENS, t), H, 1.0) for t in range(t0, t0 + T)])
+
+
+def gen_tokens_scaled(seed: int, t0: int, T: int, spec: LayerSpec, sd: float) -> np.ndarray:
+    """Like gen_tokens, with N(0, sd) activations (the same streams times sd,
+    rounded once): sd far from 1 gives tokens of tiny or huge magnitude."""
+    H = spec.hidden
+    if spec.act == "f32":
+        return np.stack([normal_f32(key(seed, TAG_TOKENS, t), H, sd) for t in range(t0, t0 + T)])
+    return np.stack([normal_bf16(key(seed, TAG_TOKENS, t), H, sd) for t in range(t0, t0 + T)])
+
+
+def gen_tokens_outliers(seed: int, t0: int, T: int, spec: LayerSpec, factor: float,
+                        group: int = 32) -> np.ndarray:
+    """Like gen_tokens, with one outlier channel in every run of `group`
+    activations (a seeded position per run, value times `factor`): the wide
+    dynamic range within a run that real activations show."""
+    H = spec.hidden
+    rows = []
+    for t in range(t0, t0 + T):
+        f32 = np.empty(H, np.float32)
+        b16 = np.empty(H, np.uint16)
+        _load().si_fill_normal_outliers(key(seed, TAG_TOKENS, t), key(seed, TAG_OUTLIER_POS, t), H, group,
+                                        float(factor), _ptr(f32), _ptr(b16))
+        rows.append(f32 if spec.act == "f32" else b16)
+    return np.stack(rows)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

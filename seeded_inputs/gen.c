@@ -151,6 +151,23 @@ void si_fill_normal_bf16(uint64_t key, uint64_t n, double sd, uint16_t* out) {
         out[i] = si_f32_to_bf16((float)(sd * si_normal_at(key, (uint64_t)i)));
 }
 
+/* Heavy-tailed activations: Normal(0, 1) draws (stream `key`) in runs of
+ * `group` elements; in every run, the one element at the position drawn from
+ * stream `key_pos` (element r of that stream for run r) is multiplied by
+ * `factor` (an outlier channel per run). Rounded once to float; to bfloat16
+ * as well when out_bf16 is given. */
+void si_fill_normal_outliers(uint64_t key, uint64_t key_pos, uint64_t n, uint64_t group, double factor,
+                             float* out_f32, uint16_t* out_bf16) {
+    for (int64_t i = 0; i < (int64_t)n; ++i) {
+        const uint64_t run = (uint64_t)i / group, at = si_at(key_pos, run) % group;
+        double v = si_normal_at(key, (uint64_t)i);
+        if ((uint64_t)i - run * group == at) v *= factor;
+        const float f = (float)v;
+        if (out_f32) out_f32[i] = f;
+        if (out_bf16) out_bf16[i] = si_f32_to_bf16(f);
+    }
+}
+
 /* Fisher-Yates permutation of 0..n-1 driven by the stream; draw j uniformly in
  * [0, i] with Lemire's multiply-shift on a 64-bit element. */
 void si_permutation(uint64_t key, int64_t n, int64_t* out) {

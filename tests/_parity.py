@@ -79,3 +79,29 @@ def compare_token(layer, x, y32, ids_gpu, w_gpu, y_out=None, Wr=None, y_bf16=Non
     if y_bf16 is not None:
         assert np.array_equal(np.asarray(y_bf16, np.uint16), f32_to_bf16_rne(np.asarray(y32, np.float32)))
     return err, flagged
+
+
+def compare_chunk(layer, X, y32, ids_gpu, w_gpu, y_bf16=None, Wr=None):
+    """Check every row of a chunk (T tokens) at once; returns (max normwise
+    error, near-tie rows). Each row's GPU selection is checked as in
+    compare_token, then the oracle evaluates all rows on those (validated)
+    selections with each expert dequantised once (oracle.moe_tokens)."""
+    if Wr is None:
+        Wr = oracle.router_weights_f64(layer.router)
+    T = len(X)
+    use, flagged = [], 0
+    for t in range(T):
+        u, fl = check_selection(layer, X[t], ids_gpu[t], Wr)
+        use.append(np.asarray(u, np.int64))
+        flagged += fl
+    Y, infos = oracle.moe_tokens(layer, X, ids=np.stack(use))
+    worst = 0.0
+    for t in range(T):
+        assert np.allclose(np.asarray(w_gpu[t], np.float64), infos[t].weights, rtol=0, atol=W_TOL), \
+            (t, w_gpu[t], infos[t].weights)
+        err = float(np.max(np.abs(np.asarray(y32[t], np.float64) - Y[t])) / max(np.max(np.abs(Y[t])), 1e-300))
+        assert err <= REL_TOL, (t, err)
+        if y_bf16 is not None:
+            assert np.array_equal(np.asarray(y_bf16[t], np.uint16), f32_to_bf16_rne(np.asarray(y32[t], np.float32))), t
+        worst = max(worst, err)
+    return worst, flagged

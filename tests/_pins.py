@@ -406,6 +406,26 @@ def pin_pure_python():
     assert np.allclose(y, yp, rtol=1e-11, atol=1e-14)
 
 
+def pin_chunk_rows():
+    """The chunk evaluation (each expert dequantised once for all its rows) gives,
+    row by row, the pure-Python restatement of the layer; with a forced
+    selection it gives the single-token oracle on that selection."""
+    for zipf, H, I in ((None, 64, 64), (1.1, 128, 64)):
+        layer = tiny_layer(seed=14, E=6, k=2, H=H, I=I, zipf=zipf)
+        X = si.gen_tokens(14, 0, 7, layer.spec)
+        Y, infos = oracle.moe_tokens(layer, X)
+        for t in range(len(X)):
+            yp, S, w = _py_layer(layer, X[t])
+            assert list(infos[t].ids) == S
+            assert np.allclose(infos[t].weights, w, rtol=0, atol=1e-14)
+            assert np.allclose(Y[t], yp, rtol=1e-11, atol=1e-14)
+        forced = np.array([[5, 0]] * len(X))
+        Yf, _ = oracle.moe_tokens(layer, X, ids=forced)
+        for t in range(len(X)):
+            yt, _ = oracle.moe_token(layer, X[t], ids=forced[t])
+            assert np.allclose(Yf[t], yt, rtol=1e-12, atol=1e-15)
+
+
 def pin_permutation_equivariance():
     """Relabelling the experts (router rows moved with them) leaves y unchanged."""
     layer = tiny_layer(seed=12, E=10, k=3, H=64, I=64)
@@ -552,7 +572,7 @@ def pin_sigmoid_layer_pure_python():
 
 ALL_PINS = [pin_dequant_q4_table, pin_dequant_q2_table, pin_q2_layer, pin_dequant_q8_table, pin_format_sizes,
             pin_zero_input_routing, pin_topk_is_full_sort, pin_routing_weights,
-            pin_silu, pin_ffn_closed_form, pin_dense_brute_force, pin_pure_python,
+            pin_silu, pin_ffn_closed_form, pin_dense_brute_force, pin_pure_python, pin_chunk_rows,
             pin_permutation_equivariance, pin_bf16_input, pin_lfu_trace, pin_lfu_prefetch_trace,
             pin_lfu_pinned_trace,
             pin_sigmoid_router_golden,

@@ -44,11 +44,11 @@ def header_constants():
 
 
 def test_binding_constants_match_header():
-    """The binding's constants (option ids, formats, paths, limits) equal the
+    """The binding's constants (option ids, formats, limits) equal the
     header's, so a call from Python means what the header documents."""
     consts = header_constants()
-    for must in ("MOE_OPT_CACHE_DEVICE", "MOE_OPT_DECODE_PATH", "MOE_W_Q2G64", "MOE_MAX_TOP_K",
-                 "MOE_STATIC_SCRATCH_BYTES", "MOE_SCORE_SIGMOID"):
+    for must in ("MOE_OPT_CACHE_DEVICE", "MOE_OPT_TEST_STALL_SHARED", "MOE_W_Q2G64",
+                 "MOE_MAX_TOP_K", "MOE_STATIC_SCRATCH_BYTES", "MOE_SCORE_SIGMOID"):
         assert must in consts, must
     checked = 0
     for name, value in consts.items():

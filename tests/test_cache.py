@@ -15,6 +15,7 @@ import pytest
 import oracle
 import quantized_routed_expert_moe_gb300 as moe
 import seeded_inputs as si
+from _parity import compare_token
 from _pins import read_lfu
 
 
@@ -138,11 +139,12 @@ def _streamed_vs_resident(layer, T, source=False, seed=31):
     y_str = torch.empty((T, spec.hidden), dtype=torch.float32, device="cuda")
     ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    ids_s = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w_s = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
     with moe.MoELayer(layer) as res:
-        res.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
         for t in range(T):
             res.decode(xs[t], None, y_res[t])
-            res.route(xs[t], 1, ids[t], w[t])
+            res.selection(1, ids[t], w[t])
         torch.cuda.synchronize()
         recs = packed_records(layer, res.desc)
     hm = []
@@ -159,10 +161,18 @@ def _streamed_vs_resident(layer, T, source=False, seed=31):
     with moe.MoELayer(layer, cache_slots=16, **kw) as st:
         for t in range(T):
             st.decode(xs[t], None, y_str[t])
+            st.selection(1, ids_s[t], w_s[t])
             torch.cuda.synchronize()
             hm.append(st.residency())
         stats = st.cache_stats()
-    return (y_res.cpu().numpy(), y_str.cpu().numpy(), ids.cpu().numpy(), hm, stats)
+    # the streamed layer's own selection equals the resident one's, and its
+    # outputs are checked against the oracle directly
+    assert torch.equal(ids_s, ids) and torch.equal(w_s, w)
+    Wr = oracle.router_weights_f64(layer.router)
+    ys = y_str.cpu().numpy()
+    for t in range(T):
+        compare_token(layer, X[t], ys[t], ids_s[t].cpu().numpy(), w_s[t].cpu().numpy(), Wr=Wr)
+    return (y_res.cpu().numpy(), ys, ids.cpu().numpy(), hm, stats)
 
 
 @pytest.mark.gpu
@@ -222,9 +232,8 @@ def test_source_failure_reported_and_recovered():
     ids = torch.empty(spec.top_k, dtype=torch.int32, device="cuda")
     w = torch.empty(spec.top_k, dtype=torch.float32, device="cuda")
     with moe.MoELayer(layer) as res:
-        res.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
         res.decode(x, None, y_ref)
-        res.route(x, 1, ids, w)
+        res.selection(1, ids, w)
         torch.cuda.synchronize()
     bad = int(ids[3].item())
     broken = {"on": True}

@@ -1,4 +1,9 @@
-"""Decode path on the GPU against the fp64 oracle (parity), through the C ABI."""
+"""Decode path on the GPU against the fp64 oracle (parity), through the C ABI.
+
+The expert IDs and weights checked are the ones moe_decode itself used: the
+selection its router kernel made, which its gate/up and down kernels read and
+combined with (moe_layer_selection).
+"""
 import numpy as np
 import pytest
 import torch
@@ -24,33 +29,35 @@ def to_dev(x_np, spec):
     return torch.from_numpy(np.ascontiguousarray(x_np, dtype=np.float32)).cuda()
 
 
-def decode_one(ml, spec, x_np):
+def decode_one(ml, spec, x_np, static=False):
+    """One decode; returns (y32, ids, w, y_bf16 bits or None, y) with ids / w
+    the selection the decode itself combined with."""
     H, k = spec.hidden, spec.top_k
     x = to_dev(x_np, spec)
     yd = torch.bfloat16 if spec.act == "bf16" else torch.float32
     y = torch.empty(H, dtype=yd, device="cuda")
     y32 = torch.empty(H, dtype=torch.float32, device="cuda")
-    ids = torch.empty(k, dtype=torch.int32, device="cuda")
-    w = torch.empty(k, dtype=torch.float32, device="cuda")
+    ids = torch.full((k,), -1, dtype=torch.int32, device="cuda")
+    w = torch.full((k,), float("nan"), dtype=torch.float32, device="cuda")
     s = torch.cuda.current_stream()
-    ml.decode(x, y, y32, stream=s)
-    ml.route(x, 1, ids, w, stream=s)
+    if static:
+        ml.decode_static_scratch(x, y, y32, stream=s)
+    else:
+        ml.decode(x, y, y32, stream=s)
+        ml.selection(1, ids, w, stream=s)
     torch.cuda.synchronize()
     yb = y.view(torch.int16).cpu().numpy().view(np.uint16) if spec.act == "bf16" else None
     return y32.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), yb, y
 
 
-PATHS = {"split": moe.MOE_PATH_SPLIT, "fused": moe.MOE_PATH_FUSED}
-
-
-def check_layer(layer, tokens, seed=100, path="fused"):
+def check_layer(layer, tokens, seed=100, tokens_fn=None):
     spec = layer.spec
     Wr = oracle.router_weights_f64(layer.router)
     errs, flags = [], 0
+    gen = tokens_fn or (lambda t: si.gen_tokens(seed, t, 1, spec)[0])
     with moe.MoELayer(layer) as ml:
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, PATHS[path])
         for t in range(tokens):
-            x = si.gen_tokens(seed, t, 1, spec)[0]
+            x = gen(t)
             y32, ids, w, yb, _ = decode_one(ml, spec, x)
             err, flagged = compare_token(layer, x, y32, ids, w, Wr=Wr, y_bf16=yb)
             errs.append(err)
@@ -60,11 +67,10 @@ def check_layer(layer, tokens, seed=100, path="fused"):
     return max(errs), flags
 
 
-@pytest.mark.parametrize("path", list(PATHS))
-def test_tiny_layer_decode(path):
+def test_tiny_layer_decode():
     layer = si.gen_layer(0, 0, si.CONFIGS["tiny"])
-    err, flags = check_layer(layer, 32, path=path)
-    print(f"tiny/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
+    err, flags = check_layer(layer, 32)
+    print(f"tiny: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
 SHAPES = {
@@ -81,59 +87,90 @@ SHAPES = {
 }
 
 
-# the fused decode's per-CTA buffers do not take the long rows (it refuses the
-# layer with MOE_E_UNSUPPORTED); the split path covers them
-SPLIT_ONLY = {"long_rows"}
-
-
-@pytest.mark.parametrize("name,path", [(n, p) for p in PATHS for n in SHAPES if p == "split" or n not in SPLIT_ONLY])
-def test_decode_shapes(name, path):
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_decode_shapes(name):
     layer = si.gen_layer(7, 1, SHAPES[name])
-    err, flags = check_layer(layer, 6, seed=7, path=path)
-    print(f"{name}/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
+    err, flags = check_layer(layer, 6, seed=7)
+    print(f"{name}: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
-@pytest.mark.parametrize("path", list(PATHS))
-def test_zero_input_exact(path):
+# Activations of very different magnitudes and with outlier channels: the
+# decode stages them with a per-token power-of-two scale and 16-bit fixed point
+# per run of 32 (an outlier sets the step of its 31 neighbours).
+RANGE_CASES = {
+    "outliers_x100": lambda spec, t: si.gen_tokens_outliers(31, t, 1, spec, 100.0)[0],
+    "outliers_x1000": lambda spec, t: si.gen_tokens_outliers(32, t, 1, spec, 1000.0)[0],
+    "tiny_1e-20": lambda spec, t: si.gen_tokens_scaled(33, t, 1, spec, 1e-20)[0],
+    "large_1e4": lambda spec, t: si.gen_tokens_scaled(34, t, 1, spec, 1e4)[0],
+    "large_1e5": lambda spec, t: si.gen_tokens_scaled(35, t, 1, spec, 1e5)[0],
+}
+
+
+@pytest.mark.parametrize("case", list(RANGE_CASES))
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_decode_dynamic_range(case, act):
+    spec = si.LayerSpec(hidden=1024, inter=512, n_experts=32, act=act)
+    layer = si.gen_layer(30, 0, spec)
+    err, flags = check_layer(layer, 4, tokens_fn=lambda t: RANGE_CASES[case](spec, t))
+    print(f"{case}/{act}: max normwise err {err:.3e}, near-tie tokens {flags}")
+
+
+def test_zero_input_exact():
     spec = si.LayerSpec(hidden=256, inter=128, n_experts=16)
     layer = si.gen_layer(3, 0, spec)
     with moe.MoELayer(layer) as ml:
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, PATHS[path])
         y32, ids, w, yb, _ = decode_one(ml, spec, np.zeros(256, np.uint16))
     assert list(ids) == list(range(8))
     assert np.all(w == np.float32(0.125))
     assert np.all(y32 == 0)
 
 
-@pytest.mark.parametrize("path", list(PATHS))
-def test_bit_reproducible(path):
+def test_bit_reproducible():
     spec = si.CONFIGS["tiny"]
     layer = si.gen_layer(0, 0, spec)
     x = si.gen_tokens(5, 0, 1, spec)[0]
     with moe.MoELayer(layer) as ml:
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, PATHS[path])
         a = decode_one(ml, spec, x)[0]
         b = decode_one(ml, spec, x)[0]
     assert np.array_equal(a, b)
 
 
-def test_fused_wait_runs_out_and_recovers():
-    """Failure detection without a GPU fault: the routing flag is never set, every
-    bounded wait on it gives up, the kernel drains out and the host reads
-    MOE_E_TIMEOUT; the next call runs normally."""
+def test_route_matches_decode_selection():
+    """moe_route and moe_decode select alike, bit for bit (both in the router
+    kernel's last block)."""
+    spec = si.LayerSpec(hidden=1024, inter=256, n_experts=128, zipf_alpha=1.1)
+    layer = si.gen_layer(12, 0, spec)
+    with moe.MoELayer(layer) as ml:
+        for t in range(8):
+            x_np = si.gen_tokens(12, t, 1, spec)[0]
+            _, ids, w, _, _ = decode_one(ml, spec, x_np)
+            ri = torch.empty(8, dtype=torch.int32, device="cuda")
+            rw = torch.empty(8, dtype=torch.float32, device="cuda")
+            ml.route(to_dev(x_np, spec), 1, ri, rw)
+            torch.cuda.synchronize()
+            assert np.array_equal(ri.cpu().numpy(), ids)
+            assert np.array_equal(rw.cpu().numpy().view(np.uint32), w.view(np.uint32))
+
+
+def test_shared_wait_runs_out_and_recovers():
+    """Failure detection without a GPU fault: the gate/up kernel never counts
+    itself in the shared-expert counter, the down kernel's bounded wait on it
+    gives up, the host reads MOE_E_TIMEOUT, and the output is still right (the
+    shared rows run after the ordinary wait instead); the next call is normal."""
     spec = si.LayerSpec(hidden=512, inter=256, n_experts=32)
     layer = si.gen_layer(8, 0, spec)
     x = si.gen_tokens(8, 0, 1, spec)[0]
     with moe.MoELayer(layer) as ml:
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_FUSED)
-        ml.set_option(moe.MOE_OPT_TEST_STALL_ROUTING, 1)
-        decode_one(ml, spec, x)
+        ml.set_option(moe.MOE_OPT_TEST_STALL_SHARED, 1)
+        y32, ids, w, yb, _ = decode_one(ml, spec, x)
         st, bits = ml.check()
         assert st == 5 and bits != 0  # MOE_E_TIMEOUT
-        ml.set_option(moe.MOE_OPT_TEST_STALL_ROUTING, 0)
-        y32, ids, w, yb, _ = decode_one(ml, spec, x)
-        assert ml.check() == (0, 0)
         compare_token(layer, x, y32, ids, w, y_bf16=yb)
+        ml.set_option(moe.MOE_OPT_TEST_STALL_SHARED, 0)
+        y32b, ids, w, yb, _ = decode_one(ml, spec, x)
+        assert ml.check() == (0, 0)
+        assert np.array_equal(y32, y32b)
+        compare_token(layer, x, y32b, ids, w, y_bf16=yb)
 
 
 def test_host_buffer_entry_matches_device_path():
@@ -185,9 +222,14 @@ def test_argument_errors():
         w = torch.empty(16, dtype=torch.float32, device="cuda")
         with pytest.raises(moe.MoEError):
             ml.route(x, 2, ids, w)  # max_tokens is 1
+        with pytest.raises(moe.MoEError):
+            ml.selection(2, ids, w)  # max_tokens is 1
         with pytest.raises(moe.MoEError) as ei:
             ml.cache_stage(ids, 1)
         assert ei.value.status == 6
+        with pytest.raises(moe.MoEError) as ei:
+            ml.set_option(1, 0)   # no such option
+        assert ei.value.status == 1
 
 
 @pytest.fixture(scope="module")
@@ -195,10 +237,9 @@ def gemma_layer():
     return si.gen_layer(0, 0, si.CONFIGS["gemma_decode"])
 
 
-@pytest.mark.parametrize("path", list(PATHS))
-def test_gemma_scale_decode(gemma_layer, path):
-    err, flags = check_layer(gemma_layer, 16, seed=0, path=path)
-    print(f"gemma/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
+def test_gemma_scale_decode(gemma_layer):
+    err, flags = check_layer(gemma_layer, 16, seed=0)
+    print(f"gemma: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
 @pytest.fixture(scope="module")
@@ -207,15 +248,15 @@ def glm_layer():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("path", list(PATHS))
-def test_glm_scale_decode(glm_layer, path):
-    err, flags = check_layer(glm_layer, 4, seed=0, path=path)
-    print(f"glm/{path}: max normwise err {err:.3e}, near-tie tokens {flags}")
+def test_glm_scale_decode(glm_layer):
+    err, flags = check_layer(glm_layer, 4, seed=0)
+    print(f"glm: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
 def test_back_to_back_decodes_match_synchronised():
     """Many decodes queued back to back over two layer instances (the kernels
-    of consecutive calls overlap through programmatic dependent launch) give
+    of consecutive calls overlap through programmatic dependent launch, and the
+    down kernel starts on the shared expert before gate/up completes) give
     bit-identical outputs to the same decodes with a synchronisation after
     every call."""
     spec = si.LayerSpec(hidden=1024, inter=512, n_experts=64, zipf_alpha=1.1)

@@ -3,7 +3,8 @@
 Every row of a prefill chunk must equal the oracle's layer output for that
 token within the normwise tolerance, with the expert IDs of that token exact
 (near-ties handled as in the decode tests), and the bf16 output must be the
-round-to-nearest-even of the fp32 output.
+round-to-nearest-even of the fp32 output. The IDs and weights checked are the
+ones the chunk itself computed and combined with (moe_layer_selection).
 """
 import dataclasses
 
@@ -14,7 +15,7 @@ import torch
 import oracle
 import quantized_routed_expert_moe_gb300 as moe
 import seeded_inputs as si
-from _parity import compare_token
+from _parity import compare_chunk
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +42,7 @@ def run_prefill(ml, spec, X, T):
     ids = torch.empty(T * k, dtype=torch.int32, device="cuda")
     w = torch.empty(T * k, dtype=torch.float32, device="cuda")
     ml.prefill_chunk(x, T, y, y32)
-    ml.route(x, T, ids, w)
+    ml.selection(T, ids, w)
     torch.cuda.synchronize()
     st, bits = ml.check()
     assert st == 0, hex(bits)
@@ -49,15 +50,9 @@ def run_prefill(ml, spec, X, T):
     return (y32.cpu().numpy().reshape(T, H), ids.cpu().numpy().reshape(T, k), w.cpu().numpy().reshape(T, k), yb)
 
 
-def check_rows(layer, X, y32, ids, w, yb, rows):
-    Wr = oracle.router_weights_f64(layer.router)
-    errs, flags = [], 0
-    for t in rows:
-        err, fl = compare_token(layer, X[t], y32[t], ids[t], w[t], Wr=Wr,
-                                y_bf16=None if yb is None else yb[t])
-        errs.append(err)
-        flags += fl
-    return max(errs), flags
+def check_rows(layer, X, y32, ids, w, yb):
+    """Every row of the chunk against the oracle."""
+    return compare_chunk(layer, X, y32, ids, w, y_bf16=yb)
 
 
 SHAPES = {
@@ -80,8 +75,33 @@ def test_prefill_shapes(name):
     X = si.gen_tokens(21, 0, T, spec)
     with moe.MoELayer(layer, max_tokens=T) as ml:
         y32, ids, w, yb = run_prefill(ml, spec, X, T)
-    err, flags = check_rows(layer, X, y32, ids, w, yb, range(T))
+    err, flags = check_rows(layer, X, y32, ids, w, yb)
     print(f"{name}: max normwise err {err:.3e}, near-tie tokens {flags}")
+
+
+# Activations far from unit scale and with outlier channels: the chunk stages
+# each token as x * 2^a in binary16 and each SwiGLU output row as h * 2^z, so
+# large tokens do not overflow binary16 (65504) and tiny ones do not flush.
+RANGE_CASES = {
+    "outliers_x1000": lambda spec, T: si.gen_tokens_outliers(61, 0, T, spec, 1000.0),
+    "tiny_1e-20": lambda spec, T: si.gen_tokens_scaled(62, 0, T, spec, 1e-20),
+    "large_1e4": lambda spec, T: si.gen_tokens_scaled(63, 0, T, spec, 1e4),
+    "large_1e5": lambda spec, T: si.gen_tokens_scaled(64, 0, T, spec, 1e5),
+}
+
+
+@pytest.mark.parametrize("case", list(RANGE_CASES))
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_prefill_dynamic_range(case, act):
+    spec = si.LayerSpec(hidden=1024, inter=512, n_experts=32, act=act, zipf_alpha=1.1)
+    layer = si.gen_layer(60, 0, spec)
+    T = 40
+    X = RANGE_CASES[case](spec, T)
+    with moe.MoELayer(layer, max_tokens=T) as ml:
+        y32, ids, w, yb = run_prefill(ml, spec, X, T)
+    assert np.all(np.isfinite(y32))
+    err, flags = check_rows(layer, X, y32, ids, w, yb)
+    print(f"{case}/{act}: max normwise err {err:.3e}, near-tie tokens {flags}")
 
 
 def test_prefill_matches_decode_rows():
@@ -141,18 +161,17 @@ def glm_layer():
     return si.gen_layer(0, 0, si.CONFIGS["glm_prefill"])
 
 
-def test_glm_prefill_chunk_sampled(glm_layer):
+def test_glm_prefill_chunk(glm_layer):
     """Full-size chunk (GLM shape, 128 tokens, Zipf(1.1) bias) in the launch
-    configuration the benchmark times; sampled rows against the oracle, and every
-    row's selection against the routing call."""
+    configuration the benchmark times; all 128 rows against the oracle."""
     spec = glm_layer.spec
     T = 128
     X = si.gen_tokens(3, 0, T, spec)
     with moe.MoELayer(glm_layer, max_tokens=T) as ml:
         y32, ids, w, yb = run_prefill(ml, spec, X, T)
     assert np.all(np.isfinite(y32))
-    err, flags = check_rows(glm_layer, X, y32, ids, w, yb, [0, 1, 63, 127])
-    print(f"glm prefill: sampled max normwise err {err:.3e}, near-tie tokens {flags}")
+    err, flags = check_rows(glm_layer, X, y32, ids, w, yb)
+    print(f"glm prefill: max normwise err {err:.3e} over 128 rows, near-tie tokens {flags}")
 
 
 def test_glm_prefill_dense_groups(glm_layer):
@@ -164,5 +183,5 @@ def test_glm_prefill_dense_groups(glm_layer):
     with moe.MoELayer(layer, max_tokens=T) as ml:
         y32, ids, w, yb = run_prefill(ml, spec, X, T)
     assert np.all(np.sort(ids, axis=1) == np.arange(8)[None, :])
-    err, flags = check_rows(layer, X, y32, ids, w, yb, [0, 77, 127])
-    print(f"glm prefill dense: sampled max normwise err {err:.3e}")
+    err, flags = check_rows(layer, X, y32, ids, w, yb)
+    print(f"glm prefill dense: max normwise err {err:.3e} over 128 rows")

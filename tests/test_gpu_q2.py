@@ -2,9 +2,9 @@
 
 Inferno README ("Model": 2-bit routed experts) and Colibri README ("What's
 implemented": packed int2, dequant-on-use), with the storage reading in
-tests/golden/q2g64_dequant.txt. Decode (split path), the allocation-free
-decode and a streamed layer are covered; prefill chunks and the fused path
-refuse 2-bit layers with MOE_E_UNSUPPORTED.
+tests/golden/q2g64_dequant.txt. Decode, the allocation-free decode, a
+streamed layer, prefill chunks through the grouped tcgen05 GEMM (resident and
+streamed through the cache) are covered.
 """
 import dataclasses
 
@@ -15,7 +15,7 @@ import torch
 import oracle
 import quantized_routed_expert_moe_gb300 as moe
 import seeded_inputs as si
-from _parity import compare_token
+from _parity import compare_chunk, compare_token
 
 pytestmark = pytest.mark.gpu
 
@@ -56,8 +56,12 @@ def run_decode(ml, spec, X, static=False):
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     for t in range(T):
-        (ml.decode_static_scratch if static else ml.decode)(xd[t], y[t], y32[t])
-        ml.route(xd[t], 1, ids[t], w[t])
+        if static:   # the static-scratch decode is checked against the selection of moe_route
+            ml.decode_static_scratch(xd[t], y[t], y32[t])
+            ml.route(xd[t], 1, ids[t], w[t])
+        else:        # the selection moe_decode itself combined with
+            ml.decode(xd[t], y[t], y32[t])
+            ml.selection(1, ids[t], w[t])
     torch.cuda.synchronize()
     yb = y.view(torch.int16).cpu().numpy().view(np.uint16) if spec.act == "bf16" else None
     return y32.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), yb
@@ -130,16 +134,77 @@ def test_q2_streamed_layer_bit_identical(device):
     assert np.array_equal(y32.cpu().numpy(), want)
 
 
-def test_q2_refused_paths():
-    spec = SHAPES["tiny_f32"]
-    layer = si.gen_layer(54, 0, spec)
-    X = si.gen_tokens(54, 0, 4, spec)
-    with moe.MoELayer(layer, max_tokens=4) as ml:
-        with pytest.raises(moe.MoEError) as ei:
-            ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_FUSED)
-        assert ei.value.status == 2
-        xd = to_dev(X.reshape(-1), spec)
-        y = torch.empty(4 * spec.hidden, dtype=torch.float32, device="cuda")
-        with pytest.raises(moe.MoEError) as ei:
-            ml.prefill_chunk(xd, 4, y)
-        assert ei.value.status == 2
+PREFILL = {
+    # name: (spec, T) -- ragged K blocks (H = 320: 5 chunks of 64, I = 192: 3),
+    # small and full groups, no shared expert, an 8-bit router
+    "tiny_f32_T16": (q2(si.CONFIGS["tiny"]), 16),
+    "bf16_T128_zipf": (q2(si.LayerSpec(hidden=512, inter=256, n_experts=64, zipf_alpha=1.1)), 128),
+    "ragged_T33": (q2(si.LayerSpec(hidden=320, inter=192, n_experts=24, top_k=6)), 33),
+    "no_shared_T7": (q2(si.LayerSpec(hidden=256, inter=128, n_experts=16, top_k=4, n_shared=0)), 7),
+    "q8_router_T64": (q2(si.LayerSpec(hidden=1088, inter=704, n_experts=40, router_fmt="q8g64")), 64),
+}
+
+
+def run_prefill(ml, spec, X, T):
+    xd = to_dev(X.reshape(-1), spec)
+    yd = torch.bfloat16 if spec.act == "bf16" else torch.float32
+    y = torch.empty(T * spec.hidden, dtype=yd, device="cuda")
+    y32 = torch.empty(T * spec.hidden, dtype=torch.float32, device="cuda")
+    ids = torch.empty(T * spec.top_k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T * spec.top_k, dtype=torch.float32, device="cuda")
+    ml.prefill_chunk(xd, T, y, y32)
+    ml.selection(T, ids, w)   # the selection the chunk itself combined with
+    torch.cuda.synchronize()
+    st, bits = ml.check()
+    assert st == 0, hex(bits)
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(T, -1) if spec.act == "bf16" else None
+    return (y32.cpu().numpy().reshape(T, -1), ids.cpu().numpy().reshape(T, -1), w.cpu().numpy().reshape(T, -1), yb)
+
+
+@pytest.mark.parametrize("name", list(PREFILL))
+def test_q2_prefill_chunk(name):
+    """2-bit experts in the grouped tcgen05 GEMM: every row against the oracle."""
+    spec, T = PREFILL[name]
+    layer = si.gen_layer(55, 0, spec)
+    X = si.gen_tokens(55, 0, T, spec)
+    with moe.MoELayer(layer, max_tokens=T) as ml:
+        y32, ids, w, yb = run_prefill(ml, spec, X, T)
+    err, flags = compare_chunk(layer, X, y32, ids, w, y_bf16=yb)
+    print(f"q2 prefill {name}: max normwise err {err:.3e}, near-tie tokens {flags}")
+
+
+def test_q2_prefill_dense_groups():
+    """Every token on the same experts: full 128-row tiles through the 2-bit dequantiser."""
+    spec = q2(si.LayerSpec(hidden=1024, inter=512, n_experts=32))
+    layer = si.gen_layer(56, 0, spec)
+    bias = np.full(32, -30.0, np.float32)
+    bias[:8] = 30.0
+    layer = dataclasses.replace(layer, router_bias=bias)
+    T = 128
+    X = si.gen_tokens(56, 0, T, spec)
+    with moe.MoELayer(layer, max_tokens=T) as ml:
+        y32, ids, w, yb = run_prefill(ml, spec, X, T)
+    assert np.all(np.sort(ids, axis=1) == np.arange(8)[None, :])
+    err, _ = compare_chunk(layer, X, y32, ids, w, y_bf16=yb)
+    print(f"q2 prefill dense: max normwise err {err:.3e}")
+
+
+def test_q2_streamed_prefill_bit_identical():
+    """A 2-bit chunk through a streamed 16-slot layer (staging waves) equals the
+    resident layer's chunk bit for bit."""
+    spec = q2(si.LayerSpec(hidden=512, inter=256, n_experts=64, zipf_alpha=1.1))
+    layer = si.gen_layer(57, 0, spec)
+    T = 48
+    X = si.gen_tokens(57, 0, T, spec)
+    with moe.MoELayer(layer, max_tokens=T) as res:
+        want = run_prefill(res, spec, X, T)
+        n = moe.moe_expert_record_bytes(res.desc)
+        recs = []
+        for ex in layer.experts:
+            buf = np.zeros(n, np.uint8)
+            moe.moe_pack_expert_record(res.desc, ex, buf)
+            recs.append(buf)
+    with moe.MoELayer(layer, max_tokens=T, cache_slots=16, records=recs) as st:
+        got = run_prefill(st, spec, X, T)
+    assert np.array_equal(got[0], want[0])
+    assert np.array_equal(got[1], want[1])

@@ -58,8 +58,12 @@ def run_decode(ml, spec, X, static=False):
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     for t in range(T):
-        (ml.decode_static_scratch if static else ml.decode)(xd[t], y[t], y32[t])
-    ml.route(xd, T, ids, w)
+        if static:   # the static-scratch decode is checked against the selection of moe_route
+            ml.decode_static_scratch(xd[t], y[t], y32[t])
+            ml.route(xd[t], 1, ids[t], w[t])
+        else:        # the selection moe_decode itself combined with
+            ml.decode(xd[t], y[t], y32[t])
+            ml.selection(1, ids[t], w[t])
     torch.cuda.synchronize()
     yb = y.view(torch.int16).cpu().numpy().view(np.uint16) if spec.act == "bf16" else None
     return y32.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), yb
@@ -82,7 +86,6 @@ def test_sigmoid_decode_and_route(name):
     T = 12
     X = si.gen_tokens(41, 0, T, spec)
     with moe.MoELayer(layer, max_tokens=T) as ml:
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
         y32, ids, w, yb = run_decode(ml, spec, X)
         st, bits = ml.check()
         assert st == 0, hex(bits)
@@ -96,7 +99,6 @@ def test_sigmoid_static_scratch_matches_decode():
     layer = si.gen_layer(42, 0, spec)
     X = si.gen_tokens(42, 0, 6, spec)
     with moe.MoELayer(layer, max_tokens=6) as ml:
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
         a = run_decode(ml, spec, X)
         b = run_decode(ml, spec, X, static=True)
     assert np.array_equal(a[0], b[0])
@@ -117,7 +119,7 @@ def test_sigmoid_prefill_chunk(name):
     w = torch.empty(T * spec.top_k, dtype=torch.float32, device="cuda")
     with moe.MoELayer(layer, max_tokens=T) as ml:
         ml.prefill_chunk(xd, T, y, y32)
-        ml.route(xd, T, ids, w)
+        ml.selection(T, ids, w)   # the selection the chunk itself combined with
         torch.cuda.synchronize()
         st, bits = ml.check()
         assert st == 0, hex(bits)
@@ -137,7 +139,6 @@ def test_sigmoid_streamed_layer_bit_identical(device):
     T = 10
     X = si.gen_tokens(44, 0, T, spec)
     with moe.MoELayer(layer, max_tokens=T) as res:
-        res.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_SPLIT)
         y_res = run_decode(res, spec, X)[0]
         n = moe.moe_expert_record_bytes(res.desc)
         recs = []
@@ -172,9 +173,6 @@ def test_sigmoid_option_errors():
     spec = SHAPES["tiny_f32"]
     layer = si.gen_layer(45, 0, spec)
     with moe.MoELayer(layer) as ml:   # the binding set sigmoid scoring
-        with pytest.raises(moe.MoEError) as ei:
-            ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_FUSED)
-        assert ei.value.status == 2   # MOE_E_UNSUPPORTED
         for bad in (0.0, -1.0, float("inf"), float("nan")):
             with pytest.raises(moe.MoEError) as ei:
                 ml.set_router_scoring(moe.MOE_SCORE_SIGMOID, bad)
@@ -182,9 +180,6 @@ def test_sigmoid_option_errors():
         with pytest.raises(moe.MoEError) as ei:
             ml.set_router_scoring(7, 1.0)
         assert ei.value.status == 1
-        # back to softmax: the fused path is allowed again, and sigmoid is then refused
+        # switching back and forth is allowed
         ml.set_router_scoring(moe.MOE_SCORE_SOFTMAX, 1.0)
-        ml.set_option(moe.MOE_OPT_DECODE_PATH, moe.MOE_PATH_FUSED)
-        with pytest.raises(moe.MoEError) as ei:
-            ml.set_router_scoring(moe.MOE_SCORE_SIGMOID, 2.5)
-        assert ei.value.status == 2
+        ml.set_router_scoring(moe.MOE_SCORE_SIGMOID, 2.5)
