@@ -384,15 +384,15 @@ moe_status moe_lfu_trace_pinned(int32_t slots, int32_t n_experts, int32_t k, int
 /* moe_decode on a resident layer runs three kernels chained with programmatic
  * dependent launch: the router (logits, then the top-k selection in its last
  * block, which raises a ready flag); gate/up + SwiGLU (computes the shared
- * expert's rows while the router runs, waits for the flag, then the routed
- * experts' rows; each completed half-group of SwiGLU outputs is quantised once
- * by the warp that completed it); down + combine (starts on the shared
- * expert's rows once its half-groups are all staged, then waits for gate/up
- * and computes the routed experts). Device-side waits on the flag and the
- * counter are bounded (0.2 s) and fall back to the ordinary wait. */
+ * expert's rows while the router runs and counts each CTA done with them,
+ * waits for the flag, then the routed experts' rows); down + combine (starts
+ * on the shared expert's rows once every gate/up CTA has counted itself, then
+ * waits for gate/up and computes the routed experts). Device-side waits on the
+ * flag and the counter are bounded (0.2 s) and fall back to the ordinary
+ * wait. */
 enum {
     /* Test hook for failure detection: while nonzero, the decode gate/up
-     * kernel never counts the shared expert's staged half-groups, so the down
+     * kernel never counts its CTAs done with the shared expert's rows, so the down
      * kernel's bounded wait on the count runs out (0.2 s), records
      * MOE_E_TIMEOUT for moe_layer_check and computes the shared expert after
      * its ordinary wait instead (the output is unchanged). */

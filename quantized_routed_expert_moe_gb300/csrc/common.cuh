@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <climits>
 #include <cstdint>
 
 #include "moe.h"
@@ -220,34 +221,40 @@ __device__ __forceinline__ void word_dp4a(uint32_t w, const uint4 xs, int& ah, i
     al = __dp4a((int)o, (int)xs.w, al);
 }
 
-// 2^f with max_abs * 2^f in [2^13, 2^14); 1 when max_abs is 0 or not finite
-__device__ __forceinline__ float q16_scale(float max_abs) {
+// 2^f with max_abs * 2^f in [2^13, 2^14); 1 when max_abs is 0 or not finite.
+// *inv gets 2^-f exactly (f <= 127, so 2^-f >= 2^-127, the one subnormal case).
+__device__ __forceinline__ float q16_scale(float max_abs, float* inv) {
     const uint32_t u = __float_as_uint(max_abs);
     const int ex = (int)((u >> 23) & 0xFF);
-    if (ex == 0 || ex == 0xFF) return 1.0f;
+    if (ex == 0 || ex == 0xFF) {
+        *inv = 1.0f;
+        return 1.0f;
+    }
     int f = 13 - (ex - 127);
     f = max(-126, min(127, f));
+    *inv = f == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - f) << 23);
     return __uint_as_float((uint32_t)(f + 127) << 23);
 }
 
-// Quantise one run v[0..7] with scale sc into the staged uint4 layout. The
-// rounding to the nearest integer (ties to even) is one fma with 1.5 * 2^23:
-// the sum lies in [2^23, 2^24), where the unit in the last place is 1, so the
-// fma's rounding is the rounding to an integer, and the integer is the low
-// bits of the sum (sc is a power of two, so v * sc is exact).
+// Quantise one run v[0..7] with scale sc into the staged uint4 layout. One
+// fma with 1.5 * 2^23 + 128 per value: the sum lies in [2^23, 2^24), where the
+// unit in the last place is 1, so the fma's rounding is the rounding of v * sc
+// to the nearest integer q (ties to even: the added constant is even; sc is a
+// power of two, so v * sc is exact), and the low 16 bits of the sum's bit
+// pattern are t = q + 128 (|q| <= 2^14). Then hi = t >> 8 is byte 1 of t and
+// lo = q - 256 hi = (t & 255) - 128 is byte 0 of t with its top bit flipped;
+// byte permutes gather them.
 __device__ __forceinline__ uint4 quant_run(const float* v, float sc) {
-    uint32_t he = 0, ho = 0, le = 0, lo = 0;
+    uint32_t t[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int q = __float_as_int(fmaf(v[i], sc, 12582912.0f)) - 0x4B400000;   // |q| <= 2^14
-        const int h = (q + 128) >> 8;                  // floor((q + 128) / 256)
-        const int l = q - 256 * h;                     // in [-128, 127]
-        const uint32_t hb = (uint32_t)(h & 0xFF), lb = (uint32_t)(l & 0xFF);
-        const int sh = 8 * (i >> 1);
-        if (i & 1) { ho |= hb << sh; lo |= lb << sh; }
-        else { he |= hb << sh; le |= lb << sh; }
-    }
-    return make_uint4(he, ho, le, lo);
+    for (int i = 0; i < 8; ++i) t[i] = __float_as_uint(fmaf(v[i], sc, 12583040.0f));   // 1.5 * 2^23 + 128
+    // pairs (i, i + 2): hi bytes (byte 1 of each), lo bytes (byte 0 of each)
+    const uint32_t h02 = __byte_perm(t[0], t[2], 0x0051), h46 = __byte_perm(t[4], t[6], 0x0051);
+    const uint32_t h13 = __byte_perm(t[1], t[3], 0x0051), h57 = __byte_perm(t[5], t[7], 0x0051);
+    const uint32_t l02 = __byte_perm(t[0], t[2], 0x0040), l46 = __byte_perm(t[4], t[6], 0x0040);
+    const uint32_t l13 = __byte_perm(t[1], t[3], 0x0040), l57 = __byte_perm(t[5], t[7], 0x0040);
+    return make_uint4(__byte_perm(h02, h46, 0x5410), __byte_perm(h13, h57, 0x5410),
+                      __byte_perm(l02, l46, 0x5410) ^ 0x80808080u, __byte_perm(l13, l57, 0x5410) ^ 0x80808080u);
 }
 
 // Stage runs of a vector: called by whole warps with a warp-uniform trip count;
@@ -263,14 +270,19 @@ __device__ __forceinline__ void stage_q16_run(const float* v, bool valid, int r,
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     s += __shfl_xor_sync(0xffffffffu, s, 1);
     s += __shfl_xor_sync(0xffffffffu, s, 2);
-    const float sc = q16_scale(m);
+    float isc;
+    const float sc = q16_scale(m, &isc);
     const uint4 q = quant_run(v, sc);
     if (valid) {
         const int hg = r >> 2, wi = r & 3;
         xq[wi * KG + hg] = q;
-        if (wi == 0) { inv[hg] = 1.0f / sc; X[hg] = s; }
+        if (wi == 0) { inv[hg] = isc; X[hg] = s; }
     }
 }
+
+// Tag of one decode token's router partials: odd, so that a zeroed word
+// never carries a valid tag; seq counts the layer's decodes on the device.
+__device__ __forceinline__ unsigned decode_tag(unsigned seq) { return (seq << 1) | 1u; }
 
 // Token scale: the exponent a with max_abs * 2^a in [1, 2) (0 when max_abs is
 // 0, subnormal or not finite). Activations are staged as x * 2^a, so that the
@@ -333,52 +345,103 @@ __device__ __forceinline__ float route_key(float l, float b, RouteMode m, float*
     return sc + b;
 }
 
-// Top k of the keys sl[0..E) (shared memory) by rank: every thread takes
-// experts e = tid, tid + blockDim, ... and counts the experts that come before
-// e in the order; the expert of rank r < k is selection r. The ranks are a
-// permutation (the index breaks ties), so each r < k is written exactly once.
-// su: shared scratch of round4(E) words. Weights, by thread 0 in selection
-// order: the softmax over the selected keys (the first selected is the
-// maximum), or, when `score` is given (sigmoid scoring), scale * score_j / sum
-// over the selection of score. Ends with the block synchronised; E <= 1024.
-__device__ __forceinline__ void block_topk_rank(const float* sl, uint32_t* su, int E, int k, int32_t* ids_out,
-                                                float* w_out, const float* score = nullptr, float scale = 1.0f) {
-    __shared__ float s_v[MOE_MAX_TOP_K];
-    __shared__ int s_i[MOE_MAX_TOP_K];
-    const int E4 = (E + 3) & ~3;
-    for (int e = threadIdx.x; e < E4; e += blockDim.x) su[e] = e < E ? key_img(sl[e]) : key_img(-INFINITY);
+// Top k of the keys sl[0..E) (shared memory): the first k experts in the
+// order by (-key, e), NaN keys counted as -inf. Each expert gets a unique
+// 64-bit sort key, (order-preserving image of its key) << 32 | ~e, so that the
+// order is plain integer order. Two levels of ranking by counting: warp w
+// ranks each expert of chunk w (E / warps contiguous experts) among the chunk,
+// and those of chunk rank < k become candidates; each candidate is then
+// ranked among all candidates, and the candidate of rank r < k is selection
+// r. This is exact: an expert that comes before one of the first k is itself
+// among the first k and comes before it in their common chunk too, so all of
+// the first k are candidates and their rank among candidates is their rank
+// among all experts. The counting loops have fixed trip counts (chunks of at
+// most 32 experts, at most 64 candidates) so that their shared-memory reads
+// are all in flight together. Weights (one warp, each lane one selection; the
+// hardware exponential and division, ~1e-6 relative): the softmax over the
+// selected keys (the first selected is the maximum), or,
+// when `score` is given (sigmoid scoring), scale * score_j / sum over the
+// selection of score; the sum runs in selection order. Ends with the block
+// synchronised. blockDim.x = 256 (8 warps), E <= 1024.
+__device__ __forceinline__ void block_topk(const float* sl, int E, int k, int32_t* ids_out, float* w_out,
+                                           const float* score = nullptr, float scale = 1.0f) {
+    constexpr int NW = 8, NC = NW * MOE_MAX_TOP_K;   // warps, candidate places
+    __shared__ __align__(16) unsigned long long s_key[1024];
+    __shared__ __align__(16) unsigned long long s_cand[NC];   // 0: no candidate
+    __shared__ int s_sel[MOE_MAX_TOP_K];
+    __shared__ int s_rank[NC];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        s_key[e] = ((unsigned long long)key_img(sl[e]) << 32) | (uint32_t)~(uint32_t)e;
+    if (threadIdx.x < NC) {
+        s_cand[threadIdx.x] = 0ull;
+        s_rank[threadIdx.x] = 0;
+    }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const uint32_t ue = su[e];
+    const int C = (E + NW - 1) / NW;
+    const int c0 = min(E, warp * C), c1 = min(E, c0 + C);
+    if (C <= 32) {
+        // one expert per lane, ranked against the 32 places of the chunk
+        // (places past the chunk's end count as absent)
+        const int e = c0 + lane;
+        const unsigned long long me = e < c1 ? s_key[e] : 0ull;
         int rank = 0;
-        for (int j0 = 0; j0 < E4; j0 += 4) {
-            const uint4 q = *reinterpret_cast<const uint4*>(su + j0);
-            // (j < e and u_j >= u_e) or (j > e and u_j > u_e); padding never
-            // counts (it equals -inf and lies past every real index)
-            rank += (q.x > ue) | ((q.x == ue) & (j0 + 0 < e));
-            rank += (q.y > ue) | ((q.y == ue) & (j0 + 1 < e));
-            rank += (q.z > ue) | ((q.z == ue) & (j0 + 2 < e));
-            rank += (q.w > ue) | ((q.w == ue) & (j0 + 3 < e));
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(s_key + (c0 & ~1) + j);
+            const int ja = (c0 & ~1) + j;
+            rank += (ja >= c0 && ja < c1 && q.x > me) + (ja + 1 >= c0 && ja + 1 < c1 && q.y > me);
         }
-        if (rank < k) {
-            const float v = sl[e];
-            s_v[rank] = (v != v) ? -INFINITY : v;
-            s_i[rank] = e;
+        if (e < c1 && rank < k) s_cand[warp * k + rank] = me;
+    } else {
+        for (int e = c0 + lane; e < c1; e += 32) {
+            const unsigned long long me = s_key[e];
+            int rank = 0;
+            for (int j = c0; j < c1; ++j) rank += s_key[j] > me;
+            if (rank < k) s_cand[warp * k + rank] = me;
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float ex[MOE_MAX_TOP_K], den = 0.f;
+    {
+        // thread t counts the candidates of quarter t / NC that come before
+        // candidate t % NC; the four counts add up in shared memory
+        const int c = threadIdx.x % NC, q4 = threadIdx.x / NC;
+        const unsigned long long me = s_cand[c];
+        int rank = 0;
 #pragma unroll
-        for (int r = 0; r < MOE_MAX_TOP_K; ++r)
-            if (r < k) {
-                ex[r] = score ? score[s_i[r]] : expf(s_v[r] - s_v[0]);
-                den += ex[r];
-            }
-        const float mul = score ? scale : 1.0f;
+        for (int i = 0; i < NC / 8; ++i) {
+            const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(s_cand + q4 * (NC / 4) + 2 * i);
+            rank += (q.x > me) + (q.y > me);
+        }
+        if (rank) atomicAdd(&s_rank[c], rank);
+    }
+    __syncthreads();
+    if (threadIdx.x < NC) {
+        const unsigned long long me = s_cand[threadIdx.x];
+        const int rank = s_rank[threadIdx.x];
+        if (me != 0ull && rank < k) s_sel[rank] = (int)~(uint32_t)me;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // lane r computes term r; the sum runs in selection order (gathered by
+        // shuffles); lane r writes selection r
+        const int r = lane < k ? lane : 0;
+        const int e = s_sel[r], e0 = s_sel[0];
+        float v = sl[e], v0 = sl[e0];
+        v = (v != v) ? -INFINITY : v;
+        v0 = (v0 != v0) ? -INFINITY : v0;
+        // the hardware exponential: relative error ~1e-6 here (v - v0 <= 0)
+        const float ex = score ? score[e] : __expf(v - v0);
+        float den = 0.f;
 #pragma unroll
-        for (int r = 0; r < MOE_MAX_TOP_K; ++r)
-            if (r < k) { ids_out[r] = s_i[r]; w_out[r] = ex[r] / den * mul; }
+        for (int j = 0; j < MOE_MAX_TOP_K; ++j) {
+            const float t = __shfl_sync(0xffffffffu, ex, j);
+            if (j < k) den += t;
+        }
+        if (lane < k) {
+            ids_out[lane] = e;
+            w_out[lane] = __fdividef(ex, den) * (score ? scale : 1.0f);   // den in (0, k]: within 2 ulp
+        }
     }
     __syncthreads();
 }

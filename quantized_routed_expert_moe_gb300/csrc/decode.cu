@@ -6,17 +6,18 @@
 //               and routing weights (router.cu), then a ready flag;
 //   gate/up  -- starts while the router runs: stages the activations and
 //               computes the shared expert's rows, which do not depend on the
-//               routing; waits (bounded) for the ready flag rather than for the
-//               router grid to retire, then computes the routed experts' rows.
-//               Row pairs are spread over every warp of the grid, one pair per
-//               warp at a time. The warp that completes a half-group of 32
-//               SwiGLU outputs (a counter per half-group) quantises it into the
-//               down kernel's staged form, so nothing is quantised twice and no
-//               CTA waits for another;
-//   down     -- starts as gate/up CTAs retire: computes the shared expert's
-//               output rows as soon as its half-groups are all staged (a
-//               counter), then waits for gate/up and computes the routed
-//               experts' rows and the weighted combine.
+//               routing, then counts the CTA as done with them; waits
+//               (bounded) for the ready flag rather than for the router grid
+//               to retire, then computes the routed experts' rows. Row pairs
+//               are spread over every warp of the grid, one or two pairs per
+//               warp at a time; each SwiGLU output is written (fp32) into
+//               every replica of the output block with plain stores, so no
+//               warp ever waits on another;
+//   down     -- starts as gate/up CTAs retire: once every gate/up CTA has
+//               counted its shared rows, quantises the shared expert's SwiGLU
+//               outputs into shared memory and computes their output rows;
+//               then waits for gate/up, quantises the routed experts' outputs
+//               and computes their rows and the weighted combine.
 // Each warp issues all of a row's weight loads (128-bit, streaming) before it
 // computes. The 4-bit codes are multiplied with 16-bit fixed-point activations
 // by integer dp4a (common.cuh).
@@ -38,6 +39,8 @@ namespace moe {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kDownThreads = 256;
+constexpr int kDownWarps = kDownThreads / 32;
 constexpr int kGuBlock = 6;           // half-groups per lane whose loads are in flight together (gate/up)
 constexpr int kDownRows = 4;          // output rows per down work item (share the staged activations)
 constexpr int kDownMaxRows = 96;      // output rows one CTA owns in the down kernel
@@ -284,12 +287,6 @@ __device__ __forceinline__ void gu_phase(int p0, int step, int pend, PtrF ptr, D
     }
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
-
 // Wait until *ctr >= target (acquire), for at most limit_ns of GPU time.
 __device__ __forceinline__ bool wait_count(const unsigned* ctr, unsigned target, uint64_t limit_ns) {
     const uint64_t t0 = bw::gtimer();
@@ -303,39 +300,78 @@ __device__ __forceinline__ bool wait_count(const unsigned* ctr, unsigned target,
     return false;
 }
 
-// The staged SwiGLU outputs of ns slots (one replica): runs hq[ns][4][I/32]
-// (uint4), then the inverse scales inv[ns][I/32], then the half-group sums
-// X[ns][I/32] -- the form stage_q16_run writes, which the down kernel's dot
-// products read.
-__host__ __device__ inline size_t hq_block_bytes(int ns, int I) { return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8; }
-
-// A whole warp quantises half-group hg of slot jj (32 SwiGLU outputs at hrow,
-// fp32, already written) into every replica of the staged block.
-__device__ __forceinline__ void stage_half_group(const float* hrow, int jj, int hg, int ns, int IG, uint8_t* hq_base,
-                                                 size_t blk, int copies) {
-    const int lane = threadIdx.x & 31;
-    const float val = __ldcg(hrow + lane);
-    float v[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) v[m] = __shfl_sync(0xffffffffu, val, ((lane & 3) << 3) | m);   // run lane & 3
-    float mx = 0.f, sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { mx = fmaxf(mx, fabsf(v[i])); sum += v[i]; }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    const float sc = q16_scale(mx);
-    const uint4 q = quant_run(v, sc);
-    if (lane < 4) {   // lanes 0..3 hold runs 0..3
-        for (int c = 0; c < copies; ++c) {
-            uint4* hq = reinterpret_cast<uint4*>(hq_base + (size_t)c * blk);
-            float* hinv = reinterpret_cast<float*>(hq + (size_t)ns * 4 * IG);
-            float* hX = hinv + ns * IG;
-            hq[(size_t)jj * 4 * IG + lane * IG + hg] = q;
-            if (lane == 0) { hinv[jj * IG + hg] = 1.0f / sc; hX[jj * IG + hg] = sum; }
+// Poll the 64-bit word *p until its high half is `tag`, for at most limit_ns
+// of GPU time; *out gets the last value read. False when the limit passed.
+__device__ __forceinline__ bool poll_tagged(const unsigned long long* p, unsigned tag, uint64_t limit_ns,
+                                            unsigned long long* out) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    const uint64_t t0 = bw::gtimer();
+    for (uint32_t i = 0; (unsigned)(v >> 32) != tag; ++i) {
+        if ((i & 15) == 15 && bw::gtimer() - t0 > limit_ns) {
+            *out = v;
+            return false;
         }
+        __nanosleep(32);
+        asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     }
+    *out = v;
+    return true;
+}
+
+__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned tag, uint32_t lo) {
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(((unsigned long long)tag << 32) | lo) : "memory");
+}
+
+// Words of shared memory the per-CTA selection uses: keys [E], then sigmoid
+// scores [E] (the layout the router's selecting block uses).
+__host__ __device__ inline int select_words(int E) { return 2 * E; }
+
+// This token's selection, computed by the whole CTA from the router's tagged
+// partial logits part_tag[splits][E]: each word is polled until it carries the
+// token's tag (for at most limit_ns; then the router grid's completion is
+// waited for instead and the error bit set), the splits are summed in order
+// (the same arithmetic as the router's selecting block, so the selection is the
+// same), and the top k are selected with their weights into ids_out / w_out
+// (shared memory). Ends with the block synchronised.
+__device__ void select_from_tagged(const unsigned long long* part_tag, unsigned tag, int splits, int E, int k,
+                                   const float* bias, RouteMode mode, float* sm, int32_t* ids_out, float* w_out,
+                                   unsigned* err) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        unsigned long long v[8];   // splits <= 8
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < splits)
+                asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v[s]) : "l"(part_tag + (size_t)s * E + e)
+                             : "memory");
+        const uint64_t t0 = bw::gtimer();
+        bool late = false;
+        for (uint32_t it = 0;; ++it) {
+            bool all = true;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+                if (s < splits && (unsigned)(v[s] >> 32) != tag) {
+                    all = false;
+                    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v[s]) : "l"(part_tag + (size_t)s * E + e)
+                                 : "memory");
+                }
+            if (all) break;
+            if (late || ((it & 15) == 15 && bw::gtimer() - t0 > kWaitNs)) {
+                if (late) break;   // read after the router's completion: take what is there
+                late = true;
+                atomicOr(err, 1u << 28);
+                pdl_wait();        // the router grid is complete: its partials are all written
+            }
+            __nanosleep(32);
+        }
+        float l = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            if (s < splits) l += __uint_as_float((uint32_t)v[s]);
+        sm[e] = route_key(l, bias ? bias[e] : 0.f, mode, sm + E + e);
+    }
+    __syncthreads();
+    block_topk(sm, E, k, ids_out, w_out, mode.sigmoid ? sm + E : nullptr, mode.scale);
 }
 
 struct GuArgs {
@@ -347,33 +383,44 @@ struct GuArgs {
     size_t rbH;                      // bytes of one gate/up row record
     const int32_t* ids;              // the token's selection [k] (the router's, or a streamed layer's)
     const unsigned* ids_ready;       // nullable: set by the router's selecting block once ids are written
-    float* h;                        // [ns][I] SwiGLU outputs times 2^2a, row-order slots
-    unsigned* hg_cnt;                // [ns][I/32] rows done per half-group; the warp that completes one
-                                     // quantises it and clears the count
-    uint8_t* hq;                     // copies x staged blocks (hq_block_bytes)
-    int copies;
+    const unsigned long long* part_tag;   // nullable: tagged router partials; every CTA selects from them
+    const unsigned* seq;             // with part_tag: the layer's decode count (the token's tag)
+    int splits;                      // with part_tag: router K-splits
+    const float* bias;               // with part_tag: router bias [E] or null
+    RouteMode mode;
+    int32_t* sel_ids;                // with part_tag: CTA 0 publishes the selection here (down reads it)
+    float* sel_wts;
+    unsigned long long* sel_tag;     // with part_tag: CTA 0 also publishes ids [k], weights [k] and the
+                                     // token exponent as tagged words (the down kernel polls them)
+    float* h;                        // copies x [ns][I] SwiGLU outputs times 2^2a, row-order slots
+    int copies;                      // replicas of the output block (<= 32): the down CTAs' reads spread over L2
     int* scale_out;                  // the token exponent a (CTA 0 writes it)
-    unsigned* shared_done;           // nullable: staged half-groups of the shared expert
+    unsigned* shared_done;           // nullable: gate/up CTAs done with the shared expert's rows
     int jj0, jj1;                    // row-order slots this launch computes
     const uint8_t* pf;               // next layer's router weights to warm into L2 (nullable)
     size_t pf_bytes;
     unsigned* err;
     unsigned long long* tr;
-    int stall_shared;                // test hook: do not count the shared expert's staged half-groups
+    int stall_shared;                // test hook: do not count the CTAs done with the shared expert's rows
 };
 
 template <int BITS, int NQ>
 __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     extern __shared__ uint4 smq[];
     __shared__ int32_t s_ids[MOE_MAX_TOP_K];
+    __shared__ float s_wsel[MOE_MAX_TOP_K];
     __shared__ float s_red[kWarps];
     __shared__ int s_skip, s_ok;
-    const int H = a.H, I = a.I, HG = H / 32, IG = I / 32, ns = a.k + a.n_shared;
+    const int H = a.H, I = a.I, HG = H / 32, ns = a.k + a.n_shared;
     uint4* xq = smq;                                                   // [4][HG]
     float* Iv = reinterpret_cast<float*>(smq + 4 * HG);                // [HG] 2^-f
     float* Xx = Iv + HG;                                               // [HG]
+    float* s_sel = Xx + HG;                                            // [select_words(E)] (part_tag only)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ktrace(a.tr, blockIdx.x, 0);
+    // the token's tag, read before any wait (the previous token's down kernel,
+    // which advanced the count, completed before the router started)
+    const unsigned tag = a.part_tag ? decode_tag(__ldcg(a.seq)) : 0u;
     if (a.pf && threadIdx.x == 0) {
         // the next layer's router weights into L2 (moe_layer_set_next): this
         // CTA's share, in 16-byte multiples, no more than 64 KB a request
@@ -391,31 +438,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     const uint64_t pol = policy_evict_first();
     const bool has_shared = a.n_shared && a.jj0 == 0;
     const int jr0 = has_shared ? 1 : a.jj0;   // first routed row-order slot
-    const size_t blk = hq_block_bytes(ns, I);
-    // pair (slot jj, row i) done: lane 0 writes h * 2^2a = (g 2^a)(u 2^a) sigmoid(g)
-    // and counts the row in its half-group; the warp that counts the 32nd row
-    // quantises the half-group
+    const size_t blk = (size_t)ns * I;   // floats of one replica
+    // pair (slot jj, row i) done: every lane holds the same warp sums, and lane
+    // c < copies writes h * 2^2a = (g 2^a)(u 2^a) sigmoid(g) into replica c
     auto done = [&](int jj, int i, float gs, float us, bool live) {
-        unsigned old = 0;
-        if (live && lane == 0) {
+        if (live && lane < a.copies) {
             const float sg = 1.0f / (1.0f + expf(-(gs * inv_a)));
-            a.h[(size_t)jj * I + i] = gs * us * sg;
-            old = atom_add_acq_rel(a.hg_cnt + jj * IG + (i >> 5), 1u);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (live && old == 31u) {   // warp-uniform
-            __syncwarp();
-            __threadfence();
-            const int hg = i >> 5;
-            stage_half_group(a.h + (size_t)jj * I + 32 * hg, jj, hg, ns, IG, a.hq, blk, a.copies);
-            __syncwarp();
-            if (lane == 0) {
-                a.hg_cnt[jj * IG + hg] = 0u;   // for the next token (its gate/up starts after this token's down)
-                if (jj == 0 && has_shared && a.shared_done && !a.stall_shared) {
-                    __threadfence();
-                    atomicAdd(a.shared_done, 1u);
-                }
-            }
+            a.h[lane * blk + (size_t)jj * I + i] = gs * us * sg;
         }
     };
     // the shared expert's rows need no routing: they overlap the router
@@ -426,21 +455,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
             [&](int p, float gs, float us, bool live) { done(0, p, gs, us, live); }, H, a.rbH, xq, Iv, Xx, pol);
     }
     ktrace(a.tr, blockIdx.x, 1);
-    // the selection: the router's selecting block raises the ready flag as
-    // soon as the ids are written (no wait for the router grid to retire); a
-    // wait that runs out falls back to the ordinary dependency wait
-    if (threadIdx.x == 0) {
-        int ok = 0;
-        if (a.ids_ready) {
-            ok = wait_count(a.ids_ready, 1u, kWaitNs) ? 1 : 0;
-            if (!ok) atomicOr(a.err, 1u << 28);
-        }
-        s_ok = ok;
+    // this CTA's shared rows are written: count it for the down kernel's early
+    // start (every writer fences its stores before the barrier)
+    if (has_shared && a.shared_done) {
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0 && !a.stall_shared) atomicAdd(a.shared_done, 1u);
     }
-    __syncthreads();
-    if (!s_ok) pdl_wait();   // the router (or, streamed, the staging of the records) is complete
-    if (threadIdx.x < a.k) s_ids[threadIdx.x] = __ldcg(a.ids + threadIdx.x);
-    __syncthreads();
+    if (a.part_tag) {
+        // the selection, computed here from the router's tagged partials as
+        // soon as they are written (no wait for the router grid to retire)
+        select_from_tagged(a.part_tag, tag, a.splits, a.E, a.k, a.bias, a.mode, s_sel, s_ids, s_wsel, a.err);
+        if (blockIdx.x == 0 && threadIdx.x < a.k) {   // for the down kernel and moe_layer_selection
+            a.sel_ids[threadIdx.x] = s_ids[threadIdx.x];
+            a.sel_wts[threadIdx.x] = s_wsel[threadIdx.x];
+            st_tagged(a.sel_tag + threadIdx.x, tag, (uint32_t)s_ids[threadIdx.x]);
+            st_tagged(a.sel_tag + a.k + threadIdx.x, tag, __float_as_uint(s_wsel[threadIdx.x]));
+            if (threadIdx.x == 0) st_tagged(a.sel_tag + 2 * a.k, tag, (uint32_t)ta);
+        }
+    } else {
+        // the router's selecting block raises the ready flag as soon as the
+        // ids are written; a wait that runs out falls back to the ordinary
+        // dependency wait
+        if (threadIdx.x == 0) {
+            int ok = 0;
+            if (a.ids_ready) {
+                ok = wait_count(a.ids_ready, 1u, kWaitNs) ? 1 : 0;
+                if (!ok) atomicOr(a.err, 1u << 28);
+            }
+            s_ok = ok;
+        }
+        __syncthreads();
+        if (!s_ok) pdl_wait();   // the router (or, streamed, the staging of the records) is complete
+        if (threadIdx.x < a.k) s_ids[threadIdx.x] = __ldcg(a.ids + threadIdx.x);
+        __syncthreads();
+    }
     pdl_trigger();   // the down kernel may launch: it starts with the shared expert's rows
     ktrace(a.tr, blockIdx.x, 2);
     if (a.jj1 > jr0) {
@@ -481,17 +530,43 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
 // combined in a fixed order: shared expert first (weight 1), then the routed
 // slots in selection order, and scaled back by 2^-2a.
 
-// Load slots [s0, s1) of a staged block (global) into the same layout in
-// shared memory. Block-wide.
-__device__ __forceinline__ void load_staged(const uint8_t* src, int s0, int s1, int ns, int IG, uint4* hq, float* Iv,
-                                            float* Xh) {
-    const uint4* g_hq = reinterpret_cast<const uint4*>(src);
-    const float* g_inv = reinterpret_cast<const float*>(g_hq + (size_t)ns * 4 * IG);
-    const float* g_X = g_inv + ns * IG;
-    for (int i = s0 * 4 * IG + threadIdx.x; i < s1 * 4 * IG; i += blockDim.x) hq[i] = __ldcg(g_hq + i);
-    for (int i = s0 * IG + threadIdx.x; i < s1 * IG; i += blockDim.x) {
-        Iv[i] = __ldcg(g_inv + i);
-        Xh[i] = __ldcg(g_X + i);
+// Quantise slots [s0, s1) of the SwiGLU outputs src[ns][I] (fp32, written by
+// the gate/up kernel, read through L2) into the staged form the dot products
+// read: slot s at hq + 4 IG s, Iv + IG s, Xh + IG s. Block-wide: each warp takes
+// blocks of 32 runs (8 half-groups) of a slot and issues the loads of
+// kStageBatch blocks before it quantises them.
+template <int kStageBatch>
+__device__ __forceinline__ void stage_slots_q16(const float* src, int s0, int s1, int I, uint4* hq, float* Iv,
+                                                float* Xh) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
+    const int nrun = I / 8, IG = I / 32, nrb = (nrun + 31) / 32;
+    const int ntask = (s1 - s0) * nrb;
+    for (int t0 = warp; t0 < ntask; t0 += kStageBatch * nw) {
+        float v[kStageBatch][8];
+        int slot[kStageBatch], run[kStageBatch];
+        bool valid[kStageBatch];
+#pragma unroll
+        for (int b = 0; b < kStageBatch; ++b) {
+            const int t = t0 + b * nw;
+            const int q = t / nrb;
+            slot[b] = s0 + q;
+            run[b] = (t - q * nrb) * 32 + lane;
+            valid[b] = t < ntask && run[b] < nrun;
+            if (valid[b]) {
+                const float4* p = reinterpret_cast<const float4*>(src + (size_t)slot[b] * I) + 2 * run[b];
+                const float4 x0 = __ldcg(p), x1 = __ldcg(p + 1);
+                v[b][0] = x0.x; v[b][1] = x0.y; v[b][2] = x0.z; v[b][3] = x0.w;
+                v[b][4] = x1.x; v[b][5] = x1.y; v[b][6] = x1.z; v[b][7] = x1.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[b][i] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kStageBatch; ++b)
+            if (t0 + b * nw < ntask)   // warp-uniform
+                stage_q16_run(v[b], valid[b], run[b], IG, hq + (size_t)slot[b] * 4 * IG, Iv + slot[b] * IG,
+                              Xh + slot[b] * IG);
     }
 }
 
@@ -510,13 +585,13 @@ __device__ __forceinline__ void down_items(int s0, int s1, int own0, int own1, i
         // on J items at a time, so that it keeps as many bytes in flight as
         // with 4-bit codes
         const int GI = IG / 2;
-        for (int it0 = warp; it0 < nit; it0 += J * kWarps) {
+        for (int it0 = warp; it0 < nit; it0 += J * kDownWarps) {
             const uint8_t* rr[J][kDownRows];
             int s2[J], n0s[J], nrs[J];
             bool live[J];
 #pragma unroll
             for (int j = 0; j < J; ++j) {
-                const int it = it0 + j * kWarps;
+                const int it = it0 + j * kDownWarps;
                 live[j] = it < nit;
                 const int itv = live[j] ? it : it0;
                 const int q = itv / nsl;
@@ -570,13 +645,13 @@ __device__ __forceinline__ void down_items(int s0, int s1, int own0, int own1, i
         // rows.
         constexpr int MB = 2 / J;
         const int M = (IG + 31) / 32;
-        for (int it0 = warp; it0 < nit; it0 += J * kWarps) {
+        for (int it0 = warp; it0 < nit; it0 += J * kDownWarps) {
             const uint8_t* rr[J][kDownRows];
             int s2[J], n0s[J], nrs[J];
             bool live[J];
 #pragma unroll
             for (int j = 0; j < J; ++j) {
-                const int it = it0 + j * kWarps;
+                const int it = it0 + j * kDownWarps;
                 live[j] = it < nit;
                 const int itv = live[j] ? it : it0;
                 const int q = itv / nsl;
@@ -649,8 +724,9 @@ struct DownArgs {
     const uint8_t* const* rec_tab;
     int k, E, n_shared, H, I;
     size_t rbI, gu_block;            // bytes of one down row record; offset of the down block in a record
-    const uint8_t* hq;               // copies x staged blocks of the SwiGLU outputs (gate/up wrote them)
+    const float* h;                  // copies x [ns][I] SwiGLU outputs (gate/up wrote them)
     int copies;
+    unsigned gu_ctas;                // gate/up CTAs that count their shared rows
     void* y;
     int y_bf16;
     float* y32;
@@ -660,12 +736,15 @@ struct DownArgs {
     unsigned* shared_done;           // with n_shared: early start on the shared rows (nullable)
     unsigned* ids_ready;             // the router's ready flag (nullable); cleared with the counters
     unsigned* down_done;             // the last CTA clears the counters
+    unsigned* seq;                   // nullable: the layer's decode count, advanced by the last CTA
+    const unsigned long long* sel_tag;   // nullable (with seq): the selection and token exponent as
+                                     // tagged words, read before the wait for gate/up
     unsigned* err;
     unsigned long long* tr;
 };
 
 template <int BITS, int J = 1>
-__global__ void __launch_bounds__(kThreads) k_down(const DownArgs a) {
+__global__ void __launch_bounds__(kDownThreads) k_down(const DownArgs a) {
     extern __shared__ uint4 smh[];
     ktrace(a.tr, blockIdx.x, 0);
     const int I = a.I, IG = I / 32, ns = a.k + a.n_shared;
@@ -675,39 +754,68 @@ __global__ void __launch_bounds__(kThreads) k_down(const DownArgs a) {
     float* ypart = Xh + ns * IG;                                         // [ns][kDownMaxRows]
     __shared__ const uint8_t* s_rows[MOE_MAX_TOP_K + 1];
     __shared__ float s_w[MOE_MAX_TOP_K + 1];
-    __shared__ int s_skip, s_early, s_scale;
+    __shared__ int s_skip, s_early, s_scale, s_have;
     // whole quads of rows per CTA (a partial quad costs a full work item)
     const int nquads_all = (a.H + kDownRows - 1) / kDownRows;
     const int own0 = kDownRows * (int)((long long)nquads_all * blockIdx.x / gridDim.x);
     const int own1 = min(a.H, kDownRows * (int)((long long)nquads_all * (blockIdx.x + 1) / gridDim.x));
     const bool counted = a.n_shared && a.shared_done;
-    const uint8_t* src = a.hq + (size_t)(blockIdx.x % a.copies) * hq_block_bytes(ns, I);   // this CTA's replica
+    const float* src = a.h + (size_t)(blockIdx.x % a.copies) * ns * I;   // this CTA's replica
     if (threadIdx.x == 0) {
-        // the shared expert's half-groups are all staged once the counter
-        // reaches I/32: its rows run before the wait for gate/up
+        // the shared expert's outputs are all written once every gate/up CTA
+        // has counted itself: its rows run before the wait for gate/up
         int ok = 0;
         if (counted) {
-            ok = wait_count(a.shared_done, (unsigned)IG, kWaitNs) ? 1 : 0;
+            ok = wait_count(a.shared_done, a.gu_ctas, kWaitNs) ? 1 : 0;
             if (!ok) atomicOr(a.err, 1u << 27);
         }
         s_early = ok;
         s_skip = 0;
+        s_have = a.sel_tag ? 1 : 0;
         if (a.n_shared) {   // slot 0: the shared expert (its record is fixed), weight 1
             s_rows[0] = a.rec_tab[a.E] + a.gu_block;
             s_w[0] = 1.0f;
         }
     }
     __syncthreads();
+    if (a.sel_tag) {
+        // the selection and the token exponent, published by gate/up CTA 0 long
+        // before this kernel starts, resolved before the wait for gate/up (a
+        // resident layer's record table does not change between launches)
+        const unsigned tag = decode_tag(__ldcg(a.seq));
+        const int nw = 2 * a.k + 1;
+        if (threadIdx.x < nw) {
+            unsigned long long v;
+            if (!poll_tagged(a.sel_tag + threadIdx.x, tag, kWaitNs, &v)) {
+                atomicOr(a.err, 1u << 25);
+                s_have = 0;   // read after the wait instead
+            }
+            const uint32_t lo = (uint32_t)v;
+            const int t = threadIdx.x;
+            if (t < a.k) {
+                int e = (int)lo;
+                if ((unsigned)e >= (unsigned)a.E) e = 0;   // a valid selection never needs the clamp
+                s_rows[a.n_shared + t] = a.rec_tab[e] + a.gu_block;
+            } else if (t < 2 * a.k) {
+                s_w[a.n_shared + t - a.k] = __uint_as_float(lo);
+            } else {
+                s_scale = (int)lo;
+            }
+        }
+        __syncthreads();
+    }
     const int early = s_early;
     if (early) {
-        load_staged(src, 0, 1, ns, IG, hq, Iv, Xh);
+        stage_slots_q16<BITS == 4 ? 4 : 2>(src, 0, 1, I, hq, Iv, Xh);
         __syncthreads();
         down_items<BITS, J>(0, 1, own0, own1, I, a.rbI, s_rows, hq, Iv, Xh, ypart);
     }
     pdl_wait();     // gate/up complete: the staged SwiGLU outputs are final
     pdl_trigger();  // the next token's router may start prefetching its weights
     ktrace(a.tr, blockIdx.x, 1);
-    if (threadIdx.x >= a.n_shared && threadIdx.x < ns) {   // the routed slots
+    const bool have = s_have;
+    __syncthreads();   // every thread has read s_have
+    if (!have && threadIdx.x >= a.n_shared && threadIdx.x < ns) {   // the routed slots
         const int s = threadIdx.x, j = s - a.n_shared;
         int e = a.sel_ids[j];
         if ((unsigned)e >= (unsigned)a.E) e = 0;   // a valid selection never needs the clamp
@@ -716,8 +824,8 @@ __global__ void __launch_bounds__(kThreads) k_down(const DownArgs a) {
         s_rows[s] = rec + a.gu_block;
         s_w[s] = a.sel_wts[j];
     }
-    if (threadIdx.x == 0) s_scale = a.scale_in ? *a.scale_in : 0;
-    load_staged(src, early, ns, ns, IG, hq, Iv, Xh);
+    if (!have && threadIdx.x == 0) s_scale = a.scale_in ? *a.scale_in : 0;
+    stage_slots_q16<BITS == 4 ? 4 : 2>(src, early, ns, I, hq, Iv, Xh);
     __syncthreads();
     ktrace(a.tr, blockIdx.x, 2);
     // a launch made before the host staged this token's experts (streamed
@@ -744,6 +852,7 @@ __global__ void __launch_bounds__(kThreads) k_down(const DownArgs a) {
         if (threadIdx.x == 0 && atomicAdd(a.down_done, 1u) == gridDim.x - 1) {
             if (a.shared_done) *a.shared_done = 0u;
             if (a.ids_ready) *a.ids_ready = 0u;
+            if (a.seq) *a.seq += 1u;   // the next token's tag
             *a.down_done = 0u;
             __threadfence();
         }
@@ -755,9 +864,10 @@ __global__ void __launch_bounds__(kThreads) k_down(const DownArgs a) {
 // launchers
 // ---------------------------------------------------------------------------
 
+// staged activations, then the per-CTA selection's scratch
 static size_t gu_smem_for(const Layer& L) {
     const int H = L.d.hidden;
-    return (size_t)H * 2 + (size_t)(H / 32) * 8;
+    return (size_t)H * 2 + (size_t)(H / 32) * 8 + (size_t)select_words(L.d.n_experts) * 4;
 }
 static size_t down_smem(int I, int ns) {
     return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8 + (size_t)ns * kDownMaxRows * 4;
@@ -783,7 +893,6 @@ static DownKernel down_kernel(const Layer& L) {
     return (L.d.inter / 32 + 31) / 32 == 1 ? k_down<4, 2> : k_down<4, 1>;
 }
 
-size_t decode_hq_block_bytes(int ns, int I) { return hq_block_bytes(ns, I); }
 
 cudaError_t decode_kernel_setup(Layer& L) {
     const int H = L.d.hidden, I = L.d.inter, ns = L.d.top_k + L.d.n_shared;
@@ -798,7 +907,7 @@ cudaError_t decode_kernel_setup(Layer& L) {
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, gu, kThreads, L.gu_smem);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, dn, kThreads, down_smem(I, ns));
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, dn, kDownThreads, down_smem(I, ns));
     if (e != cudaSuccess) return e;
     if (L.occ_gu < 1 || L.occ_down < 1) return cudaErrorInvalidConfiguration;
     // rows owned by one down CTA must fit its partial-sum buffer
@@ -824,9 +933,15 @@ static cudaError_t launch_gateup(Layer& L, const void* x, const DecodeScratch& b
     a.rbH = row_bytes(d.hidden, L.wbits);
     a.ids = b.ids;
     a.ids_ready = b.ids_ready;
+    a.part_tag = b.part_tag;
+    a.seq = b.seq;
+    a.splits = L.router_splits;
+    a.bias = (const float*)L.router_bias;
+    a.mode = L.route_mode();
+    a.sel_ids = b.ids;
+    a.sel_wts = b.wts;
+    a.sel_tag = b.sel_tag;
     a.h = b.h;
-    a.hg_cnt = b.hg_cnt;
-    a.hq = b.hq;
     a.copies = b.copies;
     a.scale_out = b.scale;
     a.shared_done = b.shared_done;
@@ -853,8 +968,9 @@ static cudaError_t launch_down(Layer& L, const DecodeScratch& b, void* y, float*
     a.I = d.inter;
     a.rbI = row_bytes(d.inter, L.wbits);
     a.gu_block = gu_block_bytes(d.hidden, d.inter, L.wbits);
-    a.hq = b.hq;
+    a.h = b.h;
     a.copies = b.copies;
+    a.gu_ctas = (unsigned)gu_grid(L);
     a.y = y;
     a.y_bf16 = d.act_dtype == MOE_BF16 ? 1 : 0;
     a.y32 = y_f32;
@@ -863,10 +979,12 @@ static cudaError_t launch_down(Layer& L, const DecodeScratch& b, void* y, float*
     a.scale_in = b.scale;
     a.shared_done = b.shared_done;
     a.ids_ready = b.ids_ready;
-    a.down_done = (b.shared_done || b.ids_ready) ? b.down_done : nullptr;
+    a.seq = b.seq;
+    a.sel_tag = b.seq ? b.sel_tag : nullptr;
+    a.down_done = (b.shared_done || b.ids_ready || b.seq) ? b.down_done : nullptr;
     a.err = error_word(L);
     a.tr = tr;
-    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(kThreads), down_smem(d.inter, ns), s, pdl, a);
+    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(kDownThreads), down_smem(d.inter, ns), s, pdl, a);
 }
 
 // gate/up over row-order slots jj0..jj1-1 and (with `down`) down + combine,
@@ -898,11 +1016,11 @@ DecodeScratch layer_decode_scratch(Layer& L, bool fast) {
     b.scale = reinterpret_cast<int*>(L.counters + CNT_TOKEN_SCALE);
     b.router_cnt = L.counters + CNT_ROUTER;
     b.h = L.h;
-    b.hg_cnt = L.hg_cnt;
-    b.hq = L.hq;
     b.copies = kHCopies;
     if (fast) {
-        b.ids_ready = L.counters + CNT_IDS_READY;
+        b.part_tag = L.part_tag;
+        b.seq = L.counters + CNT_DECODE_SEQ;
+        b.sel_tag = L.sel_tag;
         b.shared_done = L.counters + CNT_SHARED_DONE;
         b.down_done = L.counters + CNT_DOWN_DONE;
     }

@@ -42,21 +42,19 @@ CtxGetCurrentFn ctx_get_current() {
 
 inline size_t up256(size_t n) { return (n + 255) / 256 * 256; }
 
-constexpr int kParts = 9;
+constexpr int kParts = 7;
 
 // Byte offsets of the pieces within the region; the last entry is the total.
 void layout(const Layer& L, size_t off[kParts]) {
     const auto& d = L.d;
-    const size_t E = d.n_experts, k = d.top_k, I = d.inter, ns = k + d.n_shared;
+    const size_t E = d.n_experts, k = d.top_k, I = d.inter;
     off[0] = 0;                                                  // partial logits [splits][E]
     off[1] = off[0] + up256((size_t)L.router_splits * E * 4);    // keys [E]
     off[2] = off[1] + up256(E * 4);                              // ids [k]
     off[3] = off[2] + up256(k * 4);                              // weights [k]
     off[4] = off[3] + up256(k * 4);                              // the token's scale exponent
-    off[5] = off[4] + up256(4);                                  // SwiGLU outputs [k + 1][I] fp32
-    off[6] = off[5] + up256((k + 1) * I * 4);                    // half-group counters [k + 1][I / 32]
-    off[7] = off[6] + up256((k + 1) * (I / 32) * 4);             // one staged block of the SwiGLU outputs
-    off[8] = off[7] + up256(decode_hq_block_bytes((int)ns, (int)I));
+    off[5] = off[4] + up256(4);                                  // SwiGLU outputs [k + 1][I] fp32 (one replica)
+    off[6] = off[5] + up256((k + 1) * I * 4);
 }
 
 DecodeScratch carve(Layer& L, unsigned char* base) {
@@ -70,8 +68,6 @@ DecodeScratch carve(Layer& L, unsigned char* base) {
     s.scale = reinterpret_cast<int*>(base + off[4]);
     s.router_cnt = L.counters + CNT_ROUTER;   // the layer's own (zero between launches)
     s.h = reinterpret_cast<float*>(base + off[5]);
-    s.hg_cnt = reinterpret_cast<unsigned*>(base + off[6]);
-    s.hq = base + off[7];
     s.copies = 1;
     return s;   // no ready flag and no early start: nothing else in the region must start at zero
 }

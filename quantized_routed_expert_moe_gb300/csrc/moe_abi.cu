@@ -182,11 +182,11 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     Alloc sc;
     size_t o_part = sc.add((size_t)std::max(L.router_splits, L.router_splits_tok) * E * 4 * std::max(1, T));
     size_t o_logits = sc.add((size_t)T * E * 4);
+    size_t o_ptag = sc.add((size_t)L.router_splits * E * 8);
+    size_t o_stag = sc.add((size_t)(2 * k + 1) * 8);
     size_t o_ids = sc.add((size_t)T * k * 4);
     size_t o_w = sc.add((size_t)T * k * 4);
-    size_t o_h = sc.add((size_t)(k + 1) * I * 4);
-    size_t o_hq = sc.add((size_t)kDecodeHCopies * decode_hq_block_bytes(k + d.n_shared, I));
-    size_t o_hgc = sc.add((size_t)(k + 1) * (I / 32) * 4);
+    size_t o_h = sc.add((size_t)kDecodeHCopies * (k + 1) * I * 4);
     size_t o_cnt = sc.add(64 * 4);
     // prefill block layout
     const int rows = T * k + T * d.n_shared;
@@ -306,11 +306,11 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
         TRY_CUDA(cudaMemset(base, 0, sc.total));
         L.logits_part = reinterpret_cast<float*>(base + o_part);
         L.logits = reinterpret_cast<float*>(base + o_logits);
+        L.part_tag = reinterpret_cast<unsigned long long*>(base + o_ptag);
+        L.sel_tag = reinterpret_cast<unsigned long long*>(base + o_stag);
         L.ids = reinterpret_cast<int32_t*>(base + o_ids);
         L.wts = reinterpret_cast<float*>(base + o_w);
         L.h = reinterpret_cast<float*>(base + o_h);
-        L.hq = base + o_hq;
-        L.hg_cnt = reinterpret_cast<unsigned*>(base + o_hgc);
         L.counters = reinterpret_cast<unsigned*>(base + o_cnt);
     }
     if (T > 1) {
@@ -381,13 +381,19 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
     if (!g.ok) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (L.d.cache_slots > 0) return cache_decode(L, x, y, y_f32, s);
-    // the router selects in its last block and raises the ready flag that
-    // gate/up waits for; the down kernel starts early on the shared expert
+    // the router writes tagged partial logits, every gate/up CTA selects from
+    // them; the down kernel starts early on the shared expert
     const DecodeScratch b = layer_decode_scratch(L, true);
     cudaError_t e = launch_route_decode(L, x, s, 1, nullptr, nullptr, 0, nullptr, &b);
-    if (e != cudaSuccess) return cuda_fail(e, "router launch");
-    e = launch_experts_decode(L, x, y, y_f32, b, 0, L.d.top_k + L.d.n_shared, true, true, true, s);
-    if (e != cudaSuccess) return cuda_fail(e, "expert launch");
+    if (e == cudaSuccess) e = launch_experts_decode(L, x, y, y_f32, b, 0, L.d.top_k + L.d.n_shared, true, true, true, s);
+    if (e != cudaSuccess) {
+        // the token did not run to its end, so the decode count did not
+        // advance: clear the tagged partials so that the next token cannot
+        // take this one's for its own
+        cudaMemsetAsync(L.part_tag, 0, (size_t)L.router_splits * L.d.n_experts * 8, s);
+        cudaMemsetAsync(L.sel_tag, 0, (size_t)(2 * L.d.top_k + 1) * 8, s);
+        return cuda_fail(e, "decode launch");
+    }
     return MOE_OK;
 }
 

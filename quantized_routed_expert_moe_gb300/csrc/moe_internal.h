@@ -176,11 +176,11 @@ struct Layer {
     // decode scratch
     float* logits_part = nullptr;   // [max(router_splits, router_splits_tok)][max_tokens][E]
     float* logits = nullptr;        // [max_tokens][E]
+    unsigned long long* part_tag = nullptr;   // [router_splits][E] tagged partial logits (fast decode)
+    unsigned long long* sel_tag = nullptr;    // [2k + 1] the fast decode's selection, tagged
     int32_t* ids = nullptr;         // [max_tokens][k]
     float* wts = nullptr;           // [max_tokens][k]
-    float* h = nullptr;             // SwiGLU outputs [k + 1][I] fp32 (times 2^2a, the token scale)
-    uint8_t* hq = nullptr;          // kDecodeHCopies staged blocks of them (16-bit fixed point per half-group)
-    unsigned* hg_cnt = nullptr;     // [k + 1][I / 32] rows done per half-group (zero between launches)
+    float* h = nullptr;             // SwiGLU outputs, kDecodeHCopies x [k + 1][I] fp32 (times 2^2a, the token scale)
     unsigned* counters = nullptr;   // [64] counters and words of the decode kernels (CNT_*)
     int router_splits = 1;       // split-K of the one-token router
     int router_splits_tok = 1;   // split-K of the multi-token router (<= 16)
@@ -222,6 +222,7 @@ enum {
     CNT_SHARED_DONE = 1,   // decode gate/up CTAs whose shared-expert rows are written
     CNT_DOWN_DONE = 2,     // decode down CTAs done (the last one clears the decode counters)
     CNT_IDS_READY = 3,     // the router's selecting block has published the selection (decode)
+    CNT_DECODE_SEQ = 4,    // fast decodes of the layer so far (the tag of the next one's router partials)
     CNT_TOKEN_SCALE = 8,   // the token exponent a of the last decode (int)
     CNT_ERR = 20           // error bits of bounded device waits (moe_layer_check)
 };
@@ -234,8 +235,8 @@ inline unsigned* error_word(Layer& L) { return L.counters + CNT_ERR; }
 // dc (nullable): the selecting block also runs the device-managed cache's LFU step
 // Scratch one decode token works on: the router's outputs (partials, keys,
 // selection, and the ready flag the decode's gate/up waits for), the SwiGLU
-// outputs, their half-group counters and staged blocks, and the counters the
-// down kernel's early start uses (null: no early start).
+// outputs (`copies` replicas of [k + 1][I] fp32), and the counters the down
+// kernel's early start uses (null: no early start).
 struct DecodeScratch {
     float* part = nullptr;
     float* logits = nullptr;
@@ -245,15 +246,18 @@ struct DecodeScratch {
     unsigned* router_cnt = nullptr;
     unsigned* ids_ready = nullptr;
     float* h = nullptr;
-    unsigned* hg_cnt = nullptr;
-    uint8_t* hq = nullptr;
     int copies = 1;
+    // fast decode: the router's partials as tagged 64-bit words [splits][E]
+    // (tag in the high half), from which every gate/up CTA selects; seq
+    // counts the layer's decodes (the down kernel's last CTA advances it)
+    unsigned long long* part_tag = nullptr;
+    unsigned* seq = nullptr;
+    unsigned long long* sel_tag = nullptr;   // [2k + 1]: ids, weights, token exponent (tagged)
     unsigned* shared_done = nullptr;
     unsigned* down_done = nullptr;
 };
 // the layer's own scratch; `fast`: with the ready flag and the early start
 DecodeScratch layer_decode_scratch(Layer& L, bool fast);
-size_t decode_hq_block_bytes(int ns, int I);   // bytes of one staged block
 
 // out (nullable): where the partials, keys and selection go (default: the
 // layer's scratch, no ready flag)
@@ -268,7 +272,7 @@ cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y
 // K-splits of the prefill router GEMM: at most this many partial logit sets
 // are summed (in a fixed order) per token.
 constexpr int kMaxTokSplits = 32;
-constexpr int kDecodeHCopies = 8;   // replicas of the decode SwiGLU outputs (decode.cu)
+constexpr int kDecodeHCopies = 8;   // replicas of the decode SwiGLU outputs (decode.cu), <= 32
 // gate/up over row-order slots jj0..jj1-1 and (down) the down kernel, over scratch b
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, const DecodeScratch& b, int jj0,
                                   int jj1, bool down, bool pdl, bool trace, cudaStream_t s);

@@ -27,8 +27,8 @@ using namespace bw;
 // pairs in the order (0,4) (1,5) (2,6) (3,7): masking the nibbles at bits 0
 // and 16, then 4 and 20, and so on. The activation operands (x gathered here,
 // h written by the gate/up epilogue) are stored in the same order within every
-// block of 8 along K, so the products pair up as in the plain dot product.
-__host__ __device__ constexpr int blk_pos(int j) { return ((j & 3) << 1) | (j >> 2); }
+// block of 8 along K (element j at place ((j & 3) << 1) | (j >> 2)), so the
+// products pair up as in the plain dot product.
 
 // ---------------------------------------------------------------------------
 // permutation (histogram, exclusive scan, stable scatter) -- one CTA
@@ -222,6 +222,7 @@ constexpr size_t kBarBytes = 8 * (2 * kStages + 2 * kRawStages + 4) + 16;
 constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kB16 + (size_t)kRawStages * kRaw + kBarBytes;
 static_assert(kRaw % 1024 == 0 && kB16 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kTmemA + kStages * kACols <= kTmemCols, "weight stages exceed tensor memory");
+static_assert(2 * kBatchSlots <= kStages, "the token-copy barriers share the operand barriers' space");
 
 struct GemmArgs {
     const int32_t* gexp;
@@ -313,14 +314,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRaw);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kRawStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    const uint32_t b_full = saddr(bars), b_empty = b_full + 8 * kStages;
+    const uint32_t b_full = saddr(bars), b_tfull = b_full + 8 * kBatchSlots, b_empty = b_full + 8 * kStages;
     const uint32_t b_rfull = b_empty + 8 * kStages, b_rempty = b_rfull + 8 * kRawStages;
     const uint32_t b_afull = b_rempty + 8 * kRawStages, b_aempty = b_afull + 16;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kBatchSlots; ++s) {
-            mbar_init(b_full + 8 * s, kDqWarps + 1);
+            mbar_init(b_full + 8 * s, kDqWarps);   // the dequantisers' tensor-memory stores
+            mbar_init(b_tfull + 8 * s, 1);         // the token copies (the issuer's expect_tx + bytes)
             mbar_init(b_empty + 8 * s, 1);
         }
         for (int r = 0; r < kRawStages; ++r) {
@@ -354,13 +356,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
         }
         __syncwarp();
         const uint64_t pol_w = l2_evict_first();
-        uint32_t rit = 0;
-        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+        uint32_t rit = 0;   // copies issued
+        bool go = true;
+        for (int w = blockIdx.x; go && w < n_items; w += gridDim.x) {
             const int g = w / a.n_mt, mt = w - g * a.n_mt;
             const int e = a.gexp[g];
             for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++rit) {
                 const uint32_t rs = rit % kRawStages;
-                tw(b_rempty + 8 * rs, ((rit / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                const bool ok = tw(b_rempty + 8 * rs, ((rit / kRawStages) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                // after an abort nothing more is issued: a stage is only ever
+                // refilled once its consumers have released it, so each stage
+                // has at most one copy in flight and the drain below sees them all
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { go = false; break; }
                 if (elect_one()) {
                     mbar_arrive_tx(b_rfull + 8 * rs, BITS == 4 ? kRaw : kRaw2Tx);
                     const uint32_t rd = saddr(raw + rs * kRaw);
@@ -372,8 +379,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 __syncwarp();
             }
         }
-        // copies in flight land before the CTA exits (on the normal path the
-        // consumers have already waited for all of them)
+        // every copy issued lands before the CTA exits, also after an abort
+        // (on the normal path the consumers have already waited for all of them)
         const uint32_t n_tail = rit < (uint32_t)kRawStages ? rit : (uint32_t)kRawStages;
         for (uint32_t q = rit - n_tail; q < rit; ++q) {
             int dummy = 0;
@@ -390,8 +397,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
         }
         __syncwarp();
         const uint64_t pol_b = l2_evict_last();
-        uint32_t bt = 0;
-        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+        uint32_t bt = 0;   // operand blocks issued
+        bool go = true;
+        for (int w = blockIdx.x; go && w < n_items; w += gridDim.x) {
             const int g = w / a.n_mt;
             const int off = a.goff[g], m = a.gcnt[g];
             // one copy per chunk: the smallest box of 16, 32, 64 or 128 token rows that holds the group
@@ -400,15 +408,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
             for (int kb = 0; kb * kChunksPerRaw < nk; ++kb, ++bt) {
                 const uint32_t bs = bt % kBatchSlots;
                 const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
-                tw(b_empty + 8 * bs, ((bt / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                const bool ok = tw(b_empty + 8 * bs, ((bt / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_TMA);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { go = false; break; }   // as the raw copies
                 if (elect_one()) {
-                    mbar_arrive_tx(b_full + 8 * bs, (uint32_t)nc * b_bytes);
+                    mbar_arrive_tx(b_tfull + 8 * bs, (uint32_t)nc * b_bytes);
                     for (int c = 0; c < nc; ++c)
                         tma_load_2d(saddr(bst + (bs * kChunksPerRaw + c) * kB16), tmb, (kc0 + c) * 64, off,
-                                    b_full + 8 * bs, pol_b);
+                                    b_tfull + 8 * bs, pol_b);
                 }
                 __syncwarp();
             }
+        }
+        // every copy issued lands before the CTA exits (its own barrier: the
+        // dequantisers' arrivals are counted elsewhere)
+        const uint32_t n_tail = bt < (uint32_t)kBatchSlots ? bt : (uint32_t)kBatchSlots;
+        for (uint32_t q = bt - n_tail; q < bt; ++q) {
+            int dummy = 0;
+            mbar_wait(b_tfull + 8 * (q % kBatchSlots), (q / kBatchSlots) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
         // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows) and
@@ -515,7 +531,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 // one wait and one commit per block of up to 4 chunks (16 MMAs)
                 const uint32_t bs = bt % kBatchSlots;
                 const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
-                tw(b_full + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);
+                tw(b_tfull + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);   // token operand
+                tw(b_full + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);    // weight operand
                 tc_fence_after();
                 if (elect_one()) {
                     for (int c = 0; c < nc; ++c) {
@@ -766,7 +783,6 @@ cudaError_t prefill_kernel_setup(Layer& L) {
 }
 
 moe_status prefill_cache_maps(Layer& L) {
-    const auto& d = L.d;
     auto& pf = L.pf;
     if (!pf.xp) return MOE_OK;
     const uint8_t* slots = cache_slots_base(L);

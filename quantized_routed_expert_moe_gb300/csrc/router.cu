@@ -33,8 +33,8 @@ constexpr int kWarps = kThreads / 32;
 // dependent launch, the weight slice is prefetched into L2 before waiting for
 // the preceding kernel (the activations may come from it); the partials are
 // then reduced in split order by the last CTA to finish, which selects and
-// writes ids, weights and logits. It also clears the per-slot |h| maxima the
-// gate/up kernel of this token accumulates.
+// writes ids, weights and logits.
+//
 // One token's access to a device-managed cache (thread 0, on the slot state
 // the block staged in shared memory: se expert, sc count, sl last use). The
 // policy is the host's (cache.cu) step for step, with the counts and last uses
@@ -182,7 +182,8 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     const float* __restrict__ bias, float* __restrict__ part, float* __restrict__ logits,
     int32_t* __restrict__ ids, float* __restrict__ wts, int k, unsigned* __restrict__ counter,
     int select, RouteMode mode, int32_t* ids_pub, unsigned* seq_pub, unsigned seq, DevCacheArgs dc,
-    unsigned* ids_ready, unsigned* hg_clear, int n_clear, unsigned long long* __restrict__ tr) {
+    unsigned* ids_ready, unsigned long long* part_tag, const unsigned* seq_word,
+    unsigned long long* __restrict__ tr) {
     extern __shared__ float sm[];
     __shared__ unsigned s_last;
     const int cta = blockIdx.y * gridDim.x + blockIdx.x;
@@ -199,14 +200,6 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
     }
     pdl_wait();
-    if (hg_clear) {
-        // the decode's half-group counters start at zero (the previous kernel
-        // in the stream has completed; gate/up launches after every CTA's trigger)
-        const int nthr = gridDim.x * gridDim.y * blockDim.x;
-        for (int i = cta * blockDim.x + threadIdx.x; i < n_clear; i += nthr) hg_clear[i] = 0u;
-        __threadfence();
-        __syncthreads();
-    }
     pdl_trigger();
     ktrace(tr, cta, 1);
     for (int i4 = threadIdx.x; i4 < Ls / 4; i4 += blockDim.x) {
@@ -223,7 +216,19 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     __syncthreads();
     if (e < E) {
         const float acc = router_warp_dot<Q8>(W, reinterpret_cast<const float*>(sm), H, E, e, k0, Ls);
-        if (lane == 0) part[(size_t)blockIdx.y * E + e] = acc;
+        if (lane == 0) {
+            if (part_tag) {
+                // tagged partial: the token's tag beside the value in one
+                // 64-bit store, which readers poll for (no fence, no counter)
+                const unsigned long long w =
+                    ((unsigned long long)decode_tag(__ldcg(seq_word)) << 32) | __float_as_uint(acc);
+                asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(part_tag + (size_t)blockIdx.y * E + e),
+                             "l"(w)
+                             : "memory");
+            } else {
+                part[(size_t)blockIdx.y * E + e] = acc;
+            }
+        }
     }
     __syncthreads();
     ktrace(tr, cta, 2);
@@ -246,14 +251,13 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
         float l = 0.f;
 #pragma unroll
         for (int s = 0; s < 8; ++s) l += v[s];
-        // keys in sm[0, E), sigmoid scores in sm[E, 2E), key images after them
+        // keys in sm[0, E), sigmoid scores in sm[E, 2E)
         const float key = route_key(l, bias ? bias[e2] : 0.f, mode, sm + E + e2);
         sm[e2] = key;
         logits[e2] = key;
     }
     __syncthreads();
-    block_topk_rank(sm, reinterpret_cast<uint32_t*>(sm + ((2 * E + 3) & ~3)), E, k, ids, wts,
-                    mode.sigmoid ? sm + E : nullptr, mode.scale);
+    block_topk(sm, E, k, ids, wts, mode.sigmoid ? sm + E : nullptr, mode.scale);
     // the decode's gate/up waits for this flag instead of the grid's end
     // (thread 0 wrote the ids and weights)
     if (threadIdx.x == 0 && ids_ready) {
@@ -406,16 +410,15 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
         logits[(size_t)t * E + e] = key;
     }
     __syncthreads();
-    block_topk_rank(sl, reinterpret_cast<uint32_t*>(sl + ((2 * E + 3) & ~3)), E, k, ids + (size_t)t * k,
-                    wts + (size_t)t * k, mode.sigmoid ? sl + E : nullptr, mode.scale);
+    block_topk(sl, E, k, ids + (size_t)t * k, wts + (size_t)t * k, mode.sigmoid ? sl + E : nullptr, mode.scale);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 
-// keys [E], scores [E] and key images [round4(E)], 16-byte aligned
-static int select_smem_words(int E) { return ((2 * E + 3) & ~3) + ((E + 3) & ~3); }
+// keys [E], then sigmoid scores [E]
+static int select_smem_words(int E) { return 2 * E; }
 
 static size_t router_smem(const Layer& L) {
     // x slice, or the selection's arrays, or a device-managed cache's slot state
@@ -444,14 +447,14 @@ cudaError_t launch_route_decode(Layer& L, const void* x, cudaStream_t s, int sel
     float* wts = out ? out->wts : L.wts;
     unsigned* cnt = out ? out->router_cnt : L.counters + CNT_ROUTER;
     unsigned* ready = out ? out->ids_ready : nullptr;
-    unsigned* hgc = out ? out->hg_cnt : L.hg_cnt;
-    const int n_clear = (d.top_k + 1) * (d.inter / 32);
+    unsigned long long* ptag = out ? out->part_tag : nullptr;   // tagged partials, no selection here
+    if (ptag) select = 0;
     auto kern = d.router_fmt == MOE_W_F32 ? k_router_decode<false> : k_router_decode<true>;
     prof_begin(L, K_ROUTER_DECODE, s);
     const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), router_smem(L), s, L.pdl, L.router, x, xb, d.hidden,
                                      d.n_experts, L.router_splits, (const float*)L.router_bias, part, logits, ids, wts,
-                                     d.top_k, cnt, select, L.route_mode(), ids_pub, seq_pub, seq, dca, ready, hgc,
-                                     n_clear, L.split_trace(0));
+                                     d.top_k, cnt, select, L.route_mode(), ids_pub, seq_pub, seq, dca, ready,
+                                     ptag, out ? out->seq : nullptr, L.split_trace(0));
     prof_end(L, s);
     return e;
 }
