@@ -356,6 +356,17 @@ moe_status moe_cache_residency(const moe_layer* layer, int32_t* slot_expert);
 moe_status moe_cache_usage(const moe_layer* layer, uint64_t* counts);
 moe_status moe_cache_pin(moe_layer* layer, const int32_t* experts, int32_t n);
 
+/* The hottest experts by a usage count: out (host int32 [n]) receives the n
+ * experts with the largest counts[e] (host uint64 [n_experts]), the lower id
+ * first among equal counts. Host only, no device. MOE_E_INVALID for NULL
+ * pointers or n outside 0..n_experts. */
+moe_status moe_hottest(const uint64_t* counts, int32_t n_experts, int32_t n, int32_t* out);
+
+/* The learning cache's step in one call: moe_cache_usage, then moe_cache_pin
+ * of the n hottest experts by those counts (moe_hottest's order). The same
+ * errors and synchronisation as the two calls. */
+moe_status moe_cache_pin_hottest(moe_layer* layer, int32_t n);
+
 /* The cache policy alone, on the host (no device, no layer): runs n_tokens
  * tokens of k distinct expert ids each (ids: host int32 [n_tokens][k], values
  * in 0..n_experts-1) through an empty `slots`-slot cache exactly as a streamed

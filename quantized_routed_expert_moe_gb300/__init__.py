@@ -27,7 +27,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_E_INVALID", 2: "MOE_E_UNSUPPORTED", 3: "MOE_E_NOM
 # every symbol include/moe.h declares
 EXPORTS = ("moe_layer_create", "moe_layer_destroy", "moe_expert_record_bytes", "moe_pack_expert_record",
            "moe_layer_device_bytes", "moe_layer_set_next", "moe_layer_set_router_scoring", "moe_route", "moe_layer_selection", "moe_decode", "moe_decode_static_scratch", "moe_prefill_chunk",
-           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_cache_usage", "moe_cache_pin", "moe_lfu_trace", "moe_lfu_trace_pinned",
+           "moe_decode_tokens_host", "moe_cache_stage", "moe_cache_prefetch", "moe_cache_prefetch_stats", "moe_cache_stats", "moe_cache_residency", "moe_cache_usage", "moe_cache_pin", "moe_hottest", "moe_cache_pin_hottest", "moe_lfu_trace", "moe_lfu_trace_pinned",
            "moe_profile_start", "moe_profile_stop", "moe_layer_set_option", "moe_layer_check", "moe_trace_read_split",
            "moe_status_str", "moe_last_error")
 
@@ -126,6 +126,10 @@ def lib() -> ctypes.CDLL:
             L.moe_cache_usage.argtypes = [vp, vp]
             L.moe_cache_pin.restype = st
             L.moe_cache_pin.argtypes = [vp, vp, ctypes.c_int32]
+            L.moe_hottest.restype = st
+            L.moe_hottest.argtypes = [vp, i32, i32, vp]
+            L.moe_cache_pin_hottest.restype = st
+            L.moe_cache_pin_hottest.argtypes = [vp, i32]
             L.moe_lfu_trace.restype = st
             L.moe_lfu_trace.argtypes = [i32, i32, i32, i32, vp, vp, vp]
             L.moe_lfu_trace_pinned.restype = st
@@ -359,6 +363,22 @@ def moe_cache_pin(handle, experts) -> None:
            "moe_cache_pin")
 
 
+def moe_hottest(counts, n: int):
+    """The n experts with the largest counts, the lower id first among equal
+    counts (the library's ordering, host only)."""
+    import numpy as np
+    c = np.ascontiguousarray(np.asarray(counts, dtype=np.uint64))
+    out = np.zeros(max(n, 0), np.int32)
+    _check(lib().moe_hottest(ctypes.c_void_p(c.ctypes.data), len(c), n, ctypes.c_void_p(out.ctypes.data)),
+           "moe_hottest")
+    return out
+
+
+def moe_cache_pin_hottest(handle, n: int) -> None:
+    """Pin the n most used experts of a streamed layer so far."""
+    _check(lib().moe_cache_pin_hottest(handle, n), "moe_cache_pin_hottest")
+
+
 def moe_profile_start(handle, max_launches: int) -> None:
     _check(lib().moe_profile_start(handle, max_launches), "moe_profile_start")
 
@@ -490,10 +510,7 @@ class MoELayer:
 
     def pin_hottest(self, n):
         """Pin the n most used experts so far (ties: the lower id first)."""
-        import numpy as np
-        use = self.cache_usage()
-        order = sorted(range(len(use)), key=lambda e: (-int(use[e]), e))
-        self.cache_pin(np.array(order[:n], np.int32))
+        moe_cache_pin_hottest(self.handle, n)
 
     def set_option(self, option, value):
         moe_layer_set_option(self.handle, option, value)

@@ -828,6 +828,30 @@ moe_status moe_cache_pin(moe_layer* layer, const int32_t* experts, int32_t n) {
     return moe::cache_pin(L, experts, n);
 }
 
+moe_status moe_hottest(const uint64_t* counts, int32_t n_experts, int32_t n, int32_t* out) {
+    if (!counts || (!out && n > 0)) return moe::fail(MOE_E_INVALID, "NULL argument");
+    if (n_experts < 0 || n < 0 || n > n_experts) return moe::fail(MOE_E_INVALID, "n must be in 0..n_experts");
+    std::vector<int32_t> order(n_experts);
+    for (int32_t e = 0; e < n_experts; ++e) order[e] = e;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return counts[a] > counts[b]; });
+    for (int32_t i = 0; i < n; ++i) out[i] = order[i];
+    return MOE_OK;
+}
+
+moe_status moe_cache_pin_hottest(moe_layer* layer, int32_t n) {
+    if (!layer) return moe::fail(MOE_E_INVALID, "NULL layer");
+    if (!layer->L.cache) return moe::fail(MOE_E_STATE, "layer is not streamed (cache_slots == 0)");
+    const int32_t E = layer->L.d.n_experts;
+    if (n < 0 || n > E) return moe::fail(MOE_E_INVALID, "n must be in 0..n_experts");
+    std::vector<uint64_t> use(E);
+    moe_status st = moe_cache_usage(layer, use.data());
+    if (st != MOE_OK) return st;
+    std::vector<int32_t> hot(n);
+    st = moe_hottest(use.data(), E, n, hot.data());
+    if (st != MOE_OK) return st;
+    return moe_cache_pin(layer, n ? hot.data() : nullptr, n);
+}
+
 moe_status moe_cache_usage(const moe_layer* layer, uint64_t* counts) {
     if (!layer || !counts) return moe::fail(MOE_E_INVALID, "NULL argument");
     const moe::Layer& L = layer->L;

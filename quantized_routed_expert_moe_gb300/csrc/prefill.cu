@@ -222,7 +222,6 @@ constexpr size_t kBarBytes = 8 * (2 * kStages + 2 * kRawStages + 4) + 16;
 constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kB16 + (size_t)kRawStages * kRaw + kBarBytes;
 static_assert(kRaw % 1024 == 0 && kB16 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kTmemA + kStages * kACols <= kTmemCols, "weight stages exceed tensor memory");
-static_assert(2 * kBatchSlots <= kStages, "the token-copy barriers share the operand barriers' space");
 
 struct GemmArgs {
     const int32_t* gexp;
@@ -314,15 +313,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRaw);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kRawStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    const uint32_t b_full = saddr(bars), b_tfull = b_full + 8 * kBatchSlots, b_empty = b_full + 8 * kStages;
+    const uint32_t b_full = saddr(bars), b_empty = b_full + 8 * kStages;
     const uint32_t b_rfull = b_empty + 8 * kStages, b_rempty = b_rfull + 8 * kRawStages;
     const uint32_t b_afull = b_rempty + 8 * kRawStages, b_aempty = b_afull + 16;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kBatchSlots; ++s) {
-            mbar_init(b_full + 8 * s, kDqWarps);   // the dequantisers' tensor-memory stores
-            mbar_init(b_tfull + 8 * s, 1);         // the token copies (the issuer's expect_tx + bytes)
+            mbar_init(b_full + 8 * s, kDqWarps + 1);   // dequantisers' stores + the token copies
             mbar_init(b_empty + 8 * s, 1);
         }
         for (int r = 0; r < kRawStages; ++r) {
@@ -411,20 +409,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 const bool ok = tw(b_empty + 8 * bs, ((bt / kBatchSlots) & 1) ^ 1, s_abort, a.err, ERR_TMA);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) { go = false; break; }   // as the raw copies
                 if (elect_one()) {
-                    mbar_arrive_tx(b_tfull + 8 * bs, (uint32_t)nc * b_bytes);
+                    mbar_arrive_tx(b_full + 8 * bs, (uint32_t)nc * b_bytes);
                     for (int c = 0; c < nc; ++c)
                         tma_load_2d(saddr(bst + (bs * kChunksPerRaw + c) * kB16), tmb, (kc0 + c) * 64, off,
-                                    b_tfull + 8 * bs, pol_b);
+                                    b_full + 8 * bs, pol_b);
                 }
                 __syncwarp();
             }
         }
-        // every copy issued lands before the CTA exits (its own barrier: the
-        // dequantisers' arrivals are counted elsewhere)
+        // every copy issued lands before the CTA exits: the operand barrier's
+        // phase of an issued block completes once its copy has landed (the
+        // dequantisers arrive for every block, after an abort too)
         const uint32_t n_tail = bt < (uint32_t)kBatchSlots ? bt : (uint32_t)kBatchSlots;
         for (uint32_t q = bt - n_tail; q < bt; ++q) {
             int dummy = 0;
-            mbar_wait(b_tfull + 8 * (q % kBatchSlots), (q / kBatchSlots) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
+            mbar_wait(b_full + 8 * (q % kBatchSlots), (q / kBatchSlots) & 1, &dummy, a.err, ERR_DRAIN, 50000000ull);
         }
     } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
         // lane quarter q (tensor-memory lanes 32q..32q+31 = weight rows) and
@@ -531,8 +530,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                 // one wait and one commit per block of up to 4 chunks (16 MMAs)
                 const uint32_t bs = bt % kBatchSlots;
                 const int kc0 = kb * kChunksPerRaw, nc = min(nk - kc0, kChunksPerRaw);
-                tw(b_tfull + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);   // token operand
-                tw(b_full + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);    // weight operand
+                tw(b_full + 8 * bs, (bt / kBatchSlots) & 1, s_abort, a.err, ERR_MMA);
                 tc_fence_after();
                 if (elect_one()) {
                     for (int c = 0; c < nc; ++c) {

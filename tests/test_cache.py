@@ -64,6 +64,31 @@ def test_lfu_policy_golden_trace():
                 assert slot[t][j] == slot[t - 1][list(rows[t - 1][0]).index(e)] if e in rows[t - 1][0] else True
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_hottest_matches_oracle(seed):
+    """The library's ordering of experts by usage (moe_hottest, which
+    moe_cache_pin_hottest pins) equals the oracle's learning-cache "hottest" on
+    seeded Zipf traces, ties included."""
+    E, k, T = 64, 8, 40
+    rows = zipf_rows(seed, T, E, k)
+    sim = oracle.moe.LFUCache(16)
+    for r in rows:
+        sim.access([int(e) for e in r])
+    counts = np.zeros(E, np.uint64)
+    for e, c in sim.usage.items():
+        counts[e] = c
+    n_used = len(sim.usage)
+    for n in (0, 1, 6, n_used):
+        assert list(moe.moe_hottest(counts, n)) == sim.hottest(n)
+
+
+def test_hottest_rejects_bad_n():
+    counts = np.zeros(8, np.uint64)
+    for n in (-1, 9):
+        with pytest.raises(moe.MoEError):
+            moe.moe_hottest(counts, n)
+
+
 def test_lfu_policy_rejects_bad_rows():
     with pytest.raises(moe.MoEError):
         moe.moe_lfu_trace(4, 8, np.array([[1, 1]], np.int32))
