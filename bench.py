@@ -124,7 +124,8 @@ def dist_info():
     return ws, rank, local
 
 
-KERNEL_SOURCES = {"gateup_decode": ("decode.cu", "common.cuh"), "decode_fused": ("decode_fused.cu", "common.cuh")}
+KERNEL_SOURCES = {"gateup_decode": ("decode.cu", "common.cuh"),
+                  "prefill_gemm_gateup": ("prefill.cu", "sm100.cuh", "common.cuh")}
 
 
 def kernel_source_sha(kernel: str) -> str:
@@ -347,6 +348,15 @@ def run_prefill(args, emit=True):
     # the binding roof is the one the kernel is closer to; the other rides along
     main, other = (hbm_roof, tensor_roof) if (hbm_roof["frac"] or 0) > (tensor_roof["frac"] or 0) \
         else (tensor_roof, hbm_roof)
+    # DRAM traffic per launch from a stored ncu capture of the same sources
+    # (a smaller layer of the same shape), scaled to this launch by the
+    # algorithmic bytes (the expert groups streamed)
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", f"prefill_gemm_gateup_{args.workload}_traffic.json")
+    if os.path.exists(tf):
+        tj = json.load(open(tf))
+        if tj.get("kernel_source_sha") == kernel_source_sha("prefill_gemm_gateup"):
+            traffic = tj["bytes_per_launch"] * gu_bytes / tj["algorithmic_bytes_per_launch"]
     chunk_flops = flops_gu + flops_down + flops_router
     if rank != 0:
         if ws > 1:
@@ -360,7 +370,7 @@ def run_prefill(args, emit=True):
                    "l2": f"inputs larger than L2: {R} rotating layer replicas",
                    "parallelism": f"replicas x{ws}"},
         "chunk_tflops": chunk_flops * R * args.steps * ws / (ms / 1e3) / 1e12,
-        "roofline": dict(main, traffic=None, kernel="prefill_gemm_gateup", avg_launch_us=gu_avg_s * 1e6,
+        "roofline": dict(main, traffic=traffic, kernel="prefill_gemm_gateup", avg_launch_us=gu_avg_s * 1e6,
                          other_roof=other, expert_groups=n_groups),
         "kernels": kernels,
         "e2e": {"value": total_tokens / e2e_s, "unit": UNIT,
@@ -873,6 +883,36 @@ def decode_bench(args, name, spec, workload):
             a, b = prof.get(kname, (0, 0.0))
             prof[kname] = (a + n, b + t)
 
+    # phase trace (--trace): tokens decoded with MOE_OPT_TRACE on; per kernel,
+    # the per-CTA global-timer stamps (start, dependency met, main work done,
+    # end) relative to the router's first CTA, median and last CTA
+    phases = None
+    if getattr(args, "trace", False):
+        phases = []
+        n_tr = min(T, 8 * R)
+        for rep_i in range(3):
+            for h in handles:
+                moe.moe_layer_set_option(h, 3, 1)
+            for t in range(n_tr):
+                st = dec(handles[t % R], xb + t * row, yb + t * row, None, sp)
+                if st:
+                    raise moe.MoEError(st, "moe_decode", moe.moe_last_error())
+            torch.cuda.synchronize()
+            tr = moe.moe_trace_read_split(handles[(n_tr - 1) % R])
+            for h in handles:
+                moe.moe_layer_set_option(h, 3, 0)
+            base = min(c[0] for c in tr[0] if c[0])
+            ph = {}
+            for kk, kn in enumerate(("router", "gateup", "down")):
+                cs = np.array([c for c in tr[kk] if c[0]], dtype=np.float64)
+                if len(cs) == 0:
+                    continue
+                cs = (cs - base) / 1e3
+                ph[kn] = {"ctas": int(len(cs)),
+                          **{f"{p}_{w}": round(float(f(cs[:, i])), 2)
+                             for i, p in enumerate(moe.SPLIT_TRACE_POINTS) for w, f in (("med", np.median), ("max", np.max))}}
+            phases.append(ph)
+
     # per-token intervals: one step again with an event after every token. The
     # events sit between consecutive tokens' kernels (they block the overlap of
     # the next token's router prologue with this token's tail), so these are an
@@ -994,6 +1034,7 @@ def decode_bench(args, name, spec, workload):
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "avg_launch_us": dom_avg_ms * 1e3},
         "kernels": kernels,
+        **({"phase_trace_us": phases} if phases is not None else {}),
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
                 "path": "pinned host -> device copy of the step's tokens, moe_decode per token over the same "
@@ -1090,6 +1131,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
                     help="default workload: print the GLM-scale decode line without the other configurations")
+    ap.add_argument("--trace", action="store_true",
+                    help="decode workloads: add the kernels' per-CTA phase stamps of a few tokens to the line")
     ap.add_argument("--experts", type=int, default=None,
                     help="override the routed-expert count (a smaller layer of the same shape, for profiler captures)")
     args = ap.parse_args()

@@ -198,7 +198,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     size_t o_xexp = pf.add((size_t)T * 4);
     size_t o_rexp = pf.add((size_t)rows * 4);
     size_t o_hmax = pf.add((size_t)rows * 4);
-    size_t o_zexp = pf.add((size_t)rows * 4);
+    size_t o_zexp = pf.add((size_t)rows * 8);
     size_t o_gexp = pf.add((size_t)(E + 1) * 4);
     size_t o_goff = pf.add((size_t)(E + 1) * 4);
     size_t o_gcnt = pf.add((size_t)(E + 1) * 4);
@@ -324,7 +324,7 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
         L.pf.xexp = reinterpret_cast<int32_t*>(base + o_xexp);
         L.pf.rexp = reinterpret_cast<int32_t*>(base + o_rexp);
         L.pf.hmax = reinterpret_cast<unsigned*>(base + o_hmax);
-        L.pf.zexp = reinterpret_cast<int32_t*>(base + o_zexp);
+        L.pf.zfac = reinterpret_cast<float2*>(base + o_zexp);
         L.pf.group_expert = reinterpret_cast<int32_t*>(base + o_gexp);
         L.pf.group_off = reinterpret_cast<int32_t*>(base + o_goff);
         L.pf.group_cnt = reinterpret_cast<int32_t*>(base + o_gcnt);

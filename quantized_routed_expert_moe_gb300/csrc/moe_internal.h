@@ -93,7 +93,7 @@ struct PrefillScratch {
     int32_t* xexp = nullptr;          // [T] token activation exponents a
     int32_t* rexp = nullptr;          // [rows] a of each permuted row's token
     unsigned* hmax = nullptr;         // [rows] max |h32| of each row (float bits)
-    int32_t* zexp = nullptr;          // [rows] z of each row: hp = h * 2^z
+    float2* zfac = nullptr;           // [rows] (2^-e, 2^-a) of each row: hp = h * 2^(e + 2a)
     int max_rows = 0;
     // TMA descriptors: gate/up codes, gate/up meta, down codes, down meta, then
     // xp and hp with boxes of 16, 32, 64 and 128 token rows; on streamed layers

@@ -219,7 +219,8 @@ constexpr uint32_t kRawCodes = 128 * 128, kRawMeta = 128 * 16, kRaw = kRawCodes 
 constexpr uint32_t kRawCodes2 = 128 * 64, kRaw2Tx = kRawCodes2 + kRawMeta;
 constexpr uint32_t kTmemCols = 512, kTmemA = 256, kACols = 32;
 constexpr size_t kBarBytes = 8 * (2 * kStages + 2 * kRawStages + 4) + 16;
-constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kB16 + (size_t)kRawStages * kRaw + kBarBytes;
+constexpr size_t kZfBytes = 2 * 128 * 8;   // down epilogue: the tile's row factors, two tiles
+constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kB16 + (size_t)kRawStages * kRaw + kBarBytes + kZfBytes;
 static_assert(kRaw % 1024 == 0 && kB16 % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 static_assert(kTmemA + kStages * kACols <= kTmemCols, "weight stages exceed tensor memory");
 
@@ -235,7 +236,7 @@ struct GemmArgs {
     int ld_out;
     const int32_t* rexp;   // gate/up: each permuted row's activation exponent a
     unsigned* hmax;        // gate/up: each row's max |h * 2^(2a)| (float bits)
-    const int32_t* zexp;   // down: each row's operand exponent z (h * 2^z in binary16)
+    const float2* zfac;    // down: each row's (2^-e, 2^-a); its operand is h * 2^(e + 2a) in binary16
     unsigned* err;
     unsigned long long* tr;   // [gridDim][4]: wait cycles of copy / dequant / MMA, total cycles; or null
 };
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRaw);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kRawStages + 4);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    float2* s_zf = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);   // [2][128]
     const uint32_t b_full = saddr(bars), b_empty = b_full + 8 * kStages;
     const uint32_t b_rfull = b_empty + 8 * kStages, b_rempty = b_rfull + 8 * kRawStages;
     const uint32_t b_afull = b_rempty + 8 * kRawStages, b_aempty = b_afull + 16;
@@ -561,8 +563,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
             const int off = a.goff[g], m = a.gcnt[g];
             const int N = ((m + 15) >> 4) << 4;
             const uint32_t acc = tile & 1;
+            // down: each thread fetches one of the tile's row factors while the
+            // accumulator is still being computed; the four epilogue warps then
+            // share them through shared memory (double-buffered by tile)
+            float2 fz = make_float2(0.f, 0.f);
+            if (MODE == 1 && row < m) fz = __ldg(a.zfac + off + row);
             tw(b_afull + 8 * acc, (tile >> 1) & 1, s_abort, a.err, ERR_EPI);
             tc_fence_after();
+            if (MODE == 1) {
+                s_zf[acc * 128 + row] = fz;
+                asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+            }
             const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16) + acc * 128;
             for (int c0 = 0; c0 < N; c0 += 16) {
                 float v[16];
@@ -598,15 +609,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
                         if (lane < 2 && col < m) atomicMax(a.hmax + off + col, lane ? mo : me);
                     }
                 } else {
-                    // the operand was h * 2^z: scale back exactly (one rounding
-                    // only if the result is subnormal)
+                    // the operand was h * 2^(e + 2a): scale back by 2^-e, 2^-a
+                    // and 2^-a, exact powers of two (one rounding only if the
+                    // result is subnormal)
                     const int n = mt * 128 + row;
                     float* yp = static_cast<float*>(a.out);
                     if (n < a.rows_out) {
+                        float2 f[16];   // the same for every lane
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) f[j] = s_zf[acc * 128 + c0 + j];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             if (c0 + j < m)
-                                yp[(size_t)(off + c0 + j) * a.ld_out + n] = ldexpf(v[j], -__ldg(a.zexp + off + c0 + j));
+                                yp[(size_t)(off + c0 + j) * a.ld_out + n] = v[j] * f[j].x * f[j].y * f[j].y;
                     }
                 }
             }
@@ -630,13 +645,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
 //
 // Row r of the listed groups: hp[r] = fp16(h32[r] * 2^e_r) in the
 // dequantiser's order within each block of 8, e_r from the row's max |h32|
-// (fp16_fit_exp), and z_r = e_r + 2 a_r, so that hp[r] = h * 2^z_r. Grid
+// (fp16_fit_exp), so that hp[r] = h * 2^(e_r + 2 a_r); zfac[r] = (2^-e_r,
+// 2^-a_r), by which the down GEMM's epilogue scales the row back. Grid
 // (groups of the list, blocks per group); a CTA past the list's group count
 // does nothing.
 __global__ void __launch_bounds__(256) k_pf_hconv(const float* __restrict__ h32, const unsigned* __restrict__ hmax,
                                                   const int32_t* __restrict__ rexp, const int32_t* __restrict__ goff,
                                                   const int32_t* __restrict__ gcnt, const int32_t* __restrict__ n_groups,
-                                                  int I, uint4* __restrict__ hp, int32_t* __restrict__ zexp) {
+                                                  int I, uint4* __restrict__ hp, float2* __restrict__ zfac) {
     const int g = blockIdx.x;
     if (g >= *n_groups) return;
     const int off = goff[g], cnt = gcnt[g], nb = I / 8;
@@ -654,7 +670,7 @@ __global__ void __launch_bounds__(256) k_pf_hconv(const float* __restrict__ h32,
             o[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
         hp[(size_t)r * nb + b] = make_uint4(o[0], o[1], o[2], o[3]);
-        if (b == 0) zexp[r] = e + 2 * rexp[r];
+        if (b == 0) zfac[r] = make_float2(exp2i(-e), exp2i(-rexp[r]));   // |e|, |a| <= 126: normal floats
     }
 }
 
@@ -848,11 +864,11 @@ cudaError_t launch_gemm_pair(Layer& L, int wmap, const int32_t* gexp, const int3
     if (e != cudaSuccess) return e;
     prof_begin(L, K_PF_HCONV, s);
     k_pf_hconv<<<dim3(d.n_experts + 1, 8), 256, 0, s>>>(pf.h32, pf.hmax, pf.rexp, goff, gcnt, n_groups, I,
-                                                         static_cast<uint4*>(pf.hp), pf.zexp);
+                                                         static_cast<uint4*>(pf.hp), pf.zfac);
     prof_end(L, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    GemmArgs dn{gexp, goff, gcnt, n_groups, I, (H + 127) / 128, H, pf.yp, H, nullptr, nullptr, pf.zexp, pf.err,
+    GemmArgs dn{gexp, goff, gcnt, n_groups, I, (H + 127) / 128, H, pf.yp, H, nullptr, nullptr, pf.zfac, pf.err,
                 L.split_trace(4)};
     prof_begin(L, K_PF_GEMM_DOWN, s);
     (L.wbits == 4 ? k_pf_gemm<1, 4> : k_pf_gemm<1, 2>)<<<L.num_sms, kGemmThreads, kGemmSmem, s>>>(
