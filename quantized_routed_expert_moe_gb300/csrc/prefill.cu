@@ -649,15 +649,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_pf_gemm(const __grid_consta
 // 2^-a_r), by which the down GEMM's epilogue scales the row back. Grid
 // (groups of the list, blocks per group); a CTA past the list's group count
 // does nothing.
+// all_rows > 0: every row of [0, all_rows) (a whole chunk), the grid strided
+// over (row, block of 8) pairs; the group list is not read.
 __global__ void __launch_bounds__(256) k_pf_hconv(const float* __restrict__ h32, const unsigned* __restrict__ hmax,
                                                   const int32_t* __restrict__ rexp, const int32_t* __restrict__ goff,
                                                   const int32_t* __restrict__ gcnt, const int32_t* __restrict__ n_groups,
-                                                  int I, uint4* __restrict__ hp, float2* __restrict__ zfac) {
-    const int g = blockIdx.x;
-    if (g >= *n_groups) return;
-    const int off = goff[g], cnt = gcnt[g], nb = I / 8;
-    for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < cnt * nb; idx += gridDim.y * blockDim.x) {
-        const int r = off + idx / nb, b = idx - (idx / nb) * nb;
+                                                  int all_rows, int I, uint4* __restrict__ hp,
+                                                  float2* __restrict__ zfac) {
+    const int nb = I / 8;
+    int off = 0, cnt = all_rows;
+    long idx0 = (long)blockIdx.x * blockDim.x + threadIdx.x, stride = (long)gridDim.x * blockDim.x;
+    if (all_rows == 0) {
+        const int g = blockIdx.x;
+        if (g >= *n_groups) return;
+        off = goff[g];
+        cnt = gcnt[g];
+        idx0 = (long)blockIdx.y * blockDim.x + threadIdx.x;
+        stride = (long)gridDim.y * blockDim.x;
+    }
+    for (long idx = idx0; idx < (long)cnt * nb; idx += stride) {
+        const int r = off + (int)(idx / nb), b = (int)(idx - (idx / nb) * nb);
         const int e = fp16_fit_exp(__uint_as_float(__ldcg(hmax + r)));
         const float sc = exp2i(e);
         const float4* src = reinterpret_cast<const float4*>(h32 + (size_t)r * I + 8 * b);
@@ -849,8 +860,10 @@ cudaError_t launch_permute_gather(Layer& L, const void* x, int T, cudaStream_t s
 // gate/up + SwiGLU and down GEMMs over a list of groups; `wmap` selects the
 // weight maps (0: device records, 12: cache slots); group g's expert field is
 // the record (or slot) index the maps address
+// all_rows > 0: the groups cover rows [0, all_rows) (a whole chunk); 0: a
+// wave's subset of the groups
 cudaError_t launch_gemm_pair(Layer& L, int wmap, const int32_t* gexp, const int32_t* goff, const int32_t* gcnt,
-                             const int32_t* n_groups, cudaStream_t s) {
+                             const int32_t* n_groups, int all_rows, cudaStream_t s) {
     const auto& d = L.d;
     const int H = d.hidden, I = d.inter;
     auto& pf = L.pf;
@@ -863,8 +876,14 @@ cudaError_t launch_gemm_pair(Layer& L, int wmap, const int32_t* gexp, const int3
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     prof_begin(L, K_PF_HCONV, s);
-    k_pf_hconv<<<dim3(d.n_experts + 1, 8), 256, 0, s>>>(pf.h32, pf.hmax, pf.rexp, goff, gcnt, n_groups, I,
-                                                         static_cast<uint4*>(pf.hp), pf.zfac);
+    if (all_rows > 0) {
+        const long items = (long)all_rows * (I / 8);
+        k_pf_hconv<<<(int)std::min<long>((items + 255) / 256, (long)L.num_sms * 4), 256, 0, s>>>(
+            pf.h32, pf.hmax, pf.rexp, goff, gcnt, n_groups, all_rows, I, static_cast<uint4*>(pf.hp), pf.zfac);
+    } else {
+        k_pf_hconv<<<dim3(d.n_experts + 1, 8), 256, 0, s>>>(pf.h32, pf.hmax, pf.rexp, goff, gcnt, n_groups, 0, I,
+                                                             static_cast<uint4*>(pf.hp), pf.zfac);
+    }
     prof_end(L, s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -894,7 +913,8 @@ cudaError_t launch_prefill(Layer& L, const void* x, int T, void* y, float* y_f32
     auto& pf = L.pf;
     cudaError_t e = launch_permute_gather(L, x, T, s);
     if (e != cudaSuccess) return e;
-    e = launch_gemm_pair(L, 0, pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups, s);
+    e = launch_gemm_pair(L, 0, pf.group_expert, pf.group_off, pf.group_cnt, pf.n_groups,
+                         T * (L.d.top_k + L.d.n_shared), s);
     if (e != cudaSuccess) return e;
     return launch_combine(L, T, y, y_f32, s);
 }
@@ -948,7 +968,7 @@ moe_status launch_prefill_streamed(Layer& L, const void* x, int T, void* y, floa
         }
         const int len = 1 + 3 * n;
         MOE_CUDA_TRY(cudaMemcpyAsync(wd + o, w, (size_t)len * 4, cudaMemcpyHostToDevice, s));
-        MOE_CUDA_TRY(launch_gemm_pair(L, wmap, wd + o + 1, wd + o + 1 + n, wd + o + 1 + 2 * n, wd + o, s));
+        MOE_CUDA_TRY(launch_gemm_pair(L, wmap, wd + o + 1, wd + o + 1 + n, wd + o + 1 + 2 * n, wd + o, 0, s));
         o += len;
         ++pf.waves;
         return MOE_OK;

@@ -386,8 +386,26 @@ __global__ void __launch_bounds__(kThreads) k_topk_tokens(const float* __restric
     __shared__ float s_red[kWarps];
     const int t = blockIdx.x;
     if (xexp) {   // the token's activation exponent (prefill chunks)
+        // 8 activations per 16-byte load (H is a multiple of 64)
         float m = 0.f;
-        for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(load_act(x, x_bf16, (size_t)t * H + i)));
+        for (int r = threadIdx.x; r < H / 8; r += blockDim.x) {
+            float v[8];
+            if (x_bf16) {
+                const uint4 q = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (size_t)t * H) + r);
+                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[2 * i] = __uint_as_float(w4[i] << 16);
+                    v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+                }
+            } else {
+                const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * H) + 2 * r;
+                const float4 a = __ldg(p), b = __ldg(p + 1);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
