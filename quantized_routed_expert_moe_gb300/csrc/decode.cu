@@ -338,9 +338,9 @@ __device__ void select_from_tagged(const unsigned long long* part_tag, unsigned 
                                    const float* bias, RouteMode mode, float* sm, int32_t* ids_out, float* w_out,
                                    unsigned* err) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        unsigned long long v[8];   // splits <= 8
+        unsigned long long v[kMaxRouterSplits];
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
+        for (int s = 0; s < kMaxRouterSplits; ++s)
             if (s < splits)
                 asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v[s]) : "l"(part_tag + (size_t)s * E + e)
                              : "memory");
@@ -349,7 +349,7 @@ __device__ void select_from_tagged(const unsigned long long* part_tag, unsigned 
         for (uint32_t it = 0;; ++it) {
             bool all = true;
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
+            for (int s = 0; s < kMaxRouterSplits; ++s)
                 if (s < splits && (unsigned)(v[s] >> 32) != tag) {
                     all = false;
                     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v[s]) : "l"(part_tag + (size_t)s * E + e)
@@ -366,7 +366,7 @@ __device__ void select_from_tagged(const unsigned long long* part_tag, unsigned 
         }
         float l = 0.f;
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
+        for (int s = 0; s < kMaxRouterSplits; ++s)
             if (s < splits) l += __uint_as_float((uint32_t)v[s]);
         sm[e] = route_key(l, bias ? bias[e] : 0.f, mode, sm + E + e);
     }

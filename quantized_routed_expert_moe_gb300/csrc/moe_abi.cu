@@ -59,9 +59,13 @@ static size_t router_bytes(const moe_layer_desc& d) {
     return E * H + E * (H / 64) * 4;
 }
 
-static int pick_router_splits(int H) {
-    for (int s : {8, 4, 2})
-        if ((H / 64) % s == 0) return s;
+// K-splits of the one-token router: the most (at most kMaxRouterSplits, each
+// a whole number of 64-wide groups) that keep its grid of ceil(E/8) x splits
+// CTAs within two per SM, so that small layers still spread over the GPU
+static int pick_router_splits(int H, int E, int num_sms) {
+    const int cta_cols = (E + 7) / 8;
+    for (int s = kMaxRouterSplits; s > 1; --s)
+        if ((H / 64) % s == 0 && cta_cols * s <= 2 * std::max(num_sms, 1)) return s;
     return 1;
 }
 
@@ -168,12 +172,12 @@ moe_status moe_layer_create(const moe_layer_desc* desc, const moe_router* router
     L.device = device;
     L.wbits = d.expert_fmt == MOE_W_Q2G64 ? 2 : 4;
     L.rec_bytes = record_bytes(d.hidden, d.inter, L.wbits);
-    L.router_splits = pick_router_splits(d.hidden);
+    cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, device);
+    L.router_splits = pick_router_splits(d.hidden, d.n_experts, L.num_sms);
     // prefill router GEMM: enough K-splits for two CTAs per SM at 128 tokens
     // (each split a whole number of 64-wide groups)
     L.router_splits_tok = ((d.hidden / 64) % kMaxTokSplits == 0) ? kMaxTokSplits
                           : ((d.hidden / 64) % 16 == 0) ? 16 : L.router_splits;
-    cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, device);
 
     const int E = d.n_experts, H = d.hidden, I = d.inter, k = d.top_k, T = d.max_tokens;
     const size_t n_rec = (d.cache_slots == 0) ? (size_t)E + d.n_shared : (size_t)d.n_shared;

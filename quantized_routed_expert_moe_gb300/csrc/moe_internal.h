@@ -272,6 +272,7 @@ cudaError_t launch_experts_decode_sel(Layer& L, const void* x, void* y, float* y
 // K-splits of the prefill router GEMM: at most this many partial logit sets
 // are summed (in a fixed order) per token.
 constexpr int kMaxTokSplits = 32;
+constexpr int kMaxRouterSplits = 16;   // K-splits of the one-token router (moe_abi.cu)
 constexpr int kDecodeHCopies = 8;   // replicas of the decode SwiGLU outputs (decode.cu), <= 32
 // gate/up over row-order slots jj0..jj1-1 and (down) the down kernel, over scratch b
 cudaError_t launch_experts_decode(Layer& L, const void* x, void* y, float* y_f32, const DecodeScratch& b, int jj0,

@@ -698,14 +698,23 @@ __global__ void __launch_bounds__(256) k_pf_combine(const float* __restrict__ yp
     const int32_t* pt = pos + (size_t)t * (k + 1);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (n_shared) acc = __ldcg(reinterpret_cast<const float4*>(yp + (size_t)pt[k] * H + n));
-    for (int j = 0; j < k; ++j) {
-        const float w = wts[(size_t)t * k + j];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(yp + (size_t)pt[j] * H + n));
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-    }
+    // every slot's outputs in flight at once, then summed in slot order
+    float4 v[MOE_MAX_TOP_K];
+    float w[MOE_MAX_TOP_K];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOP_K; ++j)
+        if (j < k) {
+            w[j] = wts[(size_t)t * k + j];
+            v[j] = __ldcg(reinterpret_cast<const float4*>(yp + (size_t)pt[j] * H + n));
+        }
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOP_K; ++j)
+        if (j < k) {
+            acc.x = fmaf(w[j], v[j].x, acc.x);
+            acc.y = fmaf(w[j], v[j].y, acc.y);
+            acc.z = fmaf(w[j], v[j].z, acc.z);
+            acc.w = fmaf(w[j], v[j].w, acc.w);
+        }
     const size_t o = (size_t)t * H + n;
     if (y32) *reinterpret_cast<float4*>(y32 + o) = acc;
     if (y) {

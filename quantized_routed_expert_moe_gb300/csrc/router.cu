@@ -245,12 +245,13 @@ __global__ void __launch_bounds__(kThreads) k_router_decode(
     if (!s_last) { ktrace(tr, cta, 3); return; }
     __threadfence();
     for (int e2 = threadIdx.x; e2 < E; e2 += blockDim.x) {
-        float v[8];
+        float v[kMaxRouterSplits];
 #pragma unroll
-        for (int s = 0; s < 8; ++s) v[s] = (s < splits) ? __ldcg(part + (size_t)s * E + e2) : 0.f;   // splits <= 8
+        for (int s = 0; s < kMaxRouterSplits; ++s) v[s] = (s < splits) ? __ldcg(part + (size_t)s * E + e2) : 0.f;
         float l = 0.f;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) l += v[s];
+        for (int s = 0; s < kMaxRouterSplits; ++s)
+            if (s < splits) l += v[s];
         // keys in sm[0, E), sigmoid scores in sm[E, 2E)
         const float key = route_key(l, bias ? bias[e2] : 0.f, mode, sm + E + e2);
         sm[e2] = key;
