@@ -393,20 +393,23 @@ moe_status moe_lfu_trace_pinned(int32_t slots, int32_t n_experts, int32_t k, int
 /* ---- options and health ----------------------------------------------------------- */
 
 /* moe_decode on a resident layer runs three kernels chained with programmatic
- * dependent launch: the router (logits, then the top-k selection in its last
- * block, which raises a ready flag); gate/up + SwiGLU (computes the shared
- * expert's rows while the router runs and counts each CTA done with them,
- * waits for the flag, then the routed experts' rows); down + combine (starts
- * on the shared expert's rows once every gate/up CTA has counted itself, then
- * waits for gate/up and computes the routed experts). Device-side waits on the
- * flag and the counter are bounded (0.2 s) and fall back to the ordinary
- * wait. */
+ * dependent launch: the router (partial logits over K-splits, each written
+ * with the token's tag in one 64-bit word); gate/up + SwiGLU (computes the
+ * shared expert's rows while the router runs, then every CTA polls the tagged
+ * partials, selects the top k itself and computes its share of the routed
+ * experts' rows; CTA 0 publishes the selection as tagged words); down +
+ * combine (reads the published selection before its wait, then waits for
+ * gate/up and computes the shared and routed experts' rows and the fixed-order
+ * combine). Device-side polls are bounded (0.2 s) and fall back to the
+ * ordinary dependency wait, recording MOE_E_TIMEOUT for moe_layer_check. */
 enum {
-    /* Test hook for failure detection: while nonzero, the decode gate/up
-     * kernel never counts its CTAs done with the shared expert's rows, so the down
-     * kernel's bounded wait on the count runs out (0.2 s), records
-     * MOE_E_TIMEOUT for moe_layer_check and computes the shared expert after
-     * its ordinary wait instead (the output is unchanged). */
+    /* Test hook for failure detection: while nonzero, the decode kernels also
+     * run an early start on the shared expert (gate/up counts its CTAs done
+     * with the shared expert's rows; down computes them once all are counted),
+     * and gate/up never counts, so the down kernel's bounded wait on the count
+     * runs out (0.2 s), records MOE_E_TIMEOUT for moe_layer_check and computes
+     * the shared expert after its ordinary wait instead (the output is
+     * unchanged). */
     MOE_OPT_TEST_STALL_SHARED = 2,
     /* Phase tracing of the decode kernels and the prefill GEMMs: while
      * nonzero, every CTA records timestamps; read them with

@@ -804,6 +804,13 @@ __global__ void __launch_bounds__(kDownThreads) k_down(const DownArgs a) {
         }
         __syncthreads();
     }
+    // Every thread of this CTA has read the decode count and the counters: the
+    // CTA counts itself now, and the one counted last clears them at its end
+    // (every CTA has read them by then). The count's return is needed only
+    // there, so its round trip overlaps the work; the next token's kernels see
+    // the cleared words once this grid has completed.
+    unsigned order = 0;
+    if (a.down_done && threadIdx.x == 0) order = atomicAdd(a.down_done, 1u);
     const int early = s_early;
     if (early) {
         stage_slots_q16<BITS == 4 ? 4 : 2>(src, 0, 1, I, hq, Iv, Xh);
@@ -845,17 +852,11 @@ __global__ void __launch_bounds__(kDownThreads) k_down(const DownArgs a) {
             }
         }
     }
-    if (a.down_done) {
-        // the last CTA to finish clears the counters for the next token (whose
-        // router and gate/up start only after this grid has completed)
-        __syncthreads();
-        if (threadIdx.x == 0 && atomicAdd(a.down_done, 1u) == gridDim.x - 1) {
-            if (a.shared_done) *a.shared_done = 0u;
-            if (a.ids_ready) *a.ids_ready = 0u;
-            if (a.seq) *a.seq += 1u;   // the next token's tag
-            *a.down_done = 0u;
-            __threadfence();
-        }
+    if (a.down_done && threadIdx.x == 0 && order == gridDim.x - 1) {
+        if (a.shared_done) *a.shared_done = 0u;
+        if (a.ids_ready) *a.ids_ready = 0u;
+        if (a.seq) *a.seq += 1u;   // the next token's tag
+        *a.down_done = 0u;
     }
     ktrace(a.tr, blockIdx.x, 3);
 }
@@ -944,7 +945,12 @@ static cudaError_t launch_gateup(Layer& L, const void* x, const DecodeScratch& b
     a.h = b.h;
     a.copies = b.copies;
     a.scale_out = b.scale;
-    a.shared_done = b.shared_done;
+    // The count of CTAs done with the shared expert's rows (a fence and a
+    // barrier in every CTA before its selection) feeds the down kernel's early
+    // start on the shared expert; down CTAs start only as gate/up CTAs retire,
+    // so that start gains nothing and the fence costs the selection a loaded
+    // round trip. Only the bounded-wait test hook turns it on.
+    a.shared_done = L.test_stall_shared ? b.shared_done : nullptr;
     a.jj0 = jj0;
     a.jj1 = jj1;
     a.pf = (const uint8_t*)L.next_router;
@@ -977,7 +983,7 @@ static cudaError_t launch_down(Layer& L, const DecodeScratch& b, void* y, float*
     a.sel_ids = b.ids;
     a.sel_wts = b.wts;
     a.scale_in = b.scale;
-    a.shared_done = b.shared_done;
+    a.shared_done = L.test_stall_shared ? b.shared_done : nullptr;   // see launch_gateup
     a.ids_ready = b.ids_ready;
     a.seq = b.seq;
     a.sel_tag = b.seq ? b.sel_tag : nullptr;
