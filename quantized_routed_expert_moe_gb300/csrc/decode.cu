@@ -416,11 +416,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     float* Iv = reinterpret_cast<float*>(smq + 4 * HG);                // [HG] 2^-f
     float* Xx = Iv + HG;                                               // [HG]
     float* s_sel = Xx + HG;                                            // [select_words(E)] (part_tag only)
+    // [E + 1] the record table (part_tag only: a resident layer's, fixed)
+    const uint8_t** s_rtab = reinterpret_cast<const uint8_t**>(s_sel + select_words(a.E));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     ktrace(a.tr, blockIdx.x, 0);
     // the token's tag, read before any wait (the previous token's down kernel,
     // which advanced the count, completed before the router started)
     const unsigned tag = a.part_tag ? decode_tag(__ldcg(a.seq)) : 0u;
+    // a resident layer's record table into shared memory while the router
+    // runs: the routed rows' addresses then need no load after the selection
+    if (a.part_tag)
+        for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtab[i] = a.rec_tab[i];
+    const uint8_t* const* tab = a.part_tag ? s_rtab : a.rec_tab;
     if (a.pf && threadIdx.x == 0) {
         // the next layer's router weights into L2 (moe_layer_set_next): this
         // CTA's share, in 16-byte multiples, no more than 64 KB a request
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     };
     // the shared expert's rows need no routing: they overlap the router
     if (has_shared) {
-        const uint8_t* rec = a.rec_tab[a.E];   // fixed for the layer's lifetime
+        const uint8_t* rec = tab[a.E];   // fixed for the layer's lifetime
         gu_phase<BITS, NQ>(
             blockIdx.x * kWarps + warp, gridDim.x * kWarps, I, [&](int p) { return rec + (size_t)2 * p * a.rbH; },
             [&](int p, float gs, float us, bool live) { done(0, p, gs, us, live); }, H, a.rbH, xq, Iv, Xx, pol);
@@ -495,19 +502,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     if (a.jj1 > jr0) {
         // streamed layers: a launch made before the host has staged this
         // token's experts finds a missing expert's record null and does
-        // nothing (the host launches again once every expert is resident)
-        if (threadIdx.x == 0) {
-            int bad = 0;
-            for (int jj = jr0; jj < a.jj1; ++jj) bad |= a.rec_tab[row_slot_expert(jj, a.k, a.E, a.n_shared, s_ids)] == nullptr;
-            s_skip = bad;
+        // nothing (the host launches again once every expert is resident); a
+        // resident layer's records are never null
+        if (!a.part_tag) {
+            if (threadIdx.x == 0) {
+                int bad = 0;
+                for (int jj = jr0; jj < a.jj1; ++jj)
+                    bad |= a.rec_tab[row_slot_expert(jj, a.k, a.E, a.n_shared, s_ids)] == nullptr;
+                s_skip = bad;
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        if (!s_skip)
+        if (a.part_tag || !s_skip)
             gu_phase<BITS, NQ>(
                 blockIdx.x * kWarps + warp, gridDim.x * kWarps, (a.jj1 - jr0) * I,
                 [&](int p) {
                     const int jj = jr0 + p / I, i = p - (p / I) * I;
-                    return a.rec_tab[row_slot_expert(jj, a.k, a.E, a.n_shared, s_ids)] + (size_t)2 * i * a.rbH;
+                    return tab[row_slot_expert(jj, a.k, a.E, a.n_shared, s_ids)] + (size_t)2 * i * a.rbH;
                 },
                 [&](int p, float gs, float us, bool live) {
                     const int jj = jr0 + p / I;
@@ -868,7 +879,8 @@ __global__ void __launch_bounds__(kDownThreads) k_down(const DownArgs a) {
 // staged activations, then the per-CTA selection's scratch
 static size_t gu_smem_for(const Layer& L) {
     const int H = L.d.hidden;
-    return (size_t)H * 2 + (size_t)(H / 32) * 8 + (size_t)select_words(L.d.n_experts) * 4;
+    return (size_t)H * 2 + (size_t)(H / 32) * 8 + (size_t)select_words(L.d.n_experts) * 4 +
+           (size_t)(L.d.n_experts + 1) * 8;
 }
 static size_t down_smem(int I, int ns) {
     return (size_t)ns * I * 2 + (size_t)ns * (I / 32) * 8 + (size_t)ns * kDownMaxRows * 4;
