@@ -435,6 +435,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
         const size_t b0 = per * blockIdx.x, b1 = min(a.pf_bytes, b0 + per);
         for (size_t o = b0; o < b1; o += 65536) prefetch_l2(a.pf + o, (uint32_t)min((size_t)65536, b1 - o));
     }
+    // this warp's shared-expert row pairs into L2 while x is staged (HBM is
+    // idle then: the router reads its weights from L2), so that their loads
+    // after the staging hit L2
+    if (a.n_shared && a.jj0 == 0 && lane == 0) {
+        const uint8_t* rec = a.rec_tab[a.E];
+        for (int p = blockIdx.x * kWarps + warp; p < I; p += gridDim.x * kWarps)
+            prefetch_l2(rec + (size_t)2 * p * a.rbH, (uint32_t)(2 * a.rbH));
+    }
     // the token's scale and staged activations (the router waited for the
     // producer of x before this kernel could start, so x is final)
     const int ta = token_exp(block_absmax(a.x, a.x_bf16, H, s_red));
