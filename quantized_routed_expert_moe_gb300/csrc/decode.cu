@@ -39,8 +39,12 @@ namespace moe {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kDownThreads = 256;
-constexpr int kDownWarps = kDownThreads / 32;
+// Down CTAs: a warp keeps one work item in flight at a time, so the bytes in
+// flight per SM grow with its warps. 4-bit items of one slot per warp (J = 1)
+// fit two 384-thread CTAs per SM (80 registers); the others need more
+// registers and keep 256.
+template <int BITS, int J>
+constexpr int down_threads() { return BITS == 4 && J == 1 ? 384 : 256; }
 constexpr int kGuBlock = 6;           // half-groups per lane whose loads are in flight together (gate/up)
 constexpr int kDownRows = 4;          // output rows per down work item (share the staged activations)
 constexpr int kDownMaxRows = 96;      // output rows one CTA owns in the down kernel
@@ -595,6 +599,7 @@ template <int BITS, int J>
 __device__ __forceinline__ void down_items(int s0, int s1, int own0, int own1, int I, size_t rbI,
                                            const uint8_t* const* s_rows, const uint4* hq, const float* Iv,
                                            const float* Xh, float* ypart) {
+    constexpr int kDW = down_threads<BITS, J>() / 32;   // the kernel's warps
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int IG = I / 32, nsl = s1 - s0;
     const int nquad = (own1 - own0 + kDownRows - 1) / kDownRows;
@@ -604,13 +609,13 @@ __device__ __forceinline__ void down_items(int s0, int s1, int own0, int own1, i
         // on J items at a time, so that it keeps as many bytes in flight as
         // with 4-bit codes
         const int GI = IG / 2;
-        for (int it0 = warp; it0 < nit; it0 += J * kDownWarps) {
+        for (int it0 = warp; it0 < nit; it0 += J * kDW) {
             const uint8_t* rr[J][kDownRows];
             int s2[J], n0s[J], nrs[J];
             bool live[J];
 #pragma unroll
             for (int j = 0; j < J; ++j) {
-                const int it = it0 + j * kDownWarps;
+                const int it = it0 + j * kDW;
                 live[j] = it < nit;
                 const int itv = live[j] ? it : it0;
                 const int q = itv / nsl;
@@ -664,13 +669,13 @@ __device__ __forceinline__ void down_items(int s0, int s1, int own0, int own1, i
         // rows.
         constexpr int MB = 2 / J;
         const int M = (IG + 31) / 32;
-        for (int it0 = warp; it0 < nit; it0 += J * kDownWarps) {
+        for (int it0 = warp; it0 < nit; it0 += J * kDW) {
             const uint8_t* rr[J][kDownRows];
             int s2[J], n0s[J], nrs[J];
             bool live[J];
 #pragma unroll
             for (int j = 0; j < J; ++j) {
-                const int it = it0 + j * kDownWarps;
+                const int it = it0 + j * kDW;
                 live[j] = it < nit;
                 const int itv = live[j] ? it : it0;
                 const int q = itv / nsl;
@@ -762,8 +767,8 @@ struct DownArgs {
     unsigned long long* tr;
 };
 
-template <int BITS, int J = 1>
-__global__ void __launch_bounds__(kDownThreads) k_down(const DownArgs a) {
+template <int BITS, int J>
+__device__ __forceinline__ void down_body(const DownArgs& a) {
     extern __shared__ uint4 smh[];
     ktrace(a.tr, blockIdx.x, 0);
     const int I = a.I, IG = I / 32, ns = a.k + a.n_shared;
@@ -880,6 +885,15 @@ __global__ void __launch_bounds__(kDownThreads) k_down(const DownArgs a) {
     ktrace(a.tr, blockIdx.x, 3);
 }
 
+template <int BITS, int J = 1>
+__global__ void __launch_bounds__(down_threads<BITS, J>()) k_down(const DownArgs a) {
+    down_body<BITS, J>(a);
+}
+template <>
+__global__ void __launch_bounds__(down_threads<4, 1>(), 2) k_down<4, 1>(const DownArgs a) {
+    down_body<4, 1>(a);
+}
+
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
@@ -913,6 +927,10 @@ static DownKernel down_kernel(const Layer& L) {
     if (L.wbits == 2) return k_down<2, 2>;
     return (L.d.inter / 32 + 31) / 32 == 1 ? k_down<4, 2> : k_down<4, 1>;
 }
+static int down_block(const Layer& L) {
+    if (L.wbits == 2) return down_threads<2, 2>();
+    return (L.d.inter / 32 + 31) / 32 == 1 ? down_threads<4, 2>() : down_threads<4, 1>();
+}
 
 
 cudaError_t decode_kernel_setup(Layer& L) {
@@ -928,7 +946,7 @@ cudaError_t decode_kernel_setup(Layer& L) {
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_gu, gu, kThreads, L.gu_smem);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, dn, kDownThreads, down_smem(I, ns));
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ_down, dn, down_block(L), down_smem(I, ns));
     if (e != cudaSuccess) return e;
     if (L.occ_gu < 1 || L.occ_down < 1) return cudaErrorInvalidConfiguration;
     // rows owned by one down CTA must fit its partial-sum buffer
@@ -1010,7 +1028,7 @@ static cudaError_t launch_down(Layer& L, const DecodeScratch& b, void* y, float*
     a.down_done = (b.shared_done || b.ids_ready || b.seq) ? b.down_done : nullptr;
     a.err = error_word(L);
     a.tr = tr;
-    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(kDownThreads), down_smem(d.inter, ns), s, pdl, a);
+    return launch_pdl(down_kernel(L), dim3(down_grid(L)), dim3(down_block(L)), down_smem(d.inter, ns), s, pdl, a);
 }
 
 // gate/up over row-order slots jj0..jj1-1 and (with `down`) down + combine,
