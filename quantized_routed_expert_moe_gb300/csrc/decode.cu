@@ -109,6 +109,50 @@ __device__ void stage_vector_q16(const void* x, int x_bf16, int K, float xs, uin
     }
 }
 
+// The token exponent a (max|x| 2^a in [1, 2)) and the staged runs of x 2^a, in
+// one pass over x: warp w takes blocks of 32 runs w, w + warps, ... (as
+// stage_vector_q16 does), keeps them in registers across the block-wide
+// maximum and quantises them from there. Requires at most kMaxB blocks per
+// warp.
+template <int kMaxB>
+__device__ int stage_token_q16(const void* x, int x_bf16, int K, float* s_red, uint4* xq, float* inv, float* X) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
+    const int nrun = K / 8, KG = K / 32, nblk = (nrun + 31) / 32;
+    float v[kMaxB][8];
+    float m = 0.f;
+#pragma unroll
+    for (int t = 0; t < kMaxB; ++t) {
+        const int r = (warp + t * nw) * 32 + lane;
+        if (r < nrun) {
+            load_run(x, x_bf16, r, v[t]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[t][i]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[t][i] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    float mx = 0.f;
+    for (int w = 0; w < nw; ++w) mx = fmaxf(mx, s_red[w]);
+    const int ta = token_exp(mx);
+    const float xs = exp2i(ta);
+#pragma unroll
+    for (int t = 0; t < kMaxB; ++t) {
+        const int b = warp + t * nw;
+        if (b < nblk) {   // warp-uniform
+            const int r = b * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[t][i] *= xs;
+            stage_q16_run(v[t], r < nrun, r, KG, xq, inv, X);
+        }
+    }
+    return ta;
+}
+
 // ---------------------------------------------------------------------------
 // gate/up + SwiGLU
 // ---------------------------------------------------------------------------
@@ -449,8 +493,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const GuArgs a) {
     }
     // the token's scale and staged activations (the router waited for the
     // producer of x before this kernel could start, so x is final)
-    const int ta = token_exp(block_absmax(a.x, a.x_bf16, H, s_red));
-    stage_vector_q16(a.x, a.x_bf16, H, exp2i(ta), xq, Iv, Xx);
+    int ta;
+    if ((H / 8 + 31) / 32 <= 4 * kWarps) {   // H <= 8192: one pass over x
+        ta = stage_token_q16<4>(a.x, a.x_bf16, H, s_red, xq, Iv, Xx);
+    } else {
+        ta = token_exp(block_absmax(a.x, a.x_bf16, H, s_red));
+        stage_vector_q16(a.x, a.x_bf16, H, exp2i(ta), xq, Iv, Xx);
+    }
     __syncthreads();
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.scale_out) *a.scale_out = ta;   // for the down kernel
     const float inv_a = exp2i(-ta);
