@@ -243,10 +243,10 @@ moe_status moe_decode(moe_layer* layer, const void* x, void* y, float* y_f32, vo
  *
  * Arguments, layouts, result and errors are those of moe_decode, with these
  * differences:
- *   - The same three kernels run; gate/up waits for the router grid rather
- *     than for a ready flag, and the down kernel starts on the shared expert
- *     only after its wait for gate/up. Streamed layers (cache_slots > 0) get
- *     MOE_E_UNSUPPORTED.
+ *   - The same three kernels run; the router's last block selects and gate/up
+ *     waits for the router grid rather than polling tagged partials, and the
+ *     down kernel reads the selection after its wait for gate/up. Streamed
+ *     layers (cache_slots > 0) get MOE_E_UNSUPPORTED.
  *   - The scratch holds the router's partial logits [splits][E], the logits
  *     [E], ids [k], weights [k] and the SwiGLU outputs [k + 1][I] (each
  *     rounded up to 256 bytes). A layer that needs more than

@@ -806,7 +806,8 @@ struct DownArgs {
     const int32_t* sel_ids;          // the selection (the router's, or the streamed layer's)
     const float* sel_wts;
     const int* scale_in;             // the token exponent a
-    unsigned* shared_done;           // with n_shared: early start on the shared rows (nullable)
+    unsigned* shared_done;           // with n_shared: early start on the shared rows (nullable; set only
+                                     // under the bounded-wait test hook)
     unsigned* ids_ready;             // the router's ready flag (nullable); cleared with the counters
     unsigned* down_done;             // the last CTA clears the counters
     unsigned* seq;                   // nullable: the layer's decode count, advanced by the last CTA

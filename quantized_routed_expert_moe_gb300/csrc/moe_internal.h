@@ -235,8 +235,9 @@ inline unsigned* error_word(Layer& L) { return L.counters + CNT_ERR; }
 // dc (nullable): the selecting block also runs the device-managed cache's LFU step
 // Scratch one decode token works on: the router's outputs (partials, keys,
 // selection, and the ready flag the decode's gate/up waits for), the SwiGLU
-// outputs (`copies` replicas of [k + 1][I] fp32), and the counters the down
-// kernel's early start uses (null: no early start).
+// outputs (`copies` replicas of [k + 1][I] fp32), and the fast decode's tagged
+// words and counters (null: the router's last block selects, and the down
+// kernel waits for gate/up before anything).
 struct DecodeScratch {
     float* part = nullptr;
     float* logits = nullptr;
@@ -253,10 +254,11 @@ struct DecodeScratch {
     unsigned long long* part_tag = nullptr;
     unsigned* seq = nullptr;
     unsigned long long* sel_tag = nullptr;   // [2k + 1]: ids, weights, token exponent (tagged)
-    unsigned* shared_done = nullptr;
-    unsigned* down_done = nullptr;
+    unsigned* shared_done = nullptr;   // gate/up CTAs done with the shared rows (the test hook's early start)
+    unsigned* down_done = nullptr;     // down CTAs counted (the last clears the counters)
 };
-// the layer's own scratch; `fast`: with the ready flag and the early start
+// the layer's own scratch; `fast`: with the tagged words, the decode count and
+// the counters
 DecodeScratch layer_decode_scratch(Layer& L, bool fast);
 
 // out (nullable): where the partials, keys and selection go (default: the

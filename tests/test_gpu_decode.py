@@ -255,10 +255,10 @@ def test_glm_scale_decode(glm_layer):
 
 def test_back_to_back_decodes_match_synchronised():
     """Many decodes queued back to back over two layer instances (the kernels
-    of consecutive calls overlap through programmatic dependent launch, and the
-    down kernel starts on the shared expert before gate/up completes) give
-    bit-identical outputs to the same decodes with a synchronisation after
-    every call."""
+    of consecutive calls overlap through programmatic dependent launch, and
+    each kernel reads the tagged words its predecessor publishes before that
+    one completes) give bit-identical outputs to the same decodes with a
+    synchronisation after every call."""
     spec = si.LayerSpec(hidden=1024, inter=512, n_experts=64, zipf_alpha=1.1)
     layer = si.gen_layer(41, 0, spec)
     T = 96
